@@ -1,0 +1,123 @@
+"""CPU oracle for Y = act(X . W^T + bias). TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg import this package. The library under ``transformer_linear_layer_gb300``
+never does, and the two share no code.
+
+The arithmetic lives in ``oracle.c`` (plain C, double accumulation in
+ascending k); this module compiles it with gcc on first use and wraps it with
+ctypes. :func:`rel_err` is the acceptance metric the pages use for a matmul:
+the worst absolute error over max|Y_ref| ("Writing a CUDA matmul that catches
+cuBLAS", section "The measurement was nearly wrong").
+
+Every oracle function here is pinned by ``tests/test_oracle_pins.py`` against
+identity and permutation weights, exact small-integer products, brute force on
+tiny shapes and an independent library GELU.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+TOL = {0: 1e-5, 1: 5e-3, 2: 1e-2}  # fp32, tf32, bf16 inputs (acceptance bars)
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``_build/liboracle.so`` (gcc, OpenMP if present)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    base = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", _SRC, "-lm"]
+    tmp = _LIB + f".tmp{os.getpid()}"
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:] + ["-o", tmp], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base + ["-o", tmp], check=True, capture_output=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, p = ctypes.c_int64, ctypes.c_void_p
+            lib.oracle_linear.argtypes = [i64, i64, i64, p, p, p, ctypes.c_int, p, ctypes.c_int]
+            lib.oracle_linear.restype = None
+            lib.oracle_linear_entries.argtypes = [i64, p, p, i64, p, p, p, ctypes.c_int, p, ctypes.c_int]
+            lib.oracle_linear_entries.restype = None
+            lib.oracle_gelu_array.argtypes = [i64, p, p]
+            lib.oracle_gelu_array.restype = None
+            lib.oracle_max_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f32(a):
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def linear(X, W, bias=None, gelu: bool = False, nthreads: int = 0) -> np.ndarray:
+    """Y (float64, M x N) = act(X . W^T + bias); X: M x K, W: N x K (fp32 values)."""
+    X, W = _f32(X), _f32(W)
+    M, K = X.shape
+    N, K2 = W.shape
+    assert K == K2, "X and W disagree on K"
+    b = None if bias is None else _f32(bias)
+    if b is not None:
+        assert b.shape == (N,)
+    Y = np.empty((M, N), dtype=np.float64)
+    _load().oracle_linear(M, N, K, X.ctypes.data, W.ctypes.data,
+                          None if b is None else b.ctypes.data, int(bool(gelu)), Y.ctypes.data, int(nthreads))
+    return Y
+
+
+def linear_entries(X, W, ms, ns, bias=None, gelu: bool = False, nthreads: int = 0) -> np.ndarray:
+    """Selected outputs Y[ms[i], ns[i]] (float64), computed one by one."""
+    X, W = _f32(X), _f32(W)
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    assert ms.shape == ns.shape
+    assert X.shape[1] == W.shape[1]
+    assert ms.size == 0 or (ms.min() >= 0 and ms.max() < X.shape[0] and ns.min() >= 0 and ns.max() < W.shape[0])
+    b = None if bias is None else _f32(bias)
+    out = np.empty(ms.shape, dtype=np.float64)
+    _load().oracle_linear_entries(ms.size, ms.ctypes.data, ns.ctypes.data, X.shape[1], X.ctypes.data,
+                                  W.ctypes.data, None if b is None else b.ctypes.data, int(bool(gelu)),
+                                  out.ctypes.data, int(nthreads))
+    return out
+
+
+def gelu(x) -> np.ndarray:
+    """The oracle's tanh-form GELU on a float64 array."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty_like(x)
+    _load().oracle_gelu_array(x.size, x.ctypes.data, out.ctypes.data)
+    return out
+
+
+def rel_err(y, y_ref) -> float:
+    """max|y - y_ref| / max|y_ref| (max|y - y_ref| when y_ref is all zero)."""
+    y = np.asarray(y, dtype=np.float64)
+    y_ref = np.asarray(y_ref, dtype=np.float64)
+    if y.size == 0:
+        return 0.0
+    num = float(np.max(np.abs(y - y_ref)))
+    den = float(np.max(np.abs(y_ref)))
+    return num / den if den > 0 else num

@@ -1,0 +1,135 @@
+"""The oracle against facts fixed by the mathematics (CPU only).
+
+Also plants mistakes in copies of the oracle (mutants, pure numpy) and checks
+that the pins catch every one, and calibrates the acceptance metric the way
+the sgemm page does: reordered fp32 summation lands near 1e-6, a real bug
+(a misplaced tile) near 1e-1 ("Writing a CUDA matmul that catches cuBLAS",
+section "The measurement was nearly wrong").
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic_inputs as si
+from oracle_pins import LINEAR_PINS, pin_gelu_function
+
+
+def real(X, W, b, gelu):
+    return oracle.linear(X, W, b, gelu)
+
+
+@pytest.mark.parametrize("pin", LINEAR_PINS, ids=lambda p: p.__name__)
+def test_oracle_meets_pin(pin):
+    pin(real)
+
+
+def test_gelu_meets_pin():
+    pin_gelu_function(oracle.gelu)
+
+
+def test_entries_match_full():
+    X = si.normal(7, 1, (33, 129))
+    W = si.normal(7, 2, (71, 129), 0.0, 0.02)
+    b = si.normal(7, 3, (71,), 0.0, 0.02)
+    full = oracle.linear(X, W, b, True)
+    rng = np.random.default_rng(0)
+    ms, ns = rng.integers(0, 33, 500), rng.integers(0, 71, 500)
+    assert np.array_equal(oracle.linear_entries(X, W, ms, ns, b, True), full[ms, ns])
+
+
+def test_thread_count_invariance():
+    X = si.normal(8, 1, (16, 1000))
+    W = si.normal(8, 2, (50, 1000), 0.0, 0.02)
+    assert np.array_equal(oracle.linear(X, W, nthreads=1), oracle.linear(X, W, nthreads=0))
+
+
+# ---------------------------------------------------------------- mutants ---
+
+def _gelu_np(s, c1=math.sqrt(2.0 / math.pi), c3=0.044715, half=0.5):
+    return half * s * (1.0 + np.tanh(c1 * (s + c3 * s ** 3)))
+
+
+def _loop(X, W, b, gelu, acc=np.float64, klimit=None, bias_after=False, bias_index="n",
+          transpose=False, gelu_fn=_gelu_np):
+    X = X.astype(np.float64)
+    W = W.astype(np.float64)
+    if transpose:
+        if W.shape[0] != W.shape[1]:
+            raise ValueError("transposed-W mutant needs a square W")
+        W = W.T
+    M, K = X.shape
+    N = W.shape[0]
+    Y = np.zeros((M, N))
+    kk = K if klimit is None else klimit(K)
+    for m in range(M):
+        for n in range(N):
+            s = acc(0.0)
+            for k in range(kk):
+                s = acc(s + acc(X[m, k]) * acc(W[n, k]))
+            s = float(s)
+            bv = 0.0
+            if b is not None:
+                bv = float(b[n] if bias_index == "n" else b[m % len(b)])
+            if not bias_after:
+                s += bv
+            if gelu:
+                s = float(gelu_fn(np.float64(s)))
+            if bias_after:
+                s += bv
+            Y[m, n] = s
+    return Y
+
+
+MUTANTS = {
+    "transposed_W": lambda X, W, b, g: _loop(X, W, b, g, transpose=True),
+    "drops_last_k": lambda X, W, b, g: _loop(X, W, b, g, klimit=lambda K: max(K - 1, 0)),
+    "fp32_accumulator": lambda X, W, b, g: _loop(X, W, b, g, acc=np.float32),
+    "bias_after_gelu": lambda X, W, b, g: _loop(X, W, b, g, bias_after=True),
+    "bias_indexed_by_row": lambda X, W, b, g: _loop(X, W, b, g, bias_index="m"),
+    "no_bias": lambda X, W, b, g: _loop(X, W, None, g),
+    "gelu_const_0p0447": lambda X, W, b, g: _loop(X, W, b, g, gelu_fn=lambda s: _gelu_np(s, c3=0.0447)),
+    "gelu_sqrt2_over_pi": lambda X, W, b, g: _loop(
+        X, W, b, g, gelu_fn=lambda s: _gelu_np(s, c1=math.sqrt(2.0) / math.pi)),
+    "gelu_no_half": lambda X, W, b, g: _loop(X, W, b, g, gelu_fn=lambda s: _gelu_np(s, half=1.0)),
+}
+
+
+def test_mutants_reference_is_sound():
+    """The loop used by the mutants, unmutated, passes every pin (so a failing
+    mutant fails because of its planted mistake)."""
+    for pin in LINEAR_PINS:
+        pin(lambda X, W, b, g: _loop(X, W, b, g))
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name):
+    mutant = MUTANTS[name]
+    caught = []
+    for pin in LINEAR_PINS:
+        try:
+            pin(mutant)
+        except (AssertionError, ValueError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches mutant {name}"
+
+
+# ------------------------------------------------------------ calibration ---
+
+def test_metric_separates_reorder_from_bug():
+    X = si.uniform_pm1(0, 1, (256, 4096))
+    W = si.uniform_pm1(0, 2, (256, 4096))
+    ref = oracle.linear(X, W)
+    y32 = (X @ W.T).astype(np.float64)  # fp32 sums in BLAS order
+    e = oracle.rel_err(y32, ref)
+    assert 1e-9 < e < 1e-5, e
+    bad = ref.copy()
+    bad[:64, :64], bad[64:128, 64:128] = ref[64:128, 64:128], ref[:64, :64]
+    assert oracle.rel_err(bad, ref) > 5e-2
+
+
+def test_rel_err_definition():
+    assert oracle.rel_err(np.array([1.0, 2.0]), np.array([1.0, 4.0])) == 0.5
+    assert oracle.rel_err(np.array([0.5]), np.array([0.0])) == 0.5
+    assert oracle.rel_err(np.zeros((0, 3)), np.zeros((0, 3))) == 0.0

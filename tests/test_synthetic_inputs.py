@@ -1,0 +1,54 @@
+"""The seeded input generators (CPU only)."""
+import numpy as np
+import torch
+
+import synthetic_inputs as si
+
+
+def test_splitmix64_reference_values():
+    # SplitMix64 from state 0 (increment then finalise): the generator's
+    # published first outputs, 0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4.
+    with np.errstate(over="ignore"):
+        states = np.array([si.GAMMA, np.uint64(2) * si.GAMMA], dtype=np.uint64)
+    out = si._mix(states)
+    assert int(out[0]) == 0xE220A8397B1DCDAF
+    assert int(out[1]) == 0x6E789E6AA1B965F4
+
+
+def test_deterministic_and_counter_based():
+    a = si.draws(5, 3, 100)
+    assert np.array_equal(a, si.draws(5, 3, 100))
+    assert np.array_equal(a[40:], si.draws(5, 3, 60, start=40))
+    assert not np.array_equal(a, si.draws(5, 4, 100))
+    assert not np.array_equal(a, si.draws(6, 3, 100))
+
+
+def test_uniform_range_and_moments():
+    u = si.uniform_pm1(0, 1, (200000,))
+    assert u.dtype == np.float32
+    assert u.min() >= -1.0 and u.max() < 1.0
+    assert abs(u.mean()) < 0.01 and abs(u.var() - 1 / 3) < 0.01
+    # 24-bit grid: every value is k * 2^-23 - 1
+    k = (u.astype(np.float64) + 1.0) * 2.0 ** 23
+    assert np.array_equal(k, np.round(k))
+
+
+def test_normal_moments():
+    z = si.normal(0, 2, (200000,), 0.0, 0.02)
+    assert abs(z.mean()) < 2e-4 and abs(z.std() - 0.02) < 4e-4
+
+
+def test_bf16_rounding_matches_torch():
+    x = np.concatenate([si.normal(1, 1, (50000,)), si.uniform_pm1(1, 2, (50000,)) * 1e3,
+                        np.array([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -0.0, 65504.0], np.float32)])
+    ours = si.to_bf16_bits(x)
+    theirs = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, theirs)
+    assert np.array_equal(si.bf16_bits_to_f32(ours), torch.from_numpy(ours.view(np.int16)).view(torch.bfloat16).float().numpy())
+
+
+def test_workload_shapes():
+    assert si.SKINNY_16x4096.algorithmic_bytes() == 2 * (16 * 4096 + 4096 * 4096) + 2 * 16 * 4096 + 4 * 4096
+    X, W, b = si.make_inputs(si.Layer("t", 3, 5, 8, si.PREC_BF16, bias=True))
+    assert X.shape == (3, 8) and W.shape == (5, 8) and b.shape == (5,)
+    assert np.array_equal(si.round_bf16(X), X)
