@@ -1,0 +1,169 @@
+/*
+ * lin.h - C ABI of a GB300 (sm_103a) library for the transformer linear layer
+ *
+ *     Y = act(X . W^T + bias)
+ *
+ * X is M x K row-major (one row per token / batch vector), W is N x K
+ * row-major ("out x in", the way PyTorch stores a linear layer's weight), Y
+ * is M x N row-major. Each output is the dot product of one row of X with one
+ * row of W ("One multiply, one RTX 5090, eight kernels", section "The
+ * multiply"). The bias (length N, optional) and the activation are applied in
+ * the store of the product ("Writing a CUDA matmul that catches cuBLAS",
+ * sections "The bias add did not need to exist" and "The residual and GELU go
+ * the same way"). The activation is the identity or the tanh form of GELU,
+ * 0.5 s (1 + tanh(sqrt(2/pi) (s + 0.044715 s^3))), applied to (sum + bias).
+ *
+ * All pointers to X, W, bias and Y are DEVICE pointers on the context's
+ * device, owned by the caller. Every call is asynchronous on the given CUDA
+ * stream (a cudaStream_t passed as void*, NULL = legacy default stream) and
+ * returns after the work is enqueued; no call synchronises except
+ * lin_check_device. No call ever computes on the host: when the GPU path
+ * cannot run the call returns an error.
+ *
+ * Status codes: 0 on success, a negative LIN_ERR_* otherwise; lin_strerror
+ * gives a message. No C++ exception crosses this boundary.
+ */
+#ifndef LIN_H
+#define LIN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LIN_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define LIN_API __attribute__((visibility("default")))
+#else
+#define LIN_API
+#endif
+
+/* Arithmetic of the multiply.
+ * FP32: fp32 X, W, Y; fp32 fused multiply-add on the CUDA cores (exact fp32
+ *       products, fp32 sums) - the path of the sgemm ladder ("Writing a CUDA
+ *       matmul that catches cuBLAS", "Kernel 8: the loop was shaped wrong").
+ * TF32: fp32 X, W, Y; tensor-core products of the operands' TF32 parts with
+ *       fp32 accumulation ("Writing a CUDA matmul that catches cuBLAS",
+ *       "Kernel 9: the silicon I had not touched").
+ * BF16: bf16 X, W, Y; fp32 bias; tensor-core bf16 products with fp32
+ *       accumulation, output rounded to nearest-even bf16 ("One multiply, one
+ *       RTX 5090, eight kernels", "From 748 to 29 microseconds"). */
+typedef enum {
+    LIN_PREC_FP32 = 0,
+    LIN_PREC_TF32 = 1,
+    LIN_PREC_BF16 = 2
+} lin_precision;
+
+/* Activation applied after the bias. */
+typedef enum {
+    LIN_EPI_NONE = 0,
+    LIN_EPI_GELU_TANH = 1
+} lin_epilogue;
+
+typedef enum {
+    LIN_OK = 0,
+    LIN_ERR_ARG = -1,            /* NULL pointer, negative size, unknown enum, Y aliasing an input */
+    LIN_ERR_ALIGN = -2,          /* X or W not 16-byte aligned, or K * element size not a multiple of 16 */
+    LIN_ERR_WORKSPACE = -3,      /* an explicit plan needs more workspace than the context holds */
+    LIN_ERR_CUDA = -4,           /* a CUDA runtime call or kernel launch failed */
+    LIN_ERR_DEVICE_TIMEOUT = -5, /* a kernel gave up a bounded wait and skipped its work */
+    LIN_ERR_UNSUPPORTED = -6     /* the plan's kernel cannot run this shape / precision */
+} lin_status;
+
+/* Kernels a plan can name. */
+typedef enum {
+    LIN_KERNEL_NONE = 0,   /* M == 0 or N == 0: nothing to do */
+    LIN_KERNEL_FILL = 1,   /* K == 0: Y = act(bias) (or act(0)) */
+    LIN_KERNEL_SKINNY = 2, /* M <= 16, BF16: split-K W-streaming kernel, 128-bit loads */
+    LIN_KERNEL_FFMA = 3,   /* FP32: register-tiled FFMA, optional split-K */
+    LIN_KERNEL_TC = 4      /* TF32 / BF16: TMA + tcgen05 + TMEM, fused epilogue */
+} lin_kernel;
+
+/* One launch configuration, chosen by the dispatch table or given explicitly.
+ * splits > 1 is split-K: each CTA sums one range of K into the workspace and
+ * the last CTA to finish a tile adds the ranges in fixed order (0, 1, ...),
+ * so results are bitwise repeatable ("Optimizing a GPT-2-class transformer on
+ * a GPU", Act I, split-K combined by a fixed-order reduction). */
+typedef struct {
+    int kernel;   /* lin_kernel */
+    int variant;  /* kernel-specific tile configuration id (see DESIGN notes in the source) */
+    int bm, bn, bk;
+    int splits;   /* >= 1 */
+    int stages;   /* shared-memory pipeline depth (TC), 0 otherwise */
+    int grid_x, grid_y, grid_z;
+    int threads;
+    long long workspace_bytes; /* bytes of context workspace the launch uses */
+} lin_plan;
+
+typedef struct lin_ctx lin_ctx; /* opaque; owned by the library */
+
+/* Create a context on CUDA device `device`. Allocates `max_workspace_bytes`
+ * of device workspace (0 = a default of 64 MiB) for split-K partial sums and
+ * tile counters, plus one device status word. Returns LIN_ERR_CUDA when the
+ * device cannot be used. *out is NULL on failure. */
+LIN_API int lin_create(lin_ctx** out, int device, size_t max_workspace_bytes);
+
+/* Free a context and its workspace (synchronises the device first). NULL is
+ * accepted. */
+LIN_API int lin_destroy(lin_ctx* ctx);
+
+/* Y = act(X . W^T + bias), chosen kernel per the dispatch table.
+ *   M, N, K   : sizes, each >= 0 (M == 0 or N == 0 does nothing; K == 0 gives
+ *               Y = act(bias) or act(0)).
+ *   X         : M x K row-major; fp32 for FP32/TF32, bf16 for BF16.
+ *   W         : N x K row-major (out x in), same element type as X.
+ *   bias      : N fp32 values, or NULL for no bias.
+ *   Y         : M x N row-major; fp32 for FP32/TF32, bf16 for BF16. Must not
+ *               overlap X, W or bias.
+ *   epilogue  : lin_epilogue.   precision : lin_precision.
+ *   stream    : cudaStream_t (as void*).
+ * X and W must be 16-byte aligned and K * element size a multiple of 16
+ * (LIN_ERR_ALIGN otherwise); bias 4-byte aligned; Y aligned to its element.
+ * One context must not run two calls at the same time (they share the
+ * workspace): use one context per stream. */
+LIN_API int lin_forward(lin_ctx* ctx, int M, int N, int K, const void* X, const void* W,
+                const float* bias, void* Y, int epilogue, int precision, void* stream);
+
+/* Same, with an explicit launch configuration (for tuning and for tests that
+ * must reach one kernel). The plan is validated; LIN_ERR_UNSUPPORTED if its
+ * kernel cannot run the shape, LIN_ERR_WORKSPACE if it needs more workspace
+ * than the context holds. */
+LIN_API int lin_forward_plan(lin_ctx* ctx, const lin_plan* plan, int M, int N, int K, const void* X,
+                     const void* W, const float* bias, void* Y, int epilogue, int precision,
+                     void* stream);
+
+/* The dispatch table, on the host only (no GPU needed): the plan lin_forward
+ * would use for this shape on a device with `sm_count` SMs and a workspace of
+ * `workspace_bytes`. Returns LIN_ERR_ARG for invalid sizes or enums. */
+LIN_API int lin_plan_query(int sm_count, int M, int N, int K, int precision, int epilogue,
+                   size_t workspace_bytes, lin_plan* out);
+
+/* Fill *out with the default plan of a kernel family for a shape (host only),
+ * for sweeps: kernel = lin_kernel, variant = tile configuration, splits = 0
+ * lets the table choose the split. Returns LIN_ERR_UNSUPPORTED when the
+ * kernel cannot run the shape. */
+LIN_API int lin_plan_make(int sm_count, int kernel, int variant, int splits, int M, int N, int K,
+                  int precision, lin_plan* out);
+
+/* Synchronise `stream`, read and clear the context's device status word.
+ * Returns LIN_ERR_DEVICE_TIMEOUT if any kernel since the last check gave up
+ * a bounded wait (its output is then incomplete), LIN_ERR_CUDA on a CUDA
+ * error, LIN_OK otherwise. */
+LIN_API int lin_check_device(lin_ctx* ctx, void* stream);
+
+/* SM count and device ordinal of a context (host values, no GPU call). */
+LIN_API int lin_ctx_info(const lin_ctx* ctx, int* device, int* sm_count, size_t* workspace_bytes);
+
+/* Static message for a status code. */
+LIN_API const char* lin_strerror(int status);
+
+/* LIN_ABI_VERSION of the loaded library. */
+LIN_API int lin_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIN_H */

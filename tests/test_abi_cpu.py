@@ -1,0 +1,130 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the header
+declares, and its host logic (dispatch table, validation) behaves."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import transformer_linear_layer_gb300 as tll
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SM = 152
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    tll.build()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "lin.h")).read()
+    return re.findall(r"LIN_API\s+[\w\s\*]+?\b(lin_\w+)\s*\(", src)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("lin_create", "lin_forward", "lin_destroy", "lin_strerror"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported():
+    lib = ctypes.CDLL(tll.build())
+    names = declared_functions()
+    assert len(names) >= 10
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in lin.h but not exported"
+
+
+def test_abi_version_and_messages():
+    lib = tll.library()
+    assert lib.lin_abi_version() == 1
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        msg = lib.lin_strerror(code).decode()
+        assert msg and msg != "unknown status"
+    assert lib.lin_strerror(-99).decode() == "unknown status"
+
+
+def test_null_context_is_an_argument_error():
+    lib = tll.library()
+    assert lib.lin_forward(None, 16, 16, 16, None, None, None, None, 0, 2, None) == tll.ERR_ARG
+    assert lib.lin_check_device(None, None) == tll.ERR_ARG
+    assert lib.lin_destroy(None) == tll.OK
+    assert lib.lin_create(None, 0, 0) == tll.ERR_ARG
+
+
+def test_create_without_device_fails_cleanly():
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p(123)
+    assert tll.library().lin_create(ctypes.byref(h), 0, 0) == tll.ERR_CUDA
+    assert not h.value
+
+
+# ------------------------------------------------------------ dispatch table
+
+def kname(p):
+    return p.as_dict()["kernel_name"]
+
+
+def test_dispatch_skinny_for_small_m_bf16():
+    for M in (1, 8, 16):
+        p = tll.plan_query(SM, M, 4096, 4096, "bf16")
+        assert kname(p) == "skinny"
+        assert p.splits > 1 and p.grid_y == p.splits
+        assert p.grid_x * p.bn >= 4096
+    assert kname(tll.plan_query(SM, 17, 4096, 4096, "bf16")) == "tc"
+
+
+def test_dispatch_tensor_cores_for_tf32_and_wide_bf16():
+    for prec in ("tf32", "bf16"):
+        p = tll.plan_query(SM, 8192, 50257, 768, prec)
+        assert kname(p) == "tc"
+        assert p.grid_x * p.bn >= 50257 and p.grid_y * 128 >= 8192
+        assert p.splits == 1 and p.workspace_bytes == 0
+
+
+def test_dispatch_ffma_for_fp32():
+    big = tll.plan_query(SM, 4096, 4096, 4096, "fp32")
+    assert kname(big) == "ffma" and big.bm == 128 and big.splits == 1
+    for N, K in ((2304, 768), (768, 768), (3072, 768), (768, 3072)):
+        p = tll.plan_query(SM, 128, N, K, "fp32")
+        assert kname(p) == "ffma" and p.bm == 64
+        ctas = p.grid_x * p.grid_y * p.grid_z
+        assert ctas >= SM // 2, (N, K, ctas)
+        assert p.grid_z == p.splits
+
+
+def test_dispatch_degenerate_shapes():
+    assert kname(tll.plan_query(SM, 0, 10, 10, "bf16")) == "none"
+    assert kname(tll.plan_query(SM, 10, 0, 10, "fp32")) == "none"
+    assert kname(tll.plan_query(SM, 10, 10, 0, "tf32")) == "fill"
+    with pytest.raises(tll.LinError):
+        tll.plan_query(SM, -1, 10, 10, "bf16")
+    with pytest.raises(tll.LinError):
+        tll.plan_query(SM, 1, 10, 10, 9)
+
+
+def test_split_respects_workspace():
+    roomy = tll.plan_query(SM, 16, 4096, 4096, "bf16", workspace_bytes=64 << 20)
+    tight = tll.plan_query(SM, 16, 4096, 4096, "bf16", workspace_bytes=1 << 20)
+    none = tll.plan_query(SM, 16, 4096, 4096, "bf16", workspace_bytes=0)
+    assert roomy.workspace_bytes <= 64 << 20 and tight.workspace_bytes <= 1 << 20
+    assert tight.splits <= roomy.splits and none.splits == 1 and none.workspace_bytes == 0
+
+
+def test_plan_make_families():
+    for v in range(4):
+        p = tll.plan_make(SM, tll.KERNEL_SKINNY, v, 5, 16, 4096, 4096, "bf16")
+        assert p.splits == 5 and p.grid_y == 5
+    with pytest.raises(tll.LinError):
+        tll.plan_make(SM, tll.KERNEL_SKINNY, 4, 0, 16, 4096, 4096, "bf16")
+    with pytest.raises(tll.LinError):
+        tll.plan_make(SM, tll.KERNEL_SKINNY, 0, 0, 17, 4096, 4096, "bf16")
+    with pytest.raises(tll.LinError):
+        tll.plan_make(SM, tll.KERNEL_FFMA, 0, 0, 16, 64, 64, "bf16")
+    with pytest.raises(tll.LinError):
+        tll.plan_make(SM, tll.KERNEL_TC, 0, 2, 256, 256, 256, "tf32")
+    p = tll.plan_make(SM, tll.KERNEL_FFMA, 1, 7, 128, 768, 768, "fp32")
+    assert p.grid_z == 7 and p.workspace_bytes >= 7 * 128 * 768 * 4

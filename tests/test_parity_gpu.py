@@ -1,0 +1,242 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Tolerances (max|Y - Y_ref| / max|Y_ref|): 1e-5 for fp32, 5e-3 for TF32,
+1e-2 for bf16 inputs; exact-arithmetic cases (permutation weights, small
+integer inputs) must match bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic_inputs as si
+import transformer_linear_layer_gb300 as tll
+from gpu_util import PREC_NAME, check_layer, check_layer_sampled, device_inputs, run
+
+pytestmark = pytest.mark.gpu
+
+BF16, TF32, FP32 = si.PREC_BF16, si.PREC_TF32, si.PREC_FP32
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    return tll.default_context(0)
+
+
+def all_plans(ctx, M, N, K, precision):
+    """Every kernel family / variant that can run this shape, plus split choices."""
+    plans = []
+    sm = ctx.sm_count
+    if precision == BF16 and M <= 16:
+        for v in range(4):
+            for s in (0, 1, 3):
+                plans.append(tll.plan_make(sm, tll.KERNEL_SKINNY, v, s, M, N, K, "bf16"))
+    if precision in (BF16, TF32):
+        for v in range(2):
+            plans.append(tll.plan_make(sm, tll.KERNEL_TC, v, 1, M, N, K, PREC_NAME[precision]))
+    if precision == FP32:
+        for v in range(2):
+            for s in (1, 0, 3):
+                plans.append(tll.plan_make(sm, tll.KERNEL_FFMA, v, s, M, N, K, "fp32"))
+    return plans
+
+
+# ---------------------------------------------------------------- exact cases
+
+@pytest.mark.parametrize("precision", [BF16, TF32, FP32])
+@pytest.mark.parametrize("M,N,K", [(16, 96, 96), (200, 136, 136), (5, 72, 72)])
+def test_permutation_weights_exact(ctx, precision, M, N, K):
+    """W a permutation matrix (N = K): Y = X[:, p] exactly, on every kernel.
+    Pins operand roles and the smem/TMEM layouts (a one-hot probe per column)."""
+    p = (np.arange(K) * 7 + 3) % K
+    W = np.zeros((N, K), np.float32)
+    W[np.arange(N), p[:N]] = 1.0
+    X = si.uniform_pm1(3, M, (M, K))
+    if precision == BF16:
+        X = si.round_bf16(X)
+    for plan in all_plans(ctx, M, N, K, precision):
+        y = run(X, W, None, precision, plan=plan, ctx=ctx)
+        expect = X[:, p[:N]].astype(np.float64)
+        if precision == TF32:
+            # the tensor core multiplies the TF32 part of X (1 x value keeps 10 mantissa bits)
+            assert np.max(np.abs(y - expect)) <= 2.0 ** -10 * np.max(np.abs(expect)), plan
+            continue
+        assert np.array_equal(y, expect), f"plan {plan}"
+
+
+@pytest.mark.parametrize("precision", [BF16, TF32, FP32])
+@pytest.mark.parametrize("M,N,K", [(16, 256, 512), (1, 40, 64), (129, 264, 200), (300, 520, 1024)])
+def test_small_integers_bitwise(ctx, precision, M, N, K):
+    """Integer inputs in [-4, 4]: every product and partial sum is exact, so the
+    GPU must equal the oracle bit for bit (bf16 output: the oracle's value
+    rounded to nearest-even bf16)."""
+    layer = si.Layer("ints", M, N, K, precision, bias=True, x_dist="ints")
+    X, W, b = si.make_inputs(layer)
+    ref = oracle.linear(X, W, b)
+    if precision == BF16:
+        ref = si.round_bf16(ref.astype(np.float32)).astype(np.float64)
+    for plan in all_plans(ctx, M, N, K, precision):
+        y = run(X, W, b, precision, plan=plan, ctx=ctx)
+        assert np.array_equal(y, ref), f"plan {plan}: max diff {np.max(np.abs(y - ref))}"
+
+
+# ------------------------------------------------------------ the workloads
+
+def test_square_256_fp32(ctx):
+    layer = si.SQUARE_256_FP32
+    for plan in [None] + all_plans(ctx, 256, 256, 256, FP32):
+        check_layer(layer, plan=plan, ctx=ctx)
+
+
+def test_skinny_m16_4096_every_variant(ctx):
+    layer = si.SKINNY_16x4096
+    for plan in [None] + all_plans(ctx, 16, 4096, 4096, BF16):
+        check_layer(layer, plan=plan, ctx=ctx)
+
+
+@pytest.mark.parametrize("layer", si.GPT2_M128_FP32, ids=lambda l: l.name)
+def test_gpt2_m128_fp32(ctx, layer):
+    check_layer(layer, ctx=ctx)
+
+
+@pytest.mark.parametrize("layer", [si.SQUARE_4096_FP32, si.SQUARE_4096_TF32], ids=lambda l: l.name)
+def test_square_4096_sampled(layer):
+    check_layer_sampled(layer, count=1024)
+
+
+@pytest.mark.parametrize("layer", si.GPT2_M8192_BF16, ids=lambda l: l.name)
+def test_gpt2_m8192_bf16_sampled(layer):
+    check_layer_sampled(layer, count=2048)
+
+
+@pytest.mark.parametrize("precision", [BF16, TF32])
+def test_tc_midsize_full(ctx, precision):
+    """Several tiles in each direction and ragged tails, full comparison."""
+    for M, N, K in [(384, 640, 768), (257, 1000, 320), (131, 50257 % 1024 + 512, 96)]:
+        layer = si.Layer("tc_mid", M, N, K, precision, si.EPI_GELU, bias=True)
+        for plan in all_plans(ctx, M, N, K, precision):
+            check_layer(layer, plan=plan, ctx=ctx)
+
+
+# ------------------------------------------------------------- edge shapes
+
+@pytest.mark.parametrize("M", [1, 2, 15, 16, 17, 127, 129])
+def test_edge_rows_bf16(ctx, M):
+    check_layer(si.Layer("edge", M, 1000, 520, BF16, si.EPI_GELU, bias=True), ctx=ctx)
+
+
+@pytest.mark.parametrize("M", [1, 3, 63, 65, 127, 129])
+def test_edge_rows_fp32(ctx, M):
+    check_layer(si.Layer("edge", M, 333, 132, FP32, si.EPI_GELU, bias=True), ctx=ctx)
+
+
+@pytest.mark.parametrize("precision,K", [(BF16, 8), (BF16, 40), (BF16, 4104), (TF32, 4), (TF32, 36), (FP32, 4),
+                                         (FP32, 20)])
+def test_k_tails(ctx, precision, K):
+    for M in (16, 160):
+        layer = si.Layer("ktail", M, 200, K, precision, bias=True)
+        for plan in [None] + all_plans(ctx, M, 200, K, precision):
+            check_layer(layer, plan=plan, ctx=ctx)
+
+
+@pytest.mark.parametrize("precision", [BF16, TF32, FP32])
+def test_k_zero_gives_activation_of_bias(ctx, precision):
+    M, N = 7, 33
+    b = si.normal(1, 1, (N,), 0.0, 1.0)
+    x, w, bias = device_inputs(np.zeros((M, 0), np.float32), np.zeros((N, 0), np.float32), b, precision)
+    y = tll.forward(x, w, bias, epilogue="gelu", precision=PREC_NAME[precision])
+    ref = oracle.linear(np.zeros((M, 0), np.float32), np.zeros((N, 0), np.float32), b, True)
+    assert oracle.rel_err(y.float().cpu().numpy(), ref) <= oracle.TOL[precision]
+
+
+def test_empty_m_and_n(ctx):
+    x = torch.zeros((0, 64), device="cuda", dtype=torch.bfloat16)
+    w = torch.zeros((32, 64), device="cuda", dtype=torch.bfloat16)
+    assert tll.forward(x, w).shape == (0, 32)
+    x = torch.zeros((4, 64), device="cuda", dtype=torch.bfloat16)
+    w = torch.zeros((0, 64), device="cuda", dtype=torch.bfloat16)
+    assert tll.forward(x, w).shape == (4, 0)
+
+
+# ------------------------------------------------------------- properties
+
+@pytest.mark.parametrize("precision,M,N,K", [(BF16, 16, 4096, 4096), (FP32, 128, 768, 3072), (BF16, 384, 512, 768),
+                                             (TF32, 256, 384, 512)])
+def test_bitwise_repeatable(ctx, precision, M, N, K):
+    """Split-K and all: two runs give identical bits (fixed-order reduction)."""
+    X, W, b = si.make_inputs(si.Layer("rep", M, N, K, precision, bias=True))
+    y1 = run(X, W, b, precision, ctx=ctx)
+    y2 = run(X, W, b, precision, ctx=ctx)
+    assert np.array_equal(y1, y2)
+
+
+@pytest.mark.parametrize("precision,M,N,K", [(BF16, 16, 1024, 1024), (FP32, 128, 768, 768), (BF16, 256, 512, 256),
+                                             (TF32, 256, 256, 128)])
+def test_identical_rows_identical_outputs(ctx, precision, M, N, K):
+    """Every row of X the same: every row of Y must be the same, bitwise (no
+    leak between rows of a batch)."""
+    X1, W, b = si.make_inputs(si.Layer("rows", 1, N, K, precision, bias=True))
+    X = np.repeat(X1, M, axis=0)
+    y = run(X, W, b, precision, ctx=ctx)
+    assert np.array_equal(y, np.repeat(y[:1], M, axis=0))
+
+
+@pytest.mark.parametrize("precision,M,N,K", [(BF16, 16, 300, 256), (BF16, 140, 300, 256), (FP32, 70, 300, 256),
+                                             (TF32, 140, 300, 256)])
+def test_no_writes_outside_y(ctx, precision, M, N, K):
+    """Canary: Y sits inside a larger buffer filled with a sentinel; only the
+    M x N window may change."""
+    X, W, b = si.make_inputs(si.Layer("canary", M, N, K, precision, bias=True))
+    x, w, bias = device_inputs(X, W, b, precision)
+    dt = torch.bfloat16 if precision == BF16 else torch.float32
+    pad = 4096
+    buf = torch.full((pad + M * N + pad,), 12345.0, device="cuda", dtype=dt)
+    out = buf[pad:pad + M * N].view(M, N)
+    tll.forward(x, w, bias, precision=PREC_NAME[precision], out=out)
+    torch.cuda.synchronize()
+    assert bool((buf[:pad] == 12345.0).all()) and bool((buf[pad + M * N:] == 12345.0).all())
+    ref = oracle.linear(X, W, b)
+    assert oracle.rel_err(out.float().cpu().numpy(), ref) <= oracle.TOL[precision]
+
+
+# ------------------------------------------------------------ error paths
+
+def test_status_codes(ctx):
+    x = torch.zeros((16, 64), device="cuda", dtype=torch.bfloat16)
+    w = torch.zeros((32, 64), device="cuda", dtype=torch.bfloat16)
+    y = torch.empty((16, 32), device="cuda", dtype=torch.bfloat16)
+    s = torch.cuda.current_stream().cuda_stream
+    # misaligned X (2-byte offset)
+    xb = torch.zeros((16 * 64 + 8,), device="cuda", dtype=torch.bfloat16)
+    assert ctx.forward_ptr(16, 32, 64, xb.data_ptr() + 2, w.data_ptr(), None, y.data_ptr(), 0, 2, s) == tll.ERR_ALIGN
+    # K * 2 bytes not a multiple of 16
+    assert ctx.forward_ptr(16, 32, 60, x.data_ptr(), w.data_ptr(), None, y.data_ptr(), 0, 2, s) == tll.ERR_ALIGN
+    # Y overlapping X
+    assert ctx.forward_ptr(16, 32, 64, x.data_ptr(), w.data_ptr(), None, x.data_ptr(), 0, 2, s) == tll.ERR_ARG
+    # bad enums, negative sizes, NULL pointers
+    assert ctx.forward_ptr(16, 32, 64, x.data_ptr(), w.data_ptr(), None, y.data_ptr(), 7, 2, s) == tll.ERR_ARG
+    assert ctx.forward_ptr(-1, 32, 64, x.data_ptr(), w.data_ptr(), None, y.data_ptr(), 0, 2, s) == tll.ERR_ARG
+    assert ctx.forward_ptr(16, 32, 64, None, w.data_ptr(), None, y.data_ptr(), 0, 2, s) == tll.ERR_ARG
+    # a plan for another kernel family or shape
+    plan = tll.plan_make(ctx.sm_count, tll.KERNEL_FFMA, 0, 1, 16, 32, 64, "fp32")
+    assert ctx.forward_plan_ptr(plan, 16, 32, 64, x.data_ptr(), w.data_ptr(), None, y.data_ptr(), 0, 2,
+                                s) == tll.ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    ctx.check()
+
+
+def test_workspace_limit():
+    small = tll.Context(0, workspace_bytes=4096)
+    x = torch.zeros((16, 4096), device="cuda", dtype=torch.bfloat16)
+    w = torch.zeros((4096, 4096), device="cuda", dtype=torch.bfloat16)
+    # the dispatch table fits the split to the workspace (here: no split)...
+    assert small.plan(16, 4096, 4096).splits == 1
+    tll.forward(x, w, ctx=small)
+    # ...an explicit plan that needs more is refused
+    plan = tll.plan_make(small.sm_count, tll.KERNEL_SKINNY, 0, 8, 16, 4096, 4096, "bf16")
+    y = torch.empty((16, 4096), device="cuda", dtype=torch.bfloat16)
+    rc = small.forward_plan_ptr(plan, 16, 4096, 4096, x.data_ptr(), w.data_ptr(), None, y.data_ptr(), 0, 2,
+                                torch.cuda.current_stream().cuda_stream)
+    assert rc == tll.ERR_WORKSPACE
+    small.check()
+    small.close()

@@ -1,0 +1,250 @@
+"""GB300 linear layer: Y = act(X . W^T + bias), W stored out x in.
+
+A thin ctypes binding over the C ABI in ``include/lin.h`` (library
+``_build/liblin.so``, built by :func:`build`). The binding only marshals
+arguments: torch supplies device memory and the current CUDA stream, and every
+step of the multiply runs in this package's CUDA kernels. There is no CPU path:
+if the library is missing or the GPU call fails, an exception is raised.
+
+    import torch, transformer_linear_layer_gb300 as tll
+    y = tll.forward(x_bf16, w_bf16, bias_fp32, epilogue="gelu")   # -> bf16
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB as _LIB_PATH
+from .build import build
+
+__all__ = [
+    "LinError", "Context", "Plan", "forward", "forward_plan", "plan_query", "plan_make", "build",
+    "library", "PREC_FP32", "PREC_TF32", "PREC_BF16", "EPI_NONE", "EPI_GELU_TANH",
+    "KERNEL_NONE", "KERNEL_FILL", "KERNEL_SKINNY", "KERNEL_FFMA", "KERNEL_TC",
+]
+
+PREC_FP32, PREC_TF32, PREC_BF16 = 0, 1, 2
+EPI_NONE, EPI_GELU_TANH = 0, 1
+KERNEL_NONE, KERNEL_FILL, KERNEL_SKINNY, KERNEL_FFMA, KERNEL_TC = 0, 1, 2, 3, 4
+KERNEL_NAMES = {0: "none", 1: "fill", 2: "skinny", 3: "ffma", 4: "tc"}
+OK, ERR_ARG, ERR_ALIGN, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
+
+_PREC_NAMES = {"fp32": PREC_FP32, "tf32": PREC_TF32, "bf16": PREC_BF16}
+_EPI_NAMES = {"none": EPI_NONE, None: EPI_NONE, "gelu": EPI_GELU_TANH, "gelu_tanh": EPI_GELU_TANH}
+
+
+class Plan(ctypes.Structure):
+    """Mirror of ``lin_plan``."""
+
+    _fields_ = [
+        ("kernel", ctypes.c_int), ("variant", ctypes.c_int), ("bm", ctypes.c_int), ("bn", ctypes.c_int),
+        ("bk", ctypes.c_int), ("splits", ctypes.c_int), ("stages", ctypes.c_int), ("grid_x", ctypes.c_int),
+        ("grid_y", ctypes.c_int), ("grid_z", ctypes.c_int), ("threads", ctypes.c_int),
+        ("workspace_bytes", ctypes.c_longlong),
+    ]
+
+    def as_dict(self) -> dict:
+        d = {name: getattr(self, name) for name, _ in self._fields_}
+        d["kernel_name"] = KERNEL_NAMES.get(self.kernel, "?")
+        return d
+
+    def __repr__(self):
+        return f"Plan({self.as_dict()})"
+
+
+class LinError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = library().lin_strerror(status).decode()
+        super().__init__(f"{what}: status {status} ({msg})" if what else f"status {status} ({msg})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"CUDA library not built ({_LIB_PATH} missing); run "
+                    "`python -m transformer_linear_layer_gb300.build` or __graft_entry__.build()")
+            lib = ctypes.CDLL(_LIB_PATH)
+            P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            PP = ctypes.POINTER(Plan)
+            sig = {
+                "lin_create": ([ctypes.POINTER(P), I, Z], I),
+                "lin_destroy": ([P], I),
+                "lin_forward": ([P, I, I, I, P, P, P, P, I, I, P], I),
+                "lin_forward_plan": ([P, PP, I, I, I, P, P, P, P, I, I, P], I),
+                "lin_plan_query": ([I, I, I, I, I, I, Z, PP], I),
+                "lin_plan_make": ([I, I, I, I, I, I, I, I, PP], I),
+                "lin_check_device": ([P, P], I),
+                "lin_ctx_info": ([P, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(Z)], I),
+                "lin_strerror": ([I], ctypes.c_char_p),
+                "lin_abi_version": ([], I),
+            }
+            for name, (args, res) in sig.items():
+                f = getattr(lib, name)
+                f.argtypes = args
+                f.restype = res
+            _lib = lib
+    return _lib
+
+
+def _prec(p) -> int:
+    return _PREC_NAMES[p] if isinstance(p, str) else int(p)
+
+
+def _epi(e) -> int:
+    return _EPI_NAMES[e] if (e is None or isinstance(e, str)) else int(e)
+
+
+def plan_query(sm_count: int, M: int, N: int, K: int, precision="bf16", epilogue="none",
+               workspace_bytes: int = 64 << 20) -> Plan:
+    """The dispatch table's plan for a shape (host only, no GPU needed)."""
+    p = Plan()
+    rc = library().lin_plan_query(sm_count, M, N, K, _prec(precision), _epi(epilogue), workspace_bytes,
+                                  ctypes.byref(p))
+    if rc != OK:
+        raise LinError(rc, "lin_plan_query")
+    return p
+
+
+def plan_make(sm_count: int, kernel: int, variant: int, splits: int, M: int, N: int, K: int,
+              precision="bf16") -> Plan:
+    """A plan for one kernel family / tile configuration (host only)."""
+    p = Plan()
+    rc = library().lin_plan_make(sm_count, kernel, variant, splits, M, N, K, _prec(precision), ctypes.byref(p))
+    if rc != OK:
+        raise LinError(rc, "lin_plan_make")
+    return p
+
+
+class Context:
+    """Owns a ``lin_ctx``: device, split-K workspace and the device status word."""
+
+    def __init__(self, device: int = 0, workspace_bytes: int = 0):
+        self._h = ctypes.c_void_p()
+        rc = library().lin_create(ctypes.byref(self._h), int(device), int(workspace_bytes))
+        if rc != OK:
+            raise LinError(rc, "lin_create")
+        dev, sms, ws = ctypes.c_int(), ctypes.c_int(), ctypes.c_size_t()
+        library().lin_ctx_info(self._h, ctypes.byref(dev), ctypes.byref(sms), ctypes.byref(ws))
+        self.device, self.sm_count, self.workspace_bytes = dev.value, sms.value, ws.value
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if self._h:
+            library().lin_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def check(self, stream=None):
+        """Synchronise and raise if a kernel reported a timeout (status word)."""
+        rc = library().lin_check_device(self._h, _stream_ptr(stream, self.device))
+        if rc != OK:
+            raise LinError(rc, "lin_check_device")
+
+    def plan(self, M, N, K, precision="bf16", epilogue="none") -> Plan:
+        return plan_query(self.sm_count, M, N, K, precision, epilogue, self.workspace_bytes)
+
+    # raw-pointer calls (the C ABI, one to one) ---------------------------------
+    def forward_ptr(self, M, N, K, X, W, bias, Y, epilogue, precision, stream) -> int:
+        return library().lin_forward(self._h, M, N, K, X, W, bias, Y, _epi(epilogue), _prec(precision), stream)
+
+    def forward_plan_ptr(self, plan: Plan, M, N, K, X, W, bias, Y, epilogue, precision, stream) -> int:
+        return library().lin_forward_plan(self._h, ctypes.byref(plan), M, N, K, X, W, bias, Y, _epi(epilogue),
+                                          _prec(precision), stream)
+
+
+def _stream_ptr(stream, device):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+_contexts: dict = {}
+
+
+def default_context(device: int) -> Context:
+    with _lock:
+        ctx = _contexts.get(device)
+    if ctx is None:
+        ctx = Context(device)
+        with _lock:
+            _contexts.setdefault(device, ctx)
+            ctx = _contexts[device]
+    return ctx
+
+
+def _marshal(x, w, bias, out, precision):
+    import torch
+
+    prec = precision
+    if prec is None:
+        prec = "bf16" if x.dtype == torch.bfloat16 else "fp32"
+    prec = _prec(prec)
+    want = torch.bfloat16 if prec == PREC_BF16 else torch.float32
+    if x.dtype != want or w.dtype != want:
+        raise TypeError(f"precision {prec} needs {want} X and W, got {x.dtype} and {w.dtype}")
+    if not (x.is_cuda and w.is_cuda):
+        raise ValueError("X and W must be CUDA tensors")
+    if x.dim() != 2 or w.dim() != 2 or x.shape[1] != w.shape[1]:
+        raise ValueError(f"need X (M x K) and W (N x K), got {tuple(x.shape)} and {tuple(w.shape)}")
+    if not (x.is_contiguous() and w.is_contiguous()):
+        raise ValueError("X and W must be contiguous row-major")
+    M, K = x.shape
+    N = w.shape[0]
+    if bias is not None:
+        if bias.dtype != torch.float32 or not bias.is_cuda or bias.shape != (N,) or not bias.is_contiguous():
+            raise ValueError("bias must be a contiguous fp32 CUDA vector of length N")
+    if out is None:
+        out = torch.empty((M, N), dtype=want, device=x.device)
+    elif out.dtype != want or out.shape != (M, N) or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("out must be a contiguous M x N CUDA tensor of the output dtype")
+    return prec, M, N, K, out
+
+
+def forward(x, w, bias=None, epilogue="none", precision=None, out=None, ctx: Context | None = None, stream=None):
+    """Y = act(x . w^T + bias) on x's device, asynchronously on the current stream.
+
+    x: M x K, w: N x K (bf16 for precision "bf16", fp32 for "fp32"/"tf32"),
+    bias: fp32 length N or None, epilogue: "none" | "gelu". Returns Y (M x N).
+    """
+    prec, M, N, K, out = _marshal(x, w, bias, out, precision)
+    dev = x.device.index if x.device.index is not None else 0
+    ctx = ctx or default_context(dev)
+    rc = ctx.forward_ptr(M, N, K, x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(),
+                         out.data_ptr(), epilogue, prec, _stream_ptr(stream, dev))
+    if rc != OK:
+        raise LinError(rc, "lin_forward")
+    return out
+
+
+def forward_plan(plan: Plan, x, w, bias=None, epilogue="none", precision=None, out=None,
+                 ctx: Context | None = None, stream=None):
+    """As :func:`forward` with an explicit launch configuration."""
+    prec, M, N, K, out = _marshal(x, w, bias, out, precision)
+    dev = x.device.index if x.device.index is not None else 0
+    ctx = ctx or default_context(dev)
+    rc = ctx.forward_plan_ptr(plan, M, N, K, x.data_ptr(), w.data_ptr(),
+                              None if bias is None else bias.data_ptr(), out.data_ptr(), epilogue, prec,
+                              _stream_ptr(stream, dev))
+    if rc != OK:
+        raise LinError(rc, "lin_forward_plan")
+    return out

@@ -1,0 +1,58 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/lin.h"
+
+namespace lin {
+
+// Everything one launch needs; filled by the C ABI layer after validation.
+struct Problem {
+    int M, N, K;
+    const void* X;
+    const void* W;
+    const float* bias;
+    void* Y;
+    int epilogue;   // lin_epilogue
+    int precision;  // lin_precision
+    cudaStream_t stream;
+    // context resources
+    void* workspace;          // split-K partials (float) followed by tile counters (unsigned)
+    size_t workspace_bytes;
+    int* dev_status;          // device status word (LIN_ERR_DEVICE_TIMEOUT when a wait gave up)
+    int sm_count;
+};
+
+// Workspace layout helper: partial sums first, counters 256-byte aligned after.
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline size_t splitk_partial_bytes(int splits, int M, int N) {
+    return splits > 1 ? align_up((size_t)splits * (size_t)M * (size_t)N * sizeof(float), 256) : 0;
+}
+inline size_t splitk_workspace_bytes(int splits, int M, int N, int tiles) {
+    return splits > 1 ? splitk_partial_bytes(splits, M, N) + align_up((size_t)tiles * sizeof(unsigned), 256) : 0;
+}
+
+// Tile configurations per kernel family (variant ids in lin_plan).
+struct SkinnyCfg { int warps, groups, unroll; };   // rows per CTA = warps * groups * 8
+constexpr int kSkinnyVariants = 4;
+constexpr SkinnyCfg kSkinnyCfg[kSkinnyVariants] = {{4, 2, 4}, {8, 1, 4}, {4, 4, 2}, {8, 2, 2}};
+
+struct FfmaCfg { int bm, bn, bk, tm, tn; };        // 256 threads each
+constexpr int kFfmaVariants = 2;
+constexpr FfmaCfg kFfmaCfg[kFfmaVariants] = {{128, 128, 16, 8, 8}, {64, 64, 16, 4, 4}};
+
+struct TcCfg { int bn, stages; };                  // BM = 128, BK = 128 bytes of K
+constexpr int kTcVariants = 2;
+constexpr TcCfg kTcCfg[kTcVariants] = {{256, 4}, {128, 6}};
+constexpr int kTcThreads = 192;                    // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+
+// Launchers (return LIN_OK or LIN_ERR_*). They assume the plan was validated.
+int launch_fill(const Problem& p);
+int launch_skinny(const Problem& p, const lin_plan& plan);
+int launch_ffma(const Problem& p, const lin_plan& plan);
+int launch_tc(const Problem& p, const lin_plan& plan);
+
+}  // namespace lin

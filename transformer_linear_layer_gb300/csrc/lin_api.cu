@@ -1,0 +1,408 @@
+// C ABI of the linear-layer library: context, argument validation, the
+// per-shape dispatch table and the launches. No host fallback exists: when a
+// kernel cannot run, the call returns an error.
+//
+// Dispatch ("Optimizing a GPT-2-class transformer on a GPU", Act II: route each
+// shape to its measured winner; "Writing a CUDA matmul that catches cuBLAS",
+// "One kernel was never going to be enough": tile and split chosen per shape):
+//   BF16, M <= 16        -> skinny split-K W stream (HBM-bound)
+//   BF16, M > 16 ; TF32  -> tcgen05 kernel, N tile chosen for wave efficiency
+//   FP32                 -> FFMA kernel; 64x64 tiles + split-K when 128x128
+//                           tiles cannot fill the SMs
+//   K == 0               -> fill Y = act(bias)
+#include <climits>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "internal.h"
+#include "device_common.cuh"
+
+struct lin_ctx {
+    int device;
+    int sm_count;
+    void* workspace;
+    size_t workspace_bytes;
+    int* dev_status;
+};
+
+namespace lin {
+namespace {
+
+template <bool BF16, bool GELU>
+__global__ void fill_kernel(int M, int N, const float* bias, void* Y) {
+    const size_t total = (size_t)M * N;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const int n = (int)(i % N);
+        const float v = epilogue<GELU>(0.f, bias ? bias[n] : 0.f);
+        if constexpr (BF16)
+            static_cast<uint16_t*>(Y)[i] = f32_to_bf16_bits(v);
+        else
+            static_cast<float*>(Y)[i] = v;
+    }
+}
+
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+// Fraction of SM slots busy over the waves a grid of `ctas` needs.
+double wave_efficiency(long long ctas, long long slots) {
+    const long long waves = (ctas + slots - 1) / slots;
+    return waves ? (double)ctas / (double)(waves * slots) : 0.0;
+}
+
+void plan_common(lin_plan* p, int kernel, int variant) {
+    std::memset(p, 0, sizeof(*p));
+    p->kernel = kernel;
+    p->variant = variant;
+    p->splits = 1;
+}
+
+int make_skinny(int sm, int variant, int splits, int M, int N, int K, size_t ws, lin_plan* p) {
+    if (variant < 0 || variant >= kSkinnyVariants || M > 16 || M < 1 || N < 1 || K < 1) return LIN_ERR_UNSUPPORTED;
+    const SkinnyCfg c = kSkinnyCfg[variant];
+    const int rows = c.warps * c.groups * 8;
+    const int tiles = ceil_div(N, rows);
+    const int nchunks = ceil_div(K, 32);
+    int S = splits;
+    if (S <= 0) {
+        // About four CTAs per SM in one wave; each split keeps >= 2 rounds of loads.
+        const int target = 4 * sm;
+        S = ceil_div(target, tiles);
+        const int max_s = nchunks / (2 * c.unroll) > 1 ? nchunks / (2 * c.unroll) : 1;
+        if (S > max_s) S = max_s;
+        if (S < 1) S = 1;
+        while (S > 1 && splitk_workspace_bytes(S, M, N, tiles) > ws) --S;
+    }
+    if (S > nchunks) S = nchunks;
+    plan_common(p, LIN_KERNEL_SKINNY, variant);
+    p->bm = 16;
+    p->bn = rows;
+    p->bk = 32;
+    p->splits = S;
+    p->grid_x = tiles;
+    p->grid_y = S;
+    p->grid_z = 1;
+    p->threads = c.warps * 32;
+    p->workspace_bytes = (long long)splitk_workspace_bytes(S, M, N, tiles);
+    return LIN_OK;
+}
+
+int make_ffma(int sm, int variant, int splits, int M, int N, int K, size_t ws, lin_plan* p) {
+    if (M < 1 || N < 1 || K < 1) return LIN_ERR_UNSUPPORTED;
+    if (variant < 0) {
+        // 128x128 tiles when they give at least one full wave, else 64x64 + split-K.
+        const long long big = (long long)ceil_div(M, kFfmaCfg[0].bm) * ceil_div(N, kFfmaCfg[0].bn);
+        variant = big >= sm ? 0 : 1;
+    }
+    if (variant >= kFfmaVariants) return LIN_ERR_UNSUPPORTED;
+    const FfmaCfg c = kFfmaCfg[variant];
+    const int gx = ceil_div(N, c.bn), gy = ceil_div(M, c.bm);
+    const int tiles = gx * gy;
+    const int nkb = ceil_div(K, c.bk);
+    int S = splits;
+    if (S <= 0) {
+        S = tiles >= sm ? 1 : ceil_div(sm, tiles);
+        const int max_s = nkb / 4 > 1 ? nkb / 4 : 1;  // >= 4 K steps per split
+        if (S > max_s) S = max_s;
+        while (S > 1 && splitk_workspace_bytes(S, M, N, tiles) > ws) --S;
+    }
+    if (S > nkb) S = nkb;
+    plan_common(p, LIN_KERNEL_FFMA, variant);
+    p->bm = c.bm;
+    p->bn = c.bn;
+    p->bk = c.bk;
+    p->splits = S;
+    p->grid_x = gx;
+    p->grid_y = gy;
+    p->grid_z = S;
+    p->threads = 256;
+    p->workspace_bytes = (long long)splitk_workspace_bytes(S, M, N, tiles);
+    return LIN_OK;
+}
+
+int make_tc(int sm, int variant, int M, int N, int K, lin_plan* p) {
+    if (M < 1 || N < 1 || K < 1) return LIN_ERR_UNSUPPORTED;
+    if (variant < 0) {
+        // Pick the N tile with the better wave efficiency; ties go to the wider tile.
+        const long long t0 = (long long)ceil_div(M, 128) * ceil_div(N, kTcCfg[0].bn);
+        const long long t1 = (long long)ceil_div(M, 128) * ceil_div(N, kTcCfg[1].bn);
+        variant = wave_efficiency(t1, sm) > wave_efficiency(t0, sm) + 0.02 ? 1 : 0;
+    }
+    if (variant >= kTcVariants) return LIN_ERR_UNSUPPORTED;
+    plan_common(p, LIN_KERNEL_TC, variant);
+    p->bm = 128;
+    p->bn = kTcCfg[variant].bn;
+    p->bk = 0;  // 128 bytes of K: 64 bf16 or 32 fp32
+    p->stages = kTcCfg[variant].stages;
+    p->grid_x = ceil_div(N, p->bn);
+    p->grid_y = ceil_div(M, 128);
+    p->grid_z = 1;
+    p->threads = kTcThreads;
+    return LIN_OK;
+}
+
+bool valid_enums(int epilogue, int precision) {
+    return (epilogue == LIN_EPI_NONE || epilogue == LIN_EPI_GELU_TANH) &&
+           (precision == LIN_PREC_FP32 || precision == LIN_PREC_TF32 || precision == LIN_PREC_BF16);
+}
+
+int plan_default(int sm, int M, int N, int K, int precision, size_t ws, lin_plan* p) {
+    if (M == 0 || N == 0) {
+        plan_common(p, LIN_KERNEL_NONE, 0);
+        return LIN_OK;
+    }
+    if (K == 0) {
+        plan_common(p, LIN_KERNEL_FILL, 0);
+        p->grid_x = ceil_div((long long)M * N, 256) < 4 * sm ? ceil_div((long long)M * N, 256) : 4 * sm;
+        p->grid_y = p->grid_z = 1;
+        p->threads = 256;
+        return LIN_OK;
+    }
+    switch (precision) {
+        case LIN_PREC_BF16:
+            if (M <= 16) return make_skinny(sm, 0, 0, M, N, K, ws, p);
+            return make_tc(sm, -1, M, N, K, p);
+        case LIN_PREC_TF32:
+            return make_tc(sm, -1, M, N, K, p);
+        default:
+            return make_ffma(sm, -1, 0, M, N, K, ws, p);
+    }
+}
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+    if (!a || !b || an == 0 || bn == 0) return false;
+    const char* pa = static_cast<const char*>(a);
+    const char* pb = static_cast<const char*>(b);
+    return pa < pb + bn && pb < pa + an;
+}
+
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+int check_plan_fits(const lin_plan& p, int M, int N, int K, int precision) {
+    switch (p.kernel) {
+        case LIN_KERNEL_NONE: return (M == 0 || N == 0) ? LIN_OK : LIN_ERR_UNSUPPORTED;
+        case LIN_KERNEL_FILL: return (K == 0 && p.grid_x > 0) ? LIN_OK : LIN_ERR_UNSUPPORTED;
+        case LIN_KERNEL_SKINNY: {
+            if (precision != LIN_PREC_BF16 || M > 16 || K == 0) return LIN_ERR_UNSUPPORTED;
+            if (p.variant < 0 || p.variant >= kSkinnyVariants || p.splits < 1) return LIN_ERR_UNSUPPORTED;
+            const SkinnyCfg c = kSkinnyCfg[p.variant];
+            if (p.grid_x != ceil_div(N, c.warps * c.groups * 8) || p.grid_y != p.splits ||
+                p.splits > ceil_div(K, 32))
+                return LIN_ERR_UNSUPPORTED;
+            return LIN_OK;
+        }
+        case LIN_KERNEL_FFMA: {
+            if (precision != LIN_PREC_FP32 || K == 0) return LIN_ERR_UNSUPPORTED;
+            if (p.variant < 0 || p.variant >= kFfmaVariants || p.splits < 1) return LIN_ERR_UNSUPPORTED;
+            const FfmaCfg c = kFfmaCfg[p.variant];
+            if (p.bk != c.bk || p.grid_x != ceil_div(N, c.bn) || p.grid_y != ceil_div(M, c.bm) ||
+                p.grid_z != p.splits || p.splits > ceil_div(K, c.bk))
+                return LIN_ERR_UNSUPPORTED;
+            return LIN_OK;
+        }
+        case LIN_KERNEL_TC: {
+            if (precision == LIN_PREC_FP32 || K == 0) return LIN_ERR_UNSUPPORTED;
+            if (p.variant < 0 || p.variant >= kTcVariants || p.splits != 1) return LIN_ERR_UNSUPPORTED;
+            if (p.bn != kTcCfg[p.variant].bn || p.grid_x != ceil_div(N, p.bn) || p.grid_y != ceil_div(M, 128))
+                return LIN_ERR_UNSUPPORTED;
+            return LIN_OK;
+        }
+        default: return LIN_ERR_UNSUPPORTED;
+    }
+}
+
+int run(lin_ctx* ctx, const lin_plan& plan, int M, int N, int K, const void* X, const void* W, const float* bias,
+        void* Y, int epilogue, int precision, void* stream) {
+    if (!ctx || M < 0 || N < 0 || K < 0 || !valid_enums(epilogue, precision)) return LIN_ERR_ARG;
+    if (M == 0 || N == 0) return plan.kernel == LIN_KERNEL_NONE ? LIN_OK : LIN_ERR_UNSUPPORTED;
+    if (!Y || (K > 0 && (!X || !W))) return LIN_ERR_ARG;
+    const size_t ein = precision == LIN_PREC_BF16 ? 2 : 4;
+    const size_t eout = ein;
+    const size_t ybytes = (size_t)M * N * eout;
+    if (overlaps(Y, ybytes, X, (size_t)M * K * ein) || overlaps(Y, ybytes, W, (size_t)N * K * ein) ||
+        overlaps(Y, ybytes, bias, bias ? (size_t)N * 4 : 0))
+        return LIN_ERR_ARG;
+    if (K > 0 && (((uintptr_t)X | (uintptr_t)W) % 16 != 0 || ((size_t)K * ein) % 16 != 0)) return LIN_ERR_ALIGN;
+    if (((uintptr_t)Y % eout) != 0 || ((uintptr_t)bias % 4) != 0) return LIN_ERR_ALIGN;
+    const int fit = check_plan_fits(plan, M, N, K, precision);
+    if (fit != LIN_OK) return fit;
+    if ((size_t)plan.workspace_bytes > ctx->workspace_bytes) return LIN_ERR_WORKSPACE;
+
+    DeviceGuard guard(ctx->device);
+    if (!guard.ok) return LIN_ERR_CUDA;
+    Problem p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.X = X;
+    p.W = W;
+    p.bias = bias;
+    p.Y = Y;
+    p.epilogue = epilogue;
+    p.precision = precision;
+    p.stream = static_cast<cudaStream_t>(stream);
+    p.workspace = ctx->workspace;
+    p.workspace_bytes = ctx->workspace_bytes;
+    p.dev_status = ctx->dev_status;
+    p.sm_count = ctx->sm_count;
+    switch (plan.kernel) {
+        case LIN_KERNEL_FILL: return launch_fill(p);
+        case LIN_KERNEL_SKINNY: return launch_skinny(p, plan);
+        case LIN_KERNEL_FFMA: return launch_ffma(p, plan);
+        case LIN_KERNEL_TC: return launch_tc(p, plan);
+        default: return LIN_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace
+
+int launch_fill(const Problem& p) {
+    const long long total = (long long)p.M * p.N;
+    int grid = (int)((total + 255) / 256);
+    if (grid > 4 * p.sm_count) grid = 4 * p.sm_count;
+    if (grid < 1) grid = 1;
+    const bool bf16 = p.precision == LIN_PREC_BF16, gelu = p.epilogue == LIN_EPI_GELU_TANH;
+    if (bf16 && gelu) fill_kernel<true, true><<<grid, 256, 0, p.stream>>>(p.M, p.N, p.bias, p.Y);
+    else if (bf16) fill_kernel<true, false><<<grid, 256, 0, p.stream>>>(p.M, p.N, p.bias, p.Y);
+    else if (gelu) fill_kernel<false, true><<<grid, 256, 0, p.stream>>>(p.M, p.N, p.bias, p.Y);
+    else fill_kernel<false, false><<<grid, 256, 0, p.stream>>>(p.M, p.N, p.bias, p.Y);
+    return cudaGetLastError() == cudaSuccess ? LIN_OK : LIN_ERR_CUDA;
+}
+
+}  // namespace lin
+
+extern "C" {
+
+int lin_abi_version(void) { return LIN_ABI_VERSION; }
+
+const char* lin_strerror(int status) {
+    switch (status) {
+        case LIN_OK: return "success";
+        case LIN_ERR_ARG: return "invalid argument (NULL pointer, negative size, unknown enum, or Y overlapping an input)";
+        case LIN_ERR_ALIGN: return "misaligned operand (X and W need 16-byte alignment and K*element size a multiple of 16)";
+        case LIN_ERR_WORKSPACE: return "plan needs more workspace than the context holds";
+        case LIN_ERR_CUDA: return "CUDA runtime error or kernel launch failure";
+        case LIN_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait; its output is incomplete";
+        case LIN_ERR_UNSUPPORTED: return "the plan's kernel cannot run this shape or precision";
+        default: return "unknown status";
+    }
+}
+
+int lin_create(lin_ctx** out, int device, size_t max_workspace_bytes) {
+    if (!out) return LIN_ERR_ARG;
+    *out = nullptr;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
+        cudaGetLastError();
+        return LIN_ERR_CUDA;
+    }
+    lin::DeviceGuard guard(device);
+    if (!guard.ok) return LIN_ERR_CUDA;
+    lin_ctx* c = new (std::nothrow) lin_ctx();
+    if (!c) return LIN_ERR_CUDA;
+    c->device = device;
+    c->workspace_bytes = max_workspace_bytes ? max_workspace_bytes : ((size_t)64 << 20);
+    if (cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaMalloc(&c->workspace, c->workspace_bytes) != cudaSuccess ||
+        cudaMemset(c->workspace, 0, c->workspace_bytes) != cudaSuccess ||
+        cudaMalloc(reinterpret_cast<void**>(&c->dev_status), sizeof(int)) != cudaSuccess ||
+        cudaMemset(c->dev_status, 0, sizeof(int)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        if (c->workspace) cudaFree(c->workspace);
+        if (c->dev_status) cudaFree(c->dev_status);
+        delete c;
+        cudaGetLastError();
+        return LIN_ERR_CUDA;
+    }
+    *out = c;
+    return LIN_OK;
+}
+
+int lin_destroy(lin_ctx* ctx) {
+    if (!ctx) return LIN_OK;
+    int rc = LIN_OK;
+    {
+        lin::DeviceGuard guard(ctx->device);
+        if (cudaDeviceSynchronize() != cudaSuccess) rc = LIN_ERR_CUDA;
+        cudaFree(ctx->workspace);
+        cudaFree(ctx->dev_status);
+    }
+    delete ctx;
+    return rc;
+}
+
+int lin_ctx_info(const lin_ctx* ctx, int* device, int* sm_count, size_t* workspace_bytes) {
+    if (!ctx) return LIN_ERR_ARG;
+    if (device) *device = ctx->device;
+    if (sm_count) *sm_count = ctx->sm_count;
+    if (workspace_bytes) *workspace_bytes = ctx->workspace_bytes;
+    return LIN_OK;
+}
+
+int lin_plan_query(int sm_count, int M, int N, int K, int precision, int epilogue, size_t workspace_bytes,
+                   lin_plan* out) {
+    if (!out || sm_count < 1 || M < 0 || N < 0 || K < 0 || !lin::valid_enums(epilogue, precision)) return LIN_ERR_ARG;
+    return lin::plan_default(sm_count, M, N, K, precision, workspace_bytes, out);
+}
+
+int lin_plan_make(int sm_count, int kernel, int variant, int splits, int M, int N, int K, int precision,
+                  lin_plan* out) {
+    if (!out || sm_count < 1 || M < 0 || N < 0 || K < 0 || !lin::valid_enums(0, precision)) return LIN_ERR_ARG;
+    const size_t unlimited = (size_t)1 << 62;
+    switch (kernel) {
+        case LIN_KERNEL_SKINNY:
+            if (precision != LIN_PREC_BF16) return LIN_ERR_UNSUPPORTED;
+            return lin::make_skinny(sm_count, variant, splits, M, N, K, unlimited, out);
+        case LIN_KERNEL_FFMA:
+            if (precision != LIN_PREC_FP32) return LIN_ERR_UNSUPPORTED;
+            return lin::make_ffma(sm_count, variant, splits, M, N, K, unlimited, out);
+        case LIN_KERNEL_TC:
+            if (precision == LIN_PREC_FP32 || splits > 1) return LIN_ERR_UNSUPPORTED;
+            return lin::make_tc(sm_count, variant, M, N, K, out);
+        case LIN_KERNEL_NONE:
+        case LIN_KERNEL_FILL:
+            return lin::plan_default(sm_count, M, N, K, precision, unlimited, out);
+        default: return LIN_ERR_ARG;
+    }
+}
+
+int lin_forward(lin_ctx* ctx, int M, int N, int K, const void* X, const void* W, const float* bias, void* Y,
+                int epilogue, int precision, void* stream) {
+    if (!ctx || M < 0 || N < 0 || K < 0 || !lin::valid_enums(epilogue, precision)) return LIN_ERR_ARG;
+    lin_plan plan;
+    const int rc = lin::plan_default(ctx->sm_count, M, N, K, precision, ctx->workspace_bytes, &plan);
+    if (rc != LIN_OK) return rc;
+    return lin::run(ctx, plan, M, N, K, X, W, bias, Y, epilogue, precision, stream);
+}
+
+int lin_forward_plan(lin_ctx* ctx, const lin_plan* plan, int M, int N, int K, const void* X, const void* W,
+                     const float* bias, void* Y, int epilogue, int precision, void* stream) {
+    if (!plan) return LIN_ERR_ARG;
+    return lin::run(ctx, *plan, M, N, K, X, W, bias, Y, epilogue, precision, stream);
+}
+
+int lin_check_device(lin_ctx* ctx, void* stream) {
+    if (!ctx) return LIN_ERR_ARG;
+    lin::DeviceGuard guard(ctx->device);
+    if (!guard.ok) return LIN_ERR_CUDA;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LIN_ERR_CUDA;
+    int status = 0;
+    if (cudaMemcpy(&status, ctx->dev_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return LIN_ERR_CUDA;
+    if (status != 0) {
+        if (cudaMemset(ctx->dev_status, 0, sizeof(int)) != cudaSuccess) return LIN_ERR_CUDA;
+        return status;
+    }
+    return LIN_OK;
+}
+
+}  // extern "C"
