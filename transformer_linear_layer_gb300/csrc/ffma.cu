@@ -253,9 +253,8 @@ int launch_ffma(const Problem& p, const lin_plan& plan) {
     a.ws = nullptr;
     a.counters = nullptr;
     if (plan.splits > 1) {
-        a.ws = static_cast<float*>(p.workspace);
-        a.counters = reinterpret_cast<unsigned*>(static_cast<char*>(p.workspace) +
-                                                 splitk_partial_bytes(plan.splits, p.M, p.N));
+        a.ws = splitk_partials(p.workspace);
+        a.counters = splitk_counters(p.workspace);
     }
     const dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
     const bool gelu = p.epilogue == LIN_EPI_GELU_TANH;

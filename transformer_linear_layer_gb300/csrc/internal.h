@@ -26,14 +26,18 @@ struct Problem {
     int sm_count;
 };
 
-// Workspace layout helper: partial sums first, counters 256-byte aligned after.
+// Workspace layout for split-K: a fixed block of per-tile arrival counters at
+// the start (zero between launches: the last CTA of a tile re-arms its counter),
+// then the partial sums [split][M][N] in fp32. The counters never move, so no
+// launch's partial sums can overwrite another launch's counters.
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-inline size_t splitk_partial_bytes(int splits, int M, int N) {
-    return splits > 1 ? align_up((size_t)splits * (size_t)M * (size_t)N * sizeof(float), 256) : 0;
+constexpr size_t kCounterBytes = 64 * 1024;
+constexpr int kMaxSplitTiles = (int)(kCounterBytes / sizeof(unsigned));
+inline size_t splitk_workspace_bytes(int splits, int M, int N) {
+    return splits > 1 ? kCounterBytes + align_up((size_t)splits * (size_t)M * (size_t)N * sizeof(float), 256) : 0;
 }
-inline size_t splitk_workspace_bytes(int splits, int M, int N, int tiles) {
-    return splits > 1 ? splitk_partial_bytes(splits, M, N) + align_up((size_t)tiles * sizeof(unsigned), 256) : 0;
-}
+inline unsigned* splitk_counters(void* ws) { return static_cast<unsigned*>(ws); }
+inline float* splitk_partials(void* ws) { return reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes); }
 
 // Tile configurations per kernel family (variant ids in lin_plan).
 struct SkinnyCfg { int warps, groups, unroll; };   // rows per CTA = warps * groups * 8

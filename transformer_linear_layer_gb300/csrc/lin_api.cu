@@ -71,9 +71,10 @@ int make_skinny(int sm, int variant, int splits, int M, int N, int K, size_t ws,
         const int max_s = nchunks / (2 * c.unroll) > 1 ? nchunks / (2 * c.unroll) : 1;
         if (S > max_s) S = max_s;
         if (S < 1) S = 1;
-        while (S > 1 && splitk_workspace_bytes(S, M, N, tiles) > ws) --S;
+        while (S > 1 && splitk_workspace_bytes(S, M, N) > ws) --S;
     }
     if (S > nchunks) S = nchunks;
+    if (tiles > kMaxSplitTiles) S = 1;
     plan_common(p, LIN_KERNEL_SKINNY, variant);
     p->bm = 16;
     p->bn = rows;
@@ -83,7 +84,7 @@ int make_skinny(int sm, int variant, int splits, int M, int N, int K, size_t ws,
     p->grid_y = S;
     p->grid_z = 1;
     p->threads = c.warps * 32;
-    p->workspace_bytes = (long long)splitk_workspace_bytes(S, M, N, tiles);
+    p->workspace_bytes = (long long)splitk_workspace_bytes(S, M, N);
     return LIN_OK;
 }
 
@@ -104,9 +105,10 @@ int make_ffma(int sm, int variant, int splits, int M, int N, int K, size_t ws, l
         S = tiles >= sm ? 1 : ceil_div(sm, tiles);
         const int max_s = nkb / 4 > 1 ? nkb / 4 : 1;  // >= 4 K steps per split
         if (S > max_s) S = max_s;
-        while (S > 1 && splitk_workspace_bytes(S, M, N, tiles) > ws) --S;
+        while (S > 1 && splitk_workspace_bytes(S, M, N) > ws) --S;
     }
     if (S > nkb) S = nkb;
+    if (tiles > kMaxSplitTiles) S = 1;
     plan_common(p, LIN_KERNEL_FFMA, variant);
     p->bm = c.bm;
     p->bn = c.bn;
@@ -116,7 +118,7 @@ int make_ffma(int sm, int variant, int splits, int M, int N, int K, size_t ws, l
     p->grid_y = gy;
     p->grid_z = S;
     p->threads = 256;
-    p->workspace_bytes = (long long)splitk_workspace_bytes(S, M, N, tiles);
+    p->workspace_bytes = (long long)splitk_workspace_bytes(S, M, N);
     return LIN_OK;
 }
 
@@ -198,7 +200,7 @@ int check_plan_fits(const lin_plan& p, int M, int N, int K, int precision) {
             if (p.variant < 0 || p.variant >= kSkinnyVariants || p.splits < 1) return LIN_ERR_UNSUPPORTED;
             const SkinnyCfg c = kSkinnyCfg[p.variant];
             if (p.grid_x != ceil_div(N, c.warps * c.groups * 8) || p.grid_y != p.splits ||
-                p.splits > ceil_div(K, 32))
+                p.splits > ceil_div(K, 32) || (p.splits > 1 && p.grid_x > kMaxSplitTiles))
                 return LIN_ERR_UNSUPPORTED;
             return LIN_OK;
         }
@@ -207,7 +209,8 @@ int check_plan_fits(const lin_plan& p, int M, int N, int K, int precision) {
             if (p.variant < 0 || p.variant >= kFfmaVariants || p.splits < 1) return LIN_ERR_UNSUPPORTED;
             const FfmaCfg c = kFfmaCfg[p.variant];
             if (p.bk != c.bk || p.grid_x != ceil_div(N, c.bn) || p.grid_y != ceil_div(M, c.bm) ||
-                p.grid_z != p.splits || p.splits > ceil_div(K, c.bk))
+                p.grid_z != p.splits || p.splits > ceil_div(K, c.bk) ||
+                (p.splits > 1 && (long long)p.grid_x * p.grid_y > kMaxSplitTiles))
                 return LIN_ERR_UNSUPPORTED;
             return LIN_OK;
         }
