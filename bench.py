@@ -310,7 +310,8 @@ def bench_ours(layer: si.Layer, steps: int, warmup: int, world: int, rank: int, 
         value, unit = world * steps * layer.flops / max_s / 1e12, "TFLOP/s"
 
     peaks, src = load_peaks()
-    kfile = {tll.KERNEL_SKINNY: "skinny.cu", tll.KERNEL_FFMA: "ffma.cu", tll.KERNEL_TC: "tc.cu"}.get(plan.kernel)
+    kfile = {tll.KERNEL_SKINNY: "skinny.cu", tll.KERNEL_SKINNY_SK: "skinny_sk.cu", tll.KERNEL_FFMA: "ffma.cu",
+             tll.KERNEL_TC: "tc.cu"}.get(plan.kernel)
     traffic = traffic_from_profile(kfile, layer.name) if kfile else None
     roof = roofline_for(layer, per_launch_s, peaks, src, traffic)
 
@@ -363,7 +364,7 @@ def bench_ours(layer: si.Layer, steps: int, warmup: int, world: int, rank: int, 
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "parity_gate": {"rel_err": err, "tol": tol, "compared": gate}},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-        "gpu_launches": steps * (1 if plan.kernel in (tll.KERNEL_SKINNY, tll.KERNEL_FFMA, tll.KERNEL_TC) else 0),
+        "gpu_launches": steps * (0 if plan.kernel in (tll.KERNEL_NONE,) else 1),
     }
     ctx.close()
     return line

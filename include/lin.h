@@ -76,9 +76,10 @@ typedef enum {
 typedef enum {
     LIN_KERNEL_NONE = 0,   /* M == 0 or N == 0: nothing to do */
     LIN_KERNEL_FILL = 1,   /* K == 0: Y = act(bias) (or act(0)) */
-    LIN_KERNEL_SKINNY = 2, /* M <= 16, BF16: split-K W-streaming kernel, 128-bit loads */
+    LIN_KERNEL_SKINNY = 2, /* M <= 16, BF16: W stream, split-K across a thread-block cluster (no workspace) */
     LIN_KERNEL_FFMA = 3,   /* FP32: register-tiled FFMA, optional split-K */
-    LIN_KERNEL_TC = 4      /* TF32 / BF16: TMA + tcgen05 + TMEM, fused epilogue */
+    LIN_KERNEL_TC = 4,     /* TF32 / BF16: TMA + tcgen05 + TMEM, fused epilogue */
+    LIN_KERNEL_SKINNY_SK = 5 /* M <= 16, BF16: stream-K W stream over all SMs, workspace reduction */
 } lin_kernel;
 
 /* One launch configuration, chosen by the dispatch table or given explicitly.
@@ -152,6 +153,20 @@ LIN_API int lin_plan_make(int sm_count, int kernel, int variant, int splits, int
  * a bounded wait (its output is then incomplete), LIN_ERR_CUDA on a CUDA
  * error, LIN_OK otherwise. */
 LIN_API int lin_check_device(lin_ctx* ctx, void* stream);
+
+/* Context options (lin_set_option).
+ * LIN_OPT_EARLY_START (default 1): kernels that stream W may be launched as
+ *   programmatic dependents of the previous kernel on the stream and start
+ *   copying W before that kernel finishes; X and bias are read, and Y written,
+ *   only after it has finished. The library drops the early start by itself
+ *   when W overlaps the previous call's output on that stream. 0 = every call
+ *   waits for the previous kernel before it starts. */
+typedef enum {
+    LIN_OPT_EARLY_START = 1
+} lin_option;
+
+/* Set a context option. LIN_ERR_ARG for an unknown option or value. */
+LIN_API int lin_set_option(lin_ctx* ctx, int option, long long value);
 
 /* SM count and device ordinal of a context (host values, no GPU call). */
 LIN_API int lin_ctx_info(const lin_ctx* ctx, int* device, int* sm_count, size_t* workspace_bytes);

@@ -71,9 +71,8 @@ def kname(p):
 def test_dispatch_skinny_for_small_m_bf16():
     for M in (1, 8, 16):
         p = tll.plan_query(SM, M, 4096, 4096, "bf16")
-        assert kname(p) == "skinny"
-        assert p.splits > 1 and p.grid_y == p.splits
-        assert p.grid_x * p.bn >= 4096
+        assert kname(p) == "skinny" and p.splits > 1 and p.grid_y == p.splits
+        assert p.grid_x * p.bn >= 4096 and p.grid_x * p.grid_y <= SM
     assert kname(tll.plan_query(SM, 17, 4096, 4096, "bf16")) == "tc"
 
 
@@ -107,17 +106,37 @@ def test_dispatch_degenerate_shapes():
 
 
 def test_split_respects_workspace():
-    roomy = tll.plan_query(SM, 16, 4096, 4096, "bf16", workspace_bytes=64 << 20)
-    tight = tll.plan_query(SM, 16, 4096, 4096, "bf16", workspace_bytes=1 << 20)
-    none = tll.plan_query(SM, 16, 4096, 4096, "bf16", workspace_bytes=0)
-    assert roomy.workspace_bytes <= 64 << 20 and tight.workspace_bytes <= 1 << 20
+    roomy = tll.plan_query(SM, 128, 768, 3072, "fp32", workspace_bytes=64 << 20)
+    tight = tll.plan_query(SM, 128, 768, 3072, "fp32", workspace_bytes=2 << 20)
+    none = tll.plan_query(SM, 128, 768, 3072, "fp32", workspace_bytes=0)
+    assert roomy.splits > 1
+    assert roomy.workspace_bytes <= 64 << 20 and tight.workspace_bytes <= 2 << 20
     assert tight.splits <= roomy.splits and none.splits == 1 and none.workspace_bytes == 0
+
+
+def test_skinny_needs_no_workspace():
+    p = tll.plan_query(SM, 16, 4096, 4096, "bf16", workspace_bytes=0)
+    assert kname(p) == "skinny" and p.splits in (1, 2, 4, 8) and p.workspace_bytes == 0
+
+
+def test_skinny_stream_k_with_workspace():
+    p = tll.plan_make(SM, tll.KERNEL_SKINNY_SK, 0, 0, 16, 4096, 4096, "bf16")
+    assert kname(p) == "skinny_sk" and p.grid_x == SM and 0 < p.workspace_bytes <= 4 << 20
+    for v in range(5):
+        for width in (0, 2 * SM, 100):
+            q = tll.plan_make(SM, tll.KERNEL_SKINNY_SK, v, width, 16, 4096, 4096, "bf16")
+            assert q.grid_x == min(width or SM, 32 * (4096 // q.bk)) and q.splits == q.grid_x
+    tiny = tll.plan_make(SM, tll.KERNEL_SKINNY_SK, 0, 1, 3, 100, 64, "bf16")
+    assert tiny.grid_x == 1
 
 
 def test_plan_make_families():
     for v in range(4):
-        p = tll.plan_make(SM, tll.KERNEL_SKINNY, v, 5, 16, 4096, 4096, "bf16")
-        assert p.splits == 5 and p.grid_y == 5
+        for s in (1, 2, 4, 8):
+            p = tll.plan_make(SM, tll.KERNEL_SKINNY, v, s, 16, 4096, 4096, "bf16")
+            assert p.splits == s and p.grid_y == s and p.grid_x == 32
+    with pytest.raises(tll.LinError):
+        tll.plan_make(SM, tll.KERNEL_SKINNY, 0, 3, 16, 4096, 4096, "bf16")
     with pytest.raises(tll.LinError):
         tll.plan_make(SM, tll.KERNEL_SKINNY, 4, 0, 16, 4096, 4096, "bf16")
     with pytest.raises(tll.LinError):

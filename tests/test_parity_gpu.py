@@ -29,8 +29,11 @@ def all_plans(ctx, M, N, K, precision):
     sm = ctx.sm_count
     if precision == BF16 and M <= 16:
         for v in range(4):
-            for s in (0, 1, 3):
+            for s in (0, 1, 2, 8):
                 plans.append(tll.plan_make(sm, tll.KERNEL_SKINNY, v, s, M, N, K, "bf16"))
+        for v in range(5):
+            for width in (0, 2 * sm, 5):
+                plans.append(tll.plan_make(sm, tll.KERNEL_SKINNY_SK, v, width, M, N, K, "bf16"))
     if precision in (BF16, TF32):
         for v in range(2):
             plans.append(tll.plan_make(sm, tll.KERNEL_TC, v, 1, M, N, K, PREC_NAME[precision]))
@@ -227,16 +230,48 @@ def test_status_codes(ctx):
 
 def test_workspace_limit():
     small = tll.Context(0, workspace_bytes=4096)
-    x = torch.zeros((16, 4096), device="cuda", dtype=torch.bfloat16)
-    w = torch.zeros((4096, 4096), device="cuda", dtype=torch.bfloat16)
+    M, N, K = 128, 768, 3072
+    x = torch.zeros((M, K), device="cuda", dtype=torch.float32)
+    w = torch.zeros((N, K), device="cuda", dtype=torch.float32)
     # the dispatch table fits the split to the workspace (here: no split)...
-    assert small.plan(16, 4096, 4096).splits == 1
+    assert small.plan(M, N, K, "fp32").splits == 1
     tll.forward(x, w, ctx=small)
     # ...an explicit plan that needs more is refused
-    plan = tll.plan_make(small.sm_count, tll.KERNEL_SKINNY, 0, 8, 16, 4096, 4096, "bf16")
-    y = torch.empty((16, 4096), device="cuda", dtype=torch.bfloat16)
-    rc = small.forward_plan_ptr(plan, 16, 4096, 4096, x.data_ptr(), w.data_ptr(), None, y.data_ptr(), 0, 2,
+    plan = tll.plan_make(small.sm_count, tll.KERNEL_FFMA, 1, 6, M, N, K, "fp32")
+    assert plan.workspace_bytes > 4096
+    y = torch.empty((M, N), device="cuda", dtype=torch.float32)
+    rc = small.forward_plan_ptr(plan, M, N, K, x.data_ptr(), w.data_ptr(), None, y.data_ptr(), 0, 0,
                                 torch.cuda.current_stream().cuda_stream)
     assert rc == tll.ERR_WORKSPACE
     small.check()
     small.close()
+
+
+def test_back_to_back_calls_chain_through_outputs(ctx):
+    """Layer i+1 reads layer i's output (X = previous Y) and, in a second chain,
+    its weight is the previous output: both must match running the layers one
+    at a time (the early start must wait for X and must not prefetch a W that
+    the previous call writes)."""
+    M, N = 16, 512
+    X0, W, b = si.make_inputs(si.Layer("chain", M, N, N, BF16, bias=True))
+    x0, w, bias = device_inputs(X0, W, b, BF16)
+    outs = [x0]
+    for _ in range(6):
+        outs.append(tll.forward(outs[-1], w, bias, precision="bf16"))
+    torch.cuda.synchronize()
+    ref = x0
+    for i in range(6):
+        ref = tll.forward(ref, w, bias, precision="bf16")
+        torch.cuda.synchronize()
+        assert torch.equal(ref, outs[i + 1])
+    # W of call i+1 = Y of call i (N x N square so the shapes line up)
+    wsq = w.clone()
+    y1 = tll.forward(x0[:16], wsq, None, precision="bf16")          # 16 x 512
+    big = torch.empty((N, N), device="cuda", dtype=torch.bfloat16)
+    big[:16] = 0
+    tll.forward(wsq, wsq, None, precision="bf16", out=big)           # writes big (512 x 512)
+    y2 = tll.forward(x0, big, None, precision="bf16")                # reads big as W right after
+    torch.cuda.synchronize()
+    y2_ref = tll.forward(x0, big.clone(), None, precision="bf16")
+    torch.cuda.synchronize()
+    assert torch.equal(y2, y2_ref) and y1.shape == (16, N)

@@ -24,6 +24,9 @@ struct Problem {
     size_t workspace_bytes;
     int* dev_status;          // device status word (LIN_ERR_DEVICE_TIMEOUT when a wait gave up)
     int sm_count;
+    // The kernel may start (and prefetch W) before the previous kernel on the
+    // stream finishes: W does not overlap that kernel's output.
+    bool early_start;
 };
 
 // Workspace layout for split-K: a fixed block of per-tile arrival counters at
@@ -40,9 +43,14 @@ inline unsigned* splitk_counters(void* ws) { return static_cast<unsigned*>(ws); 
 inline float* splitk_partials(void* ws) { return reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes); }
 
 // Tile configurations per kernel family (variant ids in lin_plan).
-struct SkinnyCfg { int warps, groups, unroll; };   // rows per CTA = warps * groups * 8
+struct SkinnyCfg { int stages, kbox; };           // 128 W rows per cluster; splits = cluster size
 constexpr int kSkinnyVariants = 4;
-constexpr SkinnyCfg kSkinnyCfg[kSkinnyVariants] = {{4, 2, 4}, {8, 1, 4}, {4, 4, 2}, {8, 2, 2}};
+constexpr SkinnyCfg kSkinnyCfg[kSkinnyVariants] = {{3, 4}, {6, 1}, {3, 2}, {4, 3}};
+constexpr int kSkinnyThreads = 192;                // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+
+struct SkinnySkCfg { int stages, kbox; };          // stream-K skinny: K per stage = kbox * 64
+constexpr int kSkinnySkVariants = 5;
+constexpr SkinnySkCfg kSkinnySkCfg[kSkinnySkVariants] = {{6, 1}, {12, 1}, {3, 2}, {6, 2}, {3, 4}};
 
 struct FfmaCfg { int bm, bn, bk, tm, tn; };        // 256 threads each
 constexpr int kFfmaVariants = 2;
@@ -56,6 +64,8 @@ constexpr int kTcThreads = 192;                    // warp 0 TMA, warp 1 MMA, wa
 // Launchers (return LIN_OK or LIN_ERR_*). They assume the plan was validated.
 int launch_fill(const Problem& p);
 int launch_skinny(const Problem& p, const lin_plan& plan);
+int launch_skinny_sk(const Problem& p, const lin_plan& plan);
+size_t skinny_sk_workspace_bytes(int P, int M, int N, int K, int kbox);
 int launch_ffma(const Problem& p, const lin_plan& plan);
 int launch_tc(const Problem& p, const lin_plan& plan);
 

@@ -5,7 +5,8 @@
 // Dispatch ("Optimizing a GPT-2-class transformer on a GPU", Act II: route each
 // shape to its measured winner; "Writing a CUDA matmul that catches cuBLAS",
 // "One kernel was never going to be enough": tile and split chosen per shape):
-//   BF16, M <= 16        -> skinny split-K W stream (HBM-bound)
+//   BF16, M <= 16        -> skinny W stream (HBM-bound), split-K inside a
+//                           thread-block cluster, reduced through DSMEM
 //   BF16, M > 16 ; TF32  -> tcgen05 kernel, N tile chosen for wave efficiency
 //   FP32                 -> FFMA kernel; 64x64 tiles + split-K when 128x128
 //                           tiles cannot fill the SMs
@@ -13,6 +14,7 @@
 #include <climits>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "internal.h"
@@ -24,6 +26,7 @@ struct lin_ctx {
     void* workspace;
     size_t workspace_bytes;
     int* dev_status;
+    bool early_start;  // LIN_OPT_EARLY_START
 };
 
 namespace lin {
@@ -57,34 +60,57 @@ void plan_common(lin_plan* p, int kernel, int variant) {
     p->splits = 1;
 }
 
-int make_skinny(int sm, int variant, int splits, int M, int N, int K, size_t ws, lin_plan* p) {
+int make_skinny(int sm, int variant, int splits, int M, int N, int K, size_t /*ws*/, lin_plan* p) {
     if (variant < 0 || variant >= kSkinnyVariants || M > 16 || M < 1 || N < 1 || K < 1) return LIN_ERR_UNSUPPORTED;
     const SkinnyCfg c = kSkinnyCfg[variant];
-    const int rows = c.warps * c.groups * 8;
-    const int tiles = ceil_div(N, rows);
-    const int nchunks = ceil_div(K, 32);
+    const int tiles = ceil_div(N, 128);
+    const int kblocks = ceil_div(K, 64 * c.kbox);
     int S = splits;
     if (S <= 0) {
-        // About four CTAs per SM in one wave; each split keeps >= 2 rounds of loads.
-        const int target = 4 * sm;
-        S = ceil_div(target, tiles);
-        const int max_s = nchunks / (2 * c.unroll) > 1 ? nchunks / (2 * c.unroll) : 1;
-        if (S > max_s) S = max_s;
-        if (S < 1) S = 1;
-        while (S > 1 && splitk_workspace_bytes(S, M, N) > ws) --S;
+        // Cluster split-K: the largest power of two (<= 8, the portable cluster
+        // size) keeping the grid within one CTA per SM, and >= 1 K stage per CTA.
+        S = 1;
+        while (S < 8 && (long long)tiles * S * 2 <= sm && 2 * S <= kblocks) S *= 2;
     }
-    if (S > nchunks) S = nchunks;
-    if (tiles > kMaxSplitTiles) S = 1;
+    if (S != 1 && S != 2 && S != 4 && S != 8) return LIN_ERR_UNSUPPORTED;
     plan_common(p, LIN_KERNEL_SKINNY, variant);
     p->bm = 16;
-    p->bn = rows;
-    p->bk = 32;
+    p->bn = 128;
+    p->bk = 64 * c.kbox;
     p->splits = S;
+    p->stages = c.stages;
     p->grid_x = tiles;
     p->grid_y = S;
     p->grid_z = 1;
-    p->threads = c.warps * 32;
-    p->workspace_bytes = (long long)splitk_workspace_bytes(S, M, N);
+    p->threads = kSkinnyThreads;
+    p->workspace_bytes = 0;
+    return LIN_OK;
+}
+
+// Stream-K skinny over `width` CTAs (0 = one per SM, which leaves the second
+// shared-memory slot of each SM for the next call's early start).
+int make_skinny_sk(int sm, int variant, int width, int M, int N, int K, size_t ws, lin_plan* p) {
+    if (variant < 0 || variant >= kSkinnySkVariants || M > 16 || M < 1 || N < 1 || K < 1) return LIN_ERR_UNSUPPORTED;
+    if (width < 0 || width > 4 * sm) return LIN_ERR_UNSUPPORTED;
+    if (width == 0) width = sm;
+    const SkinnySkCfg c = kSkinnySkCfg[variant];
+    const int nrb = ceil_div(N, 128);
+    if (nrb > kMaxSplitTiles) return LIN_ERR_UNSUPPORTED;
+    const long long T = (long long)nrb * ceil_div(K, 64 * c.kbox);
+    const int P = (int)(T < (long long)width ? T : (long long)width);
+    const size_t need = skinny_sk_workspace_bytes(P, M, N, K, c.kbox);
+    if (need > ws) return LIN_ERR_WORKSPACE;
+    plan_common(p, LIN_KERNEL_SKINNY_SK, variant);
+    p->bm = 16;
+    p->bn = 128;
+    p->bk = 64 * c.kbox;
+    p->splits = P;
+    p->stages = c.stages;
+    p->grid_x = P;
+    p->grid_y = 1;
+    p->grid_z = 1;
+    p->threads = kSkinnyThreads;
+    p->workspace_bytes = (long long)need;
     return LIN_OK;
 }
 
@@ -191,16 +217,61 @@ struct DeviceGuard {
     }
 };
 
+// Output range of the last launch on each stream (process-wide): a kernel
+// that starts before its predecessor finishes may prefetch W only when W does
+// not overlap what that predecessor writes.
+struct LastOut {
+    cudaStream_t stream;
+    uintptr_t lo, hi;
+};
+std::mutex g_last_mu;
+LastOut g_last[64];
+int g_last_n = 0;
+
+bool early_start_ok(cudaStream_t st, const void* W, size_t wbytes, const void* Y, size_t ybytes) {
+    const uintptr_t wl = reinterpret_cast<uintptr_t>(W), wh = wl + wbytes;
+    std::lock_guard<std::mutex> lk(g_last_mu);
+    bool ok = true;
+    int slot = -1;
+    for (int i = 0; i < g_last_n; ++i)
+        if (g_last[i].stream == st) {
+            ok = !(wl < g_last[i].hi && g_last[i].lo < wh);
+            slot = i;
+            break;
+        }
+    if (slot < 0) {
+        if (g_last_n < 64) {
+            slot = g_last_n++;
+        } else {
+            slot = 0;  // table full: forget the oldest entry's stream, stay safe for this one
+            ok = false;
+        }
+    }
+    g_last[slot].stream = st;
+    g_last[slot].lo = reinterpret_cast<uintptr_t>(Y);
+    g_last[slot].hi = g_last[slot].lo + ybytes;
+    return ok;
+}
+
 int check_plan_fits(const lin_plan& p, int M, int N, int K, int precision) {
     switch (p.kernel) {
         case LIN_KERNEL_NONE: return (M == 0 || N == 0) ? LIN_OK : LIN_ERR_UNSUPPORTED;
         case LIN_KERNEL_FILL: return (K == 0 && p.grid_x > 0) ? LIN_OK : LIN_ERR_UNSUPPORTED;
         case LIN_KERNEL_SKINNY: {
             if (precision != LIN_PREC_BF16 || M > 16 || K == 0) return LIN_ERR_UNSUPPORTED;
-            if (p.variant < 0 || p.variant >= kSkinnyVariants || p.splits < 1) return LIN_ERR_UNSUPPORTED;
-            const SkinnyCfg c = kSkinnyCfg[p.variant];
-            if (p.grid_x != ceil_div(N, c.warps * c.groups * 8) || p.grid_y != p.splits ||
-                p.splits > ceil_div(K, 32) || (p.splits > 1 && p.grid_x > kMaxSplitTiles))
+            if (p.variant < 0 || p.variant >= kSkinnyVariants) return LIN_ERR_UNSUPPORTED;
+            if (p.splits != 1 && p.splits != 2 && p.splits != 4 && p.splits != 8) return LIN_ERR_UNSUPPORTED;
+            if (p.grid_x != ceil_div(N, 128) || p.grid_y != p.splits) return LIN_ERR_UNSUPPORTED;
+            return LIN_OK;
+        }
+        case LIN_KERNEL_SKINNY_SK: {
+            if (precision != LIN_PREC_BF16 || M > 16 || K == 0) return LIN_ERR_UNSUPPORTED;
+            if (p.variant < 0 || p.variant >= kSkinnySkVariants || p.grid_x < 1 || p.grid_y != 1) return LIN_ERR_UNSUPPORTED;
+            const SkinnySkCfg c = kSkinnySkCfg[p.variant];
+            const int nrb = ceil_div(N, 128);
+            const long long T = (long long)nrb * ceil_div(K, 64 * c.kbox);
+            if (nrb > kMaxSplitTiles || p.grid_x > T || p.bk != 64 * c.kbox) return LIN_ERR_UNSUPPORTED;
+            if ((long long)skinny_sk_workspace_bytes(p.grid_x, M, N, K, c.kbox) != p.workspace_bytes)
                 return LIN_ERR_UNSUPPORTED;
             return LIN_OK;
         }
@@ -259,9 +330,11 @@ int run(lin_ctx* ctx, const lin_plan& plan, int M, int N, int K, const void* X, 
     p.workspace_bytes = ctx->workspace_bytes;
     p.dev_status = ctx->dev_status;
     p.sm_count = ctx->sm_count;
+    p.early_start = early_start_ok(p.stream, W, (size_t)N * K * ein, Y, ybytes) && ctx->early_start;
     switch (plan.kernel) {
         case LIN_KERNEL_FILL: return launch_fill(p);
         case LIN_KERNEL_SKINNY: return launch_skinny(p, plan);
+        case LIN_KERNEL_SKINNY_SK: return launch_skinny_sk(p, plan);
         case LIN_KERNEL_FFMA: return launch_ffma(p, plan);
         case LIN_KERNEL_TC: return launch_tc(p, plan);
         default: return LIN_ERR_UNSUPPORTED;
@@ -315,6 +388,7 @@ int lin_create(lin_ctx** out, int device, size_t max_workspace_bytes) {
     lin_ctx* c = new (std::nothrow) lin_ctx();
     if (!c) return LIN_ERR_CUDA;
     c->device = device;
+    c->early_start = true;
     c->workspace_bytes = max_workspace_bytes ? max_workspace_bytes : ((size_t)64 << 20);
     if (cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
         cudaMalloc(&c->workspace, c->workspace_bytes) != cudaSuccess ||
@@ -344,6 +418,17 @@ int lin_destroy(lin_ctx* ctx) {
     return rc;
 }
 
+int lin_set_option(lin_ctx* ctx, int option, long long value) {
+    if (!ctx) return LIN_ERR_ARG;
+    switch (option) {
+        case LIN_OPT_EARLY_START:
+            if (value != 0 && value != 1) return LIN_ERR_ARG;
+            ctx->early_start = value != 0;
+            return LIN_OK;
+        default: return LIN_ERR_ARG;
+    }
+}
+
 int lin_ctx_info(const lin_ctx* ctx, int* device, int* sm_count, size_t* workspace_bytes) {
     if (!ctx) return LIN_ERR_ARG;
     if (device) *device = ctx->device;
@@ -366,6 +451,9 @@ int lin_plan_make(int sm_count, int kernel, int variant, int splits, int M, int 
         case LIN_KERNEL_SKINNY:
             if (precision != LIN_PREC_BF16) return LIN_ERR_UNSUPPORTED;
             return lin::make_skinny(sm_count, variant, splits, M, N, K, unlimited, out);
+        case LIN_KERNEL_SKINNY_SK:
+            if (precision != LIN_PREC_BF16) return LIN_ERR_UNSUPPORTED;
+            return lin::make_skinny_sk(sm_count, variant, splits, M, N, K, unlimited, out);
         case LIN_KERNEL_FFMA:
             if (precision != LIN_PREC_FP32) return LIN_ERR_UNSUPPORTED;
             return lin::make_ffma(sm_count, variant, splits, M, N, K, unlimited, out);

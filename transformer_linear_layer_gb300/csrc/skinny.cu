@@ -2,232 +2,324 @@
 //
 // The workload of "One multiply, one RTX 5090, eight kernels": a batch of 16
 // vectors against a 4096 x 4096 weight stored out x in. Each weight value
-// feeds only M products, so the kernel is a stream over W and its speed is
-// the rate at which W leaves HBM ("Where the time goes": the loads-only probe
-// took as long as the full kernel). Design on sm_103a:
+// feeds only M products, so the kernel is a stream over W and its speed is the
+// rate at which W leaves HBM ("Where the time goes": the loads-only probe took
+// as long as the full kernel). The page's kernels request the next K slice
+// before multiplying the current one and split K across blocks ("Inside one
+// block", "Filling the chip"); on sm_103a:
 //
-// * Every W byte is loaded exactly once, by 128-bit non-allocating global
-//   loads (ld.global.nc.L1::no_allocate.v4), double-buffered in registers
-//   one round ahead so each thread keeps several 16-byte loads in flight.
-// * The inner product uses the tensor cores through mma.m16n8k16 (bf16 x
-//   bf16 -> fp32): X is the 16 x 16 A operand and a 16 x 8 slab of W^T is
-//   the B operand. At M = 16 the FFMA units cannot keep up with HBM
-//   (16 FLOP per W byte at ~6.8 TB/s is ~108 TFLOP/s), the tensor cores can.
-// * The 8 bf16 a thread loads from one W row (k0+8t .. k0+8t+7, t = lane%4)
-//   serve two MMAs directly: the reduction over k does not depend on which
-//   k sits in which fragment slot, so slots {2t,2t+1 | 2t+8,2t+9} of MMA 0
-//   take k = 8t+{0,1 | 2,3} and those of MMA 1 take 8t+{4,5 | 6,7}; X
-//   fragments use the same map (one 16-byte X load per fragment row). This
-//   avoids any shared-memory staging of W.
-// * Split-K fills the chip ("Filling the chip": Kernel 7 splits the inner
-//   dimension of each tile into ranges, one block each). Each CTA owns
-//   R = warps*groups*8 rows of W and one K range; partial sums go to the
-//   workspace and the last CTA of a tile to arrive adds the ranges in fixed
-//   order 0..S-1, then applies bias, GELU and the bf16 store - bitwise
-//   repeatable ("Optimizing a GPT-2-class transformer on a GPU", Act I).
+// * Stream: one thread issues 2-D TMA copies of W tiles (128 rows x 128 bytes
+//   of K, 16 KiB) and the matching X tile (16 rows x 128 bytes) into a
+//   STAGES-deep shared-memory ring, so ~80 KiB of W per CTA are in flight -
+//   enough bytes in flight per SM to cover HBM latency (Little's law), which
+//   register-staged loads cannot reach at this occupancy.
+// * Multiply ("swap AB"): the tensor core computes D = W_tile . X_tile^T with
+//   tcgen05.mma M = 128 (W rows), N = 16 (the batch, zero-padded by the copy
+//   engine when M < 16), K = 16 per instruction, straight from the swizzled
+//   tiles, accumulating in 16 TMEM columns. At M = 16 the FFMA units could
+//   not keep up with HBM (16 FLOP per W byte ~ 108 TFLOP/s at 6.8 TB/s).
+// * Split-K in a thread-block cluster: the CL CTAs of a cluster share one
+//   128-row block of W and take consecutive K ranges. Each writes its 16 x 128
+//   partial sums to its own shared memory; after a cluster barrier, CTA r adds
+//   the CL partials of columns [r*128/CL, (r+1)*128/CL) through distributed
+//   shared memory in fixed rank order 0..CL-1 (bitwise repeatable, the
+//   fixed-order reduction of "Optimizing a GPT-2-class transformer on a GPU",
+//   Act I), applies bias and GELU and stores bf16. No global workspace.
+// * Programmatic dependent launch: the W copies of the first STAGES tiles are
+//   issued before griddepcontrol.wait, so a layer's weight stream starts while
+//   the previous kernel on the stream drains; X, bias and Y are touched only
+//   after the wait. The host drops the early start when W overlaps the output
+//   of the previous call on the stream.
 #include "internal.h"
 #include "device_common.cuh"
+#include "tc_common.cuh"
 
 namespace lin {
 namespace {
 
 struct SkinnyArgs {
     int M, N, K;
-    const uint16_t* X;  // bf16 bits, M x K
-    const uint16_t* W;  // bf16 bits, N x K
-    const float* bias;  // N or nullptr
-    uint16_t* Y;        // bf16 bits, M x N
-    float* ws;          // splits x M x N partials (splits > 1)
-    unsigned* counters; // one per n-tile (splits > 1), zero between launches
-    int splits;
-    int nchunks;        // ceil(K / 32)
+    const float* bias;
+    uint16_t* Y;
+    int* status;
+    int kblocks;  // ceil(K / (64 * KBOX)): stages of K per 128-row block
 };
 
-__device__ __forceinline__ uint4 ld_stream(const uint16_t* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
+constexpr int kSkRows = 128;  // W rows (outputs) per cluster
+constexpr int kSkMP = 16;     // batch rows, padded to the MMA N
+constexpr uint32_t kSkWBox = kSkRows * 128;  // one 128-byte-wide box of W
+constexpr uint32_t kSkXBox = kSkMP * 128;
+
+// A stage holds KBOX boxes of 64 K each: the boxes of one stage are issued
+// together, so each W row is read as a run of KBOX * 128 contiguous bytes
+// (DRAM rows stay open across the run). The 16 x 128 fp32 partial-sum tile
+// reuses the first W box: it is written only after the last MMA completed.
+constexpr size_t skinny_smem_bytes(int stages, int kbox) {
+    return 1024 + (size_t)stages * kbox * (kSkWBox + kSkXBox) + (2 * stages + 1) * 8 + 16;
 }
+static_assert(kSkMP * kSkRows * 4 <= kSkWBox, "partial tile fits in one W box");
 
-__device__ __forceinline__ uint4 ld_reused(const uint16_t* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
+template <int STAGES, int KBOX, int CL, bool GELU>
+__global__ void __launch_bounds__(kSkinnyThreads, 1)
+skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const SkinnyArgs a) {
+    constexpr uint32_t TMEM_COLS = 32;
+    constexpr uint32_t IDESC = make_idesc(1u, kSkRows, kSkMP);
+    constexpr int COLS = kSkRows / CL;  // output columns this CTA reduces
+    constexpr uint32_t WB = KBOX * kSkWBox, XB = KBOX * kSkXBox;
 
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sW = smem;
+    uint8_t* sX = sW + STAGES * WB;
+    float* red = reinterpret_cast<float*>(sW);  // [kSkMP][kSkRows], after the last MMA
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sX + STAGES * XB);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+    int* s_abort = reinterpret_cast<int*>(tmem_slot + 1);
 
-template <int WARPS, int G, int U, bool GELU>
-__global__ void __launch_bounds__(WARPS * 32)
-skinny_kernel(const SkinnyArgs a) {
-    constexpr int R = WARPS * G * 8;  // rows of W (output columns) per CTA
-    constexpr int NT = WARPS * 32;
-    __shared__ float tile[16][R + 1];
-    __shared__ unsigned s_last;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * kSkRows;
+    const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
+    const int kb0 = (int)((long long)rank * a.kblocks / CL);
+    const int kb1 = (int)((long long)(rank + 1) * a.kblocks / CL);
+    const int nkb = kb1 - kb0;
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES), accum_bar = smem_u32(bars + 2 * STAGES);
 
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int g = lane >> 2, t = lane & 3;
-    const int n_cta = blockIdx.x * R;
-    const int split = blockIdx.y;
-    const int c_begin = (int)((long long)split * a.nchunks / a.splits);
-    const int c_end = (int)((long long)(split + 1) * a.nchunks / a.splits);
-
-    // This thread's W rows: one per n8 group, row g of the group.
-    const uint16_t* wrow[G];
-    bool wok[G];
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-        const int n = n_cta + (warp * G + j) * 8 + g;
-        wok[j] = n < a.N;
-        wrow[j] = a.W + (size_t)(wok[j] ? n : 0) * (size_t)a.K + 8 * t;
-    }
-    const bool xa_ok = g < a.M, xb_ok = g + 8 < a.M;
-    const uint16_t* xa_row = a.X + (size_t)(xa_ok ? g : 0) * (size_t)a.K + 8 * t;
-    const uint16_t* xb_row = a.X + (size_t)(xb_ok ? g + 8 : 0) * (size_t)a.K + 8 * t;
-
-    float acc[G][4];
-#pragma unroll
-    for (int j = 0; j < G; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-
-    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-    // K is a multiple of 8, so a thread's 8-element slice is wholly in or out.
-    auto load_round = [&](uint4 (&wb)[U][G], int c0) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int k = (c0 + u) * 32;
-            const bool kin = (c0 + u < c_end) && (k + 8 * t < a.K);
-#pragma unroll
-            for (int j = 0; j < G; ++j) wb[u][j] = (kin && wok[j]) ? ld_stream(wrow[j] + k) : zero;
-        }
-    };
-    auto compute_round = [&](const uint4 (&wb)[U][G], int c0) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int k = (c0 + u) * 32;
-            const bool kin = (c0 + u < c_end) && (k + 8 * t < a.K);
-            const uint4 xa = (kin && xa_ok) ? ld_reused(xa_row + k) : zero;
-            const uint4 xb = (kin && xb_ok) ? ld_reused(xb_row + k) : zero;
-#pragma unroll
-            for (int j = 0; j < G; ++j) {
-                mma16816(acc[j], xa.x, xb.x, xa.y, xb.y, wb[u][j].x, wb[u][j].y);
-                mma16816(acc[j], xa.z, xb.z, xa.w, xb.w, wb[u][j].z, wb[u][j].w);
-            }
-        }
-    };
-
-    if (c_begin < c_end) {
-        uint4 bufA[U][G], bufB[U][G];
-        int c = c_begin;
-        load_round(bufA, c);
-        while (true) {
-            if (c + U < c_end) load_round(bufB, c + U);
-            compute_round(bufA, c);
-            c += U;
-            if (c >= c_end) break;
-            if (c + U < c_end) load_round(bufA, c + U);
-            compute_round(bufB, c);
-            c += U;
-            if (c >= c_end) break;
-        }
-    }
-
-    // Accumulator fragment (m16n8 f32): c0,c1 -> row g, cols 2t,2t+1; c2,c3 -> row g+8.
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-        const int nl = (warp * G + j) * 8 + 2 * t;
-        tile[g][nl] = acc[j][0];
-        tile[g][nl + 1] = acc[j][1];
-        tile[g + 8][nl] = acc[j][2];
-        tile[g + 8][nl + 1] = acc[j][3];
-    }
-    __syncthreads();
-
-    const int M = a.M, N = a.N;
-    if (a.splits == 1) {
-        for (int idx = threadIdx.x; idx < M * R; idx += NT) {
-            const int m = idx / R, nl = idx % R, n = n_cta + nl;
-            if (n < N) {
-                const float b = a.bias ? a.bias[n] : 0.f;
-                a.Y[(size_t)m * N + n] = f32_to_bf16_bits(epilogue<GELU>(tile[m][nl], b));
-            }
-        }
-        return;
-    }
-
-    float* part = a.ws + (size_t)split * M * N;
-    for (int idx = threadIdx.x; idx < M * R; idx += NT) {
-        const int m = idx / R, nl = idx % R, n = n_cta + nl;
-        if (n < N) __stcg(part + (size_t)m * N + n, tile[m][nl]);
-    }
-    __threadfence();
-    __syncthreads();
     if (threadIdx.x == 0) {
-        const unsigned prev = atomicAdd(&a.counters[blockIdx.x], 1u);
-        s_last = (prev == (unsigned)(a.splits - 1));
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        mbar_init(accum_bar, 1);
+        *s_abort = 0;
+        mbar_fence_init();
+        tma_prefetch_map(&tmW);
+        tma_prefetch_map(&tmX);
     }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tc_fence_before();
     __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    for (int idx = threadIdx.x; idx < M * R; idx += NT) {
-        const int m = idx / R, nl = idx % R, n = n_cta + nl;
-        if (n < N) {
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    if (threadIdx.x == 0) pdl_launch_dependents();
+
+    auto give_up = [&]() {
+        atomicExch(s_abort, 1);
+        atomicExch(a.status, (int)LIN_ERR_DEVICE_TIMEOUT);
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---- producer: W tiles early, X tiles after the dependency wait ----
+            auto load_w = [&](int i) {
+                const int s = i % STAGES;
+#pragma unroll
+                for (int b = 0; b < KBOX; ++b)
+                    tma_load_2d(smem_u32(sW + s * WB + b * kSkWBox), &tmW, full0 + 8 * s, ((kb0 + i) * KBOX + b) * 64,
+                                n0);
+            };
+            auto load_x = [&](int i) {
+                const int s = i % STAGES;
+#pragma unroll
+                for (int b = 0; b < KBOX; ++b)
+                    tma_load_2d(smem_u32(sX + s * XB + b * kSkXBox), &tmX, full0 + 8 * s, ((kb0 + i) * KBOX + b) * 64,
+                                0);
+            };
+            const int pre = nkb < STAGES ? nkb : STAGES;
+            for (int i = 0; i < pre; ++i) {
+                mbar_expect_tx(full0 + 8 * i, WB + XB);
+                load_w(i);
+            }
+            pdl_wait();
+            for (int i = 0; i < pre; ++i) load_x(i);
+            int issued = pre;
+            for (int i = pre; i < nkb; ++i) {
+                const int s = i % STAGES;
+                const uint32_t ph = (i / STAGES) & 1;
+                if (*(volatile int*)s_abort || !mbar_wait(empty0 + 8 * s, ph ^ 1)) {
+                    give_up();
+                    break;
+                }
+                mbar_expect_tx(full0 + 8 * s, WB + XB);
+                load_w(i);
+                load_x(i);
+                issued = i + 1;
+            }
+            if (*(volatile int*)s_abort) {
+                const int first = issued > STAGES ? issued - STAGES : 0;
+                for (int i = first; i < issued; ++i) mbar_wait(full0 + 8 * (i % STAGES), (i / STAGES) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && nkb > 0) {
+            // ---- MMA issuer ----
+            for (int i = 0; i < nkb; ++i) {
+                const int s = i % STAGES;
+                const uint32_t ph = (i / STAGES) & 1;
+                if (*(volatile int*)s_abort || !mbar_wait(full0 + 8 * s, ph)) {
+                    give_up();
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int b = 0; b < KBOX; ++b) {
+                    const uint64_t ad = sw128_kmajor_desc(smem_u32(sW + s * WB + b * kSkWBox));
+                    const uint64_t bd = sw128_kmajor_desc(smem_u32(sX + s * XB + b * kSkXBox));
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma<true>(tmem_base, ad + 2u * kk, bd + 2u * kk, IDESC, (i | b | kk) != 0 ? 1u : 0u);
+                }
+                tc_commit(empty0 + 8 * s);
+            }
+            tc_commit(accum_bar);
+            if (!mbar_wait(accum_bar, 0)) give_up();
+        }
+    } else {
+        // ---- epilogue warps 2..5: TMEM lane quadrant q holds W rows 32q..32q+31 ----
+        pdl_wait();
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        float v[kSkMP];
+#pragma unroll
+        for (int m = 0; m < kSkMP; ++m) v[m] = 0.f;
+        if (nkb > 0) {
+            const bool mine = mbar_wait(accum_bar, 0);
+            if (!mine) give_up();
+            tc_fence_after();
+            if (__all_sync(0xffffffffu, mine && *(volatile int*)s_abort == 0)) {
+                uint32_t r[16];
+                tmem_ld16(tmem_base + (static_cast<uint32_t>(q * 32) << 16), r);
+#pragma unroll
+                for (int m = 0; m < kSkMP; ++m) v[m] = __uint_as_float(r[m]);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < kSkMP; ++m) red[m * kSkRows + row] = v[m];
+    }
+
+    // Partial sums of every CTA of the cluster are complete and visible.
+    __syncwarp();
+    tc_fence_before();
+    if constexpr (CL > 1)
+        cluster_sync_all();
+    else
+        __syncthreads();
+
+    if (warp >= 2) {
+        const int t = threadIdx.x - 64;
+        const int M = a.M, N = a.N;
+        for (int idx = t; idx < M * COLS; idx += 128) {
+            const int m = idx / COLS;
+            const int c = (int)rank * COLS + idx % COLS;
+            const int n = n0 + c;
+            if (n >= N) continue;
+            const uint32_t local = smem_u32(red + m * kSkRows + c);
             float s = 0.f;
-            for (int sp = 0; sp < a.splits; ++sp) s += __ldcg(a.ws + ((size_t)sp * M + m) * N + n);
-            const float b = a.bias ? a.bias[n] : 0.f;
+            if constexpr (CL > 1) {
+                float part[CL];
+#pragma unroll
+                for (int j = 0; j < CL; ++j) part[j] = dsmem_ld_f32(dsmem_map(local, (uint32_t)j));
+#pragma unroll
+                for (int j = 0; j < CL; ++j) s += part[j];
+            } else {
+                s = red[m * kSkRows + c];
+            }
+            const float b = a.bias ? __ldg(a.bias + n) : 0.f;
             a.Y[(size_t)m * N + n] = f32_to_bf16_bits(epilogue<GELU>(s, b));
         }
     }
-    if (threadIdx.x == 0) a.counters[blockIdx.x] = 0u;  // re-arm for the next launch
+
+    // No CTA leaves (and frees its shared memory) while a peer may still read it.
+    tc_fence_before();
+    if constexpr (CL > 1)
+        cluster_sync_all();
+    else
+        __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
 }
 
-template <int WARPS, int G, int U>
-int launch_cfg(const SkinnyArgs& a, dim3 grid, cudaStream_t st, bool gelu) {
-    if (gelu)
-        skinny_kernel<WARPS, G, U, true><<<grid, WARPS * 32, 0, st>>>(a);
-    else
-        skinny_kernel<WARPS, G, U, false><<<grid, WARPS * 32, 0, st>>>(a);
+template <int STAGES, int KBOX, int CL, bool GELU>
+int launch_cfg(const CUtensorMap& tw, const CUtensorMap& tx, const SkinnyArgs& a, int grid_x, bool early,
+               cudaStream_t st) {
+    constexpr size_t smem = skinny_smem_bytes(STAGES, KBOX);
+    auto kern = skinny_kernel<STAGES, KBOX, CL, GELU>;
+    static unsigned long long attr_set = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LIN_ERR_CUDA;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(attr_set & bit)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return LIN_ERR_CUDA;
+        attr_set |= bit;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid_x, CL, 1);
+    cfg.blockDim = dim3(kSkinnyThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    if (CL > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = 1;
+        attrs[na].val.clusterDim.y = CL;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (early) {
+        attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    if (cudaLaunchKernelEx(&cfg, kern, tw, tx, a) != cudaSuccess) return LIN_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? LIN_OK : LIN_ERR_CUDA;
+}
+
+template <int STAGES, int KBOX, bool GELU>
+int launch_split(int splits, const CUtensorMap& tw, const CUtensorMap& tx, const SkinnyArgs& a, int grid_x,
+                 bool early, cudaStream_t st) {
+    switch (splits) {
+        case 1: return launch_cfg<STAGES, KBOX, 1, GELU>(tw, tx, a, grid_x, early, st);
+        case 2: return launch_cfg<STAGES, KBOX, 2, GELU>(tw, tx, a, grid_x, early, st);
+        case 4: return launch_cfg<STAGES, KBOX, 4, GELU>(tw, tx, a, grid_x, early, st);
+        case 8: return launch_cfg<STAGES, KBOX, 8, GELU>(tw, tx, a, grid_x, early, st);
+        default: return LIN_ERR_UNSUPPORTED;
+    }
 }
 
 }  // namespace
 
 int launch_skinny(const Problem& p, const lin_plan& plan) {
+    CUtensorMap tw, tx;
+    if (!make_kmajor_map(&tw, p.W, true, p.N, p.K, kSkRows)) return LIN_ERR_CUDA;
+    if (!make_kmajor_map(&tx, p.X, true, p.M, p.K, kSkMP)) return LIN_ERR_CUDA;
     SkinnyArgs a;
     a.M = p.M;
     a.N = p.N;
     a.K = p.K;
-    a.X = static_cast<const uint16_t*>(p.X);
-    a.W = static_cast<const uint16_t*>(p.W);
     a.bias = p.bias;
     a.Y = static_cast<uint16_t*>(p.Y);
-    a.splits = plan.splits;
-    a.nchunks = (p.K + 31) / 32;
-    a.ws = nullptr;
-    a.counters = nullptr;
-    if (plan.splits > 1) {
-        a.ws = splitk_partials(p.workspace);
-        a.counters = splitk_counters(p.workspace);
-    }
-    const dim3 grid(plan.grid_x, plan.grid_y, 1);
+    a.status = p.dev_status;
+    a.kblocks = (p.K + 64 * kSkinnyCfg[plan.variant].kbox - 1) / (64 * kSkinnyCfg[plan.variant].kbox);
     const bool gelu = p.epilogue == LIN_EPI_GELU_TANH;
+#define LIN_SKINNY_CASE(V)                                                                                 \
+    case V:                                                                                                \
+        return gelu ? launch_split<kSkinnyCfg[V].stages, kSkinnyCfg[V].kbox, true>(                   \
+                          plan.splits, tw, tx, a, plan.grid_x, p.early_start, p.stream)                    \
+                    : launch_split<kSkinnyCfg[V].stages, kSkinnyCfg[V].kbox, false>(                      \
+                          plan.splits, tw, tx, a, plan.grid_x, p.early_start, p.stream);
     switch (plan.variant) {
-        case 0: return launch_cfg<4, 2, 4>(a, grid, p.stream, gelu);
-        case 1: return launch_cfg<8, 1, 4>(a, grid, p.stream, gelu);
-        case 2: return launch_cfg<4, 4, 2>(a, grid, p.stream, gelu);
-        case 3: return launch_cfg<8, 2, 2>(a, grid, p.stream, gelu);
+        LIN_SKINNY_CASE(0)
+        LIN_SKINNY_CASE(1)
+        LIN_SKINNY_CASE(2)
+        LIN_SKINNY_CASE(3)
         default: return LIN_ERR_UNSUPPORTED;
     }
+#undef LIN_SKINNY_CASE
 }
 
 }  // namespace lin
