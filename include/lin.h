@@ -177,6 +177,37 @@ LIN_API const char* lin_strerror(int status);
 /* LIN_ABI_VERSION of the loaded library. */
 LIN_API int lin_abi_version(void);
 
+/* Size of the fixed device array behind lin_forward_fp32_static. */
+#define LIN_STATIC_SCRATCH_BYTES (4u << 20)
+
+/* The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory when they run the layer, for example:
+ * - code recording a CUDA graph (an allocation breaks the capture);
+ * - runtimes that own all device memory through their own pool;
+ * - paths where an allocation could block or fail.
+ *
+ * Y = act(X . W^T + bias) in fp32 on the CURRENT device, with the same FFMA
+ * kernel and split-K choice as lin_forward(..., LIN_PREC_FP32, ...), but with
+ * no context. It calls no cudaMalloc or cudaFree: the split-K counters and
+ * partial sums live in one fixed array of LIN_STATIC_SCRATCH_BYTES (4 MiB),
+ * a static device variable of this library that every GPU which loads the
+ * library holds until the process exits. Arguments, layouts and alignment
+ * rules are those of lin_forward; X, W, bias and Y are caller-owned device
+ * pointers.
+ *
+ * Limits and caveats:
+ * - A shape whose split needs more scratch than the array holds returns
+ *   LIN_ERR_WORKSPACE (nothing is launched).
+ * - The first call on a device looks up the array's device address; make
+ *   that first call before any stream capture.
+ * - Every call shares the one array, and the array keeps the last call's
+ *   contents. The call zeroes the counters it uses on `stream` before its
+ *   kernel.
+ * - Calls whose kernels overlap on the GPU (other streams, or other threads
+ *   without ordering) race on the array: order them on one stream. */
+LIN_API int lin_forward_fp32_static(int M, int N, int K, const float* X, const float* W,
+                                    const float* bias, float* Y, int epilogue, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

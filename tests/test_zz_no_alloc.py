@@ -1,0 +1,73 @@
+"""The fp32 entry point that allocates nothing (lin_forward_fp32_static).
+
+It serves callers that cannot allocate device memory when they run the layer
+(graph capture, runtimes that own all device memory, allocation-free hot
+paths): its split-K scratch is a fixed array inside the library. These tests
+call it through the C ABI and compare with lin_forward on the same inputs,
+twice in a row, because consecutive calls share that array. The file is named
+to be collected last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic_inputs as si
+import transformer_linear_layer_gb300 as tll
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = list(si.GPT2_M128_FP32) + [
+    si.Layer("ragged", 70, 333, 132, si.PREC_FP32, si.EPI_GELU, bias=True),
+    si.SQUARE_256_FP32,
+]
+
+
+def _static(lib, x, w, bias, y, epi):
+    return lib.lin_forward_fp32_static(x.shape[0], w.shape[0], x.shape[1], x.data_ptr(), w.data_ptr(),
+                                       None if bias is None else bias.data_ptr(), y.data_ptr(), epi,
+                                       ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
+@pytest.mark.parametrize("layer", SHAPES, ids=lambda l: l.name)
+def test_static_scratch_matches_lin_forward(layer):
+    lib = tll.library()
+    X, W, b = si.make_inputs(layer)
+    x = torch.from_numpy(X).cuda()
+    w = torch.from_numpy(W).cuda()
+    bias = None if b is None else torch.from_numpy(b).cuda()
+    epi = tll.EPI_GELU_TANH if layer.epilogue else tll.EPI_NONE
+    ref = tll.forward(x, w, bias, epilogue=epi, precision="fp32")
+    y1 = torch.full((layer.M, layer.N), float("nan"), device="cuda")
+    y2 = torch.full((layer.M, layer.N), float("nan"), device="cuda")
+    assert _static(lib, x, w, bias, y1, epi) == tll.OK
+    assert _static(lib, x, w, bias, y2, epi) == tll.OK  # second call reuses the array as left
+    torch.cuda.synchronize()
+    r = ref.double().cpu().numpy()
+    for y in (y1, y2):
+        assert oracle.rel_err(y.double().cpu().numpy(), r) <= oracle.TOL[si.PREC_FP32]
+
+
+def test_gpt2_shapes_exercise_the_split():
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    for layer in si.GPT2_M128_FP32:
+        p = tll.plan_query(sm, layer.M, layer.N, layer.K, "fp32", workspace_bytes=1 << 62)
+        assert p.splits > 1 and 0 < p.workspace_bytes <= 4 << 20
+
+
+def test_static_scratch_refuses_oversized_split():
+    lib = tll.library()
+    M, N, K = 64, 64 * 151, 256  # 151 tiles of 64x64 -> split 2 -> ~4.9 MB of partial sums
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    need = tll.plan_query(sm, M, N, K, "fp32", workspace_bytes=1 << 62).workspace_bytes
+    x = torch.zeros((M, K), device="cuda")
+    w = torch.zeros((N, K), device="cuda")
+    y = torch.zeros((M, N), device="cuda")
+    if need <= 4 << 20:
+        pytest.skip(f"on {sm} SMs this shape's split fits the array ({need} bytes)")
+    y0 = y.clone()
+    assert _static(lib, x, w, None, y, tll.EPI_NONE) == tll.ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert torch.equal(y, y0)  # nothing was launched

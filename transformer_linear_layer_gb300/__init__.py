@@ -87,6 +87,7 @@ def library() -> ctypes.CDLL:
                 "lin_check_device": ([P, P], I),
                 "lin_ctx_info": ([P, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(Z)], I),
                 "lin_set_option": ([P, I, ctypes.c_longlong], I),
+                "lin_forward_fp32_static": ([I, I, I, P, P, P, P, I, P], I),
                 "lin_strerror": ([I], ctypes.c_char_p),
                 "lin_abi_version": ([], I),
             }
