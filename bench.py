@@ -91,8 +91,10 @@ def roofline_for(layer: si.Layer, seconds_per_launch: float, peaks, peaks_src, t
 
 def traffic_from_profile(kernel_file: str, workload: str):
     """dram bytes per launch from the committed ncu summary of this kernel and
-    workload, or None when absent or when the kernel source has changed."""
-    prof = os.path.join(ROOT, "profiles", f"{workload}.md")
+    workload (profiles/<kernel>_<workload>.md), or None when absent or when the
+    kernel source has changed since the capture."""
+    kernel = kernel_file.replace(".cu", "_kernel")
+    prof = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     src = os.path.join(ROOT, "transformer_linear_layer_gb300", "csrc", kernel_file)
     try:
         text = open(prof).read()

@@ -37,18 +37,25 @@ import numpy as np
 GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
+CHUNK = 1 << 21  # elements per block: arrays are built block by block in reused buffers
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
-    """SplitMix64 finaliser (variant 13) on a uint64 array, wrapping."""
-    z = z.astype(np.uint64, copy=True)
-    with np.errstate(over="ignore"):
-        z ^= z >> np.uint64(30)
-        z *= _M1
-        z ^= z >> np.uint64(27)
-        z *= _M2
-        z ^= z >> np.uint64(31)
+    """SplitMix64 finaliser (variant 13) on a uint64 array, wrapping (returns a copy)."""
+    z = np.array(z, dtype=np.uint64, copy=True)
+    _mix_inplace(z, np.empty_like(z))
     return z
+
+
+def _mix_inplace(z: np.ndarray, tmp: np.ndarray) -> None:
+    np.right_shift(z, np.uint64(30), out=tmp)
+    np.bitwise_xor(z, tmp, out=z)
+    np.multiply(z, _M1, out=z)
+    np.right_shift(z, np.uint64(27), out=tmp)
+    np.bitwise_xor(z, tmp, out=z)
+    np.multiply(z, _M2, out=z)
+    np.right_shift(z, np.uint64(31), out=tmp)
+    np.bitwise_xor(z, tmp, out=z)
 
 
 def stream_base(seed: int, tid: int) -> np.uint64:
@@ -58,33 +65,88 @@ def stream_base(seed: int, tid: int) -> np.uint64:
     return _mix(np.array([s], dtype=np.uint64))[0]
 
 
+class _Blocks:
+    """Reused buffers for block-wise generation (large arrays without large temporaries)."""
+
+    def __init__(self, n):
+        self.iota = np.arange(1, n + 1, dtype=np.uint64)
+        self.z = np.empty(n, dtype=np.uint64)
+        self.t = np.empty(n, dtype=np.uint64)
+
+    def draws(self, base, start, n):
+        """Draws start .. start+n-1 of the stream with start state ``base`` (a view of a buffer)."""
+        z, t = self.z[:n], self.t[:n]
+        np.add(self.iota[:n], np.uint64(start), out=z)
+        np.multiply(z, GAMMA, out=z)
+        np.add(z, base, out=z)
+        _mix_inplace(z, t)
+        return z
+
+
 def draws(seed: int, tid: int, count: int, start: int = 0) -> np.ndarray:
     """uint64 draws ``start .. start+count-1`` of stream ``tid``."""
     base = stream_base(seed, tid)
-    idx = np.arange(start + 1, start + count + 1, dtype=np.uint64)
-    with np.errstate(over="ignore"):
-        return _mix(base + idx * GAMMA)
+    out = np.empty(count, dtype=np.uint64)
+    blk = _Blocks(min(max(count, 1), CHUNK))
+    for c0 in range(0, count, CHUNK):
+        n = min(CHUNK, count - c0)
+        out[c0:c0 + n] = blk.draws(base, start + c0, n)
+    return out
 
 
 def uniform_pm1(seed: int, tid: int, shape) -> np.ndarray:
-    """fp32 array uniform on [-1, 1) with 24-bit resolution."""
-    n = int(np.prod(shape))
-    u = (draws(seed, tid, n) >> np.uint64(40)).astype(np.float64)
-    return (u * 2.0 ** -23 - 1.0).astype(np.float32).reshape(shape)
+    """fp32 array uniform on [-1, 1) with 24-bit resolution: u * 2**-23 - 1 for the
+    top 24 bits u of each draw (exact in fp32)."""
+    count = int(np.prod(shape))
+    base = stream_base(seed, tid)
+    out = np.empty(count, dtype=np.float32)
+    blk = _Blocks(min(max(count, 1), CHUNK))
+    for c0 in range(0, count, CHUNK):
+        n = min(CHUNK, count - c0)
+        z = blk.draws(base, c0, n)
+        np.right_shift(z, np.uint64(40), out=z)
+        o = out[c0:c0 + n]
+        np.copyto(o, z, casting="unsafe")
+        np.multiply(o, np.float32(2.0 ** -23), out=o)
+        np.subtract(o, np.float32(1.0), out=o)
+    return out.reshape(shape)
 
 
 def normal(seed: int, tid: int, shape, mu: float = 0.0, sigma: float = 1.0) -> np.ndarray:
-    """fp32 array ~ N(mu, sigma) by Box-Muller from paired draws."""
-    n = int(np.prod(shape))
-    d = draws(seed, tid, 2 * n)
-    u1 = ((d[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0 ** -53  # (0, 1]
-    u2 = (d[1::2] >> np.uint64(11)).astype(np.float64) * 2.0 ** -53  # [0, 1)
-    z = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)
-    return (mu + sigma * z).astype(np.float32).reshape(shape)
+    """fp32 array ~ N(mu, sigma) by Box-Muller from paired draws (2i, 2i+1), in
+    float64: mu + sigma * sqrt(-2 ln u1) cos(2 pi u2), u1 in (0, 1], u2 in [0, 1)."""
+    count = int(np.prod(shape))
+    base = stream_base(seed, tid)
+    out = np.empty(count, dtype=np.float32)
+    half = max(1, min(count, CHUNK // 2))
+    blk = _Blocks(2 * half)
+    a = np.empty(half, dtype=np.float64)
+    b = np.empty(half, dtype=np.float64)
+    two_pi = 2.0 * math.pi
+    for c0 in range(0, count, half):
+        n = min(half, count - c0)
+        z = blk.draws(base, 2 * c0, 2 * n)
+        np.right_shift(z, np.uint64(11), out=z)
+        u1, u2 = a[:n], b[:n]
+        np.copyto(u1, z[0::2], casting="unsafe")
+        np.add(u1, 1.0, out=u1)
+        np.multiply(u1, 2.0 ** -53, out=u1)
+        np.copyto(u2, z[1::2], casting="unsafe")
+        np.multiply(u2, 2.0 ** -53, out=u2)
+        np.log(u1, out=u1)
+        np.multiply(u1, -2.0, out=u1)
+        np.sqrt(u1, out=u1)
+        np.multiply(u2, two_pi, out=u2)
+        np.cos(u2, out=u2)
+        np.multiply(u1, u2, out=u1)
+        np.multiply(u1, sigma, out=u1)
+        np.add(u1, mu, out=u1)
+        np.copyto(out[c0:c0 + n], u1, casting="same_kind")
+    return out.reshape(shape)
 
 
 def small_ints(seed: int, tid: int, shape, lo: int = -4, hi: int = 4) -> np.ndarray:
-    """fp32 array of integers uniform on [lo, hi]."""
+    """fp32 array of integers uniform on [lo, hi]: (draw >> 32) mod (hi - lo + 1) + lo."""
     n = int(np.prod(shape))
     span = np.uint64(hi - lo + 1)
     v = (draws(seed, tid, n) >> np.uint64(32)) % span
@@ -93,15 +155,29 @@ def small_ints(seed: int, tid: int, shape, lo: int = -4, hi: int = 4) -> np.ndar
 
 def to_bf16_bits(a: np.ndarray) -> np.ndarray:
     """Round fp32 values to nearest-even bf16; returns the uint16 bit patterns."""
-    b = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
-    rounding = ((b >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
-    with np.errstate(over="ignore"):
-        return ((b + rounding) >> np.uint32(16)).astype(np.uint16)
+    src = np.ascontiguousarray(a, dtype=np.float32).reshape(-1).view(np.uint32)
+    out = np.empty(src.size, dtype=np.uint16)
+    m = min(max(src.size, 1), CHUNK)
+    r = np.empty(m, dtype=np.uint32)
+    for c0 in range(0, src.size, CHUNK):
+        n = min(CHUNK, src.size - c0)
+        b, rr = src[c0:c0 + n], r[:n]
+        np.right_shift(b, np.uint32(16), out=rr)
+        np.bitwise_and(rr, np.uint32(1), out=rr)
+        np.add(rr, np.uint32(0x7FFF), out=rr)
+        np.add(rr, b, out=rr)  # wraps only for NaN/inf inputs, which the recipes never produce
+        np.right_shift(rr, np.uint32(16), out=rr)
+        np.copyto(out[c0:c0 + n], rr, casting="unsafe")
+    return out.reshape(np.shape(a))
 
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     """Widen bf16 bit patterns to fp32 exactly."""
-    return (np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+    src = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(src.shape, dtype=np.uint32)
+    np.copyto(out, src, casting="unsafe")
+    np.left_shift(out, np.uint32(16), out=out)
+    return out.view(np.float32)
 
 
 def round_bf16(a: np.ndarray) -> np.ndarray:

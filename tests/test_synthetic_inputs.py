@@ -52,3 +52,31 @@ def test_workload_shapes():
     X, W, b = si.make_inputs(si.Layer("t", 3, 5, 8, si.PREC_BF16, bias=True))
     assert X.shape == (3, 8) and W.shape == (5, 8) and b.shape == (5,)
     assert np.array_equal(si.round_bf16(X), X)
+
+
+def test_block_generation_equals_plain_definition(monkeypatch):
+    """Generation in reused blocks gives the same bits as the definition written
+    out on whole arrays, across block boundaries."""
+    import math
+
+    monkeypatch.setattr(si, "CHUNK", 1000)
+
+    def plain_draws(seed, tid, count):
+        base = si.stream_base(seed, tid)
+        idx = np.arange(1, count + 1, dtype=np.uint64)
+        with np.errstate(over="ignore"):
+            return si._mix(base + idx * si.GAMMA)
+
+    for n in (1, 999, 1000, 2501):
+        assert np.array_equal(si.draws(3, 4, n), plain_draws(3, 4, n))
+        u = (plain_draws(3, 4, n) >> np.uint64(40)).astype(np.float64)
+        assert np.array_equal(si.uniform_pm1(3, 4, (n,)), (u * 2.0 ** -23 - 1.0).astype(np.float32))
+        d = plain_draws(5, 6, 2 * n)
+        u1 = ((d[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0 ** -53
+        u2 = (d[1::2] >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+        z = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)
+        assert np.array_equal(si.normal(5, 6, (n,), 0.1, 0.02), (0.1 + 0.02 * z).astype(np.float32))
+        x = si.normal(7, 8, (n,))
+        b = x.view(np.uint32).astype(np.uint64)
+        plain_bits = ((b + ((b >> 16) & 1) + 0x7FFF) >> 16).astype(np.uint16)
+        assert np.array_equal(si.to_bf16_bits(x), plain_bits)
