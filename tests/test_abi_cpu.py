@@ -80,8 +80,10 @@ def test_dispatch_tensor_cores_for_tf32_and_wide_bf16():
     for prec in ("tf32", "bf16"):
         p = tll.plan_query(SM, 8192, 50257, 768, prec)
         assert kname(p) == "tc"
-        assert p.grid_x * p.bn >= 50257 and p.grid_y * 128 >= 8192
+        assert p.bn in (128, 192, 256) and p.grid_x == SM and p.grid_y == 1
         assert p.splits == 1 and p.workspace_bytes == 0
+    small = tll.plan_query(SM, 200, 300, 64, "bf16")
+    assert kname(small) == "tc" and small.grid_x == 2 * ((300 + small.bn - 1) // small.bn)
 
 
 def test_dispatch_ffma_for_fp32():
@@ -143,7 +145,10 @@ def test_plan_make_families():
         tll.plan_make(SM, tll.KERNEL_SKINNY, 0, 0, 17, 4096, 4096, "bf16")
     with pytest.raises(tll.LinError):
         tll.plan_make(SM, tll.KERNEL_FFMA, 0, 0, 16, 64, 64, "bf16")
+    for v, bn in ((0, 256), (1, 128), (2, 192)):
+        p = tll.plan_make(SM, tll.KERNEL_TC, v, 2, 4096, 4096, 256, "tf32")
+        assert p.bn == bn and p.grid_x == 2
     with pytest.raises(tll.LinError):
-        tll.plan_make(SM, tll.KERNEL_TC, 0, 2, 256, 256, 256, "tf32")
+        tll.plan_make(SM, tll.KERNEL_TC, 3, 0, 256, 256, 256, "tf32")
     p = tll.plan_make(SM, tll.KERNEL_FFMA, 1, 7, 128, 768, 768, "fp32")
     assert p.grid_z == 7 and p.workspace_bytes >= 7 * 128 * 768 * 4

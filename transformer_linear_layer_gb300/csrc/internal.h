@@ -56,10 +56,10 @@ struct FfmaCfg { int bm, bn, bk, tm, tn; };        // 256 threads each
 constexpr int kFfmaVariants = 2;
 constexpr FfmaCfg kFfmaCfg[kFfmaVariants] = {{128, 128, 16, 8, 8}, {64, 64, 16, 4, 4}};
 
-struct TcCfg { int bn, stages; };                  // BM = 128, BK = 128 bytes of K
-constexpr int kTcVariants = 2;
-constexpr TcCfg kTcCfg[kTcVariants] = {{256, 4}, {128, 6}};
-constexpr int kTcThreads = 192;                    // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+struct TcCfg { int bn; };                          // BM = 128, BK = 128 bytes of K; ring depth from smem
+constexpr int kTcVariants = 3;
+constexpr TcCfg kTcCfg[kTcVariants] = {{256}, {128}, {192}};
+constexpr int kTcThreads = 320;                    // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 
 // Launchers (return LIN_OK or LIN_ERR_*). They assume the plan was validated.
 int launch_fill(const Problem& p);

@@ -47,12 +47,6 @@ __global__ void fill_kernel(int M, int N, const float* bias, void* Y) {
 
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
-// Fraction of SM slots busy over the waves a grid of `ctas` needs.
-double wave_efficiency(long long ctas, long long slots) {
-    const long long waves = (ctas + slots - 1) / slots;
-    return waves ? (double)ctas / (double)(waves * slots) : 0.0;
-}
-
 void plan_common(lin_plan* p, int kernel, int variant) {
     std::memset(p, 0, sizeof(*p));
     p->kernel = kernel;
@@ -148,22 +142,35 @@ int make_ffma(int sm, int variant, int splits, int M, int N, int K, size_t ws, l
     return LIN_OK;
 }
 
-int make_tc(int sm, int variant, int M, int N, int K, lin_plan* p) {
-    if (M < 1 || N < 1 || K < 1) return LIN_ERR_UNSUPPORTED;
+// Persistent tcgen05 kernel: `width` CTAs walk the 128 x BN output tiles
+// (0 = one CTA per SM) in static round robin. N tile: the smallest predicted
+// time rounds(BN) x (BN + 110), where rounds = ceil(tiles / CTAs) and the
+// constant 110 (in columns) is the per-tile cost that does not scale with BN,
+// fitted to the measured M = 8192 and 4096^3 shapes.
+int make_tc(int sm, int variant, int width, int M, int N, int K, lin_plan* p) {
+    if (M < 1 || N < 1 || K < 1 || width < 0) return LIN_ERR_UNSUPPORTED;
     if (variant < 0) {
-        // Pick the N tile with the better wave efficiency; ties go to the wider tile.
-        const long long t0 = (long long)ceil_div(M, 128) * ceil_div(N, kTcCfg[0].bn);
-        const long long t1 = (long long)ceil_div(M, 128) * ceil_div(N, kTcCfg[1].bn);
-        variant = wave_efficiency(t1, sm) > wave_efficiency(t0, sm) + 0.02 ? 1 : 0;
+        double best = 0.0;
+        for (int v = 0; v < kTcVariants; ++v) {
+            const long long t = (long long)ceil_div(M, 128) * ceil_div(N, kTcCfg[v].bn);
+            const long long w = width > 0 ? width : sm;
+            const double cost = (double)((t + w - 1) / w) * (kTcCfg[v].bn + 110);
+            if (variant < 0 || cost < best) {
+                best = cost;
+                variant = v;
+            }
+        }
     }
     if (variant >= kTcVariants) return LIN_ERR_UNSUPPORTED;
+    const long long tiles = (long long)ceil_div(M, 128) * ceil_div(N, kTcCfg[variant].bn);
+    const long long w = width > 0 ? width : sm;
     plan_common(p, LIN_KERNEL_TC, variant);
     p->bm = 128;
     p->bn = kTcCfg[variant].bn;
     p->bk = 0;  // 128 bytes of K: 64 bf16 or 32 fp32
-    p->stages = kTcCfg[variant].stages;
-    p->grid_x = ceil_div(N, p->bn);
-    p->grid_y = ceil_div(M, 128);
+    p->stages = 0;  // derived in the kernel from the shared-memory budget
+    p->grid_x = (int)(tiles < w ? tiles : w);
+    p->grid_y = 1;
     p->grid_z = 1;
     p->threads = kTcThreads;
     return LIN_OK;
@@ -189,9 +196,9 @@ int plan_default(int sm, int M, int N, int K, int precision, size_t ws, lin_plan
     switch (precision) {
         case LIN_PREC_BF16:
             if (M <= 16) return make_skinny(sm, 0, 0, M, N, K, ws, p);
-            return make_tc(sm, -1, M, N, K, p);
+            return make_tc(sm, -1, 0, M, N, K, p);
         case LIN_PREC_TF32:
-            return make_tc(sm, -1, M, N, K, p);
+            return make_tc(sm, -1, 0, M, N, K, p);
         default:
             return make_ffma(sm, -1, 0, M, N, K, ws, p);
     }
@@ -288,7 +295,8 @@ int check_plan_fits(const lin_plan& p, int M, int N, int K, int precision) {
         case LIN_KERNEL_TC: {
             if (precision == LIN_PREC_FP32 || K == 0) return LIN_ERR_UNSUPPORTED;
             if (p.variant < 0 || p.variant >= kTcVariants || p.splits != 1) return LIN_ERR_UNSUPPORTED;
-            if (p.bn != kTcCfg[p.variant].bn || p.grid_x != ceil_div(N, p.bn) || p.grid_y != ceil_div(M, 128))
+            const long long tiles = (long long)ceil_div(M, 128) * ceil_div(N, kTcCfg[p.variant].bn);
+            if (p.bn != kTcCfg[p.variant].bn || p.grid_x < 1 || p.grid_x > tiles || p.grid_y != 1)
                 return LIN_ERR_UNSUPPORTED;
             return LIN_OK;
         }
@@ -458,8 +466,8 @@ int lin_plan_make(int sm_count, int kernel, int variant, int splits, int M, int 
             if (precision != LIN_PREC_FP32) return LIN_ERR_UNSUPPORTED;
             return lin::make_ffma(sm_count, variant, splits, M, N, K, unlimited, out);
         case LIN_KERNEL_TC:
-            if (precision == LIN_PREC_FP32 || splits > 1) return LIN_ERR_UNSUPPORTED;
-            return lin::make_tc(sm_count, variant, M, N, K, out);
+            if (precision == LIN_PREC_FP32) return LIN_ERR_UNSUPPORTED;
+            return lin::make_tc(sm_count, variant, splits, M, N, K, out);  // splits = CTAs (0 = one per SM)
         case LIN_KERNEL_NONE:
         case LIN_KERNEL_FILL:
             return lin::plan_default(sm_count, M, N, K, precision, unlimited, out);

@@ -39,12 +39,34 @@ struct TcArgs {
     const float* bias;
     void* Y;
     int* status;
-    int y_aligned16;  // Y's base is 16-byte aligned (vector stores allowed)
+    int y_aligned16;     // Y's base is 16-byte aligned (vector stores allowed)
+    int bias_aligned16;  // bias is 16-byte aligned (vector loads allowed)
 };
 
-template <bool BF16, int BN, int STAGES, bool GELU>
+// Epilogue staging: each epilogue warp owns a 32 x 32 output tile in shared
+// memory, rows padded by 16 bytes so the row-per-lane writes and the
+// row-segment reads below are (nearly) free of bank conflicts.
+template <bool BF16>
+constexpr int stage_row_bytes() { return BF16 ? 32 * 2 + 16 : 32 * 4 + 16; }
+template <bool BF16>
+constexpr int stage_bytes() { return 8 * 32 * stage_row_bytes<BF16>(); }
+// Ring depth: as many 128-byte K stages as fit beside the staging tiles.
+template <bool BF16, int BN>
+constexpr int tc_stages() {
+    return (227 * 1024 - 2048 - stage_bytes<BF16>()) / (128 * 128 + BN * 128) < 8
+               ? (227 * 1024 - 2048 - stage_bytes<BF16>()) / (128 * 128 + BN * 128)
+               : 8;
+}
+template <bool BF16, int BN>
+constexpr size_t tc_smem_bytes() {
+    return 1024 + (size_t)tc_stages<BF16, BN>() * (128 * 128 + BN * 128) + stage_bytes<BF16>() +
+           (2 * tc_stages<BF16, BN>() + 4) * 8 + 16;
+}
+
+template <bool BF16, int BN, bool GELU>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcArgs a) {
+    constexpr int STAGES = tc_stages<BF16, BN>();
     constexpr int BM = 128;
     constexpr int ESZ = BF16 ? 2 : 4;
     constexpr int BK = 128 / ESZ;                 // K elements per stage (128 bytes)
@@ -52,31 +74,39 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     constexpr uint32_t B_BYTES = BN * 128;
     constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES;
     constexpr int MMAS = 4;                       // 32 bytes of K per MMA
-    constexpr uint32_t TMEM_COLS = BN;            // power of two, >= 32
+    constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;  // two accumulators
+    constexpr uint32_t BUF_COLS = BN <= 128 ? BN : 256;          // column offset of the second one
     constexpr uint32_t IDESC = make_idesc(BF16 ? 1u : 2u, BM, BN);
-    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "N tile");
+    constexpr int EPI_WARPS = kTcThreads / 32 - 2;  // two per TMEM lane quadrant
+    constexpr int HALF = BN / 2;                  // columns per epilogue warp
+    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "N tile");
+    static_assert(EPI_WARPS == 8, "8 epilogue warps");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * A_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+    uint8_t* sOut = sB + STAGES * B_BYTES;  // 8 warps x 32 rows x stage_row_bytes
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + stage_bytes<BF16>());  // full[S] empty[S] tfull[2] tempty[2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
     int* s_abort = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+    const int mt = (a.M + BM - 1) / BM, nt = (a.N + BN - 1) / BN;
+    const int ntiles = mt * nt;
     const int nkb = (a.K + BK - 1) / BK;
-    const uint32_t full0 = smem_u32(bars);
-    const uint32_t empty0 = smem_u32(bars + STAGES);
-    const uint32_t accum_bar = smem_u32(bars + 2 * STAGES);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+    const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
         }
-        mbar_init(accum_bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull0 + 8 * b, 1);
+            mbar_init(tempty0 + 8 * b, EPI_WARPS);
+        }
         *s_abort = 0;
         mbar_fence_init();
         tma_prefetch_map(&tmA);
@@ -95,109 +125,165 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---- TMA producer ----
-            int issued = 0;
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int s = kb % STAGES;
-                const uint32_t ph = (kb / STAGES) & 1;
-                if (*(volatile int*)s_abort || !mbar_wait(empty0 + 8 * s, ph ^ 1)) {
-                    give_up();
-                    break;
+            // ---- TMA producer: the K stages of this CTA's tiles, in order ----
+            uint32_t it = 0, issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                const int m0 = (tile % mt) * BM, n0 = (tile / mt) * BN;
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+                    if (*(volatile int*)s_abort || !mbar_wait(empty0 + 8 * s, ph ^ 1)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(full0 + 8 * s, STAGE_TX);
+                    tma_load_2d(smem_u32(sA + s * A_BYTES), &tmA, full0 + 8 * s, kb * BK, m0);
+                    tma_load_2d(smem_u32(sB + s * B_BYTES), &tmB, full0 + 8 * s, kb * BK, n0);
+                    issued = it + 1;
                 }
-                mbar_expect_tx(full0 + 8 * s, STAGE_TX);
-                tma_load_2d(smem_u32(sA + s * A_BYTES), &tmA, full0 + 8 * s, kb * BK, m0);
-                tma_load_2d(smem_u32(sB + s * B_BYTES), &tmB, full0 + 8 * s, kb * BK, n0);
-                issued = kb + 1;
             }
             if (*(volatile int*)s_abort) {
                 // Drain this CTA's own copies still in flight before the CTA exits.
-                const int first = issued > STAGES ? issued - STAGES : 0;
-                for (int kb = first; kb < issued; ++kb) mbar_wait(full0 + 8 * (kb % STAGES), (kb / STAGES) & 1);
+                const uint32_t first = issued > (uint32_t)STAGES ? issued - STAGES : 0;
+                for (uint32_t i = first; i < issued; ++i) mbar_wait(full0 + 8 * (i % STAGES), (i / STAGES) & 1);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // ---- MMA issuer ----
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int s = kb % STAGES;
-                const uint32_t ph = (kb / STAGES) & 1;
-                if (*(volatile int*)s_abort || !mbar_wait(full0 + 8 * s, ph)) {
+            // ---- MMA issuer: accumulators alternate between two TMEM buffers ----
+            uint32_t it = 0;
+            int j = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++j) {
+                const uint32_t buf = j & 1;
+                if (*(volatile int*)s_abort || !mbar_wait(tempty0 + 8 * buf, ((j >> 1) & 1) ^ 1)) {
                     give_up();
                     break;
                 }
                 tc_fence_after();
-                const uint64_t ad = sw128_kmajor_desc(smem_u32(sA + s * A_BYTES));
-                const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + s * B_BYTES));
+                const uint32_t d = tmem_base + buf * BUF_COLS;
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+                    if (*(volatile int*)s_abort || !mbar_wait(full0 + 8 * s, ph)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = sw128_kmajor_desc(smem_u32(sA + s * A_BYTES));
+                    const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + s * B_BYTES));
 #pragma unroll
-                for (int kk = 0; kk < MMAS; ++kk)
-                    tc_mma<BF16>(tmem_base, ad + 2u * kk, bd + 2u * kk, IDESC, (kb | kk) != 0 ? 1u : 0u);
-                tc_commit(empty0 + 8 * s);
+                    for (int kk = 0; kk < MMAS; ++kk)
+                        tc_mma<BF16>(d, ad + 2u * kk, bd + 2u * kk, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                    tc_commit(empty0 + 8 * s);
+                }
+                tc_commit(tfull0 + 8 * buf);
             }
-            tc_commit(accum_bar);
             // Do not reach the teardown before this CTA's MMAs have completed.
-            if (!mbar_wait(accum_bar, 0)) give_up();
+            if (j > 0 && !mbar_wait(tfull0 + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1)) give_up();
         }
     } else {
-        // ---- epilogue: warps 2..5 ----
-        const int q = warp & 3;  // TMEM lane quadrant this warp may access
-        const int m = m0 + q * 32 + lane;
-        const bool mine = mbar_wait(accum_bar, 0);
-        if (!mine) give_up();
-        tc_fence_after();
-        // tcgen05.ld is warp-collective: the warp proceeds only if every lane saw
-        // the accumulator complete and no role of this CTA gave up.
-        const bool ok = __all_sync(0xffffffffu, mine && *(volatile int*)s_abort == 0);
-        if (ok) {
-            const int N = a.N;
+        // ---- epilogue: warp w reads TMEM lanes 32*(w%4).., columns half (w-2)/4 ----
+        const int q = warp & 3;
+        const int c_begin = ((warp - 2) >> 2) * HALF;
+        const int N = a.N;
+        int j = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+            const uint32_t buf = j & 1;
+            const int m0 = (tile % mt) * BM, n0 = (tile / mt) * BN;
+            const bool mine = mbar_wait(tfull0 + 8 * buf, (j >> 1) & 1);
+            if (!mine) give_up();
+            tc_fence_after();
+            // tcgen05.ld is warp-collective: a warp proceeds only if every lane saw
+            // the accumulator complete and no role of this CTA gave up.
+            const bool ok = __all_sync(0xffffffffu, mine && *(volatile int*)s_abort == 0);
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                const int nb = n0 + c * 32;
+            for (int c = 0; c < HALF / 32 && ok; ++c) {
+                const int col = c_begin + c * 32;
+                const int nb = n0 + col;
                 if (nb >= N) break;  // warp-uniform
                 uint32_t r[32];
-                tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c * 32), r);
-                if (m < a.M) {
-                    float v[32];
+                tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BUF_COLS + static_cast<uint32_t>(col),
+                          r);
+                const bool full = nb + 32 <= N;
+                float v[32];
+                if (a.bias && full && a.bias_aligned16) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int n = nb + j;
-                        const float b = (a.bias && n < N) ? __ldg(a.bias + n) : 0.f;
-                        v[j] = epilogue<GELU>(__uint_as_float(r[j]), b);
+                    for (int j4 = 0; j4 < 32; j4 += 4) {
+                        const float4 b4 = __ldg(reinterpret_cast<const float4*>(a.bias + nb + j4));
+                        v[j4 + 0] = epilogue<GELU>(__uint_as_float(r[j4 + 0]), b4.x);
+                        v[j4 + 1] = epilogue<GELU>(__uint_as_float(r[j4 + 1]), b4.y);
+                        v[j4 + 2] = epilogue<GELU>(__uint_as_float(r[j4 + 2]), b4.z);
+                        v[j4 + 3] = epilogue<GELU>(__uint_as_float(r[j4 + 3]), b4.w);
                     }
-                    const bool full = nb + 32 <= N;
-                    if constexpr (BF16) {
-                        uint16_t* dst = static_cast<uint16_t*>(a.Y) + (size_t)m * N + nb;
-                        if (full && (N % 8) == 0 && a.y_aligned16) {
+                } else {
 #pragma unroll
-                            for (int j = 0; j < 32; j += 8) {
-                                uint4 o;
-                                o.x = pack_bf16x2(v[j], v[j + 1]);
-                                o.y = pack_bf16x2(v[j + 2], v[j + 3]);
-                                o.z = pack_bf16x2(v[j + 4], v[j + 5]);
-                                o.w = pack_bf16x2(v[j + 6], v[j + 7]);
-                                *reinterpret_cast<uint4*>(dst + j) = o;
-                            }
-                        } else {
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const int n = nb + jj;
+                        const float b = (a.bias && n < N) ? __ldg(a.bias + n) : 0.f;
+                        v[jj] = epilogue<GELU>(__uint_as_float(r[jj]), b);
+                    }
+                }
+                // Lane = row: write the row's 32 values into this warp's staging tile...
+                constexpr int RB = stage_row_bytes<BF16>();
+                uint8_t* st = sOut + (warp - 2) * 32 * RB;
+                uint8_t* mine_row = st + lane * RB;
+                if constexpr (BF16) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (nb + j < N) dst[j] = f32_to_bf16_bits(v[j]);
+                    for (int jj = 0; jj < 32; jj += 8) {
+                        uint4 o;
+                        o.x = pack_bf16x2(v[jj], v[jj + 1]);
+                        o.y = pack_bf16x2(v[jj + 2], v[jj + 3]);
+                        o.z = pack_bf16x2(v[jj + 4], v[jj + 5]);
+                        o.w = pack_bf16x2(v[jj + 6], v[jj + 7]);
+                        *reinterpret_cast<uint4*>(mine_row + jj * 2) = o;
+                    }
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 32; jj += 4)
+                        *reinterpret_cast<float4*>(mine_row + jj * 4) = make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
+                }
+                __syncwarp();
+                // ...then store whole row segments: consecutive lanes, consecutive addresses.
+                const int mrow0 = m0 + q * 32;
+                constexpr int ESZO = BF16 ? 2 : 4;
+                constexpr int LPR = 32 * ESZO / 16;  // lanes per row with 16-byte pieces
+                if (full && (N * ESZO) % 16 == 0 && a.y_aligned16) {
+                    const int sub = lane % LPR, rsub = lane / LPR;
+#pragma unroll
+                    for (int r0 = 0; r0 < 32; r0 += 32 / LPR) {
+                        const int rr = r0 + rsub;
+                        if (mrow0 + rr < a.M) {
+                            const uint4 val = *reinterpret_cast<const uint4*>(st + rr * RB + sub * 16);
+                            uint8_t* dst = static_cast<uint8_t*>(a.Y) + ((size_t)(mrow0 + rr) * N + nb) * ESZO + sub * 16;
+                            *reinterpret_cast<uint4*>(dst) = val;
                         }
-                    } else {
-                        float* dst = static_cast<float*>(a.Y) + (size_t)m * N + nb;
-                        if (full && (N % 4) == 0 && a.y_aligned16) {
-#pragma unroll
-                            for (int j = 0; j < 32; j += 4)
-                                *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (nb + j < N) dst[j] = v[j];
+                    }
+                } else {
+                    const bool col_ok = nb + lane < N;
+#pragma unroll 4
+                    for (int rr = 0; rr < 32; ++rr) {
+                        if (mrow0 + rr < a.M && col_ok) {
+                            if constexpr (BF16)
+                                static_cast<uint16_t*>(a.Y)[(size_t)(mrow0 + rr) * N + nb + lane] =
+                                    *reinterpret_cast<const uint16_t*>(st + rr * RB + lane * 2);
+                            else
+                                static_cast<float*>(a.Y)[(size_t)(mrow0 + rr) * N + nb + lane] =
+                                    *reinterpret_cast<const float*>(st + rr * RB + lane * 4);
                         }
                     }
                 }
+                __syncwarp();  // the staging tile is rewritten by the next chunk
             }
+            // This warp's reads of the buffer are done: let the MMA issuer reuse it.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
         }
     }
 
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -208,10 +294,11 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 
 // ---------------------------------------------------------------- host side
 
-template <bool BF16, int BN, int STAGES, bool GELU>
+template <bool BF16, int BN, bool GELU>
 int launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, dim3 grid, cudaStream_t st) {
-    constexpr size_t smem = STAGES * (128 * 128 + BN * 128) + 1024 + 256;
-    auto kern = tc_kernel<BF16, BN, STAGES, GELU>;
+    constexpr size_t smem = tc_smem_bytes<BF16, BN>();
+    static_assert(tc_smem_bytes<BF16, BN>() <= 227 * 1024, "shared memory");
+    auto kern = tc_kernel<BF16, BN, GELU>;
     static unsigned long long attr_set = 0;  // one attribute call per instantiation and device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return LIN_ERR_CUDA;
@@ -229,8 +316,9 @@ template <bool BF16, bool GELU>
 int launch_variant(int variant, const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, dim3 grid,
                    cudaStream_t st) {
     switch (variant) {
-        case 0: return launch_cfg<BF16, kTcCfg[0].bn, kTcCfg[0].stages, GELU>(ta, tb, a, grid, st);
-        case 1: return launch_cfg<BF16, kTcCfg[1].bn, kTcCfg[1].stages, GELU>(ta, tb, a, grid, st);
+        case 0: return launch_cfg<BF16, kTcCfg[0].bn, GELU>(ta, tb, a, grid, st);
+        case 1: return launch_cfg<BF16, kTcCfg[1].bn, GELU>(ta, tb, a, grid, st);
+        case 2: return launch_cfg<BF16, kTcCfg[2].bn, GELU>(ta, tb, a, grid, st);
         default: return LIN_ERR_UNSUPPORTED;
     }
 }
@@ -282,6 +370,7 @@ int launch_tc(const Problem& p, const lin_plan& plan) {
     a.Y = p.Y;
     a.status = p.dev_status;
     a.y_aligned16 = (reinterpret_cast<uintptr_t>(p.Y) % 16) == 0;
+    a.bias_aligned16 = (reinterpret_cast<uintptr_t>(p.bias) % 16) == 0;
     const dim3 grid(plan.grid_x, plan.grid_y, 1);
     const bool gelu = p.epilogue == LIN_EPI_GELU_TANH;
     if (bf16)
