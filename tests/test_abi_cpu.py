@@ -145,10 +145,13 @@ def test_plan_make_families():
         tll.plan_make(SM, tll.KERNEL_SKINNY, 0, 0, 17, 4096, 4096, "bf16")
     with pytest.raises(tll.LinError):
         tll.plan_make(SM, tll.KERNEL_FFMA, 0, 0, 16, 64, 64, "bf16")
-    for v, bn in ((0, 256), (1, 128), (2, 192)):
+    for v, bn in ((0, 256), (1, 128), (2, 192), (3, 256), (4, 128), (5, 192)):
         p = tll.plan_make(SM, tll.KERNEL_TC, v, 2, 4096, 4096, 256, "tf32")
         assert p.bn == bn and p.grid_x == 2
+    for width in (0, 1, 3, 151):
+        p = tll.plan_make(SM, tll.KERNEL_TC, 3, width, 8192, 2304, 768, "bf16")
+        assert p.grid_x % 2 == 0 and 2 <= p.grid_x <= SM
     with pytest.raises(tll.LinError):
-        tll.plan_make(SM, tll.KERNEL_TC, 3, 0, 256, 256, 256, "tf32")
+        tll.plan_make(SM, tll.KERNEL_TC, 6, 0, 256, 256, 256, "tf32")
     p = tll.plan_make(SM, tll.KERNEL_FFMA, 1, 7, 128, 768, 768, "fp32")
     assert p.grid_z == 7 and p.workspace_bytes >= 7 * 128 * 768 * 4

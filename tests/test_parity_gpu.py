@@ -35,7 +35,7 @@ def all_plans(ctx, M, N, K, precision):
             for width in (0, 2 * sm, 5):
                 plans.append(tll.plan_make(sm, tll.KERNEL_SKINNY_SK, v, width, M, N, K, "bf16"))
     if precision in (BF16, TF32):
-        for v in range(3):
+        for v in range(6):  # 3-5: 2-CTA clusters multicasting the W tile
             for width in (0, 1, 3):  # persistent CTAs: one per SM, or few CTAs walking many tiles
                 plans.append(tll.plan_make(sm, tll.KERNEL_TC, v, width, M, N, K, PREC_NAME[precision]))
     if precision == FP32:

@@ -56,9 +56,10 @@ struct FfmaCfg { int bm, bn, bk, tm, tn; };        // 256 threads each
 constexpr int kFfmaVariants = 2;
 constexpr FfmaCfg kFfmaCfg[kFfmaVariants] = {{128, 128, 16, 8, 8}, {64, 64, 16, 4, 4}};
 
-struct TcCfg { int bn; };                          // BM = 128, BK = 128 bytes of K; ring depth from smem
-constexpr int kTcVariants = 3;
-constexpr TcCfg kTcCfg[kTcVariants] = {{256}, {128}, {192}};
+struct TcCfg { int bn; bool pair; };              // BM = 128, BK = 128 bytes of K; ring depth from smem
+constexpr int kTcVariants = 6;                     // pair: 2 x 1 clusters sharing (multicasting) the B tile
+constexpr TcCfg kTcCfg[kTcVariants] = {{256, false}, {128, false}, {192, false},
+                                       {256, true}, {128, true}, {192, true}};
 constexpr int kTcThreads = 320;                    // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 
 // Launchers (return LIN_OK or LIN_ERR_*). They assume the plan was validated.

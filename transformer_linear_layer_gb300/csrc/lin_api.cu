@@ -143,15 +143,18 @@ int make_ffma(int sm, int variant, int splits, int M, int N, int K, size_t ws, l
 }
 
 // Persistent tcgen05 kernel: `width` CTAs walk the 128 x BN output tiles
-// (0 = one CTA per SM) in static round robin. N tile: the smallest predicted
-// time rounds(BN) x (BN + 110), where rounds = ceil(tiles / CTAs) and the
-// constant 110 (in columns) is the per-tile cost that does not scale with BN,
-// fitted to the measured M = 8192 and 4096^3 shapes.
+// (0 = one CTA per SM) in static round robin; pair variants walk vertical
+// tile pairs with one 2-CTA cluster per pair (grid rounded down to even).
+// Default N tile: the smallest predicted time rounds(BN) x (BN + 110), where
+// rounds = ceil(work items / CTAs) and the constant 110 (in columns) is the
+// per-tile cost that does not scale with BN, fitted to the measured M = 8192
+// and 4096^3 shapes.
 int make_tc(int sm, int variant, int width, int M, int N, int K, lin_plan* p) {
     if (M < 1 || N < 1 || K < 1 || width < 0) return LIN_ERR_UNSUPPORTED;
     if (variant < 0) {
         double best = 0.0;
         for (int v = 0; v < kTcVariants; ++v) {
+            if (kTcCfg[v].pair) continue;
             const long long t = (long long)ceil_div(M, 128) * ceil_div(N, kTcCfg[v].bn);
             const long long w = width > 0 ? width : sm;
             const double cost = (double)((t + w - 1) / w) * (kTcCfg[v].bn + 110);
@@ -162,14 +165,22 @@ int make_tc(int sm, int variant, int width, int M, int N, int K, lin_plan* p) {
         }
     }
     if (variant >= kTcVariants) return LIN_ERR_UNSUPPORTED;
-    const long long tiles = (long long)ceil_div(M, 128) * ceil_div(N, kTcCfg[variant].bn);
-    const long long w = width > 0 ? width : sm;
+    const bool pair = kTcCfg[variant].pair;
+    const long long items = (long long)(pair ? ceil_div(ceil_div(M, 128), 2) : ceil_div(M, 128)) *
+                            ceil_div(N, kTcCfg[variant].bn);
+    long long w = width > 0 ? width : sm;
+    if (pair) {
+        w = (w / 2 < items ? w / 2 : items) * 2;
+        if (w < 2) w = 2;
+    } else if (w > items) {
+        w = items;
+    }
     plan_common(p, LIN_KERNEL_TC, variant);
     p->bm = 128;
     p->bn = kTcCfg[variant].bn;
     p->bk = 0;  // 128 bytes of K: 64 bf16 or 32 fp32
     p->stages = 0;  // derived in the kernel from the shared-memory budget
-    p->grid_x = (int)(tiles < w ? tiles : w);
+    p->grid_x = (int)w;
     p->grid_y = 1;
     p->grid_z = 1;
     p->threads = kTcThreads;
@@ -295,8 +306,12 @@ int check_plan_fits(const lin_plan& p, int M, int N, int K, int precision) {
         case LIN_KERNEL_TC: {
             if (precision == LIN_PREC_FP32 || K == 0) return LIN_ERR_UNSUPPORTED;
             if (p.variant < 0 || p.variant >= kTcVariants || p.splits != 1) return LIN_ERR_UNSUPPORTED;
-            const long long tiles = (long long)ceil_div(M, 128) * ceil_div(N, kTcCfg[p.variant].bn);
-            if (p.bn != kTcCfg[p.variant].bn || p.grid_x < 1 || p.grid_x > tiles || p.grid_y != 1)
+            const bool pair = kTcCfg[p.variant].pair;
+            const long long items = (long long)(pair ? ceil_div(ceil_div(M, 128), 2) : ceil_div(M, 128)) *
+                                    ceil_div(N, kTcCfg[p.variant].bn);
+            const long long ctas = pair ? 2 * items : items;
+            if (p.bn != kTcCfg[p.variant].bn || p.grid_x < 1 || p.grid_x > ctas || p.grid_y != 1 ||
+                (pair && p.grid_x % 2 != 0))
                 return LIN_ERR_UNSUPPORTED;
             return LIN_OK;
         }

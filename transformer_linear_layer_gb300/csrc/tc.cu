@@ -46,10 +46,14 @@ struct TcArgs {
 // Epilogue staging: each epilogue warp owns a 32 x 32 output tile in shared
 // memory, rows padded by 16 bytes so the row-per-lane writes and the
 // row-segment reads below are (nearly) free of bank conflicts.
+// fp32 outputs pass through in two halves of 16 rows, so both dtypes stage
+// about 20 KiB and keep the ring deep.
 template <bool BF16>
 constexpr int stage_row_bytes() { return BF16 ? 32 * 2 + 16 : 32 * 4 + 16; }
 template <bool BF16>
-constexpr int stage_bytes() { return 8 * 32 * stage_row_bytes<BF16>(); }
+constexpr int stage_rows() { return BF16 ? 32 : 16; }
+template <bool BF16>
+constexpr int stage_bytes() { return 8 * stage_rows<BF16>() * stage_row_bytes<BF16>(); }
 // Ring depth: as many 128-byte K stages as fit beside the staging tiles.
 template <bool BF16, int BN>
 constexpr int tc_stages() {
@@ -63,7 +67,14 @@ constexpr size_t tc_smem_bytes() {
            (2 * tc_stages<BF16, BN>() + 4) * 8 + 16;
 }
 
-template <bool BF16, int BN, bool GELU>
+// PAIR: the CTAs run as 2 x 1 clusters. The two CTAs of a cluster compute
+// vertically adjacent tiles (M blocks 2i and 2i+1, the same N block) in lock
+// step; each loads its own A tile and one half of the shared B tile, and
+// multicasts that half into both CTAs' shared memory, so each SM reads
+// 16 + BN*64 bytes per K stage from L2 instead of 16 + BN*128 KiB. A stage is
+// refilled only after both CTAs' MMAs released it (each MMA thread commits to
+// the "empty" barrier of both CTAs).
+template <bool BF16, int BN, bool GELU, bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcArgs a) {
     constexpr int STAGES = tc_stages<BF16, BN>();
@@ -93,7 +104,14 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int mt = (a.M + BM - 1) / BM, nt = (a.N + BN - 1) / BN;
-    const int ntiles = mt * nt;
+    // Work items: single tiles, or (for PAIR) vertical pairs of tiles per cluster.
+    const int mu = PAIR ? (mt + 1) / 2 : mt;
+    const int ntiles = mu * nt;
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const int first_item = PAIR ? (int)cluster_id_x() : (int)blockIdx.x;
+    const int item_step = PAIR ? (int)cluster_count_x() : (int)gridDim.x;
+    auto tile_m0 = [&](int item) { return (PAIR ? 2 * (item % mu) + (int)rank : item % mu) * BM; };
+    auto tile_n0 = [&](int item) { return (item / mu) * BN; };
     const int nkb = (a.K + BK - 1) / BK;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
     const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
@@ -101,7 +119,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, PAIR ? 2 : 1);  // PAIR: released by both CTAs' MMAs
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull0 + 8 * b, 1);
@@ -114,7 +132,10 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     }
     if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR)
+        cluster_sync_all();  // the peer's barriers exist before any multicast reaches them
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -128,8 +149,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             // ---- TMA producer: the K stages of this CTA's tiles, in order ----
             uint32_t it = 0, issued = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-                const int m0 = (tile % mt) * BM, n0 = (tile / mt) * BN;
+            for (int tile = first_item; tile < ntiles && ok; tile += item_step) {
+                const int m0 = tile_m0(tile), n0 = tile_n0(tile);
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                     if (*(volatile int*)s_abort || !mbar_wait(empty0 + 8 * s, ph ^ 1)) {
@@ -139,7 +160,13 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     }
                     mbar_expect_tx(full0 + 8 * s, STAGE_TX);
                     tma_load_2d(smem_u32(sA + s * A_BYTES), &tmA, full0 + 8 * s, kb * BK, m0);
-                    tma_load_2d(smem_u32(sB + s * B_BYTES), &tmB, full0 + 8 * s, kb * BK, n0);
+                    if constexpr (PAIR) {
+                        constexpr uint32_t HALF_B = (BN / 2) * 128;
+                        tma_load_2d_mc(smem_u32(sB + s * B_BYTES + rank * HALF_B), &tmB, full0 + 8 * s, kb * BK,
+                                       n0 + (int)rank * (BN / 2), (uint16_t)0x3);
+                    } else {
+                        tma_load_2d(smem_u32(sB + s * B_BYTES), &tmB, full0 + 8 * s, kb * BK, n0);
+                    }
                     issued = it + 1;
                 }
             }
@@ -155,7 +182,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             uint32_t it = 0;
             int j = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++j) {
+            for (int tile = first_item; tile < ntiles && ok; tile += item_step, ++j) {
                 const uint32_t buf = j & 1;
                 if (*(volatile int*)s_abort || !mbar_wait(tempty0 + 8 * buf, ((j >> 1) & 1) ^ 1)) {
                     give_up();
@@ -176,7 +203,10 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 #pragma unroll
                     for (int kk = 0; kk < MMAS; ++kk)
                         tc_mma<BF16>(d, ad + 2u * kk, bd + 2u * kk, IDESC, (kb | kk) != 0 ? 1u : 0u);
-                    tc_commit(empty0 + 8 * s);
+                    if constexpr (PAIR)
+                        tc_commit_mc(empty0 + 8 * s, (uint16_t)0x3);
+                    else
+                        tc_commit(empty0 + 8 * s);
                 }
                 tc_commit(tfull0 + 8 * buf);
             }
@@ -189,9 +219,9 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         const int c_begin = ((warp - 2) >> 2) * HALF;
         const int N = a.N;
         int j = 0;
-        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+        for (int tile = first_item; tile < ntiles; tile += item_step, ++j) {
             const uint32_t buf = j & 1;
-            const int m0 = (tile % mt) * BM, n0 = (tile / mt) * BN;
+            const int m0 = tile_m0(tile), n0 = tile_n0(tile);
             const bool mine = mbar_wait(tfull0 + 8 * buf, (j >> 1) & 1);
             if (!mine) give_up();
             tc_fence_after();
@@ -225,56 +255,67 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                         v[jj] = epilogue<GELU>(__uint_as_float(r[jj]), b);
                     }
                 }
-                // Lane = row: write the row's 32 values into this warp's staging tile...
+                // Lane = row: write the row's 32 values into this warp's staging tile
+                // (rows [h*RP, h*RP + RP) per pass), then store whole row segments:
+                // consecutive lanes, consecutive addresses.
                 constexpr int RB = stage_row_bytes<BF16>();
-                uint8_t* st = sOut + (warp - 2) * 32 * RB;
-                uint8_t* mine_row = st + lane * RB;
-                if constexpr (BF16) {
-#pragma unroll
-                    for (int jj = 0; jj < 32; jj += 8) {
-                        uint4 o;
-                        o.x = pack_bf16x2(v[jj], v[jj + 1]);
-                        o.y = pack_bf16x2(v[jj + 2], v[jj + 3]);
-                        o.z = pack_bf16x2(v[jj + 4], v[jj + 5]);
-                        o.w = pack_bf16x2(v[jj + 6], v[jj + 7]);
-                        *reinterpret_cast<uint4*>(mine_row + jj * 2) = o;
-                    }
-                } else {
-#pragma unroll
-                    for (int jj = 0; jj < 32; jj += 4)
-                        *reinterpret_cast<float4*>(mine_row + jj * 4) = make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
-                }
-                __syncwarp();
-                // ...then store whole row segments: consecutive lanes, consecutive addresses.
-                const int mrow0 = m0 + q * 32;
+                constexpr int RP = stage_rows<BF16>();
                 constexpr int ESZO = BF16 ? 2 : 4;
                 constexpr int LPR = 32 * ESZO / 16;  // lanes per row with 16-byte pieces
-                if (full && (N * ESZO) % 16 == 0 && a.y_aligned16) {
-                    const int sub = lane % LPR, rsub = lane / LPR;
+                uint8_t* st = sOut + (warp - 2) * RP * RB;
+                const int mrow0 = m0 + q * 32;
+                const bool vec = full && (N * ESZO) % 16 == 0 && a.y_aligned16;
 #pragma unroll
-                    for (int r0 = 0; r0 < 32; r0 += 32 / LPR) {
-                        const int rr = r0 + rsub;
-                        if (mrow0 + rr < a.M) {
-                            const uint4 val = *reinterpret_cast<const uint4*>(st + rr * RB + sub * 16);
-                            uint8_t* dst = static_cast<uint8_t*>(a.Y) + ((size_t)(mrow0 + rr) * N + nb) * ESZO + sub * 16;
-                            *reinterpret_cast<uint4*>(dst) = val;
+                for (int h = 0; h < 32 / RP; ++h) {
+                    if (lane / RP == h) {
+                        uint8_t* mine_row = st + (lane % RP) * RB;
+                        if constexpr (BF16) {
+#pragma unroll
+                            for (int jj = 0; jj < 32; jj += 8) {
+                                uint4 o;
+                                o.x = pack_bf16x2(v[jj], v[jj + 1]);
+                                o.y = pack_bf16x2(v[jj + 2], v[jj + 3]);
+                                o.z = pack_bf16x2(v[jj + 4], v[jj + 5]);
+                                o.w = pack_bf16x2(v[jj + 6], v[jj + 7]);
+                                *reinterpret_cast<uint4*>(mine_row + jj * 2) = o;
+                            }
+                        } else {
+#pragma unroll
+                            for (int jj = 0; jj < 32; jj += 4)
+                                *reinterpret_cast<float4*>(mine_row + jj * 4) =
+                                    make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
                         }
                     }
-                } else {
-                    const bool col_ok = nb + lane < N;
+                    __syncwarp();
+                    const int rbase = mrow0 + h * RP;
+                    if (vec) {
+                        const int sub = lane % LPR, rsub = lane / LPR;
+#pragma unroll
+                        for (int r0 = 0; r0 < RP; r0 += 32 / LPR) {
+                            const int rr = r0 + rsub;
+                            if (rbase + rr < a.M) {
+                                const uint4 val = *reinterpret_cast<const uint4*>(st + rr * RB + sub * 16);
+                                uint8_t* dst =
+                                    static_cast<uint8_t*>(a.Y) + ((size_t)(rbase + rr) * N + nb) * ESZO + sub * 16;
+                                *reinterpret_cast<uint4*>(dst) = val;
+                            }
+                        }
+                    } else {
+                        const bool col_ok = nb + lane < N;
 #pragma unroll 4
-                    for (int rr = 0; rr < 32; ++rr) {
-                        if (mrow0 + rr < a.M && col_ok) {
-                            if constexpr (BF16)
-                                static_cast<uint16_t*>(a.Y)[(size_t)(mrow0 + rr) * N + nb + lane] =
-                                    *reinterpret_cast<const uint16_t*>(st + rr * RB + lane * 2);
-                            else
-                                static_cast<float*>(a.Y)[(size_t)(mrow0 + rr) * N + nb + lane] =
-                                    *reinterpret_cast<const float*>(st + rr * RB + lane * 4);
+                        for (int rr = 0; rr < RP; ++rr) {
+                            if (rbase + rr < a.M && col_ok) {
+                                if constexpr (BF16)
+                                    static_cast<uint16_t*>(a.Y)[(size_t)(rbase + rr) * N + nb + lane] =
+                                        *reinterpret_cast<const uint16_t*>(st + rr * RB + lane * 2);
+                                else
+                                    static_cast<float*>(a.Y)[(size_t)(rbase + rr) * N + nb + lane] =
+                                        *reinterpret_cast<const float*>(st + rr * RB + lane * 4);
+                            }
                         }
                     }
+                    __syncwarp();  // the staging rows are rewritten by the next pass / chunk
                 }
-                __syncwarp();  // the staging tile is rewritten by the next chunk
             }
             // This warp's reads of the buffer are done: let the MMA issuer reuse it.
             tc_fence_before();
@@ -285,7 +326,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 
     __syncwarp();
     tc_fence_before();
-    __syncthreads();
+    // PAIR: neither CTA leaves while the peer's copies or arrivals may still
+    // target its shared memory.
+    if constexpr (PAIR)
+        cluster_sync_all();
+    else
+        __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
@@ -294,11 +340,11 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 
 // ---------------------------------------------------------------- host side
 
-template <bool BF16, int BN, bool GELU>
-int launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, dim3 grid, cudaStream_t st) {
+template <bool BF16, int BN, bool GELU, bool PAIR>
+int launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, int grid, cudaStream_t st) {
     constexpr size_t smem = tc_smem_bytes<BF16, BN>();
     static_assert(tc_smem_bytes<BF16, BN>() <= 227 * 1024, "shared memory");
-    auto kern = tc_kernel<BF16, BN, GELU>;
+    auto kern = tc_kernel<BF16, BN, GELU, PAIR>;
     static unsigned long long attr_set = 0;  // one attribute call per instantiation and device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return LIN_ERR_CUDA;
@@ -308,17 +354,32 @@ int launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, di
             return LIN_ERR_CUDA;
         attr_set |= bit;
     }
-    kern<<<grid, kTcThreads, smem, st>>>(ta, tb, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kTcThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = PAIR ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, a) != cudaSuccess) return LIN_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? LIN_OK : LIN_ERR_CUDA;
 }
 
 template <bool BF16, bool GELU>
-int launch_variant(int variant, const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, dim3 grid,
+int launch_variant(int variant, const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, int grid,
                    cudaStream_t st) {
     switch (variant) {
-        case 0: return launch_cfg<BF16, kTcCfg[0].bn, GELU>(ta, tb, a, grid, st);
-        case 1: return launch_cfg<BF16, kTcCfg[1].bn, GELU>(ta, tb, a, grid, st);
-        case 2: return launch_cfg<BF16, kTcCfg[2].bn, GELU>(ta, tb, a, grid, st);
+        case 0: return launch_cfg<BF16, kTcCfg[0].bn, GELU, false>(ta, tb, a, grid, st);
+        case 1: return launch_cfg<BF16, kTcCfg[1].bn, GELU, false>(ta, tb, a, grid, st);
+        case 2: return launch_cfg<BF16, kTcCfg[2].bn, GELU, false>(ta, tb, a, grid, st);
+        case 3: return launch_cfg<BF16, kTcCfg[3].bn, GELU, true>(ta, tb, a, grid, st);
+        case 4: return launch_cfg<BF16, kTcCfg[4].bn, GELU, true>(ta, tb, a, grid, st);
+        case 5: return launch_cfg<BF16, kTcCfg[5].bn, GELU, true>(ta, tb, a, grid, st);
         default: return LIN_ERR_UNSUPPORTED;
     }
 }
@@ -359,9 +420,11 @@ bool make_kmajor_map(CUtensorMap* map, const void* base, bool bf16, int rows, in
 
 int launch_tc(const Problem& p, const lin_plan& plan) {
     const bool bf16 = p.precision == LIN_PREC_BF16;
+    if (plan.variant < 0 || plan.variant >= kTcVariants) return LIN_ERR_UNSUPPORTED;
+    const bool pair = kTcCfg[plan.variant].pair;
     CUtensorMap ta, tb;
     if (!make_kmajor_map(&ta, p.X, bf16, p.M, p.K, 128)) return LIN_ERR_CUDA;
-    if (!make_kmajor_map(&tb, p.W, bf16, p.N, p.K, plan.bn)) return LIN_ERR_CUDA;
+    if (!make_kmajor_map(&tb, p.W, bf16, p.N, p.K, pair ? plan.bn / 2 : plan.bn)) return LIN_ERR_CUDA;
     TcArgs a;
     a.M = p.M;
     a.N = p.N;
@@ -371,7 +434,7 @@ int launch_tc(const Problem& p, const lin_plan& plan) {
     a.status = p.dev_status;
     a.y_aligned16 = (reinterpret_cast<uintptr_t>(p.Y) % 16) == 0;
     a.bias_aligned16 = (reinterpret_cast<uintptr_t>(p.bias) % 16) == 0;
-    const dim3 grid(plan.grid_x, plan.grid_y, 1);
+    const int grid = plan.grid_x;
     const bool gelu = p.epilogue == LIN_EPI_GELU_TANH;
     if (bf16)
         return gelu ? launch_variant<true, true>(plan.variant, ta, tb, a, grid, p.stream)
