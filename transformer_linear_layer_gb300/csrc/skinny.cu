@@ -52,28 +52,30 @@ constexpr uint32_t kSkXBox = kSkMP * 128;
 
 // A stage holds KBOX boxes of 64 K each: the boxes of one stage are issued
 // together, so each W row is read as a run of KBOX * 128 contiguous bytes
-// (DRAM rows stay open across the run). The 16 x 128 fp32 partial-sum tile
-// reuses the first W box: it is written only after the last MMA completed.
-constexpr size_t skinny_smem_bytes(int stages, int kbox) {
-    return 1024 + (size_t)stages * kbox * (kSkWBox + kSkXBox) + (2 * stages + 1) * 8 + 16;
+// (DRAM rows stay open across the run). Shared memory: the stage ring, then
+// (cluster split) the incoming partial sums of the CL CTAs for the columns
+// this CTA finishes, then the mbarriers.
+constexpr size_t skinny_smem_bytes(int stages, int kbox, int cl) {
+    return 1024 + (size_t)stages * kbox * (kSkWBox + kSkXBox) + (cl > 1 ? (size_t)cl * kSkMP * (kSkRows / cl) * 4 : 0) +
+           (2 * stages + 2) * 8 + 16;
 }
-static_assert(kSkMP * kSkRows * 4 <= kSkWBox, "partial tile fits in one W box");
 
 template <int STAGES, int KBOX, int CL, bool GELU>
 __global__ void __launch_bounds__(kSkinnyThreads, 1)
 skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const SkinnyArgs a) {
-    constexpr uint32_t TMEM_COLS = 32;
+    constexpr int NACC = KBOX < 4 ? KBOX : 4;          // independent accumulators (MMA chains)
+    constexpr uint32_t TMEM_COLS = NACC * kSkMP <= 32 ? 32 : 64;
     constexpr uint32_t IDESC = make_idesc(1u, kSkRows, kSkMP);
-    constexpr int COLS = kSkRows / CL;  // output columns this CTA reduces
+    constexpr int COLS = kSkRows / CL;  // output columns this CTA finishes
     constexpr uint32_t WB = KBOX * kSkWBox, XB = KBOX * kSkXBox;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sW = smem;
     uint8_t* sX = sW + STAGES * WB;
-    float* red = reinterpret_cast<float*>(sW);  // [kSkMP][kSkRows], after the last MMA
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sX + STAGES * XB);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+    float* inbox = reinterpret_cast<float*>(sX + STAGES * XB);  // [CL][kSkMP][COLS] (cluster split)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(inbox + (CL > 1 ? CL * kSkMP * COLS : 0));
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2);
     int* s_abort = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -82,7 +84,8 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
     const int kb0 = (int)((long long)rank * a.kblocks / CL);
     const int kb1 = (int)((long long)(rank + 1) * a.kblocks / CL);
     const int nkb = kb1 - kb0;
-    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES), accum_bar = smem_u32(bars + 2 * STAGES);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+    const uint32_t accum_bar = smem_u32(bars + 2 * STAGES), inbox_bar = smem_u32(bars + 2 * STAGES + 1);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -90,6 +93,7 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
             mbar_init(empty0 + 8 * s, 1);
         }
         mbar_init(accum_bar, 1);
+        mbar_init(inbox_bar, kSkRows);  // one arrival per W row of the block, from whichever CTA holds it
         *s_abort = 0;
         mbar_fence_init();
         tma_prefetch_map(&tmW);
@@ -99,6 +103,9 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Peers may write into this CTA's inbox only after every CTA of the cluster
+    // initialised its barriers: arrive now, wait just before the first remote write.
+    if constexpr (CL > 1) cluster_arrive_relaxed();
     const uint32_t tmem_base = *tmem_slot;
     if (threadIdx.x == 0) pdl_launch_dependents();
 
@@ -151,7 +158,8 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
         }
     } else if (warp == 1) {
         if (lane == 0 && nkb > 0) {
-            // ---- MMA issuer ----
+            // ---- MMA issuer: box b of every stage accumulates into accumulator b % NACC,
+            // so up to NACC MMA chains run side by side ----
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % STAGES;
                 const uint32_t ph = (i / STAGES) & 1;
@@ -164,9 +172,11 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
                 for (int b = 0; b < KBOX; ++b) {
                     const uint64_t ad = sw128_kmajor_desc(smem_u32(sW + s * WB + b * kSkWBox));
                     const uint64_t bd = sw128_kmajor_desc(smem_u32(sX + s * XB + b * kSkXBox));
+                    const uint32_t d = tmem_base + (uint32_t)((b % NACC) * kSkMP);
+                    const bool fresh = (i == 0) && (b < NACC);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        tc_mma<true>(tmem_base, ad + 2u * kk, bd + 2u * kk, IDESC, (i | b | kk) != 0 ? 1u : 0u);
+                        tc_mma<true>(d, ad + 2u * kk, bd + 2u * kk, IDESC, (fresh && kk == 0) ? 0u : 1u);
                 }
                 tc_commit(empty0 + 8 * s);
             }
@@ -186,54 +196,62 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
             if (!mine) give_up();
             tc_fence_after();
             if (__all_sync(0xffffffffu, mine && *(volatile int*)s_abort == 0)) {
-                uint32_t r[16];
-                tmem_ld16(tmem_base + (static_cast<uint32_t>(q * 32) << 16), r);
 #pragma unroll
-                for (int m = 0; m < kSkMP; ++m) v[m] = __uint_as_float(r[m]);
+                for (int c = 0; c < NACC; ++c) {
+                    uint32_t r[16];
+                    tmem_ld16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + (uint32_t)(c * kSkMP), r);
+#pragma unroll
+                    for (int m = 0; m < kSkMP; ++m) v[m] += __uint_as_float(r[m]);
+                }
             }
         }
-#pragma unroll
-        for (int m = 0; m < kSkMP; ++m) red[m * kSkRows + row] = v[m];
-    }
-
-    // Partial sums of every CTA of the cluster are complete and visible.
-    __syncwarp();
-    tc_fence_before();
-    if constexpr (CL > 1)
-        cluster_sync_all();
-    else
-        __syncthreads();
-
-    if (warp >= 2) {
-        const int t = threadIdx.x - 64;
         const int M = a.M, N = a.N;
-        for (int idx = t; idx < M * COLS; idx += 128) {
-            const int m = idx / COLS;
-            const int c = (int)rank * COLS + idx % COLS;
-            const int n = n0 + c;
-            if (n >= N) continue;
-            const uint32_t local = smem_u32(red + m * kSkRows + c);
-            float s = 0.f;
-            if constexpr (CL > 1) {
-                float part[CL];
+        if constexpr (CL == 1) {
+            const int n = n0 + row;
+            if (n < N) {
+                const float b = a.bias ? __ldg(a.bias + n) : 0.f;
 #pragma unroll
-                for (int j = 0; j < CL; ++j) part[j] = dsmem_ld_f32(dsmem_map(local, (uint32_t)j));
-#pragma unroll
-                for (int j = 0; j < CL; ++j) s += part[j];
-            } else {
-                s = red[m * kSkRows + c];
+                for (int m = 0; m < kSkMP; ++m)
+                    if (m < M) a.Y[(size_t)m * N + n] = f32_to_bf16_bits(epilogue<GELU>(v[m], b));
             }
-            const float b = a.bias ? __ldg(a.bias + n) : 0.f;
-            a.Y[(size_t)m * N + n] = f32_to_bf16_bits(epilogue<GELU>(s, b));
+        } else {
+            // Push this row's partial sums into the inbox of the CTA that finishes it,
+            // then arrive there (release at cluster scope covers the stores).
+            cluster_wait();
+            const uint32_t owner = (uint32_t)(row / COLS);
+            const int col = row % COLS;
+            const uint32_t dst = dsmem_map(smem_u32(inbox + ((int)rank * kSkMP) * COLS + col), owner);
+#pragma unroll
+            for (int m = 0; m < kSkMP; ++m) dsmem_st_f32(dst + (uint32_t)(m * COLS * 4), v[m]);
+            mbar_arrive_remote(dsmem_map(inbox_bar, owner));
+            // Finish this CTA's columns: the CL partial sums added in rank order.
+            const int t = threadIdx.x - 64;
+            const bool ok = mbar_wait_cluster(inbox_bar, 0);
+            if (!ok) give_up();
+            constexpr int PER = kSkMP * COLS / 128;  // outputs per thread
+#pragma unroll
+            for (int e = 0; e < PER; ++e) {
+                const int idx = t + 128 * e;
+                const int m = idx / COLS, c = idx % COLS;
+                const int n = n0 + (int)rank * COLS + c;
+                if (ok && m < M && n < N) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int r = 0; r < CL; ++r) acc += inbox[(r * kSkMP + m) * COLS + c];
+                    const float b = a.bias ? __ldg(a.bias + n) : 0.f;
+                    a.Y[(size_t)m * N + n] = f32_to_bf16_bits(epilogue<GELU>(acc, b));
+                }
+            }
         }
     }
 
-    // No CTA leaves (and frees its shared memory) while a peer may still read it.
+    __syncwarp();
+    if constexpr (CL > 1) {
+        // Every thread that arrived on the cluster barrier also waits on it.
+        if (warp < 2) cluster_wait();
+    }
     tc_fence_before();
-    if constexpr (CL > 1)
-        cluster_sync_all();
-    else
-        __syncthreads();
+    __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
@@ -243,7 +261,8 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
 template <int STAGES, int KBOX, int CL, bool GELU>
 int launch_cfg(const CUtensorMap& tw, const CUtensorMap& tx, const SkinnyArgs& a, int grid_x, bool early,
                cudaStream_t st) {
-    constexpr size_t smem = skinny_smem_bytes(STAGES, KBOX);
+    constexpr size_t smem = skinny_smem_bytes(STAGES, KBOX, CL);
+    static_assert(skinny_smem_bytes(STAGES, KBOX, CL) <= 227 * 1024, "shared memory");
     auto kern = skinny_kernel<STAGES, KBOX, CL, GELU>;
     static unsigned long long attr_set = 0;
     int dev = 0;
