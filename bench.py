@@ -248,13 +248,12 @@ def bench_ours(layer: si.Layer, steps: int, warmup: int, world: int, rank: int, 
     xp, yp = x.data_ptr(), y.data_ptr()
     bp = None if bias is None else bias.data_ptr()
     wps = [t.data_ptr() for t in ws]
-    lib_plan = plan
 
     def step(i):
-        rc = ctx.forward_plan_ptr(lib_plan, layer.M, layer.N, layer.K, xp, wps[i % n_copies], bp, yp, epi, prec,
-                                  sptr)
+        # The public call (dispatch table, refined for back-to-back calls).
+        rc = ctx.forward_ptr(layer.M, layer.N, layer.K, xp, wps[i % n_copies], bp, yp, epi, prec, sptr)
         if rc != 0:
-            raise tll.LinError(rc, "lin_forward_plan")
+            raise tll.LinError(rc, "lin_forward")
 
     # Warm-up (also sets kernel attributes before capture).
     with torch.cuda.stream(stream):
@@ -301,6 +300,35 @@ def bench_ours(layer: si.Layer, steps: int, warmup: int, world: int, rank: int, 
     clocks = sampler.stop()
     local_s = e0.elapsed_time(e1) / 1e3
     ctx.check(stream)
+    plan = ctx.last_plan()  # the plan the timed calls ran with
+    # The back-to-back steps overlap on the GPU; their result must still be right.
+    if gate == "full":
+        err_after = oracle.rel_err(y.float().cpu().numpy(), ref)
+    else:
+        got = y[torch.from_numpy(ms).to(dev), torch.from_numpy(ns).to(dev)].float().cpu().numpy()
+        err_after = oracle.rel_err(got, ref)
+    if not err_after <= tol:
+        raise SystemExit(f"output after the timed steps is wrong for {layer.name}: rel_err {err_after} > {tol}")
+
+    # The same call isolated: every call waits for the previous one to finish.
+    ctx.set_option(tll.OPT_EARLY_START, 0)
+    iso_steps = min(steps, 2000)
+    with torch.cuda.stream(stream):
+        step(0)
+    stream.synchronize()
+    g_iso = capture(min(G, iso_steps))
+    with torch.cuda.stream(stream):
+        g_iso.replay()
+        i0 = torch.cuda.Event(enable_timing=True)
+        i1 = torch.cuda.Event(enable_timing=True)
+        i0.record(stream)
+        for _ in range(max(1, iso_steps // min(G, iso_steps))):
+            g_iso.replay()
+        i1.record(stream)
+    stream.synchronize()
+    iso_plan = ctx.last_plan()
+    ctx.set_option(tll.OPT_EARLY_START, 1)
+    iso_s = i0.elapsed_time(i1) / 1e3 / (max(1, iso_steps // min(G, iso_steps)) * min(G, iso_steps))
 
     unit_bytes = layer.algorithmic_bytes()
     max_s, total_units = aggregate(local_s, float(steps) * unit_bytes, world, dev)
@@ -312,8 +340,7 @@ def bench_ours(layer: si.Layer, steps: int, warmup: int, world: int, rank: int, 
         value, unit = world * steps * layer.flops / max_s / 1e12, "TFLOP/s"
 
     peaks, src = load_peaks()
-    kfile = {tll.KERNEL_SKINNY: "skinny.cu", tll.KERNEL_SKINNY_SK: "skinny_sk.cu", tll.KERNEL_FFMA: "ffma.cu",
-             tll.KERNEL_TC: "tc.cu"}.get(plan.kernel)
+    kfile = {tll.KERNEL_SKINNY: "skinny.cu", tll.KERNEL_FFMA: "ffma.cu", tll.KERNEL_TC: "tc.cu"}.get(plan.kernel)
     traffic = traffic_from_profile(kfile, layer.name) if kfile else None
     roof = roofline_for(layer, per_launch_s, peaks, src, traffic)
 
@@ -348,6 +375,10 @@ def bench_ours(layer: si.Layer, steps: int, warmup: int, world: int, rank: int, 
     e2e_val = unit_bytes / e2e_s / 1e9 if unit == "GB/s" else layer.flops / e2e_s / 1e12
     e2e = {"value": round(e2e_val * world, 3), "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "steps": e2e_steps, "api": "transformer_linear_layer_gb300.forward (C ABI lin_forward)"}
+    iso_val = unit_bytes / iso_s / 1e9 if unit == "GB/s" else layer.flops / iso_s / 1e12
+    isolated = {"value": round(iso_val, 3), "unit": unit, "ms_per_step": round(iso_s * 1e3, 6),
+                "plan": {k: v for k, v in iso_plan.as_dict().items() if k != "kernel_name"},
+                "note": "early start off: each call waits for the previous kernel before it starts"}
 
     cpu = None
     if with_cpu_baseline and rank == 0:
@@ -364,7 +395,11 @@ def bench_ours(layer: si.Layer, steps: int, warmup: int, world: int, rank: int, 
                    "l2": f"cold W: {n_copies} rotating copies of W ({n_copies * w_bytes >> 20} MiB > L2 "
                          f"{l2 >> 20} MiB), steps replayed from a CUDA graph of {G}",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "parity_gate": {"rel_err": err, "tol": tol, "compared": gate}},
+                   "parity_gate": {"rel_err": err, "rel_err_after_timed_steps": err_after, "tol": tol,
+                                   "compared": gate},
+                   "steps_are": "independent back-to-back calls (same X, rotating W copies); a call may "
+                                "start before its predecessor finishes and writes Y after it"},
+        "isolated_call": isolated,
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         "gpu_launches": steps * (0 if plan.kernel in (tll.KERNEL_NONE,) else 1),
     }

@@ -78,8 +78,7 @@ typedef enum {
     LIN_KERNEL_FILL = 1,   /* K == 0: Y = act(bias) (or act(0)) */
     LIN_KERNEL_SKINNY = 2, /* M <= 16, BF16: W stream, split-K across a thread-block cluster (no workspace) */
     LIN_KERNEL_FFMA = 3,   /* FP32: register-tiled FFMA, optional split-K */
-    LIN_KERNEL_TC = 4,     /* TF32 / BF16: TMA + tcgen05 + TMEM, fused epilogue */
-    LIN_KERNEL_SKINNY_SK = 5 /* M <= 16, BF16: stream-K W stream over all SMs, workspace reduction */
+    LIN_KERNEL_TC = 4      /* TF32 / BF16: TMA + tcgen05 + TMEM, fused epilogue */
 } lin_kernel;
 
 /* One launch configuration, chosen by the dispatch table or given explicitly.
@@ -123,7 +122,15 @@ LIN_API int lin_destroy(lin_ctx* ctx);
  * X and W must be 16-byte aligned and K * element size a multiple of 16
  * (LIN_ERR_ALIGN otherwise); bias 4-byte aligned; Y aligned to its element.
  * One context must not run two calls at the same time (they share the
- * workspace): use one context per stream. */
+ * workspace): use one context per stream.
+ * Back-to-back calls: with LIN_OPT_EARLY_START on (the default), a call whose
+ * inputs (X, W, bias) overlap none of the previous call's output on the same
+ * stream is launched as a programmatic dependent of that call, reads its
+ * inputs before the previous kernel has finished and writes Y only after it.
+ * For such a call with M <= 16 (BF16) the skinny kernel also drops its K split
+ * (one CTA per 128 rows of W), so that consecutive independent calls stream
+ * their weights concurrently; lin_plan_query returns the plan of an isolated
+ * call. */
 LIN_API int lin_forward(lin_ctx* ctx, int M, int N, int K, const void* X, const void* W,
                 const float* bias, void* Y, int epilogue, int precision, void* stream);
 
@@ -164,6 +171,12 @@ LIN_API int lin_check_device(lin_ctx* ctx, void* stream);
 typedef enum {
     LIN_OPT_EARLY_START = 1
 } lin_option;
+
+/* The plan of the last call launched through this context (host value, no
+ * GPU call): lin_forward may refine the dispatch table's plan for a call that
+ * overlaps its predecessor. LIN_ERR_ARG if ctx or out is NULL; a context with
+ * no call yet reports LIN_KERNEL_NONE. */
+LIN_API int lin_ctx_last_plan(const lin_ctx* ctx, lin_plan* out);
 
 /* Set a context option. LIN_ERR_ARG for an unknown option or value. */
 LIN_API int lin_set_option(lin_ctx* ctx, int option, long long value);

@@ -121,17 +121,6 @@ def test_skinny_needs_no_workspace():
     assert kname(p) == "skinny" and p.splits in (1, 2, 4, 8) and p.workspace_bytes == 0
 
 
-def test_skinny_stream_k_with_workspace():
-    p = tll.plan_make(SM, tll.KERNEL_SKINNY_SK, 0, 0, 16, 4096, 4096, "bf16")
-    assert kname(p) == "skinny_sk" and p.grid_x == SM and 0 < p.workspace_bytes <= 4 << 20
-    for v in range(5):
-        for width in (0, 2 * SM, 100):
-            q = tll.plan_make(SM, tll.KERNEL_SKINNY_SK, v, width, 16, 4096, 4096, "bf16")
-            assert q.grid_x == min(width or SM, 32 * (4096 // q.bk)) and q.splits == q.grid_x
-    tiny = tll.plan_make(SM, tll.KERNEL_SKINNY_SK, 0, 1, 3, 100, 64, "bf16")
-    assert tiny.grid_x == 1
-
-
 def test_plan_make_families():
     for v in range(4):
         for s in (1, 2, 4, 8):

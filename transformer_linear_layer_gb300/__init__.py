@@ -21,13 +21,13 @@ from .build import build
 __all__ = [
     "LinError", "Context", "Plan", "forward", "forward_plan", "plan_query", "plan_make", "build",
     "library", "PREC_FP32", "PREC_TF32", "PREC_BF16", "EPI_NONE", "EPI_GELU_TANH",
-    "KERNEL_NONE", "KERNEL_FILL", "KERNEL_SKINNY", "KERNEL_FFMA", "KERNEL_TC", "KERNEL_SKINNY_SK",
+    "KERNEL_NONE", "KERNEL_FILL", "KERNEL_SKINNY", "KERNEL_FFMA", "KERNEL_TC",
 ]
 
 PREC_FP32, PREC_TF32, PREC_BF16 = 0, 1, 2
 EPI_NONE, EPI_GELU_TANH = 0, 1
-KERNEL_NONE, KERNEL_FILL, KERNEL_SKINNY, KERNEL_FFMA, KERNEL_TC, KERNEL_SKINNY_SK = 0, 1, 2, 3, 4, 5
-KERNEL_NAMES = {0: "none", 1: "fill", 2: "skinny", 3: "ffma", 4: "tc", 5: "skinny_sk"}
+KERNEL_NONE, KERNEL_FILL, KERNEL_SKINNY, KERNEL_FFMA, KERNEL_TC = 0, 1, 2, 3, 4
+KERNEL_NAMES = {0: "none", 1: "fill", 2: "skinny", 3: "ffma", 4: "tc"}
 OPT_EARLY_START = 1
 OK, ERR_ARG, ERR_ALIGN, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
 
@@ -87,6 +87,7 @@ def library() -> ctypes.CDLL:
                 "lin_check_device": ([P, P], I),
                 "lin_ctx_info": ([P, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(Z)], I),
                 "lin_set_option": ([P, I, ctypes.c_longlong], I),
+                "lin_ctx_last_plan": ([P, PP], I),
                 "lin_forward_fp32_static": ([I, I, I, P, P, P, P, I, P], I),
                 "lin_strerror": ([I], ctypes.c_char_p),
                 "lin_abi_version": ([], I),
@@ -165,6 +166,14 @@ class Context:
         rc = library().lin_set_option(self._h, int(option), int(value))
         if rc != OK:
             raise LinError(rc, "lin_set_option")
+
+    def last_plan(self) -> Plan:
+        """The plan of the last call launched through this context."""
+        p = Plan()
+        rc = library().lin_ctx_last_plan(self._h, ctypes.byref(p))
+        if rc != OK:
+            raise LinError(rc, "lin_ctx_last_plan")
+        return p
 
     def plan(self, M, N, K, precision="bf16", epilogue="none") -> Plan:
         return plan_query(self.sm_count, M, N, K, precision, epilogue, self.workspace_bytes)

@@ -24,9 +24,12 @@ struct Problem {
     size_t workspace_bytes;
     int* dev_status;          // device status word (LIN_ERR_DEVICE_TIMEOUT when a wait gave up)
     int sm_count;
-    // The kernel may start (and prefetch W) before the previous kernel on the
-    // stream finishes: W does not overlap that kernel's output.
+    // The kernel may start before the previous kernel on the stream finishes
+    // (programmatic dependent launch). early_start: W and bias do not overlap
+    // that kernel's output, so they may be read before the dependency wait;
+    // early_x: neither does X. Y is written only after the wait.
     bool early_start;
+    bool early_x;
 };
 
 // Workspace layout for split-K: a fixed block of per-tile arrival counters at
@@ -48,10 +51,6 @@ constexpr int kSkinnyVariants = 4;
 constexpr SkinnyCfg kSkinnyCfg[kSkinnyVariants] = {{3, 4}, {6, 1}, {3, 2}, {4, 3}};
 constexpr int kSkinnyThreads = 192;                // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 
-struct SkinnySkCfg { int stages, kbox; };          // stream-K skinny: K per stage = kbox * 64
-constexpr int kSkinnySkVariants = 5;
-constexpr SkinnySkCfg kSkinnySkCfg[kSkinnySkVariants] = {{6, 1}, {12, 1}, {3, 2}, {6, 2}, {3, 4}};
-
 struct FfmaCfg { int bm, bn, bk, tm, tn; };        // 256 threads each
 constexpr int kFfmaVariants = 2;
 constexpr FfmaCfg kFfmaCfg[kFfmaVariants] = {{128, 128, 16, 8, 8}, {64, 64, 16, 4, 4}};
@@ -65,8 +64,6 @@ constexpr int kTcThreads = 320;                    // warp 0 TMA, warp 1 MMA, wa
 // Launchers (return LIN_OK or LIN_ERR_*). They assume the plan was validated.
 int launch_fill(const Problem& p);
 int launch_skinny(const Problem& p, const lin_plan& plan);
-int launch_skinny_sk(const Problem& p, const lin_plan& plan);
-size_t skinny_sk_workspace_bytes(int P, int M, int N, int K, int kbox);
 int launch_ffma(const Problem& p, const lin_plan& plan);
 int launch_tc(const Problem& p, const lin_plan& plan);
 

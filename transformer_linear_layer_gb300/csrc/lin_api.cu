@@ -27,6 +27,7 @@ struct lin_ctx {
     size_t workspace_bytes;
     int* dev_status;
     bool early_start;  // LIN_OPT_EARLY_START
+    lin_plan last_plan;
 };
 
 namespace lin {
@@ -78,33 +79,6 @@ int make_skinny(int sm, int variant, int splits, int M, int N, int K, size_t /*w
     p->grid_z = 1;
     p->threads = kSkinnyThreads;
     p->workspace_bytes = 0;
-    return LIN_OK;
-}
-
-// Stream-K skinny over `width` CTAs (0 = one per SM, which leaves the second
-// shared-memory slot of each SM for the next call's early start).
-int make_skinny_sk(int sm, int variant, int width, int M, int N, int K, size_t ws, lin_plan* p) {
-    if (variant < 0 || variant >= kSkinnySkVariants || M > 16 || M < 1 || N < 1 || K < 1) return LIN_ERR_UNSUPPORTED;
-    if (width < 0 || width > 4 * sm) return LIN_ERR_UNSUPPORTED;
-    if (width == 0) width = sm;
-    const SkinnySkCfg c = kSkinnySkCfg[variant];
-    const int nrb = ceil_div(N, 128);
-    if (nrb > kMaxSplitTiles) return LIN_ERR_UNSUPPORTED;
-    const long long T = (long long)nrb * ceil_div(K, 64 * c.kbox);
-    const int P = (int)(T < (long long)width ? T : (long long)width);
-    const size_t need = skinny_sk_workspace_bytes(P, M, N, K, c.kbox);
-    if (need > ws) return LIN_ERR_WORKSPACE;
-    plan_common(p, LIN_KERNEL_SKINNY_SK, variant);
-    p->bm = 16;
-    p->bn = 128;
-    p->bk = 64 * c.kbox;
-    p->splits = P;
-    p->stages = c.stages;
-    p->grid_x = P;
-    p->grid_y = 1;
-    p->grid_z = 1;
-    p->threads = kSkinnyThreads;
-    p->workspace_bytes = (long long)need;
     return LIN_OK;
 }
 
@@ -246,14 +220,28 @@ std::mutex g_last_mu;
 LastOut g_last[64];
 int g_last_n = 0;
 
-bool early_start_ok(cudaStream_t st, const void* W, size_t wbytes, const void* Y, size_t ybytes) {
-    const uintptr_t wl = reinterpret_cast<uintptr_t>(W), wh = wl + wbytes;
+struct Range {
+    const void* p;
+    size_t bytes;
+};
+
+// Which inputs may be read before the dependency wait: *w_ok for W and bias,
+// *x_ok for X (each false when it overlaps the previous output on `st`).
+// Records Y as this stream's newest output.
+void early_reads_ok(cudaStream_t st, Range w, Range bias, Range x, Range y, bool* w_ok, bool* x_ok, bool* known) {
+    auto hits = [](const LastOut& o, Range r) {
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(r.p), hi = lo + r.bytes;
+        return r.p && r.bytes && lo < o.hi && o.lo < hi;
+    };
     std::lock_guard<std::mutex> lk(g_last_mu);
-    bool ok = true;
+    *w_ok = *x_ok = true;
+    *known = false;
     int slot = -1;
     for (int i = 0; i < g_last_n; ++i)
         if (g_last[i].stream == st) {
-            ok = !(wl < g_last[i].hi && g_last[i].lo < wh);
+            *w_ok = !hits(g_last[i], w) && !hits(g_last[i], bias);
+            *x_ok = !hits(g_last[i], x);
+            *known = true;
             slot = i;
             break;
         }
@@ -262,13 +250,12 @@ bool early_start_ok(cudaStream_t st, const void* W, size_t wbytes, const void* Y
             slot = g_last_n++;
         } else {
             slot = 0;  // table full: forget the oldest entry's stream, stay safe for this one
-            ok = false;
+            *w_ok = *x_ok = false;
         }
     }
     g_last[slot].stream = st;
-    g_last[slot].lo = reinterpret_cast<uintptr_t>(Y);
-    g_last[slot].hi = g_last[slot].lo + ybytes;
-    return ok;
+    g_last[slot].lo = reinterpret_cast<uintptr_t>(y.p);
+    g_last[slot].hi = g_last[slot].lo + y.bytes;
 }
 
 int check_plan_fits(const lin_plan& p, int M, int N, int K, int precision) {
@@ -280,17 +267,6 @@ int check_plan_fits(const lin_plan& p, int M, int N, int K, int precision) {
             if (p.variant < 0 || p.variant >= kSkinnyVariants) return LIN_ERR_UNSUPPORTED;
             if (p.splits != 1 && p.splits != 2 && p.splits != 4 && p.splits != 8) return LIN_ERR_UNSUPPORTED;
             if (p.grid_x != ceil_div(N, 128) || p.grid_y != p.splits) return LIN_ERR_UNSUPPORTED;
-            return LIN_OK;
-        }
-        case LIN_KERNEL_SKINNY_SK: {
-            if (precision != LIN_PREC_BF16 || M > 16 || K == 0) return LIN_ERR_UNSUPPORTED;
-            if (p.variant < 0 || p.variant >= kSkinnySkVariants || p.grid_x < 1 || p.grid_y != 1) return LIN_ERR_UNSUPPORTED;
-            const SkinnySkCfg c = kSkinnySkCfg[p.variant];
-            const int nrb = ceil_div(N, 128);
-            const long long T = (long long)nrb * ceil_div(K, 64 * c.kbox);
-            if (nrb > kMaxSplitTiles || p.grid_x > T || p.bk != 64 * c.kbox) return LIN_ERR_UNSUPPORTED;
-            if ((long long)skinny_sk_workspace_bytes(p.grid_x, M, N, K, c.kbox) != p.workspace_bytes)
-                return LIN_ERR_UNSUPPORTED;
             return LIN_OK;
         }
         case LIN_KERNEL_FFMA: {
@@ -319,8 +295,9 @@ int check_plan_fits(const lin_plan& p, int M, int N, int K, int precision) {
     }
 }
 
-int run(lin_ctx* ctx, const lin_plan& plan, int M, int N, int K, const void* X, const void* W, const float* bias,
-        void* Y, int epilogue, int precision, void* stream) {
+int run(lin_ctx* ctx, const lin_plan& plan_in, int M, int N, int K, const void* X, const void* W, const float* bias,
+        void* Y, int epilogue, int precision, void* stream, bool adaptive) {
+    lin_plan plan = plan_in;
     if (!ctx || M < 0 || N < 0 || K < 0 || !valid_enums(epilogue, precision)) return LIN_ERR_ARG;
     if (M == 0 || N == 0) return plan.kernel == LIN_KERNEL_NONE ? LIN_OK : LIN_ERR_UNSUPPORTED;
     if (!Y || (K > 0 && (!X || !W))) return LIN_ERR_ARG;
@@ -353,11 +330,23 @@ int run(lin_ctx* ctx, const lin_plan& plan, int M, int N, int K, const void* X, 
     p.workspace_bytes = ctx->workspace_bytes;
     p.dev_status = ctx->dev_status;
     p.sm_count = ctx->sm_count;
-    p.early_start = early_start_ok(p.stream, W, (size_t)N * K * ein, Y, ybytes) && ctx->early_start;
+    bool w_ok = false, x_ok = false, known = false;
+    early_reads_ok(p.stream, Range{W, (size_t)N * K * ein}, Range{bias, bias ? (size_t)N * 4 : 0},
+                   Range{X, (size_t)M * K * ein}, Range{Y, ybytes}, &w_ok, &x_ok, &known);
+    p.early_start = ctx->early_start && w_ok;
+    p.early_x = p.early_start && x_ok;
+    // An independent call right after another call on this stream overlaps it:
+    // the skinny stream then needs no K split to fill the SMs (the concurrent
+    // calls do), and skipping the split saves its reduction.
+    if (adaptive && known && p.early_x && plan.kernel == LIN_KERNEL_SKINNY && plan.splits > 1) {
+        lin_plan narrow;
+        if (make_skinny(ctx->sm_count, plan.variant, 1, M, N, K, ctx->workspace_bytes, &narrow) == LIN_OK)
+            plan = narrow;
+    }
+    ctx->last_plan = plan;
     switch (plan.kernel) {
         case LIN_KERNEL_FILL: return launch_fill(p);
         case LIN_KERNEL_SKINNY: return launch_skinny(p, plan);
-        case LIN_KERNEL_SKINNY_SK: return launch_skinny_sk(p, plan);
         case LIN_KERNEL_FFMA: return launch_ffma(p, plan);
         case LIN_KERNEL_TC: return launch_tc(p, plan);
         default: return LIN_ERR_UNSUPPORTED;
@@ -412,6 +401,7 @@ int lin_create(lin_ctx** out, int device, size_t max_workspace_bytes) {
     if (!c) return LIN_ERR_CUDA;
     c->device = device;
     c->early_start = true;
+    std::memset(&c->last_plan, 0, sizeof(c->last_plan));
     c->workspace_bytes = max_workspace_bytes ? max_workspace_bytes : ((size_t)64 << 20);
     if (cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
         cudaMalloc(&c->workspace, c->workspace_bytes) != cudaSuccess ||
@@ -439,6 +429,12 @@ int lin_destroy(lin_ctx* ctx) {
     }
     delete ctx;
     return rc;
+}
+
+int lin_ctx_last_plan(const lin_ctx* ctx, lin_plan* out) {
+    if (!ctx || !out) return LIN_ERR_ARG;
+    *out = ctx->last_plan;
+    return LIN_OK;
 }
 
 int lin_set_option(lin_ctx* ctx, int option, long long value) {
@@ -474,9 +470,6 @@ int lin_plan_make(int sm_count, int kernel, int variant, int splits, int M, int 
         case LIN_KERNEL_SKINNY:
             if (precision != LIN_PREC_BF16) return LIN_ERR_UNSUPPORTED;
             return lin::make_skinny(sm_count, variant, splits, M, N, K, unlimited, out);
-        case LIN_KERNEL_SKINNY_SK:
-            if (precision != LIN_PREC_BF16) return LIN_ERR_UNSUPPORTED;
-            return lin::make_skinny_sk(sm_count, variant, splits, M, N, K, unlimited, out);
         case LIN_KERNEL_FFMA:
             if (precision != LIN_PREC_FP32) return LIN_ERR_UNSUPPORTED;
             return lin::make_ffma(sm_count, variant, splits, M, N, K, unlimited, out);
@@ -496,13 +489,13 @@ int lin_forward(lin_ctx* ctx, int M, int N, int K, const void* X, const void* W,
     lin_plan plan;
     const int rc = lin::plan_default(ctx->sm_count, M, N, K, precision, ctx->workspace_bytes, &plan);
     if (rc != LIN_OK) return rc;
-    return lin::run(ctx, plan, M, N, K, X, W, bias, Y, epilogue, precision, stream);
+    return lin::run(ctx, plan, M, N, K, X, W, bias, Y, epilogue, precision, stream, true);
 }
 
 int lin_forward_plan(lin_ctx* ctx, const lin_plan* plan, int M, int N, int K, const void* X, const void* W,
                      const float* bias, void* Y, int epilogue, int precision, void* stream) {
     if (!plan) return LIN_ERR_ARG;
-    return lin::run(ctx, *plan, M, N, K, X, W, bias, Y, epilogue, precision, stream);
+    return lin::run(ctx, *plan, M, N, K, X, W, bias, Y, epilogue, precision, stream, false);
 }
 
 int lin_check_device(lin_ctx* ctx, void* stream) {

@@ -101,6 +101,7 @@ extern "C" int lin_forward_fp32_static(int M, int N, int K, const float* X, cons
     p.dev_status = nullptr;
     p.sm_count = sm;
     p.early_start = false;
+    p.early_x = false;
     if (plan.kernel == LIN_KERNEL_FILL) return launch_fill(p);
     if (plan.kernel != LIN_KERNEL_FFMA) return LIN_ERR_UNSUPPORTED;
     if (plan.splits > 1) {

@@ -19,17 +19,21 @@
 //   tiles, accumulating in 16 TMEM columns. At M = 16 the FFMA units could
 //   not keep up with HBM (16 FLOP per W byte ~ 108 TFLOP/s at 6.8 TB/s).
 // * Split-K in a thread-block cluster: the CL CTAs of a cluster share one
-//   128-row block of W and take consecutive K ranges. Each writes its 16 x 128
-//   partial sums to its own shared memory; after a cluster barrier, CTA r adds
-//   the CL partials of columns [r*128/CL, (r+1)*128/CL) through distributed
-//   shared memory in fixed rank order 0..CL-1 (bitwise repeatable, the
+//   128-row block of W and take consecutive K ranges. K is always cut into 8
+//   segments with their own TMEM accumulators; a CTA adds its segments by a
+//   balanced pairwise tree, pushes that partial into the inbox of the CTA that
+//   finishes the columns (distributed shared memory), and the finishing CTA
+//   adds the CL partials by the same tree, applies bias and GELU and stores
+//   bf16. The sum is therefore the same balanced tree over the 8 segments for
+//   every cluster size - bitwise identical across split choices and runs (the
 //   fixed-order reduction of "Optimizing a GPT-2-class transformer on a GPU",
-//   Act I), applies bias and GELU and stores bf16. No global workspace.
+//   Act I). No global workspace.
 // * Programmatic dependent launch: the W copies of the first STAGES tiles are
 //   issued before griddepcontrol.wait, so a layer's weight stream starts while
-//   the previous kernel on the stream drains; X, bias and Y are touched only
-//   after the wait. The host drops the early start when W overlaps the output
-//   of the previous call on the stream.
+//   the previous kernel on the stream drains. X is read before the wait too
+//   when it is not the previous call's output (independent layers then stream
+//   concurrently); a chained layer (X = previous Y) reads X after it. Bias and
+//   Y are touched only after the wait. The host checks those overlaps.
 #include "internal.h"
 #include "device_common.cuh"
 #include "tc_common.cuh"
@@ -43,8 +47,10 @@ struct SkinnyArgs {
     uint16_t* Y;
     int* status;
     int kblocks;  // ceil(K / (64 * KBOX)): stages of K per 128-row block
+    int early_x;  // X may be read before the dependency wait (it is not the previous call's output)
 };
 
+constexpr int kSkSegs = 8;    // K segments: the fixed shape of the summation tree
 constexpr int kSkRows = 128;  // W rows (outputs) per cluster
 constexpr int kSkMP = 16;     // batch rows, padded to the MMA N
 constexpr uint32_t kSkWBox = kSkRows * 128;  // one 128-byte-wide box of W
@@ -60,11 +66,65 @@ constexpr size_t skinny_smem_bytes(int stages, int kbox, int cl) {
            (2 * stages + 2) * 8 + 16;
 }
 
+struct Vec16 {
+    float x[kSkMP];
+};
+
+__device__ __forceinline__ Vec16 add16(const Vec16& a, const Vec16& b) {
+    Vec16 r;
+#pragma unroll
+    for (int m = 0; m < kSkMP; ++m) r.x[m] = a.x[m] + b.x[m];
+    return r;
+}
+
+// One segment's sum: its NACC accumulators added pairwise, left to right.
+template <int NACC>
+__device__ __forceinline__ Vec16 segment_sum(uint32_t lane_base, int ls) {
+    Vec16 acc[NACC];
+#pragma unroll
+    for (int c = 0; c < NACC; ++c) {
+        uint32_t r[16];
+        tmem_ld16(lane_base + (uint32_t)((ls * NACC + c) * kSkMP), r);
+#pragma unroll
+        for (int m = 0; m < kSkMP; ++m) acc[c].x[m] = __uint_as_float(r[m]);
+    }
+    if constexpr (NACC == 1) return acc[0];
+    else if constexpr (NACC == 2) return add16(acc[0], acc[1]);
+    else if constexpr (NACC == 3) return add16(add16(acc[0], acc[1]), acc[2]);
+    else return add16(add16(acc[0], acc[1]), add16(acc[2], acc[3]));
+}
+
+// Balanced pairwise tree over N consecutive local segments starting at `first`.
+template <int N, int NACC, class NonEmpty>
+__device__ __forceinline__ Vec16 tree_of_segments(uint32_t lane_base, int first, NonEmpty nonempty) {
+    if constexpr (N == 1) {
+        // tcgen05.ld is warp-collective: the condition is the same for all lanes.
+        if (nonempty(first)) return segment_sum<NACC>(lane_base, first);
+        return Vec16{};
+    } else {
+        const Vec16 lo = tree_of_segments<N / 2, NACC>(lane_base, first, nonempty);
+        const Vec16 hi = tree_of_segments<N / 2, NACC>(lane_base, first + N / 2, nonempty);
+        return add16(lo, hi);
+    }
+}
+
+// Balanced pairwise tree over the partial sums of N consecutive ranks (stride apart).
+template <int N>
+__device__ __forceinline__ float tree_of_ranks(const float* p, int stride, int first) {
+    if constexpr (N == 1)
+        return p[first * stride];
+    else
+        return tree_of_ranks<N / 2>(p, stride, first) + tree_of_ranks<N / 2>(p, stride, first + N / 2);
+}
+
 template <int STAGES, int KBOX, int CL, bool GELU>
 __global__ void __launch_bounds__(kSkinnyThreads, 1)
 skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const SkinnyArgs a) {
-    constexpr int NACC = KBOX < 4 ? KBOX : 4;          // independent accumulators (MMA chains)
-    constexpr uint32_t TMEM_COLS = NACC * kSkMP <= 32 ? 32 : 64;
+    constexpr int NACC = KBOX < 4 ? KBOX : 4;          // independent accumulators (MMA chains) per segment
+    constexpr int LSEG = kSkSegs / CL;                 // K segments of this CTA
+    constexpr int ACC_COLS = LSEG * NACC * kSkMP;
+    constexpr uint32_t TMEM_COLS = ACC_COLS <= 32 ? 32 : ACC_COLS <= 64 ? 64 : ACC_COLS <= 128 ? 128 : ACC_COLS <= 256 ? 256 : 512;
+    static_assert(kSkSegs % CL == 0 && ACC_COLS <= 512, "segments per CTA");
     constexpr uint32_t IDESC = make_idesc(1u, kSkRows, kSkMP);
     constexpr int COLS = kSkRows / CL;  // output columns this CTA finishes
     constexpr uint32_t WB = KBOX * kSkWBox, XB = KBOX * kSkXBox;
@@ -81,8 +141,12 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kSkRows;
     const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
-    const int kb0 = (int)((long long)rank * a.kblocks / CL);
-    const int kb1 = (int)((long long)(rank + 1) * a.kblocks / CL);
+    // Segment s covers K stages [s*kblocks/8, (s+1)*kblocks/8); this CTA owns
+    // segments [rank*LSEG, rank*LSEG + LSEG).
+    auto seg_begin = [&](int sg) { return (int)((long long)sg * a.kblocks / kSkSegs); };
+    const int seg0 = (int)rank * LSEG;
+    const int kb0 = seg_begin(seg0);
+    const int kb1 = seg_begin(seg0 + LSEG);
     const int nkb = kb1 - kb0;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
     const uint32_t accum_bar = smem_u32(bars + 2 * STAGES), inbox_bar = smem_u32(bars + 2 * STAGES + 1);
@@ -135,9 +199,12 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
             for (int i = 0; i < pre; ++i) {
                 mbar_expect_tx(full0 + 8 * i, WB + XB);
                 load_w(i);
+                if (a.early_x) load_x(i);
             }
-            pdl_wait();
-            for (int i = 0; i < pre; ++i) load_x(i);
+            if (!a.early_x) {
+                pdl_wait();
+                for (int i = 0; i < pre; ++i) load_x(i);
+            }
             int issued = pre;
             for (int i = pre; i < nkb; ++i) {
                 const int s = i % STAGES;
@@ -160,9 +227,12 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
         if (lane == 0 && nkb > 0) {
             // ---- MMA issuer: box b of every stage accumulates into accumulator b % NACC,
             // so up to NACC MMA chains run side by side ----
+            int ls = 0;  // local segment of the current stage
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % STAGES;
                 const uint32_t ph = (i / STAGES) & 1;
+                while (kb0 + i >= seg_begin(seg0 + ls + 1)) ++ls;
+                const bool seg_first = (kb0 + i == seg_begin(seg0 + ls));
                 if (*(volatile int*)s_abort || !mbar_wait(full0 + 8 * s, ph)) {
                     give_up();
                     break;
@@ -172,8 +242,8 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
                 for (int b = 0; b < KBOX; ++b) {
                     const uint64_t ad = sw128_kmajor_desc(smem_u32(sW + s * WB + b * kSkWBox));
                     const uint64_t bd = sw128_kmajor_desc(smem_u32(sX + s * XB + b * kSkXBox));
-                    const uint32_t d = tmem_base + (uint32_t)((b % NACC) * kSkMP);
-                    const bool fresh = (i == 0) && (b < NACC);
+                    const uint32_t d = tmem_base + (uint32_t)((ls * NACC + b % NACC) * kSkMP);
+                    const bool fresh = seg_first && (b < NACC);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         tc_mma<true>(d, ad + 2u * kk, bd + 2u * kk, IDESC, (fresh && kk == 0) ? 0u : 1u);
@@ -188,21 +258,17 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
         pdl_wait();
         const int q = warp & 3;
         const int row = q * 32 + lane;
-        float v[kSkMP];
-#pragma unroll
-        for (int m = 0; m < kSkMP; ++m) v[m] = 0.f;
+        Vec16 v = {};
         if (nkb > 0) {
             const bool mine = mbar_wait(accum_bar, 0);
             if (!mine) give_up();
             tc_fence_after();
             if (__all_sync(0xffffffffu, mine && *(volatile int*)s_abort == 0)) {
-#pragma unroll
-                for (int c = 0; c < NACC; ++c) {
-                    uint32_t r[16];
-                    tmem_ld16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + (uint32_t)(c * kSkMP), r);
-#pragma unroll
-                    for (int m = 0; m < kSkMP; ++m) v[m] += __uint_as_float(r[m]);
-                }
+                // Empty segments (fewer K stages than segments) hold no MMA result: zero.
+                const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+                v = tree_of_segments<LSEG, NACC>(lane_base, 0, [&](int ls) {
+                    return seg_begin(seg0 + ls) < seg_begin(seg0 + ls + 1);
+                });
             }
         }
         const int M = a.M, N = a.N;
@@ -212,7 +278,7 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
                 const float b = a.bias ? __ldg(a.bias + n) : 0.f;
 #pragma unroll
                 for (int m = 0; m < kSkMP; ++m)
-                    if (m < M) a.Y[(size_t)m * N + n] = f32_to_bf16_bits(epilogue<GELU>(v[m], b));
+                    if (m < M) a.Y[(size_t)m * N + n] = f32_to_bf16_bits(epilogue<GELU>(v.x[m], b));
             }
         } else {
             // Push this row's partial sums into the inbox of the CTA that finishes it,
@@ -222,7 +288,7 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
             const int col = row % COLS;
             const uint32_t dst = dsmem_map(smem_u32(inbox + ((int)rank * kSkMP) * COLS + col), owner);
 #pragma unroll
-            for (int m = 0; m < kSkMP; ++m) dsmem_st_f32(dst + (uint32_t)(m * COLS * 4), v[m]);
+            for (int m = 0; m < kSkMP; ++m) dsmem_st_f32(dst + (uint32_t)(m * COLS * 4), v.x[m]);
             mbar_arrive_remote(dsmem_map(inbox_bar, owner));
             // Finish this CTA's columns: the CL partial sums added in rank order.
             const int t = threadIdx.x - 64;
@@ -235,9 +301,7 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
                 const int m = idx / COLS, c = idx % COLS;
                 const int n = n0 + (int)rank * COLS + c;
                 if (ok && m < M && n < N) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int r = 0; r < CL; ++r) acc += inbox[(r * kSkMP + m) * COLS + c];
+                    const float acc = tree_of_ranks<CL>(inbox + m * COLS + c, kSkMP * COLS, 0);
                     const float b = a.bias ? __ldg(a.bias + n) : 0.f;
                     a.Y[(size_t)m * N + n] = f32_to_bf16_bits(epilogue<GELU>(acc, b));
                 }
@@ -324,6 +388,7 @@ int launch_skinny(const Problem& p, const lin_plan& plan) {
     a.Y = static_cast<uint16_t*>(p.Y);
     a.status = p.dev_status;
     a.kblocks = (p.K + 64 * kSkinnyCfg[plan.variant].kbox - 1) / (64 * kSkinnyCfg[plan.variant].kbox);
+    a.early_x = p.early_x ? 1 : 0;
     const bool gelu = p.epilogue == LIN_EPI_GELU_TANH;
 #define LIN_SKINNY_CASE(V)                                                                                 \
     case V:                                                                                                \
