@@ -245,12 +245,13 @@ def test_workspace_limit():
     small.close()
 
 
-def test_back_to_back_calls_chain_through_outputs(ctx):
+@pytest.mark.parametrize("M", [16, 256])
+def test_back_to_back_calls_chain_through_outputs(ctx, M):
     """Layer i+1 reads layer i's output (X = previous Y) and, in a second chain,
     its weight is the previous output: both must match running the layers one
     at a time (the early start must wait for X and must not prefetch a W that
-    the previous call writes)."""
-    M, N = 16, 512
+    the previous call writes). M = 16: skinny kernel; M = 256: tcgen05 kernel."""
+    N = 512
     X0, W, b = si.make_inputs(si.Layer("chain", M, N, N, BF16, bias=True))
     x0, w, bias = device_inputs(X0, W, b, BF16)
     outs = [x0]
@@ -273,6 +274,16 @@ def test_back_to_back_calls_chain_through_outputs(ctx):
     y2_ref = tll.forward(x0, big.clone(), None, precision="bf16")
     torch.cuda.synchronize()
     assert torch.equal(y2, y2_ref) and y1.shape == (16, N)
+    # and the bias written by the previous call
+    bsrc = torch.zeros((2, N), device="cuda", dtype=torch.float32)
+    xf = torch.from_numpy(si.normal(9, 1, (2, 64))).cuda()
+    wf = torch.from_numpy(si.normal(9, 2, (N, 64), 0.0, 0.1)).cuda()
+    tll.forward(xf, wf, None, precision="fp32", out=bsrc)             # writes the bias
+    y3 = tll.forward(x0, w, bsrc[1], precision="bf16")
+    torch.cuda.synchronize()
+    y3_ref = tll.forward(x0, w, bsrc[1].clone(), precision="bf16")
+    torch.cuda.synchronize()
+    assert torch.equal(y3, y3_ref)
 
 
 @pytest.mark.parametrize("K", [4096, 4104, 384, 200])

@@ -24,6 +24,10 @@
 //   exist": the epilogue already holds the value in a register).
 // * Tails: the copy engine fills rows and K beyond the tensor with zeros;
 //   stores are predicated on m < M and n < N.
+// * Programmatic dependent launch: CTAs may start before the previous kernel on
+//   the stream has finished (filling SMs its last round leaves idle). Operands
+//   are read before griddepcontrol.wait only when neither is that kernel's
+//   output; bias and Y always after it.
 // * Every wait is bounded (iterations and wall clock); a wait that gives up
 //   writes LIN_ERR_DEVICE_TIMEOUT to the status word, the CTA skips its
 //   stores, drains its own copies and MMAs, frees TMEM and exits.
@@ -41,6 +45,7 @@ struct TcArgs {
     int* status;
     int y_aligned16;     // Y's base is 16-byte aligned (vector stores allowed)
     int bias_aligned16;  // bias is 16-byte aligned (vector loads allowed)
+    int early_inputs;    // X and W may be read before the dependency wait (not the previous call's output)
 };
 
 // Epilogue staging: each epilogue warp owns a 32 x 32 output tile in shared
@@ -138,6 +143,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (threadIdx.x == 0) pdl_launch_dependents();
 
     auto give_up = [&]() {
         atomicExch(s_abort, 1);
@@ -147,6 +153,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     if (warp == 0) {
         if (lane == 0) {
             // ---- TMA producer: the K stages of this CTA's tiles, in order ----
+            if (!a.early_inputs) pdl_wait();
             uint32_t it = 0, issued = 0;
             bool ok = true;
             for (int tile = first_item; tile < ntiles && ok; tile += item_step) {
@@ -215,6 +222,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         }
     } else {
         // ---- epilogue: warp w reads TMEM lanes 32*(w%4).., columns half (w-2)/4 ----
+        pdl_wait();  // Y (and bias) only after the previous kernel on the stream has finished
         const int q = warp & 3;
         const int c_begin = ((warp - 2) >> 2) * HALF;
         const int N = a.N;
@@ -341,7 +349,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 // ---------------------------------------------------------------- host side
 
 template <bool BF16, int BN, bool GELU, bool PAIR>
-int launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, int grid, cudaStream_t st) {
+int launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, int grid, bool early,
+               cudaStream_t st) {
     constexpr size_t smem = tc_smem_bytes<BF16, BN>();
     static_assert(tc_smem_bytes<BF16, BN>() <= 227 * 1024, "shared memory");
     auto kern = tc_kernel<BF16, BN, GELU, PAIR>;
@@ -359,27 +368,36 @@ int launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, in
     cfg.blockDim = dim3(kTcThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 2;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = PAIR ? 1 : 0;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    if (PAIR) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = 2;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (early) {
+        attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
     if (cudaLaunchKernelEx(&cfg, kern, ta, tb, a) != cudaSuccess) return LIN_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? LIN_OK : LIN_ERR_CUDA;
 }
 
 template <bool BF16, bool GELU>
 int launch_variant(int variant, const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, int grid,
-                   cudaStream_t st) {
+                   bool early, cudaStream_t st) {
     switch (variant) {
-        case 0: return launch_cfg<BF16, kTcCfg[0].bn, GELU, false>(ta, tb, a, grid, st);
-        case 1: return launch_cfg<BF16, kTcCfg[1].bn, GELU, false>(ta, tb, a, grid, st);
-        case 2: return launch_cfg<BF16, kTcCfg[2].bn, GELU, false>(ta, tb, a, grid, st);
-        case 3: return launch_cfg<BF16, kTcCfg[3].bn, GELU, true>(ta, tb, a, grid, st);
-        case 4: return launch_cfg<BF16, kTcCfg[4].bn, GELU, true>(ta, tb, a, grid, st);
-        case 5: return launch_cfg<BF16, kTcCfg[5].bn, GELU, true>(ta, tb, a, grid, st);
+        case 0: return launch_cfg<BF16, kTcCfg[0].bn, GELU, false>(ta, tb, a, grid, early, st);
+        case 1: return launch_cfg<BF16, kTcCfg[1].bn, GELU, false>(ta, tb, a, grid, early, st);
+        case 2: return launch_cfg<BF16, kTcCfg[2].bn, GELU, false>(ta, tb, a, grid, early, st);
+        case 3: return launch_cfg<BF16, kTcCfg[3].bn, GELU, true>(ta, tb, a, grid, early, st);
+        case 4: return launch_cfg<BF16, kTcCfg[4].bn, GELU, true>(ta, tb, a, grid, early, st);
+        case 5: return launch_cfg<BF16, kTcCfg[5].bn, GELU, true>(ta, tb, a, grid, early, st);
         default: return LIN_ERR_UNSUPPORTED;
     }
 }
@@ -434,13 +452,24 @@ int launch_tc(const Problem& p, const lin_plan& plan) {
     a.status = p.dev_status;
     a.y_aligned16 = (reinterpret_cast<uintptr_t>(p.Y) % 16) == 0;
     a.bias_aligned16 = (reinterpret_cast<uintptr_t>(p.bias) % 16) == 0;
+    a.early_inputs = (p.early_start && p.early_x) ? 1 : 0;
     const int grid = plan.grid_x;
     const bool gelu = p.epilogue == LIN_EPI_GELU_TANH;
+    // Programmatic dependent launch when the context allows an early start and
+    // this grid's last round of tiles leaves at least 30% of its CTAs idle (the
+    // next call can use them); with a nearly full last round the early CTAs only
+    // compete for bandwidth (measured on the M = 8192 shapes). The kernel waits
+    // before its first load unless the inputs are independent.
+    const long long mt = (p.M + 127) / 128, nt = (p.N + plan.bn - 1) / plan.bn;
+    const long long items = (kTcCfg[plan.variant].pair ? (mt + 1) / 2 : mt) * nt;
+    const long long slots = kTcCfg[plan.variant].pair ? grid / 2 : grid;
+    const long long last = items - ((items + slots - 1) / slots - 1) * slots;
+    const bool early = p.early_start && (double)last < 0.7 * (double)slots;
     if (bf16)
-        return gelu ? launch_variant<true, true>(plan.variant, ta, tb, a, grid, p.stream)
-                    : launch_variant<true, false>(plan.variant, ta, tb, a, grid, p.stream);
-    return gelu ? launch_variant<false, true>(plan.variant, ta, tb, a, grid, p.stream)
-                : launch_variant<false, false>(plan.variant, ta, tb, a, grid, p.stream);
+        return gelu ? launch_variant<true, true>(plan.variant, ta, tb, a, grid, early, p.stream)
+                    : launch_variant<true, false>(plan.variant, ta, tb, a, grid, early, p.stream);
+    return gelu ? launch_variant<false, true>(plan.variant, ta, tb, a, grid, early, p.stream)
+                : launch_variant<false, false>(plan.variant, ta, tb, a, grid, early, p.stream);
 }
 
 }  // namespace lin
