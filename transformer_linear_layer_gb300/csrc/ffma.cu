@@ -5,25 +5,27 @@
 // rebuilt for sm_103a:
 //
 // * Block tile BM x BN, K step BK; each of 256 threads owns a TM x TN register
-//   tile, so per k it reads TM + TN values from shared memory and issues
-//   TM * TN FMAs ("Kernels 3-5: reuse, at three levels").
-// * Both operands are K-contiguous in global memory (X is M x K, W is N x K),
-//   read with 128-bit loads and stored transposed (k-major) in shared memory,
-//   so the per-k reads of the register tile are 128-bit shared loads of
-//   contiguous m (or n) values ("What the kernels were short of": the
-//   transposed, k-major A tile with 128-bit shared reads). A thread's 8 rows
-//   are two groups of 4 half a tile apart, so a quarter-warp's 128-bit reads
-//   cover 128 contiguous bytes (conflict-free).
-// * Double buffering: the next K slice is fetched into registers while the
-//   current one is multiplied, and written to the other shared buffer after,
-//   one barrier per K step ("Kernel 8: the loop was shaped wrong").
+//   tile ("Kernels 3-5: reuse, at three levels"). A thread's rows are
+//   ty, ty + BM/TM, ... and its columns tx, tx + BN/TN, ...: the B reads of a
+//   warp fall in distinct banks, the A reads are broadcasts, and the output
+//   stores of a warp are consecutive columns.
+// * Shared-memory tiles keep the operands' K-contiguous layout (X is M x K, W
+//   is N x K), rows padded to an odd number of 16-byte chunks. A thread reads
+//   a float4 of four consecutive k for each of its rows and columns (rows in
+//   groups of four) and issues 16 FMAs per 128-bit read of B; each output still
+//   accumulates in ascending k.
+// * The K slices stream through a STAGES-deep ring filled with cp.async (16-byte
+//   copies that bypass registers, zero-filled past the tensor's edge), so the
+//   loads of later slices overlap the arithmetic of the current one - the
+//   double buffering of "Kernel 8: the loop was shaped wrong", deeper.
 // * Fused epilogue: bias, optional tanh-GELU with the accurate tanhf, fp32
 //   store ("The bias add did not need to exist"; "The residual and GELU go the
 //   same way", with the feature set as a template parameter).
-// * Optional split-K for outputs too small to fill 152 SMs: each CTA sums one
-//   K range into the workspace, the last CTA of a tile adds the ranges in order
-//   ("One kernel was never going to be enough": split-K when the output is
-//   small and K is long).
+// * Optional split-K for outputs too small to fill the SMs: each CTA sums one
+//   K range into the workspace and the last CTA of a tile adds the ranges in
+//   order 0..S-1 ("One kernel was never going to be enough": split-K when the
+//   output is small and K is long; "Optimizing a GPT-2-class transformer on a
+//   GPU", Act I: fixed-order reduction).
 #include "internal.h"
 #include "device_common.cuh"
 
@@ -39,30 +41,107 @@ struct FfmaArgs {
     float* ws;
     unsigned* counters;
     int splits;
-    int nkb;          // ceil(K / BK)
-    int y_aligned16;  // Y's base is 16-byte aligned (vector stores allowed)
+    int nkb;  // ceil(K / BK)
 };
 
-template <int BM, int BN, int BK, int TM, int TN, bool GELU>
-__global__ void __launch_bounds__(256, 2)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+    // src-size 0 fills the 16 bytes with zeros (rows or K past the tensor).
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int BM, int BN, int BK, int STAGES>
+constexpr size_t ffma_smem_bytes() {
+    return (size_t)STAGES * (BM + BN) * (BK + 4) * sizeof(float);
+}
+
+// Split-K: this CTA's partial tile to the workspace; the last CTA of the tile
+// adds the S partials in split order. One gpu-scope fence per CTA (cumulative
+// over the barrier) publishes the partials before the arrival count.
+template <int TM, int TN, bool GELU, class RowOf, class ColOf>
+__device__ __forceinline__ void splitk_epilogue(const FfmaArgs& a, const float (&acc)[TM][TN], RowOf row_of,
+                                                ColOf col_of, int tid) {
+    __shared__ unsigned s_last;
+    const int split = blockIdx.z;
+    float* part = a.ws + (size_t)split * a.M * a.N;
+#pragma unroll
+    for (int r = 0; r < TM; ++r) {
+        const int m = row_of(r);
+        if (m >= a.M) continue;
+#pragma unroll
+        for (int c = 0; c < TN; ++c) {
+            const int n = col_of(c);
+            if (n < a.N) __stcg(part + (size_t)m * a.N + n, acc[r][c]);
+        }
+    }
+    __syncthreads();
+    const int tile_id = blockIdx.y * gridDim.x + blockIdx.x;
+    if (tid == 0) {
+        __threadfence();
+        const unsigned prev = atomicAdd(&a.counters[tile_id], 1u);
+        const unsigned last = prev == (unsigned)(a.splits - 1);
+        if (last) {
+            a.counters[tile_id] = 0u;  // re-arm for the next launch
+            __threadfence();
+        }
+        s_last = last;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    // Row by row: the TN values of each split are independent loads (four splits
+    // in flight), added in split order.
+    float bcol[TN];
+#pragma unroll
+    for (int c = 0; c < TN; ++c) {
+        const int n = col_of(c);
+        bcol[c] = (a.bias && n < a.N) ? __ldg(a.bias + n) : 0.f;
+    }
+#pragma unroll 1
+    for (int r = 0; r < TM; ++r) {
+        const int m = row_of(r);
+        if (m >= a.M) continue;
+        float sum[TN];
+#pragma unroll
+        for (int c = 0; c < TN; ++c) sum[c] = 0.f;
+#pragma unroll 4
+        for (int sp = 0; sp < a.splits; ++sp) {
+            const float* src = a.ws + ((size_t)sp * a.M + m) * a.N;
+            float t[TN];
+#pragma unroll
+            for (int c = 0; c < TN; ++c) {
+                const int n = col_of(c);
+                t[c] = n < a.N ? __ldcg(src + n) : 0.f;
+            }
+#pragma unroll
+            for (int c = 0; c < TN; ++c) sum[c] += t[c];
+        }
+#pragma unroll
+        for (int c = 0; c < TN; ++c) {
+            const int n = col_of(c);
+            if (n < a.N) a.Y[(size_t)m * a.N + n] = epilogue<GELU>(sum[c], bcol[c]);
+        }
+    }
+}
+
+template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool GELU, bool SPLIT>
+__global__ void __launch_bounds__(256, (BM * BN >= 128 * 128 ? 1 : 2))
 ffma_kernel(const FfmaArgs a) {
     constexpr int NT = 256;
-    constexpr int TX = BN / TN;  // threads along n
-    static_assert((BM / TM) * (BN / TN) == NT, "256 threads");
-    static_assert(TM % 4 == 0 && TN % 4 == 0, "128-bit register tiles");
-    constexpr int PAD = 4;
-    constexpr int A_LD = BM + PAD, B_LD = BN + PAD;
-    constexpr int A_VEC = BM * BK / 4 / NT;  // float4 loads per thread per K step
-    constexpr int B_VEC = BN * BK / 4 / NT;
-    static_assert(A_VEC >= 1 && B_VEC >= 1, "tile too small for 256 threads");
-    constexpr int KQ = BK / 4;  // float4 per row of a K slice
-    // Register-tile placement: TM rows as TM/4 groups of 4, groups BM/(TM/4) apart.
-    constexpr int MG = TM / 4, NG = TN / 4;
-    constexpr int M_STRIDE = BM / MG, N_STRIDE = BN / NG;
+    constexpr int TX = BN / TN, TY = BM / TM;  // threads along n and along m
+    static_assert(TX * TY == NT, "256 threads");
+    constexpr int LD = BK + 4;  // row stride in floats: BK/4 + 1 chunks of 16 bytes (odd)
+    static_assert((LD / 4) % 2 == 1, "odd number of 16-byte chunks per row");
+    constexpr int CPR = BK / 4;  // 16-byte chunks per row of a K slice
+    constexpr int A_CHUNKS = BM * CPR / NT, B_CHUNKS = BN * CPR / NT;
+    static_assert(A_CHUNKS >= 1 && B_CHUNKS >= 1 && (BM * CPR) % NT == 0 && (BN * CPR) % NT == 0, "chunks");
+    constexpr int STAGE_FLOATS = (BM + BN) * LD;
 
-    __shared__ __align__(16) float As[2][BK][A_LD];
-    __shared__ __align__(16) float Bs[2][BK][B_LD];
-    __shared__ unsigned s_last;
+    extern __shared__ __align__(16) float smem[];
 
     const int tid = threadIdx.x;
     const int tx = tid % TX, ty = tid / TX;
@@ -70,6 +149,7 @@ ffma_kernel(const FfmaArgs a) {
     const int split = blockIdx.z;
     const int kb_begin = (int)((long long)split * a.nkb / a.splits);
     const int kb_end = (int)((long long)(split + 1) * a.nkb / a.splits);
+    const int nk = kb_end - kb_begin;
 
     float acc[TM][TN];
 #pragma unroll
@@ -77,162 +157,115 @@ ffma_kernel(const FfmaArgs a) {
 #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
-    float4 ra[A_VEC], rb[B_VEC];
-    auto fetch = [&](int kb) {
+    const uint32_t smem_base = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    // Copy K slice `kb` into ring stage `st`. Thread `tid` always copies chunk
+    // column tid % CPR of rows tid / CPR + v * RSTEP, so one base pointer per
+    // operand and a row stride serve every chunk. K is a multiple of 4, so a
+    // chunk is wholly inside or outside the tensor.
+    constexpr int RSTEP = NT / CPR;
+    static_assert(NT % CPR == 0, "whole rows per pass");
+    const int lr = tid / CPR, lc = tid % CPR;
+    const float* xbase = a.X + (size_t)(m0 + lr) * a.K + 4 * lc;
+    const float* wbase = a.W + (size_t)(n0 + lr) * a.K + 4 * lc;
+    const size_t rstride = (size_t)RSTEP * a.K;
+    auto load_slice = [&](int kb, int st) {
         const int k0 = kb * BK;
+        const bool kok = k0 + 4 * lc < a.K;
+        const uint32_t sa = smem_base + (uint32_t)(st * STAGE_FLOATS + lr * LD + 4 * lc) * 4u;
+        const uint32_t sb = sa + (uint32_t)(BM * LD) * 4u;
 #pragma unroll
-        for (int v = 0; v < A_VEC; ++v) {
-            const int idx = tid + v * NT, r = idx / KQ, q = idx % KQ;
-            const int m = m0 + r, k = k0 + 4 * q;
-            ra[v] = (m < a.M && k < a.K) ? __ldg(reinterpret_cast<const float4*>(a.X + (size_t)m * a.K + k))
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int v = 0; v < A_CHUNKS; ++v) {
+            const bool ok = kok && m0 + lr + v * RSTEP < a.M;
+            cp_async16(sa + (uint32_t)(v * RSTEP * LD) * 4u, ok ? xbase + v * rstride + k0 : a.X, ok);
         }
 #pragma unroll
-        for (int v = 0; v < B_VEC; ++v) {
-            const int idx = tid + v * NT, r = idx / KQ, q = idx % KQ;
-            const int n = n0 + r, k = k0 + 4 * q;
-            rb[v] = (n < a.N && k < a.K) ? __ldg(reinterpret_cast<const float4*>(a.W + (size_t)n * a.K + k))
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    };
-    auto stash = [&](int buf) {
-#pragma unroll
-        for (int v = 0; v < A_VEC; ++v) {
-            const int idx = tid + v * NT, r = idx / KQ, q = idx % KQ;
-            As[buf][4 * q + 0][r] = ra[v].x;
-            As[buf][4 * q + 1][r] = ra[v].y;
-            As[buf][4 * q + 2][r] = ra[v].z;
-            As[buf][4 * q + 3][r] = ra[v].w;
-        }
-#pragma unroll
-        for (int v = 0; v < B_VEC; ++v) {
-            const int idx = tid + v * NT, r = idx / KQ, q = idx % KQ;
-            Bs[buf][4 * q + 0][r] = rb[v].x;
-            Bs[buf][4 * q + 1][r] = rb[v].y;
-            Bs[buf][4 * q + 2][r] = rb[v].z;
-            Bs[buf][4 * q + 3][r] = rb[v].w;
+        for (int v = 0; v < B_CHUNKS; ++v) {
+            const bool ok = kok && n0 + lr + v * RSTEP < a.N;
+            cp_async16(sb + (uint32_t)(v * RSTEP * LD) * 4u, ok ? wbase + v * rstride + k0 : a.W, ok);
         }
     };
 
-    if (kb_begin < kb_end) {
-        fetch(kb_begin);
-        stash(0);
-        __syncthreads();
-        int buf = 0;
-        for (int kb = kb_begin; kb < kb_end; ++kb) {
-            if (kb + 1 < kb_end) fetch(kb + 1);
+    // Prologue: STAGES-1 slices in flight (empty groups keep the counting uniform).
 #pragma unroll
-            for (int kk = 0; kk < BK; ++kk) {
-                float av[TM], bv[TN];
-#pragma unroll
-                for (int gq = 0; gq < MG; ++gq) {
-                    const float4 v = *reinterpret_cast<const float4*>(&As[buf][kk][gq * M_STRIDE + ty * 4]);
-                    av[4 * gq + 0] = v.x; av[4 * gq + 1] = v.y; av[4 * gq + 2] = v.z; av[4 * gq + 3] = v.w;
-                }
-#pragma unroll
-                for (int gq = 0; gq < NG; ++gq) {
-                    const float4 v = *reinterpret_cast<const float4*>(&Bs[buf][kk][gq * N_STRIDE + tx * 4]);
-                    bv[4 * gq + 0] = v.x; bv[4 * gq + 1] = v.y; bv[4 * gq + 2] = v.z; bv[4 * gq + 3] = v.w;
-                }
-#pragma unroll
-                for (int i = 0; i < TM; ++i)
-#pragma unroll
-                    for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-            }
-            if (kb + 1 < kb_end) {
-                stash(buf ^ 1);
-                __syncthreads();
-                buf ^= 1;
-            }
-        }
+    for (int s = 0; s < STAGES - 1; ++s) {
+        if (s < nk) load_slice(kb_begin + s, s);
+        cp_async_commit();
     }
-
-    // Output coordinates of acc[i][j].
-    auto row_of = [&](int i) { return m0 + (i / 4) * M_STRIDE + ty * 4 + (i % 4); };
-    auto col_of = [&](int j) { return n0 + (j / 4) * N_STRIDE + tx * 4 + (j % 4); };
-    const bool vec_ok = (a.N % 4) == 0 && a.y_aligned16;
-
-    auto store_final = [&](int i, int jg, const float (&v)[4]) {
-        const int m = row_of(i);
-        const int n = col_of(jg * 4);
-        if (m >= a.M) return;
-        float o[4];
+    for (int i = 0; i < nk; ++i) {
+        cp_async_wait<STAGES - 2>();
+        __syncthreads();  // slice i landed for every thread; slice i-1's stage is free
+        if (i + STAGES - 1 < nk) load_slice(kb_begin + i + STAGES - 1, (i + STAGES - 1) % STAGES);
+        cp_async_commit();
+        const float* As = smem + (i % STAGES) * STAGE_FLOATS;
+        const float* Bs = As + BM * LD;
+        // Rows in groups of RG (A operands held in registers), B reloaded per group:
+        // keeps a TM = 8 tile within 128 registers.
+        constexpr int RG = TM < 4 ? TM : 4;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float b = (a.bias && n + e < a.N) ? a.bias[n + e] : 0.f;
-            o[e] = epilogue<GELU>(v[e], b);
-        }
-        float* dst = a.Y + (size_t)m * a.N + n;
-        if (vec_ok && n + 3 < a.N) {
-            *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
-        } else {
+        for (int kq = 0; kq < BK / 4; ++kq) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (n + e < a.N) dst[e] = o[e];
-        }
-    };
-
-    if (a.splits == 1) {
+            for (int r0 = 0; r0 < TM; r0 += RG) {
+                float4 av[RG];
 #pragma unroll
-        for (int i = 0; i < TM; ++i)
+                for (int r = 0; r < RG; ++r)
+                    av[r] = *reinterpret_cast<const float4*>(As + (ty + (r0 + r) * TY) * LD + 4 * kq);
 #pragma unroll
-            for (int jg = 0; jg < NG; ++jg) {
-                const float v[4] = {acc[i][4 * jg], acc[i][4 * jg + 1], acc[i][4 * jg + 2], acc[i][4 * jg + 3]};
-                store_final(i, jg, v);
-            }
-        return;
-    }
-
-    // Split-K: partial tile to the workspace, last CTA of the tile reduces.
-    float* part = a.ws + (size_t)split * a.M * a.N;
+                for (int c = 0; c < TN; ++c) {
+                    const float4 bv = *reinterpret_cast<const float4*>(Bs + (tx + c * TX) * LD + 4 * kq);
 #pragma unroll
-    for (int i = 0; i < TM; ++i) {
-        const int m = row_of(i);
-        if (m >= a.M) continue;
-#pragma unroll
-        for (int j = 0; j < TN; ++j) {
-            const int n = col_of(j);
-            if (n < a.N) __stcg(part + (size_t)m * a.N + n, acc[i][j]);
-        }
-    }
-    __threadfence();
-    __syncthreads();
-    const int tile_id = blockIdx.y * gridDim.x + blockIdx.x;
-    if (tid == 0) {
-        const unsigned prev = atomicAdd(&a.counters[tile_id], 1u);
-        s_last = (prev == (unsigned)(a.splits - 1));
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-#pragma unroll
-    for (int i = 0; i < TM; ++i) {
-        const int m = row_of(i);
-#pragma unroll
-        for (int jg = 0; jg < NG; ++jg) {
-            float v[4] = {0.f, 0.f, 0.f, 0.f};
-            if (m < a.M) {
-                for (int sp = 0; sp < a.splits; ++sp) {
-                    const float* src = a.ws + ((size_t)sp * a.M + m) * a.N;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int n = col_of(jg * 4 + e);
-                        if (n < a.N) v[e] += __ldcg(src + n);
+                    for (int r = 0; r < RG; ++r) {
+                        acc[r0 + r][c] = fmaf(av[r].x, bv.x, acc[r0 + r][c]);
+                        acc[r0 + r][c] = fmaf(av[r].y, bv.y, acc[r0 + r][c]);
+                        acc[r0 + r][c] = fmaf(av[r].z, bv.z, acc[r0 + r][c]);
+                        acc[r0 + r][c] = fmaf(av[r].w, bv.w, acc[r0 + r][c]);
                     }
                 }
             }
-            store_final(i, jg, v);
         }
     }
-    if (tid == 0) a.counters[tile_id] = 0u;
+    cp_async_wait<0>();
+
+    auto row_of = [&](int r) { return m0 + ty + r * TY; };
+    auto col_of = [&](int c) { return n0 + tx + c * TX; };
+
+    if constexpr (!SPLIT) {
+#pragma unroll
+        for (int c = 0; c < TN; ++c) {
+            const int n = col_of(c);
+            if (n >= a.N) continue;
+            const float b = a.bias ? __ldg(a.bias + n) : 0.f;
+#pragma unroll
+            for (int r = 0; r < TM; ++r) {
+                const int m = row_of(r);
+                if (m < a.M) a.Y[(size_t)m * a.N + n] = epilogue<GELU>(acc[r][c], b);
+            }
+        }
+        return;
+    } else {
+        splitk_epilogue<TM, TN, GELU>(a, acc, row_of, col_of, tid);
+    }
 }
 
-template <int BM, int BN, int BK, int TM, int TN>
+template <int BM, int BN, int BK, int TM, int TN, int STAGES>
 int launch_cfg(const FfmaArgs& a, dim3 grid, cudaStream_t st, bool gelu) {
-    if (gelu)
-        ffma_kernel<BM, BN, BK, TM, TN, true><<<grid, 256, 0, st>>>(a);
-    else
-        ffma_kernel<BM, BN, BK, TM, TN, false><<<grid, 256, 0, st>>>(a);
+    constexpr size_t smem = ffma_smem_bytes<BM, BN, BK, STAGES>();
+    static_assert(smem <= 113 * 1024, "two CTAs per SM");
+    const bool split = a.splits > 1;
+    auto kern = gelu ? (split ? ffma_kernel<BM, BN, BK, TM, TN, STAGES, true, true>
+                              : ffma_kernel<BM, BN, BK, TM, TN, STAGES, true, false>)
+                     : (split ? ffma_kernel<BM, BN, BK, TM, TN, STAGES, false, true>
+                              : ffma_kernel<BM, BN, BK, TM, TN, STAGES, false, false>);
+    static unsigned long long attr_set[4] = {0, 0, 0, 0};  // per instantiation and device
+    const int which = (gelu ? 2 : 0) + (split ? 1 : 0);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LIN_ERR_CUDA;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(attr_set[which] & bit)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return LIN_ERR_CUDA;
+        attr_set[which] |= bit;
+    }
+    kern<<<grid, 256, smem, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? LIN_OK : LIN_ERR_CUDA;
 }
 
@@ -249,7 +282,6 @@ int launch_ffma(const Problem& p, const lin_plan& plan) {
     a.Y = static_cast<float*>(p.Y);
     a.splits = plan.splits;
     a.nkb = (p.K + plan.bk - 1) / plan.bk;
-    a.y_aligned16 = (reinterpret_cast<uintptr_t>(p.Y) % 16) == 0;
     a.ws = nullptr;
     a.counters = nullptr;
     if (plan.splits > 1) {
@@ -259,8 +291,10 @@ int launch_ffma(const Problem& p, const lin_plan& plan) {
     const dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
     const bool gelu = p.epilogue == LIN_EPI_GELU_TANH;
     switch (plan.variant) {
-        case 0: return launch_cfg<128, 128, 16, 8, 8>(a, grid, p.stream, gelu);
-        case 1: return launch_cfg<64, 64, 16, 4, 4>(a, grid, p.stream, gelu);
+        case 0: return launch_cfg<kFfmaCfg[0].bm, kFfmaCfg[0].bn, kFfmaCfg[0].bk, kFfmaCfg[0].tm, kFfmaCfg[0].tn, 3>(
+            a, grid, p.stream, gelu);
+        case 1: return launch_cfg<kFfmaCfg[1].bm, kFfmaCfg[1].bn, kFfmaCfg[1].bk, kFfmaCfg[1].tm, kFfmaCfg[1].tn, 4>(
+            a, grid, p.stream, gelu);
         default: return LIN_ERR_UNSUPPORTED;
     }
 }

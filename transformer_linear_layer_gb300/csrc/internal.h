@@ -53,7 +53,7 @@ constexpr int kSkinnyThreads = 192;                // warp 0 TMA, warp 1 MMA, wa
 
 struct FfmaCfg { int bm, bn, bk, tm, tn; };        // 256 threads each
 constexpr int kFfmaVariants = 2;
-constexpr FfmaCfg kFfmaCfg[kFfmaVariants] = {{128, 128, 16, 8, 8}, {64, 64, 16, 4, 4}};
+constexpr FfmaCfg kFfmaCfg[kFfmaVariants] = {{128, 128, 32, 8, 8}, {64, 64, 32, 4, 4}};
 
 struct TcCfg { int bn; bool pair; };              // BM = 128, BK = 128 bytes of K; ring depth from smem
 constexpr int kTcVariants = 6;                     // pair: 2 x 1 clusters sharing (multicasting) the B tile
