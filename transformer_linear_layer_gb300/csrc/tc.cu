@@ -59,17 +59,21 @@ template <bool BF16>
 constexpr int stage_rows() { return BF16 ? 32 : 16; }
 template <bool BF16>
 constexpr int stage_bytes() { return 8 * stage_rows<BF16>() * stage_row_bytes<BF16>(); }
-// Ring depth: as many 128-byte K stages as fit beside the staging tiles.
+// Bias staging: each epilogue warp keeps the bias of its BN/2 columns of the
+// current tile in shared memory (8 warps x BN/2 floats).
+template <int BN>
+constexpr int bias_stage_bytes() { return 8 * (BN / 2) * 4; }
+// Ring depth: as many 128-byte K stages as fit beside the staging areas.
 template <bool BF16, int BN>
 constexpr int tc_stages() {
-    return (227 * 1024 - 2048 - stage_bytes<BF16>()) / (128 * 128 + BN * 128) < 8
-               ? (227 * 1024 - 2048 - stage_bytes<BF16>()) / (128 * 128 + BN * 128)
+    return (227 * 1024 - 2048 - stage_bytes<BF16>() - bias_stage_bytes<BN>()) / (128 * 128 + BN * 128) < 8
+               ? (227 * 1024 - 2048 - stage_bytes<BF16>() - bias_stage_bytes<BN>()) / (128 * 128 + BN * 128)
                : 8;
 }
 template <bool BF16, int BN>
 constexpr size_t tc_smem_bytes() {
     return 1024 + (size_t)tc_stages<BF16, BN>() * (128 * 128 + BN * 128) + stage_bytes<BF16>() +
-           (2 * tc_stages<BF16, BN>() + 4) * 8 + 16;
+           bias_stage_bytes<BN>() + (2 * tc_stages<BF16, BN>() + 4) * 8 + 16;
 }
 
 // PAIR: the CTAs run as 2 x 1 clusters. The two CTAs of a cluster compute
@@ -103,7 +107,9 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * A_BYTES;
     uint8_t* sOut = sB + STAGES * B_BYTES;  // 8 warps x 32 rows x stage_row_bytes
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + stage_bytes<BF16>());  // full[S] empty[S] tfull[2] tempty[2]
+    float* sBiasAll = reinterpret_cast<float*>(sOut + stage_bytes<BF16>());  // 8 warps x BN/2 floats
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + stage_bytes<BF16>() + bias_stage_bytes<BN>());
+    // bars: full[S] empty[S] tfull[2] tempty[2]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
     int* s_abort = reinterpret_cast<int*>(tmem_slot + 1);
 
@@ -224,111 +230,134 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         // ---- epilogue: warp w reads TMEM lanes 32*(w%4).., columns half (w-2)/4 ----
         pdl_wait();  // Y (and bias) only after the previous kernel on the stream has finished
         const int q = warp & 3;
-        const int c_begin = ((warp - 2) >> 2) * HALF;
+        const int ew = warp - 2;
+        const int c_begin = (ew >> 2) * HALF;
         const int N = a.N;
+        float* sBias = sBiasAll + ew * HALF;
+        constexpr int CH = HALF / 32;  // 32-column chunks per warp and tile
+        constexpr int PER = BF16 ? 2 : 1;  // chunks per round trip to TMEM (fp32 staging needs the registers)
+        constexpr int RB = stage_row_bytes<BF16>();
+        constexpr int RP = stage_rows<BF16>();
+        constexpr int ESZO = BF16 ? 2 : 4;
+        constexpr int LPR = 32 * ESZO / 16;  // lanes per row with 16-byte pieces
+        uint8_t* st = sOut + ew * RP * RB;
+
+        // One 32 x 32 chunk: bias, activation, convert; lane = row. The values go
+        // through this warp's staging tile (rows [h*RP, h*RP + RP) per pass) and
+        // leave as whole row segments: consecutive lanes, consecutive addresses.
+        auto emit = [&](const uint32_t (&r)[32], int c, int m0, int n0) {
+            const int col = c_begin + c * 32;
+            const int nb = n0 + col;
+            if (nb >= N) return;  // warp-uniform
+            const bool full = nb + 32 <= N;
+            float v[32];
+#pragma unroll
+            for (int j4 = 0; j4 < 32; j4 += 4) {
+                const float4 b4 = *reinterpret_cast<const float4*>(sBias + c * 32 + j4);
+                v[j4 + 0] = epilogue<GELU>(__uint_as_float(r[j4 + 0]), b4.x);
+                v[j4 + 1] = epilogue<GELU>(__uint_as_float(r[j4 + 1]), b4.y);
+                v[j4 + 2] = epilogue<GELU>(__uint_as_float(r[j4 + 2]), b4.z);
+                v[j4 + 3] = epilogue<GELU>(__uint_as_float(r[j4 + 3]), b4.w);
+            }
+            const int mrow0 = m0 + q * 32;
+            const bool vec = full && (N * ESZO) % 16 == 0 && a.y_aligned16;
+#pragma unroll
+            for (int h = 0; h < 32 / RP; ++h) {
+                if (lane / RP == h) {
+                    uint8_t* mine_row = st + (lane % RP) * RB;
+                    if constexpr (BF16) {
+#pragma unroll
+                        for (int jj = 0; jj < 32; jj += 8) {
+                            uint4 o;
+                            o.x = pack_bf16x2(v[jj], v[jj + 1]);
+                            o.y = pack_bf16x2(v[jj + 2], v[jj + 3]);
+                            o.z = pack_bf16x2(v[jj + 4], v[jj + 5]);
+                            o.w = pack_bf16x2(v[jj + 6], v[jj + 7]);
+                            *reinterpret_cast<uint4*>(mine_row + jj * 2) = o;
+                        }
+                    } else {
+#pragma unroll
+                        for (int jj = 0; jj < 32; jj += 4)
+                            *reinterpret_cast<float4*>(mine_row + jj * 4) =
+                                make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
+                    }
+                }
+                __syncwarp();
+                const int rbase = mrow0 + h * RP;
+                if (vec) {
+                    const int sub = lane % LPR, rsub = lane / LPR;
+#pragma unroll
+                    for (int r0 = 0; r0 < RP; r0 += 32 / LPR) {
+                        const int rr = r0 + rsub;
+                        if (rbase + rr < a.M) {
+                            const uint4 val = *reinterpret_cast<const uint4*>(st + rr * RB + sub * 16);
+                            uint8_t* dst = static_cast<uint8_t*>(a.Y) + ((size_t)(rbase + rr) * N + nb) * ESZO + sub * 16;
+                            *reinterpret_cast<uint4*>(dst) = val;
+                        }
+                    }
+                } else {
+                    const bool col_ok = nb + lane < N;
+#pragma unroll 4
+                    for (int rr = 0; rr < RP; ++rr) {
+                        if (rbase + rr < a.M && col_ok) {
+                            if constexpr (BF16)
+                                static_cast<uint16_t*>(a.Y)[(size_t)(rbase + rr) * N + nb + lane] =
+                                    *reinterpret_cast<const uint16_t*>(st + rr * RB + lane * 2);
+                            else
+                                static_cast<float*>(a.Y)[(size_t)(rbase + rr) * N + nb + lane] =
+                                    *reinterpret_cast<const float*>(st + rr * RB + lane * 4);
+                        }
+                    }
+                }
+                __syncwarp();  // the staging rows are rewritten by the next pass / chunk
+            }
+        };
+
         int j = 0;
         for (int tile = first_item; tile < ntiles; tile += item_step, ++j) {
             const uint32_t buf = j & 1;
             const int m0 = tile_m0(tile), n0 = tile_n0(tile);
+            // This warp's bias columns of the tile, fetched while the MMAs run.
+#pragma unroll
+            for (int t = lane; t < HALF; t += 32) {
+                const int n = n0 + c_begin + t;
+                sBias[t] = (a.bias && n < N) ? __ldg(a.bias + n) : 0.f;
+            }
+            __syncwarp();
             const bool mine = mbar_wait(tfull0 + 8 * buf, (j >> 1) & 1);
             if (!mine) give_up();
             tc_fence_after();
             // tcgen05.ld is warp-collective: a warp proceeds only if every lane saw
             // the accumulator complete and no role of this CTA gave up.
             const bool ok = __all_sync(0xffffffffu, mine && *(volatile int*)s_abort == 0);
+            const uint32_t tbase =
+                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BUF_COLS + static_cast<uint32_t>(c_begin);
+            bool released = false;
 #pragma unroll 1
-            for (int c = 0; c < HALF / 32 && ok; ++c) {
-                const int col = c_begin + c * 32;
-                const int nb = n0 + col;
-                if (nb >= N) break;  // warp-uniform
-                uint32_t r[32];
-                tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BUF_COLS + static_cast<uint32_t>(col),
-                          r);
-                const bool full = nb + 32 <= N;
-                float v[32];
-                if (a.bias && full && a.bias_aligned16) {
-#pragma unroll
-                    for (int j4 = 0; j4 < 32; j4 += 4) {
-                        const float4 b4 = __ldg(reinterpret_cast<const float4*>(a.bias + nb + j4));
-                        v[j4 + 0] = epilogue<GELU>(__uint_as_float(r[j4 + 0]), b4.x);
-                        v[j4 + 1] = epilogue<GELU>(__uint_as_float(r[j4 + 1]), b4.y);
-                        v[j4 + 2] = epilogue<GELU>(__uint_as_float(r[j4 + 2]), b4.z);
-                        v[j4 + 3] = epilogue<GELU>(__uint_as_float(r[j4 + 3]), b4.w);
-                    }
-                } else {
-#pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int n = nb + jj;
-                        const float b = (a.bias && n < N) ? __ldg(a.bias + n) : 0.f;
-                        v[jj] = epilogue<GELU>(__uint_as_float(r[jj]), b);
-                    }
-                }
-                // Lane = row: write the row's 32 values into this warp's staging tile
-                // (rows [h*RP, h*RP + RP) per pass), then store whole row segments:
-                // consecutive lanes, consecutive addresses.
-                constexpr int RB = stage_row_bytes<BF16>();
-                constexpr int RP = stage_rows<BF16>();
-                constexpr int ESZO = BF16 ? 2 : 4;
-                constexpr int LPR = 32 * ESZO / 16;  // lanes per row with 16-byte pieces
-                uint8_t* st = sOut + (warp - 2) * RP * RB;
-                const int mrow0 = m0 + q * 32;
-                const bool vec = full && (N * ESZO) % 16 == 0 && a.y_aligned16;
-#pragma unroll
-                for (int h = 0; h < 32 / RP; ++h) {
-                    if (lane / RP == h) {
-                        uint8_t* mine_row = st + (lane % RP) * RB;
-                        if constexpr (BF16) {
-#pragma unroll
-                            for (int jj = 0; jj < 32; jj += 8) {
-                                uint4 o;
-                                o.x = pack_bf16x2(v[jj], v[jj + 1]);
-                                o.y = pack_bf16x2(v[jj + 2], v[jj + 3]);
-                                o.z = pack_bf16x2(v[jj + 4], v[jj + 5]);
-                                o.w = pack_bf16x2(v[jj + 6], v[jj + 7]);
-                                *reinterpret_cast<uint4*>(mine_row + jj * 2) = o;
-                            }
-                        } else {
-#pragma unroll
-                            for (int jj = 0; jj < 32; jj += 4)
-                                *reinterpret_cast<float4*>(mine_row + jj * 4) =
-                                    make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
-                        }
-                    }
+            for (int c = 0; c < CH && ok; c += PER) {
+                uint32_t r0[32], r1[32];
+                const bool two = PER == 2 && c + 1 < CH;
+                tmem_ld32_async(tbase + c * 32, r0);
+                if (two) tmem_ld32_async(tbase + (c + 1) * 32, r1);
+                tmem_wait_ld(r0);
+                if (two) tmem_wait_ld(r1);
+                if (c + PER >= CH) {
+                    // Last read of the accumulator: the MMA issuer may reuse it
+                    // while this warp converts and stores.
+                    tc_fence_before();
                     __syncwarp();
-                    const int rbase = mrow0 + h * RP;
-                    if (vec) {
-                        const int sub = lane % LPR, rsub = lane / LPR;
-#pragma unroll
-                        for (int r0 = 0; r0 < RP; r0 += 32 / LPR) {
-                            const int rr = r0 + rsub;
-                            if (rbase + rr < a.M) {
-                                const uint4 val = *reinterpret_cast<const uint4*>(st + rr * RB + sub * 16);
-                                uint8_t* dst =
-                                    static_cast<uint8_t*>(a.Y) + ((size_t)(rbase + rr) * N + nb) * ESZO + sub * 16;
-                                *reinterpret_cast<uint4*>(dst) = val;
-                            }
-                        }
-                    } else {
-                        const bool col_ok = nb + lane < N;
-#pragma unroll 4
-                        for (int rr = 0; rr < RP; ++rr) {
-                            if (rbase + rr < a.M && col_ok) {
-                                if constexpr (BF16)
-                                    static_cast<uint16_t*>(a.Y)[(size_t)(rbase + rr) * N + nb + lane] =
-                                        *reinterpret_cast<const uint16_t*>(st + rr * RB + lane * 2);
-                                else
-                                    static_cast<float*>(a.Y)[(size_t)(rbase + rr) * N + nb + lane] =
-                                        *reinterpret_cast<const float*>(st + rr * RB + lane * 4);
-                            }
-                        }
-                    }
-                    __syncwarp();  // the staging rows are rewritten by the next pass / chunk
+                    if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
+                    released = true;
                 }
+                emit(r0, c, m0, n0);
+                if (two) emit(r1, c + 1, m0, n0);
             }
-            // This warp's reads of the buffer are done: let the MMA issuer reuse it.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
+            if (!released) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
+            }
+            __syncwarp();  // sBias is rewritten for the next tile
         }
     }
 
