@@ -88,7 +88,10 @@ typedef enum {
  * a GPU", Act I, split-K combined by a fixed-order reduction). */
 typedef struct {
     int kernel;   /* lin_kernel */
-    int variant;  /* kernel-specific tile configuration id (see DESIGN notes in the source) */
+    int variant;  /* kernel-specific tile configuration id. TC: 0, 1, 2 = one CTA
+                   * per 128 x 256 / 128 / 192 tile; 3, 4, 5 = SM pairs (2-CTA
+                   * clusters issuing cta_group::2 MMAs) per 256 x 256 / 128 / 192
+                   * tile. SKINNY and FFMA: see the kernels' sources. */
     int bm, bn, bk;
     int splits;   /* >= 1 */
     int stages;   /* shared-memory pipeline depth (TC), 0 otherwise */

@@ -32,7 +32,7 @@ def all_plans(ctx, M, N, K, precision):
             for s in (0, 1, 2, 8):
                 plans.append(tll.plan_make(sm, tll.KERNEL_SKINNY, v, s, M, N, K, "bf16"))
     if precision in (BF16, TF32):
-        for v in range(6):  # 3-5: 2-CTA clusters multicasting the W tile
+        for v in range(6):  # 3-5: SM pairs (2-CTA clusters, cta_group::2 MMAs on 256-row tiles)
             for width in (0, 1, 3):  # persistent CTAs: one per SM, or few CTAs walking many tiles
                 plans.append(tll.plan_make(sm, tll.KERNEL_TC, v, width, M, N, K, PREC_NAME[precision]))
     if precision == FP32:

@@ -55,8 +55,8 @@ struct FfmaCfg { int bm, bn, bk, tm, tn; };        // 256 threads each
 constexpr int kFfmaVariants = 2;
 constexpr FfmaCfg kFfmaCfg[kFfmaVariants] = {{128, 128, 32, 8, 8}, {64, 64, 32, 4, 4}};
 
-struct TcCfg { int bn; bool pair; };              // BM = 128, BK = 128 bytes of K; ring depth from smem
-constexpr int kTcVariants = 6;                     // pair: 2 x 1 clusters sharing (multicasting) the B tile
+struct TcCfg { int bn; bool pair; };              // BM = 128 per CTA, BK = 128 bytes of K; ring depth from smem
+constexpr int kTcVariants = 6;                     // pair: 2 x 1 clusters, SM-pair MMAs on 256 x BN tiles
 constexpr TcCfg kTcCfg[kTcVariants] = {{256, false}, {128, false}, {192, false},
                                        {256, true}, {128, true}, {192, true}};
 constexpr int kTcThreads = 320;                    // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue

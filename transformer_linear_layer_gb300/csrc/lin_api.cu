@@ -117,21 +117,36 @@ int make_ffma(int sm, int variant, int splits, int M, int N, int K, size_t ws, l
 }
 
 // Persistent tcgen05 kernel: `width` CTAs walk the 128 x BN output tiles
-// (0 = one CTA per SM) in static round robin; pair variants walk vertical
-// tile pairs with one 2-CTA cluster per pair (grid rounded down to even).
-// Default N tile: the smallest predicted time rounds(BN) x (BN + 110), where
-// rounds = ceil(work items / CTAs) and the constant 110 (in columns) is the
-// per-tile cost that does not scale with BN, fitted to the measured M = 8192
-// and 4096^3 shapes.
-int make_tc(int sm, int variant, int width, int M, int N, int K, lin_plan* p) {
+// (0 = one CTA per SM) in static round robin; pair variants walk 256 x BN
+// tiles with one 2-CTA cluster (an SM pair) per tile (grid rounded down to
+// even). Default, from the measured M = 8192 GPT-2 shapes, the LM head and
+// 4096^3 / 8192^3:
+// * SM pair when each tile runs at least 64 K stages (K >= 4096 bf16 or 2048
+//   tf32): there the pair's lighter shared-memory traffic wins (8192^3 bf16
+//   1.91 vs 1.62 PF/s); with shorter K its per-tile synchronisation costs
+//   more than it saves.
+// * N tile: the smallest rounds_eff(BN) x r(BN), where rounds_eff is the
+//   mean of the average and the maximum tiles per CTA (a back-to-back caller
+//   overlaps part of a ragged last round with its next call) and r = 1, 0.9,
+//   0.75 for BN = 256, 192, 128 is the measured time of one round relative to
+//   BN = 256 (A is reloaded for every N tile, so narrow tiles are slower per
+//   column).
+int make_tc(int sm, int variant, int width, int M, int N, int K, int esz, lin_plan* p) {
     if (M < 1 || N < 1 || K < 1 || width < 0) return LIN_ERR_UNSUPPORTED;
     if (variant < 0) {
+        const bool want_pair = ceil_div(K, 128 / esz) >= 64;
         double best = 0.0;
         for (int v = 0; v < kTcVariants; ++v) {
-            if (kTcCfg[v].pair) continue;
-            const long long t = (long long)ceil_div(M, 128) * ceil_div(N, kTcCfg[v].bn);
-            const long long w = width > 0 ? width : sm;
-            const double cost = (double)((t + w - 1) / w) * (kTcCfg[v].bn + 110);
+            if (kTcCfg[v].pair != want_pair) continue;
+            const int bn = kTcCfg[v].bn;
+            const long long items =
+                (long long)(want_pair ? ceil_div(ceil_div(M, 128), 2) : ceil_div(M, 128)) * ceil_div(N, bn);
+            long long slots = width > 0 ? width : sm;
+            if (want_pair) slots = slots / 2 > 0 ? slots / 2 : 1;
+            const double avg = (double)items / (double)slots;
+            const double mx = (double)((items + slots - 1) / slots);
+            const double rel = bn == 256 ? 1.0 : bn == 192 ? 0.9 : 0.75;
+            const double cost = 0.5 * (avg + mx) * rel;
             if (variant < 0 || cost < best) {
                 best = cost;
                 variant = v;
@@ -181,9 +196,9 @@ int plan_default(int sm, int M, int N, int K, int precision, size_t ws, lin_plan
     switch (precision) {
         case LIN_PREC_BF16:
             if (M <= 16) return make_skinny(sm, 0, 0, M, N, K, ws, p);
-            return make_tc(sm, -1, 0, M, N, K, p);
+            return make_tc(sm, -1, 0, M, N, K, 2, p);
         case LIN_PREC_TF32:
-            return make_tc(sm, -1, 0, M, N, K, p);
+            return make_tc(sm, -1, 0, M, N, K, 4, p);
         default:
             return make_ffma(sm, -1, 0, M, N, K, ws, p);
     }
@@ -475,7 +490,8 @@ int lin_plan_make(int sm_count, int kernel, int variant, int splits, int M, int 
             return lin::make_ffma(sm_count, variant, splits, M, N, K, unlimited, out);
         case LIN_KERNEL_TC:
             if (precision == LIN_PREC_FP32) return LIN_ERR_UNSUPPORTED;
-            return lin::make_tc(sm_count, variant, splits, M, N, K, out);  // splits = CTAs (0 = one per SM)
+            // splits = CTAs (0 = one per SM)
+            return lin::make_tc(sm_count, variant, splits, M, N, K, precision == LIN_PREC_BF16 ? 2 : 4, out);
         case LIN_KERNEL_NONE:
         case LIN_KERNEL_FILL:
             return lin::plan_default(sm_count, M, N, K, precision, unlimited, out);

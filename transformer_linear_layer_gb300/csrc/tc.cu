@@ -63,40 +63,48 @@ constexpr int stage_bytes() { return 8 * stage_rows<BF16>() * stage_row_bytes<BF
 // current tile in shared memory (8 warps x BN/2 floats).
 template <int BN>
 constexpr int bias_stage_bytes() { return 8 * (BN / 2) * 4; }
+// Bytes of one K stage in a CTA: the 128-row A tile and this CTA's W rows
+// (all BN of them, or BN/2 for an SM pair).
+template <int BN, bool PAIR>
+constexpr int tc_stage_bytes() { return 128 * 128 + (PAIR ? BN / 2 : BN) * 128; }
 // Ring depth: as many 128-byte K stages as fit beside the staging areas.
-template <bool BF16, int BN>
+template <bool BF16, int BN, bool PAIR>
 constexpr int tc_stages() {
-    return (227 * 1024 - 2048 - stage_bytes<BF16>() - bias_stage_bytes<BN>()) / (128 * 128 + BN * 128) < 8
-               ? (227 * 1024 - 2048 - stage_bytes<BF16>() - bias_stage_bytes<BN>()) / (128 * 128 + BN * 128)
+    return (227 * 1024 - 2048 - stage_bytes<BF16>() - bias_stage_bytes<BN>()) / tc_stage_bytes<BN, PAIR>() < 8
+               ? (227 * 1024 - 2048 - stage_bytes<BF16>() - bias_stage_bytes<BN>()) / tc_stage_bytes<BN, PAIR>()
                : 8;
 }
-template <bool BF16, int BN>
+template <bool BF16, int BN, bool PAIR>
 constexpr size_t tc_smem_bytes() {
-    return 1024 + (size_t)tc_stages<BF16, BN>() * (128 * 128 + BN * 128) + stage_bytes<BF16>() +
-           bias_stage_bytes<BN>() + (2 * tc_stages<BF16, BN>() + 4) * 8 + 16;
+    return 1024 + (size_t)tc_stages<BF16, BN, PAIR>() * tc_stage_bytes<BN, PAIR>() + stage_bytes<BF16>() +
+           bias_stage_bytes<BN>() + (2 * tc_stages<BF16, BN, PAIR>() + 4) * 8 + 16;
 }
 
-// PAIR: the CTAs run as 2 x 1 clusters. The two CTAs of a cluster compute
-// vertically adjacent tiles (M blocks 2i and 2i+1, the same N block) in lock
-// step; each loads its own A tile and one half of the shared B tile, and
-// multicasts that half into both CTAs' shared memory, so each SM reads
-// 16 + BN*64 bytes per K stage from L2 instead of 16 + BN*128 KiB. A stage is
-// refilled only after both CTAs' MMAs released it (each MMA thread commits to
-// the "empty" barrier of both CTAs).
+// PAIR: SM-pair MMA. The CTAs run as 2 x 1 clusters and a cluster computes a
+// 256 x BN tile with tcgen05.mma.cta_group::2 issued by the even CTA: each CTA
+// loads its own 128 rows of X and one half (BN/2 rows) of the W tile into its
+// shared memory, the pair's tensor cores read both halves, and each CTA's TMEM
+// receives its 128 rows of the accumulator. Per unit of MMA work a CTA stages
+// a third less shared-memory data than with a 128 x BN tile of its own (which
+// is what bounds the single-CTA form: TMA writes plus tensor-core reads).
+// Both CTAs' copies complete the even CTA's "full" barrier; its commits
+// release the stage ("empty") and publish the accumulator ("tfull") in both
+// CTAs; both CTAs' epilogue warps release the accumulator to its "tempty".
 template <bool BF16, int BN, bool GELU, bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcArgs a) {
-    constexpr int STAGES = tc_stages<BF16, BN>();
-    constexpr int BM = 128;
+    constexpr int STAGES = tc_stages<BF16, BN, PAIR>();
+    constexpr int BM = 128;                       // rows per CTA
     constexpr int ESZ = BF16 ? 2 : 4;
     constexpr int BK = 128 / ESZ;                 // K elements per stage (128 bytes)
+    constexpr int BROWS = PAIR ? BN / 2 : BN;     // W rows this CTA loads per stage
     constexpr uint32_t A_BYTES = BM * 128;        // 16 KiB
-    constexpr uint32_t B_BYTES = BN * 128;
-    constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES;
+    constexpr uint32_t B_BYTES = BROWS * 128;
+    constexpr uint32_t STAGE_TX = (PAIR ? 2u : 1u) * (A_BYTES + B_BYTES);  // both CTAs' copies for a pair
     constexpr int MMAS = 4;                       // 32 bytes of K per MMA
     constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;  // two accumulators
     constexpr uint32_t BUF_COLS = BN <= 128 ? BN : 256;          // column offset of the second one
-    constexpr uint32_t IDESC = make_idesc(BF16 ? 1u : 2u, BM, BN);
+    constexpr uint32_t IDESC = make_idesc(BF16 ? 1u : 2u, PAIR ? 2 * BM : BM, BN);
     constexpr int EPI_WARPS = kTcThreads / 32 - 2;  // two per TMEM lane quadrant
     constexpr int HALF = BN / 2;                  // columns per epilogue warp
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "N tile");
@@ -119,6 +127,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     const int mu = PAIR ? (mt + 1) / 2 : mt;
     const int ntiles = mu * nt;
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;  // issues the MMAs; owns the full and tempty barriers
     const int first_item = PAIR ? (int)cluster_id_x() : (int)blockIdx.x;
     const int item_step = PAIR ? (int)cluster_count_x() : (int)gridDim.x;
     auto tile_m0 = [&](int item) { return (PAIR ? 2 * (item % mu) + (int)rank : item % mu) * BM; };
@@ -130,21 +139,26 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, PAIR ? 2 : 1);  // PAIR: released by both CTAs' MMAs
+            mbar_init(empty0 + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull0 + 8 * b, 1);
-            mbar_init(tempty0 + 8 * b, EPI_WARPS);
+            mbar_init(tempty0 + 8 * b, PAIR ? 2 * EPI_WARPS : EPI_WARPS);
         }
         *s_abort = 0;
         mbar_fence_init();
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
     }
-    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    if (warp == 1) {
+        if constexpr (PAIR)
+            tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+        else
+            tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    }
     tc_fence_before();
     if constexpr (PAIR)
-        cluster_sync_all();  // the peer's barriers exist before any multicast reaches them
+        cluster_sync_all();  // the peer's barriers exist before any copy, commit or arrival reaches them
     else
         __syncthreads();
     tc_fence_after();
@@ -171,33 +185,38 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(full0 + 8 * s, STAGE_TX);
-                    tma_load_2d(smem_u32(sA + s * A_BYTES), &tmA, full0 + 8 * s, kb * BK, m0);
                     if constexpr (PAIR) {
-                        constexpr uint32_t HALF_B = (BN / 2) * 128;
-                        tma_load_2d_mc(smem_u32(sB + s * B_BYTES + rank * HALF_B), &tmB, full0 + 8 * s, kb * BK,
-                                       n0 + (int)rank * (BN / 2), (uint16_t)0x3);
+                        // Both CTAs' copies complete the even CTA's barrier.
+                        if (leader) mbar_expect_tx(full0 + 8 * s, STAGE_TX);
+                        const uint32_t fb = dsmem_map(full0 + 8 * s, 0);
+                        tma_load_2d_pair(smem_u32(sA + s * A_BYTES), &tmA, fb, kb * BK, m0);
+                        tma_load_2d_pair(smem_u32(sB + s * B_BYTES), &tmB, fb, kb * BK, n0 + (int)rank * BROWS);
                     } else {
+                        mbar_expect_tx(full0 + 8 * s, STAGE_TX);
+                        tma_load_2d(smem_u32(sA + s * A_BYTES), &tmA, full0 + 8 * s, kb * BK, m0);
                         tma_load_2d(smem_u32(sB + s * B_BYTES), &tmB, full0 + 8 * s, kb * BK, n0);
                     }
                     issued = it + 1;
                 }
             }
-            if (*(volatile int*)s_abort) {
-                // Drain this CTA's own copies still in flight before the CTA exits.
+            if (*(volatile int*)s_abort && leader) {
+                // Drain the copies still in flight before the CTA exits (for a pair,
+                // the even CTA's barriers count both CTAs' copies).
                 const uint32_t first = issued > (uint32_t)STAGES ? issued - STAGES : 0;
                 for (uint32_t i = first; i < issued; ++i) mbar_wait(full0 + 8 * (i % STAGES), (i / STAGES) & 1);
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             // ---- MMA issuer: accumulators alternate between two TMEM buffers ----
             uint32_t it = 0;
             int j = 0;
             bool ok = true;
             for (int tile = first_item; tile < ntiles && ok; tile += item_step, ++j) {
                 const uint32_t buf = j & 1;
-                if (*(volatile int*)s_abort || !mbar_wait(tempty0 + 8 * buf, ((j >> 1) & 1) ^ 1)) {
+                const bool freed = PAIR ? mbar_wait_cluster(tempty0 + 8 * buf, ((j >> 1) & 1) ^ 1)
+                                        : mbar_wait(tempty0 + 8 * buf, ((j >> 1) & 1) ^ 1);
+                if (*(volatile int*)s_abort || !freed) {
                     give_up();
                     break;
                 }
@@ -213,18 +232,28 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     tc_fence_after();
                     const uint64_t ad = sw128_kmajor_desc(smem_u32(sA + s * A_BYTES));
                     const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + s * B_BYTES));
+                    if constexpr (PAIR) {
 #pragma unroll
-                    for (int kk = 0; kk < MMAS; ++kk)
-                        tc_mma<BF16>(d, ad + 2u * kk, bd + 2u * kk, IDESC, (kb | kk) != 0 ? 1u : 0u);
-                    if constexpr (PAIR)
-                        tc_commit_mc(empty0 + 8 * s, (uint16_t)0x3);
-                    else
+                        for (int kk = 0; kk < MMAS; ++kk)
+                            tc_mma_pair<BF16>(d, ad + 2u * kk, bd + 2u * kk, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        tc_commit_pair_mc(empty0 + 8 * s, (uint16_t)0x3);
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < MMAS; ++kk)
+                            tc_mma<BF16>(d, ad + 2u * kk, bd + 2u * kk, IDESC, (kb | kk) != 0 ? 1u : 0u);
                         tc_commit(empty0 + 8 * s);
+                    }
                 }
-                tc_commit(tfull0 + 8 * buf);
+                if constexpr (PAIR)
+                    tc_commit_pair_mc(tfull0 + 8 * buf, (uint16_t)0x3);
+                else
+                    tc_commit(tfull0 + 8 * buf);
             }
             // Do not reach the teardown before this CTA's MMAs have completed.
-            if (j > 0 && !mbar_wait(tfull0 + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1)) give_up();
+            if (j > 0) {
+                const uint32_t lb = tfull0 + 8 * ((j - 1) & 1), lp = ((j - 1) >> 1) & 1;
+                if (!(PAIR ? mbar_wait_cluster(lb, lp) : mbar_wait(lb, lp))) give_up();
+            }
         }
     } else {
         // ---- epilogue: warp w reads TMEM lanes 32*(w%4).., columns half (w-2)/4 ----
@@ -244,7 +273,9 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 
         // One 32 x 32 chunk: bias, activation, convert; lane = row. The values go
         // through this warp's staging tile (rows [h*RP, h*RP + RP) per pass) and
-        // leave as whole row segments: consecutive lanes, consecutive addresses.
+        // leave as whole row segments: consecutive lanes, consecutive addresses
+        // (storing each lane's own row from registers scatters every store
+        // instruction over 32 rows and was measured slower).
         auto emit = [&](const uint32_t (&r)[32], int c, int m0, int n0) {
             const int col = c_begin + c * 32;
             const int nb = n0 + col;
@@ -313,6 +344,14 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             }
         };
 
+        // Hand an accumulator buffer back to the MMA issuer (the even CTA's barrier).
+        auto release_acc = [&](uint32_t buf) {
+            if (PAIR && !leader)
+                mbar_arrive_remote(dsmem_map(tempty0 + 8 * buf, 0));
+            else
+                mbar_arrive(tempty0 + 8 * buf);
+        };
+
         int j = 0;
         for (int tile = first_item; tile < ntiles; tile += item_step, ++j) {
             const uint32_t buf = j & 1;
@@ -324,7 +363,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 sBias[t] = (a.bias && n < N) ? __ldg(a.bias + n) : 0.f;
             }
             __syncwarp();
-            const bool mine = mbar_wait(tfull0 + 8 * buf, (j >> 1) & 1);
+            const bool mine = PAIR ? mbar_wait_cluster(tfull0 + 8 * buf, (j >> 1) & 1)
+                                   : mbar_wait(tfull0 + 8 * buf, (j >> 1) & 1);
             if (!mine) give_up();
             tc_fence_after();
             // tcgen05.ld is warp-collective: a warp proceeds only if every lane saw
@@ -346,7 +386,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     // while this warp converts and stores.
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
+                    if (lane == 0) release_acc(buf);
                     released = true;
                 }
                 emit(r0, c, m0, n0);
@@ -355,7 +395,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             if (!released) {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
+                if (lane == 0) release_acc(buf);
             }
             __syncwarp();  // sBias is rewritten for the next tile
         }
@@ -371,7 +411,10 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
@@ -380,8 +423,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 template <bool BF16, int BN, bool GELU, bool PAIR>
 int launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, int grid, bool early,
                cudaStream_t st) {
-    constexpr size_t smem = tc_smem_bytes<BF16, BN>();
-    static_assert(tc_smem_bytes<BF16, BN>() <= 227 * 1024, "shared memory");
+    constexpr size_t smem = tc_smem_bytes<BF16, BN, PAIR>();
+    static_assert(tc_smem_bytes<BF16, BN, PAIR>() <= 227 * 1024, "shared memory");
     auto kern = tc_kernel<BF16, BN, GELU, PAIR>;
     static unsigned long long attr_set = 0;  // one attribute call per instantiation and device
     int dev = 0;
