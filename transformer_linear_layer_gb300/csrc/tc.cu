@@ -24,8 +24,9 @@
 //   exist": the epilogue already holds the value in a register).
 // * Tails: the copy engine fills rows and K beyond the tensor with zeros;
 //   stores are predicated on m < M and n < N.
-// * Programmatic dependent launch: CTAs may start before the previous kernel on
-//   the stream has finished (filling SMs its last round leaves idle). Operands
+// * Programmatic dependent launch: a CTA may start on an SM as soon as the
+//   previous kernel's CTA there has exited, before that whole grid finishes
+//   (its prologue overlaps the other SMs' last tiles). Operands
 //   are read before griddepcontrol.wait only when neither is that kernel's
 //   output; bias and Y always after it.
 // * Every wait is bounded (iterations and wall clock); a wait that gives up
@@ -46,6 +47,7 @@ struct TcArgs {
     int y_aligned16;     // Y's base is 16-byte aligned (vector stores allowed)
     int bias_aligned16;  // bias is 16-byte aligned (vector loads allowed)
     int early_inputs;    // X and W may be read before the dependency wait (not the previous call's output)
+    int y_tma;           // bf16 Y stored by TMA from 32 x 32 boxes (16-byte aligned rows)
 };
 
 // Epilogue staging: each epilogue warp owns a 32 x 32 output tile in shared
@@ -92,7 +94,8 @@ constexpr size_t tc_smem_bytes() {
 // CTAs; both CTAs' epilogue warps release the accumulator to its "tempty".
 template <bool BF16, int BN, bool GELU, bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1)
-tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcArgs a) {
+tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+          const __grid_constant__ CUtensorMap tmY, const TcArgs a) {
     constexpr int STAGES = tc_stages<BF16, BN, PAIR>();
     constexpr int BM = 128;                       // rows per CTA
     constexpr int ESZ = BF16 ? 2 : 4;
@@ -291,6 +294,34 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 v[j4 + 3] = epilogue<GELU>(__uint_as_float(r[j4 + 3]), b4.w);
             }
             const int mrow0 = m0 + q * 32;
+            if constexpr (BF16) {
+                if (a.y_tma) {
+                    // Into this warp's 32 x 32 box (64-byte swizzle: conflict-free
+                    // row-per-lane writes), then one TMA store, which clips rows
+                    // and columns outside Y. The box is reused once the previous
+                    // store has read it.
+                    if (mrow0 >= a.M) return;
+                    uint8_t* box = sOut + ew * 2048;
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+#pragma unroll
+                    for (int p16 = 0; p16 < 4; ++p16) {
+                        uint4 o;
+                        o.x = pack_bf16x2(v[8 * p16 + 0], v[8 * p16 + 1]);
+                        o.y = pack_bf16x2(v[8 * p16 + 2], v[8 * p16 + 3]);
+                        o.z = pack_bf16x2(v[8 * p16 + 4], v[8 * p16 + 5]);
+                        o.w = pack_bf16x2(v[8 * p16 + 6], v[8 * p16 + 7]);
+                        *reinterpret_cast<uint4*>(box + lane * 64 + ((p16 ^ ((lane >> 1) & 3)) * 16)) = o;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmY, smem_u32(box), nb, mrow0);
+                        bulk_commit();
+                    }
+                    return;
+                }
+            }
             const bool vec = full && (N * ESZO) % 16 == 0 && a.y_aligned16;
 #pragma unroll
             for (int h = 0; h < 32 / RP; ++h) {
@@ -399,6 +430,9 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             }
             __syncwarp();  // sBias is rewritten for the next tile
         }
+        // TMA stores of this warp complete before the CTA releases its shared memory.
+        if (BF16 && a.y_tma && lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     __syncwarp();
@@ -421,7 +455,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 // ---------------------------------------------------------------- host side
 
 template <bool BF16, int BN, bool GELU, bool PAIR>
-int launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, int grid, bool early,
+int launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const TcArgs& a, int grid, bool early,
                cudaStream_t st) {
     constexpr size_t smem = tc_smem_bytes<BF16, BN, PAIR>();
     static_assert(tc_smem_bytes<BF16, BN, PAIR>() <= 227 * 1024, "shared memory");
@@ -456,20 +490,20 @@ int launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, in
     }
     cfg.attrs = attrs;
     cfg.numAttrs = na;
-    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, a) != cudaSuccess) return LIN_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, a) != cudaSuccess) return LIN_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? LIN_OK : LIN_ERR_CUDA;
 }
 
 template <bool BF16, bool GELU>
-int launch_variant(int variant, const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, int grid,
+int launch_variant(int variant, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const TcArgs& a, int grid,
                    bool early, cudaStream_t st) {
     switch (variant) {
-        case 0: return launch_cfg<BF16, kTcCfg[0].bn, GELU, false>(ta, tb, a, grid, early, st);
-        case 1: return launch_cfg<BF16, kTcCfg[1].bn, GELU, false>(ta, tb, a, grid, early, st);
-        case 2: return launch_cfg<BF16, kTcCfg[2].bn, GELU, false>(ta, tb, a, grid, early, st);
-        case 3: return launch_cfg<BF16, kTcCfg[3].bn, GELU, true>(ta, tb, a, grid, early, st);
-        case 4: return launch_cfg<BF16, kTcCfg[4].bn, GELU, true>(ta, tb, a, grid, early, st);
-        case 5: return launch_cfg<BF16, kTcCfg[5].bn, GELU, true>(ta, tb, a, grid, early, st);
+        case 0: return launch_cfg<BF16, kTcCfg[0].bn, GELU, false>(ta, tb, ty, a, grid, early, st);
+        case 1: return launch_cfg<BF16, kTcCfg[1].bn, GELU, false>(ta, tb, ty, a, grid, early, st);
+        case 2: return launch_cfg<BF16, kTcCfg[2].bn, GELU, false>(ta, tb, ty, a, grid, early, st);
+        case 3: return launch_cfg<BF16, kTcCfg[3].bn, GELU, true>(ta, tb, ty, a, grid, early, st);
+        case 4: return launch_cfg<BF16, kTcCfg[4].bn, GELU, true>(ta, tb, ty, a, grid, early, st);
+        case 5: return launch_cfg<BF16, kTcCfg[5].bn, GELU, true>(ta, tb, ty, a, grid, early, st);
         default: return LIN_ERR_UNSUPPORTED;
     }
 }
@@ -508,6 +542,19 @@ bool make_kmajor_map(CUtensorMap* map, const void* base, bool bf16, int rows, in
     return r == CUDA_SUCCESS;
 }
 
+bool make_out_map_bf16(CUtensorMap* map, void* base, int M, int N) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 2};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int launch_tc(const Problem& p, const lin_plan& plan) {
     const bool bf16 = p.precision == LIN_PREC_BF16;
     if (plan.variant < 0 || plan.variant >= kTcVariants) return LIN_ERR_UNSUPPORTED;
@@ -525,23 +572,28 @@ int launch_tc(const Problem& p, const lin_plan& plan) {
     a.y_aligned16 = (reinterpret_cast<uintptr_t>(p.Y) % 16) == 0;
     a.bias_aligned16 = (reinterpret_cast<uintptr_t>(p.bias) % 16) == 0;
     a.early_inputs = (p.early_start && p.early_x) ? 1 : 0;
+    // bf16 rows 16-byte aligned: Y leaves by TMA store; otherwise (odd N, as in
+    // the LM head) through the staged row-segment stores. The fallback map is a
+    // placeholder the kernel never uses.
+    CUtensorMap ty = ta;
+    a.y_tma = 0;
+    if (bf16 && a.y_aligned16 && p.N % 8 == 0) {
+        if (!make_out_map_bf16(&ty, p.Y, p.M, p.N)) return LIN_ERR_CUDA;
+        a.y_tma = 1;
+    }
     const int grid = plan.grid_x;
     const bool gelu = p.epilogue == LIN_EPI_GELU_TANH;
-    // Programmatic dependent launch when the context allows an early start and
-    // this grid's last round of tiles leaves at least 30% of its CTAs idle (the
-    // next call can use them); with a nearly full last round the early CTAs only
-    // compete for bandwidth (measured on the M = 8192 shapes). The kernel waits
-    // before its first load unless the inputs are independent.
-    const long long mt = (p.M + 127) / 128, nt = (p.N + plan.bn - 1) / plan.bn;
-    const long long items = (kTcCfg[plan.variant].pair ? (mt + 1) / 2 : mt) * nt;
-    const long long slots = kTcCfg[plan.variant].pair ? grid / 2 : grid;
-    const long long last = items - ((items + slots - 1) / slots - 1) * slots;
-    const bool early = p.early_start && (double)last < 0.7 * (double)slots;
+    // Programmatic dependent launch whenever the context allows an early start:
+    // a CTA of this grid starts on an SM as soon as the previous kernel's CTA
+    // there has exited (prologue, TMEM allocation and, for independent inputs,
+    // the first loads overlap the previous kernel's last tiles elsewhere). The
+    // kernel waits before its first load unless the inputs are independent.
+    const bool early = p.early_start;
     if (bf16)
-        return gelu ? launch_variant<true, true>(plan.variant, ta, tb, a, grid, early, p.stream)
-                    : launch_variant<true, false>(plan.variant, ta, tb, a, grid, early, p.stream);
-    return gelu ? launch_variant<false, true>(plan.variant, ta, tb, a, grid, early, p.stream)
-                : launch_variant<false, false>(plan.variant, ta, tb, a, grid, early, p.stream);
+        return gelu ? launch_variant<true, true>(plan.variant, ta, tb, ty, a, grid, early, p.stream)
+                    : launch_variant<true, false>(plan.variant, ta, tb, ty, a, grid, early, p.stream);
+    return gelu ? launch_variant<false, true>(plan.variant, ta, tb, ty, a, grid, early, p.stream)
+                : launch_variant<false, false>(plan.variant, ta, tb, ty, a, grid, early, p.stream);
 }
 
 }  // namespace lin

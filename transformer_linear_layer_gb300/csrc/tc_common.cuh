@@ -87,6 +87,25 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// 2-D tiled TMA store of a shared-memory box to (x = inner element, y = row);
+// elements outside the tensor are not written. Completion is tracked per
+// thread with bulk groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until this thread's bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until this thread's bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -328,5 +347,9 @@ __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepc
 // 2-D tensor map over a rows x K row-major tensor, box = 128 bytes of K x box_rows,
 // 128-byte swizzle, out-of-range elements read as zero.
 bool make_kmajor_map(CUtensorMap* map, const void* base, bool bf16, int rows, int K, int box_rows);
+// 2-D tensor map over the M x N bf16 output, box = 32 columns x 32 rows with
+// the 64-byte swizzle (16-byte piece p of row r at piece p ^ ((r >> 1) & 3)).
+// Needs a 16-byte aligned base and N a multiple of 8.
+bool make_out_map_bf16(CUtensorMap* map, void* base, int M, int N);
 
 }  // namespace lin
