@@ -17,10 +17,28 @@ __device__ __forceinline__ float gelu_tanh(float s) {
     return 0.5f * s * (1.0f + tanhf(k0 * (s + k1 * s * s * s)));
 }
 
-template <bool GELU>
+// The same GELU for results that are rounded to bf16: tanh from the hardware
+// approximation (tanh.approx.f32, relative error about 2^-11 per the PTX ISA),
+// below the bf16 rounding of the result (2^-9 relative); the error it adds to
+// GELU(s) is at most |s| * 2^-12.
+__device__ __forceinline__ float tanh_hw(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float gelu_tanh_bf16out(float s) {
+    const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
+    const float k1 = 0.044715f;
+    const float hs = 0.5f * s;
+    return fmaf(hs, tanh_hw(k0 * (s + k1 * s * s * s)), hs);
+}
+
+// Bias add and activation. BF16OUT: the result is rounded to bf16 next (the
+// activation may use the hardware tanh).
+template <bool GELU, bool BF16OUT = false>
 __device__ __forceinline__ float epilogue(float acc, float b) {
     float s = acc + b;
-    if constexpr (GELU) s = gelu_tanh(s);
+    if constexpr (GELU) s = BF16OUT ? gelu_tanh_bf16out(s) : gelu_tanh(s);
     return s;
 }
 

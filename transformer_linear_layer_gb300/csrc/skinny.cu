@@ -278,7 +278,7 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
                 const float b = a.bias ? __ldg(a.bias + n) : 0.f;
 #pragma unroll
                 for (int m = 0; m < kSkMP; ++m)
-                    if (m < M) a.Y[(size_t)m * N + n] = f32_to_bf16_bits(epilogue<GELU>(v.x[m], b));
+                    if (m < M) a.Y[(size_t)m * N + n] = f32_to_bf16_bits(epilogue<GELU, true>(v.x[m], b));
             }
         } else {
             // Push this row's partial sums into the inbox of the CTA that finishes it,
@@ -303,7 +303,7 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
                 if (ok && m < M && n < N) {
                     const float acc = tree_of_ranks<CL>(inbox + m * COLS + c, kSkMP * COLS, 0);
                     const float b = a.bias ? __ldg(a.bias + n) : 0.f;
-                    a.Y[(size_t)m * N + n] = f32_to_bf16_bits(epilogue<GELU>(acc, b));
+                    a.Y[(size_t)m * N + n] = f32_to_bf16_bits(epilogue<GELU, true>(acc, b));
                 }
             }
         }

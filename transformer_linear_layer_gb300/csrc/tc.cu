@@ -288,10 +288,10 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 #pragma unroll
             for (int j4 = 0; j4 < 32; j4 += 4) {
                 const float4 b4 = *reinterpret_cast<const float4*>(sBias + c * 32 + j4);
-                v[j4 + 0] = epilogue<GELU>(__uint_as_float(r[j4 + 0]), b4.x);
-                v[j4 + 1] = epilogue<GELU>(__uint_as_float(r[j4 + 1]), b4.y);
-                v[j4 + 2] = epilogue<GELU>(__uint_as_float(r[j4 + 2]), b4.z);
-                v[j4 + 3] = epilogue<GELU>(__uint_as_float(r[j4 + 3]), b4.w);
+                v[j4 + 0] = epilogue<GELU, BF16>(__uint_as_float(r[j4 + 0]), b4.x);
+                v[j4 + 1] = epilogue<GELU, BF16>(__uint_as_float(r[j4 + 1]), b4.y);
+                v[j4 + 2] = epilogue<GELU, BF16>(__uint_as_float(r[j4 + 2]), b4.z);
+                v[j4 + 3] = epilogue<GELU, BF16>(__uint_as_float(r[j4 + 3]), b4.w);
             }
             const int mrow0 = m0 + q * 32;
             if constexpr (BF16) {
