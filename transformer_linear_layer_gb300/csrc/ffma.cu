@@ -11,9 +11,9 @@
 //   stores of a warp are consecutive columns.
 // * Shared-memory tiles keep the operands' K-contiguous layout (X is M x K, W
 //   is N x K), rows padded to an odd number of 16-byte chunks. A thread reads
-//   a float4 of four consecutive k for each of its rows and columns (rows in
-//   groups of four) and issues 16 FMAs per 128-bit read of B; each output still
-//   accumulates in ascending k.
+//   a float4 of four consecutive k for each of its rows, keeps them in
+//   registers, and streams its columns' float4s past them: 4 * TM FMAs per
+//   128-bit read of B. Each output still accumulates in ascending k.
 // * The K slices stream through a STAGES-deep ring filled with cp.async (16-byte
 //   copies that bypass registers, zero-filled past the tensor's edge), so the
 //   loads of later slices overlap the arithmetic of the current one - the
@@ -198,27 +198,23 @@ ffma_kernel(const FfmaArgs a) {
         cp_async_commit();
         const float* As = smem + (i % STAGES) * STAGE_FLOATS;
         const float* Bs = As + BM * LD;
-        // Rows in groups of RG (A operands held in registers), B reloaded per group:
-        // keeps a TM = 8 tile within 128 registers.
-        constexpr int RG = TM < 4 ? TM : 4;
+        // The A values of all TM rows for four consecutive k stay in registers
+        // while B's float4 for each column streams past (TM + TN 128-bit shared
+        // loads per 4 * TM * TN FMAs).
 #pragma unroll
         for (int kq = 0; kq < BK / 4; ++kq) {
+            float4 av[TM];
 #pragma unroll
-            for (int r0 = 0; r0 < TM; r0 += RG) {
-                float4 av[RG];
+            for (int r = 0; r < TM; ++r) av[r] = *reinterpret_cast<const float4*>(As + (ty + r * TY) * LD + 4 * kq);
 #pragma unroll
-                for (int r = 0; r < RG; ++r)
-                    av[r] = *reinterpret_cast<const float4*>(As + (ty + (r0 + r) * TY) * LD + 4 * kq);
+            for (int c = 0; c < TN; ++c) {
+                const float4 bv = *reinterpret_cast<const float4*>(Bs + (tx + c * TX) * LD + 4 * kq);
 #pragma unroll
-                for (int c = 0; c < TN; ++c) {
-                    const float4 bv = *reinterpret_cast<const float4*>(Bs + (tx + c * TX) * LD + 4 * kq);
-#pragma unroll
-                    for (int r = 0; r < RG; ++r) {
-                        acc[r0 + r][c] = fmaf(av[r].x, bv.x, acc[r0 + r][c]);
-                        acc[r0 + r][c] = fmaf(av[r].y, bv.y, acc[r0 + r][c]);
-                        acc[r0 + r][c] = fmaf(av[r].z, bv.z, acc[r0 + r][c]);
-                        acc[r0 + r][c] = fmaf(av[r].w, bv.w, acc[r0 + r][c]);
-                    }
+                for (int r = 0; r < TM; ++r) {
+                    acc[r][c] = fmaf(av[r].x, bv.x, acc[r][c]);
+                    acc[r][c] = fmaf(av[r].y, bv.y, acc[r][c]);
+                    acc[r][c] = fmaf(av[r].z, bv.z, acc[r][c]);
+                    acc[r][c] = fmaf(av[r].w, bv.w, acc[r][c]);
                 }
             }
         }
@@ -249,7 +245,7 @@ ffma_kernel(const FfmaArgs a) {
 template <int BM, int BN, int BK, int TM, int TN, int STAGES>
 int launch_cfg(const FfmaArgs& a, dim3 grid, cudaStream_t st, bool gelu) {
     constexpr size_t smem = ffma_smem_bytes<BM, BN, BK, STAGES>();
-    static_assert(smem <= 113 * 1024, "two CTAs per SM");
+    static_assert(smem <= 227 * 1024, "shared memory per CTA");
     const bool split = a.splits > 1;
     auto kern = gelu ? (split ? ffma_kernel<BM, BN, BK, TM, TN, STAGES, true, true>
                               : ffma_kernel<BM, BN, BK, TM, TN, STAGES, true, false>)
@@ -291,7 +287,7 @@ int launch_ffma(const Problem& p, const lin_plan& plan) {
     const dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
     const bool gelu = p.epilogue == LIN_EPI_GELU_TANH;
     switch (plan.variant) {
-        case 0: return launch_cfg<kFfmaCfg[0].bm, kFfmaCfg[0].bn, kFfmaCfg[0].bk, kFfmaCfg[0].tm, kFfmaCfg[0].tn, 3>(
+        case 0: return launch_cfg<kFfmaCfg[0].bm, kFfmaCfg[0].bn, kFfmaCfg[0].bk, kFfmaCfg[0].tm, kFfmaCfg[0].tn, 4>(
             a, grid, p.stream, gelu);
         case 1: return launch_cfg<kFfmaCfg[1].bm, kFfmaCfg[1].bn, kFfmaCfg[1].bk, kFfmaCfg[1].tm, kFfmaCfg[1].tn, 4>(
             a, grid, p.stream, gelu);
