@@ -153,7 +153,11 @@ LIN_API int lin_plan_query(int sm_count, int M, int N, int K, int precision, int
 
 /* Fill *out with the default plan of a kernel family for a shape (host only),
  * for sweeps: kernel = lin_kernel, variant = tile configuration, splits = 0
- * lets the table choose the split. Returns LIN_ERR_UNSUPPORTED when the
+ * lets the table choose the split. For LIN_KERNEL_TC, splits counts CTAs
+ * instead: >= 0 CTAs walking whole tiles (0 = one per SM); -1 stream-K with
+ * one CTA per SM; -c (c >= 2) stream-K with c CTAs (single-CTA variants, at
+ * least one tile per CTA; the plan's splits is then 2 and it needs workspace
+ * for one 128 x BN fp32 slot per CTA). Returns LIN_ERR_UNSUPPORTED when the
  * kernel cannot run the shape. */
 LIN_API int lin_plan_make(int sm_count, int kernel, int variant, int splits, int M, int N, int K,
                   int precision, lin_plan* out);

@@ -144,3 +144,19 @@ def test_plan_make_families():
         tll.plan_make(SM, tll.KERNEL_TC, 6, 0, 256, 256, 256, "tf32")
     p = tll.plan_make(SM, tll.KERNEL_FFMA, 1, 7, 128, 768, 768, "fp32")
     assert p.grid_z == 7 and p.workspace_bytes >= 7 * 128 * 768 * 4
+
+
+def test_plan_make_stream_k():
+    """TC stream-K plans: splits = 2, one workspace slot per CTA, single-CTA
+    variants only, at least one tile per CTA; never the default."""
+    p = tll.plan_make(SM, tll.KERNEL_TC, 0, -1, 8192, 768, 768, "bf16")
+    assert p.splits == 2 and p.grid_x == SM
+    assert p.workspace_bytes >= SM * 128 * 256 * 4
+    p = tll.plan_make(SM, tll.KERNEL_TC, 2, -5, 384, 640, 768, "tf32")
+    assert p.splits == 2 and p.grid_x == 5 and p.bn == 192
+    with pytest.raises(tll.LinError):   # SM pair
+        tll.plan_make(SM, tll.KERNEL_TC, 3, -1, 8192, 768, 768, "bf16")
+    p = tll.plan_make(SM, tll.KERNEL_TC, 0, -10, 384, 640, 768, "bf16")
+    assert p.splits == 2 and p.grid_x == 9      # no more CTAs than the 3 x 3 tiles
+    for M, N, K in ((8192, 768, 768), (8192, 2304, 768), (8192, 3072, 768), (8192, 768, 3072)):
+        assert tll.plan_query(SM, M, N, K, "bf16").splits == 1

@@ -11,7 +11,7 @@ import torch
 import oracle
 import synthetic_inputs as si
 import transformer_linear_layer_gb300 as tll
-from gpu_util import PREC_NAME, check_layer, check_layer_sampled, device_inputs, run
+from gpu_util import PREC_NAME, check_layer, check_layer_sampled, device_inputs, run, sample_indices
 
 pytestmark = pytest.mark.gpu
 
@@ -35,6 +35,12 @@ def all_plans(ctx, M, N, K, precision):
         for v in range(6):  # 3-5: SM pairs (2-CTA clusters, cta_group::2 MMAs on 256-row tiles)
             for width in (0, 1, 3):  # persistent CTAs: one per SM, or few CTAs walking many tiles
                 plans.append(tll.plan_make(sm, tll.KERNEL_TC, v, width, M, N, K, PREC_NAME[precision]))
+        for v in range(3):  # stream-K with few CTAs, so that tiles are cut between CTAs
+            for ctas in (2, 3, 5):
+                try:
+                    plans.append(tll.plan_make(sm, tll.KERNEL_TC, v, -ctas, M, N, K, PREC_NAME[precision]))
+                except tll.LinError:  # fewer tiles than CTAs: no stream-K plan
+                    pass
     if precision == FP32:
         for v in range(2):
             for s in (1, 0, 3):
@@ -284,6 +290,69 @@ def test_back_to_back_calls_chain_through_outputs(ctx, M):
     y3_ref = tll.forward(x0, w, bsrc[1].clone(), precision="bf16")
     torch.cuda.synchronize()
     assert torch.equal(y3, y3_ref)
+
+
+@pytest.mark.parametrize("precision", [BF16, TF32])
+def test_stream_k_cut_tiles(ctx, precision):
+    """Stream-K plans whose shares cut tiles at every kind of place (within
+    the first, middle and last K stages, one K stage, ragged K) against the
+    oracle, full comparison; and bitwise repeatable."""
+    for M, N, K, ctas in [(384, 640, 768, 4), (384, 640, 768, 7), (257, 1000, 320, 5), (256, 512, 136, 3),
+                          (640, 256, 1024, 4)]:
+        layer = si.Layer("sk", M, N, K, precision, si.EPI_GELU, bias=True)
+        X, W, b = si.make_inputs(layer)
+        ref = oracle.linear(X, W, b, True)
+        for v in range(3):
+            try:
+                plan = tll.plan_make(ctx.sm_count, tll.KERNEL_TC, v, -ctas, M, N, K, PREC_NAME[precision])
+            except tll.LinError:
+                continue
+            assert plan.splits == 2
+            y = run(X, W, b, precision, epilogue=si.EPI_GELU, plan=plan, ctx=ctx)
+            assert oracle.rel_err(y, ref) <= oracle.TOL[precision], (M, N, K, ctas, v)
+            y2 = run(X, W, b, precision, epilogue=si.EPI_GELU, plan=plan, ctx=ctx)
+            assert np.array_equal(y, y2)
+
+
+def test_stream_k_back_to_back(ctx):
+    """Stream-K calls launched back to back overlap on the GPU (the early
+    start) and share the workspace slots and flags: independent calls into
+    separate outputs, and a chain X = previous Y, must equal the same calls
+    made one at a time."""
+    M, N, K = 2560, 2048, 2048   # 20 x 8 tiles of 128 x 256: at least one per SM
+    plan = tll.plan_make(ctx.sm_count, tll.KERNEL_TC, 0, -1, M, N, K, "bf16")
+    assert plan.splits == 2
+    X0, _, b = si.make_inputs(si.Layer("skb2b", M, N, K, BF16, bias=True))
+    x0 = torch.from_numpy(X0).cuda().to(torch.bfloat16)
+    bias = torch.from_numpy(b).cuda()
+    ws = [torch.from_numpy(si.round_bf16(si.normal(40 + i, 2, (N, K), 0.0, 0.02))).to(torch.bfloat16).cuda()
+          for i in range(3)]
+
+    def call(x, w):
+        return tll.forward_plan(plan, x, w, bias, precision="bf16", ctx=ctx)
+
+    outs = [call(x0, ws[i % 3]) for i in range(8)]
+    torch.cuda.synchronize()
+    for i in range(8):
+        ref = call(x0, ws[i % 3])
+        torch.cuda.synchronize()
+        assert torch.equal(outs[i], ref), i
+    chain = [x0]
+    for i in range(5):
+        chain.append(call(chain[-1], ws[i % 3]))
+    torch.cuda.synchronize()
+    ref = x0
+    for i in range(5):
+        ref = call(ref, ws[i % 3])
+        torch.cuda.synchronize()
+        assert torch.equal(ref, chain[i + 1]), i
+    ctx.check()
+    # and against the oracle on sampled outputs
+    ms, ns = sample_indices(M, N, 512)
+    got = outs[0][torch.from_numpy(ms).cuda(), torch.from_numpy(ns).cuda()].float().cpu().numpy().astype(np.float64)
+    W0 = ws[0].float().cpu().numpy()
+    refv = oracle.linear_entries(X0, W0, ms, ns, b, False)
+    assert oracle.rel_err(got, refv) <= oracle.TOL[BF16]
 
 
 @pytest.mark.parametrize("K", [4096, 4104, 384, 200])

@@ -60,6 +60,14 @@ constexpr int kTcVariants = 6;                     // pair: 2 x 1 clusters, SM-p
 constexpr TcCfg kTcCfg[kTcVariants] = {{256, false}, {128, false}, {192, false},
                                        {256, true}, {128, true}, {192, true}};
 constexpr int kTcThreads = 320;                    // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
+// Stream-K hand-over flags of the tcgen05 kernel: 8 per CTA boundary, in the
+// counter block from this index on (zero between launches: the reader clears
+// them). TC plans: splits = 1 whole tiles per CTA, 2 = stream-K.
+constexpr int kTcFlagBase = 8192;
+constexpr int kTcMaxStreamKCtas = (int)(kCounterBytes / sizeof(unsigned) - kTcFlagBase) / 8;
+inline size_t tc_streamk_workspace_bytes(int ctas, int bn) {
+    return kCounterBytes + align_up((size_t)ctas * 128 * (size_t)bn * sizeof(float), 256);
+}
 
 // Launchers (return LIN_OK or LIN_ERR_*). They assume the plan was validated.
 int launch_fill(const Problem& p);

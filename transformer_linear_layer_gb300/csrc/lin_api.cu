@@ -119,20 +119,27 @@ int make_ffma(int sm, int variant, int splits, int M, int N, int K, size_t ws, l
 // Persistent tcgen05 kernel: `width` CTAs walk the 128 x BN output tiles
 // (0 = one CTA per SM) in static round robin; pair variants walk 256 x BN
 // tiles with one 2-CTA cluster (an SM pair) per tile (grid rounded down to
-// even). Default, from the measured M = 8192 GPT-2 shapes, the LM head and
+// even). `stream_k` (single-CTA variants, at least one tile per CTA): every CTA
+// takes an equal share of the (tile, K stage) sequence instead (splits = 2).
+// Default, from the measured M = 8192 GPT-2 shapes, the LM head and
 // 4096^3 / 8192^3:
 // * SM pair when each tile runs at least 64 K stages (K >= 4096 bf16 or 2048
 //   tf32): there the pair's lighter shared-memory traffic wins (8192^3 bf16
 //   1.91 vs 1.62 PF/s); with shorter K its per-tile synchronisation costs
 //   more than it saves.
-// * N tile: the smallest rounds_eff(BN) x r(BN), where rounds_eff is the
-//   mean of the average and the maximum tiles per CTA (a back-to-back caller
-//   overlaps part of a ragged last round with its next call) and r = 1, 0.9,
-//   0.75 for BN = 256, 192, 128 is the measured time of one round relative to
-//   BN = 256 (A is reloaded for every N tile, so narrow tiles are slower per
-//   column).
-int make_tc(int sm, int variant, int width, int M, int N, int K, int esz, lin_plan* p) {
+// * Otherwise whole single-CTA tiles, the N tile minimising rounds_eff(BN) x
+//   r(BN), where rounds_eff is the mean of the average and the maximum tiles
+//   per CTA (a back-to-back caller overlaps part of a ragged last round with
+//   its next call) and r = 1, 0.9, 0.75 for BN = 256, 192, 128 is the measured
+//   time of one round relative to BN = 256 (A is reloaded for every N tile, so
+//   narrow tiles are slower per column).
+// * Never stream-K by default: on the M = 8192 GPT-2 shapes it measured slower
+//   than whole tiles both back to back (where the SMs that a ragged last round
+//   frees start the next call early) and with the early start off (the cut
+//   tiles' hand-over sits on the critical path). Explicit plans reach it.
+int make_tc(int sm, int variant, int width, bool stream_k, int M, int N, int K, int esz, lin_plan* p) {
     if (M < 1 || N < 1 || K < 1 || width < 0) return LIN_ERR_UNSUPPORTED;
+    const long long w0 = width > 0 ? width : sm;
     if (variant < 0) {
         const bool want_pair = ceil_div(K, 128 / esz) >= 64;
         double best = 0.0;
@@ -141,7 +148,7 @@ int make_tc(int sm, int variant, int width, int M, int N, int K, int esz, lin_pl
             const int bn = kTcCfg[v].bn;
             const long long items =
                 (long long)(want_pair ? ceil_div(ceil_div(M, 128), 2) : ceil_div(M, 128)) * ceil_div(N, bn);
-            long long slots = width > 0 ? width : sm;
+            long long slots = w0;
             if (want_pair) slots = slots / 2 > 0 ? slots / 2 : 1;
             const double avg = (double)items / (double)slots;
             const double mx = (double)((items + slots - 1) / slots);
@@ -157,22 +164,26 @@ int make_tc(int sm, int variant, int width, int M, int N, int K, int esz, lin_pl
     const bool pair = kTcCfg[variant].pair;
     const long long items = (long long)(pair ? ceil_div(ceil_div(M, 128), 2) : ceil_div(M, 128)) *
                             ceil_div(N, kTcCfg[variant].bn);
-    long long w = width > 0 ? width : sm;
+    long long w = w0;
     if (pair) {
+        if (stream_k) return LIN_ERR_UNSUPPORTED;
         w = (w / 2 < items ? w / 2 : items) * 2;
         if (w < 2) w = 2;
     } else if (w > items) {
         w = items;
     }
+    if (stream_k && (items < w || w > kTcMaxStreamKCtas)) return LIN_ERR_UNSUPPORTED;
     plan_common(p, LIN_KERNEL_TC, variant);
     p->bm = 128;
     p->bn = kTcCfg[variant].bn;
     p->bk = 0;  // 128 bytes of K: 64 bf16 or 32 fp32
+    p->splits = stream_k ? 2 : 1;
     p->stages = 0;  // derived in the kernel from the shared-memory budget
     p->grid_x = (int)w;
     p->grid_y = 1;
     p->grid_z = 1;
     p->threads = kTcThreads;
+    p->workspace_bytes = stream_k ? (long long)tc_streamk_workspace_bytes((int)w, p->bn) : 0;
     return LIN_OK;
 }
 
@@ -196,9 +207,9 @@ int plan_default(int sm, int M, int N, int K, int precision, size_t ws, lin_plan
     switch (precision) {
         case LIN_PREC_BF16:
             if (M <= 16) return make_skinny(sm, 0, 0, M, N, K, ws, p);
-            return make_tc(sm, -1, 0, M, N, K, 2, p);
+            return make_tc(sm, -1, 0, false, M, N, K, 2, p);
         case LIN_PREC_TF32:
-            return make_tc(sm, -1, 0, M, N, K, 4, p);
+            return make_tc(sm, -1, 0, false, M, N, K, 4, p);
         default:
             return make_ffma(sm, -1, 0, M, N, K, ws, p);
     }
@@ -296,13 +307,18 @@ int check_plan_fits(const lin_plan& p, int M, int N, int K, int precision) {
         }
         case LIN_KERNEL_TC: {
             if (precision == LIN_PREC_FP32 || K == 0) return LIN_ERR_UNSUPPORTED;
-            if (p.variant < 0 || p.variant >= kTcVariants || p.splits != 1) return LIN_ERR_UNSUPPORTED;
+            if (p.variant < 0 || p.variant >= kTcVariants || (p.splits != 1 && p.splits != 2))
+                return LIN_ERR_UNSUPPORTED;
             const bool pair = kTcCfg[p.variant].pair;
             const long long items = (long long)(pair ? ceil_div(ceil_div(M, 128), 2) : ceil_div(M, 128)) *
                                     ceil_div(N, kTcCfg[p.variant].bn);
             const long long ctas = pair ? 2 * items : items;
             if (p.bn != kTcCfg[p.variant].bn || p.grid_x < 1 || p.grid_x > ctas || p.grid_y != 1 ||
                 (pair && p.grid_x % 2 != 0))
+                return LIN_ERR_UNSUPPORTED;
+            if (p.splits == 2 &&
+                (pair || p.grid_x > kTcMaxStreamKCtas ||
+                 p.workspace_bytes < (long long)tc_streamk_workspace_bytes(p.grid_x, p.bn)))
                 return LIN_ERR_UNSUPPORTED;
             return LIN_OK;
         }
@@ -490,8 +506,10 @@ int lin_plan_make(int sm_count, int kernel, int variant, int splits, int M, int 
             return lin::make_ffma(sm_count, variant, splits, M, N, K, unlimited, out);
         case LIN_KERNEL_TC:
             if (precision == LIN_PREC_FP32) return LIN_ERR_UNSUPPORTED;
-            // splits = CTAs (0 = one per SM)
-            return lin::make_tc(sm_count, variant, splits, M, N, K, precision == LIN_PREC_BF16 ? 2 : 4, out);
+            // splits >= 0: CTAs walking whole tiles (0 = one per SM); -1: stream-K with
+            // one CTA per SM; -c (c >= 2): stream-K with c CTAs.
+            return lin::make_tc(sm_count, variant, splits >= 0 ? splits : (splits == -1 ? 0 : -splits), splits < 0,
+                                M, N, K, precision == LIN_PREC_BF16 ? 2 : 4, out);
         case LIN_KERNEL_NONE:
         case LIN_KERNEL_FILL:
             return lin::plan_default(sm_count, M, N, K, precision, unlimited, out);

@@ -48,6 +48,8 @@ struct TcArgs {
     int bias_aligned16;  // bias is 16-byte aligned (vector loads allowed)
     int early_inputs;    // X and W may be read before the dependency wait (not the previous call's output)
     int y_tma;           // bf16 Y stored by TMA from 32 x 32 boxes (16-byte aligned rows)
+    float* partials;     // stream-K: one 128 x BN fp32 slot per CTA boundary
+    unsigned* flags;     // stream-K: 8 hand-over flags per CTA boundary (zero between launches)
 };
 
 // Epilogue staging: each epilogue warp owns a 32 x 32 output tile in shared
@@ -92,7 +94,17 @@ constexpr size_t tc_smem_bytes() {
 // Both CTAs' copies complete the even CTA's "full" barrier; its commits
 // release the stage ("empty") and publish the accumulator ("tfull") in both
 // CTAs; both CTAs' epilogue warps release the accumulator to its "tempty".
-template <bool BF16, int BN, bool GELU, bool PAIR>
+//
+// SK: stream-K schedule (single-CTA tiles only). The grid's work is the
+// tile-major sequence of (tile, K stage) units; CTA b takes the equal share
+// [b * U / G, (b + 1) * U / G), so every SM finishes at the same time however
+// the tile count divides the grid. Each share holds at least one tile, so a
+// tile is cut at most once, between CTAs b and b + 1: CTA b + 1 computes the
+// later K stages first, writes them to the workspace slot of that boundary and
+// sets one flag per epilogue warp; CTA b reaches the earlier K stages last,
+// waits for the flags, adds the partial sums to its accumulator in that fixed
+// order and runs the epilogue (deterministic for a given plan).
+template <bool BF16, int BN, bool GELU, bool PAIR, bool SK>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
           const __grid_constant__ CUtensorMap tmY, const TcArgs a) {
@@ -112,6 +124,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     constexpr int HALF = BN / 2;                  // columns per epilogue warp
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "N tile");
     static_assert(EPI_WARPS == 8, "8 epilogue warps");
+    static_assert(!(PAIR && SK), "stream-K runs single-CTA tiles");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -136,6 +149,28 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     auto tile_m0 = [&](int item) { return (PAIR ? 2 * (item % mu) + (int)rank : item % mu) * BM; };
     auto tile_n0 = [&](int item) { return (item / mu) * BN; };
     const int nkb = (a.K + BK - 1) / BK;
+    // This CTA's work as segments (tile, K stages [lo, hi)): whole tiles
+    // first_item, first_item + item_step, ... or, for SK, its share of units.
+    const long long units = (long long)ntiles * nkb;
+    const long long u0 = SK ? (long long)blockIdx.x * units / gridDim.x : 0;
+    const long long u1 = SK ? (long long)(blockIdx.x + 1) * units / gridDim.x : 0;
+    auto seg = [&](int j, int& tile, int& lo, int& hi) -> bool {
+        if constexpr (SK) {
+            const long long t = u0 / nkb + j;
+            const long long st = j == 0 ? u0 : t * nkb;
+            if (st >= u1) return false;
+            const long long en = u1 < (t + 1) * nkb ? u1 : (t + 1) * nkb;
+            tile = (int)t;
+            lo = (int)(st - t * nkb);
+            hi = (int)(en - t * nkb);
+            return true;
+        } else {
+            tile = first_item + j * item_step;
+            lo = 0;
+            hi = nkb;
+            return tile < ntiles;
+        }
+    };
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
     const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
 
@@ -179,9 +214,10 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             if (!a.early_inputs) pdl_wait();
             uint32_t it = 0, issued = 0;
             bool ok = true;
-            for (int tile = first_item; tile < ntiles && ok; tile += item_step) {
+            int tile, lo, hi;
+            for (int j = 0; ok && seg(j, tile, lo, hi); ++j) {
                 const int m0 = tile_m0(tile), n0 = tile_n0(tile);
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                for (int kb = lo; kb < hi; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                     if (*(volatile int*)s_abort || !mbar_wait(empty0 + 8 * s, ph ^ 1)) {
                         give_up();
@@ -213,9 +249,9 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         if (lane == 0 && leader) {
             // ---- MMA issuer: accumulators alternate between two TMEM buffers ----
             uint32_t it = 0;
-            int j = 0;
+            int j = 0, tile, lo, hi;
             bool ok = true;
-            for (int tile = first_item; tile < ntiles && ok; tile += item_step, ++j) {
+            for (; ok && seg(j, tile, lo, hi); ++j) {
                 const uint32_t buf = j & 1;
                 const bool freed = PAIR ? mbar_wait_cluster(tempty0 + 8 * buf, ((j >> 1) & 1) ^ 1)
                                         : mbar_wait(tempty0 + 8 * buf, ((j >> 1) & 1) ^ 1);
@@ -225,7 +261,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + buf * BUF_COLS;
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                for (int kb = lo; kb < hi; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                     if (*(volatile int*)s_abort || !mbar_wait(full0 + 8 * s, ph)) {
                         give_up();
@@ -238,12 +274,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     if constexpr (PAIR) {
 #pragma unroll
                         for (int kk = 0; kk < MMAS; ++kk)
-                            tc_mma_pair<BF16>(d, ad + 2u * kk, bd + 2u * kk, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                            tc_mma_pair<BF16>(d, ad + 2u * kk, bd + 2u * kk, IDESC, (kb != lo || kk != 0) ? 1u : 0u);
                         tc_commit_pair_mc(empty0 + 8 * s, (uint16_t)0x3);
                     } else {
 #pragma unroll
                         for (int kk = 0; kk < MMAS; ++kk)
-                            tc_mma<BF16>(d, ad + 2u * kk, bd + 2u * kk, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                            tc_mma<BF16>(d, ad + 2u * kk, bd + 2u * kk, IDESC, (kb != lo || kk != 0) ? 1u : 0u);
                         tc_commit(empty0 + 8 * s);
                     }
                 }
@@ -383,10 +419,28 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 mbar_arrive(tempty0 + 8 * buf);
         };
 
-        int j = 0;
-        for (int tile = first_item; tile < ntiles; tile += item_step, ++j) {
+        // Stream-K hand-over: this warp's region of a boundary slot, laid out
+        // [chunk][column][row] so that lane = row accesses are coalesced.
+        auto part_ptr = [&](int boundary) {
+            return a.partials + (size_t)boundary * (BM * BN) + (size_t)ew * (CH * 1024);
+        };
+        auto store_part = [&](const uint32_t (&r)[32], int c) {
+            float* dst = part_ptr(blockIdx.x) + c * 1024 + lane;
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) __stcg(dst + jj * 32, __uint_as_float(r[jj]));
+        };
+        auto add_part = [&](uint32_t (&r)[32], int c) {
+            const float* src = part_ptr(blockIdx.x + 1) + c * 1024 + lane;
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) r[jj] = __float_as_uint(__uint_as_float(r[jj]) + __ldcg(src + jj * 32));
+        };
+
+        int j = 0, tile, lo, hi;
+        for (; seg(j, tile, lo, hi); ++j) {
             const uint32_t buf = j & 1;
             const int m0 = tile_m0(tile), n0 = tile_n0(tile);
+            const bool part_out = SK && lo > 0;            // later K stages of a cut tile: hand over
+            const bool part_in = SK && lo == 0 && hi < nkb;  // earlier K stages: add the partner's, finish
             // This warp's bias columns of the tile, fetched while the MMAs run.
 #pragma unroll
             for (int t = lane; t < HALF; t += 32) {
@@ -400,7 +454,15 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             tc_fence_after();
             // tcgen05.ld is warp-collective: a warp proceeds only if every lane saw
             // the accumulator complete and no role of this CTA gave up.
-            const bool ok = __all_sync(0xffffffffu, mine && *(volatile int*)s_abort == 0);
+            bool ok = __all_sync(0xffffffffu, mine && *(volatile int*)s_abort == 0);
+            unsigned* flag = SK ? a.flags + (size_t)(blockIdx.x + (part_in ? 1 : 0)) * 8 + ew : nullptr;
+            if (SK && part_in && ok) {
+                // The partner (the next CTA) computed the later K stages first.
+                bool got = lane == 0 ? wait_flag_set(flag) : true;
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (!got) give_up();
+                ok = got && ld_acquire_gpu(flag) != 0u;
+            }
             const uint32_t tbase =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BUF_COLS + static_cast<uint32_t>(c_begin);
             bool released = false;
@@ -420,8 +482,30 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     if (lane == 0) release_acc(buf);
                     released = true;
                 }
+                if constexpr (SK) {
+                    if (part_out) {
+                        store_part(r0, c);
+                        if (two) store_part(r1, c + 1);
+                        continue;
+                    }
+                    if (part_in) {
+                        add_part(r0, c);
+                        if (two) add_part(r1, c + 1);
+                    }
+                }
                 emit(r0, c, m0, n0);
                 if (two) emit(r1, c + 1, m0, n0);
+            }
+            if constexpr (SK) {
+                if (part_out && ok) {
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) st_release_gpu(flag, 1u);
+                }
+                if (part_in && ok) {
+                    __syncwarp();
+                    if (lane == 0) *flag = 0u;  // re-armed for the next launch
+                }
             }
             if (!released) {
                 tc_fence_before();
@@ -454,12 +538,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 
 // ---------------------------------------------------------------- host side
 
-template <bool BF16, int BN, bool GELU, bool PAIR>
+template <bool BF16, int BN, bool GELU, bool PAIR, bool SK>
 int launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const TcArgs& a, int grid, bool early,
                cudaStream_t st) {
     constexpr size_t smem = tc_smem_bytes<BF16, BN, PAIR>();
     static_assert(tc_smem_bytes<BF16, BN, PAIR>() <= 227 * 1024, "shared memory");
-    auto kern = tc_kernel<BF16, BN, GELU, PAIR>;
+    auto kern = tc_kernel<BF16, BN, GELU, PAIR, SK>;
     static unsigned long long attr_set = 0;  // one attribute call per instantiation and device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return LIN_ERR_CUDA;
@@ -495,15 +579,23 @@ int launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& 
 }
 
 template <bool BF16, bool GELU>
-int launch_variant(int variant, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const TcArgs& a, int grid,
-                   bool early, cudaStream_t st) {
+int launch_variant(int variant, bool sk, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty,
+                   const TcArgs& a, int grid, bool early, cudaStream_t st) {
+    if (sk) {
+        switch (variant) {
+            case 0: return launch_cfg<BF16, kTcCfg[0].bn, GELU, false, true>(ta, tb, ty, a, grid, early, st);
+            case 1: return launch_cfg<BF16, kTcCfg[1].bn, GELU, false, true>(ta, tb, ty, a, grid, early, st);
+            case 2: return launch_cfg<BF16, kTcCfg[2].bn, GELU, false, true>(ta, tb, ty, a, grid, early, st);
+            default: return LIN_ERR_UNSUPPORTED;
+        }
+    }
     switch (variant) {
-        case 0: return launch_cfg<BF16, kTcCfg[0].bn, GELU, false>(ta, tb, ty, a, grid, early, st);
-        case 1: return launch_cfg<BF16, kTcCfg[1].bn, GELU, false>(ta, tb, ty, a, grid, early, st);
-        case 2: return launch_cfg<BF16, kTcCfg[2].bn, GELU, false>(ta, tb, ty, a, grid, early, st);
-        case 3: return launch_cfg<BF16, kTcCfg[3].bn, GELU, true>(ta, tb, ty, a, grid, early, st);
-        case 4: return launch_cfg<BF16, kTcCfg[4].bn, GELU, true>(ta, tb, ty, a, grid, early, st);
-        case 5: return launch_cfg<BF16, kTcCfg[5].bn, GELU, true>(ta, tb, ty, a, grid, early, st);
+        case 0: return launch_cfg<BF16, kTcCfg[0].bn, GELU, false, false>(ta, tb, ty, a, grid, early, st);
+        case 1: return launch_cfg<BF16, kTcCfg[1].bn, GELU, false, false>(ta, tb, ty, a, grid, early, st);
+        case 2: return launch_cfg<BF16, kTcCfg[2].bn, GELU, false, false>(ta, tb, ty, a, grid, early, st);
+        case 3: return launch_cfg<BF16, kTcCfg[3].bn, GELU, true, false>(ta, tb, ty, a, grid, early, st);
+        case 4: return launch_cfg<BF16, kTcCfg[4].bn, GELU, true, false>(ta, tb, ty, a, grid, early, st);
+        case 5: return launch_cfg<BF16, kTcCfg[5].bn, GELU, true, false>(ta, tb, ty, a, grid, early, st);
         default: return LIN_ERR_UNSUPPORTED;
     }
 }
@@ -572,6 +664,14 @@ int launch_tc(const Problem& p, const lin_plan& plan) {
     a.y_aligned16 = (reinterpret_cast<uintptr_t>(p.Y) % 16) == 0;
     a.bias_aligned16 = (reinterpret_cast<uintptr_t>(p.bias) % 16) == 0;
     a.early_inputs = (p.early_start && p.early_x) ? 1 : 0;
+    const bool sk = plan.splits == 2;
+    // Stream-K CTAs wait for their successor's hand-over, so all of them must
+    // be resident at once: at most one per SM.
+    if (sk && (pair || plan.grid_x > kTcMaxStreamKCtas || plan.grid_x > p.sm_count ||
+               p.workspace_bytes < tc_streamk_workspace_bytes(plan.grid_x, plan.bn)))
+        return LIN_ERR_UNSUPPORTED;
+    a.partials = sk ? splitk_partials(p.workspace) : nullptr;
+    a.flags = sk ? splitk_counters(p.workspace) + kTcFlagBase : nullptr;
     // bf16 rows 16-byte aligned: Y leaves by TMA store; otherwise (odd N, as in
     // the LM head) through the staged row-segment stores. The fallback map is a
     // placeholder the kernel never uses.
@@ -590,10 +690,10 @@ int launch_tc(const Problem& p, const lin_plan& plan) {
     // kernel waits before its first load unless the inputs are independent.
     const bool early = p.early_start;
     if (bf16)
-        return gelu ? launch_variant<true, true>(plan.variant, ta, tb, ty, a, grid, early, p.stream)
-                    : launch_variant<true, false>(plan.variant, ta, tb, ty, a, grid, early, p.stream);
-    return gelu ? launch_variant<false, true>(plan.variant, ta, tb, ty, a, grid, early, p.stream)
-                : launch_variant<false, false>(plan.variant, ta, tb, ty, a, grid, early, p.stream);
+        return gelu ? launch_variant<true, true>(plan.variant, sk, ta, tb, ty, a, grid, early, p.stream)
+                    : launch_variant<true, false>(plan.variant, sk, ta, tb, ty, a, grid, early, p.stream);
+    return gelu ? launch_variant<false, true>(plan.variant, sk, ta, tb, ty, a, grid, early, p.stream)
+                : launch_variant<false, false>(plan.variant, sk, ta, tb, ty, a, grid, early, p.stream);
 }
 
 }  // namespace lin

@@ -336,6 +336,26 @@ __device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
     return v;
 }
 
+// ---- flags in global memory (hand-over between CTAs of one grid) ----
+__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Bounded wait until *p is non-zero; false = gave up.
+__device__ __forceinline__ bool wait_flag_set(const unsigned* p) {
+    if (ld_acquire_gpu(p) != 0u) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t i = 1; i < kWaitIters; ++i) {
+        if (ld_acquire_gpu(p) != 0u) return true;
+        if ((i & 255u) == 0u && global_ns() - t0 > kWaitNs) return false;
+    }
+    return false;
+}
+
 // ---- programmatic dependent launch ----
 // Wait until the grids this launch depends on have completed and their memory
 // is visible (a no-op when launched without the programmatic attribute).
