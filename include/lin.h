@@ -198,7 +198,7 @@ LIN_API const char* lin_strerror(int status);
 LIN_API int lin_abi_version(void);
 
 /* Size of the fixed device array behind lin_forward_fp32_static. */
-#define LIN_STATIC_SCRATCH_BYTES (4u << 20)
+#define LIN_STATIC_SCRATCH_BYTES (8u << 20)
 
 /* The pages have no counterpart to this entry point; it exists for callers
  * that cannot allocate device memory when they run the layer, for example:
@@ -209,7 +209,7 @@ LIN_API int lin_abi_version(void);
  * Y = act(X . W^T + bias) in fp32 on the CURRENT device, with the same FFMA
  * kernel and split-K choice as lin_forward(..., LIN_PREC_FP32, ...), but with
  * no context. It calls no cudaMalloc or cudaFree: the split-K counters and
- * partial sums live in one fixed array of LIN_STATIC_SCRATCH_BYTES (4 MiB),
+ * partial sums live in one fixed array of LIN_STATIC_SCRATCH_BYTES (8 MiB),
  * a static device variable of this library that every GPU which loads the
  * library holds until the process exits. Arguments, layouts and alignment
  * rules are those of lin_forward; X, W, bias and Y are caller-owned device

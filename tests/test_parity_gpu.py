@@ -355,6 +355,40 @@ def test_stream_k_back_to_back(ctx):
     assert oracle.rel_err(got, refv) <= oracle.TOL[BF16]
 
 
+@pytest.mark.parametrize("N,K", [(768, 768), (768, 3072)])
+def test_ffma_back_to_back(ctx, N, K):
+    """fp32 split-K calls launched back to back (the early start) share the
+    workspace partial sums and tile counters: independent calls into separate
+    outputs, and a chain X = previous Y (N = K), must equal the same calls made
+    one at a time."""
+    M = 128
+    plan = ctx.plan(M, N, K, "fp32")
+    assert plan.splits > 1
+    X0, _, b = si.make_inputs(si.Layer("ffb2b", M, N, K, FP32, bias=True))
+    x0 = torch.from_numpy(X0).cuda()
+    bias = torch.from_numpy(b).cuda()
+    ws = [torch.from_numpy(si.normal(60 + i, 2, (N, K), 0.0, 0.02)).cuda() for i in range(3)]
+    outs = [tll.forward(x0, ws[i % 3], bias, precision="fp32") for i in range(8)]
+    torch.cuda.synchronize()
+    for i in range(8):
+        ref = tll.forward(x0, ws[i % 3], bias, precision="fp32")
+        torch.cuda.synchronize()
+        assert torch.equal(outs[i], ref), i
+    if N == K:
+        chain = [x0]
+        for i in range(5):
+            chain.append(tll.forward(chain[-1], ws[i % 3], bias, epilogue="gelu", precision="fp32"))
+        torch.cuda.synchronize()
+        ref = x0
+        for i in range(5):
+            ref = tll.forward(ref, ws[i % 3], bias, epilogue="gelu", precision="fp32")
+            torch.cuda.synchronize()
+            assert torch.equal(ref, chain[i + 1]), i
+    ctx.check()
+    refv = oracle.linear(X0, ws[0].cpu().numpy(), b)
+    assert oracle.rel_err(outs[0].cpu().numpy().astype(np.float64), refv) <= oracle.TOL[FP32]
+
+
 @pytest.mark.parametrize("K", [4096, 4104, 384, 200])
 def test_skinny_bits_independent_of_split(ctx, K):
     """The cluster split only changes who adds which K segments, never the

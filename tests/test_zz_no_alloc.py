@@ -54,18 +54,22 @@ def test_gpt2_shapes_exercise_the_split():
     sm = torch.cuda.get_device_properties(0).multi_processor_count
     for layer in si.GPT2_M128_FP32:
         p = tll.plan_query(sm, layer.M, layer.N, layer.K, "fp32", workspace_bytes=1 << 62)
-        assert p.splits > 1 and 0 < p.workspace_bytes <= 4 << 20
+        assert p.splits > 1 and 0 < p.workspace_bytes <= 8 << 20
 
 
 def test_static_scratch_refuses_oversized_split():
+    """On a device whose dispatch table splits this shape beyond the array
+    (the split fills two 64x64 CTAs per SM, so its scratch grows with the SM
+    count: ~5 MB at 152 SMs), nothing is launched and LIN_ERR_WORKSPACE comes
+    back."""
     lib = tll.library()
-    M, N, K = 64, 64 * 151, 256  # 151 tiles of 64x64 -> split 2 -> ~4.9 MB of partial sums
+    M, N, K = 64, 64 * 151, 256
     sm = torch.cuda.get_device_properties(0).multi_processor_count
     need = tll.plan_query(sm, M, N, K, "fp32", workspace_bytes=1 << 62).workspace_bytes
     x = torch.zeros((M, K), device="cuda")
     w = torch.zeros((N, K), device="cuda")
     y = torch.zeros((M, N), device="cuda")
-    if need <= 4 << 20:
+    if need <= 8 << 20:
         pytest.skip(f"on {sm} SMs this shape's split fits the array ({need} bytes)")
     y0 = y.clone()
     assert _static(lib, x, w, None, y, tll.EPI_NONE) == tll.ERR_WORKSPACE

@@ -26,6 +26,10 @@
 //   order 0..S-1 ("One kernel was never going to be enough": split-K when the
 //   output is small and K is long; "Optimizing a GPT-2-class transformer on a
 //   GPU", Act I: fixed-order reduction).
+// * Programmatic dependent launch (when the caller allows an early start): the
+//   CTAs may start while the previous kernel on the stream drains, loading X
+//   and W before griddepcontrol.wait when neither is that kernel's output;
+//   bias, Y and the split-K workspace are touched only after the wait.
 #include "internal.h"
 #include "device_common.cuh"
 
@@ -41,7 +45,8 @@ struct FfmaArgs {
     float* ws;
     unsigned* counters;
     int splits;
-    int nkb;  // ceil(K / BK)
+    int nkb;           // ceil(K / BK)
+    int early_inputs;  // X and W may be read before the dependency wait (not the previous call's output)
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
@@ -150,6 +155,8 @@ ffma_kernel(const FfmaArgs a) {
     const int kb_begin = (int)((long long)split * a.nkb / a.splits);
     const int kb_end = (int)((long long)(split + 1) * a.nkb / a.splits);
     const int nk = kb_end - kb_begin;
+    if (tid == 0) pdl_launch_dependents();
+    if (!a.early_inputs) pdl_wait();  // X or W may be the previous kernel's output
 
     float acc[TM][TN];
 #pragma unroll
@@ -220,6 +227,10 @@ ffma_kernel(const FfmaArgs a) {
         }
     }
     cp_async_wait<0>();
+    // Bias, Y and the split-K workspace only after the previous kernel on the
+    // stream has finished (it may have written the bias, or be using the
+    // workspace).
+    pdl_wait();
 
     auto row_of = [&](int r) { return m0 + ty + r * TY; };
     auto col_of = [&](int c) { return n0 + tx + c * TX; };
@@ -243,7 +254,7 @@ ffma_kernel(const FfmaArgs a) {
 }
 
 template <int BM, int BN, int BK, int TM, int TN, int STAGES>
-int launch_cfg(const FfmaArgs& a, dim3 grid, cudaStream_t st, bool gelu) {
+int launch_cfg(const FfmaArgs& a, dim3 grid, cudaStream_t st, bool gelu, bool early) {
     constexpr size_t smem = ffma_smem_bytes<BM, BN, BK, STAGES>();
     static_assert(smem <= 227 * 1024, "shared memory per CTA");
     const bool split = a.splits > 1;
@@ -261,7 +272,17 @@ int launch_cfg(const FfmaArgs& a, dim3 grid, cudaStream_t st, bool gelu) {
             return LIN_ERR_CUDA;
         attr_set[which] |= bit;
     }
-    kern<<<grid, 256, smem, st>>>(a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = early ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return LIN_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? LIN_OK : LIN_ERR_CUDA;
 }
 
@@ -278,6 +299,7 @@ int launch_ffma(const Problem& p, const lin_plan& plan) {
     a.Y = static_cast<float*>(p.Y);
     a.splits = plan.splits;
     a.nkb = (p.K + plan.bk - 1) / plan.bk;
+    a.early_inputs = (p.early_start && p.early_x) ? 1 : 0;
     a.ws = nullptr;
     a.counters = nullptr;
     if (plan.splits > 1) {
@@ -288,9 +310,9 @@ int launch_ffma(const Problem& p, const lin_plan& plan) {
     const bool gelu = p.epilogue == LIN_EPI_GELU_TANH;
     switch (plan.variant) {
         case 0: return launch_cfg<kFfmaCfg[0].bm, kFfmaCfg[0].bn, kFfmaCfg[0].bk, kFfmaCfg[0].tm, kFfmaCfg[0].tn, 4>(
-            a, grid, p.stream, gelu);
+            a, grid, p.stream, gelu, p.early_start);
         case 1: return launch_cfg<kFfmaCfg[1].bm, kFfmaCfg[1].bn, kFfmaCfg[1].bk, kFfmaCfg[1].tm, kFfmaCfg[1].tn, 4>(
-            a, grid, p.stream, gelu);
+            a, grid, p.stream, gelu, p.early_start);
         default: return LIN_ERR_UNSUPPORTED;
     }
 }

@@ -514,8 +514,9 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             }
             __syncwarp();  // sBias is rewritten for the next tile
         }
-        // TMA stores of this warp complete before the CTA releases its shared memory.
-        if (BF16 && a.y_tma && lane == 0) bulk_wait_all();
+        // The TMA stores of this warp have read their box before the CTA releases
+        // its shared memory (their global writes complete with the grid).
+        if (BF16 && a.y_tma && lane == 0) bulk_wait_read_all();
         __syncwarp();
     }
 

@@ -98,8 +98,6 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until this thread's bulk stores have finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// Wait until this thread's bulk stores have completed.
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -356,12 +354,6 @@ __device__ __forceinline__ bool wait_flag_set(const unsigned* p) {
     return false;
 }
 
-// ---- programmatic dependent launch ----
-// Wait until the grids this launch depends on have completed and their memory
-// is visible (a no-op when launched without the programmatic attribute).
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-// Allow the dependent grid to be scheduled.
-__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
 // ---- host side ----
 // 2-D tensor map over a rows x K row-major tensor, box = 128 bytes of K x box_rows,
