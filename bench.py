@@ -509,7 +509,9 @@ def main(argv=None):
         names = [n for n in WORKLOADS if n != args.workload] + [args.workload]
     for name in names:
         layer = WORKLOADS[name]
-        st = steps if name == args.workload else max(10, min(steps, int(2e11 / max(layer.flops, 1e6))))
+        # Other workloads: at least 300 steps and ~20 TFLOP, so that the timed
+        # region spans several replays of the step graph.
+        st = steps if name == args.workload else max(300, min(steps, int(2e13 / max(layer.flops, 1e6))))
         line = bench_ours(layer, st, warmup, world, rank, local_rank,
                           with_cpu_baseline=(not args.no_cpu_baseline and name == args.workload),
                           e2e_steps=args.e2e_steps if name == args.workload else 5)
