@@ -340,7 +340,8 @@ def bench_ours(layer: si.Layer, steps: int, warmup: int, world: int, rank: int, 
         value, unit = world * steps * layer.flops / max_s / 1e12, "TFLOP/s"
 
     peaks, src = load_peaks()
-    kfile = {tll.KERNEL_SKINNY: "skinny.cu", tll.KERNEL_FFMA: "ffma.cu", tll.KERNEL_TC: "tc.cu"}.get(plan.kernel)
+    kfile = {tll.KERNEL_SKINNY: "skinny.cu", tll.KERNEL_FFMA: "ffma.cu", tll.KERNEL_TC: "tc.cu",
+             tll.KERNEL_GEMV: "gemv.cu"}.get(plan.kernel)
     traffic = traffic_from_profile(kfile, layer.name) if kfile else None
     roof = roofline_for(layer, per_launch_s, peaks, src, traffic)
 

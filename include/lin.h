@@ -78,7 +78,8 @@ typedef enum {
     LIN_KERNEL_FILL = 1,   /* K == 0: Y = act(bias) (or act(0)) */
     LIN_KERNEL_SKINNY = 2, /* M <= 16, BF16: W stream, split-K across a thread-block cluster (no workspace) */
     LIN_KERNEL_FFMA = 3,   /* FP32: register-tiled FFMA, optional split-K */
-    LIN_KERNEL_TC = 4      /* TF32 / BF16: TMA + tcgen05 + TMEM, fused epilogue */
+    LIN_KERNEL_TC = 4,     /* TF32 / BF16: TMA + tcgen05 + TMEM, fused epilogue */
+    LIN_KERNEL_GEMV = 5    /* FP32 / TF32, M <= 8: one pass over W, exact fp32 (X in shared memory) */
 } lin_kernel;
 
 /* One launch configuration, chosen by the dispatch table or given explicitly.
@@ -157,7 +158,8 @@ LIN_API int lin_plan_query(int sm_count, int M, int N, int K, int precision, int
  * instead: >= 0 CTAs walking whole tiles (0 = one per SM); -1 stream-K with
  * one CTA per SM; -c (c >= 2) stream-K with c CTAs (single-CTA variants, at
  * least one tile per CTA; the plan's splits is then 2 and it needs workspace
- * for one 128 x BN fp32 slot per CTA). Returns LIN_ERR_UNSUPPORTED when the
+ * for one 128 x BN fp32 slot per CTA). For LIN_KERNEL_GEMV, splits is the
+ * CTA count (0 = as many as fit at once). Returns LIN_ERR_UNSUPPORTED when the
  * kernel cannot run the shape. */
 LIN_API int lin_plan_make(int sm_count, int kernel, int variant, int splits, int M, int N, int K,
                   int precision, lin_plan* out);
@@ -206,9 +208,10 @@ LIN_API int lin_abi_version(void);
  * - runtimes that own all device memory through their own pool;
  * - paths where an allocation could block or fail.
  *
- * Y = act(X . W^T + bias) in fp32 on the CURRENT device, with the same FFMA
- * kernel and split-K choice as lin_forward(..., LIN_PREC_FP32, ...), but with
- * no context. It calls no cudaMalloc or cudaFree: the split-K counters and
+ * Y = act(X . W^T + bias) in fp32 on the CURRENT device, with the same
+ * kernel and split-K choice as lin_forward(..., LIN_PREC_FP32, ...) (the FFMA
+ * kernel, or the GEMV for M <= 8, which needs no scratch), but with no
+ * context. It calls no cudaMalloc or cudaFree: the split-K counters and
  * partial sums live in one fixed array of LIN_STATIC_SCRATCH_BYTES (8 MiB),
  * a static device variable of this library that every GPU which loads the
  * library holds until the process exits. Arguments, layouts and alignment

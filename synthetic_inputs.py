@@ -277,4 +277,12 @@ GPT2_M8192_BF16 = (
     Layer("gpt2_lmhead_m8192_bf16", 8192, 50257, 768, PREC_BF16, bias=False),
 )
 
-ALL_WORKLOADS = (SQUARE_256_FP32, SKINNY_16x4096, SQUARE_4096_FP32, SQUARE_4096_TF32) + GPT2_M128_FP32 + GPT2_M8192_BF16
+# The one-row sites ("Optimizing a GPT-2-class transformer on a GPU", Act II:
+# only the final token's logits are needed): the LM head at M = 1.
+GPT2_LOGITS_M1 = (
+    Layer("gpt2_logits_m1_fp32", 1, 50257, 768, PREC_FP32, bias=False),
+    Layer("gpt2_logits_m1_bf16", 1, 50257, 768, PREC_BF16, bias=False),
+)
+
+ALL_WORKLOADS = ((SQUARE_256_FP32, SKINNY_16x4096, SQUARE_4096_FP32, SQUARE_4096_TF32) + GPT2_M128_FP32 + GPT2_M8192_BF16 +
+                 GPT2_LOGITS_M1)

@@ -160,3 +160,20 @@ def test_plan_make_stream_k():
     assert p.splits == 2 and p.grid_x == 9      # no more CTAs than the 3 x 3 tiles
     for M, N, K in ((8192, 768, 768), (8192, 2304, 768), (8192, 3072, 768), (8192, 768, 3072)):
         assert tll.plan_query(SM, M, N, K, "bf16").splits == 1
+
+
+def test_dispatch_gemv_for_few_fp32_rows():
+    for prec in ("fp32", "tf32"):
+        for M in (1, 2, 3, 8):
+            p = tll.plan_query(SM, M, 50257, 768, prec)
+            assert kname(p) == "gemv" and p.bm in (1, 2, 4, 8) and p.bm >= M and p.workspace_bytes == 0
+    # X (rows x K fp32) must fit in shared memory; else the tiled kernels
+    assert kname(tll.plan_query(SM, 8, 4096, 4096, "fp32")) == "ffma"
+    assert kname(tll.plan_query(SM, 9, 4096, 768, "fp32")) == "ffma"
+    assert kname(tll.plan_query(SM, 1, 4096, 4096, "bf16")) == "skinny"
+    p = tll.plan_make(SM, tll.KERNEL_GEMV, 0, 3, 5, 1000, 520, "fp32")
+    assert p.grid_x == 3 and p.bm == 8
+    with pytest.raises(tll.LinError):
+        tll.plan_make(SM, tll.KERNEL_GEMV, 0, 0, 5, 1000, 520, "bf16")
+    with pytest.raises(tll.LinError):
+        tll.plan_make(SM, tll.KERNEL_GEMV, 0, 0, 9, 1000, 520, "fp32")

@@ -45,6 +45,12 @@ def all_plans(ctx, M, N, K, precision):
         for v in range(2):
             for s in (1, 0, 3):
                 plans.append(tll.plan_make(sm, tll.KERNEL_FFMA, v, s, M, N, K, "fp32"))
+    if precision in (FP32, TF32) and M <= 8:
+        for ctas in (0, 3):  # as many CTAs as fit, or a few walking many rows of W
+            try:
+                plans.append(tll.plan_make(sm, tll.KERNEL_GEMV, 0, ctas, M, N, K, PREC_NAME[precision]))
+            except tll.LinError:  # X does not fit in shared memory
+                pass
     return plans
 
 
@@ -387,6 +393,54 @@ def test_ffma_back_to_back(ctx, N, K):
     ctx.check()
     refv = oracle.linear(X0, ws[0].cpu().numpy(), b)
     assert oracle.rel_err(outs[0].cpu().numpy().astype(np.float64), refv) <= oracle.TOL[FP32]
+
+
+@pytest.mark.parametrize("precision", [FP32, TF32])
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8])
+def test_gemv_few_rows(ctx, precision, M):
+    """The one-row sites: M <= 8 runs the exact-fp32 GEMV (also for TF32).
+    Ragged N and K, bias and GELU, against the oracle at the fp32 tolerance;
+    bitwise repeatable."""
+    for N, K in [(1000, 520), (77, 4), (2304, 768), (300, 3072)]:
+        layer = si.Layer("gemv", M, N, K, precision, si.EPI_GELU, bias=True)
+        X, W, b = si.make_inputs(layer)
+        plan = ctx.plan(M, N, K, PREC_NAME[precision])
+        assert tll.KERNEL_NAMES[plan.kernel] == "gemv"
+        y = run(X, W, b, precision, epilogue=si.EPI_GELU, ctx=ctx)
+        ref = oracle.linear(X, W, b, True)
+        assert oracle.rel_err(y, ref) <= oracle.TOL[FP32], (M, N, K)
+        assert np.array_equal(y, run(X, W, b, precision, epilogue=si.EPI_GELU, ctx=ctx))
+
+
+def test_gemv_lm_head_row_sampled():
+    """The last token's logits, fp32: 1 x 50257 x 768 (N odd), full compare."""
+    layer = si.Layer("logits", 1, 50257, 768, FP32, bias=False)
+    check_layer(layer)
+
+
+def test_gemv_back_to_back_chain(ctx):
+    """GEMV calls back to back: independent ones into separate outputs, and a
+    chain X = previous Y, equal the same calls one at a time."""
+    M, N = 4, 1024
+    X0, _, b = si.make_inputs(si.Layer("gemvb2b", M, N, N, FP32, bias=True))
+    x0 = torch.from_numpy(X0).cuda()
+    bias = torch.from_numpy(b).cuda()
+    ws = [torch.from_numpy(si.normal(70 + i, 2, (N, N), 0.0, 0.03)).cuda() for i in range(3)]
+    outs = [tll.forward(x0, ws[i % 3], bias, precision="fp32") for i in range(6)]
+    chain = [x0]
+    for i in range(6):
+        chain.append(tll.forward(chain[-1], ws[i % 3], bias, epilogue="gelu", precision="fp32"))
+    torch.cuda.synchronize()
+    for i in range(6):
+        ref = tll.forward(x0, ws[i % 3], bias, precision="fp32")
+        torch.cuda.synchronize()
+        assert torch.equal(outs[i], ref), i
+    ref = x0
+    for i in range(6):
+        ref = tll.forward(ref, ws[i % 3], bias, epilogue="gelu", precision="fp32")
+        torch.cuda.synchronize()
+        assert torch.equal(ref, chain[i + 1]), i
+    ctx.check()
 
 
 @pytest.mark.parametrize("K", [4096, 4104, 384, 200])

@@ -21,13 +21,13 @@ from .build import build
 __all__ = [
     "LinError", "Context", "Plan", "forward", "forward_plan", "plan_query", "plan_make", "build",
     "library", "PREC_FP32", "PREC_TF32", "PREC_BF16", "EPI_NONE", "EPI_GELU_TANH",
-    "KERNEL_NONE", "KERNEL_FILL", "KERNEL_SKINNY", "KERNEL_FFMA", "KERNEL_TC",
+    "KERNEL_NONE", "KERNEL_FILL", "KERNEL_SKINNY", "KERNEL_FFMA", "KERNEL_TC", "KERNEL_GEMV",
 ]
 
 PREC_FP32, PREC_TF32, PREC_BF16 = 0, 1, 2
 EPI_NONE, EPI_GELU_TANH = 0, 1
-KERNEL_NONE, KERNEL_FILL, KERNEL_SKINNY, KERNEL_FFMA, KERNEL_TC = 0, 1, 2, 3, 4
-KERNEL_NAMES = {0: "none", 1: "fill", 2: "skinny", 3: "ffma", 4: "tc"}
+KERNEL_NONE, KERNEL_FILL, KERNEL_SKINNY, KERNEL_FFMA, KERNEL_TC, KERNEL_GEMV = 0, 1, 2, 3, 4, 5
+KERNEL_NAMES = {0: "none", 1: "fill", 2: "skinny", 3: "ffma", 4: "tc", 5: "gemv"}
 OPT_EARLY_START = 1
 OK, ERR_ARG, ERR_ALIGN, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
 

@@ -122,6 +122,37 @@ int make_ffma(int sm, int variant, int splits, int M, int N, int K, size_t ws, l
     return LIN_OK;
 }
 
+// GEMV (FP32 / TF32, M <= 8): X padded to 1, 2, 4 or 8 rows in shared memory;
+// `width` CTAs of 8 warps (0 = as many as fit on the SMs at once, by shared
+// memory and by threads) take the rows of W in turn.
+int gemv_rows(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
+bool gemv_fits(int M, int K) {
+    return M >= 1 && M <= kGemvMaxRows && (size_t)gemv_rows(M) * K * sizeof(float) <= (size_t)kGemvMaxSmem;
+}
+int make_gemv(int sm, int width, int M, int N, int K, lin_plan* p) {
+    if (N < 1 || K < 1 || !gemv_fits(M, K)) return LIN_ERR_UNSUPPORTED;
+    const int rows = gemv_rows(M);
+    const long long smem = (long long)rows * K * 4 + 1024;
+    long long per_sm = (228 * 1024) / smem;
+    if (per_sm > 8) per_sm = 8;  // 2048 threads per SM
+    if (per_sm < 1) per_sm = 1;
+    long long grid = width > 0 ? width : (long long)sm * per_sm;
+    const long long need = ((long long)N + 7) / 8;  // one row per warp and pass
+    if (grid > need) grid = need;
+    plan_common(p, LIN_KERNEL_GEMV, 0);
+    p->bm = rows;
+    p->bn = 8;
+    p->bk = 0;
+    p->splits = 1;
+    p->stages = 0;
+    p->grid_x = (int)grid;
+    p->grid_y = 1;
+    p->grid_z = 1;
+    p->threads = 256;
+    p->workspace_bytes = 0;
+    return LIN_OK;
+}
+
 // Persistent tcgen05 kernel: `width` CTAs walk the 128 x BN output tiles
 // (0 = one CTA per SM) in static round robin; pair variants walk 256 x BN
 // tiles with one 2-CTA cluster (an SM pair) per tile (grid rounded down to
@@ -215,8 +246,12 @@ int plan_default(int sm, int M, int N, int K, int precision, size_t ws, lin_plan
             if (M <= 16) return make_skinny(sm, 0, 0, M, N, K, ws, p);
             return make_tc(sm, -1, 0, false, M, N, K, 2, p);
         case LIN_PREC_TF32:
+            // A few rows are a weight stream: the exact-fp32 GEMV is as fast as
+            // any tensor-core tile there, and more accurate than TF32.
+            if (gemv_fits(M, K)) return make_gemv(sm, 0, M, N, K, p);
             return make_tc(sm, -1, 0, false, M, N, K, 4, p);
         default:
+            if (gemv_fits(M, K)) return make_gemv(sm, 0, M, N, K, p);
             return make_ffma(sm, -1, 0, M, N, K, ws, p);
     }
 }
@@ -328,6 +363,11 @@ int check_plan_fits(const lin_plan& p, int M, int N, int K, int precision) {
                 return LIN_ERR_UNSUPPORTED;
             return LIN_OK;
         }
+        case LIN_KERNEL_GEMV: {
+            if (precision == LIN_PREC_BF16 || K == 0 || !gemv_fits(M, K)) return LIN_ERR_UNSUPPORTED;
+            if (p.bm != gemv_rows(M) || p.grid_x < 1 || p.grid_y != 1 || p.grid_z != 1) return LIN_ERR_UNSUPPORTED;
+            return LIN_OK;
+        }
         default: return LIN_ERR_UNSUPPORTED;
     }
 }
@@ -386,6 +426,7 @@ int run(lin_ctx* ctx, const lin_plan& plan_in, int M, int N, int K, const void* 
         case LIN_KERNEL_SKINNY: return launch_skinny(p, plan);
         case LIN_KERNEL_FFMA: return launch_ffma(p, plan);
         case LIN_KERNEL_TC: return launch_tc(p, plan);
+        case LIN_KERNEL_GEMV: return launch_gemv(p, plan);
         default: return LIN_ERR_UNSUPPORTED;
     }
 }
@@ -516,6 +557,9 @@ int lin_plan_make(int sm_count, int kernel, int variant, int splits, int M, int 
             // one CTA per SM; -c (c >= 2): stream-K with c CTAs.
             return lin::make_tc(sm_count, variant, splits >= 0 ? splits : (splits == -1 ? 0 : -splits), splits < 0,
                                 M, N, K, precision == LIN_PREC_BF16 ? 2 : 4, out);
+        case LIN_KERNEL_GEMV:
+            if (precision == LIN_PREC_BF16) return LIN_ERR_UNSUPPORTED;
+            return lin::make_gemv(sm_count, splits > 0 ? splits : 0, M, N, K, out);  // splits = CTAs (0 = fill)
         case LIN_KERNEL_NONE:
         case LIN_KERNEL_FILL:
             return lin::plan_default(sm_count, M, N, K, precision, unlimited, out);

@@ -7,8 +7,9 @@
 //   start-up and treats any other allocation as a failure;
 // - a latency-critical path where an allocation could block on the device
 //   or fail under memory pressure.
-// lin_forward_fp32_static runs the same fp32 FFMA kernel as lin_forward,
-// with the dispatch table's split-K choice. The split's scratch (tile
+// lin_forward_fp32_static runs the same fp32 kernels as lin_forward (the
+// FFMA kernel with the dispatch table's split-K choice, or the GEMV for a few
+// rows, which needs no scratch). The split's scratch (tile
 // counters, then partial sums) lives in the fixed device array below. Every
 // GPU that loads this library holds that array until the process exits.
 #include <mutex>
@@ -103,6 +104,7 @@ extern "C" int lin_forward_fp32_static(int M, int N, int K, const float* X, cons
     p.early_start = false;
     p.early_x = false;
     if (plan.kernel == LIN_KERNEL_FILL) return launch_fill(p);
+    if (plan.kernel == LIN_KERNEL_GEMV) return launch_gemv(p, plan);  // no scratch
     if (plan.kernel != LIN_KERNEL_FFMA) return LIN_ERR_UNSUPPORTED;
     if (plan.splits > 1) {
         // The array keeps the previous call's contents: zero the counters this
