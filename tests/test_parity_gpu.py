@@ -45,7 +45,7 @@ def all_plans(ctx, M, N, K, precision):
         for v in range(2):
             for s in (1, 0, 3):
                 plans.append(tll.plan_make(sm, tll.KERNEL_FFMA, v, s, M, N, K, "fp32"))
-    if precision in (FP32, TF32) and M <= 8:
+    if (precision in (FP32, TF32) and M <= 8) or (precision == BF16 and M <= 4):
         for ctas in (0, 3):  # as many CTAs as fit, or a few walking many rows of W
             try:
                 plans.append(tll.plan_make(sm, tll.KERNEL_GEMV, 0, ctas, M, N, K, PREC_NAME[precision]))
@@ -395,27 +395,30 @@ def test_ffma_back_to_back(ctx, N, K):
     assert oracle.rel_err(outs[0].cpu().numpy().astype(np.float64), refv) <= oracle.TOL[FP32]
 
 
-@pytest.mark.parametrize("precision", [FP32, TF32])
+@pytest.mark.parametrize("precision", [FP32, TF32, BF16])
 @pytest.mark.parametrize("M", [1, 2, 3, 5, 8])
 def test_gemv_few_rows(ctx, precision, M):
-    """The one-row sites: M <= 8 runs the exact-fp32 GEMV (also for TF32).
-    Ragged N and K, bias and GELU, against the oracle at the fp32 tolerance;
-    bitwise repeatable."""
-    for N, K in [(1000, 520), (77, 4), (2304, 768), (300, 3072)]:
+    """The one-row sites: fp32 / tf32 with M <= 8 and bf16 with M <= 4 run the
+    GEMV (exact fp32 arithmetic; bf16 products are exact in fp32). Ragged N and
+    K, bias and GELU, against the oracle; bitwise repeatable."""
+    if precision == BF16 and M > 4:
+        pytest.skip("bf16 with M > 4 runs the skinny tensor-core kernel")
+    tol = oracle.TOL[BF16] if precision == BF16 else oracle.TOL[FP32]
+    for N, K in [(1000, 520), (77, 8), (2304, 768), (300, 3072)]:
         layer = si.Layer("gemv", M, N, K, precision, si.EPI_GELU, bias=True)
         X, W, b = si.make_inputs(layer)
         plan = ctx.plan(M, N, K, PREC_NAME[precision])
         assert tll.KERNEL_NAMES[plan.kernel] == "gemv"
         y = run(X, W, b, precision, epilogue=si.EPI_GELU, ctx=ctx)
         ref = oracle.linear(X, W, b, True)
-        assert oracle.rel_err(y, ref) <= oracle.TOL[FP32], (M, N, K)
+        assert oracle.rel_err(y, ref) <= tol, (M, N, K)
         assert np.array_equal(y, run(X, W, b, precision, epilogue=si.EPI_GELU, ctx=ctx))
 
 
-def test_gemv_lm_head_row_sampled():
-    """The last token's logits, fp32: 1 x 50257 x 768 (N odd), full compare."""
-    layer = si.Layer("logits", 1, 50257, 768, FP32, bias=False)
-    check_layer(layer)
+@pytest.mark.parametrize("precision", [FP32, BF16])
+def test_gemv_lm_head_row(precision):
+    """The last token's logits: 1 x 50257 x 768 (N odd), full compare."""
+    check_layer(si.Layer("logits", 1, 50257, 768, precision, bias=False))
 
 
 def test_gemv_back_to_back_chain(ctx):

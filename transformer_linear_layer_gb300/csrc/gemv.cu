@@ -1,4 +1,5 @@
-// Exact-fp32 linear layer for a handful of rows (M <= 8): the one-row sites.
+// Linear layer for a handful of rows (fp32 / tf32 M <= 8, bf16 M <= 4): the
+// one-row sites.
 //
 // "Optimizing a GPT-2-class transformer on a GPU", Act II: only the final
 // token's logits are needed, and "a dedicated GEMV takes the one-row sites"
@@ -9,14 +10,20 @@
 //
 // * X (M x K fp32) is copied into shared memory once per CTA, padded with
 //   zero rows to MR = 1, 2, 4 or 8 (the instantiated row count).
-// * Each warp takes one row n of W at a time and reads it whole with 128-bit
-//   loads, lane l taking the float4s l, l + 32, ...: consecutive lanes read
-//   consecutive 16 bytes, and U = 8 loads per lane are in flight before the
-//   first is used (with several CTAs per SM, ~100 KB of W in flight per SM).
+// * Each warp takes RPW consecutive rows of W at a time and reads them with
+//   16-byte loads, lane l taking the pieces l, l + 32, ... of each row:
+//   consecutive lanes read consecutive 16 bytes, and 8 loads per lane are in
+//   flight before the first is used (RPW = 2 or 4 when rows are short, so
+//   that short rows still fill the 8 slots).
 // * Lane l accumulates its k's in ascending order into M fp32 sums; the 32
 //   lanes' sums are added by a fixed butterfly (xor 16, 8, 4, 2, 1), so the
 //   result is bitwise repeatable. Lane 0 adds the bias, applies the accurate
 //   tanh-GELU and stores the M outputs of column n.
+// * bf16 (M <= 4): X is widened to fp32 in shared memory, each 16-byte load
+//   of W carries 8 values, bf16 x bf16 products are exact in fp32 and the
+//   sums are fp32 as on the tensor cores; the result is rounded to bf16 (the
+//   GELU then uses the hardware tanh). At most 4 rows keep the convert + FMA
+//   instructions per weight well under what the SMs issue at HBM speed.
 // * Programmatic dependent launch: W streams before griddepcontrol.wait when
 //   the caller allows an early start (W is not the previous call's output), X
 //   only when it is not that output either; bias and Y after the wait.
@@ -28,85 +35,147 @@ namespace {
 
 struct GemvArgs {
     int M, N, K;
-    const float* X;
-    const float* W;
+    const void* X;     // fp32 or bf16
+    const void* W;     // fp32 or bf16
     const float* bias;
-    float* Y;
-    int early_x;  // X may be read before the dependency wait
+    void* Y;           // fp32 or bf16
+    int early_x;       // X may be read before the dependency wait
 };
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 constexpr int kGemvThreads = 256;
 constexpr int kGemvUnroll = 8;  // float4 loads of W in flight per lane
 
-template <int MR, bool GELU>
+template <int MR, int RPW, bool GELU, bool BF16>
 __global__ void __launch_bounds__(kGemvThreads)
 gemv_kernel(const GemvArgs a) {
-    extern __shared__ __align__(16) float sx[];  // MR x K
+    extern __shared__ __align__(16) float sx[];  // MR x K, fp32
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int K4 = a.K >> 2;
     if (threadIdx.x == 0) pdl_launch_dependents();
 
     if (!a.early_x) pdl_wait();
-    {
+    // The M rows of X (widened to fp32), then zeros up to the padded MR rows.
+    if constexpr (BF16) {
+        const uint2* x4 = reinterpret_cast<const uint2*>(a.X);  // 4 bf16
+        float4* s4 = reinterpret_cast<float4*>(sx);
+        for (int i = threadIdx.x; i < MR * K4; i += kGemvThreads) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i < a.M * K4) {
+                const uint2 q = __ldg(x4 + i);
+                v = make_float4(bf16_lo(q.x), bf16_hi(q.x), bf16_lo(q.y), bf16_hi(q.y));
+            }
+            s4[i] = v;
+        }
+    } else {
         const float4* x4 = reinterpret_cast<const float4*>(a.X);
         float4* s4 = reinterpret_cast<float4*>(sx);
-        // The M rows of X, then zeros up to the padded MR rows.
         for (int i = threadIdx.x; i < MR * K4; i += kGemvThreads)
             s4[i] = i < a.M * K4 ? __ldg(x4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     __syncthreads();
     const float4* sx4 = reinterpret_cast<const float4*>(sx);
+    // 16-byte loads of W: 4 fp32 or 8 bf16 values.
+    constexpr int VPL = BF16 ? 8 : 4;
+    const int KV = a.K / VPL;
 
     const int warps_total = gridDim.x * (kGemvThreads / 32);
+    constexpr int UPR = kGemvUnroll / RPW;  // load slots per row and lane
     bool waited = !a.early_x;
-    for (int n = blockIdx.x * (kGemvThreads / 32) + warp; n < a.N; n += warps_total) {
-        const float4* w4 = reinterpret_cast<const float4*>(a.W + (size_t)n * a.K);
-        float acc[MR];
+    for (int n0 = (blockIdx.x * (kGemvThreads / 32) + warp) * RPW; n0 < a.N; n0 += warps_total * RPW) {
+        float acc[RPW][MR];
 #pragma unroll
-        for (int m = 0; m < MR; ++m) acc[m] = 0.f;
-        for (int k0 = lane; k0 < K4; k0 += 32 * kGemvUnroll) {
-            float4 wv[kGemvUnroll];
+        for (int r = 0; r < RPW; ++r)
 #pragma unroll
-            for (int u = 0; u < kGemvUnroll; ++u) {
-                const int k = k0 + 32 * u;
-                wv[u] = k < K4 ? __ldcs(w4 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int m = 0; m < MR; ++m) acc[r][m] = 0.f;
+        for (int k0 = lane; k0 < KV; k0 += 32 * UPR) {
+            uint4 wv[RPW][UPR];
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) {
+                const int n = n0 + r;
+                const uint4* wrow = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.W) +
+                                                                   (size_t)n * a.K * (BF16 ? 2 : 4));
+#pragma unroll
+                for (int u = 0; u < UPR; ++u) {
+                    const int k = k0 + 32 * u;
+                    wv[r][u] = (n < a.N && k < KV) ? __ldcs(wrow + k) : make_uint4(0u, 0u, 0u, 0u);
+                }
             }
 #pragma unroll
-            for (int u = 0; u < kGemvUnroll; ++u) {
-                const int k = k0 + 32 * u;
-                if (k < K4) {
+            for (int r = 0; r < RPW; ++r) {
 #pragma unroll
-                    for (int m = 0; m < MR; ++m) {
-                        const float4 xv = sx4[m * K4 + k];
-                        acc[m] = fmaf(wv[u].x, xv.x, acc[m]);
-                        acc[m] = fmaf(wv[u].y, xv.y, acc[m]);
-                        acc[m] = fmaf(wv[u].z, xv.z, acc[m]);
-                        acc[m] = fmaf(wv[u].w, xv.w, acc[m]);
+                for (int u = 0; u < UPR; ++u) {
+                    const int k = k0 + 32 * u;
+                    if (k < KV) {
+                        if constexpr (BF16) {
+                            const uint4 q = wv[r][u];
+                            const float w0 = bf16_lo(q.x), w1 = bf16_hi(q.x), w2 = bf16_lo(q.y), w3 = bf16_hi(q.y),
+                                        w4 = bf16_lo(q.z), w5 = bf16_hi(q.z), w6 = bf16_lo(q.w), w7 = bf16_hi(q.w);
+#pragma unroll
+                            for (int m = 0; m < MR; ++m) {
+                                const float4 xa = sx4[m * K4 + 2 * k], xb = sx4[m * K4 + 2 * k + 1];
+                                float t = acc[r][m];
+                                t = fmaf(w0, xa.x, t);
+                                t = fmaf(w1, xa.y, t);
+                                t = fmaf(w2, xa.z, t);
+                                t = fmaf(w3, xa.w, t);
+                                t = fmaf(w4, xb.x, t);
+                                t = fmaf(w5, xb.y, t);
+                                t = fmaf(w6, xb.z, t);
+                                acc[r][m] = fmaf(w7, xb.w, t);
+                            }
+                        } else {
+                            const uint4 q = wv[r][u];
+#pragma unroll
+                            for (int m = 0; m < MR; ++m) {
+                                const float4 xv = sx4[m * K4 + k];
+                                float t = acc[r][m];
+                                t = fmaf(__uint_as_float(q.x), xv.x, t);
+                                t = fmaf(__uint_as_float(q.y), xv.y, t);
+                                t = fmaf(__uint_as_float(q.z), xv.z, t);
+                                acc[r][m] = fmaf(__uint_as_float(q.w), xv.w, t);
+                            }
+                        }
                     }
                 }
             }
         }
 #pragma unroll
-        for (int m = 0; m < MR; ++m) {
+        for (int r = 0; r < RPW; ++r)
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], off);
-        }
+            for (int m = 0; m < MR; ++m)
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) acc[r][m] += __shfl_xor_sync(0xffffffffu, acc[r][m], off);
         if (!waited) {
             pdl_wait();  // bias and Y only after the previous kernel has finished
             waited = true;
         }
         if (lane == 0) {
-            const float b = a.bias ? __ldg(a.bias + n) : 0.f;
 #pragma unroll
-            for (int m = 0; m < MR; ++m)
-                if (m < a.M) a.Y[(size_t)m * a.N + n] = epilogue<GELU>(acc[m], b);
+            for (int r = 0; r < RPW; ++r) {
+                const int n = n0 + r;
+                if (n >= a.N) break;
+                const float b = a.bias ? __ldg(a.bias + n) : 0.f;
+#pragma unroll
+                for (int m = 0; m < MR; ++m) {
+                    if (m < a.M) {
+                        if constexpr (BF16)
+                            static_cast<uint16_t*>(a.Y)[(size_t)m * a.N + n] =
+                                f32_to_bf16_bits(epilogue<GELU, true>(acc[r][m], b));
+                        else
+                            static_cast<float*>(a.Y)[(size_t)m * a.N + n] = epilogue<GELU>(acc[r][m], b);
+                    }
+                }
+            }
         }
     }
 }
 
-template <int MR, bool GELU>
+template <int MR, int RPW, bool GELU, bool BF16>
 int launch_mr(const GemvArgs& a, int grid, bool early, cudaStream_t st) {
-    auto kern = gemv_kernel<MR, GELU>;
+    auto kern = gemv_kernel<MR, RPW, GELU, BF16>;
     const size_t smem = (size_t)MR * a.K * sizeof(float);
     static unsigned long long attr_set = 0;  // one attribute call per instantiation and device
     int dev = 0;
@@ -131,34 +200,52 @@ int launch_mr(const GemvArgs& a, int grid, bool early, cudaStream_t st) {
     return cudaGetLastError() == cudaSuccess ? LIN_OK : LIN_ERR_CUDA;
 }
 
-template <bool GELU>
-int launch_gelu(const GemvArgs& a, int rows, int grid, bool early, cudaStream_t st) {
+template <int RPW, bool GELU, bool BF16>
+int launch_rows(const GemvArgs& a, int rows, int grid, bool early, cudaStream_t st) {
     switch (rows) {
-        case 1: return launch_mr<1, GELU>(a, grid, early, st);
-        case 2: return launch_mr<2, GELU>(a, grid, early, st);
-        case 4: return launch_mr<4, GELU>(a, grid, early, st);
-        case 8: return launch_mr<8, GELU>(a, grid, early, st);
+        case 1: return launch_mr<1, RPW, GELU, BF16>(a, grid, early, st);
+        case 2: return launch_mr<2, RPW, GELU, BF16>(a, grid, early, st);
+        case 4: return launch_mr<4, RPW, GELU, BF16>(a, grid, early, st);
+        case 8: return BF16 ? LIN_ERR_UNSUPPORTED : launch_mr<8, RPW, GELU, false>(a, grid, early, st);
         default: return LIN_ERR_UNSUPPORTED;
+    }
+}
+
+// Rows per warp pass: enough short rows to fill the 8 load slots of a lane.
+template <bool GELU, bool BF16>
+int launch_rpw(const GemvArgs& a, int rows, int grid, bool early, cudaStream_t st) {
+    const int kv = a.K / (BF16 ? 8 : 4);
+    int rpw = 1;
+    while (rpw < 4 && kv * rpw * 2 <= 32 * kGemvUnroll) rpw *= 2;
+    switch (rpw) {
+        case 1: return launch_rows<1, GELU, BF16>(a, rows, grid, early, st);
+        case 2: return launch_rows<2, GELU, BF16>(a, rows, grid, early, st);
+        default: return launch_rows<4, GELU, BF16>(a, rows, grid, early, st);
     }
 }
 
 }  // namespace
 
 int launch_gemv(const Problem& p, const lin_plan& plan) {
-    if (p.M < 1 || p.M > kGemvMaxRows || (size_t)plan.bm * p.K * sizeof(float) > (size_t)kGemvMaxSmem)
+    const bool bf16 = p.precision == LIN_PREC_BF16;
+    if (p.M < 1 || p.M > (bf16 ? kGemvMaxRowsBf16 : kGemvMaxRows) ||
+        (size_t)plan.bm * p.K * sizeof(float) > (size_t)kGemvMaxSmem || p.K % (bf16 ? 8 : 4) != 0)
         return LIN_ERR_UNSUPPORTED;
     GemvArgs a;
     a.M = p.M;
     a.N = p.N;
     a.K = p.K;
-    a.X = static_cast<const float*>(p.X);
-    a.W = static_cast<const float*>(p.W);
+    a.X = p.X;
+    a.W = p.W;
     a.bias = p.bias;
-    a.Y = static_cast<float*>(p.Y);
+    a.Y = p.Y;
     a.early_x = (p.early_start && p.early_x) ? 1 : 0;
     const bool gelu = p.epilogue == LIN_EPI_GELU_TANH;
-    return gelu ? launch_gelu<true>(a, plan.bm, plan.grid_x, p.early_start, p.stream)
-                : launch_gelu<false>(a, plan.bm, plan.grid_x, p.early_start, p.stream);
+    if (bf16)
+        return gelu ? launch_rpw<true, true>(a, plan.bm, plan.grid_x, p.early_start, p.stream)
+                    : launch_rpw<false, true>(a, plan.bm, plan.grid_x, p.early_start, p.stream);
+    return gelu ? launch_rpw<true, false>(a, plan.bm, plan.grid_x, p.early_start, p.stream)
+                : launch_rpw<false, false>(a, plan.bm, plan.grid_x, p.early_start, p.stream);
 }
 
 }  // namespace lin

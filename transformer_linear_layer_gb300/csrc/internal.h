@@ -69,9 +69,11 @@ inline size_t tc_streamk_workspace_bytes(int ctas, int bn) {
     return kCounterBytes + align_up((size_t)ctas * 128 * (size_t)bn * sizeof(float), 256);
 }
 
-// GEMV for a handful of rows (fp32 / tf32, M <= 8): X padded to 1, 2, 4 or 8
-// rows (plan.bm) lives in shared memory, so rows x K x 4 bytes must fit.
+// GEMV for a handful of rows (fp32 / tf32 M <= 8, bf16 M <= 4): X padded to
+// 1, 2, 4 or 8 rows (plan.bm) lives in shared memory as fp32, so rows x K x 4
+// bytes must fit.
 constexpr int kGemvMaxRows = 8;
+constexpr int kGemvMaxRowsBf16 = 4;
 constexpr int kGemvMaxSmem = 96 * 1024;
 
 // Launchers (return LIN_OK or LIN_ERR_*). They assume the plan was validated.

@@ -122,15 +122,16 @@ int make_ffma(int sm, int variant, int splits, int M, int N, int K, size_t ws, l
     return LIN_OK;
 }
 
-// GEMV (FP32 / TF32, M <= 8): X padded to 1, 2, 4 or 8 rows in shared memory;
+// GEMV (FP32 / TF32 M <= 8, BF16 M <= 4): X padded to 1, 2, 4 or 8 rows in shared memory;
 // `width` CTAs of 8 warps (0 = as many as fit on the SMs at once, by shared
 // memory and by threads) take the rows of W in turn.
 int gemv_rows(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
-bool gemv_fits(int M, int K) {
-    return M >= 1 && M <= kGemvMaxRows && (size_t)gemv_rows(M) * K * sizeof(float) <= (size_t)kGemvMaxSmem;
+bool gemv_fits(int M, int K, bool bf16) {
+    return M >= 1 && M <= (bf16 ? kGemvMaxRowsBf16 : kGemvMaxRows) && K % (bf16 ? 8 : 4) == 0 &&
+           (size_t)gemv_rows(M) * K * sizeof(float) <= (size_t)kGemvMaxSmem;
 }
-int make_gemv(int sm, int width, int M, int N, int K, lin_plan* p) {
-    if (N < 1 || K < 1 || !gemv_fits(M, K)) return LIN_ERR_UNSUPPORTED;
+int make_gemv(int sm, int width, int M, int N, int K, bool bf16, lin_plan* p) {
+    if (N < 1 || K < 1 || !gemv_fits(M, K, bf16)) return LIN_ERR_UNSUPPORTED;
     const int rows = gemv_rows(M);
     const long long smem = (long long)rows * K * 4 + 1024;
     long long per_sm = (228 * 1024) / smem;
@@ -243,15 +244,16 @@ int plan_default(int sm, int M, int N, int K, int precision, size_t ws, lin_plan
     }
     switch (precision) {
         case LIN_PREC_BF16:
+            if (gemv_fits(M, K, true)) return make_gemv(sm, 0, M, N, K, true, p);
             if (M <= 16) return make_skinny(sm, 0, 0, M, N, K, ws, p);
             return make_tc(sm, -1, 0, false, M, N, K, 2, p);
         case LIN_PREC_TF32:
             // A few rows are a weight stream: the exact-fp32 GEMV is as fast as
             // any tensor-core tile there, and more accurate than TF32.
-            if (gemv_fits(M, K)) return make_gemv(sm, 0, M, N, K, p);
+            if (gemv_fits(M, K, false)) return make_gemv(sm, 0, M, N, K, false, p);
             return make_tc(sm, -1, 0, false, M, N, K, 4, p);
         default:
-            if (gemv_fits(M, K)) return make_gemv(sm, 0, M, N, K, p);
+            if (gemv_fits(M, K, false)) return make_gemv(sm, 0, M, N, K, false, p);
             return make_ffma(sm, -1, 0, M, N, K, ws, p);
     }
 }
@@ -364,7 +366,7 @@ int check_plan_fits(const lin_plan& p, int M, int N, int K, int precision) {
             return LIN_OK;
         }
         case LIN_KERNEL_GEMV: {
-            if (precision == LIN_PREC_BF16 || K == 0 || !gemv_fits(M, K)) return LIN_ERR_UNSUPPORTED;
+            if (K == 0 || !gemv_fits(M, K, precision == LIN_PREC_BF16)) return LIN_ERR_UNSUPPORTED;
             if (p.bm != gemv_rows(M) || p.grid_x < 1 || p.grid_y != 1 || p.grid_z != 1) return LIN_ERR_UNSUPPORTED;
             return LIN_OK;
         }
@@ -557,9 +559,8 @@ int lin_plan_make(int sm_count, int kernel, int variant, int splits, int M, int 
             // one CTA per SM; -c (c >= 2): stream-K with c CTAs.
             return lin::make_tc(sm_count, variant, splits >= 0 ? splits : (splits == -1 ? 0 : -splits), splits < 0,
                                 M, N, K, precision == LIN_PREC_BF16 ? 2 : 4, out);
-        case LIN_KERNEL_GEMV:
-            if (precision == LIN_PREC_BF16) return LIN_ERR_UNSUPPORTED;
-            return lin::make_gemv(sm_count, splits > 0 ? splits : 0, M, N, K, out);  // splits = CTAs (0 = fill)
+        case LIN_KERNEL_GEMV:  // splits = CTAs (0 = as many as fit)
+            return lin::make_gemv(sm_count, splits > 0 ? splits : 0, M, N, K, precision == LIN_PREC_BF16, out);
         case LIN_KERNEL_NONE:
         case LIN_KERNEL_FILL:
             return lin::plan_default(sm_count, M, N, K, precision, unlimited, out);
