@@ -446,6 +446,57 @@ def test_gemv_back_to_back_chain(ctx):
     ctx.check()
 
 
+@pytest.mark.parametrize("M,precision", [(128, FP32), (1, FP32), (256, BF16), (4, BF16)])
+def test_layer_captured_in_one_graph(M, precision):
+    """A transformer layer's four GEMMs (qkv, proj, fc1 + GELU, fc2 reading
+    fc1's output) recorded in one CUDA graph and replayed: the library makes
+    no allocation and no host sync inside the calls, and the replays give the
+    eager results bit for bit (and the oracle's)."""
+    d = 768
+    dt = torch.bfloat16 if precision == BF16 else torch.float32
+    prec = PREC_NAME[precision]
+    specs = [("qkv", 3 * d, d, False), ("proj", d, d, False), ("fc1", 4 * d, d, True), ("fc2", d, 4 * d, False)]
+    inputs = {}
+    for i, (name, N, K, gelu) in enumerate(specs):
+        X, W, b = si.make_inputs(si.Layer(f"graph_{name}", M, N, K, precision, bias=True))
+        inputs[name] = (X, W, b)
+    dev = {n: (torch.from_numpy(X).to(dt).cuda(), torch.from_numpy(W).to(dt).cuda(), torch.from_numpy(b).cuda())
+           for n, (X, W, b) in inputs.items()}
+    x = dev["qkv"][0]
+    attn = dev["proj"][0]
+    outs = {n: torch.empty((M, N), device="cuda", dtype=dt) for n, N, _, _ in specs}
+
+    def layer():
+        tll.forward(x, dev["qkv"][1], dev["qkv"][2], precision=prec, out=outs["qkv"])
+        tll.forward(attn, dev["proj"][1], dev["proj"][2], precision=prec, out=outs["proj"])
+        tll.forward(x, dev["fc1"][1], dev["fc1"][2], epilogue="gelu", precision=prec, out=outs["fc1"])
+        tll.forward(outs["fc1"], dev["fc2"][1], dev["fc2"][2], precision=prec, out=outs["fc2"])
+
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        layer()  # first calls outside the capture (kernel attributes, device lookups)
+    stream.synchronize()
+    eager = {n: t.clone() for n, t in outs.items()}
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        layer()
+    for t in outs.values():
+        t.fill_(float("nan"))
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    for n in outs:
+        assert torch.equal(outs[n], eager[n]), n
+    tll.default_context(0).check()
+    # fc1 and fc2 against the oracle (fc2 on the GPU's fc1 output)
+    X, W, b = inputs["fc1"]
+    tol = oracle.TOL[precision]
+    assert oracle.rel_err(outs["fc1"].double().cpu().numpy(), oracle.linear(X, W, b, True)) <= tol
+    H = outs["fc1"].float().cpu().numpy()
+    _, W2, b2 = inputs["fc2"]
+    assert oracle.rel_err(outs["fc2"].double().cpu().numpy(), oracle.linear(H, W2, b2)) <= tol
+
+
 @pytest.mark.parametrize("K", [4096, 4104, 384, 200])
 def test_skinny_bits_independent_of_split(ctx, K):
     """The cluster split only changes who adds which K segments, never the
