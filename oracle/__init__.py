@@ -1,4 +1,4 @@
-"""CPU oracle for Y = act(X . W^T + bias). TEST INFRASTRUCTURE ONLY.
+"""CPU oracle for Y = act(X . W^T + bias) and its backward. TEST INFRASTRUCTURE ONLY.
 
 Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
 leg import this package. The library under ``transformer_linear_layer_gb300``
@@ -61,6 +61,16 @@ def _load():
             lib.oracle_gelu_array.argtypes = [i64, p, p]
             lib.oracle_gelu_array.restype = None
             lib.oracle_max_threads.restype = ctypes.c_int
+            lib.oracle_backward_dz.argtypes = [i64, i64, i64, p, p, p, p, ctypes.c_int, p, ctypes.c_int]
+            lib.oracle_backward_dz.restype = None
+            lib.oracle_gelu_backward.argtypes = [i64, p, p, p]
+            lib.oracle_gelu_backward.restype = None
+            lib.oracle_backward_dx.argtypes = [i64, i64, i64, p, p, p, ctypes.c_int]
+            lib.oracle_backward_dx.restype = None
+            lib.oracle_backward_dw.argtypes = [i64, i64, i64, p, p, p, p, ctypes.c_int]
+            lib.oracle_backward_dw.restype = None
+            lib.oracle_gelu_grad_array.argtypes = [i64, p, p]
+            lib.oracle_gelu_grad_array.restype = None
             _lib = lib
     return _lib
 
@@ -109,6 +119,61 @@ def gelu(x) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float64)
     out = np.empty_like(x)
     _load().oracle_gelu_array(x.size, x.ctypes.data, out.ctypes.data)
+    return out
+
+
+def backward_dz(X, W, dY, bias=None, gelu: bool = False, nthreads: int = 0) -> np.ndarray:
+    """dZ (float64, M x N) = dY * act'(X . W^T + bias)."""
+    X, W, dY = _f32(X), _f32(W), _f32(dY)
+    M, K = X.shape
+    N = W.shape[0]
+    assert W.shape[1] == K and dY.shape == (M, N)
+    b = None if bias is None else _f32(bias)
+    out = np.empty((M, N), dtype=np.float64)
+    _load().oracle_backward_dz(M, N, K, X.ctypes.data, W.ctypes.data, None if b is None else b.ctypes.data,
+                               dY.ctypes.data, int(bool(gelu)), out.ctypes.data, int(nthreads))
+    return out
+
+
+def gelu_backward(dY, Z) -> np.ndarray:
+    """dZ (float64) = dY * gelu'(Z), elementwise; dY and Z hold fp32 values."""
+    dY, Z = _f32(dY), _f32(Z)
+    assert dY.shape == Z.shape
+    out = np.empty(dY.shape, dtype=np.float64)
+    _load().oracle_gelu_backward(dY.size, dY.ctypes.data, Z.ctypes.data, out.ctypes.data)
+    return out
+
+
+def backward_dx(dZ, W, nthreads: int = 0) -> np.ndarray:
+    """dX (float64, M x K) = dZ . W; dZ: M x N, W: N x K (fp32 values)."""
+    dZ, W = _f32(dZ), _f32(W)
+    M, N = dZ.shape
+    N2, K = W.shape
+    assert N == N2
+    out = np.empty((M, K), dtype=np.float64)
+    _load().oracle_backward_dx(M, N, K, dZ.ctypes.data, W.ctypes.data, out.ctypes.data, int(nthreads))
+    return out
+
+
+def backward_dw(dZ, X, with_bias: bool = True, nthreads: int = 0):
+    """(dW (float64, N x K) = dZ^T . X, db (float64, N) = column sums of dZ or
+    None); dZ: M x N, X: M x K (fp32 values)."""
+    dZ, X = _f32(dZ), _f32(X)
+    M, N = dZ.shape
+    M2, K = X.shape
+    assert M == M2
+    dW = np.empty((N, K), dtype=np.float64)
+    db = np.empty((N,), dtype=np.float64) if with_bias else None
+    _load().oracle_backward_dw(M, N, K, dZ.ctypes.data, X.ctypes.data, dW.ctypes.data,
+                               None if db is None else db.ctypes.data, int(nthreads))
+    return dW, db
+
+
+def gelu_grad(x) -> np.ndarray:
+    """The oracle's slope of the tanh-form GELU on a float64 array."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty_like(x)
+    _load().oracle_gelu_grad_array(x.size, x.ctypes.data, out.ctypes.data)
     return out
 
 

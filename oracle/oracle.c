@@ -23,6 +23,8 @@
  *   evaluation but print no formula; this form and its constants are those of
  *   Hendrycks and Gimpel, "Gaussian Error Linear Units" (2016).
  *
+ * The backward of the same layer (dZ, dX, dW, db) is defined further down.
+ *
  * OpenMP splits the (m, n) outputs across threads; each output's k order is
  * fixed, so the result does not depend on the thread count.
  * Build with -ffp-contract=off so no multiply-add is fused and x86 and Arm
@@ -87,6 +89,106 @@ void oracle_gelu_array(int64_t count, const double* in, double* out)
 {
     for (int64_t i = 0; i < count; ++i)
         out[i] = oracle_gelu_tanh(in[i]);
+}
+
+/*
+ * Backward of Y = act(Z), Z = X W^T + bias (the definitions written out).
+ * The pages' backward pass ("Writing a CUDA matmul that catches cuBLAS",
+ * the section on the backward transpose cases) needs dX = dY W^T and
+ * dW = dY^T X for a weight stored in x out; with W stored out x in as here:
+ *
+ *   dZ[m][n] = dY[m][n] * act'(Z[m][n])      (act' = 1, or the GELU slope)
+ *   dX[m][k] = sum_n dZ[m][n] * W[n][k]      (M x K)
+ *   dW[n][k] = sum_m dZ[m][n] * X[m][k]      (N x K)
+ *   db[n]    = sum_m dZ[m][n]
+ *
+ * Sums in double, in ascending order of the summed index, one output at a
+ * time. The slope of the tanh-form GELU g(z) = 0.5 z (1 + tanh u),
+ * u = c (z + a z^3), c = sqrt(2/pi), a = 0.044715, is
+ *   g'(z) = 0.5 (1 + tanh u) + 0.5 z (1 - tanh^2 u) c (1 + 3 a z^2).
+ */
+double oracle_gelu_tanh_grad(double z)
+{
+    const double c = sqrt(2.0 / 3.14159265358979323846);
+    const double a = 0.044715;
+    const double t = tanh(c * (z + a * z * z * z));
+    return 0.5 * (1.0 + t) + 0.5 * z * (1.0 - t * t) * c * (1.0 + 3.0 * a * z * z);
+}
+
+/* dZ from dY and the layer's own inputs (Z recomputed in double).
+   dY: M*N, dZ: M*N (double). */
+void oracle_backward_dz(int64_t M, int64_t N, int64_t K, const float* X, const float* W,
+                        const float* bias, const float* dY, int gelu, double* dZ, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for collapse(2) schedule(static) num_threads(nthreads)
+#endif
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            const double g = (double)dY[m * N + n];
+            dZ[m * N + n] = gelu ? g * oracle_gelu_tanh_grad(one_output(K, X + m * K, W + n * K, bias, n, 0)) : g;
+        }
+    (void)nthreads;
+}
+
+/* dZ from dY and a given pre-activation Z (fp32 values): M*N each. */
+void oracle_gelu_backward(int64_t count, const float* dY, const float* Z, double* dZ)
+{
+    for (int64_t i = 0; i < count; ++i)
+        dZ[i] = (double)dY[i] * oracle_gelu_tanh_grad((double)Z[i]);
+}
+
+/* dX = dZ W. dZ: M*N, W: N*K (fp32 values), dX: M*K (double). */
+void oracle_backward_dx(int64_t M, int64_t N, int64_t K, const float* dZ, const float* W, double* dX,
+                        int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for collapse(2) schedule(static) num_threads(nthreads)
+#endif
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k) {
+            double s = 0.0;
+            for (int64_t n = 0; n < N; ++n)
+                s += (double)dZ[m * N + n] * (double)W[n * K + k];
+            dX[m * K + k] = s;
+        }
+    (void)nthreads;
+}
+
+/* dW = dZ^T X and db = column sums of dZ. dZ: M*N, X: M*K (fp32 values),
+   dW: N*K, db: N or NULL (double). */
+void oracle_backward_dw(int64_t M, int64_t N, int64_t K, const float* dZ, const float* X, double* dW,
+                        double* db, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for collapse(2) schedule(static) num_threads(nthreads)
+#endif
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) {
+            double s = 0.0;
+            for (int64_t m = 0; m < M; ++m)
+                s += (double)dZ[m * N + n] * (double)X[m * K + k];
+            dW[n * K + k] = s;
+        }
+    if (db) {
+        for (int64_t n = 0; n < N; ++n) {
+            double s = 0.0;
+            for (int64_t m = 0; m < M; ++m)
+                s += (double)dZ[m * N + n];
+            db[n] = s;
+        }
+    }
+    (void)nthreads;
+}
+
+/* gelu slope over an array (for its own pins). */
+void oracle_gelu_grad_array(int64_t count, const double* in, double* out)
+{
+    for (int64_t i = 0; i < count; ++i)
+        out[i] = oracle_gelu_tanh_grad(in[i]);
 }
 
 int oracle_max_threads(void)

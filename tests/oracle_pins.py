@@ -166,3 +166,97 @@ LINEAR_PINS = (
     pin_identity, pin_permutation, pin_selector_rect, pin_small_ints, pin_bruteforce_fsum,
     pin_numpy_f64, pin_bias_only, pin_empty_k, pin_bias_then_gelu, pin_golden_hand_example,
 )
+
+
+# ----------------------------------------------------------------- backward
+#
+# Backward pins take ``bwd = (dz, dx, dw)``: dz(X, W, b, dY, gelu) -> dZ,
+# dx(dZ, W) -> dX, dw(dZ, X) -> (dW, db), and ``gg(z) -> gelu'(z)``; the
+# forward ``f`` is the (already pinned) forward oracle.
+
+def _grid(seed, stream, shape, step=2.0 ** -8):
+    """Values on a dyadic grid in [-1, 1): X +- 2^-12 stays exact in fp32."""
+    return (np.round(si.uniform_pm1(seed, stream, shape) / step) * step).astype(np.float32)
+
+
+def pin_gelu_grad_function(gg, g):
+    """gelu'(0) = 1/2; gelu'(z) + gelu'(-z) = 1 (from g(z) - g(-z) = z); the
+    slope tends to 1 and 0 in the tails; it is the central difference of the
+    forward GELU; and torch autograd of gelu(approximate="tanh") agrees."""
+    assert gg(np.array([0.0]))[0] == 0.5
+    z = np.linspace(-6.0, 6.0, 241)
+    assert np.max(np.abs(gg(z) + gg(-z) - 1.0)) <= 1e-14
+    assert abs(gg(np.array([12.0]))[0] - 1.0) <= 1e-12 and abs(gg(np.array([-12.0]))[0]) <= 1e-12
+    h = 1e-5
+    fd = (g(z + h) - g(z - h)) / (2 * h)
+    assert np.max(np.abs(gg(z) - fd)) <= 1e-8
+    t = torch.tensor(z, dtype=torch.float64, requires_grad=True)
+    torch.nn.functional.gelu(t, approximate="tanh").sum().backward()
+    assert np.max(np.abs(gg(z) - t.grad.numpy())) <= 1e-12
+
+
+def pin_backward_finite_differences(f, bwd):
+    """d/dX, d/dW, d/db of L = sum(G * f(X, W, b, act)) by central differences
+    of the forward oracle equal dX = dZ W, dW = dZ^T X, db = sum_m dZ with
+    dZ = G * act'(Z), for the identity and for GELU."""
+    dz, dx, dw = bwd
+    M, N, K = 3, 4, 5
+    X, W, b, G = _grid(51, 1, (M, K)), _grid(51, 2, (N, K)), _grid(51, 3, (N,)), _grid(51, 4, (M, N))
+    h = 2.0 ** -12
+    for gelu in (False, True):
+        L = lambda X_, W_, b_: float(np.sum(G.astype(np.float64) * f(X_, W_, b_, gelu)))
+        dZ = dz(X, W, b, G, gelu)
+        dZf = dZ.astype(np.float32)  # the backward GEMMs take fp32 operands
+        gx, (gw, gb) = dx(dZf, W), dw(dZf, X)
+        num_x, num_w, num_b = np.zeros((M, K)), np.zeros((N, K)), np.zeros(N)
+        for idx in np.ndindex(M, K):
+            Xp, Xm = X.copy(), X.copy()
+            Xp[idx] += h
+            Xm[idx] -= h
+            num_x[idx] = (L(Xp, W, b) - L(Xm, W, b)) / (2 * h)
+        for idx in np.ndindex(N, K):
+            Wp, Wm = W.copy(), W.copy()
+            Wp[idx] += h
+            Wm[idx] -= h
+            num_w[idx] = (L(X, Wp, b) - L(X, Wm, b)) / (2 * h)
+        for n in range(N):
+            bp, bm = b.copy(), b.copy()
+            bp[n] += h
+            bm[n] -= h
+            num_b[n] = (L(X, W, bp) - L(X, W, bm)) / (2 * h)
+        # dZ is rounded to fp32 before the GEMMs: allow that (2^-24 relative)
+        for got, num, what in ((gx, num_x, "dX"), (gw, num_w, "dW"), (gb, num_b, "db")):
+            assert np.max(np.abs(got - num)) <= 1e-5 * max(1.0, np.max(np.abs(num))), f"{what} gelu={gelu}"
+
+
+def pin_backward_closed_forms(bwd):
+    """Index maps: W = I gives dX = dZ; X = I gives dW = dZ^T; a one-hot dZ at
+    (m0, n0) gives dX = W[n0] in row m0 and dW = X[m0] in row n0 (non-square,
+    so a transposed map cannot pass); dZ = 1 gives db = M."""
+    dz, dx, dw = bwd
+    M, N, K = 5, 7, 3
+    dZ = _grid(52, 1, (M, N))
+    assert np.array_equal(dx(dZ, np.eye(N, dtype=np.float32)), dZ.astype(np.float64))
+    dW, _ = dw(dZ, np.eye(M, dtype=np.float32))
+    assert np.array_equal(dW, dZ.T.astype(np.float64))
+    X, W = _grid(52, 2, (M, K)), _grid(52, 3, (N, K))
+    one = np.zeros((M, N), dtype=np.float32)
+    one[3, 5] = 1.0
+    ex = np.zeros((M, K))
+    ex[3] = W[5]
+    assert np.array_equal(dx(one, W), ex), "one-hot dX"
+    ew = np.zeros((N, K))
+    ew[5] = X[3]
+    dW, db = dw(one, X)
+    assert np.array_equal(dW, ew), "one-hot dW"
+    ebias = np.zeros(N)
+    ebias[5] = 1.0
+    assert np.array_equal(db, ebias), "one-hot db"
+    _, db = dw(np.ones((M, N), dtype=np.float32), X)
+    assert np.array_equal(db, np.full(N, float(M))), "db of ones"
+    # identity activation: dZ = dY exactly
+    dY = _grid(52, 4, (M, N))
+    assert np.array_equal(dz(X, W, None, dY, False), dY.astype(np.float64))
+
+
+BACKWARD_PINS = (pin_backward_finite_differences, pin_backward_closed_forms)

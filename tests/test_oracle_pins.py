@@ -133,3 +133,94 @@ def test_rel_err_definition():
     assert oracle.rel_err(np.array([1.0, 2.0]), np.array([1.0, 4.0])) == 0.5
     assert oracle.rel_err(np.array([0.5]), np.array([0.0])) == 0.5
     assert oracle.rel_err(np.zeros((0, 3)), np.zeros((0, 3))) == 0.0
+
+
+# -------------------------------------------------------------- backward ---
+
+from oracle_pins import BACKWARD_PINS, pin_backward_closed_forms, pin_backward_finite_differences, \
+    pin_gelu_grad_function  # noqa: E402
+
+REAL_BWD = (lambda X, W, b, dY, g: oracle.backward_dz(X, W, dY, b, g),
+            lambda dZ, W: oracle.backward_dx(dZ, W),
+            lambda dZ, X: oracle.backward_dw(dZ, X))
+
+
+def test_gelu_grad_meets_pin():
+    pin_gelu_grad_function(oracle.gelu_grad, oracle.gelu)
+
+
+@pytest.mark.parametrize("pin", BACKWARD_PINS, ids=lambda p: p.__name__)
+def test_backward_meets_pin(pin):
+    if pin is pin_backward_finite_differences:
+        pin(real, REAL_BWD)
+    else:
+        pin(REAL_BWD)
+
+
+def test_gelu_backward_matches_dz():
+    """The elementwise form (given Z) equals the recomputing form."""
+    X = si.normal(9, 1, (6, 40))
+    W = si.normal(9, 2, (11, 40), 0.0, 0.2)
+    b = si.normal(9, 3, (11,), 0.0, 0.1)
+    dY = si.normal(9, 4, (6, 11))
+    Z = oracle.linear(X, W, b, False).astype(np.float32)
+    ref = oracle.backward_dz(X, W, dY, b, True)
+    got = oracle.gelu_backward(dY, Z)
+    assert np.max(np.abs(got - ref)) <= 1e-6 * np.max(np.abs(ref))
+
+
+def _gg_np(z, c3=0.044715, three=3.0, half_sign=1.0):
+    c = math.sqrt(2.0 / math.pi)
+    t = np.tanh(c * (z + c3 * z ** 3))
+    return 0.5 * (1.0 + t) + half_sign * 0.5 * z * (1.0 - t * t) * c * (1.0 + three * c3 * z * z)
+
+
+def _bwd_np(dz_gelu_grad=_gg_np, dx_transposed=False, dw_transposed=False, db_rows=False, no_grad=False):
+    """Numpy restatement with one optional planted mistake."""
+    def dz(X, W, b, dY, gelu):
+        Z = X.astype(np.float64) @ W.astype(np.float64).T + (0 if b is None else b.astype(np.float64))
+        g = dY.astype(np.float64)
+        return g * dz_gelu_grad(Z) if (gelu and not no_grad) else g
+
+    def dx(dZ, W):
+        dZ, W = dZ.astype(np.float64), W.astype(np.float64)
+        if dx_transposed:  # W read as in x out
+            return dZ @ W.reshape(W.shape[1], W.shape[0]).T if W.shape[0] != W.shape[1] else dZ @ W.T
+        return dZ @ W
+
+    def dw(dZ, X):
+        dZ, X = dZ.astype(np.float64), X.astype(np.float64)
+        dW = (X.T @ dZ).reshape(dZ.shape[1], X.shape[1]) if dw_transposed else dZ.T @ X
+        db = dZ.sum(axis=1)[: dZ.shape[1]] if db_rows else dZ.sum(axis=0)
+        if db_rows and db.shape[0] < dZ.shape[1]:
+            db = np.resize(db, dZ.shape[1])
+        return dW, db
+    return dz, dx, dw
+
+
+BWD_MUTANTS = {
+    "dx_transposed_W": _bwd_np(dx_transposed=True),
+    "dw_transposed": _bwd_np(dw_transposed=True),
+    "db_over_rows": _bwd_np(db_rows=True),
+    "gelu_slope_missing": _bwd_np(no_grad=True),
+    "gelu_slope_a_not_3a": _bwd_np(dz_gelu_grad=lambda z: _gg_np(z, three=1.0)),
+    "gelu_slope_sign": _bwd_np(dz_gelu_grad=lambda z: _gg_np(z, half_sign=-1.0)),
+}
+
+
+def test_backward_mutant_reference_is_sound():
+    ref = _bwd_np()
+    pin_backward_closed_forms(ref)
+    pin_backward_finite_differences(real, ref)
+
+
+@pytest.mark.parametrize("name", sorted(BWD_MUTANTS))
+def test_backward_pins_catch_mutant(name):
+    mutant = BWD_MUTANTS[name]
+    caught = False
+    for pin in (pin_backward_closed_forms, lambda b: pin_backward_finite_differences(real, b)):
+        try:
+            pin(mutant)
+        except (AssertionError, ValueError):
+            caught = True
+    assert caught, f"no backward pin catches mutant {name}"
