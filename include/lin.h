@@ -164,6 +164,40 @@ LIN_API int lin_plan_query(int sm_count, int M, int N, int K, int precision, int
 LIN_API int lin_plan_make(int sm_count, int kernel, int variant, int splits, int M, int N, int K,
                   int precision, lin_plan* out);
 
+/* ---- Backward (training) ----
+ * The backward pass of the same layer ("Writing a CUDA matmul that catches
+ * cuBLAS", the backward transpose cases: dX = dY W^T and dW = dY^T X for a
+ * weight stored in x out; here W is stored out x in):
+ *   dZ = dY * act'(Z)           (lin_gelu_backward, or dZ = dY for no activation)
+ *   dX = dZ . W      (M x K)    (lin_backward_data)
+ *   dW = dZ^T . X    (N x K)    (lin_backward_weight, with db = sum over rows of dZ)
+ * Operands are in the precision's input type and results in its output type
+ * (bf16 for LIN_PREC_BF16, fp32 otherwise; db is always fp32). BF16 runs on
+ * the tensor cores with the transposes folded into the operands' shared-memory
+ * layout (nothing is transposed in memory); FP32 and TF32 run exact fp32
+ * FFMAs. Results are bitwise repeatable. Calls are asynchronous on `stream`
+ * and follow lin_forward's early-start rules. */
+
+/* dX (M x K) = dZ (M x N) . W (N x K), all row-major. dZ, W and dX 16-byte
+ * aligned; K * element size a multiple of 16; for BF16 also N * 2 (the rows
+ * of dZ are read by TMA). dX must not overlap dZ or W. N == 0 gives zeros. */
+LIN_API int lin_backward_data(lin_ctx* ctx, int M, int N, int K, const void* dZ, const void* W, void* dX,
+                              int precision, void* stream);
+
+/* dW (N x K) = dZ^T . X (dZ: M x N, X: M x K), and db[n] = sum_m dZ[m][n]
+ * in fp32 when db is not NULL (two passes over fixed row chunks, in order;
+ * uses the context workspace: LIN_ERR_WORKSPACE when it is too small). The
+ * alignment rules of lin_backward_data apply to dZ, X and dW; db is 4-byte
+ * aligned. M == 0 gives zeros. */
+LIN_API int lin_backward_weight(lin_ctx* ctx, int M, int N, int K, const void* dZ, const void* X, void* dW,
+                                float* db, int precision, void* stream);
+
+/* dZ = dY * gelu'(Z) elementwise over `count` values, Z the pre-activation
+ * (act's input) of the forward; the slope of the tanh form used by the
+ * forward. dZ may be dY (in place) but not Z. */
+LIN_API int lin_gelu_backward(lin_ctx* ctx, long long count, const void* dY, const void* Z, void* dZ,
+                              int precision, void* stream);
+
 /* Synchronise `stream`, read and clear the context's device status word.
  * Returns LIN_ERR_DEVICE_TIMEOUT if any kernel since the last check gave up
  * a bounded wait (its output is then incomplete), LIN_ERR_CUDA on a CUDA

@@ -20,6 +20,7 @@ from .build import build
 
 __all__ = [
     "LinError", "Context", "Plan", "forward", "forward_plan", "plan_query", "plan_make", "build",
+    "backward_data", "backward_weight", "gelu_backward",
     "library", "PREC_FP32", "PREC_TF32", "PREC_BF16", "EPI_NONE", "EPI_GELU_TANH",
     "KERNEL_NONE", "KERNEL_FILL", "KERNEL_SKINNY", "KERNEL_FFMA", "KERNEL_TC", "KERNEL_GEMV",
 ]
@@ -89,6 +90,9 @@ def library() -> ctypes.CDLL:
                 "lin_set_option": ([P, I, ctypes.c_longlong], I),
                 "lin_ctx_last_plan": ([P, PP], I),
                 "lin_forward_fp32_static": ([I, I, I, P, P, P, P, I, P], I),
+                "lin_backward_data": ([P, I, I, I, P, P, P, I, P], I),
+                "lin_backward_weight": ([P, I, I, I, P, P, P, P, I, P], I),
+                "lin_gelu_backward": ([P, ctypes.c_longlong, P, P, P, I, P], I),
                 "lin_strerror": ([I], ctypes.c_char_p),
                 "lin_abi_version": ([], I),
             }
@@ -264,4 +268,90 @@ def forward_plan(plan: Plan, x, w, bias=None, epilogue="none", precision=None, o
                               _stream_ptr(stream, dev))
     if rc != OK:
         raise LinError(rc, "lin_forward_plan")
+    return out
+
+
+# ---------------------------------------------------------------- backward
+
+def _bwd_dtype(t, precision):
+    import torch
+
+    prec = precision
+    if prec is None:
+        prec = "bf16" if t.dtype == torch.bfloat16 else "fp32"
+    prec = _prec(prec)
+    return prec, (torch.bfloat16 if prec == PREC_BF16 else torch.float32)
+
+
+def _check(t, want, shape, what):
+    if t.dtype != want or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{what} must be a contiguous {want} CUDA tensor of shape {tuple(shape)}")
+
+
+def backward_data(dz, w, out=None, precision=None, ctx: Context | None = None, stream=None):
+    """dX (M x K) = dz (M x N) . w (N x K): the input gradient of the layer
+    (dz = dY times the activation's slope)."""
+    import torch
+
+    prec, want = _bwd_dtype(dz, precision)
+    M, N = dz.shape
+    K = w.shape[1]
+    _check(dz, want, (M, N), "dz")
+    _check(w, want, (N, K), "w")
+    if out is None:
+        out = torch.empty((M, K), dtype=want, device=dz.device)
+    _check(out, want, (M, K), "out")
+    dev = dz.device.index if dz.device.index is not None else 0
+    ctx = ctx or default_context(dev)
+    rc = library().lin_backward_data(ctx._h, M, N, K, dz.data_ptr(), w.data_ptr(), out.data_ptr(), prec,
+                                     _stream_ptr(stream, dev))
+    if rc != OK:
+        raise LinError(rc, "lin_backward_data")
+    return out
+
+
+def backward_weight(dz, x, out=None, db=None, precision=None, ctx: Context | None = None, stream=None):
+    """dW (N x K) = dz^T . x (dz: M x N, x: M x K) and, when ``db`` is True or
+    an fp32 tensor of length N, db = the column sums of dz. Returns (dW, db)."""
+    import torch
+
+    prec, want = _bwd_dtype(dz, precision)
+    M, N = dz.shape
+    K = x.shape[1]
+    _check(dz, want, (M, N), "dz")
+    _check(x, want, (M, K), "x")
+    if out is None:
+        out = torch.empty((N, K), dtype=want, device=dz.device)
+    _check(out, want, (N, K), "out")
+    if db is True:
+        db = torch.empty((N,), dtype=torch.float32, device=dz.device)
+    if db is not None and db is not False:
+        _check(db, torch.float32, (N,), "db")
+    else:
+        db = None
+    dev = dz.device.index if dz.device.index is not None else 0
+    ctx = ctx or default_context(dev)
+    rc = library().lin_backward_weight(ctx._h, M, N, K, dz.data_ptr(), x.data_ptr(), out.data_ptr(),
+                                       None if db is None else db.data_ptr(), prec, _stream_ptr(stream, dev))
+    if rc != OK:
+        raise LinError(rc, "lin_backward_weight")
+    return out, db
+
+
+def gelu_backward(dy, z, out=None, precision=None, ctx: Context | None = None, stream=None):
+    """dZ = dy * gelu'(z) (z: the forward's pre-activation), elementwise."""
+    import torch
+
+    prec, want = _bwd_dtype(dy, precision)
+    _check(dy, want, tuple(dy.shape), "dy")
+    _check(z, want, tuple(dy.shape), "z")
+    if out is None:
+        out = torch.empty_like(dy)
+    _check(out, want, tuple(dy.shape), "out")
+    dev = dy.device.index if dy.device.index is not None else 0
+    ctx = ctx or default_context(dev)
+    rc = library().lin_gelu_backward(ctx._h, dy.numel(), dy.data_ptr(), z.data_ptr(), out.data_ptr(), prec,
+                                     _stream_ptr(stream, dev))
+    if rc != OK:
+        raise LinError(rc, "lin_gelu_backward")
     return out

@@ -47,6 +47,8 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
     return *reinterpret_cast<uint16_t*>(&h);
 }
 
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
 }

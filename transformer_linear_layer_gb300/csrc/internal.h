@@ -83,4 +83,26 @@ int launch_ffma(const Problem& p, const lin_plan& plan);
 int launch_tc(const Problem& p, const lin_plan& plan);
 int launch_gemv(const Problem& p, const lin_plan& plan);
 
+// Backward (training) GEMMs of the layer: which 1: dX = dZ W (M x K);
+// which 2: dW = dZ^T X (N x K). B is W (which 1) or X (which 2).
+struct BwdProblem {
+    int which;
+    int M, N, K;       // the forward layer's sizes
+    const void* dZ;    // M x N
+    const void* B;     // W (N x K) or X (M x K)
+    void* out;         // dX (M x K) or dW (N x K)
+    cudaStream_t stream;
+    int* dev_status;
+    int sm_count;
+    bool early_start;  // may start before the previous kernel on the stream finishes
+    bool early_x;      // and read dZ and B before it finishes
+};
+int launch_tc_backward(const BwdProblem& q);
+int launch_bwd_ffma(int which, int M, int N, int K, const float* dZ, const float* B, float* out, cudaStream_t st,
+                    bool early);
+int launch_gelu_backward(long long count, const void* dY, const void* Z, void* dZ, bool bf16, int sm_count,
+                         cudaStream_t st, bool early);
+size_t colsum_workspace_bytes(int M, int N);
+int launch_colsum(int M, int N, const void* dZ, float* db, bool bf16, void* workspace, cudaStream_t st);
+
 }  // namespace lin

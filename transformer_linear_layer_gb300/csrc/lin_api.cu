@@ -327,6 +327,18 @@ void early_reads_ok(cudaStream_t st, Range w, Range bias, Range x, Range y, bool
     g_last[slot].hi = g_last[slot].lo + y.bytes;
 }
 
+// Record `y` as the last output on stream `st` (for a call whose last kernel
+// writes a different range than its main output).
+void note_output(cudaStream_t st, Range y) {
+    std::lock_guard<std::mutex> lk(g_last_mu);
+    for (int i = 0; i < g_last_n; ++i)
+        if (g_last[i].stream == st) {
+            g_last[i].lo = reinterpret_cast<uintptr_t>(y.p);
+            g_last[i].hi = g_last[i].lo + y.bytes;
+            return;
+        }
+}
+
 int check_plan_fits(const lin_plan& p, int M, int N, int K, int precision) {
     switch (p.kernel) {
         case LIN_KERNEL_NONE: return (M == 0 || N == 0) ? LIN_OK : LIN_ERR_UNSUPPORTED;
@@ -575,6 +587,115 @@ int lin_forward(lin_ctx* ctx, int M, int N, int K, const void* X, const void* W,
     const int rc = lin::plan_default(ctx->sm_count, M, N, K, precision, ctx->workspace_bytes, &plan);
     if (rc != LIN_OK) return rc;
     return lin::run(ctx, plan, M, N, K, X, W, bias, Y, epilogue, precision, stream, true);
+}
+
+namespace {
+
+// Shared checks of the two backward GEMMs: returns LIN_OK and fills q, or an error.
+int backward_setup(lin_ctx* ctx, int which, int M, int N, int K, const void* dZ, const void* B, void* out,
+                   int precision, void* stream, lin::BwdProblem* q) {
+    using namespace lin;
+    if (!ctx || M < 0 || N < 0 || K < 0 || !valid_enums(0, precision)) return LIN_ERR_ARG;
+    const size_t esz = precision == LIN_PREC_BF16 ? 2 : 4;
+    const int Mo = which == 1 ? M : N;
+    const size_t out_bytes = (size_t)Mo * K * esz;
+    if (Mo == 0 || K == 0) return LIN_OK;
+    if (!out || (M > 0 && N > 0 && (!dZ || !B))) return LIN_ERR_ARG;
+    const size_t dz_bytes = (size_t)M * N * esz;
+    const size_t b_bytes = (size_t)(which == 1 ? N : M) * K * esz;
+    if (overlaps(out, out_bytes, dZ, dz_bytes) || overlaps(out, out_bytes, B, b_bytes)) return LIN_ERR_ARG;
+    if ((((uintptr_t)dZ | (uintptr_t)B | (uintptr_t)out) % 16) != 0 || ((size_t)K * esz) % 16 != 0) return LIN_ERR_ALIGN;
+    if (precision == LIN_PREC_BF16 && ((size_t)N * esz) % 16 != 0) return LIN_ERR_ALIGN;  // dZ rows by TMA
+    q->which = which;
+    q->M = M;
+    q->N = N;
+    q->K = K;
+    q->dZ = dZ;
+    q->B = B;
+    q->out = out;
+    q->stream = static_cast<cudaStream_t>(stream);
+    q->dev_status = ctx->dev_status;
+    q->sm_count = ctx->sm_count;
+    bool w_ok = false, x_ok = false, known = false;
+    early_reads_ok(q->stream, Range{B, b_bytes}, Range{nullptr, 0}, Range{dZ, dz_bytes}, Range{out, out_bytes}, &w_ok,
+                   &x_ok, &known);
+    q->early_start = ctx->early_start && w_ok;
+    q->early_x = q->early_start && x_ok;
+    return LIN_OK;
+}
+
+int backward_run(const lin::BwdProblem& q, int precision) {
+    using namespace lin;
+    const int R = q.which == 1 ? q.N : q.M;
+    const int Mo = q.which == 1 ? q.M : q.N;
+    if (R == 0)
+        return cudaMemsetAsync(q.out, 0, (size_t)Mo * q.K * (precision == LIN_PREC_BF16 ? 2 : 4), q.stream) == cudaSuccess
+                   ? LIN_OK
+                   : LIN_ERR_CUDA;
+    if (precision == LIN_PREC_BF16) return launch_tc_backward(q);
+    return launch_bwd_ffma(q.which, q.M, q.N, q.K, static_cast<const float*>(q.dZ), static_cast<const float*>(q.B),
+                           static_cast<float*>(q.out), q.stream, q.early_start);
+}
+
+}  // namespace
+
+int lin_backward_data(lin_ctx* ctx, int M, int N, int K, const void* dZ, const void* W, void* dX, int precision,
+                      void* stream) {
+    lin::BwdProblem q;
+    q.which = 0;
+    const int rc = backward_setup(ctx, 1, M, N, K, dZ, W, dX, precision, stream, &q);
+    if (rc != LIN_OK || q.which == 0) return rc;
+    lin::DeviceGuard guard(ctx->device);
+    if (!guard.ok) return LIN_ERR_CUDA;
+    return backward_run(q, precision);
+}
+
+int lin_backward_weight(lin_ctx* ctx, int M, int N, int K, const void* dZ, const void* X, void* dW, float* db,
+                        int precision, void* stream) {
+    using namespace lin;
+    lin::BwdProblem q;
+    q.which = 0;
+    int rc = backward_setup(ctx, 2, M, N, K, dZ, X, dW, precision, stream, &q);
+    if (rc != LIN_OK) return rc;
+    if (db) {
+        if ((uintptr_t)db % 4 != 0) return LIN_ERR_ALIGN;
+        const size_t esz = precision == LIN_PREC_BF16 ? 2 : 4;
+        if (overlaps(db, (size_t)N * 4, dZ, (size_t)M * N * esz) || overlaps(db, (size_t)N * 4, X, (size_t)M * K * esz) ||
+            overlaps(db, (size_t)N * 4, dW, (size_t)N * K * esz))
+            return LIN_ERR_ARG;
+        if (M > 0 && N > 0 && colsum_workspace_bytes(M, N) > ctx->workspace_bytes) return LIN_ERR_WORKSPACE;
+    }
+    lin::DeviceGuard guard(ctx->device);
+    if (!guard.ok) return LIN_ERR_CUDA;
+    if (q.which != 0) {
+        rc = backward_run(q, precision);
+        if (rc != LIN_OK) return rc;
+    }
+    if (db && N > 0) {
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        rc = launch_colsum(M, N, dZ, db, precision == LIN_PREC_BF16, ctx->workspace, st);
+        if (rc != LIN_OK) return rc;
+        note_output(st, Range{db, (size_t)N * 4});
+    }
+    return LIN_OK;
+}
+
+int lin_gelu_backward(lin_ctx* ctx, long long count, const void* dY, const void* Z, void* dZ, int precision,
+                      void* stream) {
+    using namespace lin;
+    if (!ctx || count < 0 || !valid_enums(0, precision)) return LIN_ERR_ARG;
+    if (count == 0) return LIN_OK;
+    if (!dY || !Z || !dZ) return LIN_ERR_ARG;
+    const size_t esz = precision == LIN_PREC_BF16 ? 2 : 4;
+    const size_t bytes = (size_t)count * esz;
+    if (overlaps(dZ, bytes, Z, bytes)) return LIN_ERR_ARG;  // dZ may overwrite dY in place
+    if ((((uintptr_t)dY | (uintptr_t)Z | (uintptr_t)dZ) % esz) != 0) return LIN_ERR_ALIGN;
+    DeviceGuard guard(ctx->device);
+    if (!guard.ok) return LIN_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    bool w_ok = false, x_ok = false, known = false;
+    early_reads_ok(st, Range{Z, bytes}, Range{nullptr, 0}, Range{dY, bytes}, Range{dZ, bytes}, &w_ok, &x_ok, &known);
+    return launch_gelu_backward(count, dY, Z, dZ, precision == LIN_PREC_BF16, ctx->sm_count, st, ctx->early_start);
 }
 
 int lin_forward_plan(lin_ctx* ctx, const lin_plan* plan, int M, int N, int K, const void* X, const void* W,

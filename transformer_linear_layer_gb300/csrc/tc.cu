@@ -104,7 +104,17 @@ constexpr size_t tc_smem_bytes() {
 // sets one flag per epilogue warp; CTA b reaches the earlier K stages last,
 // waits for the flags, adds the partial sums to its accumulator in that fixed
 // order and runs the epilogue (deterministic for a given plan).
-template <bool BF16, int BN, bool GELU, bool PAIR, bool SK>
+//
+// LAY: operand layouts (bf16, single-CTA, whole tiles only). 0: both K-major
+// (the forward, Y = X W^T). 1: B MN-major (dX = dZ W: A = dZ, B = W read with
+// the output column contiguous). 2: A and B MN-major (dW = dZ^T X: A = dZ and
+// B = X, both read with the reduction index as the row). The transposes of
+// the backward pass are index maps of the TMA boxes and the descriptors'
+// major-ness ("Writing a CUDA matmul that catches cuBLAS": keep each operand
+// in the layout that makes staging a vector copy, choose the fragment layout
+// to match); nothing is transposed in memory. An MN-major stage is one box of
+// 64 (MN) x 64 (K rows) per 64 rows or columns of the tile.
+template <bool BF16, int BN, bool GELU, bool PAIR, bool SK, int LAY>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
           const __grid_constant__ CUtensorMap tmY, const TcArgs a) {
@@ -119,7 +129,9 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     constexpr int MMAS = 4;                       // 32 bytes of K per MMA
     constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;  // two accumulators
     constexpr uint32_t BUF_COLS = BN <= 128 ? BN : 256;          // column offset of the second one
-    constexpr uint32_t IDESC = make_idesc(BF16 ? 1u : 2u, PAIR ? 2 * BM : BM, BN);
+    constexpr bool A_MN = LAY == 2, B_MN = LAY >= 1;
+    static_assert(LAY == 0 || (BF16 && !PAIR && !SK), "MN-major operands: bf16, single-CTA tiles");
+    constexpr uint32_t IDESC = make_idesc(BF16 ? 1u : 2u, PAIR ? 2 * BM : BM, BN, A_MN, B_MN);
     constexpr int EPI_WARPS = kTcThreads / 32 - 2;  // two per TMEM lane quadrant
     constexpr int HALF = BN / 2;                  // columns per epilogue warp
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "N tile");
@@ -232,8 +244,22 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                         tma_load_2d_pair(smem_u32(sB + s * B_BYTES), &tmB, fb, kb * BK, n0 + (int)rank * BROWS);
                     } else {
                         mbar_expect_tx(full0 + 8 * s, STAGE_TX);
-                        tma_load_2d(smem_u32(sA + s * A_BYTES), &tmA, full0 + 8 * s, kb * BK, m0);
-                        tma_load_2d(smem_u32(sB + s * B_BYTES), &tmB, full0 + 8 * s, kb * BK, n0);
+                        if constexpr (A_MN) {
+#pragma unroll
+                            for (int j = 0; j < BM / 64; ++j)
+                                tma_load_2d(smem_u32(sA + s * A_BYTES + j * 8192), &tmA, full0 + 8 * s, m0 + 64 * j,
+                                            kb * BK);
+                        } else {
+                            tma_load_2d(smem_u32(sA + s * A_BYTES), &tmA, full0 + 8 * s, kb * BK, m0);
+                        }
+                        if constexpr (B_MN) {
+#pragma unroll
+                            for (int j = 0; j < BN / 64; ++j)
+                                tma_load_2d(smem_u32(sB + s * B_BYTES + j * 8192), &tmB, full0 + 8 * s, n0 + 64 * j,
+                                            kb * BK);
+                        } else {
+                            tma_load_2d(smem_u32(sB + s * B_BYTES), &tmB, full0 + 8 * s, kb * BK, n0);
+                        }
                     }
                     issued = it + 1;
                 }
@@ -269,8 +295,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = sw128_kmajor_desc(smem_u32(sA + s * A_BYTES));
-                    const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + s * B_BYTES));
+                    const uint64_t ad = A_MN ? sw128_mnmajor_desc(smem_u32(sA + s * A_BYTES))
+                                             : sw128_kmajor_desc(smem_u32(sA + s * A_BYTES));
+                    const uint64_t bd = B_MN ? sw128_mnmajor_desc(smem_u32(sB + s * B_BYTES))
+                                             : sw128_kmajor_desc(smem_u32(sB + s * B_BYTES));
+                    // K advance per MMA: 32 bytes of a K-major row, or 16 rows of an MN-major tile.
+                    constexpr uint32_t ASTEP = A_MN ? 128u : 2u, BSTEP = B_MN ? 128u : 2u;
                     if constexpr (PAIR) {
 #pragma unroll
                         for (int kk = 0; kk < MMAS; ++kk)
@@ -279,7 +309,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     } else {
 #pragma unroll
                         for (int kk = 0; kk < MMAS; ++kk)
-                            tc_mma<BF16>(d, ad + 2u * kk, bd + 2u * kk, IDESC, (kb != lo || kk != 0) ? 1u : 0u);
+                            tc_mma<BF16>(d, ad + ASTEP * kk, bd + BSTEP * kk, IDESC, (kb != lo || kk != 0) ? 1u : 0u);
                         tc_commit(empty0 + 8 * s);
                     }
                 }
@@ -539,12 +569,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 
 // ---------------------------------------------------------------- host side
 
-template <bool BF16, int BN, bool GELU, bool PAIR, bool SK>
+template <bool BF16, int BN, bool GELU, bool PAIR, bool SK, int LAY = 0>
 int launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const TcArgs& a, int grid, bool early,
                cudaStream_t st) {
     constexpr size_t smem = tc_smem_bytes<BF16, BN, PAIR>();
     static_assert(tc_smem_bytes<BF16, BN, PAIR>() <= 227 * 1024, "shared memory");
-    auto kern = tc_kernel<BF16, BN, GELU, PAIR, SK>;
+    auto kern = tc_kernel<BF16, BN, GELU, PAIR, SK, LAY>;
     static unsigned long long attr_set = 0;  // one attribute call per instantiation and device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return LIN_ERR_CUDA;
@@ -646,6 +676,60 @@ bool make_out_map_bf16(CUtensorMap* map, void* base, int M, int N) {
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool make_mnmajor_map(CUtensorMap* map, const void* base, int rows, int cols) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    cuuint32_t box[2] = {64, 64};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// bf16 backward GEMMs on the tensor cores, 128 x 256 single-CTA tiles:
+//   which 1: dX (M x K) = dZ (M x N) . W (N x K): A = dZ K-major, B = W MN-major.
+//   which 2: dW (N x K) = dZ^T . X (M x K):       A = dZ MN-major, B = X MN-major.
+// Rows of dZ, W and X must be 16-byte aligned (N and K multiples of 8).
+int launch_tc_backward(const BwdProblem& q) {
+    const int Mo = q.which == 1 ? q.M : q.N;  // output rows
+    const int No = q.K;                       // output columns
+    const int R = q.which == 1 ? q.N : q.M;   // reduction
+    CUtensorMap ta, tb, ty;
+    if (q.which == 1) {
+        if (!make_kmajor_map(&ta, q.dZ, true, q.M, q.N, 128)) return LIN_ERR_CUDA;
+        if (!make_mnmajor_map(&tb, q.B, q.N, q.K)) return LIN_ERR_CUDA;
+    } else {
+        if (!make_mnmajor_map(&ta, q.dZ, q.M, q.N)) return LIN_ERR_CUDA;
+        if (!make_mnmajor_map(&tb, q.B, q.M, q.K)) return LIN_ERR_CUDA;
+    }
+    TcArgs a = {};
+    a.M = Mo;
+    a.N = No;
+    a.K = R;
+    a.bias = nullptr;
+    a.Y = q.out;
+    a.status = q.dev_status;
+    a.y_aligned16 = (reinterpret_cast<uintptr_t>(q.out) % 16) == 0;
+    a.bias_aligned16 = 0;
+    a.early_inputs = q.early_x ? 1 : 0;
+    a.partials = nullptr;
+    a.flags = nullptr;
+    ty = ta;
+    a.y_tma = 0;
+    if (a.y_aligned16 && No % 8 == 0) {
+        if (!make_out_map_bf16(&ty, q.out, Mo, No)) return LIN_ERR_CUDA;
+        a.y_tma = 1;
+    }
+    const long long tiles = (long long)((Mo + 127) / 128) * ((No + 255) / 256);
+    const int grid = (int)(tiles < q.sm_count ? tiles : q.sm_count);
+    if (q.which == 1)
+        return launch_cfg<true, kTcCfg[0].bn, false, false, false, 1>(ta, tb, ty, a, grid, q.early_start, q.stream);
+    return launch_cfg<true, kTcCfg[0].bn, false, false, false, 2>(ta, tb, ty, a, grid, q.early_start, q.stream);
 }
 
 int launch_tc(const Problem& p, const lin_plan& plan) {

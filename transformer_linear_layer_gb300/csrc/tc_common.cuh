@@ -145,12 +145,28 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
     return d;
 }
 
+// Descriptor for an MN-major tile written by TMA boxes of 64 (MN, 128 bytes)
+// x 64 (K rows) with the 128-byte swizzle: the leading byte offset is the
+// distance between 64-element MN chunks (one box, 8 KiB), the stride byte
+// offset the distance between 8-row K groups (1 KiB). One MMA of K = 16
+// advances the start by 16 rows = 2 KiB (+128 in the low field). Checked
+// against a CPU product for MN-major A, B and both.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(8192u >> 4) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
 // Instruction descriptor (kind::f16 / kind::tf32): D fp32 (bits 4-5 = 1),
-// A and B format (bits 7-9, 10-12: 1 = bf16, 2 = tf32), both K-major
-// (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-constexpr uint32_t make_idesc(uint32_t ab_format, int m, int n) {
-    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
-           (static_cast<uint32_t>(m >> 4) << 24);
+// A and B format (bits 7-9, 10-12: 1 = bf16, 2 = tf32), A and B MN-major
+// flags (bits 15, 16; 0 = K-major), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t make_idesc(uint32_t ab_format, int m, int n, bool a_mn = false, bool b_mn = false) {
+    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 template <bool BF16>
@@ -363,5 +379,9 @@ bool make_kmajor_map(CUtensorMap* map, const void* base, bool bf16, int rows, in
 // the 64-byte swizzle (16-byte piece p of row r at piece p ^ ((r >> 1) & 3)).
 // Needs a 16-byte aligned base and N a multiple of 8.
 bool make_out_map_bf16(CUtensorMap* map, void* base, int M, int N);
+// 2-D tensor map over a rows x cols row-major bf16 tensor read MN-major: box =
+// 64 columns (128 bytes, the MN direction) x 64 rows (the K direction), 128-byte
+// swizzle, out-of-range elements read as zero. Needs cols a multiple of 8.
+bool make_mnmajor_map(CUtensorMap* map, const void* base, int rows, int cols);
 
 }  // namespace lin
