@@ -408,6 +408,154 @@ def bench_ours(layer: si.Layer, steps: int, warmup: int, world: int, rank: int, 
     return line
 
 
+# ---------------------------------------------------------------- backward
+
+class BwdWork:
+    """A backward GEMM of a layer: which 1 is dX = dZ W (M x K, reduction N),
+    which 2 is dW = dZ^T X (N x K, reduction M)."""
+
+    def __init__(self, name, which, M, N, K, precision):
+        self.name, self.which, self.M, self.N, self.K, self.precision = name, which, M, N, K, precision
+        self.flops = 2.0 * M * N * K
+
+    def algorithmic_bytes(self):
+        esz = 2 if self.precision == si.PREC_BF16 else 4
+        other = self.N * self.K if self.which == 1 else self.M * self.K   # W or X
+        out = self.M * self.K if self.which == 1 else self.N * self.K     # dX or dW
+        return (self.M * self.N + other + out) * esz
+
+
+BWD_WORKLOADS = [BwdWork(f"{base}_{'dx' if which == 1 else 'dw'}", which, M, N, K, prec)
+                 for base, M, N, K, prec in (("gpt2_fc1_m8192_bf16", 8192, 3072, 768, si.PREC_BF16),
+                                             ("gpt2_fc2_m8192_bf16", 8192, 768, 3072, si.PREC_BF16),
+                                             ("gpt2_fc1_m128_fp32", 128, 3072, 768, si.PREC_FP32),
+                                             ("gpt2_fc2_m128_fp32", 128, 768, 3072, si.PREC_FP32))
+                 for which in (1, 2)]
+
+
+def bench_backward(work: BwdWork, steps: int, warmup: int, world: int, rank: int, local_rank: int):
+    """Back-to-back backward GEMMs through the C ABI (lin_backward_data /
+    lin_backward_weight), dZ rotating over copies larger than L2, replayed from
+    a CUDA graph; parity gate on sampled output rows against the oracle."""
+    import torch
+
+    import oracle
+    import transformer_linear_layer_gb300 as tll
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    ctx = tll.Context(local_rank)
+    lib = tll.library()
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20))
+    prec = PREC_NAME[work.precision]
+    dt = torch.bfloat16 if work.precision == si.PREC_BF16 else torch.float32
+    esz = 2 if work.precision == si.PREC_BF16 else 4
+    M, N, K = work.M, work.N, work.K
+    dZ = si.normal(31, 1, (M, N), 0.0, 0.1)
+    B = si.normal(31, 2, (N, K), 0.0, 0.02) if work.which == 1 else si.normal(31, 3, (M, K))
+    if work.precision == si.PREC_BF16:
+        dZ, B = si.round_bf16(dZ), si.round_bf16(B)
+    dz0 = torch.from_numpy(dZ).to(dev).to(dt)
+    b_dev = torch.from_numpy(B).to(dev).to(dt)
+    dz_bytes = M * N * esz
+    n_copies = max(2, math.ceil(4 * l2 / dz_bytes))
+    while n_copies > 2 and n_copies * dz_bytes > (8 << 30):
+        n_copies -= 1
+    dzs = [dz0] + [dz0.clone() for _ in range(n_copies - 1)]
+    out = torch.empty((M, K) if work.which == 1 else (N, K), dtype=dt, device=dev)
+    stream = torch.cuda.Stream(dev)
+    sptr = stream.cuda_stream
+    fn = lib.lin_backward_data if work.which == 1 else lib.lin_backward_weight
+
+    def step(i):
+        if work.which == 1:
+            rc = fn(ctx._h, M, N, K, dzs[i % n_copies].data_ptr(), b_dev.data_ptr(), out.data_ptr(),
+                    work.precision, sptr)
+        else:
+            rc = fn(ctx._h, M, N, K, dzs[i % n_copies].data_ptr(), b_dev.data_ptr(), out.data_ptr(), None,
+                    work.precision, sptr)
+        if rc != 0:
+            raise tll.LinError(rc, "lin_backward")
+
+    with torch.cuda.stream(stream):
+        step(0)
+    stream.synchronize()
+    ctx.check(stream)
+    rng = np.random.default_rng(2)
+    rows = np.unique(np.concatenate([rng.integers(0, out.shape[0], 64), [0, out.shape[0] - 1]]))
+    if work.which == 1:
+        ref = oracle.backward_dx(dZ[rows], B)
+    else:
+        ref, _ = oracle.backward_dw(dZ[:, rows], B, with_bias=False)
+    got = out[torch.from_numpy(rows).to(dev)].float().cpu().numpy()
+    err = oracle.rel_err(got, ref)
+    tol = oracle.TOL[si.PREC_BF16] if work.precision == si.PREC_BF16 else oracle.TOL[si.PREC_FP32]
+    if not err <= tol:
+        raise SystemExit(f"correctness gate failed for {work.name}: rel_err {err} > {tol}")
+
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 3)):
+            step(i)
+    stream.synchronize()
+    G = n_copies * max(1, 64 // n_copies)
+
+    def capture(nsteps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(nsteps):
+                step(i)
+        return g
+
+    graph = capture(G)
+    rem = steps % G
+    graph_rem = capture(rem) if rem else None
+    stream.synchronize()
+    sampler = ClockSampler(local_rank)
+    soak_until = time.perf_counter() + 1.0
+    with torch.cuda.stream(stream):
+        while time.perf_counter() < soak_until:
+            graph.replay()
+    stream.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps // G):
+            graph.replay()
+        if graph_rem is not None:
+            graph_rem.replay()
+        e1.record(stream)
+    stream.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    local_s = e0.elapsed_time(e1) / 1e3
+    ctx.check(stream)
+    got = out[torch.from_numpy(rows).to(dev)].float().cpu().numpy()
+    err_after = oracle.rel_err(got, ref)
+    if not err_after <= tol:
+        raise SystemExit(f"output after the timed steps is wrong for {work.name}: rel_err {err_after} > {tol}")
+    max_s, _ = aggregate(local_s, float(steps) * work.algorithmic_bytes(), world, dev)
+    peaks, src = load_peaks()
+    roof = roofline_for(work, local_s / steps, peaks, src, None)
+    line = {
+        "metric": METRIC, "value": round(world * steps * work.flops / max_s / 1e12, 3), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": steps, "warmup": warmup, "ms_per_step": round(max_s / steps * 1e3, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": prec, "data": "synthetic",
+        "config": {"workload": work.name, "M": M, "N": N, "K": K,
+                   "computes": "dX = dZ W" if work.which == 1 else "dW = dZ^T X",
+                   "kernel": "tc (MN-major operands)" if work.precision == si.PREC_BF16 else "bwd_ffma",
+                   "l2": f"cold dZ: {n_copies} rotating copies ({n_copies * dz_bytes >> 20} MiB > L2 {l2 >> 20} MiB), "
+                         f"steps replayed from a CUDA graph of {G}",
+                   "parity_gate": {"rel_err": err, "rel_err_after_timed_steps": err_after, "tol": tol,
+                                   "compared": f"{len(rows)} sampled output rows"}},
+        "roofline": roof, "clocks": clocks, "gpu_launches": steps,
+    }
+    ctx.close()
+    return line
+
+
 def cpu_baseline(layer: si.Layer, X, W, b, unit, budget_s=10.0):
     """The oracle as it stands on the host cores: whole layers when one takes
     under a second, else a seeded sample of rows, repeated for ~budget_s."""
@@ -476,13 +624,16 @@ def bench_reference(layer: si.Layer, steps: int, warmup: int):
 
 # ------------------------------------------------------------------- main
 
+BWD_BY_NAME = {w.name: w for w in BWD_WORKLOADS}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS) + sorted(BWD_BY_NAME))
     ap.add_argument("--all", action="store_true", help="one line per workload (stdout), default line last")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
@@ -492,6 +643,9 @@ def main(argv=None):
 
     if args.impl == "reference":
         if rank != 0:
+            return 0
+        if args.workload in BWD_BY_NAME:
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times forward workloads only"}))
             return 0
         ref_steps = min(steps, 200)
         line = bench_reference(WORKLOADS[args.workload], ref_steps, warmup)
@@ -505,9 +659,20 @@ def main(argv=None):
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
 
+    if args.workload in BWD_BY_NAME:
+        work = BWD_BY_NAME[args.workload]
+        line = bench_backward(work, steps, warmup, world, rank, local_rank)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return 0
     names = [args.workload]
     if args.all:
         names = [n for n in WORKLOADS if n != args.workload] + [args.workload]
+        for work in BWD_WORKLOADS:
+            st = max(300, min(steps, int(2e13 / work.flops)))
+            line = bench_backward(work, st, warmup, world, rank, local_rank)
+            if rank == 0:
+                print(json.dumps(line), flush=True)
     for name in names:
         layer = WORKLOADS[name]
         # Other workloads: at least 300 steps and ~20 TFLOP, so that the timed

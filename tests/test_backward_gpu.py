@@ -198,3 +198,28 @@ def test_backward_gpt2_fc1_m8192_bf16_sampled():
     assert oracle.rel_err(_host(dx)[ms], ref_dx) <= oracle.TOL[BF16]
     assert oracle.rel_err(_host(dw)[ns], ref_dw) <= oracle.TOL[BF16]
     assert oracle.rel_err(db.double().cpu().numpy()[ns], ref_db) <= oracle.TOL[FP32]
+
+
+@pytest.mark.parametrize("precision", [FP32, BF16])
+def test_backward_back_to_back(precision):
+    """Backward calls launched back to back (early start; fp32 split-K shares
+    the workspace): independent calls into separate outputs equal the same
+    calls made one at a time."""
+    M, N, K = 128, 3072, 768
+    dZ, W, X = _inputs(M, N, K, precision, seed=77)
+    dzs = [_dev(dZ * (1 + i), precision) for i in range(3)]
+    w, x = _dev(W, precision), _dev(X, precision)
+    prec = PREC_NAME[precision]
+    outs = []
+    for i in range(6):
+        outs.append(tll.backward_data(dzs[i % 3], w, precision=prec))
+        outs.append(tll.backward_weight(dzs[i % 3], x, db=True, precision=prec))
+    torch.cuda.synchronize()
+    for i in range(6):
+        ref_dx = tll.backward_data(dzs[i % 3], w, precision=prec)
+        torch.cuda.synchronize()
+        ref_dw, ref_db = tll.backward_weight(dzs[i % 3], x, db=True, precision=prec)
+        torch.cuda.synchronize()
+        assert torch.equal(outs[2 * i], ref_dx), i
+        assert torch.equal(outs[2 * i + 1][0], ref_dw) and torch.equal(outs[2 * i + 1][1], ref_db), i
+    tll.default_context(0).check()

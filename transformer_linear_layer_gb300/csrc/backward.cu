@@ -92,6 +92,9 @@ struct BwdArgs {
     int lda;         // row length of dZ (N)
     int ldb;         // row length of B (K; a multiple of 4)
     int a_vec;       // dZ rows are 16-byte aligned (N a multiple of 4): float4 loads
+    int splits;      // split-K: CTA z sums reduction stages [z * nst / S, (z + 1) * nst / S)
+    float* ws;       // split-K partial sums [S][I][J]
+    unsigned* counters;
 };
 
 constexpr int kBT = 64;   // output tile (I and J)
@@ -105,7 +108,10 @@ __global__ void __launch_bounds__(kBTh) bwd_ffma_kernel(const BwdArgs a) {
     const int tid = threadIdx.x;
     const int tx = tid % 16, ty = tid / 16;
     const int i0 = blockIdx.y * kBT, j0 = blockIdx.x * kBT;
-    const int nst = (a.R + kBR - 1) / kBR;
+    const int nst_all = (a.R + kBR - 1) / kBR;
+    const int st_begin = (int)((long long)blockIdx.z * nst_all / a.splits);
+    const int st_end = (int)((long long)(blockIdx.z + 1) * nst_all / a.splits);
+    const int nst = st_end - st_begin;
     pdl_wait();
 
     // Each thread stages one float4 of A and one of B per stage.
@@ -174,13 +180,13 @@ __global__ void __launch_bounds__(kBTh) bwd_ffma_kernel(const BwdArgs a) {
         for (int q = 0; q < 4; ++q) acc[p][q] = 0.f;
 
     if (nst > 0) {
-        fetch(0);
+        fetch(st_begin);
         store(0);
     }
     __syncthreads();
     for (int st = 0; st < nst; ++st) {
         const int buf = st & 1;
-        if (st + 1 < nst) fetch(st + 1);  // the next stage's loads overlap this stage's FMAs
+        if (st + 1 < nst) fetch(st_begin + st + 1);  // the next stage's loads overlap this stage's FMAs
 #pragma unroll
         for (int r = 0; r < kBR; ++r) {
             const float4 av = *reinterpret_cast<const float4*>(&As[buf][r][4 * ty]);
@@ -195,6 +201,23 @@ __global__ void __launch_bounds__(kBTh) bwd_ffma_kernel(const BwdArgs a) {
         if (st + 1 < nst) store(buf ^ 1);
         __syncthreads();
     }
+    if (a.splits == 1) {
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int i = i0 + 4 * ty + p;
+            if (i >= a.I) continue;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = j0 + 4 * tx + q;
+                if (j < a.J) a.C[(size_t)i * a.J + j] = acc[p][q];
+            }
+        }
+        return;
+    }
+    // Split-K: this CTA's partial tile to the workspace; the last CTA of the
+    // tile adds the partials in split order (fixed, so bitwise repeatable).
+    __shared__ unsigned s_last;
+    float* part = a.ws + (size_t)blockIdx.z * a.I * a.J;
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
         const int i = i0 + 4 * ty + p;
@@ -202,7 +225,41 @@ __global__ void __launch_bounds__(kBTh) bwd_ffma_kernel(const BwdArgs a) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int j = j0 + 4 * tx + q;
-            if (j < a.J) a.C[(size_t)i * a.J + j] = acc[p][q];
+            if (j < a.J) __stcg(part + (size_t)i * a.J + j, acc[p][q]);
+        }
+    }
+    __syncthreads();
+    const int tile_id = blockIdx.y * gridDim.x + blockIdx.x;
+    if (tid == 0) {
+        __threadfence();
+        const unsigned prev = atomicAdd(&a.counters[tile_id], 1u);
+        const unsigned last = prev == (unsigned)(a.splits - 1);
+        if (last) {
+            a.counters[tile_id] = 0u;  // re-armed for the next launch
+            __threadfence();
+        }
+        s_last = last;
+    }
+    __syncthreads();
+    if (!s_last) return;
+#pragma unroll 1
+    for (int p = 0; p < 4; ++p) {
+        const int i = i0 + 4 * ty + p;
+        if (i >= a.I) continue;
+        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int sp = 0; sp < a.splits; ++sp) {
+            const float* src = a.ws + (size_t)sp * a.I * a.J + (size_t)i * a.J;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = j0 + 4 * tx + q;
+                if (j < a.J) sum[q] += __ldcg(src + j);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int j = j0 + 4 * tx + q;
+            if (j < a.J) a.C[(size_t)i * a.J + j] = sum[q];
         }
     }
 }
@@ -255,9 +312,28 @@ int launch_colsum(int M, int N, const void* dZ, float* db, bool bf16, void* work
     return cudaGetLastError() == cudaSuccess ? LIN_OK : LIN_ERR_CUDA;
 }
 
-int launch_bwd_ffma(int which, int M, int N, int K, const float* dZ, const float* B, float* out, cudaStream_t st,
-                    bool early) {
+int bwd_ffma_splits(int which, int M, int N, int K, int sm_count, size_t ws_bytes) {
+    const int I = which == 1 ? M : N, J = K, R = which == 1 ? N : M;
+    const long long tiles = (long long)((I + kBT - 1) / kBT) * ((J + kBT - 1) / kBT);
+    const int nst = (R + kBR - 1) / kBR;
+    // Fill four resident 256-thread CTAs per SM without a second wave, >= 4
+    // reduction stages per split ("split-K when the output is small and K is long").
+    const long long slots = 4LL * sm_count;
+    int S = tiles >= slots ? 1 : (int)(slots / tiles);
+    const int max_s = nst / 4 > 1 ? nst / 4 : 1;
+    if (S > max_s) S = max_s;
+    if (S < 1) S = 1;
+    if (tiles > kMaxSplitTiles) S = 1;
+    while (S > 1 && splitk_workspace_bytes(S, I, J) > ws_bytes) --S;
+    return S;
+}
+
+int launch_bwd_ffma(int which, int M, int N, int K, const float* dZ, const float* B, float* out, int splits,
+                    void* workspace, cudaStream_t st, bool early) {
     BwdArgs a;
+    a.splits = splits < 1 ? 1 : splits;
+    a.ws = a.splits > 1 ? splitk_partials(workspace) : nullptr;
+    a.counters = a.splits > 1 ? splitk_counters(workspace) : nullptr;
     a.A = dZ;
     a.B = B;
     a.C = out;
@@ -276,7 +352,7 @@ int launch_bwd_ffma(int which, int M, int N, int K, const float* dZ, const float
     if (a.I <= 0 || a.J <= 0) return LIN_OK;
     if (a.R <= 0)
         return cudaMemsetAsync(out, 0, (size_t)a.I * a.J * sizeof(float), st) == cudaSuccess ? LIN_OK : LIN_ERR_CUDA;
-    const dim3 grid((a.J + kBT - 1) / kBT, (a.I + kBT - 1) / kBT);
+    const dim3 grid((a.J + kBT - 1) / kBT, (a.I + kBT - 1) / kBT, a.splits);
     return which == 1 ? launch_ex(bwd_ffma_kernel<1>, grid, dim3(kBTh), 0, st, early, a)
                       : launch_ex(bwd_ffma_kernel<2>, grid, dim3(kBTh), 0, st, early, a);
 }

@@ -98,8 +98,9 @@ struct BwdProblem {
     bool early_x;      // and read dZ and B before it finishes
 };
 int launch_tc_backward(const BwdProblem& q);
-int launch_bwd_ffma(int which, int M, int N, int K, const float* dZ, const float* B, float* out, cudaStream_t st,
-                    bool early);
+int bwd_ffma_splits(int which, int M, int N, int K, int sm_count, size_t ws_bytes);
+int launch_bwd_ffma(int which, int M, int N, int K, const float* dZ, const float* B, float* out, int splits,
+                    void* workspace, cudaStream_t st, bool early);
 int launch_gelu_backward(long long count, const void* dY, const void* Z, void* dZ, bool bf16, int sm_count,
                          cudaStream_t st, bool early);
 size_t colsum_workspace_bytes(int M, int N);

@@ -624,7 +624,7 @@ int backward_setup(lin_ctx* ctx, int which, int M, int N, int K, const void* dZ,
     return LIN_OK;
 }
 
-int backward_run(const lin::BwdProblem& q, int precision) {
+int backward_run(const lin::BwdProblem& q, int precision, lin_ctx* ctx) {
     using namespace lin;
     const int R = q.which == 1 ? q.N : q.M;
     const int Mo = q.which == 1 ? q.M : q.N;
@@ -633,8 +633,9 @@ int backward_run(const lin::BwdProblem& q, int precision) {
                    ? LIN_OK
                    : LIN_ERR_CUDA;
     if (precision == LIN_PREC_BF16) return launch_tc_backward(q);
+    const int S = bwd_ffma_splits(q.which, q.M, q.N, q.K, ctx->sm_count, ctx->workspace_bytes);
     return launch_bwd_ffma(q.which, q.M, q.N, q.K, static_cast<const float*>(q.dZ), static_cast<const float*>(q.B),
-                           static_cast<float*>(q.out), q.stream, q.early_start);
+                           static_cast<float*>(q.out), S, ctx->workspace, q.stream, q.early_start);
 }
 
 }  // namespace
@@ -647,7 +648,7 @@ int lin_backward_data(lin_ctx* ctx, int M, int N, int K, const void* dZ, const v
     if (rc != LIN_OK || q.which == 0) return rc;
     lin::DeviceGuard guard(ctx->device);
     if (!guard.ok) return LIN_ERR_CUDA;
-    return backward_run(q, precision);
+    return backward_run(q, precision, ctx);
 }
 
 int lin_backward_weight(lin_ctx* ctx, int M, int N, int K, const void* dZ, const void* X, void* dW, float* db,
@@ -668,7 +669,7 @@ int lin_backward_weight(lin_ctx* ctx, int M, int N, int K, const void* dZ, const
     lin::DeviceGuard guard(ctx->device);
     if (!guard.ok) return LIN_ERR_CUDA;
     if (q.which != 0) {
-        rc = backward_run(q, precision);
+        rc = backward_run(q, precision, ctx);
         if (rc != LIN_OK) return rc;
     }
     if (db && N > 0) {
