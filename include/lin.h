@@ -96,7 +96,8 @@ typedef struct {
     int bm, bn, bk;
     int splits;   /* >= 1 */
     int stages;   /* shared-memory pipeline depth (TC), 0 otherwise */
-    int grid_x, grid_y, grid_z;
+    int grid_x, grid_y, grid_z; /* TC: grid_z = K splits (1 = none; the splits of a tile
+                                 * are added in order by the last one to finish) */
     int threads;
     long long workspace_bytes; /* bytes of context workspace the launch uses */
 } lin_plan;

@@ -223,3 +223,25 @@ def test_backward_back_to_back(precision):
         assert torch.equal(outs[2 * i], ref_dx), i
         assert torch.equal(outs[2 * i + 1][0], ref_dw) and torch.equal(outs[2 * i + 1][1], ref_db), i
     tll.default_context(0).check()
+
+
+def test_backward_weight_k_split():
+    """A weight gradient with few output tiles and a long reduction, called
+    on a fresh stream (nothing to overlap with): the tensor cores split the
+    reduction and add the splits in order. Against the oracle on sampled
+    rows, and bitwise repeatable."""
+    M, N, K = 8192, 768, 256
+    dZ, _, X = _inputs(M, N, K, BF16, seed=123)
+    dz, x = _dev(dZ, BF16), _dev(X, BF16)
+    outs = []
+    for _ in range(2):
+        st = torch.cuda.Stream()
+        with torch.cuda.stream(st):
+            outs.append(tll.backward_weight(dz, x, db=True, stream=st))
+        st.synchronize()
+    dw, db = outs[0]
+    assert torch.equal(dw, outs[1][0]) and torch.equal(db, outs[1][1])
+    rows = np.unique(np.concatenate([np.random.default_rng(3).integers(0, N, 40), [0, N - 1]]))
+    ref_dw, ref_db = oracle.backward_dw(dZ[:, rows], X)
+    assert oracle.rel_err(_host(dw)[rows], ref_dw) <= oracle.TOL[BF16]
+    assert oracle.rel_err(db.double().cpu().numpy()[rows], ref_db) <= oracle.TOL[FP32]

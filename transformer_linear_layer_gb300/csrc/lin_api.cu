@@ -175,11 +175,15 @@ int make_gemv(int sm, int width, int M, int N, int K, bool bf16, lin_plan* p) {
 //   than whole tiles both back to back (where the SMs that a ragged last round
 //   frees start the next call early) and with the early start off (the cut
 //   tiles' hand-over sits on the critical path). Explicit plans reach it.
-int make_tc(int sm, int variant, int width, bool stream_k, int M, int N, int K, int esz, lin_plan* p) {
+int make_tc(int sm, int variant, int width, bool stream_k, int M, int N, int K, int esz, lin_plan* p,
+            size_t ksplit_ws = 0) {
     if (M < 1 || N < 1 || K < 1 || width < 0) return LIN_ERR_UNSUPPORTED;
     const long long w0 = width > 0 ? width : sm;
     if (variant < 0) {
-        const bool want_pair = ceil_div(K, 128 / esz) >= 64;
+        // SM pairs for long K, unless the single-CTA tiles are so few that a K
+        // split (below) is what fills the SMs.
+        const long long tiles256 = (long long)ceil_div(M, 128) * ceil_div(N, 256);
+        const bool want_pair = ceil_div(K, 128 / esz) >= 64 && !(ksplit_ws > 0 && tiles256 * 2 <= sm);
         double best = 0.0;
         for (int v = 0; v < kTcVariants; ++v) {
             if (kTcCfg[v].pair != want_pair) continue;
@@ -222,6 +226,17 @@ int make_tc(int sm, int variant, int width, bool stream_k, int M, int N, int K, 
     p->grid_z = 1;
     p->threads = kTcThreads;
     p->workspace_bytes = stream_k ? (long long)tc_streamk_workspace_bytes((int)w, p->bn) : 0;
+    // Few tiles with a long K (and room in the workspace): split K so that
+    // the (tile, split) items fill the SMs; grid_z = splits.
+    if (!pair && !stream_k && ksplit_ws > 0) {
+        const int S = tc_ksplits(items, ceil_div(K, 128 / esz), sm, ksplit_ws, p->bn);
+        if (S > 1) {
+            const long long w2 = width > 0 ? width : sm;
+            p->grid_z = S;
+            p->grid_x = (int)(items * S < w2 ? items * S : w2);
+            p->workspace_bytes = (long long)tc_ksplit_workspace_bytes(items, S, p->bn);
+        }
+    }
     return LIN_OK;
 }
 
@@ -246,12 +261,12 @@ int plan_default(int sm, int M, int N, int K, int precision, size_t ws, lin_plan
         case LIN_PREC_BF16:
             if (gemv_fits(M, K, true)) return make_gemv(sm, 0, M, N, K, true, p);
             if (M <= 16) return make_skinny(sm, 0, 0, M, N, K, ws, p);
-            return make_tc(sm, -1, 0, false, M, N, K, 2, p);
+            return make_tc(sm, -1, 0, false, M, N, K, 2, p, ws);
         case LIN_PREC_TF32:
             // A few rows are a weight stream: the exact-fp32 GEMV is as fast as
             // any tensor-core tile there, and more accurate than TF32.
             if (gemv_fits(M, K, false)) return make_gemv(sm, 0, M, N, K, false, p);
-            return make_tc(sm, -1, 0, false, M, N, K, 4, p);
+            return make_tc(sm, -1, 0, false, M, N, K, 4, p, ws);
         default:
             if (gemv_fits(M, K, false)) return make_gemv(sm, 0, M, N, K, false, p);
             return make_ffma(sm, -1, 0, M, N, K, ws, p);
@@ -367,7 +382,7 @@ int check_plan_fits(const lin_plan& p, int M, int N, int K, int precision) {
             const bool pair = kTcCfg[p.variant].pair;
             const long long items = (long long)(pair ? ceil_div(ceil_div(M, 128), 2) : ceil_div(M, 128)) *
                                     ceil_div(N, kTcCfg[p.variant].bn);
-            const long long ctas = pair ? 2 * items : items;
+            const long long ctas = pair ? 2 * items : items * (p.grid_z > 1 ? p.grid_z : 1);
             if (p.bn != kTcCfg[p.variant].bn || p.grid_x < 1 || p.grid_x > ctas || p.grid_y != 1 ||
                 (pair && p.grid_x % 2 != 0))
                 return LIN_ERR_UNSUPPORTED;
@@ -375,6 +390,15 @@ int check_plan_fits(const lin_plan& p, int M, int N, int K, int precision) {
                 (pair || p.grid_x > kTcMaxStreamKCtas ||
                  p.workspace_bytes < (long long)tc_streamk_workspace_bytes(p.grid_x, p.bn)))
                 return LIN_ERR_UNSUPPORTED;
+            if (p.grid_z > 1) {  // K split
+                const long long tiles = (long long)ceil_div(M, 128) * ceil_div(N, p.bn);
+                if (pair || p.splits != 1 || p.grid_z > 16 || tiles > kTcMaxKSplitTiles ||
+                    ceil_div(K, precision == LIN_PREC_BF16 ? 64 : 32) < p.grid_z ||
+                    p.workspace_bytes < (long long)tc_ksplit_workspace_bytes(tiles, p.grid_z, p.bn))
+                    return LIN_ERR_UNSUPPORTED;
+            } else if (p.grid_z != 1) {
+                return LIN_ERR_UNSUPPORTED;
+            }
             return LIN_OK;
         }
         case LIN_KERNEL_GEMV: {
@@ -433,6 +457,13 @@ int run(lin_ctx* ctx, const lin_plan& plan_in, int M, int N, int K, const void* 
         lin_plan narrow;
         if (make_skinny(ctx->sm_count, plan.variant, 1, M, N, K, ctx->workspace_bytes, &narrow) == LIN_OK)
             plan = narrow;
+    }
+    // Likewise a tensor-core K split (measured: it helps an isolated call and
+    // costs a back-to-back one).
+    if (adaptive && known && p.early_x && plan.kernel == LIN_KERNEL_TC && plan.grid_z > 1) {
+        lin_plan whole;
+        if (make_tc(ctx->sm_count, -1, 0, false, M, N, K, precision == LIN_PREC_BF16 ? 2 : 4, &whole) == LIN_OK)
+            plan = whole;
     }
     ctx->last_plan = plan;
     switch (plan.kernel) {
@@ -621,6 +652,11 @@ int backward_setup(lin_ctx* ctx, int which, int M, int N, int K, const void* dZ,
                    &x_ok, &known);
     q->early_start = ctx->early_start && w_ok;
     q->early_x = q->early_start && x_ok;
+    q->workspace = ctx->workspace;
+    q->workspace_bytes = ctx->workspace_bytes;
+    // Right after an independent call the two overlap (early start) and fill
+    // the SMs together: a K split would only add its round trip.
+    q->ksplit_ok = !(known && q->early_x);
     return LIN_OK;
 }
 

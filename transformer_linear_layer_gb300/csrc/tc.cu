@@ -48,8 +48,10 @@ struct TcArgs {
     int bias_aligned16;  // bias is 16-byte aligned (vector loads allowed)
     int early_inputs;    // X and W may be read before the dependency wait (not the previous call's output)
     int y_tma;           // bf16 Y stored by TMA from 32 x 32 boxes (16-byte aligned rows)
-    float* partials;     // stream-K: one 128 x BN fp32 slot per CTA boundary
-    unsigned* flags;     // stream-K: 8 hand-over flags per CTA boundary (zero between launches)
+    float* partials;     // stream-K: one 128 x BN fp32 slot per CTA boundary; K split: one per (tile, split)
+    unsigned* flags;     // stream-K: 8 hand-over flags per CTA boundary; K split: 8 counters per tile
+                         // (zero between launches)
+    int ksplits;         // K split (whole tiles, single CTA): each tile's K stages cut in ksplits ranges
 };
 
 // Epilogue staging: each epilogue warp owns a 32 x 32 output tile in shared
@@ -166,6 +168,11 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     const long long units = (long long)ntiles * nkb;
     const long long u0 = SK ? (long long)blockIdx.x * units / gridDim.x : 0;
     const long long u1 = SK ? (long long)(blockIdx.x + 1) * units / gridDim.x : 0;
+    // K split (ksplits > 1, whole single-CTA tiles): the work items are
+    // (tile, split) pairs, split-major; each covers K stages
+    // [split * nkb / S, (split + 1) * nkb / S) of its tile.
+    const int ksplits = (SK || PAIR) ? 1 : a.ksplits;
+    int cur_split = 0;  // split of the last segment returned (epilogue)
     auto seg = [&](int j, int& tile, int& lo, int& hi) -> bool {
         if constexpr (SK) {
             const long long t = u0 / nkb + j;
@@ -177,10 +184,13 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             hi = (int)(en - t * nkb);
             return true;
         } else {
-            tile = first_item + j * item_step;
-            lo = 0;
-            hi = nkb;
-            return tile < ntiles;
+            const int item = first_item + j * item_step;
+            if (item >= ntiles * ksplits) return false;
+            tile = item % ntiles;
+            cur_split = item / ntiles;
+            lo = (int)((long long)cur_split * nkb / ksplits);
+            hi = (int)((long long)(cur_split + 1) * nkb / ksplits);
+            return true;
         }
     };
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
@@ -464,6 +474,10 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) r[jj] = __float_as_uint(__uint_as_float(r[jj]) + __ldcg(src + jj * 32));
         };
+        // K split: this warp's region of the (tile, split) slot, same layout.
+        auto ks_ptr = [&](int tile_, int split_) {
+            return a.partials + (((size_t)tile_ * ksplits + split_) * EPI_WARPS + ew) * (CH * 1024);
+        };
 
         int j = 0, tile, lo, hi;
         for (; seg(j, tile, lo, hi); ++j) {
@@ -471,6 +485,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             const int m0 = tile_m0(tile), n0 = tile_n0(tile);
             const bool part_out = SK && lo > 0;            // later K stages of a cut tile: hand over
             const bool part_in = SK && lo == 0 && hi < nkb;  // earlier K stages: add the partner's, finish
+            const bool kpart = ksplits > 1;                // one K range of a split tile
+            const int split = cur_split;
             // This warp's bias columns of the tile, fetched while the MMAs run.
 #pragma unroll
             for (int t = lane; t < HALF; t += 32) {
@@ -512,6 +528,17 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     if (lane == 0) release_acc(buf);
                     released = true;
                 }
+                if (kpart) {
+                    float* dst = ks_ptr(tile, split) + lane;
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) __stcg(dst + c * 1024 + jj * 32, __uint_as_float(r0[jj]));
+                    if (two) {
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj)
+                            __stcg(dst + (c + 1) * 1024 + jj * 32, __uint_as_float(r1[jj]));
+                    }
+                    continue;
+                }
                 if constexpr (SK) {
                     if (part_out) {
                         store_part(r0, c);
@@ -525,6 +552,38 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 }
                 emit(r0, c, m0, n0);
                 if (two) emit(r1, c + 1, m0, n0);
+            }
+            if (kpart && ok) {
+                // Count this region in; the last of the tile's splits adds all of
+                // them in split order and finishes the region.
+                __threadfence();
+                __syncwarp();
+                unsigned* cnt = a.flags + (size_t)tile * EPI_WARPS + ew;
+                unsigned last = 0;
+                if (lane == 0) {
+                    last = atomicAdd(cnt, 1u) == (unsigned)(ksplits - 1);
+                    if (last) *cnt = 0u;  // re-armed for the next launch
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence();
+#pragma unroll 1
+                    for (int c = 0; c < CH; ++c) {
+                        float sum[32];
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) sum[jj] = 0.f;
+#pragma unroll 1
+                        for (int sp = 0; sp < ksplits; ++sp) {
+                            const float* src = ks_ptr(tile, sp) + c * 1024 + lane;
+#pragma unroll
+                            for (int jj = 0; jj < 32; ++jj) sum[jj] += __ldcg(src + jj * 32);
+                        }
+                        uint32_t r[32];
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) r[jj] = __float_as_uint(sum[jj]);
+                        emit(r, c, m0, n0);
+                    }
+                }
             }
             if constexpr (SK) {
                 if (part_out && ok) {
@@ -691,7 +750,9 @@ bool make_mnmajor_map(CUtensorMap* map, const void* base, int rows, int cols) {
     return r == CUDA_SUCCESS;
 }
 
-// bf16 backward GEMMs on the tensor cores, 128 x 256 single-CTA tiles:
+// bf16 backward GEMMs on the tensor cores, 128 x 256 single-CTA tiles (K
+// split when the tiles are few, the reduction long and no independent
+// predecessor on the stream fills the idle SMs instead):
 //   which 1: dX (M x K) = dZ (M x N) . W (N x K): A = dZ K-major, B = W MN-major.
 //   which 2: dW (N x K) = dZ^T . X (M x K):       A = dZ MN-major, B = X MN-major.
 // Rows of dZ, W and X must be 16-byte aligned (N and K multiples of 8).
@@ -719,14 +780,21 @@ int launch_tc_backward(const BwdProblem& q) {
     a.early_inputs = q.early_x ? 1 : 0;
     a.partials = nullptr;
     a.flags = nullptr;
+    // Small outputs with a long reduction (the weight gradients): split K.
+    const long long ntile = (long long)((Mo + 127) / 128) * ((No + 255) / 256);
+    a.ksplits = q.ksplit_ok ? tc_ksplits(ntile, (R + 63) / 64, q.sm_count, q.workspace_bytes, kTcCfg[0].bn) : 1;
+    if (a.ksplits > 1) {
+        a.partials = splitk_partials(q.workspace);
+        a.flags = splitk_counters(q.workspace);
+    }
     ty = ta;
     a.y_tma = 0;
     if (a.y_aligned16 && No % 8 == 0) {
         if (!make_out_map_bf16(&ty, q.out, Mo, No)) return LIN_ERR_CUDA;
         a.y_tma = 1;
     }
-    const long long tiles = (long long)((Mo + 127) / 128) * ((No + 255) / 256);
-    const int grid = (int)(tiles < q.sm_count ? tiles : q.sm_count);
+    const long long items = ntile * a.ksplits;
+    const int grid = (int)(items < q.sm_count ? items : q.sm_count);
     if (q.which == 1)
         return launch_cfg<true, kTcCfg[0].bn, false, false, false, 1>(ta, tb, ty, a, grid, q.early_start, q.stream);
     return launch_cfg<true, kTcCfg[0].bn, false, false, false, 2>(ta, tb, ty, a, grid, q.early_start, q.stream);
@@ -757,6 +825,15 @@ int launch_tc(const Problem& p, const lin_plan& plan) {
         return LIN_ERR_UNSUPPORTED;
     a.partials = sk ? splitk_partials(p.workspace) : nullptr;
     a.flags = sk ? splitk_counters(p.workspace) + kTcFlagBase : nullptr;
+    a.ksplits = plan.grid_z > 1 ? plan.grid_z : 1;
+    if (a.ksplits > 1) {
+        const long long ntile = (long long)((p.M + 127) / 128) * ((p.N + plan.bn - 1) / plan.bn);
+        if (sk || pair || ntile > kTcMaxKSplitTiles ||
+            p.workspace_bytes < tc_ksplit_workspace_bytes(ntile, a.ksplits, plan.bn))
+            return LIN_ERR_UNSUPPORTED;
+        a.partials = splitk_partials(p.workspace);
+        a.flags = splitk_counters(p.workspace);
+    }
     // bf16 rows 16-byte aligned: Y leaves by TMA store; otherwise (odd N, as in
     // the LM head) through the staged row-segment stores. The fallback map is a
     // placeholder the kernel never uses.
