@@ -199,6 +199,24 @@ LIN_API int lin_backward_weight(lin_ctx* ctx, int M, int N, int K, const void* d
 LIN_API int lin_gelu_backward(lin_ctx* ctx, long long count, const void* dY, const void* Z, void* dZ,
                               int precision, void* stream);
 
+/* Measured dispatch ("Optimizing a GPT-2-class transformer on a GPU", Act II:
+ * route each shape to its measured winner). Install `plan` as the context's
+ * choice for lin_forward calls with exactly these sizes, precision and
+ * epilogue (checked like lin_forward_plan; LIN_ERR_UNSUPPORTED or
+ * LIN_ERR_WORKSPACE when it cannot run the shape in this context; a refused
+ * plan leaves any earlier entry in place). A NULL plan removes the entry
+ * (LIN_OK whether or not there was one). The plan is copied; entries are
+ * guarded by a lock, so installing while another thread calls lin_forward is
+ * safe. lin_forward consults these entries before the
+ * built-in table and runs an installed plan as given (no adaptive change for
+ * back-to-back calls). The Python package's autotuner measures candidates and
+ * installs winners through this call. */
+LIN_API int lin_set_plan_override(lin_ctx* ctx, int M, int N, int K, int precision, int epilogue,
+                                  const lin_plan* plan);
+
+/* Remove every installed plan of the context. */
+LIN_API int lin_clear_plan_overrides(lin_ctx* ctx);
+
 /* Synchronise `stream`, read and clear the context's device status word.
  * Returns LIN_ERR_DEVICE_TIMEOUT if any kernel since the last check gave up
  * a bounded wait (its output is then incomplete), LIN_ERR_CUDA on a CUDA

@@ -180,3 +180,78 @@ def test_dispatch_gemv_for_few_fp32_rows():
         tll.plan_make(SM, tll.KERNEL_GEMV, 0, 0, 5, 1000, 520, "bf16")
     with pytest.raises(tll.LinError):
         tll.plan_make(SM, tll.KERNEL_GEMV, 0, 0, 9, 1000, 520, "fp32")
+
+
+def test_autotune_menu():
+    """The tuner's menu: valid plans only, no duplicates, each family that can
+    run the shape, and the built-in choice among them for the common shapes."""
+    from transformer_linear_layer_gb300 import autotune
+
+    for (M, N, K, prec, fams) in [(8192, 2304, 768, "bf16", {tll.KERNEL_TC}),
+                                  (8, 768, 768, "bf16", {tll.KERNEL_SKINNY, tll.KERNEL_TC}),
+                                  (4, 768, 768, "bf16", {tll.KERNEL_SKINNY, tll.KERNEL_TC, tll.KERNEL_GEMV}),
+                                  (128, 3072, 768, "fp32", {tll.KERNEL_FFMA}),
+                                  (1, 50257, 768, "fp32", {tll.KERNEL_FFMA, tll.KERNEL_GEMV}),
+                                  (4096, 4096, 4096, "tf32", {tll.KERNEL_TC})]:
+        menu = autotune.candidates(152, M, N, K, prec, 64 << 20)
+        keys = [autotune._plan_key(p) for p in menu]
+        assert len(keys) == len(set(keys))
+        assert {p.kernel for p in menu} == fams
+        assert all(p.workspace_bytes <= 64 << 20 for p in menu)
+        assert autotune._plan_key(tll.plan_query(152, M, N, K, prec, "none")) in keys
+    # no workspace: no split plans
+    assert all(p.workspace_bytes == 0 for p in autotune.candidates(152, 128, 3072, 768, "fp32", 0))
+
+
+def test_roofline_floor():
+    from transformer_linear_layer_gb300 import autotune
+
+    # bf16 M=16: HBM-bound, the weight dominates
+    t = autotune.roofline_floor_s(16, 4096, 4096, "bf16")
+    assert abs(t - 2 * (16 * 4096 * 2 + 4096 * 4096) / 6783.1e9) < 1e-12
+    # bf16 8192^3: compute-bound
+    t = autotune.roofline_floor_s(8192, 8192, 8192, "bf16")
+    assert abs(t - 2 * 8192 ** 3 / 1891.6e12) < 1e-12
+
+
+def test_autotune_features_and_residual_fit():
+    """The cost model's inputs on known plans, and the residual regression
+    recovering coefficients planted in synthetic timings."""
+    import math
+    import random
+
+    from transformer_linear_layer_gb300 import autotune
+
+    # 8192 x 2304 bf16 on 128 x 256 tiles: 64 x 9 = 576 tiles on 152 SMs -> 4 waves, 576 / 608 busy
+    p = tll.plan_make(152, tll.KERNEL_TC, 0, 0, 8192, 2304, 768, "bf16")
+    f = autotune.features(152, 8192, 2304, 768, "bf16", p)
+    assert f["family"] == "tc" and abs(f["fill"] - 576 / 608) < 1e-12 and f["tile_fill"] == 1.0
+    # 128 x 768 fp32 on 64 x 64 tiles split 3: 72 units in 304 slots; 100 rows pad to 128
+    p = tll.plan_make(152, tll.KERNEL_FFMA, 1, 3, 100, 768, 768, "fp32")
+    f = autotune.features(152, 100, 768, 768, "fp32", p)
+    assert f["split"] == 3 and abs(f["fill"] - 72 / 304) < 1e-12 and abs(f["tile_fill"] - 100 / 128) < 1e-12
+    # the prior: an HBM-bound skinny layer costs its bytes at the copy peak, split or not (on-chip reduce)
+    p1 = tll.plan_make(152, tll.KERNEL_SKINNY, 0, 4, 16, 4096, 4096, "bf16")
+    t = autotune.predict_prior_s(16, 4096, 4096, "bf16", autotune.features(152, 16, 4096, 4096, "bf16", p1))
+    assert abs(t - autotune.roofline_floor_s(16, 4096, 4096, "bf16")) < 1e-12
+
+    m = autotune.ResidualModel(ridge=1e-9)
+    rng = random.Random(3)
+    for _ in range(80):
+        f = {"fill": rng.uniform(0.05, 1), "tile_fill": rng.uniform(0.3, 1), "split": rng.choice([1, 2, 4, 8]),
+             "family": rng.choice(["tc", "tc_pair", "skinny", "ffma", "gemv"]), "stream_k": rng.random() < 0.2}
+        true = 0.2 - 0.7 * math.log(1 / f["fill"]) + 0.1 * math.log2(f["split"]) + (0.3 if f["stream_k"] else 0)
+        m.add(f, 1e-5 * math.exp(true), 1e-5)
+    assert not autotune.ResidualModel().trusted and m.trusted
+    m.fit()
+    coef = {r["feature"]: r for r in m.report()}
+    assert abs(coef["bias"]["coef"] - 0.2) < 1e-3 and abs(coef["log_idle_waves"]["coef"] + 0.7) < 1e-3
+    assert abs(coef["log2_split"]["coef"] - 0.1) < 1e-3 and abs(coef["stream_k"]["coef"] - 0.3) < 1e-3
+    assert coef["log_idle_waves"]["prior"] == "OVERprices" and coef["ffma"]["prior"] == "as priced"
+
+
+def test_skinny_ring_for_many_row_tiles():
+    """More 128-row tiles of W than SMs: the 96 KB ring (two CTAs per SM)."""
+    p = tll.plan_query(SM, 8, 50257, 768, "bf16")
+    assert kname(p) == "skinny" and p.variant == 1 and p.splits == 1
+    assert tll.plan_query(SM, 16, 4096, 4096, "bf16").variant == 0

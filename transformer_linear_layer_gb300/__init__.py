@@ -93,6 +93,8 @@ def library() -> ctypes.CDLL:
                 "lin_backward_data": ([P, I, I, I, P, P, P, I, P], I),
                 "lin_backward_weight": ([P, I, I, I, P, P, P, P, I, P], I),
                 "lin_gelu_backward": ([P, ctypes.c_longlong, P, P, P, I, P], I),
+                "lin_set_plan_override": ([P, I, I, I, I, I, PP], I),
+                "lin_clear_plan_overrides": ([P], I),
                 "lin_strerror": ([I], ctypes.c_char_p),
                 "lin_abi_version": ([], I),
             }
@@ -180,7 +182,20 @@ class Context:
         return p
 
     def plan(self, M, N, K, precision="bf16", epilogue="none") -> Plan:
+        """The built-in table's plan (installed overrides are not consulted)."""
         return plan_query(self.sm_count, M, N, K, precision, epilogue, self.workspace_bytes)
+
+    def set_override(self, M, N, K, precision, epilogue, plan: Plan | None):
+        """Install (or, with None, remove) the plan lin_forward uses for this call signature."""
+        rc = library().lin_set_plan_override(self._h, M, N, K, _prec(precision), _epi(epilogue),
+                                             None if plan is None else ctypes.byref(plan))
+        if rc != OK:
+            raise LinError(rc, "lin_set_plan_override")
+
+    def clear_overrides(self):
+        rc = library().lin_clear_plan_overrides(self._h)
+        if rc != OK:
+            raise LinError(rc, "lin_clear_plan_overrides")
 
     # raw-pointer calls (the C ABI, one to one) ---------------------------------
     def forward_ptr(self, M, N, K, X, W, bias, Y, epilogue, precision, stream) -> int:

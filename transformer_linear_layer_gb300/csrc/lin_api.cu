@@ -15,10 +15,17 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 #include <new>
 
 #include "internal.h"
 #include "device_common.cuh"
+
+// A measured winner installed for one exact call signature.
+struct lin_override {
+    int M, N, K, precision, epilogue;
+    lin_plan plan;
+};
 
 struct lin_ctx {
     int device;
@@ -28,6 +35,8 @@ struct lin_ctx {
     int* dev_status;
     bool early_start;  // LIN_OPT_EARLY_START
     lin_plan last_plan;
+    std::mutex override_mu;
+    std::vector<lin_override> overrides;  // consulted by lin_forward before the table
 };
 
 namespace lin {
@@ -82,7 +91,9 @@ int make_skinny(int sm, int variant, int splits, int M, int N, int K, size_t /*w
     return LIN_OK;
 }
 
-int make_ffma(int sm, int variant, int splits, int M, int N, int K, size_t ws, lin_plan* p) {
+// `min_steps`: the fewest K steps of 32 a split keeps (4 for a call that runs
+// alone; a call that overlaps an independent predecessor passes more, see run()).
+int make_ffma(int sm, int variant, int splits, int M, int N, int K, size_t ws, lin_plan* p, int min_steps = 4) {
     if (M < 1 || N < 1 || K < 1) return LIN_ERR_UNSUPPORTED;
     if (variant < 0) {
         // 128x128 tiles when they give at least one full wave, else 64x64 + split-K.
@@ -102,7 +113,7 @@ int make_ffma(int sm, int variant, int splits, int M, int N, int K, size_t ws, l
         // against rounding the split up to one CTA per SM).
         const int slots = variant == 0 ? sm : 2 * sm;
         S = tiles >= slots ? 1 : slots / tiles;
-        const int max_s = nkb / 4 > 1 ? nkb / 4 : 1;
+        const int max_s = nkb / min_steps > 1 ? nkb / min_steps : 1;
         if (S > max_s) S = max_s;
         if (S < 1) S = 1;
         while (S > 1 && splitk_workspace_bytes(S, M, N) > ws) --S;
@@ -260,7 +271,10 @@ int plan_default(int sm, int M, int N, int K, int precision, size_t ws, lin_plan
     switch (precision) {
         case LIN_PREC_BF16:
             if (gemv_fits(M, K, true)) return make_gemv(sm, 0, M, N, K, true, p);
-            if (M <= 16) return make_skinny(sm, 0, 0, M, N, K, ws, p);
+            // More row tiles than SMs: the 96 KB ring (two CTAs per SM) instead
+            // of the 192 KB one, so the tiles run in fewer waves (measured on
+            // the last token's logits, 50257 rows: 15.7 -> 12.1 us).
+            if (M <= 16) return make_skinny(sm, ceil_div(N, 128) > sm ? 1 : 0, 0, M, N, K, ws, p);
             return make_tc(sm, -1, 0, false, M, N, K, 2, p, ws);
         case LIN_PREC_TF32:
             // A few rows are a weight stream: the exact-fp32 GEMV is as fast as
@@ -465,6 +479,14 @@ int run(lin_ctx* ctx, const lin_plan& plan_in, int M, int N, int K, const void* 
         if (make_tc(ctx->sm_count, -1, 0, false, M, N, K, precision == LIN_PREC_BF16 ? 2 : 4, &whole) == LIN_OK)
             plan = whole;
     }
+    // And the FFMA split: back to back, the next call's CTAs fill the SMs that
+    // a split would, so a split must now pay for its reduction with a long K
+    // (>= 24 steps of 32 each; measured on the GPT-2 M = 128 layers: proj
+    // 8.6 -> 4.1 us, qkv 14.7 -> 11.9 us, fc2 keeps a split of 4).
+    if (adaptive && known && p.early_x && plan.kernel == LIN_KERNEL_FFMA && plan.splits > 1) {
+        lin_plan fewer;
+        if (make_ffma(ctx->sm_count, -1, 0, M, N, K, ctx->workspace_bytes, &fewer, 24) == LIN_OK) plan = fewer;
+    }
     ctx->last_plan = plan;
     switch (plan.kernel) {
         case LIN_KERNEL_FILL: return launch_fill(p);
@@ -614,10 +636,41 @@ int lin_plan_make(int sm_count, int kernel, int variant, int splits, int M, int 
 int lin_forward(lin_ctx* ctx, int M, int N, int K, const void* X, const void* W, const float* bias, void* Y,
                 int epilogue, int precision, void* stream) {
     if (!ctx || M < 0 || N < 0 || K < 0 || !lin::valid_enums(epilogue, precision)) return LIN_ERR_ARG;
+    {
+        std::lock_guard<std::mutex> lk(ctx->override_mu);
+        for (const lin_override& o : ctx->overrides)
+            if (o.M == M && o.N == N && o.K == K && o.precision == precision && o.epilogue == epilogue)
+                return lin::run(ctx, o.plan, M, N, K, X, W, bias, Y, epilogue, precision, stream, false);
+    }
     lin_plan plan;
     const int rc = lin::plan_default(ctx->sm_count, M, N, K, precision, ctx->workspace_bytes, &plan);
     if (rc != LIN_OK) return rc;
     return lin::run(ctx, plan, M, N, K, X, W, bias, Y, epilogue, precision, stream, true);
+}
+
+int lin_set_plan_override(lin_ctx* ctx, int M, int N, int K, int precision, int epilogue, const lin_plan* plan) {
+    if (!ctx || M < 0 || N < 0 || K < 0 || !lin::valid_enums(epilogue, precision)) return LIN_ERR_ARG;
+    if (plan) {  // a refused plan leaves the table as it was
+        const int fit = lin::check_plan_fits(*plan, M, N, K, precision);
+        if (fit != LIN_OK) return fit;
+        if ((size_t)plan->workspace_bytes > ctx->workspace_bytes) return LIN_ERR_WORKSPACE;
+    }
+    std::lock_guard<std::mutex> lk(ctx->override_mu);
+    auto& v = ctx->overrides;
+    for (size_t i = 0; i < v.size(); ++i)
+        if (v[i].M == M && v[i].N == N && v[i].K == K && v[i].precision == precision && v[i].epilogue == epilogue) {
+            v.erase(v.begin() + (long)i);
+            break;
+        }
+    if (plan) v.push_back(lin_override{M, N, K, precision, epilogue, *plan});
+    return LIN_OK;
+}
+
+int lin_clear_plan_overrides(lin_ctx* ctx) {
+    if (!ctx) return LIN_ERR_ARG;
+    std::lock_guard<std::mutex> lk(ctx->override_mu);
+    ctx->overrides.clear();
+    return LIN_OK;
 }
 
 namespace {
