@@ -1,4 +1,5 @@
-"""CPU oracle for Y = act(X . W^T + bias) and its backward. TEST INFRASTRUCTURE ONLY.
+"""CPU oracle for Y = act(X . W^T + bias), its backward, the fused residual,
+the LayerNorm fold and the dX carried through a GELU. TEST INFRASTRUCTURE ONLY.
 
 Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
 leg import this package. The library under ``transformer_linear_layer_gb300``
@@ -71,6 +72,14 @@ def _load():
             lib.oracle_backward_dw.restype = None
             lib.oracle_gelu_grad_array.argtypes = [i64, p, p]
             lib.oracle_gelu_grad_array.restype = None
+            lib.oracle_linear_residual.argtypes = [i64, i64, i64, p, p, p, p, ctypes.c_int, p, ctypes.c_int]
+            lib.oracle_linear_residual.restype = None
+            lib.oracle_layernorm.argtypes = [i64, i64, p, p, p, ctypes.c_double, p]
+            lib.oracle_layernorm.restype = None
+            lib.oracle_fold_layernorm.argtypes = [i64, i64, p, p, p, p, p, p]
+            lib.oracle_fold_layernorm.restype = None
+            lib.oracle_backward_dx_gelu.argtypes = [i64, i64, i64, p, p, p, p, ctypes.c_int]
+            lib.oracle_backward_dx_gelu.restype = None
             _lib = lib
     return _lib
 
@@ -174,6 +183,59 @@ def gelu_grad(x) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float64)
     out = np.empty_like(x)
     _load().oracle_gelu_grad_array(x.size, x.ctypes.data, out.ctypes.data)
+    return out
+
+
+def linear_residual(X, W, R, bias=None, gelu: bool = False, nthreads: int = 0) -> np.ndarray:
+    """Y (float64, M x N) = act(X . W^T + bias) + R; R: M x N (fp32 values)."""
+    X, W, R = _f32(X), _f32(W), _f32(R)
+    M, K = X.shape
+    N, K2 = W.shape
+    assert K == K2 and R.shape == (M, N)
+    b = None if bias is None else _f32(bias)
+    Y = np.empty((M, N), dtype=np.float64)
+    _load().oracle_linear_residual(M, N, K, X.ctypes.data, W.ctypes.data, None if b is None else b.ctypes.data,
+                                   R.ctypes.data, int(bool(gelu)), Y.ctypes.data, int(nthreads))
+    return Y
+
+
+def layernorm(X, gamma=None, beta=None, eps: float = 1e-5) -> np.ndarray:
+    """LayerNorm over the last axis in float64 (gamma / beta None: xhat alone)."""
+    X = _f32(X)
+    M, K = X.shape
+    g = None if gamma is None else _f32(gamma)
+    bt = None if beta is None else _f32(beta)
+    out = np.empty((M, K), dtype=np.float64)
+    _load().oracle_layernorm(M, K, X.ctypes.data, None if g is None else g.ctypes.data,
+                             None if bt is None else bt.ctypes.data, float(eps), out.ctypes.data)
+    return out
+
+
+def fold_layernorm(W, gamma, beta=None, bias=None):
+    """(Wf, bf) in float64: the next layer's weight and bias with LayerNorm's
+    scale and shift folded in (Wf = W diag(gamma), bf = bias + W beta)."""
+    W, g = _f32(W), _f32(gamma)
+    N, K = W.shape
+    assert g.shape == (K,)
+    bt = None if beta is None else _f32(beta)
+    b = None if bias is None else _f32(bias)
+    Wf = np.empty((N, K), dtype=np.float64)
+    bf = np.empty((N,), dtype=np.float64)
+    _load().oracle_fold_layernorm(N, K, W.ctypes.data, None if b is None else b.ctypes.data, g.ctypes.data,
+                                  None if bt is None else bt.ctypes.data, Wf.ctypes.data, bf.ctypes.data)
+    return Wf, bf
+
+
+def backward_dx_gelu(dZ, W, Zp, nthreads: int = 0) -> np.ndarray:
+    """dZp (float64, M x K) = (dZ . W) * gelu'(Zp): dX carried through the GELU
+    that produced X from the previous layer's pre-activation Zp (M x K)."""
+    dZ, W, Zp = _f32(dZ), _f32(W), _f32(Zp)
+    M, N = dZ.shape
+    N2, K = W.shape
+    assert N == N2 and Zp.shape == (M, K)
+    out = np.empty((M, K), dtype=np.float64)
+    _load().oracle_backward_dx_gelu(M, N, K, dZ.ctypes.data, W.ctypes.data, Zp.ctypes.data, out.ctypes.data,
+                                    int(nthreads))
     return out
 
 

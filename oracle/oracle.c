@@ -23,7 +23,8 @@
  *   evaluation but print no formula; this form and its constants are those of
  *   Hendrycks and Gimpel, "Gaussian Error Linear Units" (2016).
  *
- * The backward of the same layer (dZ, dX, dW, db) is defined further down.
+ * The backward of the same layer (dZ, dX, dW, db), the fused residual, the
+ * LayerNorm fold and the dX carried through a GELU are defined further down.
  *
  * OpenMP splits the (m, n) outputs across threads; each output's k order is
  * fixed, so the result does not depend on the thread count.
@@ -189,6 +190,103 @@ void oracle_gelu_grad_array(int64_t count, const double* in, double* out)
 {
     for (int64_t i = 0; i < count; ++i)
         out[i] = oracle_gelu_tanh_grad(in[i]);
+}
+
+/*
+ * Residual add in the GEMM's store ("Optimizing a GPT-2-class transformer on
+ * a GPU", Act II, rung 10: bias, relu and residual adds move inside the GEMM's
+ * store; "Writing a CUDA matmul that catches cuBLAS", "The residual and GELU
+ * go the same way"):
+ *
+ *   Y[m][n] = act(Z[m][n]) + R[m][n],   Z = X W^T + bias,
+ *
+ * R (M x N, fp32 values) is the residual stream, added after the activation
+ * (the transformer's x + sublayer(x); the pages give no order, the
+ * activation-free case is the one a GPT block uses).
+ */
+void oracle_linear_residual(int64_t M, int64_t N, int64_t K, const float* X, const float* W,
+                            const float* bias, const float* R, int gelu, double* Y, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for collapse(2) schedule(static) num_threads(nthreads)
+#endif
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            Y[m * N + n] = one_output(K, X + m * K, W + n * K, bias, n, gelu) + (double)R[m * N + n];
+    (void)nthreads;
+}
+
+/*
+ * LayerNorm over the last axis (the definition, in double):
+ *   mean = (1/K) sum_k x[k],  var = (1/K) sum_k (x[k] - mean)^2,
+ *   xhat[k] = (x[k] - mean) / sqrt(var + eps),
+ *   out[k] = gamma[k] xhat[k] + beta[k]   (gamma / beta NULL: xhat alone).
+ * Sums in ascending k. X: M*K fp32 values, out: M*K double.
+ */
+void oracle_layernorm(int64_t M, int64_t K, const float* X, const float* gamma, const float* beta,
+                      double eps, double* out)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        const float* x = X + m * K;
+        double mean = 0.0, var = 0.0;
+        for (int64_t k = 0; k < K; ++k) mean += (double)x[k];
+        mean /= (double)K;
+        for (int64_t k = 0; k < K; ++k) var += ((double)x[k] - mean) * ((double)x[k] - mean);
+        var /= (double)K;
+        const double inv = 1.0 / sqrt(var + eps);
+        for (int64_t k = 0; k < K; ++k) {
+            double v = ((double)x[k] - mean) * inv;
+            if (gamma) v *= (double)gamma[k];
+            if (beta) v += (double)beta[k];
+            out[m * K + k] = v;
+        }
+    }
+}
+
+/*
+ * LayerNorm fold (Act II, rung 10: the scale and shift of a layernorm feed
+ * only linear maps, so they fold into the next layer's weights offline, in
+ * double). With LN(x) = gamma * xhat + beta,
+ *   W LN(x) + b = (W diag(gamma)) xhat + (W beta + b), so
+ *   Wf[n][k] = W[n][k] * gamma[k],   bf[n] = b[n] + sum_k W[n][k] * beta[k]
+ * (ascending k; bias or beta NULL count as zero). W: N*K, gamma, beta: K
+ * (fp32 values); Wf: N*K, bf: N (double).
+ */
+void oracle_fold_layernorm(int64_t N, int64_t K, const float* W, const float* bias, const float* gamma,
+                           const float* beta, double* Wf, double* bf)
+{
+    for (int64_t n = 0; n < N; ++n) {
+        double s = bias ? (double)bias[n] : 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            Wf[n * K + k] = (double)W[n * K + k] * (double)gamma[k];
+            if (beta) s += (double)W[n * K + k] * (double)beta[k];
+        }
+        bf[n] = s;
+    }
+}
+
+/*
+ * dX of a layer whose input is the GELU of the previous layer's
+ * pre-activation Zp (X = gelu(Zp)), carried through that GELU in the same
+ * pass: dZp[m][k] = (sum_n dZ[m][n] W[n][k]) * gelu'(Zp[m][k]).
+ * dZ: M*N, W: N*K, Zp: M*K (fp32 values); dZp: M*K (double).
+ */
+void oracle_backward_dx_gelu(int64_t M, int64_t N, int64_t K, const float* dZ, const float* W,
+                             const float* Zp, double* dZp, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for collapse(2) schedule(static) num_threads(nthreads)
+#endif
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k) {
+            double s = 0.0;
+            for (int64_t n = 0; n < N; ++n)
+                s += (double)dZ[m * N + n] * (double)W[n * K + k];
+            dZp[m * K + k] = s * oracle_gelu_tanh_grad((double)Zp[m * K + k]);
+        }
+    (void)nthreads;
 }
 
 int oracle_max_threads(void)

@@ -260,3 +260,112 @@ def pin_backward_closed_forms(bwd):
 
 
 BACKWARD_PINS = (pin_backward_finite_differences, pin_backward_closed_forms)
+
+
+# ------------------------------------------- fused residual, LayerNorm fold, dX through GELU
+
+
+def pin_residual(fr):
+    """Y = act(X W^T + b) + R: W = 0 and no bias give Y = R exactly (gelu(0) = 0);
+    small integers match a brute-force integer sum exactly; the residual is
+    added after the activation (bias-only layer: gelu(b) + R, with GELU from
+    torch, not gelu(b + R))."""
+    rng = _rng(61)
+    M, N, K = 3, 5, 4
+    R = rng.integers(-9, 10, (M, N)).astype(np.float32)
+    X = rng.integers(-3, 4, (M, K)).astype(np.float32)
+    for gelu in (False, True):
+        assert np.array_equal(fr(X, np.zeros((N, K), np.float32), R, None, gelu), R.astype(np.float64))
+    W = rng.integers(-3, 4, (N, K)).astype(np.float32)
+    b = rng.integers(-5, 6, (N,)).astype(np.float32)
+    want = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            want[m, n] = sum(int(X[m, k]) * int(W[n, k]) for k in range(K)) + int(b[n]) + int(R[m, n])
+    assert np.array_equal(fr(X, W, R, b, False), want)
+    bias = np.array([1.0, -0.5, 2.0], np.float32)
+    Rb = np.full((2, 3), 1.5, np.float32)
+    g = torch.nn.functional.gelu(torch.tensor(bias, dtype=torch.float64), approximate="tanh").numpy()
+    got = fr(np.zeros((2, 1), np.float32), np.zeros((3, 1), np.float32), Rb, bias, True)
+    assert np.max(np.abs(got - (g[None, :] + 1.5))) <= 1e-15
+
+
+def pin_layernorm(ln):
+    """LayerNorm equals torch's layer_norm in float64 (biased variance, eps
+    inside the root); xhat has mean 0 and mean square var / (var + eps); with
+    eps = 0 it is invariant to x -> a x + c (a > 0)."""
+    rng = _rng(62)
+    X = (rng.standard_normal((4, 37)) * 3 + 1).astype(np.float32)
+    gamma = rng.standard_normal(37).astype(np.float32)
+    beta = rng.standard_normal(37).astype(np.float32)
+    ref = torch.nn.functional.layer_norm(torch.tensor(X, dtype=torch.float64), (37,),
+                                         torch.tensor(gamma, dtype=torch.float64),
+                                         torch.tensor(beta, dtype=torch.float64), eps=1e-5).numpy()
+    assert np.max(np.abs(ln(X, gamma, beta, 1e-5) - ref)) <= 1e-12
+    xh = ln(X, None, None, 1e-5)
+    Xd = X.astype(np.float64)
+    var = Xd.var(axis=1)
+    assert np.max(np.abs(xh.mean(axis=1))) <= 1e-14
+    assert np.max(np.abs((xh ** 2).mean(axis=1) - var / (var + 1e-5))) <= 1e-12
+    Y = (X * 4.0 + 3.0).astype(np.float32)  # exact in fp32 for these magnitudes? close enough at 1e-6
+    assert np.max(np.abs(ln(Y, None, None, 0.0) - ln(X, None, None, 0.0))) <= 1e-5
+
+
+def pin_fold(fold, ln):
+    """The fold is exact algebra: W LN(x) + b = Wf xhat + bf for random data
+    (LayerNorm from torch, products by numpy in float64); gamma = 1, beta = 0
+    leave W and b unchanged; small integers match a brute-force fold."""
+    rng = _rng(63)
+    N, K, M = 7, 11, 5  # N != K: a transposed or mis-indexed fold cannot pass
+    W = rng.standard_normal((N, K)).astype(np.float32)
+    b = rng.standard_normal(N).astype(np.float32)
+    gamma = (rng.standard_normal(K) + 1).astype(np.float32)
+    beta = rng.standard_normal(K).astype(np.float32)
+    X = rng.standard_normal((M, K)).astype(np.float32)
+    t = lambda a: torch.tensor(a, dtype=torch.float64)
+    lnx = torch.nn.functional.layer_norm(t(X), (K,), t(gamma), t(beta), eps=1e-5).numpy()
+    xhat = torch.nn.functional.layer_norm(t(X), (K,), None, None, eps=1e-5).numpy()
+    Wf, bf = fold(W, gamma, beta, b)
+    want = lnx @ W.astype(np.float64).T + b.astype(np.float64)
+    got = xhat @ Wf.T + bf
+    assert np.max(np.abs(got - want)) <= 1e-12 * max(1.0, np.max(np.abs(want)))
+    Wf1, bf1 = fold(W, np.ones(K, np.float32), np.zeros(K, np.float32), b)
+    assert np.array_equal(Wf1, W.astype(np.float64)) and np.array_equal(bf1, b.astype(np.float64))
+    Wi = rng.integers(-4, 5, (N, K)).astype(np.float32)
+    gi = rng.integers(-3, 4, K).astype(np.float32)
+    bi = rng.integers(-3, 4, K).astype(np.float32)
+    ci = rng.integers(-9, 10, N).astype(np.float32)
+    Wf, bf = fold(Wi, gi, bi, ci)
+    for n in range(N):
+        assert bf[n] == int(ci[n]) + sum(int(Wi[n, k]) * int(bi[k]) for k in range(K))
+        for k in range(K):
+            assert Wf[n, k] == int(Wi[n, k]) * int(gi[k])
+    _, bf0 = fold(Wi, gi, None, None)
+    assert np.array_equal(bf0, np.zeros(N))
+
+
+def pin_dx_gelu(dxg):
+    """dX carried through the GELU of the previous layer: the central
+    difference of L(Zp) = sum(G * (gelu(Zp) W^T + b)) (GELU from torch, the
+    product by numpy, all in float64) equals dxg(G, W, Zp); at Zp = 0 the
+    slope is 1/2, so W = I gives G / 2 exactly."""
+    M, N, K = 3, 4, 5
+    G, W, b, Zp = _grid(64, 1, (M, N)), _grid(64, 2, (N, K)), _grid(64, 3, (N,)), _grid(64, 4, (M, K))
+    gelu_t = lambda z: torch.nn.functional.gelu(torch.tensor(z, dtype=torch.float64), approximate="tanh").numpy()
+    Wd, bd, Gd = W.astype(np.float64), b.astype(np.float64), G.astype(np.float64)
+    L = lambda Z: float(np.sum(Gd * (gelu_t(Z) @ Wd.T + bd)))
+    h = 2.0 ** -12
+    num = np.zeros((M, K))
+    for idx in np.ndindex(M, K):
+        Zpp, Zpm = Zp.astype(np.float64).copy(), Zp.astype(np.float64).copy()
+        Zpp[idx] += h
+        Zpm[idx] -= h
+        num[idx] = (L(Zpp) - L(Zpm)) / (2 * h)
+    got = dxg(G, W, Zp)
+    assert np.max(np.abs(got - num)) <= 1e-6 * max(1.0, np.max(np.abs(num)))
+    Gs = _grid(64, 5, (M, K))
+    assert np.array_equal(dxg(Gs, np.eye(K, dtype=np.float32), np.zeros((M, K), np.float32)),
+                          Gs.astype(np.float64) / 2)
+
+
+NEXT4_PINS = (pin_residual, pin_layernorm, pin_fold, pin_dx_gelu)

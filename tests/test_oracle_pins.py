@@ -224,3 +224,98 @@ def test_backward_pins_catch_mutant(name):
         except (AssertionError, ValueError):
             caught = True
     assert caught, f"no backward pin catches mutant {name}"
+
+
+# ------------------------------------- fused residual, LayerNorm fold, dX through GELU
+
+from oracle_pins import NEXT4_PINS, pin_dx_gelu, pin_fold, pin_layernorm, pin_residual  # noqa: E402
+
+REAL_NEXT4 = {
+    pin_residual: (lambda X, W, R, b, g: oracle.linear_residual(X, W, R, b, g),),
+    pin_layernorm: (lambda X, g, b, eps: oracle.layernorm(X, g, b, eps),),
+    pin_fold: (lambda W, g, bt, b: oracle.fold_layernorm(W, g, bt, b), oracle.layernorm),
+    pin_dx_gelu: (lambda dZ, W, Zp: oracle.backward_dx_gelu(dZ, W, Zp),),
+}
+
+
+@pytest.mark.parametrize("pin", NEXT4_PINS, ids=lambda p: p.__name__)
+def test_next4_meets_pin(pin):
+    pin(*REAL_NEXT4[pin])
+
+
+def _resid_np(after_act=True, drop=False):
+    def fr(X, W, R, b, gelu):
+        Z = X.astype(np.float64) @ W.astype(np.float64).T + (0 if b is None else b.astype(np.float64))
+        Rd = 0.0 if drop else R.astype(np.float64)
+        if not after_act:
+            Z = Z + Rd
+        Y = _gelu_np(Z) if gelu else Z
+        return Y + Rd if after_act else Y
+    return fr
+
+
+def _fold_np(transposed=False, no_bias=False, beta_scaled=False, gamma_on_rows=False):
+    def fold(W, gamma, beta=None, bias=None):
+        W = W.astype(np.float64)
+        g = gamma.astype(np.float64)
+        bt = np.zeros(W.shape[1]) if beta is None else beta.astype(np.float64)
+        b = np.zeros(W.shape[0]) if (bias is None or no_bias) else bias.astype(np.float64)
+        if gamma_on_rows:  # scale row n by gamma[n] (gamma read with the wrong index)
+            Wf = W * np.resize(g, W.shape[0])[:, None]
+        elif transposed:
+            Wf = (W.T * g[:, None]).T.copy() if W.shape[0] == W.shape[1] else W * np.resize(g, W.shape[0])[:, None]
+        else:
+            Wf = W * g[None, :]
+        bf = b + ((W * g[None, :]) @ bt if beta_scaled else W @ bt)
+        return Wf, bf
+    return fold
+
+
+def _ln_np(biased=True, eps_outside=False):
+    def ln(X, gamma=None, beta=None, eps=1e-5):
+        X = X.astype(np.float64)
+        mu = X.mean(axis=1, keepdims=True)
+        var = X.var(axis=1, keepdims=True, ddof=0 if biased else 1)
+        xh = (X - mu) / (np.sqrt(var) + eps if eps_outside else np.sqrt(var + eps))
+        if gamma is not None:
+            xh = xh * gamma.astype(np.float64)
+        if beta is not None:
+            xh = xh + beta.astype(np.float64)
+        return xh
+    return ln
+
+
+def _dxg_np(no_slope=False, slope_of_dx=False):
+    def dxg(dZ, W, Zp):
+        dx = dZ.astype(np.float64) @ W.astype(np.float64)
+        if no_slope:
+            return dx
+        return dx * _gg_np(dx if slope_of_dx else Zp.astype(np.float64))
+    return dxg
+
+
+NEXT4_MUTANTS = {
+    "residual_before_activation": (pin_residual, (_resid_np(after_act=False),)),
+    "residual_dropped": (pin_residual, (_resid_np(drop=True),)),
+    "layernorm_unbiased_variance": (pin_layernorm, (_ln_np(biased=False),)),
+    "layernorm_eps_outside_root": (pin_layernorm, (_ln_np(eps_outside=True),)),
+    "fold_gamma_on_rows": (pin_fold, (_fold_np(gamma_on_rows=True), _ln_np())),
+    "fold_bias_dropped": (pin_fold, (_fold_np(no_bias=True), _ln_np())),
+    "fold_beta_scaled_by_gamma": (pin_fold, (_fold_np(beta_scaled=True), _ln_np())),
+    "dx_gelu_slope_missing": (pin_dx_gelu, (_dxg_np(no_slope=True),)),
+    "dx_gelu_slope_of_wrong_tensor": (pin_dx_gelu, (_dxg_np(slope_of_dx=True),)),
+}
+
+
+def test_next4_mutant_references_are_sound():
+    pin_residual(_resid_np())
+    pin_layernorm(_ln_np())
+    pin_fold(_fold_np(), _ln_np())
+    pin_dx_gelu(_dxg_np())
+
+
+@pytest.mark.parametrize("name", sorted(NEXT4_MUTANTS))
+def test_next4_pins_catch_mutant(name):
+    pin, args = NEXT4_MUTANTS[name]
+    with pytest.raises(AssertionError):
+        pin(*args)
