@@ -411,8 +411,13 @@ def bench_ours(layer: si.Layer, steps: int, warmup: int, world: int, rank: int, 
 # ---------------------------------------------------------------- backward
 
 class BwdWork:
-    """A backward GEMM of a layer: which 1 is dX = dZ W (M x K, reduction N),
-    which 2 is dW = dZ^T X (N x K, reduction M)."""
+    """A backward GEMM of a layer or a fused forward: which 1 is dX = dZ W
+    (M x K, reduction N), 2 is dW = dZ^T X (N x K, reduction M), 3 is dX
+    carried through the previous layer's GELU, (dZ W) * gelu'(Zp) (reads Zp,
+    M x K, too), 4 is the forward with the residual add in its store,
+    Y = X W^T + bias + R (reads R, M x N)."""
+
+    COMPUTES = {1: "dX = dZ W", 2: "dW = dZ^T X", 3: "dZp = (dZ W) * gelu'(Zp)", 4: "Y = X W^T + bias + R"}
 
     def __init__(self, name, which, M, N, K, precision):
         self.name, self.which, self.M, self.N, self.K, self.precision = name, which, M, N, K, precision
@@ -420,9 +425,13 @@ class BwdWork:
 
     def algorithmic_bytes(self):
         esz = 2 if self.precision == si.PREC_BF16 else 4
-        other = self.N * self.K if self.which == 1 else self.M * self.K   # W or X
-        out = self.M * self.K if self.which == 1 else self.N * self.K     # dX or dW
-        return (self.M * self.N + other + out) * esz
+        M, N, K = self.M, self.N, self.K
+        if self.which == 4:  # X, W, R and Y once each, plus the fp32 bias
+            return (M * K + N * K + 2 * M * N) * esz + 4 * N
+        other = N * K if self.which in (1, 3) else M * K   # W or X
+        out = M * K if self.which in (1, 3) else N * K     # dX or dW
+        extra = M * K if self.which == 3 else 0            # Zp
+        return (M * N + other + out + extra) * esz
 
 
 BWD_WORKLOADS = [BwdWork(f"{base}_{'dx' if which == 1 else 'dw'}", which, M, N, K, prec)
@@ -430,13 +439,20 @@ BWD_WORKLOADS = [BwdWork(f"{base}_{'dx' if which == 1 else 'dw'}", which, M, N, 
                                              ("gpt2_fc2_m8192_bf16", 8192, 768, 3072, si.PREC_BF16),
                                              ("gpt2_fc1_m128_fp32", 128, 3072, 768, si.PREC_FP32),
                                              ("gpt2_fc2_m128_fp32", 128, 768, 3072, si.PREC_FP32))
-                 for which in (1, 2)]
+                 for which in (1, 2)] + [
+    BwdWork("gpt2_fc2_m8192_bf16_dx_gelu", 3, 8192, 768, 3072, si.PREC_BF16),
+    BwdWork("gpt2_fc2_m128_fp32_dx_gelu", 3, 128, 768, 3072, si.PREC_FP32),
+    BwdWork("gpt2_proj_m8192_bf16_residual", 4, 8192, 768, 768, si.PREC_BF16),
+    BwdWork("gpt2_fc2_m8192_bf16_residual", 4, 8192, 768, 3072, si.PREC_BF16),
+    BwdWork("gpt2_proj_m128_fp32_residual", 4, 128, 768, 768, si.PREC_FP32)]
 
 
 def bench_backward(work: BwdWork, steps: int, warmup: int, world: int, rank: int, local_rank: int):
-    """Back-to-back backward GEMMs through the C ABI (lin_backward_data /
-    lin_backward_weight), dZ rotating over copies larger than L2, replayed from
-    a CUDA graph; parity gate on sampled output rows against the oracle."""
+    """Back-to-back backward GEMMs or fused forwards through the C ABI
+    (lin_backward_data, lin_backward_weight, lin_backward_data_gelu,
+    lin_forward_residual), the streamed operand (dZ, or W for the forward)
+    rotating over copies larger than L2, replayed from a CUDA graph; parity
+    gate on sampled output rows against the oracle."""
     import torch
 
     import oracle
@@ -451,31 +467,48 @@ def bench_backward(work: BwdWork, steps: int, warmup: int, world: int, rank: int
     dt = torch.bfloat16 if work.precision == si.PREC_BF16 else torch.float32
     esz = 2 if work.precision == si.PREC_BF16 else 4
     M, N, K = work.M, work.N, work.K
-    dZ = si.normal(31, 1, (M, N), 0.0, 0.1)
-    B = si.normal(31, 2, (N, K), 0.0, 0.02) if work.which == 1 else si.normal(31, 3, (M, K))
-    if work.precision == si.PREC_BF16:
-        dZ, B = si.round_bf16(dZ), si.round_bf16(B)
+    rnd = si.round_bf16 if work.precision == si.PREC_BF16 else (lambda a: a)
+    if work.which == 4:  # forward: "dZ" is X (M x K), B is W (N x K), plus bias and the residual R
+        dZ = rnd(si.normal(31, 1, (M, K)))
+        B = rnd(si.normal(31, 2, (N, K), 0.0, 0.02))
+        R = rnd(si.normal(31, 4, (M, N)))
+        bias_h = si.normal(31, 5, (N,), 0.0, 0.02)
+        bias_d = torch.from_numpy(bias_h).to(dev)
+        r_dev = torch.from_numpy(R).to(dev).to(dt)
+    else:
+        dZ = rnd(si.normal(31, 1, (M, N), 0.0, 0.1))
+        B = rnd(si.normal(31, 2, (N, K), 0.0, 0.02) if work.which in (1, 3) else si.normal(31, 3, (M, K)))
+        if work.which == 3:
+            Zp = rnd(si.normal(31, 4, (M, K)))
+            zp_dev = torch.from_numpy(Zp).to(dev).to(dt)
     dz0 = torch.from_numpy(dZ).to(dev).to(dt)
     b_dev = torch.from_numpy(B).to(dev).to(dt)
-    dz_bytes = M * N * esz
-    n_copies = max(2, math.ceil(4 * l2 / dz_bytes))
-    while n_copies > 2 and n_copies * dz_bytes > (8 << 30):
+    rot0 = b_dev if work.which == 4 else dz0  # the operand streamed from HBM every step
+    rot_bytes = rot0.numel() * esz
+    n_copies = max(2, math.ceil(4 * l2 / rot_bytes))
+    while n_copies > 2 and n_copies * rot_bytes > (8 << 30):
         n_copies -= 1
-    dzs = [dz0] + [dz0.clone() for _ in range(n_copies - 1)]
-    out = torch.empty((M, K) if work.which == 1 else (N, K), dtype=dt, device=dev)
+    rots = [rot0] + [rot0.clone() for _ in range(n_copies - 1)]
+    out = torch.empty((M, N) if work.which == 4 else ((M, K) if work.which in (1, 3) else (N, K)), dtype=dt,
+                      device=dev)
     stream = torch.cuda.Stream(dev)
     sptr = stream.cuda_stream
-    fn = lib.lin_backward_data if work.which == 1 else lib.lin_backward_weight
 
     def step(i):
+        r = rots[i % n_copies].data_ptr()
         if work.which == 1:
-            rc = fn(ctx._h, M, N, K, dzs[i % n_copies].data_ptr(), b_dev.data_ptr(), out.data_ptr(),
-                    work.precision, sptr)
+            rc = lib.lin_backward_data(ctx._h, M, N, K, r, b_dev.data_ptr(), out.data_ptr(), work.precision, sptr)
+        elif work.which == 2:
+            rc = lib.lin_backward_weight(ctx._h, M, N, K, r, b_dev.data_ptr(), out.data_ptr(), None,
+                                         work.precision, sptr)
+        elif work.which == 3:
+            rc = lib.lin_backward_data_gelu(ctx._h, M, N, K, r, b_dev.data_ptr(), zp_dev.data_ptr(), out.data_ptr(),
+                                            work.precision, sptr)
         else:
-            rc = fn(ctx._h, M, N, K, dzs[i % n_copies].data_ptr(), b_dev.data_ptr(), out.data_ptr(), None,
-                    work.precision, sptr)
+            rc = lib.lin_forward_residual(ctx._h, M, N, K, dz0.data_ptr(), r, bias_d.data_ptr(), r_dev.data_ptr(),
+                                          out.data_ptr(), 0, work.precision, sptr)
         if rc != 0:
-            raise tll.LinError(rc, "lin_backward")
+            raise tll.LinError(rc, work.COMPUTES[work.which])
 
     with torch.cuda.stream(stream):
         step(0)
@@ -485,8 +518,12 @@ def bench_backward(work: BwdWork, steps: int, warmup: int, world: int, rank: int
     rows = np.unique(np.concatenate([rng.integers(0, out.shape[0], 64), [0, out.shape[0] - 1]]))
     if work.which == 1:
         ref = oracle.backward_dx(dZ[rows], B)
-    else:
+    elif work.which == 2:
         ref, _ = oracle.backward_dw(dZ[:, rows], B, with_bias=False)
+    elif work.which == 3:
+        ref = oracle.backward_dx_gelu(dZ[rows], B, Zp[rows])
+    else:
+        ref = oracle.linear_residual(dZ[rows], B, R[rows], bias_h)
     got = out[torch.from_numpy(rows).to(dev)].float().cpu().numpy()
     err = oracle.rel_err(got, ref)
     tol = oracle.TOL[si.PREC_BF16] if work.precision == si.PREC_BF16 else oracle.TOL[si.PREC_FP32]
@@ -544,9 +581,11 @@ def bench_backward(work: BwdWork, steps: int, warmup: int, world: int, rank: int
         "n_gpus": world, "steps": steps, "warmup": warmup, "ms_per_step": round(max_s / steps * 1e3, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": prec, "data": "synthetic",
         "config": {"workload": work.name, "M": M, "N": N, "K": K,
-                   "computes": "dX = dZ W" if work.which == 1 else "dW = dZ^T X",
-                   "kernel": "tc (MN-major operands)" if work.precision == si.PREC_BF16 else "bwd_ffma",
-                   "l2": f"cold dZ: {n_copies} rotating copies ({n_copies * dz_bytes >> 20} MiB > L2 {l2 >> 20} MiB), "
+                   "computes": work.COMPUTES[work.which],
+                   "kernel": tll.KERNEL_NAMES[ctx.last_plan().kernel] if work.which == 4 else
+                   ("tc (MN-major operands)" if work.precision == si.PREC_BF16 else "bwd_ffma"),
+                   "l2": f"cold {'W' if work.which == 4 else 'dZ'}: {n_copies} rotating copies "
+                         f"({n_copies * rot_bytes >> 20} MiB > L2 {l2 >> 20} MiB), "
                          f"steps replayed from a CUDA graph of {G}",
                    "parity_gate": {"rel_err": err, "rel_err_after_timed_steps": err_after, "tol": tol,
                                    "compared": f"{len(rows)} sampled output rows"}},

@@ -132,12 +132,44 @@ LIN_API int lin_destroy(lin_ctx* ctx);
  * inputs (X, W, bias) overlap none of the previous call's output on the same
  * stream is launched as a programmatic dependent of that call, reads its
  * inputs before the previous kernel has finished and writes Y only after it.
- * For such a call with M <= 16 (BF16) the skinny kernel also drops its K split
- * (one CTA per 128 rows of W), so that consecutive independent calls stream
- * their weights concurrently; lin_plan_query returns the plan of an isolated
+ * For such a call the built-in plan may also drop its K split (the skinny
+ * kernel's cluster split, the tensor-core K split, an FFMA split over a short
+ * K), so that consecutive independent calls fill the SMs together; see
+ * LIN_OPT_ADAPTIVE_PLANS. lin_plan_query returns the plan of an isolated
  * call. */
 LIN_API int lin_forward(lin_ctx* ctx, int M, int N, int K, const void* X, const void* W,
                 const float* bias, void* Y, int epilogue, int precision, void* stream);
+
+/* Y = act(X . W^T + bias) + R: the residual add in the GEMM's store
+ * ("Optimizing a GPT-2-class transformer on a GPU", Act II, rung 10: bias,
+ * relu and residual adds move inside the GEMM's store; "Writing a CUDA matmul
+ * that catches cuBLAS", "The residual and GELU go the same way"). A
+ * transformer block's x = x + proj(h) is this call with R = Y = x.
+ *   R : M x N row-major, Y's element type; added after the activation, in
+ *       fp32, with one rounding of the sum to Y's type. R may be Y itself (in
+ *       place) and must otherwise not overlap Y; NULL is LIN_ERR_ARG (use
+ *       lin_forward). Aligned to its element.
+ * Everything else as lin_forward (same dispatch, installed plans included). */
+LIN_API int lin_forward_residual(lin_ctx* ctx, int M, int N, int K, const void* X, const void* W,
+                                 const float* bias, const void* R, void* Y, int epilogue, int precision,
+                                 void* stream);
+
+/* LayerNorm fold ("Optimizing a GPT-2-class transformer on a GPU", Act II,
+ * rung 10: a layernorm's scale and shift feed only linear maps, so they fold
+ * into the next layer's weights offline, in double). With
+ * LN(x) = gamma * xhat + beta, xhat = (x - mean) / sqrt(var + eps):
+ *   W LN(x) + bias = W_out xhat + bias_out,
+ *   W_out[n][k] = W[n][k] * gamma[k],  bias_out[n] = bias[n] + sum_k W[n][k] * beta[k].
+ *   W        : N x K fp32 (device), the layer's weight (out x in).
+ *   bias     : N fp32 or NULL (zero).   gamma : K fp32.   beta : K fp32 or NULL (zero).
+ *   W_out    : N x K in the storage type of `precision` (fp32 for FP32/TF32,
+ *              bf16 for BF16); may be W itself for fp32 storage (in place).
+ *   bias_out : N fp32; may be bias itself.
+ * Products and the sum (ascending k) in double; each output rounded once to
+ * nearest even. Other overlaps: LIN_ERR_ARG; pointers aligned to their
+ * elements (LIN_ERR_ALIGN). Asynchronous on `stream`. */
+LIN_API int lin_fold_layernorm(lin_ctx* ctx, int N, int K, const float* W, const float* bias, const float* gamma,
+                               const float* beta, void* W_out, float* bias_out, int precision, void* stream);
 
 /* Same, with an explicit launch configuration (for tuning and for tests that
  * must reach one kernel). The plan is validated; LIN_ERR_UNSUPPORTED if its
@@ -199,6 +231,17 @@ LIN_API int lin_backward_weight(lin_ctx* ctx, int M, int N, int K, const void* d
 LIN_API int lin_gelu_backward(lin_ctx* ctx, long long count, const void* dY, const void* Z, void* dZ,
                               int precision, void* stream);
 
+/* dX carried through the previous layer's GELU in the same pass: when this
+ * layer's input was X = gelu(Zp) (Zp the previous layer's pre-activation),
+ *   dZp = (dZ . W) * gelu'(Zp)      (M x K),
+ * i.e. lin_backward_data followed by lin_gelu_backward, with the slope
+ * applied in the GEMM's store instead of a second pass over M x K.
+ *   Zp : M x K row-major in the precision's storage type; dZp may be Zp
+ *        itself (in place) and must otherwise not overlap it.
+ * Everything else as lin_backward_data. */
+LIN_API int lin_backward_data_gelu(lin_ctx* ctx, int M, int N, int K, const void* dZ, const void* W,
+                                   const void* Zp, void* dZp, int precision, void* stream);
+
 /* Measured dispatch ("Optimizing a GPT-2-class transformer on a GPU", Act II:
  * route each shape to its measured winner). Install `plan` as the context's
  * choice for lin_forward calls with exactly these sizes, precision and
@@ -229,9 +272,19 @@ LIN_API int lin_check_device(lin_ctx* ctx, void* stream);
  *   copying W before that kernel finishes; X and bias are read, and Y written,
  *   only after it has finished. The library drops the early start by itself
  *   when W overlaps the previous call's output on that stream. 0 = every call
- *   waits for the previous kernel before it starts. */
+ *   waits for the previous kernel before it starts.
+ * LIN_OPT_ADAPTIVE_PLANS (default 1): a call that overlaps an independent
+ *   predecessor on its stream (both launched with the early start) may drop
+ *   the K split of its built-in plan: the neighbouring call then fills the SMs
+ *   the split would. A split changes the order of the fp32 sums, so with this
+ *   option on, the last bits of a result can depend on the call before it on
+ *   the stream (never beyond the precision's tolerance). 0 = the plan of a
+ *   call depends only on its sizes, precision and epilogue, so identical
+ *   inputs give identical bits whatever ran before. Installed plans
+ *   (lin_set_plan_override) and lin_forward_plan are never adapted. */
 typedef enum {
-    LIN_OPT_EARLY_START = 1
+    LIN_OPT_EARLY_START = 1,
+    LIN_OPT_ADAPTIVE_PLANS = 2
 } lin_option;
 
 /* The plan of the last call launched through this context (host value, no

@@ -69,7 +69,7 @@ def kname(p):
 
 
 def test_dispatch_skinny_for_small_m_bf16():
-    for M in (5, 8, 16):  # (M <= 4 with X fitting in shared memory: the GEMV)
+    for M in (2, 5, 8, 16):  # (one row with X fitting in shared memory: the GEMV)
         p = tll.plan_query(SM, M, 4096, 4096, "bf16")
         assert kname(p) == "skinny" and p.splits > 1 and p.grid_y == p.splits
         assert p.grid_x * p.bn >= 4096 and p.grid_x * p.grid_y <= SM
@@ -170,9 +170,12 @@ def test_dispatch_gemv_for_few_fp32_rows():
     # X (rows x K fp32) must fit in shared memory; else the tiled kernels
     assert kname(tll.plan_query(SM, 8, 4096, 4096, "fp32")) == "ffma"
     assert kname(tll.plan_query(SM, 9, 4096, 768, "fp32")) == "ffma"
-    for M in (1, 3, 4):
-        assert kname(tll.plan_query(SM, M, 4096, 4096, "bf16")) == "gemv"
-    assert kname(tll.plan_query(SM, 5, 4096, 4096, "bf16")) == "skinny"
+    # bf16: one row, at most one 128-row tile of W per SM
+    assert kname(tll.plan_query(SM, 1, 4096, 4096, "bf16")) == "gemv"
+    assert kname(tll.plan_query(SM, 1, 128 * SM, 768, "bf16")) == "gemv"
+    assert kname(tll.plan_query(SM, 1, 128 * SM + 1, 768, "bf16")) == "skinny"
+    for M in (2, 4, 5):
+        assert kname(tll.plan_query(SM, M, 4096, 4096, "bf16")) == "skinny"
     assert kname(tll.plan_query(SM, 1, 4096, 32768, "bf16")) == "skinny"  # X does not fit as fp32
     p = tll.plan_make(SM, tll.KERNEL_GEMV, 0, 3, 5, 1000, 520, "fp32")
     assert p.grid_x == 3 and p.bm == 8

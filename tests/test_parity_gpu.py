@@ -431,27 +431,34 @@ def test_ffma_back_to_back(ctx, N, K):
 @pytest.mark.parametrize("precision", [FP32, TF32, BF16])
 @pytest.mark.parametrize("M", [1, 2, 3, 5, 8])
 def test_gemv_few_rows(ctx, precision, M):
-    """The one-row sites: fp32 / tf32 with M <= 8 and bf16 with M <= 4 run the
-    GEMV (exact fp32 arithmetic; bf16 products are exact in fp32). Ragged N and
-    K, bias and GELU, against the oracle; bitwise repeatable."""
+    """The one-row sites: fp32 / tf32 with M <= 8 and bf16 with one row run the
+    GEMV by default (exact fp32 arithmetic; bf16 products are exact in fp32);
+    bf16 with 2-4 rows runs it through an explicit plan. Ragged N and K, bias
+    and GELU, against the oracle; bitwise repeatable."""
     if precision == BF16 and M > 4:
-        pytest.skip("bf16 with M > 4 runs the skinny tensor-core kernel")
+        pytest.skip("the bf16 GEMV takes at most 4 rows")
     tol = oracle.TOL[BF16] if precision == BF16 else oracle.TOL[FP32]
     for N, K in [(1000, 520), (77, 8), (2304, 768), (300, 3072)]:
         layer = si.Layer("gemv", M, N, K, precision, si.EPI_GELU, bias=True)
         X, W, b = si.make_inputs(layer)
-        plan = ctx.plan(M, N, K, PREC_NAME[precision])
-        assert tll.KERNEL_NAMES[plan.kernel] == "gemv"
-        y = run(X, W, b, precision, epilogue=si.EPI_GELU, ctx=ctx)
+        plan = None
+        if precision == BF16 and M > 1:
+            plan = tll.plan_make(ctx.sm_count, tll.KERNEL_GEMV, 0, 0, M, N, K, "bf16")
+        else:
+            assert tll.KERNEL_NAMES[ctx.plan(M, N, K, PREC_NAME[precision]).kernel] == "gemv"
+        y = run(X, W, b, precision, epilogue=si.EPI_GELU, plan=plan, ctx=ctx)
         ref = oracle.linear(X, W, b, True)
         assert oracle.rel_err(y, ref) <= tol, (M, N, K)
-        assert np.array_equal(y, run(X, W, b, precision, epilogue=si.EPI_GELU, ctx=ctx))
+        assert np.array_equal(y, run(X, W, b, precision, epilogue=si.EPI_GELU, plan=plan, ctx=ctx))
 
 
 @pytest.mark.parametrize("precision", [FP32, BF16])
-def test_gemv_lm_head_row(precision):
-    """The last token's logits: 1 x 50257 x 768 (N odd), full compare."""
-    check_layer(si.Layer("logits", 1, 50257, 768, precision, bias=False))
+def test_gemv_lm_head_row(ctx, precision):
+    """The last token's logits: 1 x 50257 x 768 (N odd), full compare, through
+    the built-in table (GEMV for fp32, the skinny kernel for bf16) and the GEMV."""
+    layer = si.Layer("logits", 1, 50257, 768, precision, bias=False)
+    check_layer(layer)
+    check_layer(layer, plan=tll.plan_make(ctx.sm_count, tll.KERNEL_GEMV, 0, 0, 1, 50257, 768, PREC_NAME[precision]))
 
 
 def test_gemv_back_to_back_chain(ctx):
@@ -508,6 +515,7 @@ def test_layer_captured_in_one_graph(M, precision):
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         layer()  # first calls outside the capture (kernel attributes, device lookups)
+        layer()  # and the same call history as the captured calls (adaptive plans)
     stream.synchronize()
     eager = {n: t.clone() for n, t in outs.items()}
     g = torch.cuda.CUDAGraph()

@@ -30,6 +30,7 @@ EPI_NONE, EPI_GELU_TANH = 0, 1
 KERNEL_NONE, KERNEL_FILL, KERNEL_SKINNY, KERNEL_FFMA, KERNEL_TC, KERNEL_GEMV = 0, 1, 2, 3, 4, 5
 KERNEL_NAMES = {0: "none", 1: "fill", 2: "skinny", 3: "ffma", 4: "tc", 5: "gemv"}
 OPT_EARLY_START = 1
+OPT_ADAPTIVE_PLANS = 2
 OK, ERR_ARG, ERR_ALIGN, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
 
 _PREC_NAMES = {"fp32": PREC_FP32, "tf32": PREC_TF32, "bf16": PREC_BF16}
@@ -93,6 +94,9 @@ def library() -> ctypes.CDLL:
                 "lin_backward_data": ([P, I, I, I, P, P, P, I, P], I),
                 "lin_backward_weight": ([P, I, I, I, P, P, P, P, I, P], I),
                 "lin_gelu_backward": ([P, ctypes.c_longlong, P, P, P, I, P], I),
+                "lin_forward_residual": ([P, I, I, I, P, P, P, P, P, I, I, P], I),
+                "lin_backward_data_gelu": ([P, I, I, I, P, P, P, P, I, P], I),
+                "lin_fold_layernorm": ([P, I, I, P, P, P, P, P, P, I, P], I),
                 "lin_set_plan_override": ([P, I, I, I, I, I, PP], I),
                 "lin_clear_plan_overrides": ([P], I),
                 "lin_strerror": ([I], ctypes.c_char_p),
@@ -272,6 +276,56 @@ def forward(x, w, bias=None, epilogue="none", precision=None, out=None, ctx: Con
     return out
 
 
+def forward_residual(x, w, residual, bias=None, epilogue="none", precision=None, out=None,
+                     ctx: Context | None = None, stream=None):
+    """Y = act(x . w^T + bias) + residual, the add in the GEMM's store.
+    ``out`` may be ``residual`` itself (x = x + layer(h) in place); by
+    default Y is a new tensor."""
+    prec, M, N, K, out = _marshal(x, w, bias, out, precision)
+    _check(residual, out.dtype, (M, N), "residual")
+    dev = x.device.index if x.device.index is not None else 0
+    ctx = ctx or default_context(dev)
+    rc = library().lin_forward_residual(ctx._h, M, N, K, x.data_ptr(), w.data_ptr(),
+                                        None if bias is None else bias.data_ptr(), residual.data_ptr(),
+                                        out.data_ptr(), _epi(epilogue), prec, _stream_ptr(stream, dev))
+    if rc != OK:
+        raise LinError(rc, "lin_forward_residual")
+    return out
+
+
+def fold_layernorm(w, gamma, beta=None, bias=None, precision="fp32", w_out=None, bias_out=None,
+                   ctx: Context | None = None, stream=None):
+    """The next layer's (W, bias) with a LayerNorm's scale and shift folded in,
+    computed on the device in double: W_out = w diag(gamma), bias_out =
+    bias + w beta. ``w`` (N x K), ``gamma``, ``beta`` and ``bias`` are fp32;
+    W_out has the storage type of ``precision``. Returns (W_out, bias_out)."""
+    import torch
+
+    N, K = w.shape
+    _check(w, torch.float32, (N, K), "w")
+    _check(gamma, torch.float32, (K,), "gamma")
+    if beta is not None:
+        _check(beta, torch.float32, (K,), "beta")
+    if bias is not None:
+        _check(bias, torch.float32, (N,), "bias")
+    prec = _prec(precision)
+    wdt = torch.bfloat16 if prec == PREC_BF16 else torch.float32
+    if w_out is None:
+        w_out = torch.empty((N, K), dtype=wdt, device=w.device)
+    _check(w_out, wdt, (N, K), "w_out")
+    if bias_out is None:
+        bias_out = torch.empty((N,), dtype=torch.float32, device=w.device)
+    _check(bias_out, torch.float32, (N,), "bias_out")
+    dev = w.device.index if w.device.index is not None else 0
+    ctx = ctx or default_context(dev)
+    rc = library().lin_fold_layernorm(ctx._h, N, K, w.data_ptr(), None if bias is None else bias.data_ptr(),
+                                      gamma.data_ptr(), None if beta is None else beta.data_ptr(), w_out.data_ptr(),
+                                      bias_out.data_ptr(), prec, _stream_ptr(stream, dev))
+    if rc != OK:
+        raise LinError(rc, "lin_fold_layernorm")
+    return w_out, bias_out
+
+
 def forward_plan(plan: Plan, x, w, bias=None, epilogue="none", precision=None, out=None,
                  ctx: Context | None = None, stream=None):
     """As :func:`forward` with an explicit launch configuration."""
@@ -322,6 +376,30 @@ def backward_data(dz, w, out=None, precision=None, ctx: Context | None = None, s
                                      _stream_ptr(stream, dev))
     if rc != OK:
         raise LinError(rc, "lin_backward_data")
+    return out
+
+
+def backward_data_gelu(dz, w, zp, out=None, precision=None, ctx: Context | None = None, stream=None):
+    """dZp (M x K) = (dz . w) * gelu'(zp): the input gradient carried through
+    the GELU that made this layer's input from the previous layer's
+    pre-activation ``zp`` (M x K), in one pass. ``out`` may be ``zp``."""
+    import torch
+
+    prec, want = _bwd_dtype(dz, precision)
+    M, N = dz.shape
+    K = w.shape[1]
+    _check(dz, want, (M, N), "dz")
+    _check(w, want, (N, K), "w")
+    _check(zp, want, (M, K), "zp")
+    if out is None:
+        out = torch.empty((M, K), dtype=want, device=dz.device)
+    _check(out, want, (M, K), "out")
+    dev = dz.device.index if dz.device.index is not None else 0
+    ctx = ctx or default_context(dev)
+    rc = library().lin_backward_data_gelu(ctx._h, M, N, K, dz.data_ptr(), w.data_ptr(), zp.data_ptr(),
+                                          out.data_ptr(), prec, _stream_ptr(stream, dev))
+    if rc != OK:
+        raise LinError(rc, "lin_backward_data_gelu")
     return out
 
 

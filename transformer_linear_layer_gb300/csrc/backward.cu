@@ -24,17 +24,6 @@ namespace {
 
 // ------------------------------------------------------------ gelu backward
 
-// Slope of the tanh-form GELU (the derivative of the forward's
-// 0.5 s (1 + tanh(c (s + a s^3)))): 0.5 (1 + t) + 0.5 s (1 - t^2) c (1 + 3 a s^2).
-template <bool BF16OUT>
-__device__ __forceinline__ float gelu_tanh_slope(float s) {
-    const float c = 0.7978845608028654f;  // sqrt(2/pi)
-    const float a = 0.044715f;
-    const float u = c * (s + a * s * s * s);
-    const float t = BF16OUT ? tanh_hw(u) : tanhf(u);
-    return 0.5f * (1.0f + t) + 0.5f * s * (1.0f - t * t) * c * (1.0f + 3.0f * a * s * s);
-}
-
 template <bool BF16>
 __global__ void __launch_bounds__(256) gelu_backward_kernel(long long count, const void* dY, const void* Z, void* dZ) {
     const long long step = (long long)gridDim.x * blockDim.x;
@@ -95,6 +84,7 @@ struct BwdArgs {
     int splits;      // split-K: CTA z sums reduction stages [z * nst / S, (z + 1) * nst / S)
     float* ws;       // split-K partial sums [S][I][J]
     unsigned* counters;
+    const float* Zp; // WHICH 1: the previous layer's pre-activation (I x J): C *= gelu'(Zp); or null
 };
 
 constexpr int kBT = 64;   // output tile (I and J)
@@ -209,7 +199,10 @@ __global__ void __launch_bounds__(kBTh) bwd_ffma_kernel(const BwdArgs a) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int j = j0 + 4 * tx + q;
-                if (j < a.J) a.C[(size_t)i * a.J + j] = acc[p][q];
+                if (j < a.J) {
+                    const size_t o = (size_t)i * a.J + j;
+                    a.C[o] = a.Zp ? acc[p][q] * gelu_tanh_slope<false>(a.Zp[o]) : acc[p][q];
+                }
             }
         }
         return;
@@ -259,7 +252,10 @@ __global__ void __launch_bounds__(kBTh) bwd_ffma_kernel(const BwdArgs a) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int j = j0 + 4 * tx + q;
-            if (j < a.J) a.C[(size_t)i * a.J + j] = sum[q];
+            if (j < a.J) {
+                const size_t o = (size_t)i * a.J + j;
+                a.C[o] = a.Zp ? sum[q] * gelu_tanh_slope<false>(a.Zp[o]) : sum[q];
+            }
         }
     }
 }
@@ -329,8 +325,9 @@ int bwd_ffma_splits(int which, int M, int N, int K, int sm_count, size_t ws_byte
 }
 
 int launch_bwd_ffma(int which, int M, int N, int K, const float* dZ, const float* B, float* out, int splits,
-                    void* workspace, cudaStream_t st, bool early) {
-    BwdArgs a;
+                    void* workspace, cudaStream_t st, bool early, const float* Zp) {
+    BwdArgs a = {};
+    a.Zp = which == 1 ? Zp : nullptr;
     a.splits = splits < 1 ? 1 : splits;
     a.ws = a.splits > 1 ? splitk_partials(workspace) : nullptr;
     a.counters = a.splits > 1 ? splitk_counters(workspace) : nullptr;

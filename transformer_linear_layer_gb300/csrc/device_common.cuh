@@ -33,6 +33,17 @@ __device__ __forceinline__ float gelu_tanh_bf16out(float s) {
     return fmaf(hs, tanh_hw(k0 * (s + k1 * s * s * s)), hs);
 }
 
+// Slope of the tanh-form GELU (the derivative of 0.5 s (1 + tanh(c (s + a s^3)))):
+// 0.5 (1 + t) + 0.5 s (1 - t^2) c (1 + 3 a s^2). BF16OUT: the hardware tanh.
+template <bool BF16OUT>
+__device__ __forceinline__ float gelu_tanh_slope(float s) {
+    const float c = 0.7978845608028654f;  // sqrt(2/pi)
+    const float a = 0.044715f;
+    const float u = c * (s + a * s * s * s);
+    const float t = BF16OUT ? tanh_hw(u) : tanhf(u);
+    return 0.5f * (1.0f + t) + 0.5f * s * (1.0f - t * t) * c * (1.0f + 3.0f * a * s * s);
+}
+
 // Bias add and activation. BF16OUT: the result is rounded to bf16 next (the
 // activation may use the hardware tanh).
 template <bool GELU, bool BF16OUT = false>

@@ -42,6 +42,7 @@ struct FfmaArgs {
     const float* W;
     const float* bias;
     float* Y;
+    const float* R;    // residual added after the activation (M x N, may be Y itself), or null
     float* ws;
     unsigned* counters;
     int splits;
@@ -128,7 +129,10 @@ __device__ __forceinline__ void splitk_epilogue(const FfmaArgs& a, const float (
 #pragma unroll
         for (int c = 0; c < TN; ++c) {
             const int n = col_of(c);
-            if (n < a.N) a.Y[(size_t)m * a.N + n] = epilogue<GELU>(sum[c], bcol[c]);
+            if (n < a.N) {
+                const size_t i = (size_t)m * a.N + n;
+                a.Y[i] = epilogue<GELU>(sum[c], bcol[c]) + (a.R ? a.R[i] : 0.f);
+            }
         }
     }
 }
@@ -244,7 +248,10 @@ ffma_kernel(const FfmaArgs a) {
 #pragma unroll
             for (int r = 0; r < TM; ++r) {
                 const int m = row_of(r);
-                if (m < a.M) a.Y[(size_t)m * a.N + n] = epilogue<GELU>(acc[r][c], b);
+                if (m < a.M) {
+                    const size_t i = (size_t)m * a.N + n;
+                    a.Y[i] = epilogue<GELU>(acc[r][c], b) + (a.R ? a.R[i] : 0.f);
+                }
             }
         }
         return;
@@ -289,7 +296,7 @@ int launch_cfg(const FfmaArgs& a, dim3 grid, cudaStream_t st, bool gelu, bool ea
 }  // namespace
 
 int launch_ffma(const Problem& p, const lin_plan& plan) {
-    FfmaArgs a;
+    FfmaArgs a = {};
     a.M = p.M;
     a.N = p.N;
     a.K = p.K;
@@ -297,6 +304,7 @@ int launch_ffma(const Problem& p, const lin_plan& plan) {
     a.W = static_cast<const float*>(p.W);
     a.bias = p.bias;
     a.Y = static_cast<float*>(p.Y);
+    a.R = static_cast<const float*>(p.residual);
     a.splits = plan.splits;
     a.nkb = (p.K + plan.bk - 1) / plan.bk;
     a.early_inputs = (p.early_start && p.early_x) ? 1 : 0;

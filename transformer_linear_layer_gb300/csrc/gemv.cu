@@ -39,6 +39,7 @@ struct GemvArgs {
     const void* W;     // fp32 or bf16
     const float* bias;
     void* Y;           // fp32 or bf16
+    const void* R;     // residual added after the activation (M x N in Y's type, may be Y), or null
     int early_x;       // X may be read before the dependency wait
 };
 
@@ -161,11 +162,14 @@ gemv_kernel(const GemvArgs a) {
 #pragma unroll
                 for (int m = 0; m < MR; ++m) {
                     if (m < a.M) {
-                        if constexpr (BF16)
-                            static_cast<uint16_t*>(a.Y)[(size_t)m * a.N + n] =
-                                f32_to_bf16_bits(epilogue<GELU, true>(acc[r][m], b));
-                        else
-                            static_cast<float*>(a.Y)[(size_t)m * a.N + n] = epilogue<GELU>(acc[r][m], b);
+                        const size_t i = (size_t)m * a.N + n;
+                        if constexpr (BF16) {
+                            const float res = a.R ? bf16_bits_to_f32(static_cast<const uint16_t*>(a.R)[i]) : 0.f;
+                            static_cast<uint16_t*>(a.Y)[i] = f32_to_bf16_bits(epilogue<GELU, true>(acc[r][m], b) + res);
+                        } else {
+                            const float res = a.R ? static_cast<const float*>(a.R)[i] : 0.f;
+                            static_cast<float*>(a.Y)[i] = epilogue<GELU>(acc[r][m], b) + res;
+                        }
                     }
                 }
             }
@@ -231,7 +235,7 @@ int launch_gemv(const Problem& p, const lin_plan& plan) {
     if (p.M < 1 || p.M > (bf16 ? kGemvMaxRowsBf16 : kGemvMaxRows) ||
         (size_t)plan.bm * p.K * sizeof(float) > (size_t)kGemvMaxSmem || p.K % (bf16 ? 8 : 4) != 0)
         return LIN_ERR_UNSUPPORTED;
-    GemvArgs a;
+    GemvArgs a = {};
     a.M = p.M;
     a.N = p.N;
     a.K = p.K;
@@ -239,6 +243,7 @@ int launch_gemv(const Problem& p, const lin_plan& plan) {
     a.W = p.W;
     a.bias = p.bias;
     a.Y = p.Y;
+    a.R = p.residual;
     a.early_x = (p.early_start && p.early_x) ? 1 : 0;
     const bool gelu = p.epilogue == LIN_EPI_GELU_TANH;
     if (bf16)

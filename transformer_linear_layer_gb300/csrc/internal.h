@@ -11,25 +11,29 @@ namespace lin {
 
 // Everything one launch needs; filled by the C ABI layer after validation.
 struct Problem {
-    int M, N, K;
-    const void* X;
-    const void* W;
-    const float* bias;
-    void* Y;
-    int epilogue;   // lin_epilogue
-    int precision;  // lin_precision
-    cudaStream_t stream;
+    int M = 0, N = 0, K = 0;
+    const void* X = nullptr;
+    const void* W = nullptr;
+    const float* bias = nullptr;
+    void* Y = nullptr;
+    // Residual added after the activation: M x N in Y's type, Y itself (in
+    // place) or not overlapping Y; null for none. Read after the dependency
+    // wait, like Y.
+    const void* residual = nullptr;
+    int epilogue = 0;   // lin_epilogue
+    int precision = 0;  // lin_precision
+    cudaStream_t stream = nullptr;
     // context resources
-    void* workspace;          // split-K partials (float) followed by tile counters (unsigned)
-    size_t workspace_bytes;
-    int* dev_status;          // device status word (LIN_ERR_DEVICE_TIMEOUT when a wait gave up)
-    int sm_count;
+    void* workspace = nullptr;    // split-K partials (float) followed by tile counters (unsigned)
+    size_t workspace_bytes = 0;
+    int* dev_status = nullptr;    // device status word (LIN_ERR_DEVICE_TIMEOUT when a wait gave up)
+    int sm_count = 0;
     // The kernel may start before the previous kernel on the stream finishes
     // (programmatic dependent launch). early_start: W and bias do not overlap
     // that kernel's output, so they may be read before the dependency wait;
     // early_x: neither does X. Y is written only after the wait.
-    bool early_start;
-    bool early_x;
+    bool early_start = false;
+    bool early_x = false;
 };
 
 // Workspace layout for split-K: a fixed block of per-tile arrival counters at
@@ -106,27 +110,31 @@ int launch_gemv(const Problem& p, const lin_plan& plan);
 // Backward (training) GEMMs of the layer: which 1: dX = dZ W (M x K);
 // which 2: dW = dZ^T X (N x K). B is W (which 1) or X (which 2).
 struct BwdProblem {
-    int which;
-    int M, N, K;       // the forward layer's sizes
-    const void* dZ;    // M x N
-    const void* B;     // W (N x K) or X (M x K)
-    void* out;         // dX (M x K) or dW (N x K)
-    cudaStream_t stream;
-    int* dev_status;
-    int sm_count;
-    bool early_start;  // may start before the previous kernel on the stream finishes
-    bool early_x;      // and read dZ and B before it finishes
-    void* workspace;   // context workspace (K split of small outputs)
-    size_t workspace_bytes;
-    bool ksplit_ok;    // no independent call before it on the stream to overlap with
+    int which = 0;
+    int M = 0, N = 0, K = 0;       // the forward layer's sizes
+    const void* dZ = nullptr;      // M x N
+    const void* B = nullptr;       // W (N x K) or X (M x K)
+    void* out = nullptr;           // dX (M x K) or dW (N x K)
+    cudaStream_t stream = nullptr;
+    int* dev_status = nullptr;
+    int sm_count = 0;
+    bool early_start = false;      // may start before the previous kernel on the stream finishes
+    bool early_x = false;          // and read dZ and B before it finishes
+    void* workspace = nullptr;     // context workspace (K split of small outputs)
+    size_t workspace_bytes = 0;
+    bool ksplit_ok = false;        // no independent call before it on the stream to overlap with
+    const void* aux = nullptr;     // which 1: the previous layer's pre-activation (M x K): out *= gelu'(aux); or null
 };
 int launch_tc_backward(const BwdProblem& q);
 int bwd_ffma_splits(int which, int M, int N, int K, int sm_count, size_t ws_bytes);
 int launch_bwd_ffma(int which, int M, int N, int K, const float* dZ, const float* B, float* out, int splits,
-                    void* workspace, cudaStream_t st, bool early);
+                    void* workspace, cudaStream_t st, bool early, const float* Zp = nullptr);
 int launch_gelu_backward(long long count, const void* dY, const void* Z, void* dZ, bool bf16, int sm_count,
                          cudaStream_t st, bool early);
 size_t colsum_workspace_bytes(int M, int N);
 int launch_colsum(int M, int N, const void* dZ, float* db, bool bf16, void* workspace, cudaStream_t st);
+
+int launch_fold_layernorm(int N, int K, const float* W, const float* bias, const float* gamma, const float* beta,
+                          void* W_out, float* bias_out, bool bf16, int sm_count, cudaStream_t st);
 
 }  // namespace lin

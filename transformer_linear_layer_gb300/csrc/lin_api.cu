@@ -34,6 +34,7 @@ struct lin_ctx {
     size_t workspace_bytes;
     int* dev_status;
     bool early_start;  // LIN_OPT_EARLY_START
+    bool adaptive;     // LIN_OPT_ADAPTIVE_PLANS
     lin_plan last_plan;
     std::mutex override_mu;
     std::vector<lin_override> overrides;  // consulted by lin_forward before the table
@@ -43,15 +44,16 @@ namespace lin {
 namespace {
 
 template <bool BF16, bool GELU>
-__global__ void fill_kernel(int M, int N, const float* bias, void* Y) {
+__global__ void fill_kernel(int M, int N, const float* bias, const void* R, void* Y) {
     const size_t total = (size_t)M * N;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
         const int n = (int)(i % N);
         const float v = epilogue<GELU>(0.f, bias ? bias[n] : 0.f);
         if constexpr (BF16)
-            static_cast<uint16_t*>(Y)[i] = f32_to_bf16_bits(v);
+            static_cast<uint16_t*>(Y)[i] =
+                f32_to_bf16_bits(v + (R ? bf16_bits_to_f32(static_cast<const uint16_t*>(R)[i]) : 0.f));
         else
-            static_cast<float*>(Y)[i] = v;
+            static_cast<float*>(Y)[i] = v + (R ? static_cast<const float*>(R)[i] : 0.f);
     }
 }
 
@@ -270,7 +272,11 @@ int plan_default(int sm, int M, int N, int K, int precision, size_t ws, lin_plan
     }
     switch (precision) {
         case LIN_PREC_BF16:
-            if (gemv_fits(M, K, true)) return make_gemv(sm, 0, M, N, K, true, p);
+            // The GEMV only for one row and at most one 128-row tile of W per
+            // SM; measured back to back, the skinny tensor-core kernel wins
+            // everywhere else (4 x 50257 x 768: 12.1 against 41.5 us; one row
+            // of 50257: 11.9 against 14.3 us; one row of 2304: 1.9 against 1.3 us).
+            if (M == 1 && ceil_div(N, 128) <= sm && gemv_fits(M, K, true)) return make_gemv(sm, 0, M, N, K, true, p);
             // More row tiles than SMs: the 96 KB ring (two CTAs per SM) instead
             // of the 192 KB one, so the tiles run in fewer waves (measured on
             // the last token's logits, 50257 rows: 15.7 -> 12.1 us).
@@ -425,7 +431,7 @@ int check_plan_fits(const lin_plan& p, int M, int N, int K, int precision) {
 }
 
 int run(lin_ctx* ctx, const lin_plan& plan_in, int M, int N, int K, const void* X, const void* W, const float* bias,
-        void* Y, int epilogue, int precision, void* stream, bool adaptive) {
+        void* Y, int epilogue, int precision, void* stream, bool adaptive, const void* R = nullptr) {
     lin_plan plan = plan_in;
     if (!ctx || M < 0 || N < 0 || K < 0 || !valid_enums(epilogue, precision)) return LIN_ERR_ARG;
     if (M == 0 || N == 0) return plan.kernel == LIN_KERNEL_NONE ? LIN_OK : LIN_ERR_UNSUPPORTED;
@@ -436,8 +442,9 @@ int run(lin_ctx* ctx, const lin_plan& plan_in, int M, int N, int K, const void* 
     if (overlaps(Y, ybytes, X, (size_t)M * K * ein) || overlaps(Y, ybytes, W, (size_t)N * K * ein) ||
         overlaps(Y, ybytes, bias, bias ? (size_t)N * 4 : 0))
         return LIN_ERR_ARG;
+    if (R && R != Y && overlaps(Y, ybytes, R, ybytes)) return LIN_ERR_ARG;  // in place, or apart
     if (K > 0 && (((uintptr_t)X | (uintptr_t)W) % 16 != 0 || ((size_t)K * ein) % 16 != 0)) return LIN_ERR_ALIGN;
-    if (((uintptr_t)Y % eout) != 0 || ((uintptr_t)bias % 4) != 0) return LIN_ERR_ALIGN;
+    if ((((uintptr_t)Y | (uintptr_t)R) % eout) != 0 || ((uintptr_t)bias % 4) != 0) return LIN_ERR_ALIGN;
     const int fit = check_plan_fits(plan, M, N, K, precision);
     if (fit != LIN_OK) return fit;
     if ((size_t)plan.workspace_bytes > ctx->workspace_bytes) return LIN_ERR_WORKSPACE;
@@ -452,6 +459,7 @@ int run(lin_ctx* ctx, const lin_plan& plan_in, int M, int N, int K, const void* 
     p.W = W;
     p.bias = bias;
     p.Y = Y;
+    p.residual = R;
     p.epilogue = epilogue;
     p.precision = precision;
     p.stream = static_cast<cudaStream_t>(stream);
@@ -467,14 +475,14 @@ int run(lin_ctx* ctx, const lin_plan& plan_in, int M, int N, int K, const void* 
     // An independent call right after another call on this stream overlaps it:
     // the skinny stream then needs no K split to fill the SMs (the concurrent
     // calls do), and skipping the split saves its reduction.
-    if (adaptive && known && p.early_x && plan.kernel == LIN_KERNEL_SKINNY && plan.splits > 1) {
+    if (adaptive && ctx->adaptive && known && p.early_x && plan.kernel == LIN_KERNEL_SKINNY && plan.splits > 1) {
         lin_plan narrow;
         if (make_skinny(ctx->sm_count, plan.variant, 1, M, N, K, ctx->workspace_bytes, &narrow) == LIN_OK)
             plan = narrow;
     }
     // Likewise a tensor-core K split (measured: it helps an isolated call and
     // costs a back-to-back one).
-    if (adaptive && known && p.early_x && plan.kernel == LIN_KERNEL_TC && plan.grid_z > 1) {
+    if (adaptive && ctx->adaptive && known && p.early_x && plan.kernel == LIN_KERNEL_TC && plan.grid_z > 1) {
         lin_plan whole;
         if (make_tc(ctx->sm_count, -1, 0, false, M, N, K, precision == LIN_PREC_BF16 ? 2 : 4, &whole) == LIN_OK)
             plan = whole;
@@ -483,7 +491,7 @@ int run(lin_ctx* ctx, const lin_plan& plan_in, int M, int N, int K, const void* 
     // a split would, so a split must now pay for its reduction with a long K
     // (>= 24 steps of 32 each; measured on the GPT-2 M = 128 layers: proj
     // 8.6 -> 4.1 us, qkv 14.7 -> 11.9 us, fc2 keeps a split of 4).
-    if (adaptive && known && p.early_x && plan.kernel == LIN_KERNEL_FFMA && plan.splits > 1) {
+    if (adaptive && ctx->adaptive && known && p.early_x && plan.kernel == LIN_KERNEL_FFMA && plan.splits > 1) {
         lin_plan fewer;
         if (make_ffma(ctx->sm_count, -1, 0, M, N, K, ctx->workspace_bytes, &fewer, 24) == LIN_OK) plan = fewer;
     }
@@ -506,10 +514,11 @@ int launch_fill(const Problem& p) {
     if (grid > 4 * p.sm_count) grid = 4 * p.sm_count;
     if (grid < 1) grid = 1;
     const bool bf16 = p.precision == LIN_PREC_BF16, gelu = p.epilogue == LIN_EPI_GELU_TANH;
-    if (bf16 && gelu) fill_kernel<true, true><<<grid, 256, 0, p.stream>>>(p.M, p.N, p.bias, p.Y);
-    else if (bf16) fill_kernel<true, false><<<grid, 256, 0, p.stream>>>(p.M, p.N, p.bias, p.Y);
-    else if (gelu) fill_kernel<false, true><<<grid, 256, 0, p.stream>>>(p.M, p.N, p.bias, p.Y);
-    else fill_kernel<false, false><<<grid, 256, 0, p.stream>>>(p.M, p.N, p.bias, p.Y);
+    const void* R = p.residual;
+    if (bf16 && gelu) fill_kernel<true, true><<<grid, 256, 0, p.stream>>>(p.M, p.N, p.bias, R, p.Y);
+    else if (bf16) fill_kernel<true, false><<<grid, 256, 0, p.stream>>>(p.M, p.N, p.bias, R, p.Y);
+    else if (gelu) fill_kernel<false, true><<<grid, 256, 0, p.stream>>>(p.M, p.N, p.bias, R, p.Y);
+    else fill_kernel<false, false><<<grid, 256, 0, p.stream>>>(p.M, p.N, p.bias, R, p.Y);
     return cudaGetLastError() == cudaSuccess ? LIN_OK : LIN_ERR_CUDA;
 }
 
@@ -546,6 +555,7 @@ int lin_create(lin_ctx** out, int device, size_t max_workspace_bytes) {
     if (!c) return LIN_ERR_CUDA;
     c->device = device;
     c->early_start = true;
+    c->adaptive = true;
     std::memset(&c->last_plan, 0, sizeof(c->last_plan));
     c->workspace_bytes = max_workspace_bytes ? max_workspace_bytes : ((size_t)64 << 20);
     if (cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
@@ -588,6 +598,10 @@ int lin_set_option(lin_ctx* ctx, int option, long long value) {
         case LIN_OPT_EARLY_START:
             if (value != 0 && value != 1) return LIN_ERR_ARG;
             ctx->early_start = value != 0;
+            return LIN_OK;
+        case LIN_OPT_ADAPTIVE_PLANS:
+            if (value != 0 && value != 1) return LIN_ERR_ARG;
+            ctx->adaptive = value != 0;
             return LIN_OK;
         default: return LIN_ERR_ARG;
     }
@@ -633,19 +647,36 @@ int lin_plan_make(int sm_count, int kernel, int variant, int splits, int M, int 
     }
 }
 
-int lin_forward(lin_ctx* ctx, int M, int N, int K, const void* X, const void* W, const float* bias, void* Y,
-                int epilogue, int precision, void* stream) {
+namespace {
+
+// lin_forward and lin_forward_residual: an installed plan for the call
+// signature, else the built-in table (adapted to the call's neighbour).
+int forward_dispatch(lin_ctx* ctx, int M, int N, int K, const void* X, const void* W, const float* bias,
+                     const void* R, void* Y, int epilogue, int precision, void* stream) {
     if (!ctx || M < 0 || N < 0 || K < 0 || !lin::valid_enums(epilogue, precision)) return LIN_ERR_ARG;
     {
         std::lock_guard<std::mutex> lk(ctx->override_mu);
         for (const lin_override& o : ctx->overrides)
             if (o.M == M && o.N == N && o.K == K && o.precision == precision && o.epilogue == epilogue)
-                return lin::run(ctx, o.plan, M, N, K, X, W, bias, Y, epilogue, precision, stream, false);
+                return lin::run(ctx, o.plan, M, N, K, X, W, bias, Y, epilogue, precision, stream, false, R);
     }
     lin_plan plan;
     const int rc = lin::plan_default(ctx->sm_count, M, N, K, precision, ctx->workspace_bytes, &plan);
     if (rc != LIN_OK) return rc;
-    return lin::run(ctx, plan, M, N, K, X, W, bias, Y, epilogue, precision, stream, true);
+    return lin::run(ctx, plan, M, N, K, X, W, bias, Y, epilogue, precision, stream, true, R);
+}
+
+}  // namespace
+
+int lin_forward(lin_ctx* ctx, int M, int N, int K, const void* X, const void* W, const float* bias, void* Y,
+                int epilogue, int precision, void* stream) {
+    return forward_dispatch(ctx, M, N, K, X, W, bias, nullptr, Y, epilogue, precision, stream);
+}
+
+int lin_forward_residual(lin_ctx* ctx, int M, int N, int K, const void* X, const void* W, const float* bias,
+                         const void* R, void* Y, int epilogue, int precision, void* stream) {
+    if (!R && M > 0 && N > 0) return LIN_ERR_ARG;
+    return forward_dispatch(ctx, M, N, K, X, W, bias, R, Y, epilogue, precision, stream);
 }
 
 int lin_set_plan_override(lin_ctx* ctx, int M, int N, int K, int precision, int epilogue, const lin_plan* plan) {
@@ -709,7 +740,8 @@ int backward_setup(lin_ctx* ctx, int which, int M, int N, int K, const void* dZ,
     q->workspace_bytes = ctx->workspace_bytes;
     // Right after an independent call the two overlap (early start) and fill
     // the SMs together: a K split would only add its round trip.
-    q->ksplit_ok = !(known && q->early_x);
+    q->ksplit_ok = !(ctx->adaptive && known && q->early_x);
+    q->aux = nullptr;
     return LIN_OK;
 }
 
@@ -724,7 +756,8 @@ int backward_run(const lin::BwdProblem& q, int precision, lin_ctx* ctx) {
     if (precision == LIN_PREC_BF16) return launch_tc_backward(q);
     const int S = bwd_ffma_splits(q.which, q.M, q.N, q.K, ctx->sm_count, ctx->workspace_bytes);
     return launch_bwd_ffma(q.which, q.M, q.N, q.K, static_cast<const float*>(q.dZ), static_cast<const float*>(q.B),
-                           static_cast<float*>(q.out), S, ctx->workspace, q.stream, q.early_start);
+                           static_cast<float*>(q.out), S, ctx->workspace, q.stream, q.early_start,
+                           static_cast<const float*>(q.aux));
 }
 
 }  // namespace
@@ -735,6 +768,24 @@ int lin_backward_data(lin_ctx* ctx, int M, int N, int K, const void* dZ, const v
     q.which = 0;
     const int rc = backward_setup(ctx, 1, M, N, K, dZ, W, dX, precision, stream, &q);
     if (rc != LIN_OK || q.which == 0) return rc;
+    lin::DeviceGuard guard(ctx->device);
+    if (!guard.ok) return LIN_ERR_CUDA;
+    return backward_run(q, precision, ctx);
+}
+
+int lin_backward_data_gelu(lin_ctx* ctx, int M, int N, int K, const void* dZ, const void* W, const void* Zp,
+                           void* dX, int precision, void* stream) {
+    lin::BwdProblem q;
+    q.which = 0;
+    if (!ctx || !lin::valid_enums(0, precision)) return LIN_ERR_ARG;
+    const size_t esz = precision == LIN_PREC_BF16 ? 2 : 4;
+    const size_t bytes = (size_t)(M > 0 ? M : 0) * (K > 0 ? K : 0) * esz;
+    if (bytes > 0 && !Zp) return LIN_ERR_ARG;
+    if (Zp != dX && lin::overlaps(Zp, bytes, dX, bytes)) return LIN_ERR_ARG;  // in place, or apart
+    if ((uintptr_t)Zp % esz != 0) return LIN_ERR_ALIGN;
+    const int rc = backward_setup(ctx, 1, M, N, K, dZ, W, dX, precision, stream, &q);
+    if (rc != LIN_OK || q.which == 0) return rc;
+    q.aux = Zp;
     lin::DeviceGuard guard(ctx->device);
     if (!guard.ok) return LIN_ERR_CUDA;
     return backward_run(q, precision, ctx);
@@ -786,6 +837,37 @@ int lin_gelu_backward(lin_ctx* ctx, long long count, const void* dY, const void*
     bool w_ok = false, x_ok = false, known = false;
     early_reads_ok(st, Range{Z, bytes}, Range{nullptr, 0}, Range{dY, bytes}, Range{dZ, bytes}, &w_ok, &x_ok, &known);
     return launch_gelu_backward(count, dY, Z, dZ, precision == LIN_PREC_BF16, ctx->sm_count, st, ctx->early_start);
+}
+
+int lin_fold_layernorm(lin_ctx* ctx, int N, int K, const float* W, const float* bias, const float* gamma,
+                       const float* beta, void* W_out, float* bias_out, int precision, void* stream) {
+    using namespace lin;
+    if (!ctx || N < 0 || K < 0 || !valid_enums(0, precision)) return LIN_ERR_ARG;
+    if (N == 0) return LIN_OK;
+    if (!W_out || !bias_out || (K > 0 && (!W || !gamma))) return LIN_ERR_ARG;
+    const size_t eout = precision == LIN_PREC_BF16 ? 2 : 4;
+    const size_t wbytes = (size_t)N * K * 4, wobytes = (size_t)N * K * eout;
+    // In place: W_out = W (fp32 storage) and bias_out = bias are allowed; no other overlap.
+    if (!(W_out == W && eout == 4) && overlaps(W_out, wobytes, W, wbytes)) return LIN_ERR_ARG;
+    if (overlaps(W_out, wobytes, gamma, (size_t)K * 4) || overlaps(W_out, wobytes, beta, beta ? (size_t)K * 4 : 0) ||
+        overlaps(W_out, wobytes, bias, bias ? (size_t)N * 4 : 0) || overlaps(W_out, wobytes, bias_out, (size_t)N * 4))
+        return LIN_ERR_ARG;
+    if (bias_out != bias && overlaps(bias_out, (size_t)N * 4, bias, bias ? (size_t)N * 4 : 0)) return LIN_ERR_ARG;
+    if (overlaps(bias_out, (size_t)N * 4, W, wbytes) || overlaps(bias_out, (size_t)N * 4, gamma, (size_t)K * 4) ||
+        overlaps(bias_out, (size_t)N * 4, beta, beta ? (size_t)K * 4 : 0))
+        return LIN_ERR_ARG;
+    if ((((uintptr_t)W | (uintptr_t)bias | (uintptr_t)gamma | (uintptr_t)beta | (uintptr_t)bias_out) % 4) != 0 ||
+        ((uintptr_t)W_out % eout) != 0)
+        return LIN_ERR_ALIGN;
+    DeviceGuard guard(ctx->device);
+    if (!guard.ok) return LIN_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int rc = launch_fold_layernorm(N, K, W, bias, gamma, beta, W_out, bias_out, precision == LIN_PREC_BF16,
+                                         ctx->sm_count, st);
+    if (rc == LIN_OK) {
+        note_output(st, Range{W_out, wobytes});
+    }
+    return rc;
 }
 
 int lin_forward_plan(lin_ctx* ctx, const lin_plan* plan, int M, int N, int K, const void* X, const void* W,

@@ -45,6 +45,7 @@ struct SkinnyArgs {
     int M, N, K;
     const float* bias;
     uint16_t* Y;
+    const uint16_t* R;  // residual added after the activation (M x N bf16, may be Y itself), or null
     int* status;
     int kblocks;  // ceil(K / (64 * KBOX)): stages of K per 128-row block
     int early_x;  // X may be read before the dependency wait (it is not the previous call's output)
@@ -278,7 +279,11 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
                 const float b = a.bias ? __ldg(a.bias + n) : 0.f;
 #pragma unroll
                 for (int m = 0; m < kSkMP; ++m)
-                    if (m < M) a.Y[(size_t)m * N + n] = f32_to_bf16_bits(epilogue<GELU, true>(v.x[m], b));
+                    if (m < M) {
+                        const size_t i = (size_t)m * N + n;
+                        const float r = a.R ? bf16_bits_to_f32(a.R[i]) : 0.f;
+                        a.Y[i] = f32_to_bf16_bits(epilogue<GELU, true>(v.x[m], b) + r);
+                    }
             }
         } else {
             // Push this row's partial sums into the inbox of the CTA that finishes it,
@@ -303,7 +308,9 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
                 if (ok && m < M && n < N) {
                     const float acc = tree_of_ranks<CL>(inbox + m * COLS + c, kSkMP * COLS, 0);
                     const float b = a.bias ? __ldg(a.bias + n) : 0.f;
-                    a.Y[(size_t)m * N + n] = f32_to_bf16_bits(epilogue<GELU, true>(acc, b));
+                    const size_t i = (size_t)m * N + n;
+                    const float r = a.R ? bf16_bits_to_f32(a.R[i]) : 0.f;
+                    a.Y[i] = f32_to_bf16_bits(epilogue<GELU, true>(acc, b) + r);
                 }
             }
         }
@@ -380,12 +387,13 @@ int launch_skinny(const Problem& p, const lin_plan& plan) {
     CUtensorMap tw, tx;
     if (!make_kmajor_map(&tw, p.W, true, p.N, p.K, kSkRows)) return LIN_ERR_CUDA;
     if (!make_kmajor_map(&tx, p.X, true, p.M, p.K, kSkMP)) return LIN_ERR_CUDA;
-    SkinnyArgs a;
+    SkinnyArgs a = {};
     a.M = p.M;
     a.N = p.N;
     a.K = p.K;
     a.bias = p.bias;
     a.Y = static_cast<uint16_t*>(p.Y);
+    a.R = static_cast<const uint16_t*>(p.residual);
     a.status = p.dev_status;
     a.kblocks = (p.K + 64 * kSkinnyCfg[plan.variant].kbox - 1) / (64 * kSkinnyCfg[plan.variant].kbox);
     a.early_x = p.early_x ? 1 : 0;

@@ -52,6 +52,9 @@ struct TcArgs {
     unsigned* flags;     // stream-K: 8 hand-over flags per CTA boundary; K split: 8 counters per tile
                          // (zero between launches)
     int ksplits;         // K split (whole tiles, single CTA): each tile's K stages cut in ksplits ranges
+    const void* aux;     // M x N in Y's type (may be Y itself), read in the epilogue, or null:
+    int aux_mode;        //   1 adds it after the activation (residual), 2 multiplies by the GELU slope at it
+    int aux_vec;         // aux rows are 16-byte aligned (vector loads)
 };
 
 // Epilogue staging: each epilogue warp owns a 32 x 32 output tile in shared
@@ -370,6 +373,52 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 v[j4 + 3] = epilogue<GELU, BF16>(__uint_as_float(r[j4 + 3]), b4.w);
             }
             const int mrow0 = m0 + q * 32;
+            // The auxiliary tensor at this lane's row: the residual stream
+            // (added), or the previous layer's pre-activation (GELU slope).
+            if (a.aux_mode && mrow0 + lane < a.M) {
+                const size_t rowoff = (size_t)(mrow0 + lane) * N + nb;
+                float t[32];
+                if (full && a.aux_vec) {
+                    if constexpr (BF16) {
+                        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.aux) + rowoff);
+#pragma unroll
+                        for (int p16 = 0; p16 < 4; ++p16) {
+                            const uint4 w = src[p16];
+                            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                t[8 * p16 + 2 * h] = __uint_as_float(ws[h] << 16);
+                                t[8 * p16 + 2 * h + 1] = __uint_as_float(ws[h] & 0xffff0000u);
+                            }
+                        }
+                    } else {
+                        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(a.aux) + rowoff);
+#pragma unroll
+                        for (int p4 = 0; p4 < 8; ++p4) {
+                            const float4 w = src[p4];
+                            t[4 * p4] = w.x;
+                            t[4 * p4 + 1] = w.y;
+                            t[4 * p4 + 2] = w.z;
+                            t[4 * p4 + 3] = w.w;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        t[j] = 0.f;
+                        if (nb + j < N)
+                            t[j] = BF16 ? bf16_bits_to_f32(static_cast<const uint16_t*>(a.aux)[rowoff + j])
+                                        : static_cast<const float*>(a.aux)[rowoff + j];
+                    }
+                }
+                if (a.aux_mode == 1) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] += t[j];
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] *= gelu_tanh_slope<BF16>(t[j]);
+                }
+            }
             if constexpr (BF16) {
                 if (a.y_tma) {
                     // Into this warp's 32 x 32 box (64-byte swizzle: conflict-free
@@ -780,6 +829,9 @@ int launch_tc_backward(const BwdProblem& q) {
     a.early_inputs = q.early_x ? 1 : 0;
     a.partials = nullptr;
     a.flags = nullptr;
+    a.aux = q.which == 1 ? q.aux : nullptr;
+    a.aux_mode = a.aux ? 2 : 0;
+    a.aux_vec = (reinterpret_cast<uintptr_t>(a.aux) % 16) == 0 && (No * 2) % 16 == 0;
     // Small outputs with a long reduction (the weight gradients): split K.
     const long long ntile = (long long)((Mo + 127) / 128) * ((No + 255) / 256);
     a.ksplits = q.ksplit_ok ? tc_ksplits(ntile, (R + 63) / 64, q.sm_count, q.workspace_bytes, kTcCfg[0].bn) : 1;
@@ -807,7 +859,7 @@ int launch_tc(const Problem& p, const lin_plan& plan) {
     CUtensorMap ta, tb;
     if (!make_kmajor_map(&ta, p.X, bf16, p.M, p.K, 128)) return LIN_ERR_CUDA;
     if (!make_kmajor_map(&tb, p.W, bf16, p.N, p.K, pair ? plan.bn / 2 : plan.bn)) return LIN_ERR_CUDA;
-    TcArgs a;
+    TcArgs a = {};
     a.M = p.M;
     a.N = p.N;
     a.K = p.K;
@@ -817,6 +869,9 @@ int launch_tc(const Problem& p, const lin_plan& plan) {
     a.y_aligned16 = (reinterpret_cast<uintptr_t>(p.Y) % 16) == 0;
     a.bias_aligned16 = (reinterpret_cast<uintptr_t>(p.bias) % 16) == 0;
     a.early_inputs = (p.early_start && p.early_x) ? 1 : 0;
+    a.aux = p.residual;
+    a.aux_mode = p.residual ? 1 : 0;
+    a.aux_vec = (reinterpret_cast<uintptr_t>(p.residual) % 16) == 0 && ((size_t)p.N * (bf16 ? 2 : 4)) % 16 == 0;
     const bool sk = plan.splits == 2;
     // Stream-K CTAs wait for their successor's hand-over, so all of them must
     // be resident at once: at most one per SM.
