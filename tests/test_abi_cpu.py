@@ -51,6 +51,17 @@ def test_null_context_is_an_argument_error():
     assert lib.lin_check_device(None, None) == tll.ERR_ARG
     assert lib.lin_destroy(None) == tll.OK
     assert lib.lin_create(None, 0, 0) == tll.ERR_ARG
+    # every other entry point that takes a context refuses a null one before touching a device
+    assert lib.lin_forward_plan(None, None, 16, 16, 16, None, None, None, None, 0, 2, None) == tll.ERR_ARG
+    assert lib.lin_forward_residual(None, 16, 16, 16, None, None, None, None, None, 0, 2, None) == tll.ERR_ARG
+    assert lib.lin_backward_data(None, 16, 16, 16, None, None, None, 2, None) == tll.ERR_ARG
+    assert lib.lin_backward_weight(None, 16, 16, 16, None, None, None, None, 2, None) == tll.ERR_ARG
+    assert lib.lin_backward_data_gelu(None, 16, 16, 16, None, None, None, None, 2, None) == tll.ERR_ARG
+    assert lib.lin_gelu_backward(None, 16, None, None, None, 2, None) == tll.ERR_ARG
+    assert lib.lin_fold_layernorm(None, 16, 16, None, None, None, None, None, None, 0, None) == tll.ERR_ARG
+    assert lib.lin_set_plan_override(None, 16, 16, 16, 2, 0, None) == tll.ERR_ARG
+    assert lib.lin_clear_plan_overrides(None) == tll.ERR_ARG
+    assert lib.lin_set_option(None, 1, 1) == tll.ERR_ARG
 
 
 def test_create_without_device_fails_cleanly():
@@ -258,3 +269,21 @@ def test_skinny_ring_for_many_row_tiles():
     p = tll.plan_query(SM, 8, 50257, 768, "bf16")
     assert kname(p) == "skinny" and p.variant == 1 and p.splits == 1
     assert tll.plan_query(SM, 16, 4096, 4096, "bf16").variant == 0
+
+
+def test_autotune_save_format(tmp_path):
+    """The tuner's table on disk: one entry per tuned signature with a winner,
+    every plan field kept, readable back into a Plan (host only)."""
+    import json
+
+    from transformer_linear_layer_gb300 import autotune
+
+    p = tll.plan_make(SM, tll.KERNEL_FFMA, 1, 3, 128, 768, 768, "fp32")
+    reports = [{"shape": [128, 768, 768], "precision": "fp32", "epilogue": "none", "winner": p.as_dict()},
+               {"shape": [16, 4096, 4096], "precision": "bf16", "epilogue": "none", "winner": None}]
+    path = tmp_path / "plans.json"
+    autotune.save(reports, str(path))
+    table = json.loads(path.read_text())
+    assert len(table) == 1 and table[0]["shape"] == [128, 768, 768]
+    back = autotune._plan_from_dict(table[0]["plan"])
+    assert autotune._plan_key(back) == autotune._plan_key(p)

@@ -654,13 +654,18 @@ namespace {
 int forward_dispatch(lin_ctx* ctx, int M, int N, int K, const void* X, const void* W, const float* bias,
                      const void* R, void* Y, int epilogue, int precision, void* stream) {
     if (!ctx || M < 0 || N < 0 || K < 0 || !lin::valid_enums(epilogue, precision)) return LIN_ERR_ARG;
-    {
-        std::lock_guard<std::mutex> lk(ctx->override_mu);
-        for (const lin_override& o : ctx->overrides)
-            if (o.M == M && o.N == N && o.K == K && o.precision == precision && o.epilogue == epilogue)
-                return lin::run(ctx, o.plan, M, N, K, X, W, bias, Y, epilogue, precision, stream, false, R);
-    }
     lin_plan plan;
+    bool installed = false;
+    {
+        std::lock_guard<std::mutex> lk(ctx->override_mu);  // copy the entry; launch outside the lock
+        for (const lin_override& o : ctx->overrides)
+            if (o.M == M && o.N == N && o.K == K && o.precision == precision && o.epilogue == epilogue) {
+                plan = o.plan;
+                installed = true;
+                break;
+            }
+    }
+    if (installed) return lin::run(ctx, plan, M, N, K, X, W, bias, Y, epilogue, precision, stream, false, R);
     const int rc = lin::plan_default(ctx->sm_count, M, N, K, precision, ctx->workspace_bytes, &plan);
     if (rc != LIN_OK) return rc;
     return lin::run(ctx, plan, M, N, K, X, W, bias, Y, epilogue, precision, stream, true, R);
