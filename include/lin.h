@@ -79,7 +79,7 @@ typedef enum {
     LIN_KERNEL_SKINNY = 2, /* M <= 16, BF16: W stream on the tensor cores, split-K in a cluster (no workspace) */
     LIN_KERNEL_FFMA = 3,   /* FP32: register-tiled FFMA, optional split-K */
     LIN_KERNEL_TC = 4,     /* TF32 / BF16: TMA + tcgen05 + TMEM, fused epilogue */
-    LIN_KERNEL_GEMV = 5    /* FP32 / TF32 M <= 8, BF16 M <= 4: one pass over W in fp32 FMAs (X in shared memory) */
+    LIN_KERNEL_GEMV = 5    /* FP32 / TF32 M <= 8, BF16 M <= 4 (the table: BF16 one row only): one pass over W in fp32 FMAs */
 } lin_kernel;
 
 /* One launch configuration, chosen by the dispatch table or given explicitly.
