@@ -253,12 +253,6 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
                  : "memory");
 }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane, waited for.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    tmem_ld32_async(taddr, r);
-    tmem_wait_ld(r);
-}
-
 // 16 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
@@ -342,12 +336,6 @@ __device__ __forceinline__ uint32_t dsmem_map(uint32_t saddr, uint32_t rank) {
     uint32_t out;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(saddr), "r"(rank));
     return out;
-}
-
-__device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
 }
 
 // ---- flags in global memory (hand-over between CTAs of one grid) ----
