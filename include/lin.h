@@ -185,6 +185,15 @@ LIN_API int lin_forward_plan(lin_ctx* ctx, const lin_plan* plan, int M, int N, i
 LIN_API int lin_plan_query(int sm_count, int M, int N, int K, int precision, int epilogue,
                    size_t workspace_bytes, lin_plan* out);
 
+/* Check a plan against a shape on the host (no GPU needed): LIN_OK when
+ * lin_forward_plan would accept it in a context with `workspace_bytes` of
+ * workspace, else the status it would return (LIN_ERR_UNSUPPORTED: the kernel
+ * cannot run this shape / precision with this grid; LIN_ERR_WORKSPACE; or
+ * LIN_ERR_ARG for a NULL plan, negative sizes or an unknown precision).
+ * Limits that depend on the device (stream-K CTAs at most one per SM) are
+ * checked when the call is launched. */
+LIN_API int lin_plan_check(const lin_plan* plan, int M, int N, int K, int precision, size_t workspace_bytes);
+
 /* Fill *out with the default plan of a kernel family for a shape (host only),
  * for sweeps: kernel = lin_kernel, variant = tile configuration, splits = 0
  * lets the table choose the split. For LIN_KERNEL_TC, splits counts CTAs

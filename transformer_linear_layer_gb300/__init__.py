@@ -95,6 +95,7 @@ def library() -> ctypes.CDLL:
                 "lin_backward_weight": ([P, I, I, I, P, P, P, P, I, P], I),
                 "lin_gelu_backward": ([P, ctypes.c_longlong, P, P, P, I, P], I),
                 "lin_forward_residual": ([P, I, I, I, P, P, P, P, P, I, I, P], I),
+                "lin_plan_check": ([PP, I, I, I, I, ctypes.c_size_t], I),
                 "lin_backward_data_gelu": ([P, I, I, I, P, P, P, P, I, P], I),
                 "lin_fold_layernorm": ([P, I, I, P, P, P, P, P, P, I, P], I),
                 "lin_set_plan_override": ([P, I, I, I, I, I, PP], I),
@@ -137,6 +138,12 @@ def plan_make(sm_count: int, kernel: int, variant: int, splits: int, M: int, N: 
     if rc != OK:
         raise LinError(rc, "lin_plan_make")
     return p
+
+
+def plan_check(plan: Plan, M: int, N: int, K: int, precision="bf16", workspace_bytes: int = 64 << 20) -> int:
+    """Status lin_forward_plan would return for this plan and shape (host only;
+    0 = accepted)."""
+    return library().lin_plan_check(ctypes.byref(plan), M, N, K, _prec(precision), workspace_bytes)
 
 
 class Context:

@@ -621,6 +621,14 @@ int lin_plan_query(int sm_count, int M, int N, int K, int precision, int epilogu
     return lin::plan_default(sm_count, M, N, K, precision, workspace_bytes, out);
 }
 
+int lin_plan_check(const lin_plan* plan, int M, int N, int K, int precision, size_t workspace_bytes) {
+    if (!plan || M < 0 || N < 0 || K < 0 || !lin::valid_enums(0, precision)) return LIN_ERR_ARG;
+    if (M == 0 || N == 0) return plan->kernel == LIN_KERNEL_NONE ? LIN_OK : LIN_ERR_UNSUPPORTED;
+    const int fit = lin::check_plan_fits(*plan, M, N, K, precision);
+    if (fit != LIN_OK) return fit;
+    return (size_t)plan->workspace_bytes > workspace_bytes ? LIN_ERR_WORKSPACE : LIN_OK;
+}
+
 int lin_plan_make(int sm_count, int kernel, int variant, int splits, int M, int N, int K, int precision,
                   lin_plan* out) {
     if (!out || sm_count < 1 || M < 0 || N < 0 || K < 0 || !lin::valid_enums(0, precision)) return LIN_ERR_ARG;
