@@ -15,7 +15,8 @@ library's own kernels:
   learns only the prior's error (the residual), refit after every shape;
   its coefficients say which penalty the prior over- or underprices;
 - which experiment runs next: candidates the corrected model puts far above
-  the incumbent are pruned before any timing, the rest are timed once;
+  the incumbent are pruned before any timing, unless their family is one
+  the fit has barely seen (where it is uncertain); the rest are timed once;
 - how a result is scored: as efficiency, the physical floor (the layer's
   own roofline) over the time, with a stopping rule (an incumbent already
   at ``stop`` of its floor is not searched), and the choice is paired:
@@ -182,10 +183,18 @@ class ResidualModel:
     def __init__(self, ridge: float = 1e-2):
         self.rows, self.ys, self.ridge = [], [], ridge
         self.beta = [0.0] * len(_FEATURE_NAMES)
+        self.per_family = {}
 
     def add(self, f: dict, measured_s: float, prior_s: float):
         self.rows.append(_phi(f))
         self.ys.append(math.log(measured_s / prior_s))
+        self.per_family[f["family"]] = self.per_family.get(f["family"], 0) + 1
+
+    def knows(self, f: dict, min_samples: int = 3) -> bool:
+        """The fit has seen this plan's family often enough to prune with it;
+        a family it has not seen is exactly where it is uncertain, so such
+        candidates are timed, not pruned."""
+        return self.trusted and self.per_family.get(f["family"], 0) >= min_samples
 
     @property
     def trusted(self) -> bool:
@@ -275,19 +284,23 @@ class _Bench:
 
 def autotune(ctx: Context, shapes, rounds: int = 5, reps: int = 20, prune: float = 2.0, slack: float = 0.15,
              pair_top: int = 4, margin: float = 0.03, stop: float = 0.97, install: bool = True,
-             model: ResidualModel | None = None):
+             model: ResidualModel | None = None, bench_factory=None):
     """Tune each (M, N, K, precision, epilogue) in ``shapes``; returns one
     report dict per shape (the incumbent, the efficiencies, the screened and
     paired candidates and the winner, None when the built-in plan stays) and,
     with ``install``, installs the winners (an old override for a tuned shape
     is removed first). ``model`` (refit after each shape) carries the learnt
-    residual from shape to shape and across calls."""
+    residual from shape to shape and across calls. ``bench_factory(ctx, M, N,
+    K, precision, epilogue, reps)`` makes the timing backend (default: CUDA
+    graphs of back-to-back calls on the context's device): an object with
+    ``graph(plan or None)``, ``time(graph) -> seconds per call`` and ``stream``."""
     model = model if model is not None else ResidualModel()
+    bench_factory = bench_factory or _Bench
     reports = []
     for (M, N, K, precision, epilogue) in shapes:
         ctx.set_override(M, N, K, precision, epilogue, None)  # time the built-in table, not an old winner
         incumbent = ctx.plan(M, N, K, precision, epilogue)
-        bench = _Bench(ctx, M, N, K, precision, epilogue, reps=reps)
+        bench = bench_factory(ctx, M, N, K, precision, epilogue, reps=reps)
         g_inc = bench.graph(None)
         t_inc = bench.time(g_inc)
         floor = roofline_floor_s(M, N, K, precision)
@@ -304,8 +317,8 @@ def autotune(ctx: Context, shapes, rounds: int = 5, reps: int = 20, prune: float
         for p in cands:
             f = features(ctx.sm_count, M, N, K, precision, p)
             prior = predict_prior_s(M, N, K, precision, f)
-            # analytic pruning before the stopwatch, once the residual has data behind it
-            if model.trusted and model.predict_s(f, prior) > prune * t_inc:
+            # analytic pruning before the stopwatch, where the residual has data behind it
+            if model.knows(f) and model.predict_s(f, prior) > prune * t_inc:
                 rep["pruned"].append(_label(p))
                 continue
             try:
