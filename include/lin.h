@@ -128,15 +128,15 @@ LIN_API int lin_destroy(lin_ctx* ctx);
  * (LIN_ERR_ALIGN otherwise); bias 4-byte aligned; Y aligned to its element.
  * One context must not run two calls at the same time (they share the
  * workspace): use one context per stream.
- * Back-to-back calls: with LIN_OPT_EARLY_START on (the default), a call whose
- * inputs (X, W, bias) overlap none of the previous call's output on the same
- * stream is launched as a programmatic dependent of that call, reads its
- * inputs before the previous kernel has finished and writes Y only after it.
- * For such a call the built-in plan may also drop its K split (the skinny
- * kernel's cluster split, the tensor-core K split, an FFMA split over a short
- * K), so that consecutive independent calls fill the SMs together; see
- * LIN_OPT_ADAPTIVE_PLANS. lin_plan_query returns the plan of an isolated
- * call. */
+ * Back-to-back calls: with LIN_OPT_EARLY_START at 2 (off by default; see
+ * that option for when it is safe), a call whose inputs (X, W, bias) overlap
+ * none of the previous call's output on the same stream is launched as a
+ * programmatic dependent of that call, reads its inputs before the previous
+ * kernel has finished and writes Y only after it. For such a call the built-in
+ * plan may also drop its K split (the skinny kernel's cluster split, the
+ * tensor-core K split, an FFMA split over a short K), so that consecutive
+ * independent calls fill the SMs together; see LIN_OPT_ADAPTIVE_PLANS.
+ * lin_plan_query returns the plan of an isolated call. */
 LIN_API int lin_forward(lin_ctx* ctx, int M, int N, int K, const void* X, const void* W,
                 const float* bias, void* Y, int epilogue, int precision, void* stream);
 
@@ -276,14 +276,24 @@ LIN_API int lin_clear_plan_overrides(lin_ctx* ctx);
 LIN_API int lin_check_device(lin_ctx* ctx, void* stream);
 
 /* Context options (lin_set_option).
- * LIN_OPT_EARLY_START (default 1): kernels that stream W may be launched as
- *   programmatic dependents of the previous kernel on the stream and start
- *   copying W before that kernel finishes; X and bias are read, and Y written,
- *   only after it has finished. The library drops the early start by itself
- *   when W overlaps the previous call's output on that stream. 0 = every call
- *   waits for the previous kernel before it starts.
+ * LIN_OPT_EARLY_START (default 0): whether a call may start before the
+ *   previous kernel on its stream has finished (programmatic dependent launch).
+ *   0: no; every call waits for all earlier work on the stream, like any
+ *      stream-ordered library.
+ *   1: the call is launched as a programmatic dependent of the previous kernel;
+ *      its prologue overlaps that kernel's tail, and W and bias may be read
+ *      before that kernel has finished. X is read, and Y written, only after it.
+ *   2: as 1, and X may be read early too.
+ *   The library only sees its own calls: it drops the early reads of W / bias
+ *   (and X) by itself when they overlap the previous library call's output on
+ *   that stream, but it cannot see other work. Use 1 only when no other work on
+ *   the stream writes the next call's W or bias between two library calls (an
+ *   optimizer step does), and 2 only when nothing but library calls write its X
+ *   either (a framework kernel that produces X, such as a layernorm, does).
+ *   With 2, a call that overlaps an independent predecessor may also narrow its
+ *   plan (LIN_OPT_ADAPTIVE_PLANS).
  * LIN_OPT_ADAPTIVE_PLANS (default 1): a call that overlaps an independent
- *   predecessor on its stream (both launched with the early start) may drop
+ *   predecessor on its stream (early start level 2) may drop
  *   the K split of its built-in plan: the neighbouring call then fills the SMs
  *   the split would. A split changes the order of the fp32 sums, so with this
  *   option on, the last bits of a result can depend on the call before it on

@@ -124,10 +124,10 @@ def test_fixed_plans_give_history_independent_bits(ctx):
     def pair():
         """(isolated call's Y, plan), (back-to-back call's Y, plan)."""
         with torch.cuda.stream(s):
-            ctx.set_option(tll.OPT_EARLY_START, 0)
+            ctx.set_option(tll.OPT_EARLY_START, tll.EARLY_NONE)
             y1 = tll.forward(x, w, bias, precision="fp32", ctx=ctx)
             p1 = ctx.last_plan()
-            ctx.set_option(tll.OPT_EARLY_START, 1)
+            ctx.set_option(tll.OPT_EARLY_START, tll.EARLY_ALL)
             tll.forward(x, w2, bias, precision="fp32", ctx=ctx, out=torch.empty_like(y1))
             y2 = tll.forward(x, w, bias, precision="fp32", ctx=ctx)
             p2 = ctx.last_plan()
@@ -136,7 +136,7 @@ def test_fixed_plans_give_history_independent_bits(ctx):
         return (y1, p1), (y2, p2)
 
     (y1, p1), (y2, p2) = pair()
-    assert p1.splits > 1 and p2.splits < p1.splits  # the default drops the split back to back
+    assert p1.splits > 1 and p2.splits < p1.splits  # adaptive plans drop the split back to back
     for y in (y1, y2):
         assert oracle.rel_err(y.double().cpu().numpy(), ref) <= oracle.TOL[FP32]
     ctx.set_option(tll.OPT_ADAPTIVE_PLANS, 0)
@@ -144,4 +144,5 @@ def test_fixed_plans_give_history_independent_bits(ctx):
         (y1, p1), (y2, p2) = pair()
     finally:
         ctx.set_option(tll.OPT_ADAPTIVE_PLANS, 1)
+        ctx.set_option(tll.OPT_EARLY_START, tll.EARLY_NONE)
     assert _same(p1, p2) and torch.equal(y1, y2)

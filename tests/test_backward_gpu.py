@@ -14,6 +14,16 @@ pytestmark = pytest.mark.gpu
 FP32, TF32, BF16 = si.PREC_FP32, si.PREC_TF32, si.PREC_BF16
 
 
+@pytest.fixture(scope="module", autouse=True)
+def _early_start_all():
+    """Back-to-back library calls only: the programmatic early start is safe
+    here and is what the back-to-back tests exercise (the default is off)."""
+    c = tll.default_context(0)
+    c.set_option(tll.OPT_EARLY_START, tll.EARLY_ALL)
+    yield
+    c.set_option(tll.OPT_EARLY_START, tll.EARLY_NONE)
+
+
 def _dt(precision):
     return torch.bfloat16 if precision == BF16 else torch.float32
 

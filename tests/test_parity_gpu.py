@@ -23,6 +23,17 @@ def ctx():
     return tll.default_context(0)
 
 
+@pytest.fixture(scope="module", autouse=True)
+def _early_start_all():
+    """These tests run back-to-back library calls only, so the programmatic
+    early start (inputs read before the previous kernel finishes) is safe and
+    is what they exercise; the library's default is off."""
+    c = tll.default_context(0)
+    c.set_option(tll.OPT_EARLY_START, tll.EARLY_ALL)
+    yield
+    c.set_option(tll.OPT_EARLY_START, tll.EARLY_NONE)
+
+
 def all_plans(ctx, M, N, K, precision):
     """Every kernel family / variant that can run this shape, plus split choices."""
     plans = []

@@ -31,6 +31,10 @@ KERNEL_NONE, KERNEL_FILL, KERNEL_SKINNY, KERNEL_FFMA, KERNEL_TC, KERNEL_GEMV = 0
 KERNEL_NAMES = {0: "none", 1: "fill", 2: "skinny", 3: "ffma", 4: "tc", 5: "gemv"}
 OPT_EARLY_START = 1
 OPT_ADAPTIVE_PLANS = 2
+# LIN_OPT_EARLY_START levels: nothing before the previous kernel finishes (the
+# default); W and bias may be read early; X too (only when no other work on the
+# stream writes a call's inputs between library calls).
+EARLY_NONE, EARLY_WEIGHTS, EARLY_ALL = 0, 1, 2
 OK, ERR_ARG, ERR_ALIGN, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
 
 _PREC_NAMES = {"fp32": PREC_FP32, "tf32": PREC_TF32, "bf16": PREC_BF16}

@@ -26,9 +26,11 @@ library's own kernels:
 
 The incumbent is timed through ``lin_forward`` itself (the built-in table,
 with its adaptive choices), a candidate through ``lin_forward_plan`` (which an
-installed override also uses): both back to back on one stream, the early
-start included, with the weight rotated over enough copies to exceed the L2,
-so that each call reads its weight from HBM as a layer of a model does.
+installed override also uses): both back to back on one stream with the
+context's early-start level (LIN_OPT_EARLY_START), with the weight rotated
+over enough copies to exceed the L2, so that each call reads its weight from
+HBM as a layer of a model does. Winners are found for the context as it is
+configured: tune with the early-start level the caller will run with.
 """
 from __future__ import annotations
 

@@ -33,7 +33,7 @@ struct lin_ctx {
     void* workspace;
     size_t workspace_bytes;
     int* dev_status;
-    bool early_start;  // LIN_OPT_EARLY_START
+    int early_level;   // LIN_OPT_EARLY_START: 0 none, 1 W and bias, 2 also X
     bool adaptive;     // LIN_OPT_ADAPTIVE_PLANS
     lin_plan last_plan;
     std::mutex override_mu;
@@ -470,8 +470,8 @@ int run(lin_ctx* ctx, const lin_plan& plan_in, int M, int N, int K, const void* 
     bool w_ok = false, x_ok = false, known = false;
     early_reads_ok(p.stream, Range{W, (size_t)N * K * ein}, Range{bias, bias ? (size_t)N * 4 : 0},
                    Range{X, (size_t)M * K * ein}, Range{Y, ybytes}, &w_ok, &x_ok, &known);
-    p.early_start = ctx->early_start && w_ok;
-    p.early_x = p.early_start && x_ok;
+    p.early_start = ctx->early_level >= 1 && w_ok;
+    p.early_x = p.early_start && ctx->early_level >= 2 && x_ok;
     // An independent call right after another call on this stream overlaps it:
     // the skinny stream then needs no K split to fill the SMs (the concurrent
     // calls do), and skipping the split saves its reduction.
@@ -554,7 +554,7 @@ int lin_create(lin_ctx** out, int device, size_t max_workspace_bytes) {
     lin_ctx* c = new (std::nothrow) lin_ctx();
     if (!c) return LIN_ERR_CUDA;
     c->device = device;
-    c->early_start = true;
+    c->early_level = 0;
     c->adaptive = true;
     std::memset(&c->last_plan, 0, sizeof(c->last_plan));
     c->workspace_bytes = max_workspace_bytes ? max_workspace_bytes : ((size_t)64 << 20);
@@ -596,8 +596,8 @@ int lin_set_option(lin_ctx* ctx, int option, long long value) {
     if (!ctx) return LIN_ERR_ARG;
     switch (option) {
         case LIN_OPT_EARLY_START:
-            if (value != 0 && value != 1) return LIN_ERR_ARG;
-            ctx->early_start = value != 0;
+            if (value < 0 || value > 2) return LIN_ERR_ARG;
+            ctx->early_level = (int)value;
             return LIN_OK;
         case LIN_OPT_ADAPTIVE_PLANS:
             if (value != 0 && value != 1) return LIN_ERR_ARG;
@@ -747,8 +747,8 @@ int backward_setup(lin_ctx* ctx, int which, int M, int N, int K, const void* dZ,
     bool w_ok = false, x_ok = false, known = false;
     early_reads_ok(q->stream, Range{B, b_bytes}, Range{nullptr, 0}, Range{dZ, dz_bytes}, Range{out, out_bytes}, &w_ok,
                    &x_ok, &known);
-    q->early_start = ctx->early_start && w_ok;
-    q->early_x = q->early_start && x_ok;
+    q->early_start = ctx->early_level >= 1 && w_ok;
+    q->early_x = q->early_start && ctx->early_level >= 2 && x_ok;
     q->workspace = ctx->workspace;
     q->workspace_bytes = ctx->workspace_bytes;
     // Right after an independent call the two overlap (early start) and fill
@@ -849,7 +849,8 @@ int lin_gelu_backward(lin_ctx* ctx, long long count, const void* dY, const void*
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     bool w_ok = false, x_ok = false, known = false;
     early_reads_ok(st, Range{Z, bytes}, Range{nullptr, 0}, Range{dY, bytes}, Range{dZ, bytes}, &w_ok, &x_ok, &known);
-    return launch_gelu_backward(count, dY, Z, dZ, precision == LIN_PREC_BF16, ctx->sm_count, st, ctx->early_start);
+    return launch_gelu_backward(count, dY, Z, dZ, precision == LIN_PREC_BF16, ctx->sm_count, st,
+                                ctx->early_level >= 1);
 }
 
 int lin_fold_layernorm(lin_ctx* ctx, int N, int K, const float* W, const float* bias, const float* gamma,
