@@ -111,3 +111,71 @@ def test_broken_plans_are_refused():
     assert tll.plan_check(tc, 0, N, K, "bf16", 1 << 62) == tll.ERR_UNSUPPORTED
     assert tll.plan_check(tll.plan_query(152, 0, N, K, "bf16"), 0, N, K, "bf16", 0) == tll.OK
     assert tll.library().lin_plan_check(None, M, N, K, 2, 0) == tll.ERR_ARG
+
+
+# ---------------------------------------------------------------- the table's rules
+
+
+def _cdiv(a, b):
+    return -(-a // b)
+
+
+def test_skinny_cluster_rule():
+    """Isolated skinny calls take the largest cluster (a power of two, at most
+    8) that keeps one CTA per SM and at least one K stage per CTA; the 96 KB
+    ring when W has more 128-row tiles than SMs."""
+    for sm in SMS:
+        for M in (2, 8, 16):
+            for N in (136, 768, 4096, 16384, 50257):
+                for K in (64, 768, 4096):
+                    p = tll.plan_query(sm, M, N, K, "bf16")
+                    assert p.kernel == tll.KERNEL_SKINNY
+                    tiles = _cdiv(N, 128)
+                    assert p.variant == (1 if tiles > sm else 0)
+                    kblocks = _cdiv(K, 64 * (4 if p.variant == 0 else 1))
+                    S = 1
+                    while S < 8 and tiles * S * 2 <= sm and 2 * S <= kblocks:
+                        S *= 2
+                    assert p.splits == S and p.grid_x == tiles and p.grid_y == S, (sm, M, N, K, p)
+
+
+def test_ffma_split_rule():
+    """FP32: 128x128 tiles when they give a full wave; else 64x64 tiles split so
+    that the (tile, split) CTAs fill two per SM without a second wave, with at
+    least 4 K steps of 32 per split, within the workspace."""
+    for sm in SMS:
+        for M in (9, 64, 128, 256, 1024, 4096):
+            for N in (64, 768, 2304, 3072, 4096):
+                for K in (64, 768, 3072):
+                    for ws in (0, 64 << 20):
+                        p = tll.plan_query(sm, M, N, K, "fp32", workspace_bytes=ws)
+                        assert p.kernel == tll.KERNEL_FFMA
+                        big = _cdiv(M, 128) * _cdiv(N, 128)
+                        assert p.variant == (0 if big >= sm else 1)
+                        tm = 128 if p.variant == 0 else 64
+                        tiles = _cdiv(M, tm) * _cdiv(N, tm)
+                        slots = sm if p.variant == 0 else 2 * sm
+                        assert tiles * p.splits <= max(slots, tiles)
+                        assert p.splits == 1 or _cdiv(K, 32) // p.splits >= 4
+                        assert p.workspace_bytes <= ws
+                        if ws and 2 * tiles <= slots and _cdiv(K, 32) >= 8:
+                            assert p.splits > 1, (sm, M, N, K, p)  # room for two CTAs per tile
+
+
+def test_tc_k_split_rule():
+    """tcgen05 K split: only when the tiles fill at most half of the SMs, with
+    at least 32 K stages per split, at most 16 splits, and never for the SM
+    pair; the pair for long K otherwise."""
+    for sm in SMS:
+        for M in (32, 128, 256, 1024, 8192):
+            for N in (256, 768, 3072):
+                for K in (768, 2048, 4096, 16384):
+                    p = tll.plan_query(sm, M, N, K, "bf16")
+                    assert p.kernel == tll.KERNEL_TC
+                    pair = p.variant >= 3
+                    if p.grid_z > 1:
+                        tiles = _cdiv(M, 128) * _cdiv(N, p.bn)
+                        assert not pair and tiles * 2 <= sm and p.grid_z <= 16
+                        assert _cdiv(K, 64) // p.grid_z >= 32
+                    if pair:
+                        assert _cdiv(K, 64) >= 64
