@@ -6,8 +6,9 @@ bias ("One multiply, one RTX 5090, eight kernels", "The multiply"). A step is
 one call of the layer (dispatch, split-K stream of W, fixed-order reduction,
 epilogue). Metric: achieved HBM GB/s over the algorithmic bytes (X + W + Y +
 bias once each) with W cold: each step reads one of R identical copies of W
-(R x 32 MiB > 4 x L2), so no step finds its W in L2 ("Where the time goes":
-the lab rotates through several identical copies of the weights).
+(R x 32 MiB > 4 x L2), so no step finds its W in L2 (the page's section
+"Where the time goes" keeps its weights cold the same way, cycling through
+copies of them).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME | --all]

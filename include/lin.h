@@ -5,8 +5,8 @@
  *
  * X is M x K row-major (one row per token / batch vector), W is N x K
  * row-major ("out x in", the way PyTorch stores a linear layer's weight), Y
- * is M x N row-major. Each output is the dot product of one row of X with one
- * row of W ("One multiply, one RTX 5090, eight kernels", section "The
+ * is M x N row-major. Output (m, n) is the inner product of row m of X and
+ * row n of W ("One multiply, one RTX 5090, eight kernels", section "The
  * multiply"). The bias (length N, optional) and the activation are applied in
  * the store of the product ("Writing a CUDA matmul that catches cuBLAS",
  * sections "The bias add did not need to exist" and "The residual and GELU go
@@ -141,9 +141,10 @@ LIN_API int lin_forward(lin_ctx* ctx, int M, int N, int K, const void* X, const 
                 const float* bias, void* Y, int epilogue, int precision, void* stream);
 
 /* Y = act(X . W^T + bias) + R: the residual add in the GEMM's store
- * ("Optimizing a GPT-2-class transformer on a GPU", Act II, rung 10: bias,
- * relu and residual adds move inside the GEMM's store; "Writing a CUDA matmul
- * that catches cuBLAS", "The residual and GELU go the same way"). A
+ * ("Optimizing a GPT-2-class transformer on a GPU", Act II, rung 10, where
+ * the bias, the activation and the residual add stop being kernels of their
+ * own; "Writing a CUDA matmul that catches cuBLAS", "The residual and GELU go
+ * the same way"). A
  * transformer block's x = x + proj(h) is this call with R = Y = x.
  *   R : M x N row-major, Y's element type; added after the activation, in
  *       fp32, with one rounding of the sum to Y's type. R may be Y itself (in
@@ -155,8 +156,9 @@ LIN_API int lin_forward_residual(lin_ctx* ctx, int M, int N, int K, const void* 
                                  void* stream);
 
 /* LayerNorm fold ("Optimizing a GPT-2-class transformer on a GPU", Act II,
- * rung 10: a layernorm's scale and shift feed only linear maps, so they fold
- * into the next layer's weights offline, in double). With
+ * rung 10: since LayerNorm's scale and shift reach the output only through
+ * the linear layer after it, they can be moved into that layer's weight and
+ * bias once, ahead of time, in double). With
  * LN(x) = gamma * xhat + beta, xhat = (x - mean) / sqrt(var + eps):
  *   W LN(x) + bias = W_out xhat + bias_out,
  *   W_out[n][k] = W[n][k] * gamma[k],  bias_out[n] = bias[n] + sum_k W[n][k] * beta[k].

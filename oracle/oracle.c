@@ -8,8 +8,8 @@
  *   Y[m][n] = act( sum_{k=0}^{K-1} X[m][k] * W[n][k]  +  bias[n] )
  *
  * - X is M x K row-major, W is N x K row-major ("out x in", the way PyTorch
- *   stores a linear layer's weight), Y is M x N row-major. Each output is the
- *   dot product of one row of X with one row of W
+ *   stores a linear layer's weight), Y is M x N row-major. Output (m, n) is
+ *   the inner product of row m of X and row n of W
  *   ("One multiply, one RTX 5090, eight kernels", section "The multiply").
  * - The sum is accumulated in double, in ascending k, one scalar at a time.
  *   Inputs are the fp32 values the GPU receives (bf16 inputs arrive here
@@ -194,9 +194,9 @@ void oracle_gelu_grad_array(int64_t count, const double* in, double* out)
 
 /*
  * Residual add in the GEMM's store ("Optimizing a GPT-2-class transformer on
- * a GPU", Act II, rung 10: bias, relu and residual adds move inside the GEMM's
- * store; "Writing a CUDA matmul that catches cuBLAS", "The residual and GELU
- * go the same way"):
+ * a GPU", Act II, rung 10, where the bias, the activation and the residual
+ * add stop being kernels of their own; "Writing a CUDA matmul that catches
+ * cuBLAS", "The residual and GELU go the same way"):
  *
  *   Y[m][n] = act(Z[m][n]) + R[m][n],   Z = X W^T + bias,
  *
@@ -245,9 +245,10 @@ void oracle_layernorm(int64_t M, int64_t K, const float* X, const float* gamma, 
 }
 
 /*
- * LayerNorm fold (Act II, rung 10: the scale and shift of a layernorm feed
- * only linear maps, so they fold into the next layer's weights offline, in
- * double). With LN(x) = gamma * xhat + beta,
+ * LayerNorm fold (Act II, rung 10: LayerNorm's scale and shift reach the
+ * output only through the next linear layer, so they can be moved into its
+ * weight and bias once, ahead of time, in double). With
+ * LN(x) = gamma * xhat + beta,
  *   W LN(x) + b = (W diag(gamma)) xhat + (W beta + b), so
  *   Wf[n][k] = W[n][k] * gamma[k],   bf[n] = b[n] + sum_k W[n][k] * beta[k]
  * (ascending k; bias or beta NULL count as zero). W: N*K, gamma, beta: K

@@ -22,8 +22,8 @@ Distributions
   ``sqrt(-2 ln u1) * cos(2 pi u2)``, scaled, then rounded to fp32 (and, for
   bf16 tensors, rounded to nearest-even bf16).
 
-The pages fix only "the same seeded generator" for every version of a kernel
-(a GPT-2-class transformer on a GPU, "Results"); the generator choice is this
+The pages only require that every version of a kernel is fed from one seeded
+generator (a GPT-2-class transformer on a GPU, "Results"); the generator choice is this
 project's reading, and parity does not depend on it because the oracle and the
 GPU receive the identical arrays.
 """

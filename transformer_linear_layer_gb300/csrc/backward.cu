@@ -4,13 +4,13 @@
 // dX = dY W^T and dW = dY^T X for a weight stored in x out, which with W
 // stored out x in reads
 //   dZ = dY * act'(Z),  dX = dZ W (M x K),  dW = dZ^T X (N x K),  db = sum_m dZ.
-// The page folds each transpose into the shared-memory staging ("each of the
-// four transpose cases is just a different index map"). Here:
+// The page folds each transpose into the shared-memory staging, so that each
+// transpose case becomes an index map of its own. Here:
 // * bf16: the tcgen05 kernel with MN-major operand descriptors (tc.cu).
 // * fp32 / tf32: bwd_ffma_kernel below, exact fp32 FFMAs. Both operands are
 //   staged as [reduction][output] tiles, so that every thread reads float4s
-//   of 4 consecutive output rows and columns ("the fp32 kernel stores As[k][m]
-//   and gets a straight vector copy"): an operand whose reduction index is
+//   of 4 consecutive output rows and columns (the page's fp32 kernel keeps its
+//   A tile k-major so that staging is a plain vector copy): an operand whose reduction index is
 //   its row (W in dX; dZ and X in dW) is a straight 16-byte copy, and dZ in dX
 //   (reduction index contiguous) is transposed on its way through registers.
 // * gelu_backward_kernel: dZ = dY * gelu'(Z), elementwise.
@@ -313,7 +313,8 @@ int bwd_ffma_splits(int which, int M, int N, int K, int sm_count, size_t ws_byte
     const long long tiles = (long long)((I + kBT - 1) / kBT) * ((J + kBT - 1) / kBT);
     const int nst = (R + kBR - 1) / kBR;
     // Fill four resident 256-thread CTAs per SM without a second wave, >= 4
-    // reduction stages per split ("split-K when the output is small and K is long").
+    // reduction stages per split (the page splits K when the output is small and
+    // the reduction long).
     const long long slots = 4LL * sm_count;
     int S = tiles >= slots ? 1 : (int)(slots / tiles);
     const int max_s = nst / 4 > 1 ? nst / 4 : 1;

@@ -23,9 +23,9 @@
 //   same way", with the feature set as a template parameter).
 // * Optional split-K for outputs too small to fill the SMs: each CTA sums one
 //   K range into the workspace and the last CTA of a tile adds the ranges in
-//   order 0..S-1 ("One kernel was never going to be enough": split-K when the
-//   output is small and K is long; "Optimizing a GPT-2-class transformer on a
-//   GPU", Act I: fixed-order reduction).
+//   order 0..S-1 ("One kernel was never going to be enough": the page splits
+//   K for small outputs with long reductions; "Optimizing a GPT-2-class
+//   transformer on a GPU", Act I: fixed-order reduction).
 // * Programmatic dependent launch (when the caller allows an early start): the
 //   CTAs may start while the previous kernel on the stream drains, loading X
 //   and W before griddepcontrol.wait when neither is that kernel's output;

@@ -2,8 +2,8 @@
 // one-row sites.
 //
 // "Optimizing a GPT-2-class transformer on a GPU", Act II: only the final
-// token's logits are needed, and "a dedicated GEMV takes the one-row sites"
-// of the routing table. With M <= 8 every weight value feeds at most 8
+// token's logits are needed, and the routing table sends the one-row sites
+// to a GEMV of their own. With M <= 8 every weight value feeds at most 8
 // products, so the layer is a single pass over W and its time is W's bytes
 // over the HBM bandwidth; tiles of 64 or 128 rows would multiply 56-127 rows
 // of padding.
@@ -22,11 +22,13 @@
 // * bf16 (M <= 4): X is widened to fp32 in shared memory, each 16-byte load
 //   of W carries 8 values, bf16 x bf16 products are exact in fp32 and the
 //   sums are fp32 as on the tensor cores; the result is rounded to bf16 (the
-//   GELU then uses the hardware tanh). At most 4 rows keep the convert + FMA
-//   instructions per weight well under what the SMs issue at HBM speed.
-// * Programmatic dependent launch: W streams before griddepcontrol.wait when
-//   the caller allows an early start (W is not the previous call's output), X
-//   only when it is not that output either; bias and Y after the wait.
+//   GELU then uses the hardware tanh). Up to 4 rows run here through explicit
+//   plans; the built-in table sends bf16 here for one row only (measured: from
+//   2 rows on the skinny tensor-core kernel streams W faster).
+// * Programmatic dependent launch: when the caller allows X to be read early
+//   (early start level 2) and X is not the previous call's output, X and then
+//   W are read before griddepcontrol.wait; otherwise the kernel waits first.
+//   Bias and Y only after the wait.
 #include "internal.h"
 #include "device_common.cuh"
 
