@@ -287,3 +287,28 @@ def test_autotune_save_format(tmp_path):
     assert len(table) == 1 and table[0]["shape"] == [128, 768, 768]
     back = autotune._plan_from_dict(table[0]["plan"])
     assert autotune._plan_key(back) == autotune._plan_key(p)
+
+
+def test_header_is_plain_c_and_links(tmp_path):
+    """include/lin.h compiles as C99 with warnings as errors, and a C program
+    linked against the built library runs its host-only calls (no GPU)."""
+    import shutil
+    import subprocess
+
+    import importlib
+
+    B = importlib.import_module("transformer_linear_layer_gb300.build")
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    lib = B.build()
+    here = os.path.dirname(os.path.abspath(__file__))
+    exe = str(tmp_path / "c_abi_host_calls")
+    cmd = [cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", B.INCLUDE,
+           os.path.join(here, "c_abi_host_calls.c"), lib, "-Wl,-rpath," + os.path.dirname(lib), "-o", exe]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.count("ok ") == 10
