@@ -312,3 +312,25 @@ def test_header_is_plain_c_and_links(tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.count("ok ") == 10
+
+
+def test_no_cpu_fallback_in_the_binding():
+    """Host tensors are refused by every compute entry point of the binding
+    (nothing is computed on the CPU), and so are mismatched dtypes and shapes."""
+    import torch
+
+    x = torch.randn(4, 64)
+    w = torch.randn(8, 64)
+    for call in (lambda: tll.forward(x, w),
+                 lambda: tll.forward_residual(x, w, torch.zeros(4, 8)),
+                 lambda: tll.backward_data(torch.randn(4, 8), w),
+                 lambda: tll.backward_weight(torch.randn(4, 8), x),
+                 lambda: tll.backward_data_gelu(torch.randn(4, 8), w, x),
+                 lambda: tll.gelu_backward(torch.randn(4, 8), torch.randn(4, 8)),
+                 lambda: tll.fold_layernorm(w, torch.ones(64))):
+        with pytest.raises((ValueError, TypeError)):
+            call()
+    with pytest.raises(TypeError):
+        tll.forward(x.bfloat16(), w)  # bf16 X with fp32 W
+    with pytest.raises((ValueError, TypeError)):
+        tll.forward(x, torch.randn(8, 63))  # K mismatch
