@@ -331,9 +331,11 @@ LIN_API int lin_abi_version(void);
 
 /* The pages have no counterpart to this entry point; it exists for callers
  * that cannot allocate device memory when they run the layer, for example:
- * - code recording a CUDA graph (an allocation breaks the capture);
- * - runtimes that own all device memory through their own pool;
- * - paths where an allocation could block or fail.
+ * - runtimes that reserve all device memory for their own pool at start-up
+ *   and treat any other allocation as a failure;
+ * - latency-critical paths where an allocation could block on the device or
+ *   fail under memory pressure;
+ * - plug-ins that are handed device pointers but no allocator.
  *
  * Y = act(X . W^T + bias) in fp32 on the CURRENT device, with the same
  * kernel and split-K choice as lin_forward(..., LIN_PREC_FP32, ...) (the FFMA
@@ -346,10 +348,14 @@ LIN_API int lin_abi_version(void);
  * pointers.
  *
  * Limits and caveats:
- * - A shape whose split needs more scratch than the array holds returns
- *   LIN_ERR_WORKSPACE (nothing is launched).
- * - The first call on a device looks up the array's device address; make
- *   that first call before any stream capture.
+ * - The split is the one lin_forward would take, so the result is bitwise
+ *   that of lin_forward. A shape whose split needs more scratch than the
+ *   array holds returns LIN_ERR_WORKSPACE (nothing is launched); the split
+ *   fills the SMs, so its scratch grows with the SM count (about 5 MB on 152
+ *   SMs) and not with the shape.
+ * - The first call on a device (and the first after that device's context
+ *   was created anew) looks up the array's device address; make that first
+ *   call before any stream capture.
  * - Every call shares the one array, and the array keeps the last call's
  *   contents. The call zeroes the counters it uses on `stream` before its
  *   kernel.

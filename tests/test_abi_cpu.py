@@ -6,6 +6,7 @@ import re
 
 import pytest
 
+import synthetic_inputs as si
 import transformer_linear_layer_gb300 as tll
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -334,3 +335,25 @@ def test_no_cpu_fallback_in_the_binding():
         tll.forward(x.bfloat16(), w)  # bf16 X with fp32 W
     with pytest.raises((ValueError, TypeError)):
         tll.forward(x, torch.randn(8, 63))  # K mismatch
+
+
+def test_static_scratch_rule_on_the_host():
+    """lin_forward_fp32_static runs the dispatch table's split, refusing a
+    shape whose split needs more than the fixed array. The split fills the
+    SMs, so its scratch grows with the SM count and not with the shape: every
+    GPT-2 and square fp32 shape fits on 152 SMs, and the refusal shape of the
+    GPU test needs more than the array only on a much larger device. The
+    binding's constant is the header's."""
+    import re
+
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "lin.h")).read()
+    m = re.search(r"#define LIN_STATIC_SCRATCH_BYTES \((\d+)u << (\d+)\)", hdr)
+    assert m and int(m.group(1)) << int(m.group(2)) == tll.STATIC_SCRATCH_BYTES
+    for sm in (132, 148, 152, 160):
+        for layer in list(si.GPT2_M128_FP32) + [si.SQUARE_256_FP32, si.SQUARE_4096_FP32]:
+            p = tll.plan_query(sm, layer.M, layer.N, layer.K, "fp32", workspace_bytes=1 << 62)
+            assert p.workspace_bytes <= tll.STATIC_SCRATCH_BYTES, (sm, layer.name)
+    M, N, K = 64, 512, 8192
+    assert tll.plan_query(152, M, N, K, "fp32", workspace_bytes=1 << 62).workspace_bytes <= tll.STATIC_SCRATCH_BYTES
+    big = tll.plan_query(1024, M, N, K, "fp32", workspace_bytes=1 << 62)
+    assert big.splits > 1 and big.workspace_bytes > tll.STATIC_SCRATCH_BYTES

@@ -36,6 +36,8 @@ OPT_ADAPTIVE_PLANS = 2
 # stream writes a call's inputs between library calls).
 EARLY_NONE, EARLY_WEIGHTS, EARLY_ALL = 0, 1, 2
 OK, ERR_ARG, ERR_ALIGN, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
+# LIN_STATIC_SCRATCH_BYTES: the fixed device array behind lin_forward_fp32_static.
+STATIC_SCRATCH_BYTES = 8 << 20
 
 _PREC_NAMES = {"fp32": PREC_FP32, "tf32": PREC_TF32, "bf16": PREC_BF16}
 _EPI_NAMES = {"none": EPI_NONE, None: EPI_NONE, "gelu": EPI_GELU_TANH, "gelu_tanh": EPI_GELU_TANH}

@@ -269,16 +269,9 @@ int launch_cfg(const FfmaArgs& a, dim3 grid, cudaStream_t st, bool gelu, bool ea
                               : ffma_kernel<BM, BN, BK, TM, TN, STAGES, true, false>)
                      : (split ? ffma_kernel<BM, BN, BK, TM, TN, STAGES, false, true>
                               : ffma_kernel<BM, BN, BK, TM, TN, STAGES, false, false>);
-    static unsigned long long attr_set[4] = {0, 0, 0, 0};  // per instantiation and device
+    static std::atomic<unsigned long long> attr_set[4];  // per instantiation: one bit per device
     const int which = (gelu ? 2 : 0) + (split ? 1 : 0);
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return LIN_ERR_CUDA;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(attr_set[which] & bit)) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return LIN_ERR_CUDA;
-        attr_set[which] |= bit;
-    }
+    if (ensure_smem_attr(attr_set[which], kern, smem) != LIN_OK) return LIN_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(256, 1, 1);

@@ -183,15 +183,8 @@ template <int MR, int RPW, bool GELU, bool BF16>
 int launch_mr(const GemvArgs& a, int grid, bool early, cudaStream_t st) {
     auto kern = gemv_kernel<MR, RPW, GELU, BF16>;
     const size_t smem = (size_t)MR * a.K * sizeof(float);
-    static unsigned long long attr_set = 0;  // one attribute call per instantiation and device
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return LIN_ERR_CUDA;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(attr_set & bit)) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvMaxSmem) != cudaSuccess)
-            return LIN_ERR_CUDA;
-        attr_set |= bit;
-    }
+    static std::atomic<unsigned long long> attr_set{0};  // per instantiation: one bit per device
+    if (ensure_smem_attr(attr_set, kern, kGemvMaxSmem) != LIN_OK) return LIN_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(kGemvThreads, 1, 1);

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/lin.h"
 
 namespace lin {
@@ -99,6 +101,22 @@ inline int tc_ksplits(long long tiles, int nkb, int sm, size_t ws_bytes, int bn)
 constexpr int kGemvMaxRows = 8;
 constexpr int kGemvMaxRowsBf16 = 4;
 constexpr int kGemvMaxSmem = 96 * 1024;
+
+// Raise a kernel's dynamic shared-memory limit on the current device, once per
+// device ordinal below 64 (one bit each in `done`; higher ordinals set it on
+// every call). Launches from several host threads may race to the first call:
+// both then set the same value, and the mask is only read and or-ed atomically.
+template <class Kernel>
+int ensure_smem_attr(std::atomic<unsigned long long>& done, Kernel kern, size_t smem) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LIN_ERR_CUDA;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return LIN_OK;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return LIN_ERR_CUDA;
+    if (bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    return LIN_OK;
+}
 
 // Launchers (return LIN_OK or LIN_ERR_*). They assume the plan was validated.
 int launch_fill(const Problem& p);

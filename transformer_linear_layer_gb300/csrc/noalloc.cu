@@ -1,17 +1,18 @@
 // A context-free fp32 entry point that allocates no device memory.
 //
 // Some callers cannot call cudaMalloc at the moment they run a layer:
-// - a program recording a CUDA graph (an allocation during stream capture
-//   breaks the capture);
 // - a serving runtime that reserved all device memory for its own pool at
 //   start-up and treats any other allocation as a failure;
 // - a latency-critical path where an allocation could block on the device
-//   or fail under memory pressure.
+//   or fail under memory pressure;
+// - a plug-in that is handed device pointers but no allocator.
 // lin_forward_fp32_static runs the same fp32 kernels as lin_forward (the
 // FFMA kernel with the dispatch table's split-K choice, or the GEMV for a few
 // rows, which needs no scratch). The split's scratch (tile
 // counters, then partial sums) lives in the fixed device array below. Every
 // GPU that loads this library holds that array until the process exits.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "internal.h"
@@ -24,25 +25,55 @@ namespace {
 static __device__ __align__(256) unsigned char g_static_scratch[LIN_STATIC_SCRATCH_BYTES];
 
 std::mutex g_scratch_mu;
-void* g_scratch_addr[64];  // device address of g_static_scratch, per device ordinal
+// Device address of g_static_scratch per device ordinal, with the context it
+// was looked up in: a context created anew (after cudaDeviceReset) loads the
+// module again, so the address is looked up again.
+struct ScratchAddr {
+    CUcontext ctx;
+    void* addr;
+};
+ScratchAddr g_scratch_addr[64];
 
-// Device address of the scratch array on the current device. Looked up once
-// per device with that device current; host code must not use the symbol's
-// host-side name as an address.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current_fn() {
+    static CtxGetCurrentFn fn = [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return (CtxGetCurrentFn) nullptr;
+        return reinterpret_cast<CtxGetCurrentFn>(ptr);
+    }();
+    return fn;
+}
+
+// Device address of the scratch array on the current device, looked up with
+// that device current. Host code must not use the symbol's host-side name as
+// an address.
 int scratch_on_current_device(void** out, int* device) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return LIN_ERR_CUDA;
     if (dev < 0 || dev >= 64) return LIN_ERR_UNSUPPORTED;
+    CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+    CUcontext ctx = nullptr;
+    if (!get_ctx || get_ctx(&ctx) != CUDA_SUCCESS) return LIN_ERR_CUDA;
+    if (!ctx) {
+        // No context on this thread yet: cudaSetDevice creates the device's
+        // primary context and makes it current.
+        if (cudaSetDevice(dev) != cudaSuccess || get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return LIN_ERR_CUDA;
+    }
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    ScratchAddr& e = g_scratch_addr[dev];
+    if (!e.addr || e.ctx != ctx) {
         void* addr = nullptr;
         if (cudaGetSymbolAddress(&addr, g_static_scratch) != cudaSuccess || !addr) {
             cudaGetLastError();
             return LIN_ERR_CUDA;
         }
-        g_scratch_addr[dev] = addr;
+        e.ctx = ctx;
+        e.addr = addr;
     }
-    *out = g_scratch_addr[dev];
+    *out = e.addr;
     *device = dev;
     return LIN_OK;
 }
@@ -79,8 +110,10 @@ extern "C" int lin_forward_fp32_static(int M, int N, int K, const float* X, cons
     int sm = 0;
     if (cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return LIN_ERR_CUDA;
 
-    // The table's plan for this shape, as if scratch were unlimited; a shape
-    // whose split needs more than the fixed array is refused, not shrunk.
+    // The table's plan for this shape, as if scratch were unlimited: the same
+    // split as lin_forward, so the same bits. A shape whose split needs more
+    // than the fixed array is refused, not shrunk (the split fills the SMs, so
+    // this happens only on GPUs with far more SMs than 152).
     lin_plan plan;
     rc = lin_plan_query(sm, M, N, K, LIN_PREC_FP32, epilogue, (size_t)1 << 62, &plan);
     if (rc != LIN_OK) return rc;

@@ -335,15 +335,8 @@ int launch_cfg(const CUtensorMap& tw, const CUtensorMap& tx, const SkinnyArgs& a
     constexpr size_t smem = skinny_smem_bytes(STAGES, KBOX, CL);
     static_assert(skinny_smem_bytes(STAGES, KBOX, CL) <= 227 * 1024, "shared memory");
     auto kern = skinny_kernel<STAGES, KBOX, CL, GELU>;
-    static unsigned long long attr_set = 0;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return LIN_ERR_CUDA;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(attr_set & bit)) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return LIN_ERR_CUDA;
-        attr_set |= bit;
-    }
+    static std::atomic<unsigned long long> attr_set{0};  // per instantiation: one bit per device
+    if (ensure_smem_attr(attr_set, kern, smem) != LIN_OK) return LIN_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_x, CL, 1);
     cfg.blockDim = dim3(kSkinnyThreads, 1, 1);

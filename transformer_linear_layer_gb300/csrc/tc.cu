@@ -683,15 +683,8 @@ int launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& 
     constexpr size_t smem = tc_smem_bytes<BF16, BN, PAIR>();
     static_assert(tc_smem_bytes<BF16, BN, PAIR>() <= 227 * 1024, "shared memory");
     auto kern = tc_kernel<BF16, BN, GELU, PAIR, SK, LAY>;
-    static unsigned long long attr_set = 0;  // one attribute call per instantiation and device
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return LIN_ERR_CUDA;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(attr_set & bit)) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return LIN_ERR_CUDA;
-        attr_set |= bit;
-    }
+    static std::atomic<unsigned long long> attr_set{0};  // per instantiation: one bit per device
+    if (ensure_smem_attr(attr_set, kern, smem) != LIN_OK) return LIN_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(kTcThreads, 1, 1);
