@@ -3,15 +3,33 @@
 Default workload: the skinny linear layer, M = 16 vectors against a
 4096 x 4096 bf16 weight stored out x in, fp32 accumulate, bf16 output, fp32
 bias ("One multiply, one RTX 5090, eight kernels", "The multiply"). A step is
-one call of the layer (dispatch, split-K stream of W, fixed-order reduction,
-epilogue). Metric: achieved HBM GB/s over the algorithmic bytes (X + W + Y +
-bias once each) with W cold: each step reads one of R identical copies of W
-(R x 32 MiB > 4 x L2), so no step finds its W in L2 (the page's section
-"Where the time goes" keeps its weights cold the same way, cycling through
-copies of them).
+one call of the layer through the C ABI (dispatch, split-K stream of W,
+fixed-order reduction, epilogue). Metric: achieved HBM GB/s over the
+algorithmic bytes (X + W + Y + bias once each) with W cold: each step reads
+one of R identical copies of W (R x 32 MiB > 4 x L2), and the L2 is flushed
+by a read of a buffer twice its size before every timed region, so no step
+finds its W in L2 (the page's section "Where the time goes" keeps its weights
+cold the same way, cycling through copies of them).
+
+Three ways of calling the layer back to back are timed, each over exactly
+--steps calls replayed from warm CUDA graphs:
+  back_to_back  independent calls (same X, rotating W), the early start at
+                level 2: a call may launch and read its inputs before its
+                predecessor finishes (the JSON line's `value`);
+  isolated_call the library default (no early start): every call waits for
+                the previous kernel to finish before it reads anything;
+  chained_call  X of call i+1 is Y of call i (a stack of layers), the early
+                start at level 1: W streams before the wait, X after it.
+Each also reports its steady state over a longer run and the difference (the
+pipeline fill and drain that a short run pays once).
+
+`per_config` times every configuration of the benchmark list in the same run
+(fp32 256^3, the M = 16 layer, 4096^3 FFMA and TF32, GPT-2 seq-128 fp32 and
+batched bf16 layers, the LM head) as isolated and back-to-back calls, each
+with its full-output error against the CPU oracle.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME | --all]
+                    [--workload NAME | --all] [--no-per-config]
 
 --impl reference times the CPU oracle (the plain double-accumulating triple
 loop) on the host cores on the same workload. Under torchrun (N > 1) each
@@ -44,7 +62,11 @@ METRIC = "GEMM TFLOP/s (GB/s for M=16) per shape and % of GB300 roofline, cold W
 PREC_NAME = {si.PREC_FP32: "fp32", si.PREC_TF32: "tf32", si.PREC_BF16: "bf16"}
 WORKLOADS = {w.name: w for w in si.ALL_WORKLOADS}
 DEFAULT_WORKLOAD = si.SKINNY_16x4096.name
+# The benchmark's configurations, in the order the line lists them.
+PER_CONFIG = ((si.SQUARE_256_FP32, si.SKINNY_16x4096, si.SQUARE_4096_FP32, si.SQUARE_4096_TF32) +
+              si.GPT2_M128_FP32 + si.GPT2_M8192_BF16)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+MAX_GRAPH = 2048  # calls per captured graph
 
 
 def log(*a):
@@ -63,30 +85,38 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def roofline_for(layer: si.Layer, seconds_per_launch: float, peaks, peaks_src, traffic):
-    """The bound that applies to this layer and the achieved fraction of it."""
+def is_hbm_bound(layer) -> bool:
+    """The bound of a layer: bytes at the copy peak against FLOPs at the
+    tensor peak (the fp32 path is always FFMA-bound at the shapes here)."""
+    if layer.precision == si.PREC_FP32:
+        return False
+    return layer.algorithmic_bytes() / 6.8e12 >= layer.flops / 1.9e15
+
+
+def roofline_for(layer, seconds_per_launch: float, peaks, peaks_src, traffic, ffma=None):
+    """The bound that applies to this layer and the achieved fraction of it.
+    `ffma`: the FFMA peak measured in this run ({"tflops": ...}), else the
+    nominal unit count x clock."""
     flops = layer.flops
     byts = layer.algorithmic_bytes()
-    hbm = peaks["hbm_gbs"] * 1e9
-    # Tensor peaks: bf16 measured; TF32 = bf16 x nominal ratio (1.1 / 2.25 PF dense).
-    if layer.precision == si.PREC_BF16:
-        tens, tens_note = peaks["bf16_tflops"] * 1e12, "bf16 dense, " + peaks_src
-    elif layer.precision == si.PREC_TF32:
-        tens, tens_note = peaks["bf16_tflops"] * 1e12 * (1.1 / 2.25), f"tf32 = bf16 {peaks_src} x 1.1/2.25 nominal"
-    else:
-        # FFMA: 152 SMs x 128 lanes x 2 FLOP x max SM clock (nominal unit counts and clock)
-        tens = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6
-        tens_note = "fp32 FFMA = 152 SMs x 128 lanes x 2 x sm_max_mhz"
-    t_mem, t_cmp = byts / hbm, flops / tens
-    if t_mem >= t_cmp:
+    if is_hbm_bound(layer):
         ach = byts / seconds_per_launch / 1e9
         return {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": traffic,
                 "peak_source": f"hbm copy, {peaks_src}", "algorithmic_bytes_per_launch": byts}
+    if layer.precision == si.PREC_BF16:
+        tens, note = peaks["bf16_tflops"] * 1e12, f"bf16 dense burst, {peaks_src}"
+    elif layer.precision == si.PREC_TF32:
+        tens, note = peaks["bf16_tflops"] * 1e12 * (1.1 / 2.25), f"tf32 = bf16 burst {peaks_src} x 1.1/2.25 nominal"
+    elif ffma:
+        tens, note = ffma["tflops"] * 1e12, "fp32 FFMA, measured in this run (lin_probe_ffma)"
+    else:
+        tens = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6
+        note = "fp32 FFMA nominal = 152 SMs x 128 lanes x 2 x sm_max_mhz"
     ach = flops / seconds_per_launch / 1e12
     bound = "alu" if layer.precision == si.PREC_FP32 else "tensor"
     return {"bound": bound, "achieved": round(ach, 2), "peak": round(tens / 1e12, 1), "unit": "TFLOP/s",
-            "frac": round(ach * 1e12 / tens, 4), "traffic": traffic, "peak_source": tens_note,
+            "frac": round(ach * 1e12 / tens, 4), "traffic": traffic, "peak_source": note,
             "algorithmic_flops_per_launch": flops}
 
 
@@ -194,10 +224,305 @@ def barrier(world):
         dist.barrier()
 
 
+# ------------------------------------------------------------------ timing
+
+class CallTimer:
+    """Times exactly n back-to-back calls of `step(i)` (call i) on `stream`.
+
+    The calls are captured in CUDA graphs whose length is a multiple of
+    `period` (the W copies rotate with that period, so consecutive replays
+    continue the rotation), replayed twice before any timing (a graph's first
+    replay pays its upload), and the L2 is flushed by reading a buffer twice
+    its size right before the timed region (reads leave no dirty lines for
+    the timed calls to write back). The region is bracketed by CUDA events
+    on `stream` with a device synchronisation on both sides."""
+
+    def __init__(self, torch, stream, step, period, flush_buf, world=1):
+        self.torch, self.stream, self.step, self.period, self.flush_buf = torch, stream, step, period, flush_buf
+        self.world = world
+        self.graphs = {}
+        self._sink = torch.empty((), dtype=flush_buf.dtype, device=flush_buf.device)
+
+    def _capture(self, n):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            for i in range(n):
+                self.step(i)
+        return g
+
+    def _plan(self, n):
+        if n not in self.graphs:
+            G = max(self.period, (MAX_GRAPH // self.period) * self.period)
+            if n <= G:
+                parts = [(self._capture(n), 1)]
+            else:
+                parts = [(self._capture(G), n // G)]
+                if n % G:
+                    parts.append((self._capture(n % G), 1))
+            with self.torch.cuda.stream(self.stream):
+                for g, _ in parts:
+                    g.replay()
+                    g.replay()
+            self.stream.synchronize()
+            self.graphs[n] = parts
+        return self.graphs[n]
+
+    def flush(self):
+        with self.torch.cuda.stream(self.stream):
+            self.torch.sum(self.flush_buf, dim=0, out=self._sink)
+
+    def measure(self, n) -> float:
+        """Seconds for exactly n calls."""
+        torch = self.torch
+        parts = self._plan(n)
+        self.flush()
+        self.stream.synchronize()
+        barrier(self.world)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            for g, reps in parts:
+                for _ in range(reps):
+                    g.replay()
+            e1.record(self.stream)
+        self.stream.synchronize()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3
+
+    def soak(self, seconds):
+        """Replay the largest prepared graph for about `seconds` (clocks settle)."""
+        parts = max(self.graphs.values(), key=lambda p: p[0][1])
+        until = time.perf_counter() + seconds
+        with self.torch.cuda.stream(self.stream):
+            while time.perf_counter() < until:
+                parts[0][0].replay()
+                self.stream.synchronize()
+
+
+def steady_calls(seconds_per_call_guess: float, steps: int, budget_s=0.05, cap=20000) -> int:
+    """Calls in the long run that gives a mode's steady state: >= steps, about
+    budget_s of work, at most cap."""
+    n = int(budget_s / max(seconds_per_call_guess, 1e-7))
+    return max(steps, min(cap, n))
+
+
+def measure_ffma_peak(torch, ctx, dev, stream):
+    """The fp32 FMA pipe's throughput from lin_probe_ffma (CUDA events, after
+    a warm-up launch): the FFMA kernels' roofline in this run."""
+    out = torch.zeros(1, device=dev)
+    iters = 4096
+    with torch.cuda.stream(stream):
+        ctx.probe_ffma_ptr(iters, out.data_ptr(), stream.cuda_stream)
+    stream.synchronize()
+    best = None
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            flops = ctx.probe_ffma_ptr(iters, out.data_ptr(), stream.cuda_stream)
+            e1.record(stream)
+        stream.synchronize()
+        s = e0.elapsed_time(e1) / 1e3
+        best = s if best is None else min(best, s)
+    nominal = 152 * 128 * 2 * 2070e6 / 1e12
+    return {"tflops": round(flops / best / 1e12, 2), "seconds": round(best, 6), "flops": flops,
+            "nominal_tflops": round(nominal, 1),
+            "how": "lin_probe_ffma: SMs x 4 CTAs x 256 threads, 8 independent fmaf chains each, best of 5 "
+                   "(CUDA events)"}
+
+
 # --------------------------------------------------------------- our arm
 
+class LayerBench:
+    """One layer on the device: inputs, rotating W copies, output, the full
+    oracle result, and the three ways of calling it."""
+
+    def __init__(self, torch, tll, oracle, layer, ctx, dev, stream, flush_buf, world=1, want_chain=False):
+        self.torch, self.tll, self.layer, self.ctx, self.dev, self.stream = torch, tll, layer, ctx, dev, stream
+        self.prec = PREC_NAME[layer.precision]
+        self.dt = torch.bfloat16 if layer.in_bf16 else torch.float32
+        self.esz = 2 if layer.in_bf16 else 4
+        self.epi = "gelu" if layer.epilogue else "none"
+        props = torch.cuda.get_device_properties(dev)
+        self.l2 = int(getattr(props, "L2_cache_size", 126 << 20))
+        X, W, b = si.make_inputs(layer)
+        self.X, self.W, self.b = X, W, b
+        self.x = torch.from_numpy(X).to(dev).to(self.dt)
+        w0 = torch.from_numpy(W).to(dev).to(self.dt)
+        self.bias = None if b is None else torch.from_numpy(b).to(dev)
+        self.w_bytes = layer.N * layer.K * self.esz
+        n = max(2, math.ceil(4 * self.l2 / self.w_bytes))
+        n += n % 2  # even: the chained mode alternates two activation buffers
+        while n > 2 and n * self.w_bytes > (8 << 30):
+            n -= 2
+        self.n_copies = n
+        self.ws = [w0] + [w0.clone() for _ in range(n - 1)]
+        self.y = torch.empty((layer.M, layer.N), dtype=self.dt, device=dev)
+        self.xp, self.yp = self.x.data_ptr(), self.y.data_ptr()
+        self.bp = None if self.bias is None else self.bias.data_ptr()
+        self.wps = [t.data_ptr() for t in self.ws]
+        self.chain = None
+        if want_chain and layer.N == layer.K:
+            # Two activation buffers: call i reads buf[i % 2] and writes buf[(i + 1) % 2].
+            self.chain = [self.x.clone(), torch.empty_like(self.x)]
+        self.world = world
+        self.timer = {}
+        self.flush_buf = flush_buf
+        self.oracle = oracle
+        self.ref = None
+
+    # one call of each kind (i = position in the sequence)
+    def _call(self, xp, wp, yp):
+        L = self.layer
+        rc = self.ctx.forward_ptr(L.M, L.N, L.K, xp, wp, self.bp, yp, self.epi, self.prec, self.stream.cuda_stream)
+        if rc != 0:
+            raise self.tll.LinError(rc, "lin_forward")
+
+    def step_independent(self, i):
+        self._call(self.xp, self.wps[i % self.n_copies], self.yp)
+
+    def step_chained(self, i):
+        a, b = self.chain[i % 2], self.chain[(i + 1) % 2]
+        self._call(a.data_ptr(), self.wps[i % self.n_copies], b.data_ptr())
+
+    def parity(self):
+        """Full-output parity of one call against the oracle (all M x N)."""
+        torch, oracle = self.torch, self.oracle
+        with torch.cuda.stream(self.stream):
+            self.step_independent(0)
+        self.stream.synchronize()
+        self.ctx.check(self.stream)
+        self.ref = oracle.linear(self.X, self.W, self.b, bool(self.layer.epilogue))
+        got = self.y.float().cpu().numpy().astype(np.float64)
+        err = oracle.rel_err(got, self.ref)
+        tol = oracle.TOL[self.layer.precision]
+        if not (np.all(np.isfinite(got)) and err <= tol):
+            raise SystemExit(f"correctness gate failed for {self.layer.name}: rel_err {err} > {tol}")
+        return err, tol
+
+    def parity_after(self):
+        got = self.y.float().cpu().numpy().astype(np.float64)
+        return self.oracle.rel_err(got, self.ref)
+
+    def chain_parity(self):
+        """Two chained calls: each output against the oracle applied to the
+        exact values the call read (the previous call's bf16 output)."""
+        torch, oracle = self.torch, self.oracle
+        a0 = self.chain[0].float().cpu().numpy()
+        with torch.cuda.stream(self.stream):
+            self.step_chained(0)
+            self.step_chained(1)
+        self.stream.synchronize()
+        self.ctx.check(self.stream)
+        y1 = self.chain[1].float().cpu().numpy()
+        y2 = self.chain[0].float().cpu().numpy()
+        e1 = oracle.rel_err(y1.astype(np.float64), oracle.linear(a0, self.W, self.b, bool(self.layer.epilogue)))
+        e2 = oracle.rel_err(y2.astype(np.float64), oracle.linear(y1, self.W, self.b, bool(self.layer.epilogue)))
+        tol = oracle.TOL[self.layer.precision]
+        if not (e1 <= tol and e2 <= tol):
+            raise SystemExit(f"chained calls are wrong for {self.layer.name}: rel_err {e1}, {e2} > {tol}")
+        # Restore buffer 0 to X for the timed chain (its values do not change the work).
+        self.chain[0].copy_(self.x)
+        torch.cuda.synchronize()
+        return max(e1, e2)
+
+    def mode(self, name, early_level, step):
+        torch = self.torch
+        self.ctx.set_option(self.tll.OPT_EARLY_START, early_level)
+        # Warm-up in this mode (attributes set, the stream's last output known).
+        with torch.cuda.stream(self.stream):
+            for i in range(3):
+                step(i)
+        self.stream.synchronize()
+        if name not in self.timer:
+            self.timer[name] = CallTimer(torch, self.stream, step, self.n_copies, self.flush_buf, self.world)
+        return self.timer[name]
+
+    def time_mode(self, name, early_level, step, steps, steady=True):
+        """{"seconds": exactly `steps` calls, "steady_s_per_call": over a
+        longer run, "fill_drain_us", "plan"} for one way of calling."""
+        t = self.mode(name, early_level, step)
+        secs = t.measure(steps)
+        plan = self.ctx.last_plan()
+        out = {"seconds": secs, "calls": steps, "plan": plan}
+        if steady:
+            n_long = steady_calls(secs / steps, steps)
+            if n_long > steps:
+                long_s = t.measure(n_long)
+                out["steady_s_per_call"] = long_s / n_long
+                out["steady_calls"] = n_long
+            else:
+                out["steady_s_per_call"] = secs / steps
+                out["steady_calls"] = steps
+            out["fill_drain_us"] = round((secs - steps * out["steady_s_per_call"]) * 1e6, 3)
+        return out
+
+    def value_of(self, s_per_call):
+        L = self.layer
+        if is_hbm_bound(L):
+            return L.algorithmic_bytes() / s_per_call / 1e9, "GB/s"
+        return L.flops / s_per_call / 1e12, "TFLOP/s"
+
+
+def plan_dict(plan):
+    return {k: v for k, v in plan.as_dict().items() if k != "kernel_name"}
+
+
+def mode_summary(lb: LayerBench, m, peaks, src, ffma, traffic=None):
+    per_call = m["seconds"] / m["calls"]
+    v, unit = lb.value_of(per_call)
+    roof = roofline_for(lb.layer, per_call, peaks, src, traffic, ffma)
+    d = {"value": round(v, 3), "unit": unit, "ms_per_step": round(per_call * 1e3, 6), "frac": roof["frac"],
+         "kernel": m["plan"].as_dict()["kernel_name"], "plan": plan_dict(m["plan"])}
+    if "steady_s_per_call" in m:
+        sv, _ = lb.value_of(m["steady_s_per_call"])
+        d["steady"] = {"value": round(sv, 3), "ms_per_step": round(m["steady_s_per_call"] * 1e3, 6),
+                       "calls": m["steady_calls"]}
+        d["fill_drain_us"] = m["fill_drain_us"]
+    return d
+
+
+def per_config_entries(torch, tll, oracle, ctx, dev, stream, flush_buf, peaks, src, ffma, done=None):
+    """Every benchmark configuration, isolated and back to back, with its
+    full-output parity against the oracle."""
+    out = []
+    for layer in PER_CONFIG:
+        if done and layer.name in done:
+            out.append(done[layer.name])
+            continue
+        t0 = time.perf_counter()
+        lb = LayerBench(torch, tll, oracle, layer, ctx, dev, stream, flush_buf)
+        err, tol = lb.parity()
+        rate = 50e12 if layer.precision == si.PREC_FP32 else 1e15
+        guess = max(layer.flops / rate, layer.algorithmic_bytes() / 6e12, 3e-6)
+        n = max(20, min(2000, int(0.02 / guess)))
+        iso = lb.time_mode("isolated", tll.EARLY_NONE, lb.step_independent, n, steady=False)
+        b2b = lb.time_mode("back_to_back", tll.EARLY_ALL, lb.step_independent, n, steady=False)
+        err_after = lb.parity_after()
+        if not err_after <= tol:
+            raise SystemExit(f"{layer.name}: output after the timed calls is wrong (rel_err {err_after})")
+        e = {"workload": layer.name, "M": layer.M, "N": layer.N, "K": layer.K, "precision": lb.prec,
+             "epilogue": lb.epi, "bias": layer.bias, "bound": "hbm" if is_hbm_bound(layer) else
+             ("alu" if layer.precision == si.PREC_FP32 else "tensor"),
+             "isolated": mode_summary(lb, iso, peaks, src, ffma),
+             "back_to_back": mode_summary(lb, b2b, peaks, src, ffma),
+             "rel_err": err, "rel_err_after_timed_calls": err_after, "tol": tol,
+             "compared": f"all {layer.M * layer.N} outputs", "calls_timed": n,
+             "w_copies": lb.n_copies}
+        out.append(e)
+        log(f"per_config {layer.name}: isolated {e['isolated']['value']} {e['isolated']['unit']} "
+            f"({e['isolated']['frac']}), back to back {e['back_to_back']['value']} ({e['back_to_back']['frac']}), "
+            f"rel_err {err:.2e} [{time.perf_counter() - t0:.1f} s]")
+        del lb
+        torch.cuda.empty_cache()
+    return out
+
+
 def bench_ours(layer: si.Layer, steps: int, warmup: int, world: int, rank: int, local_rank: int,
-               with_cpu_baseline: bool, e2e_steps: int):
+               with_cpu_baseline: bool, e2e_steps: int, with_per_config: bool):
     import torch
 
     import oracle
@@ -206,165 +531,68 @@ def bench_ours(layer: si.Layer, steps: int, warmup: int, world: int, rank: int, 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     ctx = tll.Context(local_rank)
-    # The timed steps are library calls back to back and nothing else writes
-    # their inputs on the stream: the programmatic early start is valid.
-    ctx.set_option(tll.OPT_EARLY_START, tll.EARLY_ALL)
-    props = torch.cuda.get_device_properties(dev)
-    l2 = int(getattr(props, "L2_cache_size", 126 << 20))
-    prec = PREC_NAME[layer.precision]
-    dt = torch.bfloat16 if layer.in_bf16 else torch.float32
-    esz = 2 if layer.in_bf16 else 4
-
-    X, W, b = si.make_inputs(layer)
-    x = torch.from_numpy(X).to(dev).to(dt)
-    w0 = torch.from_numpy(W).to(dev).to(dt)
-    bias = None if b is None else torch.from_numpy(b).to(dev)
-    w_bytes = layer.N * layer.K * esz
-    n_copies = max(2, math.ceil(4 * l2 / w_bytes))
-    while n_copies > 2 and n_copies * w_bytes > (8 << 30):
-        n_copies -= 1
-    ws = [w0] + [w0.clone() for _ in range(n_copies - 1)]
-    y = torch.empty((layer.M, layer.N), dtype=dt, device=dev)
-    epi = "gelu" if layer.epilogue else "none"
-    plan = ctx.plan(layer.M, layer.N, layer.K, prec, epi)
-
-    # Correctness gate before any timing (full output for small layers, sampled otherwise).
-    tll.forward(x, ws[-1], bias, epilogue=epi, precision=prec, out=y, ctx=ctx)
-    torch.cuda.synchronize()
-    ctx.check()
-    if layer.M * layer.N * layer.K <= 1 << 31:
-        ref = oracle.linear(X, W, b, bool(layer.epilogue))
-        err = oracle.rel_err(y.float().cpu().numpy(), ref)
-        gate = "full"
-    else:
-        rng = np.random.default_rng(1)
-        ms, ns = rng.integers(0, layer.M, 512), rng.integers(0, layer.N, 512)
-        ref = oracle.linear_entries(X, W, ms, ns, b, bool(layer.epilogue))
-        got = y[torch.from_numpy(ms).to(dev), torch.from_numpy(ns).to(dev)].float().cpu().numpy()
-        err = oracle.rel_err(got, ref)
-        gate = "512 sampled outputs"
-    tol = oracle.TOL[layer.precision]
-    if not err <= tol:
-        raise SystemExit(f"correctness gate failed for {layer.name}: rel_err {err} > {tol}")
-
     stream = torch.cuda.Stream(dev)
-    sptr = stream.cuda_stream
-    xp, yp = x.data_ptr(), y.data_ptr()
-    bp = None if bias is None else bias.data_ptr()
-    wps = [t.data_ptr() for t in ws]
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20))
+    flush_buf = torch.ones((2 * l2) // 4, dtype=torch.float32, device=dev)
+    peaks, src = load_peaks()
+    ffma = measure_ffma_peak(torch, ctx, dev, stream)
+    log(f"ffma probe: {ffma['tflops']} TFLOP/s (nominal {ffma['nominal_tflops']})")
 
-    def step(i):
-        # The public call (dispatch table, refined for back-to-back calls).
-        rc = ctx.forward_ptr(layer.M, layer.N, layer.K, xp, wps[i % n_copies], bp, yp, epi, prec, sptr)
-        if rc != 0:
-            raise tll.LinError(rc, "lin_forward")
-
-    # Warm-up (also sets kernel attributes before capture).
-    with torch.cuda.stream(stream):
-        for i in range(max(warmup, 3)):
-            step(i)
-    stream.synchronize()
-
-    # CUDA graphs of G back-to-back steps (the launch tax is ~ the kernel time here).
-    G = n_copies * max(1, 64 // n_copies)
-
-    def capture(nsteps):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(nsteps):
-                step(i)
-        return g
-
-    graph = capture(G)
-    rem = steps % G
-    graph_rem = capture(rem) if rem else None
-    stream.synchronize()
+    lb = LayerBench(torch, tll, oracle, layer, ctx, dev, stream, flush_buf, world, want_chain=True)
+    err, tol = lb.parity()
+    chain_err = lb.chain_parity() if lb.chain is not None else None
+    for i in range(max(warmup, 3)):
+        lb.step_independent(i)
+    torch.cuda.synchronize()
 
     sampler = ClockSampler(local_rank)
-    # Soak so the clock samples see the loaded state, then the timed region.
-    soak_until = time.perf_counter() + 1.0
-    with torch.cuda.stream(stream):
-        while time.perf_counter() < soak_until:
-            graph.replay()
-    stream.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(steps // G):
-            graph.replay()
-        if graph_rem is not None:
-            graph_rem.replay()
-        e1.record(stream)
-    stream.synchronize()
-    torch.cuda.synchronize()
-    barrier(world)
+    b2b_t = lb.mode("back_to_back", tll.EARLY_ALL, lb.step_independent)
+    b2b_t.measure(steps)  # prepares and warms the graphs
+    b2b_t.soak(1.0)
+    b2b = lb.time_mode("back_to_back", tll.EARLY_ALL, lb.step_independent, steps)
     clocks = sampler.stop()
-    local_s = e0.elapsed_time(e1) / 1e3
     ctx.check(stream)
-    plan = ctx.last_plan()  # the plan the timed calls ran with
-    # The back-to-back steps overlap on the GPU; their result must still be right.
-    if gate == "full":
-        err_after = oracle.rel_err(y.float().cpu().numpy(), ref)
-    else:
-        got = y[torch.from_numpy(ms).to(dev), torch.from_numpy(ns).to(dev)].float().cpu().numpy()
-        err_after = oracle.rel_err(got, ref)
+    err_after = lb.parity_after()
     if not err_after <= tol:
         raise SystemExit(f"output after the timed steps is wrong for {layer.name}: rel_err {err_after} > {tol}")
-
-    # The same call isolated: every call waits for the previous one to finish.
-    ctx.set_option(tll.OPT_EARLY_START, 0)
-    iso_steps = min(steps, 2000)
-    with torch.cuda.stream(stream):
-        step(0)
-    stream.synchronize()
-    g_iso = capture(min(G, iso_steps))
-    with torch.cuda.stream(stream):
-        g_iso.replay()
-        i0 = torch.cuda.Event(enable_timing=True)
-        i1 = torch.cuda.Event(enable_timing=True)
-        i0.record(stream)
-        for _ in range(max(1, iso_steps // min(G, iso_steps))):
-            g_iso.replay()
-        i1.record(stream)
-    stream.synchronize()
-    iso_plan = ctx.last_plan()
-    # End to end the inputs arrive by host copies on the same stream, which the
-    # library does not track: the library's default (no early start).
-    iso_s = i0.elapsed_time(i1) / 1e3 / (max(1, iso_steps // min(G, iso_steps)) * min(G, iso_steps))
+    iso = lb.time_mode("isolated", tll.EARLY_NONE, lb.step_independent, steps)
+    chained = None
+    if lb.chain is not None:
+        chained = lb.time_mode("chained", tll.EARLY_WEIGHTS, lb.step_chained, steps)
+    ctx.set_option(tll.OPT_EARLY_START, tll.EARLY_NONE)
 
     unit_bytes = layer.algorithmic_bytes()
+    local_s = b2b["seconds"]
     max_s, total_units = aggregate(local_s, float(steps) * unit_bytes, world, dev)
     per_launch_s = local_s / steps
-    hbm_bound = unit_bytes / 6.8e12 >= layer.flops / 1.9e15 if layer.precision != si.PREC_FP32 else False
-    if hbm_bound:
+    if is_hbm_bound(layer):
         value, unit = total_units / max_s / 1e9, "GB/s"
     else:
         value, unit = world * steps * layer.flops / max_s / 1e12, "TFLOP/s"
-
-    peaks, src = load_peaks()
+    plan = b2b["plan"]
     kfile = {tll.KERNEL_SKINNY: "skinny.cu", tll.KERNEL_FFMA: "ffma.cu", tll.KERNEL_TC: "tc.cu",
              tll.KERNEL_GEMV: "gemv.cu"}.get(plan.kernel)
     traffic = traffic_from_profile(kfile, layer.name) if kfile else None
-    roof = roofline_for(layer, per_launch_s, peaks, src, traffic)
+    roof = roofline_for(layer, per_launch_s, peaks, src, traffic, ffma)
 
     # End to end through the public API with host buffers: pinned host X, W,
-    # bias in, Y out, every step, copies inside the timed region.
-    hx = torch.from_numpy(X).to(dt).pin_memory()
-    hw = torch.from_numpy(W).to(dt).pin_memory()
-    hb = None if b is None else torch.from_numpy(b).pin_memory()
+    # bias in, Y out, every step, copies inside the timed region, the
+    # library's default early start (the inputs arrive by host copies on the
+    # same stream, which the library does not track).
+    dt, esz = lb.dt, lb.esz
+    hx = torch.from_numpy(lb.X).to(dt).pin_memory()
+    hw = torch.from_numpy(lb.W).to(dt).pin_memory()
+    hb = None if lb.b is None else torch.from_numpy(lb.b).pin_memory()
     hy = torch.empty((layer.M, layer.N), dtype=dt).pin_memory()
-    dx, dw = torch.empty_like(x), torch.empty_like(w0)
-    db = None if bias is None else torch.empty_like(bias)
+    dx, dw = torch.empty_like(lb.x), torch.empty_like(lb.ws[0])
+    db = None if lb.bias is None else torch.empty_like(lb.bias)
 
     def e2e_step():
         dx.copy_(hx, non_blocking=True)
         dw.copy_(hw, non_blocking=True)
         if db is not None:
             db.copy_(hb, non_blocking=True)
-        out = tll.forward(dx, dw, db, epilogue=epi, precision=prec, ctx=ctx)
+        out = tll.forward(dx, dw, db, epilogue=lb.epi, precision=lb.prec, ctx=ctx)
         hy.copy_(out, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -376,40 +604,55 @@ def bench_ours(layer: si.Layer, steps: int, warmup: int, world: int, rank: int, 
             e2e_step()
         stream.synchronize()
         e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_err = oracle.rel_err(hy.float().numpy().astype(np.float64), lb.ref)
+    if not e2e_err <= tol:
+        raise SystemExit(f"end-to-end output is wrong for {layer.name}: rel_err {e2e_err}")
     h2d = hx.numel() * esz + hw.numel() * esz + (0 if hb is None else hb.numel() * 4)
     d2h = hy.numel() * esz
     e2e_val = unit_bytes / e2e_s / 1e9 if unit == "GB/s" else layer.flops / e2e_s / 1e12
     e2e = {"value": round(e2e_val * world, 3), "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "steps": e2e_steps, "api": "transformer_linear_layer_gb300.forward (C ABI lin_forward)"}
-    iso_val = unit_bytes / iso_s / 1e9 if unit == "GB/s" else layer.flops / iso_s / 1e12
-    isolated = {"value": round(iso_val, 3), "unit": unit, "ms_per_step": round(iso_s * 1e3, 6),
-                "plan": {k: v for k, v in iso_plan.as_dict().items() if k != "kernel_name"},
-                "note": "early start off (the library default): each call waits for the previous kernel"}
+           "steps": e2e_steps, "api": "transformer_linear_layer_gb300.forward (C ABI lin_forward)",
+           "rel_err": e2e_err}
 
     cpu = None
     if with_cpu_baseline and rank == 0:
-        cpu = cpu_baseline(layer, X, W, b, unit)
+        cpu = cpu_baseline(layer, lb.X, lb.W, lb.b, unit)
 
+    per_cfg = None
+    if with_per_config and rank == 0:
+        del hx, hw, hy, dx, dw
+        per_cfg = per_config_entries(torch, tll, oracle, ctx, dev, stream, flush_buf, peaks, src, ffma)
+
+    b2b_sum = mode_summary(lb, b2b, peaks, src, ffma, traffic)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": round(max_s / steps * 1e3, 6), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": prec, "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": lb.prec, "data": "synthetic",
         "config": {"workload": layer.name, "M": layer.M, "N": layer.N, "K": layer.K,
-                   "bias": layer.bias, "epilogue": epi, "precision": prec,
-                   "kernel": plan.as_dict()["kernel_name"],
-                   "plan": {k: v for k, v in plan.as_dict().items() if k != "kernel_name"},
-                   "l2": f"cold W: {n_copies} rotating copies of W ({n_copies * w_bytes >> 20} MiB > L2 "
-                         f"{l2 >> 20} MiB), steps replayed from a CUDA graph of {G}",
+                   "bias": layer.bias, "epilogue": lb.epi, "precision": lb.prec,
+                   "kernel": plan.as_dict()["kernel_name"], "plan": plan_dict(plan),
+                   "l2": f"cold W: {lb.n_copies} rotating copies of W ({lb.n_copies * lb.w_bytes >> 20} MiB > L2 "
+                         f"{l2 >> 20} MiB) and a read of {2 * l2 >> 20} MiB before each timed region; exactly "
+                         f"`steps` calls replayed from warm CUDA graphs",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "parity_gate": {"rel_err": err, "rel_err_after_timed_steps": err_after, "tol": tol,
-                                   "compared": gate},
-                   "steps_are": "independent back-to-back calls (same X, rotating W copies) with the early "
-                                "start at level 2 (LIN_OPT_EARLY_START): a call may start and read its inputs "
-                                "before its predecessor finishes and writes Y after it; e2e and isolated_call "
-                                "use the library default (off)"},
-        "isolated_call": isolated,
+                                   "compared": f"all {layer.M * layer.N} outputs",
+                                   "chained_rel_err": chain_err},
+                   "steps_are": "independent back-to-back calls (same X, rotating W copies) with the early start "
+                                "at level 2 (LIN_OPT_EARLY_START): a call may start and read its inputs before its "
+                                "predecessor finishes and writes Y after it; isolated_call and e2e use the library "
+                                "default (off), chained_call level 1 with X = the previous call's Y"},
+        "back_to_back": b2b_sum,
+        "isolated_call": dict(mode_summary(lb, iso, peaks, src, ffma),
+                              note="early start off (the library default): each call waits for the previous kernel "
+                                   "to finish before it reads anything"),
+        "chained_call": None if chained is None else dict(
+            mode_summary(lb, chained, peaks, src, ffma),
+            note="X of call i+1 = Y of call i; early start level 1: W streams before the wait, X after it"),
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+        "ffma_peak": ffma,
         "gpu_launches": steps * (0 if plan.kernel in (tll.KERNEL_NONE,) else 1),
+        "per_config": per_cfg,
     }
     ctx.close()
     return line
@@ -458,8 +701,8 @@ def bench_backward(work: BwdWork, steps: int, warmup: int, world: int, rank: int
     """Back-to-back backward GEMMs or fused forwards through the C ABI
     (lin_backward_data, lin_backward_weight, lin_backward_data_gelu,
     lin_forward_residual), the streamed operand (dZ, or W for the forward)
-    rotating over copies larger than L2, replayed from a CUDA graph; parity
-    gate on sampled output rows against the oracle."""
+    rotating over copies larger than L2, exactly `steps` calls replayed from
+    warm CUDA graphs; full-output parity gate against the oracle."""
     import torch
 
     import oracle
@@ -522,18 +765,15 @@ def bench_backward(work: BwdWork, steps: int, warmup: int, world: int, rank: int
         step(0)
     stream.synchronize()
     ctx.check(stream)
-    rng = np.random.default_rng(2)
-    rows = np.unique(np.concatenate([rng.integers(0, out.shape[0], 64), [0, out.shape[0] - 1]]))
     if work.which == 1:
-        ref = oracle.backward_dx(dZ[rows], B)
+        ref = oracle.backward_dx(dZ, B)
     elif work.which == 2:
-        ref, _ = oracle.backward_dw(dZ[:, rows], B, with_bias=False)
+        ref, _ = oracle.backward_dw(dZ, B, with_bias=False)
     elif work.which == 3:
-        ref = oracle.backward_dx_gelu(dZ[rows], B, Zp[rows])
+        ref = oracle.backward_dx_gelu(dZ, B, Zp)
     else:
-        ref = oracle.linear_residual(dZ[rows], B, R[rows], bias_h)
-    got = out[torch.from_numpy(rows).to(dev)].float().cpu().numpy()
-    err = oracle.rel_err(got, ref)
+        ref = oracle.linear_residual(dZ, B, R, bias_h)
+    err = oracle.rel_err(out.float().cpu().numpy().astype(np.float64), ref)
     tol = oracle.TOL[si.PREC_BF16] if work.precision == si.PREC_BF16 else oracle.TOL[si.PREC_FP32]
     if not err <= tol:
         raise SystemExit(f"correctness gate failed for {work.name}: rel_err {err} > {tol}")
@@ -542,43 +782,15 @@ def bench_backward(work: BwdWork, steps: int, warmup: int, world: int, rank: int
         for i in range(max(warmup, 3)):
             step(i)
     stream.synchronize()
-    G = n_copies * max(1, 64 // n_copies)
-
-    def capture(nsteps):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(nsteps):
-                step(i)
-        return g
-
-    graph = capture(G)
-    rem = steps % G
-    graph_rem = capture(rem) if rem else None
-    stream.synchronize()
+    flush_buf = torch.ones((2 * l2) // 4, dtype=torch.float32, device=dev)
+    timer = CallTimer(torch, stream, step, n_copies, flush_buf, world)
+    timer.measure(steps)
     sampler = ClockSampler(local_rank)
-    soak_until = time.perf_counter() + 1.0
-    with torch.cuda.stream(stream):
-        while time.perf_counter() < soak_until:
-            graph.replay()
-    stream.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(steps // G):
-            graph.replay()
-        if graph_rem is not None:
-            graph_rem.replay()
-        e1.record(stream)
-    stream.synchronize()
-    barrier(world)
+    timer.soak(1.0)
+    local_s = timer.measure(steps)
     clocks = sampler.stop()
-    local_s = e0.elapsed_time(e1) / 1e3
     ctx.check(stream)
-    got = out[torch.from_numpy(rows).to(dev)].float().cpu().numpy()
-    err_after = oracle.rel_err(got, ref)
+    err_after = oracle.rel_err(out.float().cpu().numpy().astype(np.float64), ref)
     if not err_after <= tol:
         raise SystemExit(f"output after the timed steps is wrong for {work.name}: rel_err {err_after} > {tol}")
     max_s, _ = aggregate(local_s, float(steps) * work.algorithmic_bytes(), world, dev)
@@ -593,10 +805,10 @@ def bench_backward(work: BwdWork, steps: int, warmup: int, world: int, rank: int
                    "kernel": tll.KERNEL_NAMES[ctx.last_plan().kernel] if work.which == 4 else
                    ("tc (MN-major operands)" if work.precision == si.PREC_BF16 else "bwd_ffma"),
                    "l2": f"cold {'W' if work.which == 4 else 'dZ'}: {n_copies} rotating copies "
-                         f"({n_copies * rot_bytes >> 20} MiB > L2 {l2 >> 20} MiB), "
-                         f"steps replayed from a CUDA graph of {G}",
+                         f"({n_copies * rot_bytes >> 20} MiB > L2 {l2 >> 20} MiB), exactly `steps` calls "
+                         f"replayed from warm CUDA graphs",
                    "parity_gate": {"rel_err": err, "rel_err_after_timed_steps": err_after, "tol": tol,
-                                   "compared": f"{len(rows)} sampled output rows"}},
+                                   "compared": f"all {out.numel()} outputs"}},
         "roofline": roof, "clocks": clocks, "gpu_launches": steps,
     }
     ctx.close()
@@ -640,8 +852,7 @@ def bench_reference(layer: si.Layer, steps: int, warmup: int):
     import oracle
 
     X, W, b = si.make_inputs(layer)
-    hbm_bound = layer.precision != si.PREC_FP32 and layer.algorithmic_bytes() / 6.8e12 >= layer.flops / 1.9e15
-    unit = "GB/s" if hbm_bound else "TFLOP/s"
+    unit = "GB/s" if is_hbm_bound(layer) else "TFLOP/s"
     cores = oracle.max_threads()
     # Each step: the oracle on a bounded sample of rows (whole layer when small).
     rows = layer.M
@@ -677,12 +888,13 @@ BWD_BY_NAME = {w.name: w for w in BWD_WORKLOADS}
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS) + sorted(BWD_BY_NAME))
     ap.add_argument("--all", action="store_true", help="one line per workload (stdout), default line last")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the per_config section")
     ap.add_argument("--e2e-steps", type=int, default=50)
     args = ap.parse_args(argv)
     rank, world, local_rank = dist_env()
@@ -722,12 +934,13 @@ def main(argv=None):
                 print(json.dumps(line), flush=True)
     for name in names:
         layer = WORKLOADS[name]
-        # Other workloads: at least 300 steps and ~20 TFLOP, so that the timed
-        # region spans several replays of the step graph.
-        st = steps if name == args.workload else max(300, min(steps, int(2e13 / max(layer.flops, 1e6))))
+        default = name == args.workload
+        # Other workloads: at least 300 steps and ~20 TFLOP.
+        st = steps if default else max(300, min(steps, int(2e13 / max(layer.flops, 1e6))))
         line = bench_ours(layer, st, warmup, world, rank, local_rank,
-                          with_cpu_baseline=(not args.no_cpu_baseline and name == args.workload),
-                          e2e_steps=args.e2e_steps if name == args.workload else 5)
+                          with_cpu_baseline=(not args.no_cpu_baseline and default),
+                          e2e_steps=args.e2e_steps if default else 5,
+                          with_per_config=(default and not args.no_per_config and world == 1))
         if rank == 0:
             print(json.dumps(line), flush=True)
     if world > 1:

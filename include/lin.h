@@ -320,6 +320,17 @@ LIN_API int lin_set_option(lin_ctx* ctx, int option, long long value);
 /* SM count and device ordinal of a context (host values, no GPU call). */
 LIN_API int lin_ctx_info(const lin_ctx* ctx, int* device, int* sm_count, size_t* workspace_bytes);
 
+/* Throughput probe of the exact-fp32 FMA pipe (the roofline of the FFMA
+ * kernels; the pages derive their fp32 peak from unit counts and the clock,
+ * "Writing a CUDA matmul that catches cuBLAS", opening section). Launches, on
+ * `stream`, the context's SM count x 4 CTAs of 256 threads, each thread
+ * running 8 independent fmaf chains for iters x 16 steps, and nothing else;
+ * *flops (if not NULL) receives the FLOPs launched (2 per fmaf). The caller
+ * times the launch (CUDA events on `stream`). `out`: a device float the
+ * kernel writes only in a case that cannot occur, which keeps the chains
+ * live. Returns LIN_ERR_ARG for iters < 1 or a NULL out. */
+LIN_API int lin_probe_ffma(lin_ctx* ctx, int iters, float* out, double* flops, void* stream);
+
 /* Static message for a status code. */
 LIN_API const char* lin_strerror(int status);
 

@@ -48,33 +48,3 @@ def check_layer(layer: si.Layer, plan=None, ctx=None, tol=None):
     assert np.all(np.isfinite(y)), f"{layer.name}: non-finite output"
     assert err <= tol, f"{layer.name} plan={plan}: rel_err {err:.3e} > {tol:g}"
     return err
-
-
-def sample_indices(M, N, count, seed=0):
-    """Sampled (m, n) pairs: random ones plus the first/last row and column."""
-    rng = np.random.default_rng(seed)
-    ms = list(rng.integers(0, M, count))
-    ns = list(rng.integers(0, N, count))
-    for n in np.linspace(0, N - 1, 64).astype(int):
-        ms += [0, M - 1]
-        ns += [int(n), int(n)]
-    for m in np.linspace(0, M - 1, 64).astype(int):
-        ms += [int(m), int(m)]
-        ns += [0, N - 1]
-    return np.array(ms, np.int64), np.array(ns, np.int64)
-
-
-def check_layer_sampled(layer: si.Layer, count=2048, plan=None):
-    """Large-shape parity on sampled outputs computed one by one by the oracle.
-    The scale max|Y_ref| comes from the sampled entries (a lower bound of the
-    full max), which makes the test stricter, not looser."""
-    X, W, b = si.make_inputs(layer)
-    y = run_t(X, W, b, layer.precision, layer.epilogue, plan=plan)
-    ms, ns = sample_indices(layer.M, layer.N, count)
-    got = y[torch.from_numpy(ms).cuda(), torch.from_numpy(ns).cuda()].float().cpu().numpy().astype(np.float64)
-    ref = oracle.linear_entries(X, W, ms, ns, b, bool(layer.epilogue))
-    err = oracle.rel_err(got, ref)
-    tol = oracle.TOL[layer.precision]
-    assert bool(torch.isfinite(y).all()), f"{layer.name}: non-finite output"
-    assert err <= tol, f"{layer.name}: sampled rel_err {err:.3e} > {tol:g}"
-    return err

@@ -106,6 +106,7 @@ def library() -> ctypes.CDLL:
                 "lin_fold_layernorm": ([P, I, I, P, P, P, P, P, P, I, P], I),
                 "lin_set_plan_override": ([P, I, I, I, I, I, PP], I),
                 "lin_clear_plan_overrides": ([P], I),
+                "lin_probe_ffma": ([P, I, P, ctypes.POINTER(ctypes.c_double), P], I),
                 "lin_strerror": ([I], ctypes.c_char_p),
                 "lin_abi_version": ([], I),
             }
@@ -217,6 +218,15 @@ class Context:
     # raw-pointer calls (the C ABI, one to one) ---------------------------------
     def forward_ptr(self, M, N, K, X, W, bias, Y, epilogue, precision, stream) -> int:
         return library().lin_forward(self._h, M, N, K, X, W, bias, Y, _epi(epilogue), _prec(precision), stream)
+
+    def probe_ffma_ptr(self, iters: int, out, stream) -> float:
+        """Launch the fp32 FMA throughput probe (lin_probe_ffma) on `stream`;
+        returns the FLOPs launched. The caller times it."""
+        flops = ctypes.c_double()
+        rc = library().lin_probe_ffma(self._h, int(iters), out, ctypes.byref(flops), stream)
+        if rc != OK:
+            raise LinError(rc, "lin_probe_ffma")
+        return flops.value
 
     def forward_plan_ptr(self, plan: Plan, M, N, K, X, W, bias, Y, epilogue, precision, stream) -> int:
         return library().lin_forward_plan(self._h, ctypes.byref(plan), M, N, K, X, W, bias, Y, _epi(epilogue),

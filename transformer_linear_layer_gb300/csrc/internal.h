@@ -152,6 +152,10 @@ int launch_gelu_backward(long long count, const void* dY, const void* Z, void* d
 size_t colsum_workspace_bytes(int M, int N);
 int launch_colsum(int M, int N, const void* dZ, float* db, bool bf16, void* workspace, cudaStream_t st);
 
+// fp32 FMA throughput probe: sm_count x 4 CTAs of 256 threads, each running
+// independent fmaf chains for `iters` x 16 steps; *flops = the FLOPs launched.
+int launch_ffma_probe(int sm_count, int iters, float* out, cudaStream_t st, double* flops);
+
 int launch_fold_layernorm(int N, int K, const float* W, const float* bias, const float* gamma, const float* beta,
                           void* W_out, float* bias_out, bool bf16, int sm_count, cudaStream_t st);
 

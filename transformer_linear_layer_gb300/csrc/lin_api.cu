@@ -890,6 +890,14 @@ int lin_forward_plan(lin_ctx* ctx, const lin_plan* plan, int M, int N, int K, co
     return lin::run(ctx, *plan, M, N, K, X, W, bias, Y, epilogue, precision, stream, false);
 }
 
+int lin_probe_ffma(lin_ctx* ctx, int iters, float* out, double* flops, void* stream) {
+    if (!ctx || iters < 1 || !out) return LIN_ERR_ARG;
+    if ((uintptr_t)out % 4 != 0) return LIN_ERR_ALIGN;
+    lin::DeviceGuard guard(ctx->device);
+    if (!guard.ok) return LIN_ERR_CUDA;
+    return lin::launch_ffma_probe(ctx->sm_count, iters, out, static_cast<cudaStream_t>(stream), flops);
+}
+
 int lin_check_device(lin_ctx* ctx, void* stream) {
     if (!ctx) return LIN_ERR_ARG;
     lin::DeviceGuard guard(ctx->device);
