@@ -278,13 +278,21 @@ LIN_API int lin_clear_plan_overrides(lin_ctx* ctx);
 LIN_API int lin_check_device(lin_ctx* ctx, void* stream);
 
 /* Context options (lin_set_option).
- * LIN_OPT_EARLY_START (default 0): whether a call may start before the
- *   previous kernel on its stream has finished (programmatic dependent launch).
- *   0: no; every call waits for all earlier work on the stream, like any
- *      stream-ordered library.
- *   1: the call is launched as a programmatic dependent of the previous kernel;
- *      its prologue overlaps that kernel's tail, and W and bias may be read
- *      before that kernel has finished. X is read, and Y written, only after it.
+ * LIN_OPT_PROGRAMMATIC_LAUNCH (default 1): calls are launched as programmatic
+ *   dependents of the previous kernel on their stream: a call's CTAs may start
+ *   on SMs as the previous kernel's CTAs leave them, set up (barriers, tensor
+ *   memory, descriptors) and ask the L2 cache to fetch their first operand
+ *   tiles, and then wait (griddepcontrol.wait) until that kernel has finished
+ *   and its writes are visible before they read anything. An L2 prefetch
+ *   returns no data to the kernel and L2 is where all writes meet, so this
+ *   changes no result whatever the previous kernel writes. 0 = plain stream
+ *   order (the CTAs start only after all earlier work has finished).
+ * LIN_OPT_EARLY_START (default 0): which operands may be READ before the
+ *   previous kernel on the stream has finished (needs programmatic launch).
+ *   0: none; every call reads its operands only after all earlier work on the
+ *      stream, like any stream-ordered library.
+ *   1: W and bias may be read before that kernel has finished. X is read, and
+ *      Y written, only after it.
  *   2: as 1, and X may be read early too.
  *   The library only sees its own calls: it drops the early reads of W / bias
  *   (and X) by itself when they overlap the previous library call's output on
@@ -305,7 +313,8 @@ LIN_API int lin_check_device(lin_ctx* ctx, void* stream);
  *   (lin_set_plan_override) and lin_forward_plan are never adapted. */
 typedef enum {
     LIN_OPT_EARLY_START = 1,
-    LIN_OPT_ADAPTIVE_PLANS = 2
+    LIN_OPT_ADAPTIVE_PLANS = 2,
+    LIN_OPT_PROGRAMMATIC_LAUNCH = 3
 } lin_option;
 
 /* The plan of the last call launched through this context (host value, no

@@ -84,7 +84,7 @@ def test_dispatch_skinny_for_small_m_bf16():
     for M in (2, 5, 8, 16):  # (one row with X fitting in shared memory: the GEMV)
         p = tll.plan_query(SM, M, 4096, 4096, "bf16")
         assert kname(p) == "skinny" and p.splits > 1 and p.grid_y == p.splits
-        assert p.grid_x * p.bn >= 4096 and p.grid_x * p.grid_y <= SM
+        assert p.grid_x * p.bn >= 4096 and p.grid_x * p.grid_y <= 2 * SM  # two CTAs per SM
     assert kname(tll.plan_query(SM, 17, 4096, 4096, "bf16")) == "tc"
 
 
@@ -134,14 +134,14 @@ def test_skinny_needs_no_workspace():
 
 
 def test_plan_make_families():
-    for v in range(4):
+    for v in range(5):
         for s in (1, 2, 4, 8):
             p = tll.plan_make(SM, tll.KERNEL_SKINNY, v, s, 16, 4096, 4096, "bf16")
             assert p.splits == s and p.grid_y == s and p.grid_x == 32
     with pytest.raises(tll.LinError):
         tll.plan_make(SM, tll.KERNEL_SKINNY, 0, 3, 16, 4096, 4096, "bf16")
     with pytest.raises(tll.LinError):
-        tll.plan_make(SM, tll.KERNEL_SKINNY, 4, 0, 16, 4096, 4096, "bf16")
+        tll.plan_make(SM, tll.KERNEL_SKINNY, 5, 0, 16, 4096, 4096, "bf16")
     with pytest.raises(tll.LinError):
         tll.plan_make(SM, tll.KERNEL_SKINNY, 0, 0, 17, 4096, 4096, "bf16")
     with pytest.raises(tll.LinError):
@@ -266,10 +266,12 @@ def test_autotune_features_and_residual_fit():
 
 
 def test_skinny_ring_for_many_row_tiles():
-    """More 128-row tiles of W than SMs: the 96 KB ring (two CTAs per SM)."""
+    """More 128-row tiles of W than SMs: the 6 x 1 ring (two CTAs per SM)
+    without a split; otherwise the 5 x 1 ring split over a cluster."""
     p = tll.plan_query(SM, 8, 50257, 768, "bf16")
     assert kname(p) == "skinny" and p.variant == 1 and p.splits == 1
-    assert tll.plan_query(SM, 16, 4096, 4096, "bf16").variant == 0
+    p = tll.plan_query(SM, 16, 4096, 4096, "bf16")
+    assert p.variant == 4 and p.splits == 8
 
 
 def test_autotune_save_format(tmp_path):

@@ -39,7 +39,7 @@ def all_plans(ctx, M, N, K, precision):
     plans = []
     sm = ctx.sm_count
     if precision == BF16 and M <= 16:
-        for v in range(4):
+        for v in range(5):
             for s in (0, 1, 2, 8):
                 plans.append(tll.plan_make(sm, tll.KERNEL_SKINNY, v, s, M, N, K, "bf16"))
     if precision in (BF16, TF32):
@@ -557,7 +557,7 @@ def test_skinny_bits_independent_of_split(ctx, K):
     shape of the summation tree: every split gives the same bits (so the
     library may choose the split per call without changing results)."""
     X, W, b = si.make_inputs(si.Layer("split_inv", 16, 1024, K, BF16, bias=True))
-    for v in range(4):
+    for v in range(5):
         outs = [run(X, W, b, BF16, plan=tll.plan_make(ctx.sm_count, tll.KERNEL_SKINNY, v, cl, 16, 1024, K, "bf16"),
                     ctx=ctx) for cl in (1, 2, 4, 8)]
         for o in outs[1:]:

@@ -59,7 +59,7 @@ def _family_plans(sm, M, N, K, prec):
     out = []
     menu = []
     if prec == "bf16":
-        menu += [(tll.KERNEL_SKINNY, v, s) for v in range(4) for s in (0, 1, 2, 4, 8)]
+        menu += [(tll.KERNEL_SKINNY, v, s) for v in range(5) for s in (0, 1, 2, 4, 8)]
     if prec in ("bf16", "tf32"):
         menu += [(tll.KERNEL_TC, v, w) for v in range(6) for w in (0, 1, 3, sm)]
         menu += [(tll.KERNEL_TC, v, -c) for v in range(3) for c in (1, 2, 5)]
@@ -121,9 +121,10 @@ def _cdiv(a, b):
 
 
 def test_skinny_cluster_rule():
-    """Isolated skinny calls take the largest cluster (a power of two, at most
-    8) that keeps one CTA per SM and at least one K stage per CTA; the 96 KB
-    ring when W has more 128-row tiles than SMs."""
+    """Skinny calls take the 5 x 1 ring (two CTAs per SM) and the largest
+    cluster (a power of two, at most 8) that keeps the grid within two CTAs per
+    SM and at least two K stages per CTA; the 6 x 1 ring without a split when W
+    has more 128-row tiles than SMs."""
     for sm in SMS:
         for M in (2, 8, 16):
             for N in (136, 768, 4096, 16384, 50257):
@@ -131,10 +132,13 @@ def test_skinny_cluster_rule():
                     p = tll.plan_query(sm, M, N, K, "bf16")
                     assert p.kernel == tll.KERNEL_SKINNY
                     tiles = _cdiv(N, 128)
-                    assert p.variant == (1 if tiles > sm else 0)
-                    kblocks = _cdiv(K, 64 * (4 if p.variant == 0 else 1))
+                    if tiles > sm:
+                        assert p.variant == 1 and p.splits == 1, (sm, M, N, K, p)
+                        continue
+                    assert p.variant == 4
+                    kblocks = _cdiv(K, 64)
                     S = 1
-                    while S < 8 and tiles * S * 2 <= sm and 2 * S <= kblocks:
+                    while S < 8 and tiles * S * 2 <= 2 * sm and 2 * S <= kblocks:
                         S *= 2
                     assert p.splits == S and p.grid_x == tiles and p.grid_y == S, (sm, M, N, K, p)
 

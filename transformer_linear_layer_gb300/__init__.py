@@ -31,6 +31,7 @@ KERNEL_NONE, KERNEL_FILL, KERNEL_SKINNY, KERNEL_FFMA, KERNEL_TC, KERNEL_GEMV = 0
 KERNEL_NAMES = {0: "none", 1: "fill", 2: "skinny", 3: "ffma", 4: "tc", 5: "gemv"}
 OPT_EARLY_START = 1
 OPT_ADAPTIVE_PLANS = 2
+OPT_PROGRAMMATIC_LAUNCH = 3
 # LIN_OPT_EARLY_START levels: nothing before the previous kernel finishes (the
 # default); W and bias may be read early; X too (only when no other work on the
 # stream writes a call's inputs between library calls).

@@ -75,7 +75,7 @@ def candidates(sm_count: int, M: int, N: int, K: int, precision, workspace_bytes
             out.append(p)
 
     if prec == PREC_BF16 and M <= 16:
-        for v in range(4):
+        for v in range(5):  # the skinny kernel's ring variants
             for s in (1, 2, 4, 8):
                 add(KERNEL_SKINNY, v, s)
     if prec in (PREC_BF16, PREC_TF32):

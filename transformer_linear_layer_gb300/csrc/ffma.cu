@@ -48,6 +48,7 @@ struct FfmaArgs {
     int splits;
     int nkb;           // ceil(K / BK)
     int early_inputs;  // X and W may be read before the dependency wait (not the previous call's output)
+    int prefetch;      // otherwise ask the L2 for the first slices of them before the wait
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
@@ -160,7 +161,23 @@ ffma_kernel(const FfmaArgs a) {
     const int kb_end = (int)((long long)(split + 1) * a.nkb / a.splits);
     const int nk = kb_end - kb_begin;
     if (tid == 0) pdl_launch_dependents();
-    if (!a.early_inputs) pdl_wait();  // X or W may be the previous kernel's output
+    if (!a.early_inputs) {
+        // X or W may be the previous kernel's output: read nothing before the
+        // wait, but have the L2 fetch the first ring's worth of this CTA's rows
+        // (one bulk prefetch per row; no data comes back before the wait).
+        if (a.prefetch && nk > 0) {
+            const int k0 = kb_begin * BK;
+            const int k1 = (kb_begin + STAGES - 1 < kb_end ? kb_begin + STAGES - 1 : kb_end) * BK;
+            const unsigned bytes = (unsigned)((k1 < a.K ? k1 : a.K) - k0) * 4u;
+            const int r = tid < BM ? m0 + tid : n0 + tid - BM;
+            const bool is_x = tid < BM;
+            if (tid < BM + BN && r < (is_x ? a.M : a.N) && bytes > 0) {
+                const float* src = (is_x ? a.X : a.W) + (size_t)r * a.K + k0;
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+            }
+        }
+        pdl_wait();
+    }
 
     float acc[TM][TN];
 #pragma unroll
@@ -301,6 +318,7 @@ int launch_ffma(const Problem& p, const lin_plan& plan) {
     a.splits = plan.splits;
     a.nkb = (p.K + plan.bk - 1) / plan.bk;
     a.early_inputs = (p.early_start && p.early_x) ? 1 : 0;
+    a.prefetch = p.early_start ? 1 : 0;
     a.ws = nullptr;
     a.counters = nullptr;
     if (plan.splits > 1) {

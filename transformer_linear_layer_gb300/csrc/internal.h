@@ -30,11 +30,14 @@ struct Problem {
     size_t workspace_bytes = 0;
     int* dev_status = nullptr;    // device status word (LIN_ERR_DEVICE_TIMEOUT when a wait gave up)
     int sm_count = 0;
-    // The kernel may start before the previous kernel on the stream finishes
-    // (programmatic dependent launch). early_start: W and bias do not overlap
-    // that kernel's output, so they may be read before the dependency wait;
-    // early_x: neither does X. Y is written only after the wait.
+    // early_start: launch as a programmatic dependent of the previous kernel on
+    // the stream (the CTAs may start before it finishes; nothing is read before
+    // griddepcontrol.wait unless early_w / early_x say so; L2 prefetches of the
+    // operands may be issued before it). early_w: W and bias do not overlap that
+    // kernel's output and may be read before the wait; early_x: neither does X.
+    // Y is written only after the wait.
     bool early_start = false;
+    bool early_w = false;
     bool early_x = false;
 };
 
@@ -53,8 +56,12 @@ inline float* splitk_partials(void* ws) { return reinterpret_cast<float*>(static
 
 // Tile configurations per kernel family (variant ids in lin_plan).
 struct SkinnyCfg { int stages, kbox; };           // 128 W rows per cluster; splits = cluster size
-constexpr int kSkinnyVariants = 4;
-constexpr SkinnyCfg kSkinnyCfg[kSkinnyVariants] = {{3, 4}, {6, 1}, {3, 2}, {4, 3}};
+constexpr int kSkinnyVariants = 5;
+// Ring (stages x boxes of 64 K): 0 = 3 x 4 (~200 KB, one CTA per SM), 1 = 6 x 1
+// (~110 KB), 2 = 3 x 2, 3 = 4 x 3, 4 = 5 x 1 (~99 KB with the cluster inbox:
+// two CTAs per SM, so a call's CTAs can start while the previous call's run).
+constexpr SkinnyCfg kSkinnyCfg[kSkinnyVariants] = {{3, 4}, {6, 1}, {3, 2}, {4, 3}, {5, 1}};
+constexpr int kSkinnyTwoPerSm = 4;                 // the variant two CTAs of which fit on an SM
 constexpr int kSkinnyThreads = 192;                // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 
 struct FfmaCfg { int bm, bn, bk, tm, tn; };        // 256 threads each
@@ -136,7 +143,7 @@ struct BwdProblem {
     cudaStream_t stream = nullptr;
     int* dev_status = nullptr;
     int sm_count = 0;
-    bool early_start = false;      // may start before the previous kernel on the stream finishes
+    bool early_start = false;      // programmatic launch: may start (not read) before the previous kernel finishes
     bool early_x = false;          // and read dZ and B before it finishes
     void* workspace = nullptr;     // context workspace (K split of small outputs)
     size_t workspace_bytes = 0;

@@ -34,6 +34,7 @@ struct lin_ctx {
     size_t workspace_bytes;
     int* dev_status;
     int early_level;   // LIN_OPT_EARLY_START: 0 none, 1 W and bias, 2 also X
+    bool programmatic; // LIN_OPT_PROGRAMMATIC_LAUNCH
     bool adaptive;     // LIN_OPT_ADAPTIVE_PLANS
     lin_plan last_plan;
     std::mutex override_mu;
@@ -74,9 +75,11 @@ int make_skinny(int sm, int variant, int splits, int M, int N, int K, size_t /*w
     int S = splits;
     if (S <= 0) {
         // Cluster split-K: the largest power of two (<= 8, the portable cluster
-        // size) keeping the grid within one CTA per SM, and >= 1 K stage per CTA.
+        // size) keeping the grid within the CTAs the SMs hold at once (one per SM,
+        // two for the small ring), with >= 2 K stages per CTA.
+        const long long slots = variant == kSkinnyTwoPerSm ? 2LL * sm : (long long)sm;
         S = 1;
-        while (S < 8 && (long long)tiles * S * 2 <= sm && 2 * S <= kblocks) S *= 2;
+        while (S < 8 && (long long)tiles * S * 2 <= slots && 2 * S <= kblocks) S *= 2;
     }
     if (S != 1 && S != 2 && S != 4 && S != 8) return LIN_ERR_UNSUPPORTED;
     plan_common(p, LIN_KERNEL_SKINNY, variant);
@@ -277,10 +280,12 @@ int plan_default(int sm, int M, int N, int K, int precision, size_t ws, lin_plan
             // everywhere else (4 x 50257 x 768: 12.1 against 41.5 us; one row
             // of 50257: 11.9 against 14.3 us; one row of 2304: 1.9 against 1.3 us).
             if (M == 1 && ceil_div(N, 128) <= sm && gemv_fits(M, K, true)) return make_gemv(sm, 0, M, N, K, true, p);
-            // More row tiles than SMs: the 96 KB ring (two CTAs per SM) instead
-            // of the 192 KB one, so the tiles run in fewer waves (measured on
-            // the last token's logits, 50257 rows: 15.7 -> 12.1 us).
-            if (M <= 16) return make_skinny(sm, ceil_div(N, 128) > sm ? 1 : 0, 0, M, N, K, ws, p);
+            // More row tiles than SMs: the 6 x 1 ring (two CTAs per SM) without a
+            // split, so the tiles run in fewer waves (measured on the last
+            // token's logits, 50257 rows: 15.7 -> 12.1 us). Otherwise the 5 x 1
+            // ring split over a cluster (two CTAs per SM): the next call's CTAs
+            // start beside this call's and stream their W into L2 meanwhile.
+            if (M <= 16) return make_skinny(sm, ceil_div(N, 128) > sm ? 1 : kSkinnyTwoPerSm, 0, M, N, K, ws, p);
             return make_tc(sm, -1, 0, false, M, N, K, 2, p, ws);
         case LIN_PREC_TF32:
             // A few rows are a weight stream: the exact-fp32 GEMV is as fast as
@@ -470,15 +475,16 @@ int run(lin_ctx* ctx, const lin_plan& plan_in, int M, int N, int K, const void* 
     bool w_ok = false, x_ok = false, known = false;
     early_reads_ok(p.stream, Range{W, (size_t)N * K * ein}, Range{bias, bias ? (size_t)N * 4 : 0},
                    Range{X, (size_t)M * K * ein}, Range{Y, ybytes}, &w_ok, &x_ok, &known);
-    p.early_start = ctx->early_level >= 1 && w_ok;
-    p.early_x = p.early_start && ctx->early_level >= 2 && x_ok;
+    p.early_start = ctx->programmatic;
+    p.early_w = p.early_start && ctx->early_level >= 1 && w_ok;
+    p.early_x = p.early_w && ctx->early_level >= 2 && x_ok;
     // An independent call right after another call on this stream overlaps it:
     // the skinny stream then needs no K split to fill the SMs (the concurrent
     // calls do), and skipping the split saves its reduction.
     if (adaptive && ctx->adaptive && known && p.early_x && plan.kernel == LIN_KERNEL_SKINNY && plan.splits > 1) {
         lin_plan narrow;
-        if (make_skinny(ctx->sm_count, plan.variant, 1, M, N, K, ctx->workspace_bytes, &narrow) == LIN_OK)
-            plan = narrow;
+        const int v = plan.variant == kSkinnyTwoPerSm ? 0 : plan.variant;  // the deep ring for a lone cluster
+        if (make_skinny(ctx->sm_count, v, 1, M, N, K, ctx->workspace_bytes, &narrow) == LIN_OK) plan = narrow;
     }
     // Likewise a tensor-core K split (measured: it helps an isolated call and
     // costs a back-to-back one).
@@ -555,6 +561,7 @@ int lin_create(lin_ctx** out, int device, size_t max_workspace_bytes) {
     if (!c) return LIN_ERR_CUDA;
     c->device = device;
     c->early_level = 0;
+    c->programmatic = true;
     c->adaptive = true;
     std::memset(&c->last_plan, 0, sizeof(c->last_plan));
     c->workspace_bytes = max_workspace_bytes ? max_workspace_bytes : ((size_t)64 << 20);
@@ -602,6 +609,10 @@ int lin_set_option(lin_ctx* ctx, int option, long long value) {
         case LIN_OPT_ADAPTIVE_PLANS:
             if (value != 0 && value != 1) return LIN_ERR_ARG;
             ctx->adaptive = value != 0;
+            return LIN_OK;
+        case LIN_OPT_PROGRAMMATIC_LAUNCH:
+            if (value != 0 && value != 1) return LIN_ERR_ARG;
+            ctx->programmatic = value != 0;
             return LIN_OK;
         default: return LIN_ERR_ARG;
     }
@@ -747,8 +758,8 @@ int backward_setup(lin_ctx* ctx, int which, int M, int N, int K, const void* dZ,
     bool w_ok = false, x_ok = false, known = false;
     early_reads_ok(q->stream, Range{B, b_bytes}, Range{nullptr, 0}, Range{dZ, dz_bytes}, Range{out, out_bytes}, &w_ok,
                    &x_ok, &known);
-    q->early_start = ctx->early_level >= 1 && w_ok;
-    q->early_x = q->early_start && ctx->early_level >= 2 && x_ok;
+    q->early_start = ctx->programmatic;
+    q->early_x = q->early_start && ctx->early_level >= 1 && w_ok && ctx->early_level >= 2 && x_ok;
     q->workspace = ctx->workspace;
     q->workspace_bytes = ctx->workspace_bytes;
     // Right after an independent call the two overlap (early start) and fill
@@ -850,7 +861,7 @@ int lin_gelu_backward(lin_ctx* ctx, long long count, const void* dY, const void*
     bool w_ok = false, x_ok = false, known = false;
     early_reads_ok(st, Range{Z, bytes}, Range{nullptr, 0}, Range{dY, bytes}, Range{dZ, bytes}, &w_ok, &x_ok, &known);
     return launch_gelu_backward(count, dY, Z, dZ, precision == LIN_PREC_BF16, ctx->sm_count, st,
-                                ctx->early_level >= 1);
+                                ctx->programmatic);
 }
 
 int lin_fold_layernorm(lin_ctx* ctx, int N, int K, const float* W, const float* bias, const float* gamma,

@@ -28,12 +28,16 @@
 //   every cluster size - bitwise identical across split choices and runs (the
 //   fixed-order reduction of "Optimizing a GPT-2-class transformer on a GPU",
 //   Act I). No global workspace.
-// * Programmatic dependent launch: the W copies of the first STAGES tiles are
-//   issued before griddepcontrol.wait, so a layer's weight stream starts while
-//   the previous kernel on the stream drains. X is read before the wait too
-//   when it is not the previous call's output (independent layers then stream
-//   concurrently); a chained layer (X = previous Y) reads X after it. Bias and
-//   Y are touched only after the wait. The host checks those overlaps.
+// * Programmatic dependent launch: a call's CTAs start as the previous
+//   kernel's CTAs leave the SMs and, before griddepcontrol.wait, ask the L2 to
+//   fetch this CTA's whole share of W and X (an L2 prefetch returns nothing to
+//   the SM, so it is safe whatever the previous kernel writes): HBM keeps
+//   streaming across the call boundary, and after the wait the copies into
+//   shared memory hit the L2. When the caller allows it (the host checks that
+//   W does not overlap the previous call's output), the W copies of the first
+//   STAGES stages go straight to shared memory before the wait, and X too when
+//   it is not the previous call's output (independent layers then stream
+//   concurrently). Bias, the residual and Y are touched only after the wait.
 #include "internal.h"
 #include "device_common.cuh"
 #include "tc_common.cuh"
@@ -48,7 +52,9 @@ struct SkinnyArgs {
     const uint16_t* R;  // residual added after the activation (M x N bf16, may be Y itself), or null
     int* status;
     int kblocks;  // ceil(K / (64 * KBOX)): stages of K per 128-row block
-    int early_x;  // X may be read before the dependency wait (it is not the previous call's output)
+    int early_w;  // W may be read before the dependency wait (it is not the previous call's output)
+    int early_x;  // X may be read before the dependency wait (implies early_w)
+    int prefetch; // ask the L2 for this CTA's share of W and X before the dependency wait
 };
 
 constexpr int kSkSegs = 8;    // K segments: the fixed shape of the summation tree
@@ -196,15 +202,43 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
                     tma_load_2d(smem_u32(sX + s * XB + b * kSkXBox), &tmX, full0 + 8 * s, ((kb0 + i) * KBOX + b) * 64,
                                 0);
             };
+            // L2 prefetch of stages [from, nkb): boxes past K are skipped.
+            auto prefetch = [&](int from, bool w, bool x) {
+                for (int i = from; i < nkb; ++i)
+#pragma unroll
+                    for (int b = 0; b < KBOX; ++b) {
+                        const int kx = ((kb0 + i) * KBOX + b) * 64;
+                        if (kx >= a.K) break;
+                        if (w) tma_prefetch_l2_2d(&tmW, kx, n0);
+                        if (x) tma_prefetch_l2_2d(&tmX, kx, 0);
+                    }
+            };
             const int pre = nkb < STAGES ? nkb : STAGES;
-            for (int i = 0; i < pre; ++i) {
-                mbar_expect_tx(full0 + 8 * i, WB + XB);
-                load_w(i);
-                if (a.early_x) load_x(i);
-            }
-            if (!a.early_x) {
+            if (a.early_w) {
+                // W (and X when allowed) straight into the ring; the rest of the
+                // share to L2 while the previous kernel finishes.
+                for (int i = 0; i < pre; ++i) {
+                    mbar_expect_tx(full0 + 8 * i, WB + XB);
+                    load_w(i);
+                    if (a.early_x) load_x(i);
+                }
+                if (a.prefetch) {
+                    prefetch(pre, true, a.early_x);
+                    if (!a.early_x) prefetch(0, false, true);
+                }
+                if (!a.early_x) {
+                    pdl_wait();
+                    for (int i = 0; i < pre; ++i) load_x(i);
+                }
+            } else {
+                // Nothing is read before the wait: the share goes to L2 meanwhile.
+                if (a.prefetch) prefetch(0, true, true);
                 pdl_wait();
-                for (int i = 0; i < pre; ++i) load_x(i);
+                for (int i = 0; i < pre; ++i) {
+                    mbar_expect_tx(full0 + 8 * i, WB + XB);
+                    load_w(i);
+                    load_x(i);
+                }
             }
             int issued = pre;
             for (int i = pre; i < nkb; ++i) {
@@ -259,6 +293,21 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
         pdl_wait();
         const int q = warp & 3;
         const int row = q * 32 + lane;
+        const int M = a.M, N = a.N;
+        // The bias and residual values this thread adds, fetched while the
+        // accumulators fill. Without a cluster split a thread finishes its W row
+        // n for every batch row; with one it finishes PER outputs of one column
+        // (128 threads, a multiple of the COLS columns this CTA finishes).
+        static_assert(CL == 1 || 128 % COLS == 0, "columns per finishing thread");
+        constexpr int PER = CL == 1 ? kSkMP : kSkMP * COLS / 128;
+        const int t = threadIdx.x - 64;
+        const int n_out = CL == 1 ? n0 + row : n0 + (int)rank * COLS + t % COLS;
+        auto m_out = [&](int e) { return CL == 1 ? e : (t + 128 * e) / COLS; };
+        const float b_out = (a.bias && n_out < N) ? __ldg(a.bias + n_out) : 0.f;
+        float r_out[PER];
+#pragma unroll
+        for (int e = 0; e < PER; ++e)
+            r_out[e] = (a.R && m_out(e) < M && n_out < N) ? bf16_bits_to_f32(a.R[(size_t)m_out(e) * N + n_out]) : 0.f;
         Vec16 v = {};
         if (nkb > 0) {
             const bool mine = mbar_wait(accum_bar, 0);
@@ -272,18 +321,12 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
                 });
             }
         }
-        const int M = a.M, N = a.N;
         if constexpr (CL == 1) {
-            const int n = n0 + row;
+            const int n = n_out;
             if (n < N) {
-                const float b = a.bias ? __ldg(a.bias + n) : 0.f;
 #pragma unroll
                 for (int m = 0; m < kSkMP; ++m)
-                    if (m < M) {
-                        const size_t i = (size_t)m * N + n;
-                        const float r = a.R ? bf16_bits_to_f32(a.R[i]) : 0.f;
-                        a.Y[i] = f32_to_bf16_bits(epilogue<GELU, true>(v.x[m], b) + r);
-                    }
+                    if (m < M) a.Y[(size_t)m * N + n] = f32_to_bf16_bits(epilogue<GELU, true>(v.x[m], b_out) + r_out[m]);
             }
         } else {
             // Push this row's partial sums into the inbox of the CTA that finishes it,
@@ -296,21 +339,15 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
             for (int m = 0; m < kSkMP; ++m) dsmem_st_f32(dst + (uint32_t)(m * COLS * 4), v.x[m]);
             mbar_arrive_remote(dsmem_map(inbox_bar, owner));
             // Finish this CTA's columns: the CL partial sums added in rank order.
-            const int t = threadIdx.x - 64;
             const bool ok = mbar_wait_cluster(inbox_bar, 0);
             if (!ok) give_up();
-            constexpr int PER = kSkMP * COLS / 128;  // outputs per thread
+            const int c = t % COLS;
 #pragma unroll
             for (int e = 0; e < PER; ++e) {
-                const int idx = t + 128 * e;
-                const int m = idx / COLS, c = idx % COLS;
-                const int n = n0 + (int)rank * COLS + c;
-                if (ok && m < M && n < N) {
+                const int m = m_out(e);
+                if (ok && m < M && n_out < N) {
                     const float acc = tree_of_ranks<CL>(inbox + m * COLS + c, kSkMP * COLS, 0);
-                    const float b = a.bias ? __ldg(a.bias + n) : 0.f;
-                    const size_t i = (size_t)m * N + n;
-                    const float r = a.R ? bf16_bits_to_f32(a.R[i]) : 0.f;
-                    a.Y[i] = f32_to_bf16_bits(epilogue<GELU, true>(acc, b) + r);
+                    a.Y[(size_t)m * N + n_out] = f32_to_bf16_bits(epilogue<GELU, true>(acc, b_out) + r_out[e]);
                 }
             }
         }
@@ -389,7 +426,9 @@ int launch_skinny(const Problem& p, const lin_plan& plan) {
     a.R = static_cast<const uint16_t*>(p.residual);
     a.status = p.dev_status;
     a.kblocks = (p.K + 64 * kSkinnyCfg[plan.variant].kbox - 1) / (64 * kSkinnyCfg[plan.variant].kbox);
+    a.early_w = p.early_w ? 1 : 0;
     a.early_x = p.early_x ? 1 : 0;
+    a.prefetch = p.early_start ? 1 : 0;  // useful only when the CTAs can start before the wait ends
     const bool gelu = p.epilogue == LIN_EPI_GELU_TANH;
 #define LIN_SKINNY_CASE(V)                                                                                 \
     case V:                                                                                                \
@@ -402,6 +441,7 @@ int launch_skinny(const Problem& p, const lin_plan& plan) {
         LIN_SKINNY_CASE(1)
         LIN_SKINNY_CASE(2)
         LIN_SKINNY_CASE(3)
+        LIN_SKINNY_CASE(4)
         default: return LIN_ERR_UNSUPPORTED;
     }
 #undef LIN_SKINNY_CASE

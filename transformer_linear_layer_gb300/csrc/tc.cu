@@ -47,6 +47,7 @@ struct TcArgs {
     int y_aligned16;     // Y's base is 16-byte aligned (vector stores allowed)
     int bias_aligned16;  // bias is 16-byte aligned (vector loads allowed)
     int early_inputs;    // X and W may be read before the dependency wait (not the previous call's output)
+    int prefetch;        // otherwise ask the L2 for the first ring's worth of them before the wait
     int y_tma;           // bf16 Y stored by TMA from 32 x 32 boxes (16-byte aligned rows)
     float* partials;     // stream-K: one 128 x BN fp32 slot per CTA boundary; K split: one per (tile, split)
     unsigned* flags;     // stream-K: 8 hand-over flags per CTA boundary; K split: 8 counters per tile
@@ -236,7 +237,21 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     if (warp == 0) {
         if (lane == 0) {
             // ---- TMA producer: the K stages of this CTA's tiles, in order ----
-            if (!a.early_inputs) pdl_wait();
+            if (!a.early_inputs) {
+                // The first ring's worth of operands to L2 while the previous
+                // kernel finishes (no data comes back before the wait).
+                if (LAY == 0 && a.prefetch) {
+                    int t0, l0, h0;
+                    if (seg(0, t0, l0, h0)) {
+                        const int m0 = tile_m0(t0), nb0 = tile_n0(t0) + (int)rank * BROWS;
+                        for (int kb = l0; kb < h0 && kb < l0 + STAGES; ++kb) {
+                            if (m0 < a.M) tma_prefetch_l2_2d(&tmA, kb * BK, m0);
+                            if (nb0 < a.N) tma_prefetch_l2_2d(&tmB, kb * BK, nb0);
+                        }
+                    }
+                }
+                pdl_wait();
+            }
             uint32_t it = 0, issued = 0;
             bool ok = true;
             int tile, lo, hi;
@@ -820,6 +835,7 @@ int launch_tc_backward(const BwdProblem& q) {
     a.y_aligned16 = (reinterpret_cast<uintptr_t>(q.out) % 16) == 0;
     a.bias_aligned16 = 0;
     a.early_inputs = q.early_x ? 1 : 0;
+    a.prefetch = 0;
     a.partials = nullptr;
     a.flags = nullptr;
     a.aux = q.which == 1 ? q.aux : nullptr;
@@ -862,6 +878,7 @@ int launch_tc(const Problem& p, const lin_plan& plan) {
     a.y_aligned16 = (reinterpret_cast<uintptr_t>(p.Y) % 16) == 0;
     a.bias_aligned16 = (reinterpret_cast<uintptr_t>(p.bias) % 16) == 0;
     a.early_inputs = (p.early_start && p.early_x) ? 1 : 0;
+    a.prefetch = p.early_start ? 1 : 0;
     a.aux = p.residual;
     a.aux_mode = p.residual ? 1 : 0;
     a.aux_vec = (reinterpret_cast<uintptr_t>(p.residual) % 16) == 0 && ((size_t)p.N * (bf16 ? 2 : 4)) % 16 == 0;

@@ -75,6 +75,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Ask the L2 cache to fetch the box at (x, y) of a tensor map (no data comes
+// back to the SM; the L2 is where all writes meet, so a prefetch issued before
+// griddepcontrol.wait changes no result, whatever the previous kernel writes).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y)
+                 : "memory");
+}
+
 // SM-pair form (cta_group::2) of the TMA load: the box lands in this CTA's
 // shared memory and completes the mbarrier at `bar_cluster`, a shared::cluster
 // address that may lie in the peer CTA of the pair.
