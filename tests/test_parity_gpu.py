@@ -146,6 +146,31 @@ def test_tc_midsize_full(ctx, precision):
             check_layer(layer, plan=plan, ctx=ctx)
 
 
+@pytest.mark.parametrize("r", range(1, 8))
+def test_unaligned_rows_bf16(ctx, r):
+    """bf16 Y with rows that are not 16-byte aligned (N = 8q + r): the row
+    segments of a chunk start at every misalignment, and the vector-store
+    epilogue must write each element once and nothing beyond the row, on the
+    single-CTA and SM-pair 256-column tiles (several tiles, a ragged M and the
+    matrix's last column chunk), with and without GELU."""
+    N = 1024 + 256 + r
+    for M, K, epi in ((300, 256, si.EPI_GELU), (131, 320, si.EPI_NONE)):
+        layer = si.Layer("unaligned", M, N, K, BF16, epi, bias=True)
+        for v in (0, 3):
+            plan = tll.plan_make(ctx.sm_count, tll.KERNEL_TC, v, 0, M, N, K, "bf16")
+            check_layer(layer, plan=plan, ctx=ctx)
+    # the neighbours of Y are untouched
+    X, W, b = si.make_inputs(si.Layer("unaligned_guard", 130, N, 256, BF16, bias=True))
+    x, w, bias = device_inputs(X, W, b, BF16)
+    big = torch.full((130 * N + 64,), 7.0, dtype=torch.bfloat16, device="cuda")
+    y = big[16:16 + 130 * N].view(130, N)  # 32-byte offset: 16-byte aligned base
+    tll.forward(x, w, bias, precision="bf16", out=y, ctx=ctx)
+    torch.cuda.synchronize()
+    assert bool((big[:16] == 7.0).all()) and bool((big[16 + 130 * N:] == 7.0).all())
+    ref = oracle.linear(X, W, b)
+    assert oracle.rel_err(y.double().cpu().numpy(), ref) <= oracle.TOL[BF16]
+
+
 # ------------------------------------------------------------- edge shapes
 
 @pytest.mark.parametrize("M", [1, 2, 15, 16, 17, 127, 129])

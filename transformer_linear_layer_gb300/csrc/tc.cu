@@ -67,8 +67,12 @@ template <bool BF16>
 constexpr int stage_row_bytes() { return BF16 ? 32 * 2 + 16 : 32 * 4 + 16; }
 template <bool BF16>
 constexpr int stage_rows() { return BF16 ? 32 : 16; }
+// Per warp: its rows, plus (bf16) 16 bytes after every 8 rows, which spreads the
+// shifted row writes of the unaligned-row store path over the banks.
 template <bool BF16>
-constexpr int stage_bytes() { return 8 * stage_rows<BF16>() * stage_row_bytes<BF16>(); }
+constexpr int stage_warp_bytes() { return stage_rows<BF16>() * stage_row_bytes<BF16>() + (BF16 ? 64 : 0); }
+template <bool BF16>
+constexpr int stage_bytes() { return 8 * stage_warp_bytes<BF16>(); }
 // Bias staging: each epilogue warp keeps the bias of its BN/2 columns of the
 // current tile in shared memory (8 warps x BN/2 floats).
 template <int BN>
@@ -120,7 +124,10 @@ constexpr size_t tc_smem_bytes() {
 // in the layout that makes staging a vector copy, choose the fragment layout
 // to match); nothing is transposed in memory. An MN-major stage is one box of
 // 64 (MN) x 64 (K rows) per 64 rows or columns of the tile.
-template <bool BF16, int BN, bool GELU, bool PAIR, bool SK, int LAY>
+// YODD: bf16 Y whose rows are not 16-byte aligned (N not a multiple of 8)
+// leaves by the shifted-staging vector stores below (a separate instantiation,
+// so that the other paths keep their registers).
+template <bool BF16, int BN, bool GELU, bool PAIR, bool SK, int LAY, bool YODD = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
           const __grid_constant__ CUtensorMap tmY, const TcArgs a) {
@@ -366,7 +373,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         constexpr int RP = stage_rows<BF16>();
         constexpr int ESZO = BF16 ? 2 : 4;
         constexpr int LPR = 32 * ESZO / 16;  // lanes per row with 16-byte pieces
-        uint8_t* st = sOut + ew * RP * RB;
+        uint8_t* st = sOut + ew * stage_warp_bytes<BF16>();
 
         // One 32 x 32 chunk: bias, activation, convert; lane = row. The values go
         // through this warp's staging tile (rows [h*RP, h*RP + RP) per pass) and
@@ -459,6 +466,65 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                         tma_store_2d(&tmY, smem_u32(box), nb, mrow0);
                         bulk_commit();
                     }
+                    return;
+                }
+                if (YODD && full && a.y_aligned16 && (N * ESZO) % 16 != 0) {
+                    // Rows that are not 16-byte aligned (N not a multiple of 8, as
+                    // in a 50257-word LM head): each lane writes its row into the
+                    // staging tile shifted by the row's misalignment s (elements),
+                    // so that the row's 16-byte blocks of Y sit on 16-byte
+                    // boundaries there; the blocks wholly inside this chunk leave
+                    // by vector stores, the few elements of the two partial blocks
+                    // one by one.
+                    auto row_at = [&](int r) { return st + r * RB + (r >> 3) * 16; };
+                    {
+                        uint32_t w[17];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+                        w[16] = 0u;
+                        const long long g = (long long)(mrow0 + lane) * N + nb;
+                        const int s = (int)(g & 7);
+                        const bool odd = (s & 1) != 0;
+                        uint32_t* dst = reinterpret_cast<uint32_t*>(row_at(lane)) + (s >> 1);
+                        // odd s: word k holds elements (2k - 1, 2k) of the chunk
+                        uint32_t prev = 0u;
+#pragma unroll
+                        for (int j = 0; j < 17; ++j) {
+                            dst[j] = odd ? __byte_perm(prev, w[j], 0x5432) : w[j];
+                            prev = w[j];
+                        }
+                    }
+                    __syncwarp();
+                    // Whole blocks: rows x blocks 0..3 of the shifted row (block 0
+                    // only when the row is aligned).
+#pragma unroll
+                    for (int it = 0; it < 4; ++it) {
+                        const int item = it * 32 + lane;
+                        const int r = item >> 2, k = item & 3;
+                        const int m = mrow0 + r;
+                        const long long g = (long long)m * N + nb;
+                        const int s = (int)(g & 7);
+                        if (m < a.M && (k > 0 || s == 0)) {
+                            const uint4 val = *reinterpret_cast<const uint4*>(row_at(r) + 16 * k);
+                            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.Y) + (g - s) + 8 * k) = val;
+                        }
+                    }
+                    // Partial blocks: the first 8 - s and the last s elements of a
+                    // row with s > 0.
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int item = it * 32 + lane;
+                        const int r = item >> 3, idx = item & 7;
+                        const int m = mrow0 + r;
+                        const long long g = (long long)m * N + nb;
+                        const int s = (int)(g & 7);
+                        if (m < a.M && s > 0) {
+                            const int e = idx < 8 - s ? idx : 24 + idx;
+                            static_cast<uint16_t*>(a.Y)[g + e] =
+                                *reinterpret_cast<const uint16_t*>(row_at(r) + 2 * (s + e));
+                        }
+                    }
+                    __syncwarp();  // the staging rows are rewritten by the next chunk
                     return;
                 }
             }
@@ -556,6 +622,19 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             for (int t = lane; t < HALF; t += 32) {
                 const int n = n0 + c_begin + t;
                 sBias[t] = (a.bias && n < N) ? __ldg(a.bias + n) : 0.f;
+            }
+            // The auxiliary tensor's part of this warp's region (one row segment
+            // per lane) to L2 while the MMAs run, so that the epilogue's row loads
+            // of it hit the L2 instead of waiting on HBM.
+            if (a.aux_mode && a.aux_vec) {
+                const int arow = m0 + q * 32 + lane, acol = n0 + c_begin;
+                const int ncols = N - acol < HALF ? N - acol : HALF;
+                if (arow < a.M && ncols > 0) {
+                    const char* src = static_cast<const char*>(a.aux) + ((size_t)arow * N + acol) * (BF16 ? 2 : 4);
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src),
+                                 "r"((unsigned)ncols * (BF16 ? 2u : 4u))
+                                 : "memory");
+                }
             }
             __syncwarp();
             const bool mine = PAIR ? mbar_wait_cluster(tfull0 + 8 * buf, (j >> 1) & 1)
@@ -692,12 +771,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 
 // ---------------------------------------------------------------- host side
 
-template <bool BF16, int BN, bool GELU, bool PAIR, bool SK, int LAY = 0>
+template <bool BF16, int BN, bool GELU, bool PAIR, bool SK, int LAY = 0, bool YODD = false>
 int launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const TcArgs& a, int grid, bool early,
                cudaStream_t st) {
     constexpr size_t smem = tc_smem_bytes<BF16, BN, PAIR>();
     static_assert(tc_smem_bytes<BF16, BN, PAIR>() <= 227 * 1024, "shared memory");
-    auto kern = tc_kernel<BF16, BN, GELU, PAIR, SK, LAY>;
+    auto kern = tc_kernel<BF16, BN, GELU, PAIR, SK, LAY, YODD>;
     static std::atomic<unsigned long long> attr_set{0};  // per instantiation: one bit per device
     if (ensure_smem_attr(attr_set, kern, smem) != LIN_OK) return LIN_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -728,6 +807,8 @@ int launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& 
 template <bool BF16, bool GELU>
 int launch_variant(int variant, bool sk, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty,
                    const TcArgs& a, int grid, bool early, cudaStream_t st) {
+    // Whole tiles of bf16 Y with unaligned rows: the vector-store epilogue.
+    const bool yodd = BF16 && a.ksplits <= 1 && !a.y_tma && a.y_aligned16 && (a.N % 8) != 0;
     if (sk) {
         switch (variant) {
             case 0: return launch_cfg<BF16, kTcCfg[0].bn, GELU, false, true>(ta, tb, ty, a, grid, early, st);
@@ -737,10 +818,14 @@ int launch_variant(int variant, bool sk, const CUtensorMap& ta, const CUtensorMa
         }
     }
     switch (variant) {
-        case 0: return launch_cfg<BF16, kTcCfg[0].bn, GELU, false, false>(ta, tb, ty, a, grid, early, st);
+        case 0:
+            if (BF16 && yodd) return launch_cfg<BF16, kTcCfg[0].bn, GELU, false, false, 0, true>(ta, tb, ty, a, grid, early, st);
+            return launch_cfg<BF16, kTcCfg[0].bn, GELU, false, false>(ta, tb, ty, a, grid, early, st);
         case 1: return launch_cfg<BF16, kTcCfg[1].bn, GELU, false, false>(ta, tb, ty, a, grid, early, st);
         case 2: return launch_cfg<BF16, kTcCfg[2].bn, GELU, false, false>(ta, tb, ty, a, grid, early, st);
-        case 3: return launch_cfg<BF16, kTcCfg[3].bn, GELU, true, false>(ta, tb, ty, a, grid, early, st);
+        case 3:
+            if (BF16 && yodd) return launch_cfg<BF16, kTcCfg[3].bn, GELU, true, false, 0, true>(ta, tb, ty, a, grid, early, st);
+            return launch_cfg<BF16, kTcCfg[3].bn, GELU, true, false>(ta, tb, ty, a, grid, early, st);
         case 4: return launch_cfg<BF16, kTcCfg[4].bn, GELU, true, false>(ta, tb, ty, a, grid, early, st);
         case 5: return launch_cfg<BF16, kTcCfg[5].bn, GELU, true, false>(ta, tb, ty, a, grid, early, st);
         default: return LIN_ERR_UNSUPPORTED;
