@@ -880,6 +880,37 @@ def bench_reference(layer: si.Layer, steps: int, warmup: int):
     }
 
 
+# ------------------------------------------------------------------- ncu
+
+def profile_launches(name: str, n: int) -> int:
+    """A small, self-contained launch sequence for a profiler: the workload's
+    inputs, one call checked against the oracle, then n independent calls on
+    rotating W copies (the library's default launch mode), synchronised. The
+    launches to capture are the last n."""
+    import torch
+
+    import oracle
+    import transformer_linear_layer_gb300 as tll
+
+    dev = torch.device("cuda", 0)
+    ctx = tll.Context(0)
+    stream = torch.cuda.Stream(dev)
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20))
+    flush = torch.ones((2 * l2) // 4, dtype=torch.float32, device=dev)
+    if name in BWD_BY_NAME:
+        raise SystemExit("--profile-launches covers forward workloads")
+    lb = LayerBench(torch, tll, oracle, WORKLOADS[name], ctx, dev, stream, flush)
+    err, tol = lb.parity()
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            lb.step_independent(i + 1)
+    stream.synchronize()
+    ctx.check(stream)
+    log(f"{name}: {n} launches of {ctx.last_plan().as_dict()['kernel_name']}, parity rel_err {err:.3e} (tol {tol})")
+    ctx.close()
+    return 0
+
+
 # ------------------------------------------------------------------- main
 
 BWD_BY_NAME = {w.name: w for w in BWD_WORKLOADS}
@@ -896,6 +927,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="skip the per_config section")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--profile-launches", type=int, default=0,
+                    help="for ncu: only a parity-checked call and this many plain launches of the workload "
+                         "(no graphs, no timing), then exit")
     args = ap.parse_args(argv)
     rank, world, local_rank = dist_env()
     steps, warmup = max(1, args.steps), max(3, args.warmup)
@@ -918,6 +952,8 @@ def main(argv=None):
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
 
+    if args.profile_launches > 0:
+        return profile_launches(args.workload, args.profile_launches)
     if args.workload in BWD_BY_NAME:
         work = BWD_BY_NAME[args.workload]
         line = bench_backward(work, steps, warmup, world, rank, local_rank)

@@ -146,6 +146,35 @@ def test_tc_midsize_full(ctx, precision):
             check_layer(layer, plan=plan, ctx=ctx)
 
 
+@pytest.mark.parametrize("M,N,K,precision", [(8192, 768, 768, BF16), (8192, 768, 3072, BF16),
+                                             (2560, 2560, 512, BF16), (4352, 1280, 512, TF32)])
+def test_tail_split(M, N, K, precision):
+    """More tiles than SMs with a ragged last round: whole rounds of tiles, then
+    the remaining tiles split in K and added in split order (a call with no
+    independent predecessor, on its own context and stream). Every output
+    against the oracle, bitwise repeatable."""
+    c = tll.Context(0)
+    plan = c.plan(M, N, K, PREC_NAME[precision])
+    tiles = ((M + 127) // 128) * ((N + plan.bn - 1) // plan.bn)
+    assert plan.kernel == tll.KERNEL_TC and plan.grid_z > 1 and tiles > plan.grid_x, plan
+    layer = si.Layer("tail_split", M, N, K, precision, si.EPI_GELU, bias=True,
+                     x_dist="uniform" if precision == TF32 else "normal")
+    X, W, b = si.make_inputs(layer)
+    st = torch.cuda.Stream()
+    outs = []
+    for _ in range(2):
+        with torch.cuda.stream(st):
+            x, w, bias = device_inputs(X, W, b, precision)
+            outs.append(tll.forward(x, w, bias, epilogue="gelu", precision=PREC_NAME[precision], ctx=c, stream=st))
+        st.synchronize()
+    c.check(st)
+    assert c.last_plan().grid_z == plan.grid_z
+    assert torch.equal(outs[0], outs[1])
+    ref = oracle.linear(X, W, b, True)
+    assert oracle.rel_err(outs[0].double().cpu().numpy(), ref) <= oracle.TOL[precision]
+    c.close()
+
+
 @pytest.mark.parametrize("r", range(1, 8))
 def test_unaligned_rows_bf16(ctx, r):
     """bf16 Y with rows that are not 16-byte aligned (N = 8q + r): the row

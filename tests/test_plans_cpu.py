@@ -167,9 +167,12 @@ def test_ffma_split_rule():
 
 
 def test_tc_k_split_rule():
-    """tcgen05 K split: only when the tiles fill at most half of the SMs, with
-    at least 32 K stages per split, at most 16 splits, and never for the SM
-    pair; the pair for long K otherwise."""
+    """tcgen05 K split: of every tile only when the tiles fill at most half of
+    the SMs, with at least 32 K stages per split; of the ragged last round's
+    tiles only when there are more tiles than CTAs and that round is at most
+    half full (whole rounds run unsplit), its pieces filling one round with at
+    least 4 K stages each; at most 16 splits, never for the SM pair; the pair
+    for long K otherwise."""
     for sm in SMS:
         for M in (32, 128, 256, 1024, 8192):
             for N in (256, 768, 3072):
@@ -179,7 +182,13 @@ def test_tc_k_split_rule():
                     pair = p.variant >= 3
                     if p.grid_z > 1:
                         tiles = _cdiv(M, 128) * _cdiv(N, p.bn)
-                        assert not pair and tiles * 2 <= sm and p.grid_z <= 16
-                        assert _cdiv(K, 64) // p.grid_z >= 32
+                        assert not pair and p.grid_z <= 16
+                        if tiles * 2 <= sm:
+                            assert _cdiv(K, 64) // p.grid_z >= 32
+                        else:
+                            assert tiles > p.grid_x == sm
+                            rest = tiles % p.grid_x
+                            assert 0 < rest * 2 <= sm and rest * p.grid_z <= p.grid_x
+                            assert _cdiv(K, 64) // p.grid_z >= 4
                     if pair:
                         assert _cdiv(K, 64) >= 64

@@ -251,6 +251,17 @@ int make_tc(int sm, int variant, int width, bool stream_k, int M, int N, int K, 
             p->grid_z = S;
             p->grid_x = (int)(items * S < w2 ? items * S : w2);
             p->workspace_bytes = (long long)tc_ksplit_workspace_bytes(items, S, p->bn);
+        } else if (items > w) {
+            // More tiles than CTAs with a ragged last round of at most half
+            // the grid (the 8192 x 768 x 768 layer: 192 tiles on 152 SMs): whole
+            // rounds first, then the remaining tiles split in K so that their
+            // pieces fill the SMs in one short round, added in split order.
+            const long long whole = tc_tail_whole(items, (int)w);
+            const int S2 = tc_tail_splits(items - whole, (int)w, ceil_div(K, 128 / esz), ksplit_ws, p->bn);
+            if (S2 > 1) {
+                p->grid_z = S2;
+                p->workspace_bytes = (long long)tc_ksplit_workspace_bytes(items - whole, S2, p->bn);
+            }
         }
     }
     return LIN_OK;
@@ -415,11 +426,12 @@ int check_plan_fits(const lin_plan& p, int M, int N, int K, int precision) {
                 (pair || p.grid_x > kTcMaxStreamKCtas ||
                  p.workspace_bytes < (long long)tc_streamk_workspace_bytes(p.grid_x, p.bn)))
                 return LIN_ERR_UNSUPPORTED;
-            if (p.grid_z > 1) {  // K split
+            if (p.grid_z > 1) {  // K split (of every tile, or of the tiles past the whole rounds)
                 const long long tiles = (long long)ceil_div(M, 128) * ceil_div(N, p.bn);
-                if (pair || p.splits != 1 || p.grid_z > 16 || tiles > kTcMaxKSplitTiles ||
+                const long long split_tiles = tiles - tc_tail_whole(tiles, p.grid_x);
+                if (pair || p.splits != 1 || p.grid_z > 16 || split_tiles < 1 || split_tiles > kTcMaxKSplitTiles ||
                     ceil_div(K, precision == LIN_PREC_BF16 ? 64 : 32) < p.grid_z ||
-                    p.workspace_bytes < (long long)tc_ksplit_workspace_bytes(tiles, p.grid_z, p.bn))
+                    p.workspace_bytes < (long long)tc_ksplit_workspace_bytes(split_tiles, p.grid_z, p.bn))
                     return LIN_ERR_UNSUPPORTED;
             } else if (p.grid_z != 1) {
                 return LIN_ERR_UNSUPPORTED;

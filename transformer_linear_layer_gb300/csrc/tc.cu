@@ -53,6 +53,7 @@ struct TcArgs {
     unsigned* flags;     // stream-K: 8 hand-over flags per CTA boundary; K split: 8 counters per tile
                          // (zero between launches)
     int ksplits;         // K split (whole tiles, single CTA): each tile's K stages cut in ksplits ranges
+    int tail_whole;      // with ksplits > 1: the first tail_whole tiles run whole, only the rest are split
     const void* aux;     // M x N in Y's type (may be Y itself), read in the epilogue, or null:
     int aux_mode;        //   1 adds it after the activation (residual), 2 multiplies by the GELU slope at it
     int aux_vec;         // aux rows are 16-byte aligned (vector loads)
@@ -181,9 +182,13 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     const long long u1 = SK ? (long long)(blockIdx.x + 1) * units / gridDim.x : 0;
     // K split (ksplits > 1, whole single-CTA tiles): the work items are
     // (tile, split) pairs, split-major; each covers K stages
-    // [split * nkb / S, (split + 1) * nkb / S) of its tile.
+    // [split * nkb / S, (split + 1) * nkb / S) of its tile. With tail_whole > 0
+    // (the grid's whole rounds of tiles), the first tail_whole items are whole
+    // tiles and only the remaining tiles (the ragged last round) are split, so
+    // that their pieces fill the SMs in one short round.
     const int ksplits = (SK || PAIR) ? 1 : a.ksplits;
-    int cur_split = 0;  // split of the last segment returned (epilogue)
+    const int tail0 = ksplits > 1 ? a.tail_whole : 0;
+    int cur_split = 0;  // split of the last segment returned (epilogue); -1 = a whole tile
     auto seg = [&](int j, int& tile, int& lo, int& hi) -> bool {
         if constexpr (SK) {
             const long long t = u0 / nkb + j;
@@ -196,11 +201,20 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             return true;
         } else {
             const int item = first_item + j * item_step;
-            if (item >= ntiles * ksplits) return false;
-            tile = item % ntiles;
-            cur_split = item / ntiles;
-            lo = (int)((long long)cur_split * nkb / ksplits);
-            hi = (int)((long long)(cur_split + 1) * nkb / ksplits);
+            if (tail0 > 0 && item < tail0) {
+                tile = item;
+                cur_split = -1;
+                lo = 0;
+                hi = nkb;
+                return true;
+            }
+            const int rest = ntiles - tail0;  // tiles split in K
+            const int it2 = item - tail0;
+            if (it2 >= rest * ksplits) return false;
+            tile = tail0 + it2 % rest;
+            cur_split = ksplits > 1 ? it2 / rest : -1;
+            lo = ksplits > 1 ? (int)((long long)cur_split * nkb / ksplits) : 0;
+            hi = ksplits > 1 ? (int)((long long)(cur_split + 1) * nkb / ksplits) : nkb;
             return true;
         }
     };
@@ -605,8 +619,9 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             for (int jj = 0; jj < 32; ++jj) r[jj] = __float_as_uint(__uint_as_float(r[jj]) + __ldcg(src + jj * 32));
         };
         // K split: this warp's region of the (tile, split) slot, same layout.
+        // Slots and counters are numbered from the first split tile.
         auto ks_ptr = [&](int tile_, int split_) {
-            return a.partials + (((size_t)tile_ * ksplits + split_) * EPI_WARPS + ew) * (CH * 1024);
+            return a.partials + (((size_t)(tile_ - tail0) * ksplits + split_) * EPI_WARPS + ew) * (CH * 1024);
         };
 
         int j = 0, tile, lo, hi;
@@ -615,8 +630,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             const int m0 = tile_m0(tile), n0 = tile_n0(tile);
             const bool part_out = SK && lo > 0;            // later K stages of a cut tile: hand over
             const bool part_in = SK && lo == 0 && hi < nkb;  // earlier K stages: add the partner's, finish
-            const bool kpart = ksplits > 1;                // one K range of a split tile
             const int split = cur_split;
+            const bool kpart = ksplits > 1 && split >= 0;  // one K range of a split tile
             // This warp's bias columns of the tile, fetched while the MMAs run.
 #pragma unroll
             for (int t = lane; t < HALF; t += 32) {
@@ -701,7 +716,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 // them in split order and finishes the region.
                 __threadfence();
                 __syncwarp();
-                unsigned* cnt = a.flags + (size_t)tile * EPI_WARPS + ew;
+                unsigned* cnt = a.flags + (size_t)(tile - tail0) * EPI_WARPS + ew;
                 unsigned last = 0;
                 if (lane == 0) {
                     last = atomicAdd(cnt, 1u) == (unsigned)(ksplits - 1);
@@ -976,10 +991,13 @@ int launch_tc(const Problem& p, const lin_plan& plan) {
     a.partials = sk ? splitk_partials(p.workspace) : nullptr;
     a.flags = sk ? splitk_counters(p.workspace) + kTcFlagBase : nullptr;
     a.ksplits = plan.grid_z > 1 ? plan.grid_z : 1;
+    a.tail_whole = 0;
     if (a.ksplits > 1) {
         const long long ntile = (long long)((p.M + 127) / 128) * ((p.N + plan.bn - 1) / plan.bn);
-        if (sk || pair || ntile > kTcMaxKSplitTiles ||
-            p.workspace_bytes < tc_ksplit_workspace_bytes(ntile, a.ksplits, plan.bn))
+        a.tail_whole = (int)tc_tail_whole(ntile, plan.grid_x);
+        const long long split_tiles = ntile - a.tail_whole;
+        if (sk || pair || split_tiles < 1 || split_tiles > kTcMaxKSplitTiles ||
+            p.workspace_bytes < tc_ksplit_workspace_bytes(split_tiles, a.ksplits, plan.bn))
             return LIN_ERR_UNSUPPORTED;
         a.partials = splitk_partials(p.workspace);
         a.flags = splitk_counters(p.workspace);
