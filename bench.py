@@ -235,7 +235,8 @@ class CallTimer:
     replay pays its upload), and the L2 is flushed by reading a buffer twice
     its size right before the timed region (reads leave no dirty lines for
     the timed calls to write back). The region is bracketed by CUDA events
-    on `stream` with a device synchronisation on both sides."""
+    on `stream`, with a barrier and a device synchronisation before the
+    flush and after the end event."""
 
     def __init__(self, torch, stream, step, period, flush_buf, world=1):
         self.torch, self.stream, self.step, self.period, self.flush_buf = torch, stream, step, period, flush_buf
@@ -273,15 +274,19 @@ class CallTimer:
             self.torch.sum(self.flush_buf, dim=0, out=self._sink)
 
     def measure(self, n) -> float:
-        """Seconds for exactly n calls."""
+        """Seconds for exactly n calls. After the barrier and device
+        synchronisation, the L2 flush is enqueued directly before the start
+        event: while it reads (tens of microseconds) the host enqueues the
+        graphs, so the timed region holds the n calls and not the host's
+        graph-launch latency, and the calls still find the L2 cold."""
         torch = self.torch
         parts = self._plan(n)
-        self.flush()
         self.stream.synchronize()
         barrier(self.world)
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        self.flush()
         with torch.cuda.stream(self.stream):
             e0.record(self.stream)
             for g, reps in parts:

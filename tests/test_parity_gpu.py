@@ -149,14 +149,20 @@ def test_tc_midsize_full(ctx, precision):
 @pytest.mark.parametrize("M,N,K,precision", [(8192, 768, 768, BF16), (8192, 768, 3072, BF16),
                                              (2560, 2560, 512, BF16), (4352, 1280, 512, TF32)])
 def test_tail_split(M, N, K, precision):
-    """More tiles than SMs with a ragged last round: whole rounds of tiles, then
-    the remaining tiles split in K and added in split order (a call with no
-    independent predecessor, on its own context and stream). Every output
-    against the oracle, bitwise repeatable."""
+    """More tiles than SMs with a ragged last round, through an explicit plan
+    (the built-in table runs such tiles whole): whole rounds of tiles, then
+    the remaining tiles split in K and added in split order (on its own context
+    and stream). Every output against the oracle, bitwise repeatable."""
     c = tll.Context(0)
-    plan = c.plan(M, N, K, PREC_NAME[precision])
+    plan = tll.plan_make(c.sm_count, tll.KERNEL_TC, 0, 0, M, N, K, PREC_NAME[precision])
     tiles = ((M + 127) // 128) * ((N + plan.bn - 1) // plan.bn)
-    assert plan.kernel == tll.KERNEL_TC and plan.grid_z > 1 and tiles > plan.grid_x, plan
+    rest = tiles - tiles // plan.grid_x * plan.grid_x
+    nkb = (K * (2 if precision == BF16 else 4) + 127) // 128
+    splits = min(plan.grid_x // rest, nkb // 4, 16)
+    assert tiles > plan.grid_x and 0 < 2 * rest <= plan.grid_x and splits > 1, (tiles, rest, splits)
+    plan.grid_z = splits
+    plan.workspace_bytes = (64 << 10) + rest * splits * 128 * plan.bn * 4
+    assert tll.plan_check(plan, M, N, K, PREC_NAME[precision], c.workspace_bytes) == tll.OK
     layer = si.Layer("tail_split", M, N, K, precision, si.EPI_GELU, bias=True,
                      x_dist="uniform" if precision == TF32 else "normal")
     X, W, b = si.make_inputs(layer)
@@ -165,7 +171,8 @@ def test_tail_split(M, N, K, precision):
     for _ in range(2):
         with torch.cuda.stream(st):
             x, w, bias = device_inputs(X, W, b, precision)
-            outs.append(tll.forward(x, w, bias, epilogue="gelu", precision=PREC_NAME[precision], ctx=c, stream=st))
+            outs.append(tll.forward_plan(plan, x, w, bias, epilogue="gelu", precision=PREC_NAME[precision], ctx=c,
+                                         stream=st))
         st.synchronize()
     c.check(st)
     assert c.last_plan().grid_z == plan.grid_z
@@ -198,6 +205,31 @@ def test_unaligned_rows_bf16(ctx, r):
     assert bool((big[:16] == 7.0).all()) and bool((big[16 + 130 * N:] == 7.0).all())
     ref = oracle.linear(X, W, b)
     assert oracle.rel_err(y.double().cpu().numpy(), ref) <= oracle.TOL[BF16]
+
+
+def test_unaligned_rows_bf16_each_element_written_once(ctx):
+    """The odd-row store path (16-byte blocks of each row's segment, the block
+    shared by two chunks of a warp completed from the previous chunk) against
+    the element-by-element path of the same kernel (Y at a 2-byte offset): the
+    same bits, and no output left unwritten (Y starts as NaN), for every row
+    misalignment, ragged M and a partial last chunk."""
+    for r in range(1, 8):
+        N = 1024 + 256 + 32 + r
+        M, K = 260, 192
+        X, W, b = si.make_inputs(si.Layer("unaligned_once", M, N, K, BF16, si.EPI_GELU, bias=True))
+        x, w, bias = device_inputs(X, W, b, BF16)
+        for v in (0, 3):
+            plan = tll.plan_make(ctx.sm_count, tll.KERNEL_TC, v, 0, M, N, K, "bf16")
+            y_vec = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+            flat = torch.full((M * N + 8,), float("nan"), dtype=torch.bfloat16, device="cuda")
+            y_el = flat[1:1 + M * N].view(M, N)  # 2-byte offset: the element-by-element path
+            tll.forward_plan(plan, x, w, bias, epilogue="gelu", precision="bf16", out=y_vec, ctx=ctx)
+            tll.forward_plan(plan, x, w, bias, epilogue="gelu", precision="bf16", out=y_el, ctx=ctx)
+            torch.cuda.synchronize()
+            ctx.check()
+            assert not bool(torch.isnan(y_vec).any()), f"N={N} variant {v}: an output was not written"
+            assert torch.equal(y_vec, y_el), f"N={N} variant {v}"
+            assert oracle.rel_err(y_vec.double().cpu().numpy(), oracle.linear(X, W, b, True)) <= oracle.TOL[BF16]
 
 
 # ------------------------------------------------------------- edge shapes

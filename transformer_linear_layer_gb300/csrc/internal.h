@@ -92,16 +92,6 @@ inline size_t tc_ksplit_workspace_bytes(long long tiles, int splits, int bn) {
 // of tiles unsplit and splits only the rest (the ragged last round): the
 // number of tiles that run whole.
 inline long long tc_tail_whole(long long tiles, int grid) { return tiles > grid ? tiles / grid * grid : 0; }
-// Splits of the last round's `rest` tiles (rest <= grid / 2) so that their
-// pieces fill the grid in one round, each keeping >= 4 K stages; 1 = none.
-inline int tc_tail_splits(long long rest, int grid, int nkb, size_t ws_bytes, int bn) {
-    if (rest < 1 || rest * 2 > grid || rest > kTcMaxKSplitTiles) return 1;
-    int S = (int)(grid / rest);
-    if (S > nkb / 4) S = nkb / 4;
-    if (S > 16) S = 16;
-    while (S > 1 && tc_ksplit_workspace_bytes(rest, S, bn) > ws_bytes) --S;
-    return S < 2 ? 1 : S;
-}
 // Splits for a grid of `tiles` tiles with `nkb` K stages on `sm` SMs: enough
 // (tile, split) items to fill the SMs once, >= 32 K stages per split, and only
 // when the tiles alone fill at most half of the SMs. Measured on GB300: the

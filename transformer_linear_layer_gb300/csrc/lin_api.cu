@@ -251,18 +251,14 @@ int make_tc(int sm, int variant, int width, bool stream_k, int M, int N, int K, 
             p->grid_z = S;
             p->grid_x = (int)(items * S < w2 ? items * S : w2);
             p->workspace_bytes = (long long)tc_ksplit_workspace_bytes(items, S, p->bn);
-        } else if (items > w) {
-            // More tiles than CTAs with a ragged last round of at most half
-            // the grid (the 8192 x 768 x 768 layer: 192 tiles on 152 SMs): whole
-            // rounds first, then the remaining tiles split in K so that their
-            // pieces fill the SMs in one short round, added in split order.
-            const long long whole = tc_tail_whole(items, (int)w);
-            const int S2 = tc_tail_splits(items - whole, (int)w, ceil_div(K, 128 / esz), ksplit_ws, p->bn);
-            if (S2 > 1) {
-                p->grid_z = S2;
-                p->workspace_bytes = (long long)tc_ksplit_workspace_bytes(items - whole, S2, p->bn);
-            }
         }
+        // A ragged last round (more tiles than CTAs) is not split by default:
+        // measured on GB300 as isolated calls, splitting the last round's tiles
+        // in K was slower than running them whole (8192 x 768 x 768: 20.7 against
+        // 13.8 us; 8192 x 3072 x 768 with GELU: 43.0 against 36.3 us; 8192 x 768 x
+        // 3072: 37.6 against 36.5 us): the split pieces' partial sums pass through
+        // the L2 and the last piece's reduction sits on the critical path.
+        // Explicit plans (grid_z > 1 with more tiles than CTAs) still run it.
     }
     return LIN_OK;
 }

@@ -730,8 +730,24 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                         float sum[32];
 #pragma unroll
                         for (int jj = 0; jj < 32; ++jj) sum[jj] = 0.f;
+                        // Two splits' loads in flight per round trip to the L2;
+                        // the adds stay in split order.
+                        int sp = 0;
 #pragma unroll 1
-                        for (int sp = 0; sp < ksplits; ++sp) {
+                        for (; sp + 1 < ksplits; sp += 2) {
+                            const float* s0 = ks_ptr(tile, sp) + c * 1024 + lane;
+                            const float* s1 = ks_ptr(tile, sp + 1) + c * 1024 + lane;
+                            float t0[32], t1[32];
+#pragma unroll
+                            for (int jj = 0; jj < 32; ++jj) t0[jj] = __ldcg(s0 + jj * 32);
+#pragma unroll
+                            for (int jj = 0; jj < 32; ++jj) t1[jj] = __ldcg(s1 + jj * 32);
+#pragma unroll
+                            for (int jj = 0; jj < 32; ++jj) sum[jj] += t0[jj];
+#pragma unroll
+                            for (int jj = 0; jj < 32; ++jj) sum[jj] += t1[jj];
+                        }
+                        if (sp < ksplits) {
                             const float* src = ks_ptr(tile, sp) + c * 1024 + lane;
 #pragma unroll
                             for (int jj = 0; jj < 32; ++jj) sum[jj] += __ldcg(src + jj * 32);
