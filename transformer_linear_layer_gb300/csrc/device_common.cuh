@@ -26,11 +26,13 @@ __device__ __forceinline__ float tanh_hw(float x) {
     asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// The tanh argument is evaluated as s (k0 + k0 k1 s^2), one multiply fewer
+// than k0 (s + k1 s^3); the two differ by fp32 rounding only.
 __device__ __forceinline__ float gelu_tanh_bf16out(float s) {
     const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
-    const float k1 = 0.044715f;
+    const float k0k1 = 0.7978845608028654f * 0.044715f;
     const float hs = 0.5f * s;
-    return fmaf(hs, tanh_hw(k0 * (s + k1 * s * s * s)), hs);
+    return fmaf(hs, tanh_hw(s * fmaf(k0k1, s * s, k0)), hs);
 }
 
 // Slope of the tanh-form GELU (the derivative of 0.5 s (1 + tanh(c (s + a s^3)))):
@@ -60,8 +62,11 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 
+// Two values rounded to nearest-even bf16 by one paired conversion, lo in the
+// low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    return (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // ---- programmatic dependent launch ----

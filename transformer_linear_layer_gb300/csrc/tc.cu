@@ -411,48 +411,104 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             const int mrow0 = m0 + q * 32;
             // The auxiliary tensor at this lane's row: the residual stream
             // (added), or the previous layer's pre-activation (GELU slope).
-            if (a.aux_mode && mrow0 + lane < a.M) {
-                const size_t rowoff = (size_t)(mrow0 + lane) * N + nb;
+            if (a.aux_mode) {
                 float t[32];
-                if (full && a.aux_vec) {
-                    if constexpr (BF16) {
-                        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.aux) + rowoff);
+                bool staged = false;
+                if constexpr (BF16) {
+                    if (a.y_tma && full && a.aux_vec && mrow0 < a.M) {
+                        // Coalesced: four passes of 8 rows x 64 bytes (lane = 16
+                        // bytes of a row), through this warp's output box (free once
+                        // the previous store has read it), then each lane reads its
+                        // own row back. A row per lane straight from global memory
+                        // would touch 32 rows per load instruction.
+                        uint4 piece[4];
+#pragma unroll
+                        for (int it = 0; it < 4; ++it) {
+                            const int r = it * 8 + (lane >> 2), k = lane & 3;
+                            piece[it] = make_uint4(0u, 0u, 0u, 0u);
+                            if (mrow0 + r < a.M)
+                                piece[it] = *reinterpret_cast<const uint4*>(
+                                    static_cast<const uint16_t*>(a.aux) + (size_t)(mrow0 + r) * N + nb + 8 * k);
+                        }
+                        uint8_t* box = sOut + ew * 2048;
+                        if (lane == 0) bulk_wait_read_all();
+                        __syncwarp();
+#pragma unroll
+                        for (int it = 0; it < 4; ++it) {
+                            const int r = it * 8 + (lane >> 2), k = lane & 3;
+                            *reinterpret_cast<uint4*>(box + r * 64 + ((k ^ ((r >> 1) & 3)) * 16)) = piece[it];
+                        }
+                        __syncwarp();
+                        // Applied 8 values at a time as they come back (fewer live
+                        // registers than unpacking the whole row first).
 #pragma unroll
                         for (int p16 = 0; p16 < 4; ++p16) {
-                            const uint4 w = src[p16];
+                            const uint4 w = *reinterpret_cast<const uint4*>(box + lane * 64 + ((p16 ^ ((lane >> 1) & 3)) * 16));
                             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                             for (int h = 0; h < 4; ++h) {
-                                t[8 * p16 + 2 * h] = __uint_as_float(ws[h] << 16);
-                                t[8 * p16 + 2 * h + 1] = __uint_as_float(ws[h] & 0xffff0000u);
+                                const float lo = __uint_as_float(ws[h] << 16);
+                                const float hi = __uint_as_float(ws[h] & 0xffff0000u);
+                                float& v0 = v[8 * p16 + 2 * h];
+                                float& v1 = v[8 * p16 + 2 * h + 1];
+                                if (a.aux_mode == 1) {
+                                    v0 += lo;
+                                    v1 += hi;
+                                } else {
+                                    v0 *= gelu_tanh_slope<BF16>(lo);
+                                    v1 *= gelu_tanh_slope<BF16>(hi);
+                                }
+                            }
+                        }
+                        __syncwarp();  // the box takes this chunk's output next
+                        staged = true;
+                    }
+                }
+                const bool row_ok = mrow0 + lane < a.M;
+                if (!staged && row_ok) {
+                    const size_t rowoff = (size_t)(mrow0 + lane) * N + nb;
+                    if (full && a.aux_vec) {
+                        if constexpr (BF16) {
+                            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.aux) + rowoff);
+#pragma unroll
+                            for (int p16 = 0; p16 < 4; ++p16) {
+                                const uint4 w = src[p16];
+                                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                                for (int h = 0; h < 4; ++h) {
+                                    t[8 * p16 + 2 * h] = __uint_as_float(ws[h] << 16);
+                                    t[8 * p16 + 2 * h + 1] = __uint_as_float(ws[h] & 0xffff0000u);
+                                }
+                            }
+                        } else {
+                            const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(a.aux) + rowoff);
+#pragma unroll
+                            for (int p4 = 0; p4 < 8; ++p4) {
+                                const float4 w = src[p4];
+                                t[4 * p4] = w.x;
+                                t[4 * p4 + 1] = w.y;
+                                t[4 * p4 + 2] = w.z;
+                                t[4 * p4 + 3] = w.w;
                             }
                         }
                     } else {
-                        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(a.aux) + rowoff);
 #pragma unroll
-                        for (int p4 = 0; p4 < 8; ++p4) {
-                            const float4 w = src[p4];
-                            t[4 * p4] = w.x;
-                            t[4 * p4 + 1] = w.y;
-                            t[4 * p4 + 2] = w.z;
-                            t[4 * p4 + 3] = w.w;
+                        for (int j = 0; j < 32; ++j) {
+                            t[j] = 0.f;
+                            if (nb + j < N)
+                                t[j] = BF16 ? bf16_bits_to_f32(static_cast<const uint16_t*>(a.aux)[rowoff + j])
+                                            : static_cast<const float*>(a.aux)[rowoff + j];
                         }
                     }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        t[j] = 0.f;
-                        if (nb + j < N)
-                            t[j] = BF16 ? bf16_bits_to_f32(static_cast<const uint16_t*>(a.aux)[rowoff + j])
-                                        : static_cast<const float*>(a.aux)[rowoff + j];
-                    }
                 }
-                if (a.aux_mode == 1) {
+                if (!staged && row_ok) {
+                    if (a.aux_mode == 1) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] += t[j];
-                } else {
+                        for (int j = 0; j < 32; ++j) v[j] += t[j];
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] *= gelu_tanh_slope<BF16>(t[j]);
+                        for (int j = 0; j < 32; ++j) v[j] *= gelu_tanh_slope<BF16>(t[j]);
+                    }
                 }
             }
             if constexpr (BF16) {
