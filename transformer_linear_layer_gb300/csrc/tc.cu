@@ -394,7 +394,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         // leave as whole row segments: consecutive lanes, consecutive addresses
         // (storing each lane's own row from registers scatters every store
         // instruction over 32 rows and was measured slower).
-        auto emit = [&](const uint32_t (&r)[32], int c, int m0, int n0) {
+        // `pre`: the chunk's auxiliary pieces, already loaded (see aux_pieces), or null.
+        auto emit = [&](const uint32_t (&r)[32], int c, int m0, int n0, const uint4* pre = nullptr) {
             const int col = c_begin + c * 32;
             const int nb = n0 + col;
             if (nb >= N) return;  // warp-uniform
@@ -425,10 +426,14 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 #pragma unroll
                         for (int it = 0; it < 4; ++it) {
                             const int r = it * 8 + (lane >> 2), k = lane & 3;
-                            piece[it] = make_uint4(0u, 0u, 0u, 0u);
-                            if (mrow0 + r < a.M)
-                                piece[it] = *reinterpret_cast<const uint4*>(
-                                    static_cast<const uint16_t*>(a.aux) + (size_t)(mrow0 + r) * N + nb + 8 * k);
+                            if (pre) {
+                                piece[it] = pre[it];
+                            } else {
+                                piece[it] = make_uint4(0u, 0u, 0u, 0u);
+                                if (mrow0 + r < a.M)
+                                    piece[it] = *reinterpret_cast<const uint4*>(
+                                        static_cast<const uint16_t*>(a.aux) + (size_t)(mrow0 + r) * N + nb + 8 * k);
+                            }
                         }
                         uint8_t* box = sOut + ew * 2048;
                         if (lane == 0) bulk_wait_read_all();
@@ -651,6 +656,26 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             }
         };
 
+        // The coalesced auxiliary pieces of chunk c (the layout emit's staged path
+        // reads), loaded ahead so that their latency overlaps other work. Only
+        // for whole bf16 chunks whose output leaves by TMA store.
+        auto aux_pieces = [&](int c, int m0, int n0, uint4 (&p)[4]) {
+            const int nb = n0 + c_begin + c * 32;
+            const int mrow0 = m0 + q * 32;
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                const int r = it * 8 + (lane >> 2), k = lane & 3;
+                p[it] = make_uint4(0u, 0u, 0u, 0u);
+                if (mrow0 + r < a.M)
+                    p[it] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.aux) +
+                                                           (size_t)(mrow0 + r) * N + nb + 8 * k);
+            }
+        };
+        auto aux_ahead_ok = [&](int c, int m0, int n0) {
+            return BF16 && a.aux_mode && a.y_tma && a.aux_vec && c < CH && m0 + q * 32 < a.M &&
+                   n0 + c_begin + c * 32 + 32 <= N;
+        };
+
         // Hand an accumulator buffer back to the MMA issuer (the even CTA's barrier).
         auto release_acc = [&](uint32_t buf) {
             if (PAIR && !leader)
@@ -708,6 +733,16 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 }
             }
             __syncwarp();
+            // With an auxiliary tensor, chunks go one per round trip to TMEM and
+            // the next chunk's pieces are loaded while this one is processed; the
+            // first chunk's before the accumulator is ready.
+            const bool aux_ahead = !kpart && !SK && a.aux_mode && a.y_tma && a.aux_vec;
+            uint4 ahead[4];
+            bool have_ahead = false;
+            if (aux_ahead && aux_ahead_ok(0, m0, n0)) {
+                aux_pieces(0, m0, n0, ahead);
+                have_ahead = true;
+            }
             const bool mine = PAIR ? mbar_wait_cluster(tfull0 + 8 * buf, (j >> 1) & 1)
                                    : mbar_wait(tfull0 + 8 * buf, (j >> 1) & 1);
             if (!mine) give_up();
@@ -726,8 +761,31 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             const uint32_t tbase =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BUF_COLS + static_cast<uint32_t>(c_begin);
             bool released = false;
+            if (aux_ahead) {
+                // One chunk per round trip to TMEM; the next chunk's pieces are
+                // loaded before this chunk is processed.
 #pragma unroll 1
-            for (int c = 0; c < CH && ok; c += PER) {
+                for (int c = 0; c < CH && ok; ++c) {
+                    uint4 cur[4];
+                    const bool have_cur = have_ahead;
+#pragma unroll
+                    for (int it = 0; it < 4; ++it) cur[it] = ahead[it];
+                    have_ahead = aux_ahead_ok(c + 1, m0, n0);
+                    if (have_ahead) aux_pieces(c + 1, m0, n0, ahead);
+                    uint32_t r0[32];
+                    tmem_ld32_async(tbase + c * 32, r0);
+                    tmem_wait_ld(r0);
+                    if (c + 1 >= CH) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) release_acc(buf);
+                        released = true;
+                    }
+                    emit(r0, c, m0, n0, have_cur ? cur : nullptr);
+                }
+            }
+#pragma unroll 1
+            for (int c = 0; c < CH && ok && !aux_ahead; c += PER) {
                 uint32_t r0[32], r1[32];
                 const bool two = PER == 2 && c + 1 < CH;
                 tmem_ld32_async(tbase + c * 32, r0);
