@@ -916,6 +916,134 @@ def profile_launches(name: str, n: int) -> int:
     return 0
 
 
+# ---------------------------------------------------------------- timelines
+
+TIMELINE_TC = ("gpt2_qkv_m8192_bf16", "gpt2_proj_m8192_bf16", "gpt2_fc1_m8192_bf16", "gpt2_fc2_m8192_bf16",
+               "gpt2_lmhead_m8192_bf16")
+
+
+def _med(a):
+    return round(float(np.median(a)) / 1e3, 3) if len(a) else None
+
+
+def timeline_report() -> int:
+    """Kernel timelines from the timeline build (stamps compiled in, see
+    lin_timeline): one JSON line per case on stdout.
+
+    tc: one cold launch (after an L2 flush) of each M = 8192 GPT-2 layer and
+    the LM head, with the table's plan and with the SM-pair plan; per work
+    item j (medians over CTAs, us): the MMA issue span (first MMA to the
+    accumulator's commit), the epilogue span (accumulator ready to the last
+    store issued, warps 2 and 9), the item's end, and the pace of K stages.
+    skinny: four consecutive calls of the M = 16 layer in each calling mode;
+    per call (us from the first CTA's start): first and last CTA start, median
+    dependency-wait release, median first and last stage landed, last CTA
+    done."""
+    import torch
+
+    import oracle
+    import transformer_linear_layer_gb300 as tll
+
+    tll.use_timeline_build()
+    dev = torch.device("cuda", 0)
+    ctx = tll.Context(0)
+    stream = torch.cuda.Stream(dev)
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20))
+    flush = torch.ones((2 * l2) // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+    sm = ctx.sm_count
+
+    for name in TIMELINE_TC:
+        layer = WORKLOADS[name]
+        lb = LayerBench(torch, tll, oracle, layer, ctx, dev, stream, flush)
+        if name == TIMELINE_TC[0]:
+            lb.parity()  # the stamped kernel computes what the library's does
+        nkb = (layer.K * lb.esz + 127) // 128
+        for variant in (None, 3):
+            plan = ctx.plan(layer.M, layer.N, layer.K, lb.prec, lb.epi) if variant is None else \
+                tll.plan_make(sm, tll.KERNEL_TC, variant, 0, layer.M, layer.N, layer.K, lb.prec)
+            with torch.cuda.stream(stream):
+                for i in range(3):
+                    rc = ctx.forward_plan_ptr(plan, layer.M, layer.N, layer.K, lb.xp, lb.wps[i % lb.n_copies], lb.bp,
+                                              lb.yp, lb.epi, lb.prec, stream.cuda_stream)
+                    if rc != 0:
+                        raise tll.LinError(rc, "lin_forward_plan")
+                torch.sum(flush, dim=0, out=sink)
+            stream.synchronize()
+            tll.timeline_clear(tll.KERNEL_TC)
+            with torch.cuda.stream(stream):
+                ctx.forward_plan_ptr(plan, layer.M, layer.N, layer.K, lb.xp, lb.wps[3 % lb.n_copies], lb.bp, lb.yp,
+                                     lb.epi, lb.prec, stream.cuda_stream)
+            stream.synchronize()
+            ctx.check(stream)
+            t = tll.timeline(tll.KERNEL_TC)[:plan.grid_x]
+            t0 = t[:, 0][t[:, 0] > 0].min()
+            items = []
+            for j in range(32):
+                ms, mc, et, ed, e9 = t[:, 8 + 4 * j], t[:, 9 + 4 * j], t[:, 10 + 4 * j], t[:, 11 + 4 * j], t[:, 136 + j]
+                mm = (ms > 0) & (mc > 0)
+                ee = (et > 0) & (ed > 0) & (e9 > 0)
+                if not ee.any():
+                    break
+                items.append({"j": j, "ctas": int(ee.sum()),
+                              "mma_issue_us": _med((mc - ms)[mm]), "epilogue_us": _med((np.maximum(ed, e9) - et)[ee]),
+                              "done_us": _med((np.maximum(ed, e9) - t0)[ee])})
+            done = [it["done_us"] for it in items]
+            pace = [round(done[i + 1] - done[i], 3) for i in range(len(done) - 1)]
+            rec = {"timeline": "tc_kernel", "workload": name, "plan": plan_dict(plan), "k_stages": nkb,
+                   "span_us": round(float(t[:, 2].max() - t0) / 1e3, 3), "items": items[:8],
+                   "item_pace_us": pace[:8],
+                   "stage_pace_us": [round(p / nkb, 4) for p in pace[:8]]}
+            print(json.dumps(rec), flush=True)
+        del lb
+        torch.cuda.empty_cache()
+
+    layer = WORKLOADS[DEFAULT_WORKLOAD]
+    lb = LayerBench(torch, tll, oracle, layer, ctx, dev, stream, flush, want_chain=True)
+    lb.parity()
+    for mode, level, step in (("isolated", tll.EARLY_NONE, lb.step_independent),
+                              ("chained", tll.EARLY_WEIGHTS, lb.step_chained),
+                              ("back_to_back", tll.EARLY_ALL, lb.step_independent)):
+        ctx.set_option(tll.OPT_EARLY_START, level)
+        with torch.cuda.stream(stream):
+            for i in range(6):
+                step(i)
+        stream.synchronize()
+        plan = ctx.last_plan()  # the plan this calling mode gets
+        nblk = plan.grid_x * plan.grid_y
+        ncall = max(1, min(4, tll.TIMELINE_CTAS // nblk))
+        with torch.cuda.stream(stream):
+            torch.sum(flush, dim=0, out=sink)
+        stream.synchronize()
+        tll.timeline_clear(tll.KERNEL_SKINNY)
+        with torch.cuda.stream(stream):
+            for i in range(ncall):
+                step(6 + i)
+        stream.synchronize()
+        ctx.check(stream)
+        t = tll.timeline(tll.KERNEL_SKINNY)[:nblk * ncall]
+        t0 = t[:, 0][t[:, 0] > 0].min()
+        calls = []
+        for k in range(ncall):
+            tk = t[k * nblk:(k + 1) * nblk]
+            st = tk[:, 16:176]
+            first = np.where(st > 0, st, np.iinfo(np.int64).max).min(axis=1)
+            last = np.where(st > 0, st, 0).max(axis=1)
+            r = lambda a: round(float(a - t0) / 1e3, 3)
+            calls.append({"start_first": r(tk[:, 0].min()), "start_last": r(tk[:, 0].max()),
+                          "wait_released": r(np.median(tk[:, 1])) if (tk[:, 1] > 0).all() else None,
+                          "first_stage": r(np.median(first)),
+                          "last_stage": r(np.median(last)), "last_stage_max": r(last.max()),
+                          "done": r(tk[:, 3].max())})
+        ends = [c["done"] for c in calls]
+        print(json.dumps({"timeline": "skinny_kernel", "workload": layer.name, "mode": mode, "plan": plan_dict(plan),
+                          "calls": calls, "call_to_call_us": [round(ends[i + 1] - ends[i], 3)
+                                                              for i in range(len(ends) - 1)]}), flush=True)
+    ctx.set_option(tll.OPT_EARLY_START, tll.EARLY_NONE)
+    ctx.close()
+    return 0
+
+
 # ------------------------------------------------------------------- main
 
 BWD_BY_NAME = {w.name: w for w in BWD_WORKLOADS}
@@ -935,6 +1063,8 @@ def main(argv=None):
     ap.add_argument("--profile-launches", type=int, default=0,
                     help="for ncu: only a parity-checked call and this many plain launches of the workload "
                          "(no graphs, no timing), then exit")
+    ap.add_argument("--timeline", action="store_true",
+                    help="kernel timelines from the timeline build (JSON lines), then exit")
     args = ap.parse_args(argv)
     rank, world, local_rank = dist_env()
     steps, warmup = max(1, args.steps), max(3, args.warmup)
@@ -959,6 +1089,8 @@ def main(argv=None):
 
     if args.profile_launches > 0:
         return profile_launches(args.workload, args.profile_launches)
+    if args.timeline:
+        return timeline_report()
     if args.workload in BWD_BY_NAME:
         work = BWD_BY_NAME[args.workload]
         line = bench_backward(work, steps, warmup, world, rank, local_rank)

@@ -346,6 +346,31 @@ LIN_API const char* lin_strerror(int status);
 /* LIN_ABI_VERSION of the loaded library. */
 LIN_API int lin_abi_version(void);
 
+/* Kernel timeline (measurement aid; "One multiply, one RTX 5090, eight
+ * kernels", "Where the time goes", times parts of a kernel separately to see
+ * where its time goes). In the separate timeline build of this library
+ * (compiled with -DLIN_TIMELINE), the tcgen05 kernel and the skinny kernel
+ * record %globaltimer nanoseconds at fixed points of each CTA's schedule into
+ * device arrays of LIN_TIMELINE_CTAS x LIN_TIMELINE_SLOTS unsigned 64-bit
+ * values (0 = point not reached):
+ *   kernel LIN_KERNEL_TC, record = blockIdx.x: [0] set up, [1] producer past
+ *     its dependency wait, [2] teardown; for work item j < 32: [8 + 4j] MMAs
+ *     start (accumulator free), [8 + 4j + 1] last MMA and commit issued,
+ *     [8 + 4j + 2] epilogue warp 2 sees the accumulator, [8 + 4j + 3]
+ *     epilogue warp 2 done, [136 + j] epilogue warp 9 done;
+ *   kernel LIN_KERNEL_SKINNY, records in the order CTAs start (consecutive
+ *     launches follow one another): [0] set up, [1] producer past its
+ *     dependency wait, [2] MMAs complete, [3] done, [16 + i] stage i landed.
+ * lin_timeline copies the first `bytes` of that kernel's array to `host_dst`
+ * (synchronously; both NULL/0 to skip the copy), then zeroes the array (and
+ * the skinny record counter) if `clear` is non-zero. A stamped launch is
+ * identical to the library build's in everything else. Returns
+ * LIN_ERR_UNSUPPORTED in the library build, LIN_ERR_ARG for another kernel
+ * id or a NULL/non-zero mismatch of host_dst and bytes. */
+#define LIN_TIMELINE_CTAS 1024
+#define LIN_TIMELINE_SLOTS 192
+LIN_API int lin_timeline(int kernel, void* host_dst, size_t bytes, int clear);
+
 /* Size of the fixed device array behind lin_forward_fp32_static. */
 #define LIN_STATIC_SCRATCH_BYTES (8u << 20)
 

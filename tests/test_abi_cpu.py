@@ -359,3 +359,15 @@ def test_static_scratch_rule_on_the_host():
     assert tll.plan_query(152, M, N, K, "fp32", workspace_bytes=1 << 62).workspace_bytes <= tll.STATIC_SCRATCH_BYTES
     big = tll.plan_query(1024, M, N, K, "fp32", workspace_bytes=1 << 62)
     assert big.splits > 1 and big.workspace_bytes > tll.STATIC_SCRATCH_BYTES
+
+
+def test_timeline_needs_the_timeline_build():
+    """lin_timeline is exported by the library build but only the timeline
+    build records stamps; arguments are checked first."""
+    lib = tll.library()
+    assert lib.lin_timeline(tll.KERNEL_TC, None, 0, 1) == tll.ERR_UNSUPPORTED
+    assert lib.lin_timeline(tll.KERNEL_SKINNY, None, 0, 0) == tll.ERR_UNSUPPORTED
+    assert lib.lin_timeline(tll.KERNEL_FFMA, None, 0, 1) == tll.ERR_ARG
+    buf = ctypes.create_string_buffer(64)
+    assert lib.lin_timeline(tll.KERNEL_TC, buf, 0, 0) == tll.ERR_ARG
+    assert lib.lin_timeline(tll.KERNEL_TC, None, 64, 0) == tll.ERR_ARG

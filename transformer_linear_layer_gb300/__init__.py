@@ -16,6 +16,7 @@ import os
 import threading
 
 from .build import LIB as _LIB_PATH
+from .build import TIMELINE_LIB as _TIMELINE_LIB_PATH
 from .build import build
 
 __all__ = [
@@ -108,6 +109,7 @@ def library() -> ctypes.CDLL:
                 "lin_set_plan_override": ([P, I, I, I, I, I, PP], I),
                 "lin_clear_plan_overrides": ([P], I),
                 "lin_probe_ffma": ([P, I, P, ctypes.POINTER(ctypes.c_double), P], I),
+                "lin_timeline": ([I, P, Z, I], I),
                 "lin_strerror": ([I], ctypes.c_char_p),
                 "lin_abi_version": ([], I),
             }
@@ -117,6 +119,44 @@ def library() -> ctypes.CDLL:
                 f.restype = res
             _lib = lib
     return _lib
+
+
+# Shape of a kernel timeline array (LIN_TIMELINE_CTAS x LIN_TIMELINE_SLOTS).
+TIMELINE_CTAS, TIMELINE_SLOTS = 1024, 192
+
+
+def use_timeline_build() -> str:
+    """Build (if stale) the timeline library (kernels compiled with
+    -DLIN_TIMELINE) and load it instead of the library build. Call before the
+    first library call of the process; returns the library path."""
+    global _LIB_PATH
+    path = build(timeline=True)
+    with _lock:
+        if _lib is not None and _LIB_PATH != path:
+            raise RuntimeError("the library build is already loaded in this process")
+        _LIB_PATH = path
+    return path
+
+
+def timeline(kernel: int, clear: bool = True):
+    """The stamp array of ``kernel`` (KERNEL_TC or KERNEL_SKINNY) as an int64
+    numpy array of TIMELINE_CTAS x TIMELINE_SLOTS nanoseconds (0 = not
+    reached), synchronously; zeroes it afterwards if ``clear``. Needs the
+    timeline build (:func:`use_timeline_build`)."""
+    import numpy as np
+
+    buf = np.zeros(TIMELINE_CTAS * TIMELINE_SLOTS, dtype=np.uint64)
+    rc = library().lin_timeline(kernel, buf.ctypes.data, buf.nbytes, 1 if clear else 0)
+    if rc != OK:
+        raise LinError(rc, "lin_timeline")
+    return buf.reshape(TIMELINE_CTAS, TIMELINE_SLOTS).astype(np.int64)
+
+
+def timeline_clear(kernel: int):
+    """Zero a kernel's stamp array (timeline build only)."""
+    rc = library().lin_timeline(kernel, None, 0, 1)
+    if rc != OK:
+        raise LinError(rc, "lin_timeline")
 
 
 def _prec(p) -> int:

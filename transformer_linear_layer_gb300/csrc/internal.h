@@ -155,6 +155,12 @@ struct BwdProblem {
     const void* aux = nullptr;     // which 1: the previous layer's pre-activation (M x K): out *= gelu'(aux); or null
 };
 int launch_tc_backward(const BwdProblem& q);
+
+// Kernel timelines (timeline build only, see timeline.cuh): copy up to `bytes`
+// of the stamp array to host memory at `dst` (if not null), then zero it (if
+// `clear`). LIN_ERR_UNSUPPORTED in the library build.
+int timeline_copy_tc(void* dst, size_t bytes, bool clear);
+int timeline_copy_skinny(void* dst, size_t bytes, bool clear);
 int bwd_ffma_splits(int which, int M, int N, int K, int sm_count, size_t ws_bytes);
 int launch_bwd_ffma(int which, int M, int N, int K, const float* dZ, const float* B, float* out, int splits,
                     void* workspace, cudaStream_t st, bool early, const float* Zp = nullptr);

@@ -552,6 +552,15 @@ extern "C" {
 
 int lin_abi_version(void) { return LIN_ABI_VERSION; }
 
+int lin_timeline(int kernel, void* host_dst, size_t bytes, int clear) {
+    if ((host_dst == nullptr) != (bytes == 0)) return LIN_ERR_ARG;
+    switch (kernel) {
+        case LIN_KERNEL_TC: return lin::timeline_copy_tc(host_dst, bytes, clear != 0);
+        case LIN_KERNEL_SKINNY: return lin::timeline_copy_skinny(host_dst, bytes, clear != 0);
+        default: return LIN_ERR_ARG;
+    }
+}
+
 const char* lin_strerror(int status) {
     switch (status) {
         case LIN_OK: return "success";

@@ -45,9 +45,19 @@
 #include "internal.h"
 #include "device_common.cuh"
 #include "tc_common.cuh"
+#include "timeline.cuh"
 
 namespace lin {
 namespace {
+
+#ifdef LIN_TIMELINE
+// Timeline stamps per CTA, records numbered in the order the CTAs start
+// (consecutive launches follow one another): [0] set up, [1] producer past
+// its dependency wait, [2] MMAs complete, [3] done; [16 + i] stage i's
+// copies landed (seen by the MMA issuer), i < 160.
+__device__ unsigned long long g_timeline_skinny[kTimelineCtas * kTimelineSlots];
+__device__ unsigned g_timeline_skinny_next;
+#endif
 
 struct SkinnyArgs {
     int M, N, K;
@@ -163,6 +173,10 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
     const uint32_t accum_bar = smem_u32(bars + 2 * STAGES), inbox_bar = smem_u32(bars + 2 * STAGES + 1);
 
+#ifdef LIN_TIMELINE
+    __shared__ unsigned timeline_rec_sh;
+    if (threadIdx.x == 0) timeline_rec_sh = atomicAdd(&g_timeline_skinny_next, 1u);
+#endif
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full0 + 8 * s, 1);
@@ -183,7 +197,11 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
     // initialised its barriers: arrive now, wait just before the first remote write.
     if constexpr (CL > 1) cluster_arrive_relaxed();
     const uint32_t tmem_base = *tmem_slot;
+#ifdef LIN_TIMELINE
+    const unsigned trec = timeline_rec_sh;
+#endif
     if (threadIdx.x == 0) pdl_launch_dependents();
+    if (threadIdx.x == 0) LIN_STAMP(g_timeline_skinny, trec, 0);
 
     auto give_up = [&]() {
         atomicExch(s_abort, 1);
@@ -218,12 +236,14 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
                 }
                 if (!a.early_x) {
                     pdl_wait();
+                    LIN_STAMP(g_timeline_skinny, trec, 1);
                     for (int i = 0; i < pre; ++i) load_x(i);
                 }
             } else {
                 // Nothing is read before the wait (the epilogue threads ask the
                 // L2 for the share meanwhile).
                 pdl_wait();
+                LIN_STAMP(g_timeline_skinny, trec, 1);
                 for (int i = 0; i < pre; ++i) {
                     mbar_expect_tx(full0 + 8 * i, WB + XB);
                     load_w(i);
@@ -262,6 +282,7 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
                     give_up();
                     break;
                 }
+                if (i < 160) LIN_STAMP(g_timeline_skinny, trec, 16 + i);
                 tc_fence_after();
 #pragma unroll
                 for (int b = 0; b < KBOX; ++b) {
@@ -277,6 +298,7 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
             }
             tc_commit(accum_bar);
             if (!mbar_wait(accum_bar, 0)) give_up();
+            LIN_STAMP(g_timeline_skinny, trec, 2);
         }
     } else {
         // ---- epilogue warps 2..5: TMEM lane quadrant q holds W rows 32q..32q+31 ----
@@ -356,6 +378,7 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
         }
     }
 
+    if (threadIdx.x == 64) LIN_STAMP(g_timeline_skinny, trec, 3);
     __syncwarp();
     if constexpr (CL > 1) {
         // Every thread that arrived on the cluster barrier also waits on it.
@@ -449,6 +472,28 @@ int launch_skinny(const Problem& p, const lin_plan& plan) {
         default: return LIN_ERR_UNSUPPORTED;
     }
 #undef LIN_SKINNY_CASE
+}
+
+int timeline_copy_skinny(void* dst, size_t bytes, bool clear) {
+#ifdef LIN_TIMELINE
+    const size_t total = sizeof(unsigned long long) * kTimelineCtas * kTimelineSlots;
+    if (dst && bytes > 0 &&
+        cudaMemcpyFromSymbol(dst, g_timeline_skinny, bytes < total ? bytes : total) != cudaSuccess)
+        return LIN_ERR_CUDA;
+    if (clear) {
+        void* p = nullptr;
+        const unsigned zero = 0;
+        if (cudaGetSymbolAddress(&p, g_timeline_skinny) != cudaSuccess || cudaMemset(p, 0, total) != cudaSuccess ||
+            cudaMemcpyToSymbol(g_timeline_skinny_next, &zero, sizeof(zero)) != cudaSuccess)
+            return LIN_ERR_CUDA;
+    }
+    return LIN_OK;
+#else
+    (void)dst;
+    (void)bytes;
+    (void)clear;
+    return LIN_ERR_UNSUPPORTED;
+#endif
 }
 
 }  // namespace lin

@@ -35,9 +35,19 @@
 #include "internal.h"
 #include "device_common.cuh"
 #include "tc_common.cuh"
+#include "timeline.cuh"
 
 namespace lin {
 namespace {
+
+#ifdef LIN_TIMELINE
+// Timeline stamps per CTA (blockIdx.x): [0] set up, [1] producer past its
+// dependency wait, [2] teardown; per work item j < 32: [8 + 4j] MMAs start
+// (accumulator free), [8 + 4j + 1] last MMA and commit issued, [8 + 4j + 2]
+// epilogue warp 2 sees the accumulator, [8 + 4j + 3] epilogue warp 2 done,
+// [136 + j] epilogue warp 9 done.
+__device__ unsigned long long g_timeline_tc[kTimelineCtas * kTimelineSlots];
+#endif
 
 struct TcArgs {
     int M, N, K;
@@ -249,6 +259,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     if (threadIdx.x == 0) pdl_launch_dependents();
+    if (threadIdx.x == 0) LIN_STAMP(g_timeline_tc, blockIdx.x, 0);
 
     auto give_up = [&]() {
         atomicExch(s_abort, 1);
@@ -273,6 +284,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 }
                 pdl_wait();
             }
+            LIN_STAMP(g_timeline_tc, blockIdx.x, 1);
             uint32_t it = 0, issued = 0;
             bool ok = true;
             int tile, lo, hi;
@@ -336,6 +348,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + buf * BUF_COLS;
+                if (j < 32) LIN_STAMP(g_timeline_tc, blockIdx.x, 8 + 4 * j);
                 for (int kb = lo; kb < hi; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                     if (*(volatile int*)s_abort || !mbar_wait(full0 + 8 * s, ph)) {
@@ -366,6 +379,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     tc_commit_pair_mc(tfull0 + 8 * buf, (uint16_t)0x3);
                 else
                     tc_commit(tfull0 + 8 * buf);
+                if (j < 32) LIN_STAMP(g_timeline_tc, blockIdx.x, 8 + 4 * j + 1);
             }
             // Do not reach the teardown before this CTA's MMAs have completed.
             if (j > 0) {
@@ -747,6 +761,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                                    : mbar_wait(tfull0 + 8 * buf, (j >> 1) & 1);
             if (!mine) give_up();
             tc_fence_after();
+            if (warp == 2 && lane == 0 && j < 32) LIN_STAMP(g_timeline_tc, blockIdx.x, 8 + 4 * j + 2);
             // tcgen05.ld is warp-collective: a warp proceeds only if every lane saw
             // the accumulator complete and no role of this CTA gave up.
             bool ok = __all_sync(0xffffffffu, mine && *(volatile int*)s_abort == 0);
@@ -884,6 +899,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     if (lane == 0) *flag = 0u;  // re-armed for the next launch
                 }
             }
+            if (lane == 0 && j < 32 && warp == 2) LIN_STAMP(g_timeline_tc, blockIdx.x, 8 + 4 * j + 3);
+            if (lane == 0 && j < 32 && warp == 9) LIN_STAMP(g_timeline_tc, blockIdx.x, 136 + j);
             if (!released) {
                 tc_fence_before();
                 __syncwarp();
@@ -899,6 +916,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 
     __syncwarp();
     tc_fence_before();
+    if (threadIdx.x == 64) LIN_STAMP(g_timeline_tc, blockIdx.x, 2);
     // PAIR: neither CTA leaves while the peer's copies or arrivals may still
     // target its shared memory.
     if constexpr (PAIR)
@@ -1154,6 +1172,26 @@ int launch_tc(const Problem& p, const lin_plan& plan) {
                     : launch_variant<true, false>(plan.variant, sk, ta, tb, ty, a, grid, early, p.stream);
     return gelu ? launch_variant<false, true>(plan.variant, sk, ta, tb, ty, a, grid, early, p.stream)
                 : launch_variant<false, false>(plan.variant, sk, ta, tb, ty, a, grid, early, p.stream);
+}
+
+int timeline_copy_tc(void* dst, size_t bytes, bool clear) {
+#ifdef LIN_TIMELINE
+    const size_t total = sizeof(unsigned long long) * kTimelineCtas * kTimelineSlots;
+    if (dst && bytes > 0 &&
+        cudaMemcpyFromSymbol(dst, g_timeline_tc, bytes < total ? bytes : total) != cudaSuccess)
+        return LIN_ERR_CUDA;
+    if (clear) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_timeline_tc) != cudaSuccess || cudaMemset(p, 0, total) != cudaSuccess)
+            return LIN_ERR_CUDA;
+    }
+    return LIN_OK;
+#else
+    (void)dst;
+    (void)bytes;
+    (void)clear;
+    return LIN_ERR_UNSUPPORTED;
+#endif
 }
 
 }  // namespace lin
