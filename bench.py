@@ -275,10 +275,11 @@ class CallTimer:
 
     def measure(self, n) -> float:
         """Seconds for exactly n calls. After the barrier and device
-        synchronisation, the L2 flush is enqueued directly before the start
-        event: while it reads (tens of microseconds) the host enqueues the
-        graphs, so the timed region holds the n calls and not the host's
-        graph-launch latency, and the calls still find the L2 cold."""
+        synchronisation, the L2 flush and a ~0.2 ms spin of the GPU (no memory
+        traffic) are enqueued directly before the start event: meanwhile the
+        host enqueues the graphs, so the timed region holds the n calls and not
+        the host's graph-launch latency, and the calls still find the L2
+        cold."""
         torch = self.torch
         parts = self._plan(n)
         self.stream.synchronize()
@@ -288,6 +289,7 @@ class CallTimer:
         e1 = torch.cuda.Event(enable_timing=True)
         self.flush()
         with torch.cuda.stream(self.stream):
+            torch.cuda._sleep(400_000)  # clock cycles
             e0.record(self.stream)
             for g, reps in parts:
                 for _ in range(reps):

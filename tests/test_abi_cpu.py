@@ -257,8 +257,10 @@ def test_autotune_features_and_residual_fit():
              "family": rng.choice(["tc", "tc_pair", "skinny", "ffma", "gemv"]), "stream_k": rng.random() < 0.2}
         true = 0.2 - 0.7 * math.log(1 / f["fill"]) + 0.1 * math.log2(f["split"]) + (0.3 if f["stream_k"] else 0)
         m.add(f, 1e-5 * math.exp(true), 1e-5)
-    assert not autotune.ResidualModel().trusted and m.trusted
+    # trusted only once a fit has been made on enough samples (pruning uses the fit)
+    assert not autotune.ResidualModel().trusted and not m.trusted
     m.fit()
+    assert m.trusted
     coef = {r["feature"]: r for r in m.report()}
     assert abs(coef["bias"]["coef"] - 0.2) < 1e-3 and abs(coef["log_idle_waves"]["coef"] + 0.7) < 1e-3
     assert abs(coef["log2_split"]["coef"] - 0.1) < 1e-3 and abs(coef["stream_k"]["coef"] - 0.3) < 1e-3

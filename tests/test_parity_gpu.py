@@ -53,7 +53,7 @@ def all_plans(ctx, M, N, K, precision):
                 except tll.LinError:  # fewer tiles than CTAs: no stream-K plan
                     pass
     if precision == FP32:
-        for v in range(2):
+        for v in range(4):  # 128x128, 64x64, 128x128 with K steps of 64, 128x64
             for s in (1, 0, 3):
                 plans.append(tll.plan_make(sm, tll.KERNEL_FFMA, v, s, M, N, K, "fp32"))
     if (precision in (FP32, TF32) and M <= 8) or (precision == BF16 and M <= 4):
@@ -498,10 +498,20 @@ def test_ffma_back_to_back(ctx, N, K):
     """fp32 split-K calls launched back to back (the early start) share the
     workspace partial sums and tile counters: independent calls into separate
     outputs, and a chain X = previous Y (N = K), must equal the same calls made
-    one at a time."""
+    one at a time. Adaptive plans are off, so that every call takes the
+    table's split plan whatever precedes it (with them on, a call's split may
+    depend on whether its predecessor on the stream is independent of it)."""
     M = 128
     plan = ctx.plan(M, N, K, "fp32")
     assert plan.splits > 1
+    ctx.set_option(tll.OPT_ADAPTIVE_PLANS, 0)
+    try:
+        _ffma_back_to_back(ctx, M, N, K)
+    finally:
+        ctx.set_option(tll.OPT_ADAPTIVE_PLANS, 1)
+
+
+def _ffma_back_to_back(ctx, M, N, K):
     X0, _, b = si.make_inputs(si.Layer("ffb2b", M, N, K, FP32, bias=True))
     x0 = torch.from_numpy(X0).cuda()
     bias = torch.from_numpy(b).cuda()

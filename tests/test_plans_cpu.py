@@ -64,7 +64,7 @@ def _family_plans(sm, M, N, K, prec):
         menu += [(tll.KERNEL_TC, v, w) for v in range(6) for w in (0, 1, 3, sm)]
         menu += [(tll.KERNEL_TC, v, -c) for v in range(3) for c in (1, 2, 5)]
     if prec == "fp32":
-        menu += [(tll.KERNEL_FFMA, v, s) for v in range(2) for s in (0, 1, 2, 3, 7, 12)]
+        menu += [(tll.KERNEL_FFMA, v, s) for v in range(4) for s in (0, 1, 2, 3, 7, 12)]
     menu += [(tll.KERNEL_GEMV, 0, c) for c in (0, 3)]
     for kernel, v, s in menu:
         try:
@@ -144,35 +144,35 @@ def test_skinny_cluster_rule():
 
 
 def test_ffma_split_rule():
-    """FP32: 128x128 tiles when they give a full wave; else 64x64 tiles split so
-    that the (tile, split) CTAs fill two per SM without a second wave, with at
-    least 4 K steps of 32 per split, within the workspace."""
+    """FP32: 128x128 tiles (K in steps of 64) when they give a full wave; else
+    64x64 tiles split so that the (tile, split) CTAs fill two per SM without a
+    second wave, with at least 4 K steps of 32 per split and at least 16 steps
+    in all, within the workspace."""
     for sm in SMS:
         for M in (9, 64, 128, 256, 1024, 4096):
             for N in (64, 768, 2304, 3072, 4096):
-                for K in (64, 768, 3072):
+                for K in (64, 256, 512, 768, 3072):
                     for ws in (0, 64 << 20):
                         p = tll.plan_query(sm, M, N, K, "fp32", workspace_bytes=ws)
                         assert p.kernel == tll.KERNEL_FFMA
                         big = _cdiv(M, 128) * _cdiv(N, 128)
-                        assert p.variant == (0 if big >= sm else 1)
-                        tm = 128 if p.variant == 0 else 64
+                        assert p.variant == (2 if big >= sm else 1)
+                        tm = 128 if p.variant == 2 else 64
                         tiles = _cdiv(M, tm) * _cdiv(N, tm)
-                        slots = sm if p.variant == 0 else 2 * sm
+                        slots = sm if p.variant == 2 else 2 * sm
+                        steps = _cdiv(K, p.bk)
                         assert tiles * p.splits <= max(slots, tiles)
-                        assert p.splits == 1 or _cdiv(K, 32) // p.splits >= 4
+                        assert p.splits == 1 or (steps // p.splits >= 4 and steps >= 16)
                         assert p.workspace_bytes <= ws
-                        if ws and 2 * tiles <= slots and _cdiv(K, 32) >= 8:
+                        if ws and 2 * tiles <= slots and steps >= 16:
                             assert p.splits > 1, (sm, M, N, K, p)  # room for two CTAs per tile
 
 
 def test_tc_k_split_rule():
     """tcgen05 K split: of every tile only when the tiles fill at most half of
-    the SMs, with at least 32 K stages per split; of the ragged last round's
-    tiles only when there are more tiles than CTAs and that round is at most
-    half full (whole rounds run unsplit), its pieces filling one round with at
-    least 4 K stages each; at most 16 splits, never for the SM pair; the pair
-    for long K otherwise."""
+    the SMs, with at least 32 K stages per split, at most 16 splits, never for
+    the SM pair; a ragged last round is not split by the table (explicit
+    plans only); the pair for long K otherwise."""
     for sm in SMS:
         for M in (32, 128, 256, 1024, 8192):
             for N in (256, 768, 3072):
@@ -183,12 +183,7 @@ def test_tc_k_split_rule():
                     if p.grid_z > 1:
                         tiles = _cdiv(M, 128) * _cdiv(N, p.bn)
                         assert not pair and p.grid_z <= 16
-                        if tiles * 2 <= sm:
-                            assert _cdiv(K, 64) // p.grid_z >= 32
-                        else:
-                            assert tiles > p.grid_x == sm
-                            rest = tiles % p.grid_x
-                            assert 0 < rest * 2 <= sm and rest * p.grid_z <= p.grid_x
-                            assert _cdiv(K, 64) // p.grid_z >= 4
+                        assert tiles * 2 <= sm, (sm, M, N, K, p)
+                        assert _cdiv(K, 64) // p.grid_z >= 32
                     if pair:
                         assert _cdiv(K, 64) >= 64

@@ -84,7 +84,7 @@ def candidates(sm_count: int, M: int, N: int, K: int, precision, workspace_bytes
         for v in range(3):
             add(KERNEL_TC, v, -1)  # stream-K
     if prec == PREC_FP32:
-        for v in range(2):
+        for v in range(4):  # FFMA tile variants (lin_plan variant ids)
             for s in (1, 2, 3, 4, 6, 8, 12):
                 add(KERNEL_FFMA, v, s)
     if M <= 8:
@@ -132,7 +132,7 @@ def features(sm: int, M: int, N: int, K: int, precision, p: Plan) -> dict:
         mpad, npad = 16, -(-N // 128) * 128
         fam = "skinny"
     elif p.kernel == KERNEL_FFMA:
-        units, slots = p.grid_x * p.grid_y * p.grid_z, sm * (1 if p.variant == 0 else 2)
+        units, slots = p.grid_x * p.grid_y * p.grid_z, sm * (2 if p.variant in (1, 3) else 1)
         split = p.grid_z
         mpad, npad = -(-M // p.bm) * p.bm, -(-N // p.bn) * p.bn
         fam = "ffma"
@@ -186,6 +186,9 @@ class ResidualModel:
         self.rows, self.ys, self.ridge = [], [], ridge
         self.beta = [0.0] * len(_FEATURE_NAMES)
         self.per_family = {}
+        # What the current beta was fitted on: pruning trusts the fit, not
+        # samples added since (within a search the fit runs after screening).
+        self.n_fit, self.fam_fit = 0, {}
 
     def add(self, f: dict, measured_s: float, prior_s: float):
         self.rows.append(_phi(f))
@@ -196,12 +199,12 @@ class ResidualModel:
         """The fit has seen this plan's family often enough to prune with it;
         a family it has not seen is exactly where it is uncertain, so such
         candidates are timed, not pruned."""
-        return self.trusted and self.per_family.get(f["family"], 0) >= min_samples
+        return self.trusted and self.fam_fit.get(f["family"], 0) >= min_samples
 
     @property
     def trusted(self) -> bool:
-        """Enough samples to prune with (two per feature)."""
-        return len(self.ys) >= 2 * len(_FEATURE_NAMES)
+        """The fit was made on enough samples to prune with (two per feature)."""
+        return self.n_fit >= 2 * len(_FEATURE_NAMES)
 
     def fit(self):
         import numpy as np
@@ -213,6 +216,7 @@ class ResidualModel:
         reg = self.ridge * np.eye(A.shape[1])
         reg[0, 0] = 0.0  # the intercept is not shrunk
         self.beta = list(np.linalg.solve(A.T @ A + reg, A.T @ y))
+        self.n_fit, self.fam_fit = len(self.ys), dict(self.per_family)
 
     def predict_s(self, f: dict, prior_s: float) -> float:
         return prior_s * math.exp(sum(b * x for b, x in zip(self.beta, _phi(f))))

@@ -328,10 +328,15 @@ int launch_ffma(const Problem& p, const lin_plan& plan) {
     const dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
     const bool gelu = p.epilogue == LIN_EPI_GELU_TANH;
     switch (plan.variant) {
-        case 0: return launch_cfg<kFfmaCfg[0].bm, kFfmaCfg[0].bn, kFfmaCfg[0].bk, kFfmaCfg[0].tm, kFfmaCfg[0].tn, 4>(
-            a, grid, p.stream, gelu, p.early_start);
-        case 1: return launch_cfg<kFfmaCfg[1].bm, kFfmaCfg[1].bn, kFfmaCfg[1].bk, kFfmaCfg[1].tm, kFfmaCfg[1].tn, 4>(
-            a, grid, p.stream, gelu, p.early_start);
+#define LIN_FFMA_CASE(V)                                                                                       \
+    case V:                                                                                                    \
+        return launch_cfg<kFfmaCfg[V].bm, kFfmaCfg[V].bn, kFfmaCfg[V].bk, kFfmaCfg[V].tm, kFfmaCfg[V].tn,     \
+                          kFfmaCfg[V].stages>(a, grid, p.stream, gelu, p.early_start);
+        LIN_FFMA_CASE(0)
+        LIN_FFMA_CASE(1)
+        LIN_FFMA_CASE(2)
+        LIN_FFMA_CASE(3)
+#undef LIN_FFMA_CASE
         default: return LIN_ERR_UNSUPPORTED;
     }
 }

@@ -64,9 +64,13 @@ constexpr SkinnyCfg kSkinnyCfg[kSkinnyVariants] = {{3, 4}, {6, 1}, {3, 2}, {4, 3
 constexpr int kSkinnyTwoPerSm = 4;                 // the variant two CTAs of which fit on an SM
 constexpr int kSkinnyThreads = 192;                // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 
-struct FfmaCfg { int bm, bn, bk, tm, tn; };        // 256 threads each
-constexpr int kFfmaVariants = 2;
-constexpr FfmaCfg kFfmaCfg[kFfmaVariants] = {{128, 128, 32, 8, 8}, {64, 64, 32, 4, 4}};
+struct FfmaCfg { int bm, bn, bk, tm, tn, stages; };  // 256 threads each
+constexpr int kFfmaVariants = 4;
+// 0: 128 x 128, K steps of 32, 4 stages (one CTA per SM); 1: 64 x 64 (two per
+// SM); 2: 128 x 128 with K steps of 64 in 3 stages (half the barriers);
+// 3: 128 x 64 (two per SM: more warps to hide the shared-memory latency).
+constexpr FfmaCfg kFfmaCfg[kFfmaVariants] = {
+    {128, 128, 32, 8, 8, 4}, {64, 64, 32, 4, 4, 4}, {128, 128, 64, 8, 8, 3}, {128, 64, 32, 8, 4, 4}};
 
 struct TcCfg { int bn; bool pair; };              // BM = 128 per CTA, BK = 128 bytes of K; ring depth from smem
 constexpr int kTcVariants = 6;                     // pair: 2 x 1 clusters, SM-pair MMAs on 256 x BN tiles

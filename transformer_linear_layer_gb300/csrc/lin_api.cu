@@ -102,8 +102,10 @@ int make_ffma(int sm, int variant, int splits, int M, int N, int K, size_t ws, l
     if (M < 1 || N < 1 || K < 1) return LIN_ERR_UNSUPPORTED;
     if (variant < 0) {
         // 128x128 tiles when they give at least one full wave, else 64x64 + split-K.
+        // The 128x128 tiles take K in steps of 64 over 3 stages (variant 2):
+        // half the barriers of steps of 32 (4096^3: 50.2 -> 53.2 TF/s).
         const long long big = (long long)ceil_div(M, kFfmaCfg[0].bm) * ceil_div(N, kFfmaCfg[0].bn);
-        variant = big >= sm ? 0 : 1;
+        variant = big >= sm ? 2 : 1;
     }
     if (variant >= kFfmaVariants) return LIN_ERR_UNSUPPORTED;
     const FfmaCfg c = kFfmaCfg[variant];
@@ -116,9 +118,11 @@ int make_ffma(int sm, int variant, int splits, int M, int N, int K, size_t ws, l
         // SM) without starting a second wave, keeping >= 4 K steps per split
         // (measured on the GPT-2 M = 128 shapes: qkv 22 -> 17 us, fc1 29 -> 23 us
         // against rounding the split up to one CTA per SM).
-        const int slots = variant == 0 ? sm : 2 * sm;
+        const int slots = (variant == 1 || variant == 3) ? 2 * sm : sm;  // resident CTAs
         S = tiles >= slots ? 1 : slots / tiles;
-        const int max_s = nkb / min_steps > 1 ? nkb / min_steps : 1;
+        // A short reduction is not split (256^3, 8 steps: 9.8 us whole against
+        // 12.1 us in two halves, measured as isolated calls).
+        const int max_s = nkb >= 16 && nkb / min_steps > 1 ? nkb / min_steps : 1;
         if (S > max_s) S = max_s;
         if (S < 1) S = 1;
         while (S > 1 && splitk_workspace_bytes(S, M, N) > ws) --S;
