@@ -235,26 +235,47 @@ __global__ void __launch_bounds__(kBTh) bwd_ffma_kernel(const BwdArgs a) {
     }
     __syncthreads();
     if (!s_last) return;
+    // The thread's 4 x 4 outputs of four splits at a time are independent loads
+    // (one round trip to the L2 per four splits), added in split order.
+    float sum[4][4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sum[p][q] = 0.f;
 #pragma unroll 1
+    for (int sp0 = 0; sp0 < a.splits; sp0 += 4) {
+        float t[4][4][4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const int i = i0 + 4 * ty + p;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int j = j0 + 4 * tx + q;
+                    t[b][p][q] = (sp0 + b < a.splits && i < a.I && j < a.J)
+                                     ? __ldcg(a.ws + (size_t)(sp0 + b) * a.I * a.J + (size_t)i * a.J + j)
+                                     : 0.f;
+                }
+            }
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (sp0 + b < a.splits) sum[p][q] += t[b][p][q];
+    }
+#pragma unroll
     for (int p = 0; p < 4; ++p) {
         const int i = i0 + 4 * ty + p;
         if (i >= a.I) continue;
-        float sum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-        for (int sp = 0; sp < a.splits; ++sp) {
-            const float* src = a.ws + (size_t)sp * a.I * a.J + (size_t)i * a.J;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int j = j0 + 4 * tx + q;
-                if (j < a.J) sum[q] += __ldcg(src + j);
-            }
-        }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int j = j0 + 4 * tx + q;
             if (j < a.J) {
                 const size_t o = (size_t)i * a.J + j;
-                a.C[o] = a.Zp ? sum[q] * gelu_tanh_slope<false>(a.Zp[o]) : sum[q];
+                a.C[o] = a.Zp ? sum[p][q] * gelu_tanh_slope<false>(a.Zp[o]) : sum[p][q];
             }
         }
     }

@@ -100,39 +100,56 @@ __device__ __forceinline__ void splitk_epilogue(const FfmaArgs& a, const float (
     }
     __syncthreads();
     if (!s_last) return;
-    // Row by row: the TN values of each split are independent loads (four splits
-    // in flight), added in split order.
+    // The thread's TM x TN outputs of SB splits at a time are independent loads
+    // (one round trip to the L2 per SB splits), added in split order.
+    constexpr int SB = TM * TN <= 16 ? 4 : TM * TN <= 32 ? 2 : 1;
     float bcol[TN];
 #pragma unroll
     for (int c = 0; c < TN; ++c) {
         const int n = col_of(c);
         bcol[c] = (a.bias && n < a.N) ? __ldg(a.bias + n) : 0.f;
     }
+    float sum[TM][TN];
+#pragma unroll
+    for (int r = 0; r < TM; ++r)
+#pragma unroll
+        for (int c = 0; c < TN; ++c) sum[r][c] = 0.f;
 #pragma unroll 1
+    for (int sp0 = 0; sp0 < a.splits; sp0 += SB) {
+        float t[SB][TM][TN];
+#pragma unroll
+        for (int b = 0; b < SB; ++b) {
+            const int sp = sp0 + b;
+#pragma unroll
+            for (int r = 0; r < TM; ++r) {
+                const int m = row_of(r);
+#pragma unroll
+                for (int c = 0; c < TN; ++c) {
+                    const int n = col_of(c);
+                    t[b][r][c] = (sp < a.splits && m < a.M && n < a.N)
+                                     ? __ldcg(a.ws + ((size_t)sp * a.M + m) * a.N + n)
+                                     : 0.f;
+                }
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < SB; ++b)
+#pragma unroll
+            for (int r = 0; r < TM; ++r)
+#pragma unroll
+                for (int c = 0; c < TN; ++c)
+                    if (sp0 + b < a.splits) sum[r][c] += t[b][r][c];
+    }
+#pragma unroll
     for (int r = 0; r < TM; ++r) {
         const int m = row_of(r);
         if (m >= a.M) continue;
-        float sum[TN];
-#pragma unroll
-        for (int c = 0; c < TN; ++c) sum[c] = 0.f;
-#pragma unroll 4
-        for (int sp = 0; sp < a.splits; ++sp) {
-            const float* src = a.ws + ((size_t)sp * a.M + m) * a.N;
-            float t[TN];
-#pragma unroll
-            for (int c = 0; c < TN; ++c) {
-                const int n = col_of(c);
-                t[c] = n < a.N ? __ldcg(src + n) : 0.f;
-            }
-#pragma unroll
-            for (int c = 0; c < TN; ++c) sum[c] += t[c];
-        }
 #pragma unroll
         for (int c = 0; c < TN; ++c) {
             const int n = col_of(c);
             if (n < a.N) {
                 const size_t i = (size_t)m * a.N + n;
-                a.Y[i] = epilogue<GELU>(sum[c], bcol[c]) + (a.R ? a.R[i] : 0.f);
+                a.Y[i] = epilogue<GELU>(sum[r][c], bcol[c]) + (a.R ? a.R[i] : 0.f);
             }
         }
     }

@@ -519,9 +519,18 @@ int run(lin_ctx* ctx, const lin_plan& plan_in, int M, int N, int K, const void* 
     // a split would, so a split must now pay for its reduction with a long K
     // (>= 24 steps of 32 each; measured on the GPT-2 M = 128 layers: proj
     // 8.6 -> 4.1 us, qkv 14.7 -> 11.9 us, fc2 keeps a split of 4).
+    // Without a split, wide outputs of a few rows take 128 x 64 tiles (two CTAs
+    // per SM; measured back to back at M = 128, K = 768: N = 2304 10.5 -> 9.4 us,
+    // N = 3072 14.3 -> 13.4 us; N = 768 unchanged).
     if (adaptive && ctx->adaptive && known && p.early_x && plan.kernel == LIN_KERNEL_FFMA && plan.splits > 1) {
         lin_plan fewer;
-        if (make_ffma(ctx->sm_count, -1, 0, M, N, K, ctx->workspace_bytes, &fewer, 24) == LIN_OK) plan = fewer;
+        if (make_ffma(ctx->sm_count, -1, 0, M, N, K, ctx->workspace_bytes, &fewer, 24) == LIN_OK) {
+            plan = fewer;
+            lin_plan wide;
+            if (plan.splits == 1 && plan.variant == 1 && M <= 128 && N >= 2048 &&
+                make_ffma(ctx->sm_count, 3, 1, M, N, K, ctx->workspace_bytes, &wide) == LIN_OK)
+                plan = wide;
+        }
     }
     ctx->last_plan = plan;
     switch (plan.kernel) {
