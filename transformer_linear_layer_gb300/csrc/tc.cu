@@ -396,7 +396,9 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         const int N = a.N;
         float* sBias = sBiasAll + ew * HALF;
         constexpr int CH = HALF / 32;  // 32-column chunks per warp and tile
-        constexpr int PER = BF16 ? 2 : 1;  // chunks per round trip to TMEM (fp32 staging needs the registers)
+        // Chunks per round trip to TMEM: one where the registers are needed
+        // elsewhere (fp32 staging; the odd-row store path, which spilled with two).
+        constexpr int PER = (BF16 && !YODD) ? 2 : 1;
         constexpr int RB = stage_row_bytes<BF16>();
         constexpr int RP = stage_rows<BF16>();
         constexpr int ESZO = BF16 ? 2 : 4;
