@@ -1,5 +1,6 @@
 """CPU oracle for Y = act(X . W^T + bias), its backward, the fused residual,
-the LayerNorm fold and the dX carried through a GELU. TEST INFRASTRUCTURE ONLY.
+the LayerNorm fold, the dX carried through a GELU and the self-attention that
+reads the qkv projection. TEST INFRASTRUCTURE ONLY.
 
 Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
 leg import this package. The library under ``transformer_linear_layer_gb300``
@@ -80,6 +81,8 @@ def _load():
             lib.oracle_fold_layernorm.restype = None
             lib.oracle_backward_dx_gelu.argtypes = [i64, i64, i64, p, p, p, p, ctypes.c_int]
             lib.oracle_backward_dx_gelu.restype = None
+            lib.oracle_attention.argtypes = [i64, i64, i64, i64, p, ctypes.c_int, ctypes.c_double, p, p, ctypes.c_int]
+            lib.oracle_attention.restype = None
             _lib = lib
     return _lib
 
@@ -237,6 +240,24 @@ def backward_dx_gelu(dZ, W, Zp, nthreads: int = 0) -> np.ndarray:
     _load().oracle_backward_dx_gelu(M, N, K, dZ.ctypes.data, W.ctypes.data, Zp.ctypes.data, out.ctypes.data,
                                     int(nthreads))
     return out
+
+
+def attention(qkv, B: int, T: int, H: int, D: int, causal: bool = True, scale: float | None = None,
+              with_lse: bool = False, nthreads: int = 0):
+    """Self-attention from the qkv projection's output (float64).
+
+    qkv: (B*T) x 3C fp32 values (C = H*D; q, k, v at column offsets 0, C, 2C,
+    head h at h*D within each); returns out ((B*T) x C), and lse (B x H x T,
+    the log of each query's softmax denominator plus its row max) when
+    ``with_lse``. scale defaults to 1/sqrt(D)."""
+    qkv = _f32(qkv)
+    assert qkv.shape == (B * T, 3 * H * D)
+    sc = 1.0 / float(np.sqrt(D)) if scale is None else float(scale)
+    out = np.empty((B * T, H * D), dtype=np.float64)
+    lse = np.empty((B, H, T), dtype=np.float64) if with_lse else None
+    _load().oracle_attention(B, T, H, D, qkv.ctypes.data, int(bool(causal)), sc, out.ctypes.data,
+                             None if lse is None else lse.ctypes.data, int(nthreads))
+    return (out, lse) if with_lse else out
 
 
 def rel_err(y, y_ref) -> float:

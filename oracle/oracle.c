@@ -24,7 +24,8 @@
  *   Hendrycks and Gimpel, "Gaussian Error Linear Units" (2016).
  *
  * The backward of the same layer (dZ, dX, dW, db), the fused residual, the
- * LayerNorm fold and the dX carried through a GELU are defined further down.
+ * LayerNorm fold, the dX carried through a GELU and the self-attention that
+ * reads the qkv projection are defined further down.
  *
  * OpenMP splits the (m, n) outputs across threads; each output's k order is
  * fixed, so the result does not depend on the thread count.
@@ -287,6 +288,64 @@ void oracle_backward_dx_gelu(int64_t M, int64_t N, int64_t K, const float* dZ, c
                 s += (double)dZ[m * N + n] * (double)W[n * K + k];
             dZp[m * K + k] = s * oracle_gelu_tanh_grad((double)Zp[m * K + k]);
         }
+    (void)nthreads;
+}
+
+/*
+ * Causal or full self-attention of one transformer layer, read straight out
+ * of the qkv projection's output ("Writing a CUDA matmul that catches
+ * cuBLAS", section "Fusing attention: the score matrix never exists": the
+ * fused kernel indexes q, k and v in the (B, T, 3C) projection; one head is a
+ * fixed column offset).
+ *
+ *   qkv: (B*T) x 3C fp32 values, C = H*D; for token t of sequence b and head h
+ *        q = qkv[b*T + t][h*D .. h*D + D), k at column C + h*D, v at 2C + h*D.
+ *   out: (B*T) x C (double), out[b*T + i][h*D + d] = sum_j p_ij v_j[d] with
+ *        p_ij = exp(s_ij - m_i) / l_i,  s_ij = (q_i . k_j) * scale,
+ *        m_i = max_j s_ij,  l_i = sum_j exp(s_ij - m_i),
+ *        over the keys j visible to query i: j <= i when causal, else all T.
+ *   lse: B*H*T (double, may be NULL), lse[(b*H + h)*T + i] = m_i + log(l_i).
+ *
+ * This is the definition written out (two passes over a row of scores, all
+ * in double, each sum in ascending index order); the pages compute the same
+ * result with a running max and sum, which changes only the rounding.
+ */
+void oracle_attention(int64_t B, int64_t T, int64_t H, int64_t D, const float* qkv, int causal, double scale,
+                      double* out, double* lse, int nthreads)
+{
+    const int64_t C = H * D, ld = 3 * C;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for collapse(3) schedule(static) num_threads(nthreads)
+#endif
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t h = 0; h < H; ++h)
+            for (int64_t i = 0; i < T; ++i) {
+                const float* q = qkv + (b * T + i) * ld + h * D;
+                const int64_t nj = causal ? i + 1 : T;
+                double m = -INFINITY;
+                for (int64_t j = 0; j < nj; ++j) {
+                    const float* k = qkv + (b * T + j) * ld + C + h * D;
+                    double s = 0.0;
+                    for (int64_t d = 0; d < D; ++d) s += (double)q[d] * (double)k[d];
+                    s *= scale;
+                    if (s > m) m = s;
+                }
+                double l = 0.0;
+                double* o = out + (b * T + i) * C + h * D;
+                for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+                for (int64_t j = 0; j < nj; ++j) {
+                    const float* k = qkv + (b * T + j) * ld + C + h * D;
+                    const float* v = qkv + (b * T + j) * ld + 2 * C + h * D;
+                    double s = 0.0;
+                    for (int64_t d = 0; d < D; ++d) s += (double)q[d] * (double)k[d];
+                    const double e = exp(s * scale - m);
+                    l += e;
+                    for (int64_t d = 0; d < D; ++d) o[d] += e * (double)v[d];
+                }
+                for (int64_t d = 0; d < D; ++d) o[d] /= l;
+                if (lse) lse[(b * H + h) * T + i] = m + log(l);
+            }
     (void)nthreads;
 }
 

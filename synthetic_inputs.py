@@ -286,3 +286,43 @@ GPT2_LOGITS_M1 = (
 
 ALL_WORKLOADS = ((SQUARE_256_FP32, SKINNY_16x4096, SQUARE_4096_FP32, SQUARE_4096_TF32) + GPT2_M128_FP32 + GPT2_M8192_BF16 +
                  GPT2_LOGITS_M1)
+
+
+@dataclass(frozen=True)
+class Attention:
+    """One self-attention problem read from the qkv projection's output:
+    B sequences of T tokens, H heads of width D, bf16 q/k/v."""
+
+    name: str
+    B: int
+    T: int
+    H: int
+    D: int
+    causal: bool = True
+    seed: int = 0
+
+    @property
+    def C(self) -> int:
+        return self.H * self.D
+
+    @property
+    def flops(self) -> int:
+        """Multiply-adds of q k^T and p v, counted as 2 FLOPs each (the causal
+        case visits half of the key-query pairs)."""
+        pairs = self.T * (self.T + 1) // 2 if self.causal else self.T * self.T
+        return 4 * self.B * self.H * pairs * self.D
+
+    def algorithmic_bytes(self) -> int:
+        """q, k, v read and the output written once, bf16."""
+        return 2 * (3 * self.B * self.T * self.C + self.B * self.T * self.C)
+
+
+def make_qkv(att: Attention) -> np.ndarray:
+    """The (B*T) x 3C qkv projection output, N(0, 1) rounded to bf16 (fp32
+    array of the exact values the GPU receives). Tensor stream id 4."""
+    return round_bf16(normal(att.seed, 4, (att.B * att.T, 3 * att.C), 0.0, 1.0))
+
+
+# GPT-2 small's attention at the batched shape (64 sequences x 128 tokens, 12
+# heads of 64), causal, reading the qkv layer's output.
+GPT2_ATTN_B64 = Attention("gpt2_attn_b64_t128_bf16", 64, 128, 12, 64, causal=True)

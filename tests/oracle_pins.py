@@ -369,3 +369,90 @@ def pin_dx_gelu(dxg):
 
 
 NEXT4_PINS = (pin_residual, pin_layernorm, pin_fold, pin_dx_gelu)
+
+
+# ------------------------------------------------------------------ self-attention
+#
+# An attention callable: attn(qkv, B, T, H, D, causal, scale) -> (out, lse) in
+# float64, with qkv the (B*T) x 3C projection output (C = H*D; q, k, v at
+# column offsets 0, C, 2C, head h at h*D), out (B*T) x C and lse B x H x T.
+
+
+def _qkv_split(qkv, B, T, H, D):
+    """(q, k, v), each B x H x T x D float64, from the projection layout."""
+    x = qkv.astype(np.float64).reshape(B, T, 3, H, D)
+    return tuple(np.ascontiguousarray(x[:, :, i].transpose(0, 2, 1, 3)) for i in range(3))
+
+
+def pin_attention_library(attn):
+    """Equals torch's scaled_dot_product_attention in float64 (causal and not,
+    a non-square shape so that a swapped axis cannot pass, scale 1/sqrt(D) and
+    another), and lse equals torch.logsumexp of the scaled, masked scores."""
+    rng = _rng(71)
+    B, T, H, D = 2, 7, 3, 5
+    qkv = rng.standard_normal((B * T, 3 * H * D)).astype(np.float32)
+    q, k, v = (torch.tensor(a) for a in _qkv_split(qkv, B, T, H, D))
+    for causal in (True, False):
+        for scale in (1.0 / math.sqrt(D), 0.37):
+            out, lse = attn(qkv, B, T, H, D, causal, scale)
+            ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=causal, scale=scale)
+            ref = ref.permute(0, 2, 1, 3).reshape(B * T, H * D).numpy()
+            assert np.max(np.abs(out - ref)) <= 1e-13, (causal, scale)
+            s = (q @ k.transpose(-1, -2)) * scale
+            if causal:
+                s = s.masked_fill(torch.ones(T, T, dtype=torch.bool).triu(1), float("-inf"))
+            assert np.max(np.abs(lse - torch.logsumexp(s, dim=-1).numpy())) <= 1e-13, (causal, scale)
+
+
+def pin_attention_uniform(attn):
+    """q = 0: every visible key scores 0, so a query's output is the mean of
+    the visible values (the prefix mean when causal) and lse is the log of
+    their count."""
+    rng = _rng(72)
+    B, T, H, D = 1, 6, 2, 3
+    qkv = rng.standard_normal((B * T, 3 * H * D)).astype(np.float32)
+    qkv[:, : H * D] = 0.0
+    _, _, v = _qkv_split(qkv, B, T, H, D)
+    for causal in (True, False):
+        out, lse = attn(qkv, B, T, H, D, causal, 0.5)
+        for h in range(H):
+            for i in range(T):
+                n = i + 1 if causal else T
+                want = v[0, h, :n].mean(axis=0)
+                assert np.max(np.abs(out[i, h * D:(h + 1) * D] - want)) <= 1e-15, (causal, h, i)
+                assert abs(lse[0, h, i] - math.log(n)) <= 1e-15
+
+
+def pin_attention_one_hot(attn):
+    """Orthogonal keys and queries that each point at one visible key with a
+    large score: the softmax picks that key and the output is its value (the
+    rest weigh e^-40 of it); causal queries point at key i // 2, full ones at
+    key T - 1 - i (a non-involutive choice, so a transposed index fails)."""
+    B, T, H, D = 1, 6, 1, 6
+    rng = _rng(73)
+    v = rng.standard_normal((T, D)).astype(np.float32)
+    for causal in (True, False):
+        pick = [i // 2 if causal else (2 * i + 1) % T for i in range(T)]
+        qkv = np.zeros((T, 3 * D), np.float32)
+        qkv[np.arange(T), np.array(pick)] = 40.0          # q_i = 40 e_pick(i)
+        qkv[np.arange(T), D + np.arange(T)] = 1.0          # k_j = e_j
+        qkv[:, 2 * D:] = v
+        out, _ = attn(qkv, B, T, H, D, causal, 1.0)
+        assert np.max(np.abs(out - v[pick].astype(np.float64))) <= 1e-14, causal
+
+
+def pin_attention_key_order(attn):
+    """Full (non-causal) attention does not depend on the order of the keys:
+    permuting the k and v rows together (q fixed) leaves every output."""
+    rng = _rng(74)
+    B, T, H, D = 1, 9, 2, 4
+    qkv = rng.standard_normal((B * T, 3 * H * D)).astype(np.float32)
+    perm = (np.arange(T) * 4 + 1) % T
+    shuffled = qkv.copy()
+    shuffled[:, H * D:] = qkv[perm, H * D:]
+    a, la = attn(qkv, B, T, H, D, False, 0.5)
+    b, lb = attn(shuffled, B, T, H, D, False, 0.5)
+    assert np.max(np.abs(a - b)) <= 1e-14 and np.max(np.abs(la - lb)) <= 1e-14
+
+
+ATTENTION_PINS = (pin_attention_library, pin_attention_uniform, pin_attention_one_hot, pin_attention_key_order)

@@ -319,3 +319,77 @@ def test_next4_pins_catch_mutant(name):
     pin, args = NEXT4_MUTANTS[name]
     with pytest.raises(AssertionError):
         pin(*args)
+
+
+# ------------------------------------------------------------------ self-attention
+
+from oracle_pins import ATTENTION_PINS  # noqa: E402
+
+
+def _real_attention(qkv, B, T, H, D, causal, scale):
+    return oracle.attention(qkv, B, T, H, D, causal, scale, with_lse=True)
+
+
+@pytest.mark.parametrize("pin", ATTENTION_PINS, ids=lambda p: p.__name__)
+def test_attention_meets_pin(pin):
+    pin(_real_attention)
+
+
+def _attn_np(scale_ignored=False, off_by_one=False, mask_missing=False, v_from_k=False, swap_kv_offsets=False,
+             divide_by_max=False, lse_without_max=False):
+    def attn(qkv, B, T, H, D, causal, scale):
+        C = H * D
+        x = qkv.astype(np.float64)
+        out = np.zeros((B * T, C))
+        lse = np.zeros((B, H, T))
+        ko, vo = (2 * C, C) if swap_kv_offsets else (C, 2 * C)
+        if v_from_k:
+            vo = ko
+        sc = 1.0 if scale_ignored else scale
+        for b in range(B):
+            for h in range(H):
+                q = x[b * T:(b + 1) * T, h * D:(h + 1) * D]
+                k = x[b * T:(b + 1) * T, ko + h * D:ko + (h + 1) * D]
+                v = x[b * T:(b + 1) * T, vo + h * D:vo + (h + 1) * D]
+                s = (q @ k.T) * sc
+                if causal and not mask_missing:
+                    s = np.where(np.tril(np.ones((T, T)), -1 if off_by_one else 0) > 0, s, -np.inf)
+                    if off_by_one:
+                        s[0, 0] = 0.0  # the first query would see nothing: keep the row finite
+                m = s.max(axis=1, keepdims=True)
+                e = np.exp(s - m)
+                l = e.sum(axis=1, keepdims=True)
+                out[b * T:(b + 1) * T, h * D:(h + 1) * D] = (e @ v) / (np.max(e, axis=1, keepdims=True)
+                                                                    if divide_by_max else l)
+                lse[b, h] = (np.log(l) if lse_without_max else m + np.log(l))[:, 0]
+        return out, lse
+    return attn
+
+
+ATTENTION_MUTANTS = {
+    "scale_ignored": _attn_np(scale_ignored=True),
+    "causal_mask_off_by_one": _attn_np(off_by_one=True),
+    "causal_mask_missing": _attn_np(mask_missing=True),
+    "values_read_from_keys": _attn_np(v_from_k=True),
+    "k_and_v_offsets_swapped": _attn_np(swap_kv_offsets=True),
+    "divided_by_max_not_sum": _attn_np(divide_by_max=True),
+    "lse_without_row_max": _attn_np(lse_without_max=True),
+}
+
+
+def test_attention_mutant_reference_is_sound():
+    ref = _attn_np()
+    for pin in ATTENTION_PINS:
+        pin(ref)
+
+
+@pytest.mark.parametrize("name", sorted(ATTENTION_MUTANTS))
+def test_attention_pins_catch_mutant(name):
+    mutant = ATTENTION_MUTANTS[name]
+    caught = False
+    for pin in ATTENTION_PINS:
+        try:
+            pin(mutant)
+        except AssertionError:
+            caught = True
+    assert caught, f"no attention pin catches mutant {name}"
