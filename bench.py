@@ -120,11 +120,12 @@ def roofline_for(layer, seconds_per_launch: float, peaks, peaks_src, traffic, ff
             "algorithmic_flops_per_launch": flops}
 
 
-def traffic_from_profile(kernel_file: str, workload: str):
+def traffic_from_profile(kernel_file: str, workload: str, kernel: str | None = None):
     """dram bytes per launch from the committed ncu summary of this kernel and
-    workload (profiles/<kernel>_<workload>.md), or None when absent or when the
-    kernel source has changed since the capture."""
-    kernel = kernel_file.replace(".cu", "_kernel")
+    workload (profiles/<kernel>_<workload>.md; the kernel name defaults to the
+    file's stem + "_kernel"), or None when absent or when the kernel source has
+    changed since the capture."""
+    kernel = kernel or kernel_file.replace(".cu", "_kernel")
     prof = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     src = os.path.join(ROOT, "transformer_linear_layer_gb300", "csrc", kernel_file)
     try:
@@ -822,6 +823,135 @@ def bench_backward(work: BwdWork, steps: int, warmup: int, world: int, rank: int
     return line
 
 
+# ---------------------------------------------------------------- attention
+
+ATTN_WORKLOADS = {si.GPT2_ATTN_B64.name: si.GPT2_ATTN_B64}
+
+
+def attention_bound(att, qkv, out, scale):
+    """Per-element bound on |out - oracle| from the kernel's arithmetic: P
+    rounded to bf16 (relative error at most 2^-8) before its product with v,
+    the output rounded to bf16 (2^-8), fp32 sums:
+    1.05 * 2^-8 (sum_j p_ij |v_j| + |out_ref|) + 1e-5."""
+    B, T, H, D = att.B, att.T, att.H, att.D
+    x = qkv.astype(np.float64).reshape(B, T, 3, H, D)
+    s = np.einsum("bihd,bjhd->bhij", x[:, :, 0], x[:, :, 1]) * scale
+    if att.causal:
+        s = np.where(np.tril(np.ones((T, T), dtype=bool)), s, -np.inf)
+    p = np.exp(s - s.max(axis=-1, keepdims=True))
+    p /= p.sum(axis=-1, keepdims=True)
+    a = np.einsum("bhij,bjhd->bihd", p, np.abs(x[:, :, 2])).reshape(B * T, H * D)
+    return 1.05 * 2.0 ** -8 * (a + np.abs(out)) + 1e-5
+
+
+def bench_attention(att, steps: int, warmup: int, world: int, rank: int, local_rank: int, cpu: bool = True):
+    """Back-to-back fused attention forwards through the C ABI
+    (lin_attention_forward), the qkv input rotating over copies larger than
+    L2, exactly `steps` calls replayed from warm CUDA graphs; every output
+    element checked against the oracle before and after the timed calls."""
+    import torch
+
+    import oracle
+    import transformer_linear_layer_gb300 as tll
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    ctx = tll.Context(local_rank)
+    lib = tll.library()
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20))
+    qkv = si.make_qkv(att)
+    scale = 1.0 / math.sqrt(att.D)
+    q0 = torch.from_numpy(qkv).to(dev).to(torch.bfloat16)
+    in_bytes = q0.numel() * 2
+    n_copies = max(2, math.ceil(4 * l2 / in_bytes))
+    rots = [q0] + [q0.clone() for _ in range(n_copies - 1)]
+    out = torch.empty((att.B * att.T, att.C), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(dev)
+    sptr = stream.cuda_stream
+
+    def step(i):
+        rc = lib.lin_attention_forward(ctx._h, att.B, att.T, att.H, att.D, rots[i % n_copies].data_ptr(),
+                                       out.data_ptr(), None, int(att.causal), 0.0, sptr)
+        if rc != 0:
+            raise tll.LinError(rc, "lin_attention_forward")
+
+    with torch.cuda.stream(stream):
+        step(0)
+    stream.synchronize()
+    ctx.check(stream)
+    ref = oracle.attention(qkv, att.B, att.T, att.H, att.D, causal=att.causal, scale=scale)
+    bound = attention_bound(att, qkv, ref, scale)
+
+    def gate(what):
+        got = out.float().cpu().numpy().astype(np.float64)
+        r = float(np.max(np.abs(got - ref) / bound))
+        if not r <= 1.0:
+            raise SystemExit(f"{what} for {att.name}: max |out - oracle| / bound = {r}")
+        return r
+
+    err = gate("correctness gate failed")
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 3)):
+            step(i)
+    stream.synchronize()
+    flush_buf = torch.ones((2 * l2) // 4, dtype=torch.float32, device=dev)
+    timer = CallTimer(torch, stream, step, n_copies, flush_buf, world)
+    timer.measure(steps)
+    sampler = ClockSampler(local_rank)
+    timer.soak(1.0)
+    local_s = timer.measure(steps)
+    clocks = sampler.stop()
+    ctx.check(stream)
+    err_after = gate("output after the timed steps is wrong")
+    byts = att.algorithmic_bytes()
+    max_s, total = aggregate(local_s, float(steps) * byts, world, dev)
+    peaks, src = load_peaks()
+    per = local_s / steps
+    ach = byts / per / 1e9
+    tflops = att.flops / per / 1e12
+    roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(ach / peaks["hbm_gbs"], 4),
+            "traffic": traffic_from_profile("attn.cu", att.name, kernel="attn_fwd_kernel"),
+            "peak_source": f"hbm copy, {src}",
+            "algorithmic_bytes_per_launch": byts,
+            "tensor": {"achieved_tflops": round(tflops, 2), "peak": peaks["bf16_tflops"],
+                       "frac": round(tflops / peaks["bf16_tflops"], 4),
+                       "algorithmic_flops_per_launch": att.flops}}
+    cpu_line = None
+    if cpu and rank == 0 and world == 1:
+        cores = oracle.max_threads()
+        nb = max(1, min(att.B, 4))
+        sub = qkv[:nb * att.T]
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            oracle.attention(sub, nb, att.T, att.H, att.D, causal=att.causal, scale=scale, nthreads=cores)
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= 10.0 or reps >= 1000:
+                break
+        per_cpu = el / reps * att.B / nb
+        cpu_line = {"value": round(byts / per_cpu / 1e9, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                    "sample": f"{reps} x oracle attention on {nb} of {att.B} sequences ({el:.1f} s), scaled to "
+                              f"the whole batch"}
+    line = {
+        "metric": METRIC, "value": round(total / max_s / 1e9, 3), "unit": "GB/s",
+        "n_gpus": world, "steps": steps, "warmup": warmup, "ms_per_step": round(max_s / steps * 1e3, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": att.name, "B": att.B, "T": att.T, "H": att.H, "D": att.D, "causal": att.causal,
+                   "computes": "out = softmax(q k^T / sqrt(D)) v per head, q/k/v read from the qkv projection's "
+                               "(B*T) x 3C output", "kernel": "attn_fwd_kernel",
+                   "tflops": round(world * steps * att.flops / max_s / 1e12, 3),
+                   "l2": f"cold qkv: {n_copies} rotating copies ({n_copies * in_bytes >> 20} MiB > L2 "
+                         f"{l2 >> 20} MiB), exactly `steps` calls replayed from warm CUDA graphs",
+                   "parity_gate": {"max_err_over_bound": err, "after_timed_steps": err_after,
+                                   "bound": "1.05 * 2^-8 (sum_j p_ij |v_j| + |ref|) + 1e-5 per element",
+                                   "compared": f"all {out.numel()} outputs"}},
+        "roofline": roof, "cpu_baseline": cpu_line, "clocks": clocks, "gpu_launches": steps,
+    }
+    ctx.close()
+    return line
+
+
 def cpu_baseline(layer: si.Layer, X, W, b, unit, budget_s=10.0):
     """The oracle as it stands on the host cores: whole layers when one takes
     under a second, else a seeded sample of rows, repeated for ~budget_s."""
@@ -905,7 +1035,22 @@ def profile_launches(name: str, n: int) -> int:
     l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20))
     flush = torch.ones((2 * l2) // 4, dtype=torch.float32, device=dev)
     if name in BWD_BY_NAME:
-        raise SystemExit("--profile-launches covers forward workloads")
+        raise SystemExit("--profile-launches covers forward workloads and attention")
+    if name in ATTN_WORKLOADS:
+        att = ATTN_WORKLOADS[name]
+        dq = torch.from_numpy(si.make_qkv(att)).to(dev).to(torch.bfloat16)
+        qs = [dq] + [dq.clone() for _ in range(3)]
+        out = torch.empty((att.B * att.T, att.C), dtype=torch.bfloat16, device=dev)
+        with torch.cuda.stream(stream):
+            for i in range(n + 1):
+                torch.sum(flush, dim=0)
+                tll.attention_forward(qs[i % 4], att.B, att.T, att.H, causal=att.causal, out=out, ctx=ctx,
+                                      stream=stream)
+        stream.synchronize()
+        ctx.check(stream)
+        log(f"{name}: {n + 1} launches of attn_fwd_kernel")
+        ctx.close()
+        return 0
     lb = LayerBench(torch, tll, oracle, WORKLOADS[name], ctx, dev, stream, flush)
     err, tol = lb.parity()
     with torch.cuda.stream(stream):
@@ -1057,7 +1202,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS) + sorted(BWD_BY_NAME))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(WORKLOADS) + sorted(BWD_BY_NAME) + sorted(ATTN_WORKLOADS))
     ap.add_argument("--all", action="store_true", help="one line per workload (stdout), default line last")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="skip the per_config section")
@@ -1074,7 +1220,7 @@ def main(argv=None):
     if args.impl == "reference":
         if rank != 0:
             return 0
-        if args.workload in BWD_BY_NAME:
+        if args.workload in BWD_BY_NAME or args.workload in ATTN_WORKLOADS:
             print(json.dumps({"impl": "reference", "unavailable": "the reference arm times forward workloads only"}))
             return 0
         ref_steps = min(steps, 200)
@@ -1099,12 +1245,22 @@ def main(argv=None):
         if rank == 0:
             print(json.dumps(line), flush=True)
         return 0
+    if args.workload in ATTN_WORKLOADS:
+        line = bench_attention(ATTN_WORKLOADS[args.workload], steps, warmup, world, rank, local_rank,
+                               cpu=not args.no_cpu_baseline)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return 0
     names = [args.workload]
     if args.all:
         names = [n for n in WORKLOADS if n != args.workload] + [args.workload]
         for work in BWD_WORKLOADS:
             st = max(300, min(steps, int(2e13 / work.flops)))
             line = bench_backward(work, st, warmup, world, rank, local_rank)
+            if rank == 0:
+                print(json.dumps(line), flush=True)
+        for att in ATTN_WORKLOADS.values():
+            line = bench_attention(att, max(300, steps), warmup, world, rank, local_rank, cpu=False)
             if rank == 0:
                 print(json.dumps(line), flush=True)
     for name in names:

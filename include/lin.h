@@ -360,13 +360,21 @@ LIN_API int lin_abi_version(void);
  *     epilogue warp 2 done, [136 + j] epilogue warp 9 done;
  *   kernel LIN_KERNEL_SKINNY, records in the order CTAs start (consecutive
  *     launches follow one another): [0] set up, [1] producer past its
- *     dependency wait, [2] MMAs complete, [3] done, [16 + i] stage i landed.
+ *     dependency wait, [2] MMAs complete, [3] done, [16 + i] stage i landed;
+ *   kernel LIN_TIMELINE_ATTENTION (lin_attention_forward), record =
+ *     blockIdx.x: [0] set up, [1] producer past its dependency wait, [2]
+ *     teardown; for the CTA's work item n < 16, at 8 + 10n + k: k = 0 Q copy
+ *     issued, 1 first K/V copy issued, 2 MMA warp saw the first K/V land, 3
+ *     first S MMAs committed, 4 softmax warp 2 saw the first S, 5 it released
+ *     the last P, 6 last P.V MMAs committed, 7 softmax warp 2 saw the last
+ *     P.V, 8 softmax warp 2 stored its rows, 9 softmax warp 9 stored its rows.
  * lin_timeline copies the first `bytes` of that kernel's array to `host_dst`
  * (synchronously; both NULL/0 to skip the copy), then zeroes the array (and
  * the skinny record counter) if `clear` is non-zero. A stamped launch is
  * identical to the library build's in everything else. Returns
  * LIN_ERR_UNSUPPORTED in the library build, LIN_ERR_ARG for another kernel
  * id or a NULL/non-zero mismatch of host_dst and bytes. */
+#define LIN_TIMELINE_ATTENTION 16
 #define LIN_TIMELINE_CTAS 1024
 #define LIN_TIMELINE_SLOTS 192
 LIN_API int lin_timeline(int kernel, void* host_dst, size_t bytes, int clear);
@@ -408,6 +416,38 @@ LIN_API int lin_timeline(int kernel, void* host_dst, size_t bytes, int clear);
  *   without ordering) race on the array: order them on one stream. */
 LIN_API int lin_forward_fp32_static(int M, int N, int K, const float* X, const float* W,
                                     const float* bias, float* Y, int epilogue, void* stream);
+
+/* Fused self-attention forward, the step between the qkv projection and the
+ * output projection ("Writing a CUDA matmul that catches cuBLAS", section
+ * "Fusing attention: the score matrix never exists": q, k and v are read
+ * straight from the projection's output, a running row max and sum replace
+ * the stored score matrix, and causality is the loop bound). For sequence b,
+ * head h and query token i:
+ *   s_ij  = (q_i . k_j) * scale over the visible keys j (j <= i when causal,
+ *           all j < T otherwise),
+ *   out[b*T + i][h*64 + d] = sum_j exp(s_ij - m_i) v_j[d] / l_i,
+ *   m_i = max_j s_ij, l_i = sum_j exp(s_ij - m_i),
+ *   lse[(b*H + h)*T + i] = m_i + log(l_i)            (when lse is not NULL).
+ *   qkv : DEVICE, (B*T) x 3C bf16 row-major, C = H*D; token t of sequence b is
+ *         row b*T + t, holding q, k, v at column offsets 0, C, 2C and head h
+ *         at h*D within each (the layout of the qkv linear layer's output).
+ *   out : DEVICE, (B*T) x C bf16 row-major (the output projection's input);
+ *         must not overlap qkv or lse.
+ *   lse : DEVICE fp32 B x H x T, or NULL (the softmax statistics a backward
+ *         pass rebuilds the probabilities from).
+ *   D   : head width; 64 only (LIN_ERR_UNSUPPORTED otherwise).
+ *   causal: 1 (decoder attention) or 0.
+ *   scale: softmax scale > 0; 0 selects 1/sqrt(D).
+ * Arithmetic: bf16 q, k products accumulated in fp32 on the tensor cores,
+ * softmax in fp32 (base-2 exponent of the scaled scores, hardware ex2),
+ * probabilities rounded to bf16 for the product with v (fp32 accumulation),
+ * output rounded to nearest-even bf16. qkv and out must be 16-byte aligned
+ * (LIN_ERR_ALIGN), lse 4-byte aligned; B*T < 2^31. B, T or H == 0: nothing to
+ * do. Asynchronous on `stream`; launched as a programmatic dependent of the
+ * previous kernel (when LIN_OPT_PROGRAMMATIC_LAUNCH is on) but reads qkv and
+ * writes out / lse only after that kernel has finished. */
+LIN_API int lin_attention_forward(lin_ctx* ctx, int B, int T, int H, int D, const void* qkv, void* out, float* lse,
+                                  int causal, float scale, void* stream);
 
 #ifdef __cplusplus
 }

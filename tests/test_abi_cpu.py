@@ -63,6 +63,7 @@ def test_null_context_is_an_argument_error():
     assert lib.lin_set_plan_override(None, 16, 16, 16, 2, 0, None) == tll.ERR_ARG
     assert lib.lin_clear_plan_overrides(None) == tll.ERR_ARG
     assert lib.lin_set_option(None, 1, 1) == tll.ERR_ARG
+    assert lib.lin_attention_forward(None, 1, 128, 12, 64, None, None, None, 1, 0.0, None) == tll.ERR_ARG
 
 
 def test_create_without_device_fails_cleanly():
@@ -369,6 +370,7 @@ def test_timeline_needs_the_timeline_build():
     lib = tll.library()
     assert lib.lin_timeline(tll.KERNEL_TC, None, 0, 1) == tll.ERR_UNSUPPORTED
     assert lib.lin_timeline(tll.KERNEL_SKINNY, None, 0, 0) == tll.ERR_UNSUPPORTED
+    assert lib.lin_timeline(tll.TIMELINE_ATTENTION, None, 0, 1) == tll.ERR_UNSUPPORTED
     assert lib.lin_timeline(tll.KERNEL_FFMA, None, 0, 1) == tll.ERR_ARG
     buf = ctypes.create_string_buffer(64)
     assert lib.lin_timeline(tll.KERNEL_TC, buf, 0, 0) == tll.ERR_ARG

@@ -21,7 +21,7 @@ from .build import build
 
 __all__ = [
     "LinError", "Context", "Plan", "forward", "forward_plan", "plan_query", "plan_make", "build",
-    "backward_data", "backward_weight", "gelu_backward",
+    "backward_data", "backward_weight", "gelu_backward", "attention_forward",
     "library", "PREC_FP32", "PREC_TF32", "PREC_BF16", "EPI_NONE", "EPI_GELU_TANH",
     "KERNEL_NONE", "KERNEL_FILL", "KERNEL_SKINNY", "KERNEL_FFMA", "KERNEL_TC", "KERNEL_GEMV",
 ]
@@ -110,6 +110,7 @@ def library() -> ctypes.CDLL:
                 "lin_clear_plan_overrides": ([P], I),
                 "lin_probe_ffma": ([P, I, P, ctypes.POINTER(ctypes.c_double), P], I),
                 "lin_timeline": ([I, P, Z, I], I),
+                "lin_attention_forward": ([P, I, I, I, I, P, P, P, I, ctypes.c_float, P], I),
                 "lin_strerror": ([I], ctypes.c_char_p),
                 "lin_abi_version": ([], I),
             }
@@ -121,8 +122,10 @@ def library() -> ctypes.CDLL:
     return _lib
 
 
-# Shape of a kernel timeline array (LIN_TIMELINE_CTAS x LIN_TIMELINE_SLOTS).
+# Shape of a kernel timeline array (LIN_TIMELINE_CTAS x LIN_TIMELINE_SLOTS),
+# and the timeline id of the attention kernel (LIN_TIMELINE_ATTENTION).
 TIMELINE_CTAS, TIMELINE_SLOTS = 1024, 192
+TIMELINE_ATTENTION = 16
 
 
 def use_timeline_build() -> str:
@@ -139,7 +142,8 @@ def use_timeline_build() -> str:
 
 
 def timeline(kernel: int, clear: bool = True):
-    """The stamp array of ``kernel`` (KERNEL_TC or KERNEL_SKINNY) as an int64
+    """The stamp array of ``kernel`` (KERNEL_TC, KERNEL_SKINNY or
+    TIMELINE_ATTENTION) as an int64
     numpy array of TIMELINE_CTAS x TIMELINE_SLOTS nanoseconds (0 = not
     reached), synchronously; zeroes it afterwards if ``clear``. Needs the
     timeline build (:func:`use_timeline_build`)."""
@@ -512,3 +516,35 @@ def gelu_backward(dy, z, out=None, precision=None, ctx: Context | None = None, s
     if rc != OK:
         raise LinError(rc, "lin_gelu_backward")
     return out
+
+
+# ---------------------------------------------------------------- attention
+
+def attention_forward(qkv, B: int, T: int, H: int, causal: bool = True, scale: float | None = None, out=None,
+                      lse=None, with_lse: bool = False, ctx: Context | None = None, stream=None):
+    """Fused self-attention forward from the qkv projection's output.
+
+    qkv: contiguous bf16 CUDA tensor of (B*T) x 3C (C = 64 H; q, k, v at
+    column offsets 0, C, 2C, head h at 64 h within each). Returns out
+    ((B*T) x C bf16), or (out, lse) with lse (B, H, T) fp32 when ``with_lse``
+    or an lse tensor is given. scale defaults to 1/sqrt(64)."""
+    import torch
+
+    D = 64
+    C = H * D
+    _check(qkv, torch.bfloat16, (B * T, 3 * C), "qkv")
+    if out is None:
+        out = torch.empty((B * T, C), dtype=torch.bfloat16, device=qkv.device)
+    _check(out, torch.bfloat16, (B * T, C), "out")
+    if lse is None and with_lse:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=qkv.device)
+    if lse is not None:
+        _check(lse, torch.float32, (B, H, T), "lse")
+    dev = qkv.device.index if qkv.device.index is not None else 0
+    ctx = ctx or default_context(dev)
+    rc = library().lin_attention_forward(ctx._h, B, T, H, D, qkv.data_ptr(), out.data_ptr(),
+                                         None if lse is None else lse.data_ptr(), int(bool(causal)),
+                                         0.0 if scale is None else float(scale), _stream_ptr(stream, dev))
+    if rc != OK:
+        raise LinError(rc, "lin_attention_forward")
+    return (out, lse) if lse is not None else out

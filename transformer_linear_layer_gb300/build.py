@@ -28,7 +28,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "liblin.so")
 TIMELINE_LIB = os.path.join(BUILD, "liblin_timeline.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ("lin_api.cu", "skinny.cu", "ffma.cu", "tc.cu", "gemv.cu", "backward.cu", "noalloc.cu", "fold.cu", "probe.cu")
+SOURCES = ("lin_api.cu", "skinny.cu", "ffma.cu", "tc.cu", "gemv.cu", "backward.cu", "noalloc.cu", "fold.cu", "probe.cu", "attn.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", f"-I{INCLUDE}"]

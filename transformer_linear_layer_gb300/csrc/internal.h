@@ -160,11 +160,29 @@ struct BwdProblem {
 };
 int launch_tc_backward(const BwdProblem& q);
 
+// Fused self-attention forward (attn.cu): bf16 q, k, v read from the qkv
+// projection's (B*T) x 3C output, heads of 64, output (B*T) x C bf16, row
+// log-sum-exp (B x H x T fp32) when lse is not null.
+struct AttnProblem {
+    int B = 0, T = 0, H = 0;
+    const void* qkv = nullptr;
+    void* out = nullptr;
+    float* lse = nullptr;
+    bool causal = true;
+    float scale = 0.f;             // softmax scale (> 0)
+    cudaStream_t stream = nullptr;
+    int* dev_status = nullptr;
+    int sm_count = 0;
+    bool early_start = false;      // programmatic launch (nothing is read before the dependency wait)
+};
+int launch_attention(const AttnProblem& p);
+
 // Kernel timelines (timeline build only, see timeline.cuh): copy up to `bytes`
 // of the stamp array to host memory at `dst` (if not null), then zero it (if
 // `clear`). LIN_ERR_UNSUPPORTED in the library build.
 int timeline_copy_tc(void* dst, size_t bytes, bool clear);
 int timeline_copy_skinny(void* dst, size_t bytes, bool clear);
+int timeline_copy_attn(void* dst, size_t bytes, bool clear);
 int bwd_ffma_splits(int which, int M, int N, int K, int sm_count, size_t ws_bytes);
 int launch_bwd_ffma(int which, int M, int N, int K, const float* dZ, const float* B, float* out, int splits,
                     void* workspace, cudaStream_t st, bool early, const float* Zp = nullptr);

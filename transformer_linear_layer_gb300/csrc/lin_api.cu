@@ -570,6 +570,7 @@ int lin_timeline(int kernel, void* host_dst, size_t bytes, int clear) {
     switch (kernel) {
         case LIN_KERNEL_TC: return lin::timeline_copy_tc(host_dst, bytes, clear != 0);
         case LIN_KERNEL_SKINNY: return lin::timeline_copy_skinny(host_dst, bytes, clear != 0);
+        case LIN_TIMELINE_ATTENTION: return lin::timeline_copy_attn(host_dst, bytes, clear != 0);
         default: return LIN_ERR_ARG;
     }
 }
@@ -947,6 +948,46 @@ int lin_probe_ffma(lin_ctx* ctx, int iters, float* out, double* flops, void* str
     lin::DeviceGuard guard(ctx->device);
     if (!guard.ok) return LIN_ERR_CUDA;
     return lin::launch_ffma_probe(ctx->sm_count, iters, out, static_cast<cudaStream_t>(stream), flops);
+}
+
+int lin_attention_forward(lin_ctx* ctx, int B, int T, int H, int D, const void* qkv, void* out, float* lse,
+                          int causal, float scale, void* stream) {
+    using namespace lin;
+    if (!ctx || B < 0 || T < 0 || H < 0 || D < 0 || (causal != 0 && causal != 1)) return LIN_ERR_ARG;
+    if (!(scale >= 0.f) || isinf(scale)) return LIN_ERR_ARG;  // NaN, negative or infinite
+    if (B == 0 || T == 0 || H == 0) return LIN_OK;
+    if (D != 64) return LIN_ERR_UNSUPPORTED;
+    const long long rows = (long long)B * T;
+    const long long nqb = (T + 127) / 128;
+    if (rows > INT_MAX || (long long)H * D * 3 > INT_MAX || (long long)B * H * nqb > INT_MAX) return LIN_ERR_UNSUPPORTED;
+    if (!qkv || !out) return LIN_ERR_ARG;
+    const size_t C = (size_t)H * D;
+    const size_t in_bytes = (size_t)rows * 3 * C * 2, out_bytes = (size_t)rows * C * 2;
+    const size_t lse_bytes = lse ? (size_t)B * H * T * 4 : 0;
+    if (overlaps(out, out_bytes, qkv, in_bytes) || overlaps(lse, lse_bytes, qkv, in_bytes) ||
+        overlaps(lse, lse_bytes, out, out_bytes))
+        return LIN_ERR_ARG;
+    if ((((uintptr_t)qkv | (uintptr_t)out) % 16) != 0 || ((uintptr_t)lse % 4) != 0) return LIN_ERR_ALIGN;
+    DeviceGuard guard(ctx->device);
+    if (!guard.ok) return LIN_ERR_CUDA;
+    AttnProblem p;
+    p.B = B;
+    p.T = T;
+    p.H = H;
+    p.qkv = qkv;
+    p.out = out;
+    p.lse = lse;
+    p.causal = causal != 0;
+    p.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
+    p.stream = static_cast<cudaStream_t>(stream);
+    p.dev_status = ctx->dev_status;
+    p.sm_count = ctx->sm_count;
+    p.early_start = ctx->programmatic;
+    // Its output is a later call's input: note it for the early-read checks.
+    bool w_ok = false, x_ok = false, known = false;
+    early_reads_ok(p.stream, Range{nullptr, 0}, Range{nullptr, 0}, Range{qkv, in_bytes}, Range{out, out_bytes}, &w_ok,
+                   &x_ok, &known);
+    return launch_attention(p);
 }
 
 int lin_check_device(lin_ctx* ctx, void* stream) {
