@@ -17,33 +17,34 @@
 //
 // On sm_103a (not the page's design, which was written for mma.sync on
 // sm_89): a persistent CTA per SM walks work items (sequence, head, block of
-// 128 queries), largest causal items first.
-//   warp 0      TMA: Q (128 x 64, K-major, 128-byte swizzle) into a 3-deep
-//               ring, K (128 keys x 64, K-major) and V (128 keys x 64,
-//               MN-major: two 64-key boxes) into a 3-deep ring, up to two
-//               items ahead. Before the dependency wait it asks the L2 for its
-//               first items' tiles.
-//   warp 1      tcgen05.mma: S = Q K^T (M 128, N 128, K 64) into one of two
-//               TMEM buffers (columns 0-127, 128-255, alternating blocks), and
-//               O += P V (M 128, N 64, K 128) into one of two O buffers
-//               (columns 256-319, 320-383, alternating items). It polls its
-//               barriers and issues whichever of the next S or the next P.V
-//               has its inputs first, up to two S ahead.
-//   warps 2-9   softmax and output: warp w reads TMEM lanes 32*(w%4).. (its
-//               query rows) and one half of the 128 key columns; the two
-//               warps of a row exchange their row maxima (and the previous
-//               item's row sums) through shared memory. Scores are scaled into
-//               base-2 units (scale * log2 e) by a packed fp32x2 FMA and
-//               exponentiated with the hardware ex2; P is rounded to bf16 into
-//               shared memory in the operand layout of the next MMA. A 32-key
-//               chunk that no row of a warp sees (above the causal diagonal,
-//               or past T) is neither read nor exponentiated. When a later key
-//               block raises a row's max, the warp scales that row's O in TMEM
-//               by alpha = 2^(m - m') before the block's P.V adds to it. An
-//               item's output (O / l, bf16) is written during the next block,
-//               once its last P.V has completed: through a 32 x 32 box per warp
-//               in shared memory and a TMA store of a B x T x C view of the
-//               output, which leaves out the rows past a sequence's end.
+// 128 queries), largest causal items first. Its softmax warps form two groups
+// that take alternate items, so that one group's softmax runs while the
+// other waits for its MMAs, its TMEM loads or its output store.
+//   warp 0      TMA: the Q tile (128 x 64, K-major, 128-byte swizzle) of item
+//               n into group n % 2's stage, K (128 keys x 64, K-major) and V
+//               (128 keys x 64, MN-major: two 64-key boxes) through a 3-deep
+//               ring, in item order. Before the dependency wait it asks the L2
+//               for its first items' tiles.
+//   warp 1      tcgen05.mma for both groups: S = Q K^T (M 128, N 128, K 64)
+//               into the group's TMEM S buffer (columns 0-127 or 128-255) and
+//               O += P V (M 128, N 64, K 128) into its O buffer (columns
+//               256-319 or 320-383). It polls the barriers and issues
+//               whatever has its inputs first.
+//   warps 2-5,  the two softmax groups: warp w reads TMEM lanes 32*(w%4)..
+//   warps 6-9   (its 32 query rows), one thread per row and all 128 keys of a
+//               block, so no exchange between warps is needed. Scores are
+//               scaled into base-2 units (scale * log2 e) by a packed fp32x2
+//               FMA and exponentiated with the hardware ex2; P is rounded to
+//               bf16 into the group's shared-memory P buffer in the operand
+//               layout of the next MMA. A 32-key chunk that no row of a warp
+//               sees (above the causal diagonal, or past T) is neither read
+//               nor exponentiated. When a later key block raises a row's max,
+//               the warp scales that row's O in TMEM by alpha = 2^(m - m')
+//               before the block's P.V adds to it. At an item's end the warp
+//               divides O by l, stages its rows as two 32 x 32 bf16 boxes in
+//               its part of the P buffer and stores them by TMA through a
+//               B x T x C view of the output, which leaves out the rows past a
+//               sequence's end.
 // Every wait is bounded (about 1 s); a CTA that gives up sets the device
 // status word to LIN_ERR_DEVICE_TIMEOUT and leaves its output incomplete.
 #include <math.h>
@@ -59,10 +60,10 @@ namespace {
 // Timeline stamps (timeline build only): record = blockIdx.x; [0] set up,
 // [1] producer past its dependency wait, [2] teardown; for the CTA's work item
 // n < 16, at 8 + 10 n + k: k 0 Q copy issued, 1 first K/V copy issued, 2 MMA
-// warp saw the first K/V block land, 3 first S MMAs committed, 4 softmax warp 2
-// saw the first S, 5 softmax warp 2 released the last P, 6 last P.V MMAs
-// committed, 7 softmax warp 2 saw the last P.V, 8 softmax warp 2 stored its
-// rows, 9 softmax warp 9 stored its rows.
+// warp saw the first K/V block land, 3 first S MMAs committed, 4 the item's
+// softmax group (warp 2 or 6) saw the first S, 5 it released the last P, 6
+// last P.V MMAs committed, 7 warp 2 or 6 saw the last P.V, 8 it issued its
+// output store, 9 warp 5 or 9 issued its output store.
 __device__ unsigned long long g_timeline_attn[kTimelineCtas * kTimelineSlots];
 #define AT_STAMP(n, k) \
     do {                \
@@ -72,23 +73,27 @@ __device__ unsigned long long g_timeline_attn[kTimelineCtas * kTimelineSlots];
 constexpr int kAtBM = 128;                          // query rows per work item
 constexpr int kAtBN = 128;                          // keys per block
 constexpr int kAtD = 64;                            // head width
-constexpr int kAtThreads = 320;                     // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
-constexpr int kAtQStages = 3;
+constexpr int kAtThreads = 384;                     // warp 0 TMA, warp 1 MMA, warps 4-7 and 8-11 softmax
+// Register split (setmaxnreg, per warpgroup): launched at kAtLaunchRegs a
+// thread, warpgroup 0 (TMA, MMA, two idle warps) gives registers back down to
+// kAtRegsLow and the two softmax warpgroups take kAtRegsHigh:
+// 128 * 72 + 256 * 216 = 64512 = 384 * 168. The host refuses to launch when
+// the compiled kernel holds fewer than kAtLaunchRegs registers a thread (the
+// increase could then never be granted).
+constexpr int kAtLaunchRegs = 168, kAtRegsLow = 72, kAtRegsHigh = 216;
+static_assert(128 * kAtRegsLow + 256 * kAtRegsHigh <= kAtThreads * kAtLaunchRegs, "register split");
+constexpr int kAtQStages = 2;                       // one Q tile per softmax group
 constexpr int kAtKvStages = 3;
 constexpr uint32_t kAtQBytes = kAtBM * kAtD * 2;    // 16 KiB
 constexpr uint32_t kAtKBytes = kAtBN * kAtD * 2;    // 16 KiB
 constexpr uint32_t kAtVBytes = kAtBN * kAtD * 2;    // 16 KiB (two 64-key boxes)
-constexpr uint32_t kAtPBytes = kAtBM * kAtBN * 2;   // 32 KiB (two 64-key K-major blocks)
-constexpr uint32_t kAtOutBoxBytes = 32 * 32 * 2;    // one softmax warp's 32 x 32 bf16 output box
-constexpr uint32_t kAtTmemCols = 512;               // S in columns 0-127 and 128-255 (alternating blocks)
-constexpr uint32_t kAtOCol = 256;                   // O of even items in columns 256-319, odd items 320-383
-constexpr int kAtRedFloats = 2 * 2 * 2 * 128;      // row maxima and row sums, each [parity][half][row]
-constexpr int kAtOkInts = 32;                       // [parity][warp] after maxima, [warp] after sums
-constexpr int kAtBars = 2 * kAtQStages + 2 * kAtKvStages + 6;
+constexpr uint32_t kAtPBytes = kAtBM * kAtBN * 2;   // 32 KiB per group (two 64-key K-major blocks)
+constexpr uint32_t kAtTmemCols = 512;               // S of group 0 / 1 in columns 0-127 / 128-255,
+constexpr uint32_t kAtOCol = 256;                   // O of group 0 / 1 in columns 256-319 / 320-383
+constexpr int kAtBars = 2 * kAtQStages + 2 * kAtKvStages + 8;
 
 constexpr size_t at_smem_bytes() {
-    return 1024 + kAtQStages * kAtQBytes + kAtKvStages * (kAtKBytes + kAtVBytes) + kAtPBytes + 8 * kAtOutBoxBytes +
-           kAtRedFloats * 4 + kAtOkInts * 4 + kAtBars * 8 + 16;
+    return 1024 + kAtQStages * kAtQBytes + kAtKvStages * (kAtKBytes + kAtVBytes) + 2 * kAtPBytes + kAtBars * 8 + 16;
 }
 static_assert(at_smem_bytes() <= 227 * 1024, "shared memory");
 
@@ -120,25 +125,44 @@ __device__ __forceinline__ Item at_item(const AttnArgs& a, int i) {
     return it;
 }
 
-// The CTA's key blocks in order: items blockIdx.x, blockIdx.x + gridDim.x, ...
-struct Walker {
-    int i, n, j;         // item, item count so far, key block within the item
+// The CTA's items are blockIdx.x, blockIdx.x + gridDim.x, ... (local index n
+// = 0, 1, 2, ...), their key blocks numbered in that order (g = 0, 1, 2, ...:
+// the order of the K/V ring). Softmax group grp takes the items with n % 2 ==
+// grp; its walker steps over the other group's items.
+struct GWalker {
+    int i, n, j, g;      // item, local item index, key block within it, CTA block index
+    int nkb;             // key blocks of item i
     bool valid;
-    Item it;
-    __device__ __forceinline__ void init(const AttnArgs& a) {
+    __device__ __forceinline__ static int blocks(const AttnArgs& a, int i) {
+        return a.causal ? a.nqb - i / (a.B * a.H) : a.nqb;  // query block + 1, or all
+    }
+    __device__ __forceinline__ void init(const AttnArgs& a, int grp) {
         i = blockIdx.x;
         n = 0;
         j = 0;
+        g = 0;
         valid = i < a.items;
-        if (valid) it = at_item(a, i);
+        nkb = valid ? blocks(a, i) : 0;
+        if (grp == 1 && valid) skip(a);
     }
-    __device__ __forceinline__ void next(const AttnArgs& a) {
-        if (++j < it.nkb) return;
-        j = 0;
+    // Move to item n + 1 (from the start of item n).
+    __device__ __forceinline__ void skip(const AttnArgs& a) {
+        g += nkb;
         ++n;
         i += gridDim.x;
         valid = i < a.items;
-        if (valid) it = at_item(a, i);
+        nkb = valid ? blocks(a, i) : 0;
+    }
+    __device__ __forceinline__ void next(const AttnArgs& a) {
+        ++j;
+        if (j < nkb) {
+            ++g;
+            return;
+        }
+        j = 0;
+        g -= nkb - 1;  // back to the item's first block
+        skip(a);
+        if (valid) skip(a);
     }
 };
 
@@ -201,6 +225,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+__device__ __forceinline__ void regs_release_low() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kAtRegsLow));
+}
+__device__ __forceinline__ void regs_take_high() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kAtRegsHigh));
+}
+
 // Non-blocking test of an mbarrier phase (the MMA thread polls two barriers).
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     uint32_t done;
@@ -214,37 +245,29 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
 __global__ void __launch_bounds__(kAtThreads, 1)
-attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_constant__ CUtensorMap tmV,
-                const __grid_constant__ CUtensorMap tmO, const AttnArgs a) {
+attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_constant__ CUtensorMap tmQ32,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const AttnArgs a) {
     constexpr uint32_t IDESC_S = make_idesc(1u, kAtBM, kAtBN);               // Q, K both K-major
     constexpr uint32_t IDESC_O = make_idesc(1u, kAtBM, kAtD, false, true);   // P K-major, V MN-major
     constexpr int QS = kAtQStages, KS = kAtKvStages;
+    constexpr int GROUP_WARPS = 4;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = smem;
+    uint8_t* sQ = smem;                    // Q of group 0 / 1
     uint8_t* sK = sQ + QS * kAtQBytes;
     uint8_t* sV = sK + KS * kAtKBytes;
-    uint8_t* sP = sV + KS * kAtVBytes;
-    uint8_t* sOut = sP + kAtPBytes;                              // 8 output boxes
-    float* red_max = reinterpret_cast<float*>(sOut + 8 * kAtOutBoxBytes);  // [parity][half][row]
-    float* red_sum = red_max + 2 * 2 * 128;                      // [parity][half][row]
-    int* red_ok = reinterpret_cast<int*>(red_sum + 2 * 2 * 128); // [parity][8]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(red_ok + kAtOkInts);
+    uint8_t* sP = sV + KS * kAtVBytes;     // P of group 0 / 1
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * kAtPBytes);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kAtBars);
     int* s_abort = reinterpret_cast<int*>(tmem_slot + 1);
 
-    // bars: qfull[QS] qempty[QS] kvfull[KS] kvempty[KS] sfull[2] sfree[2] pfull pvfull
-    // (S buffer b = block g % 2 holds its u = g / 2-th block: phase u of sfull[b], sfree[b])
+    // bars: qfull[2] qempty[2] kvfull[KS] kvempty[KS] sfull[2] sfree[2] pfull[2] pvfull[2];
+    // the per-group barriers count that group's blocks (phase = its block count).
     const uint32_t qfull0 = smem_u32(bars), qempty0 = qfull0 + 8 * QS;
     const uint32_t kvfull0 = qempty0 + 8 * QS, kvempty0 = kvfull0 + 8 * KS;
-    const uint32_t sfull0 = kvempty0 + 8 * KS, sfree0 = sfull0 + 16, pfull = sfull0 + 32, pvfull = sfull0 + 40;
-    constexpr int SOFT_WARPS = kAtThreads / 32 - 2;
+    const uint32_t sfull0 = kvempty0 + 8 * KS, sfree0 = sfull0 + 16, pfull0 = sfull0 + 32, pvfull0 = sfull0 + 48;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -256,15 +279,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_constant_
             mbar_init(kvfull0 + 8 * s, 1);
             mbar_init(kvempty0 + 8 * s, 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(sfull0 + 8 * b, 1);
-            mbar_init(sfree0 + 8 * b, SOFT_WARPS);
+        for (int grp = 0; grp < 2; ++grp) {
+            mbar_init(sfull0 + 8 * grp, 1);
+            mbar_init(sfree0 + 8 * grp, GROUP_WARPS);
+            mbar_init(pfull0 + 8 * grp, GROUP_WARPS);
+            mbar_init(pvfull0 + 8 * grp, 1);
         }
-        mbar_init(pfull, SOFT_WARPS);
-        mbar_init(pvfull, 1);
         *s_abort = 0;
         mbar_fence_init();
         tma_prefetch_map(&tmQK);
+        tma_prefetch_map(&tmQ32);
         tma_prefetch_map(&tmV);
         tma_prefetch_map(&tmO);
     }
@@ -276,20 +300,23 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_constant_
     if (threadIdx.x == 0) pdl_launch_dependents();
     if (threadIdx.x == 0) LIN_STAMP(g_timeline_attn, blockIdx.x, 0);
 
+
     auto give_up = [&]() {
         atomicExch(s_abort, 1);
         atomicExch(a.status, (int)LIN_ERR_DEVICE_TIMEOUT);
     };
     auto aborted = [&]() { return *(volatile int*)s_abort != 0; };
 
+    if (warp < 4) regs_release_low();  // warpgroup 0: TMA, MMA and two idle warps
     if (warp == 0) {
         if (lane == 0) {
-            // ---- TMA producer ----
+            // ---- TMA producer: the CTA's items in order; Q of item n to
+            // stage n % 2 (its group's), K/V blocks through the ring ----
             // The first items' Q, K and V to L2 while the previous kernel
             // finishes: an L2 prefetch returns nothing to the SM, and the L2 is
             // where all writes meet, so this changes no result whatever that
             // kernel writes. The copies into shared memory wait for it.
-            for (int i = blockIdx.x, n = 0; i < a.items && n < QS; i += gridDim.x, ++n) {
+            for (int i = blockIdx.x, n = 0; i < a.items && n < 2; i += gridDim.x, ++n) {
                 const Item it = at_item(a, i);
                 const int row0 = it.b * a.T;
                 tma_prefetch_l2_2d(&tmQK, it.h * kAtD, row0 + it.qb * kAtBM);  // rows < B*T: a query block starts inside
@@ -309,8 +336,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_constant_
                     ok = false;
                     break;
                 }
+                // Q in four 32-row boxes; group 1 (odd items) takes them in
+                // reverse order, so that the TMEM lane quadrant that holds a
+                // block's last (causally heaviest) rows in one group holds the
+                // first rows in the other, and each SM sub-partition carries one
+                // heavy and one light warp.
                 mbar_expect_tx(qfull0 + 8 * qs, kAtQBytes);
-                tma_load_2d(smem_u32(sQ + qs * kAtQBytes), &tmQK, qfull0 + 8 * qs, it.h * kAtD, row0 + it.qb * kAtBM);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int quad = (nq & 1) ? 3 - k : k;
+                    tma_load_2d(smem_u32(sQ + qs * kAtQBytes + quad * 4096), &tmQ32, qfull0 + 8 * qs, it.h * kAtD,
+                                row0 + it.qb * kAtBM + 32 * k);
+                }
                 AT_STAMP(nq, 0);
                 ++nq;
                 for (int j = 0; j < it.nkb; ++j) {
@@ -341,63 +378,76 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_constant_
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // ---- MMA issuer: S of blocks g + 1 and g + 2 (two TMEM buffers) may
-            // go before P.V of block g, so that they overlap the softmax of
-            // block g; whichever has its inputs first is issued first ----
-            Walker ws, wp;
-            ws.init(a);
-            wp.init(a);
-            uint32_t gs = 0, gp = 0;
-            auto s_ready = [&]() -> bool {
-                const uint32_t s = gs % KS, ph = (gs / KS) & 1;
-                const uint32_t qs = ws.n % QS, qph = (ws.n / QS) & 1;
-                const uint32_t b = gs & 1, u = gs >> 1;  // S buffer and its use
-                return (ws.j != 0 || mbar_test(qfull0 + 8 * qs, qph)) && mbar_test(kvfull0 + 8 * s, ph) &&
-                       (u == 0 || mbar_test(sfree0 + 8 * b, (u - 1) & 1));
+            // ---- MMA issuer for both groups: per group, S of its next block
+            // (into its S buffer, once the softmax has read the last one) and
+            // P.V of its current block (once its P is in shared memory), at
+            // most one S ahead; whichever has its inputs first goes first ----
+            GWalker ws[2], wp[2];
+            uint32_t cs[2] = {0u, 0u}, cp[2] = {0u, 0u};  // S and P.V issued per group
+            for (int grp = 0; grp < 2; ++grp) {
+                ws[grp].init(a, grp);
+                wp[grp].init(a, grp);
+            }
+            auto s_ready = [&](int grp) -> bool {
+                const GWalker& w = ws[grp];
+                const uint32_t s = w.g % KS, ph = (w.g / KS) & 1;
+                const uint32_t qph = (w.n / QS) & 1;  // Q stage = group
+                return (w.j != 0 || mbar_test(qfull0 + 8 * grp, qph)) && mbar_test(kvfull0 + 8 * s, ph) &&
+                       (cs[grp] == 0 || mbar_test(sfree0 + 8 * grp, (cs[grp] - 1) & 1));
             };
-            auto issue_s = [&]() {
-                const uint32_t s = gs % KS, qs = ws.n % QS;
-                if (ws.j == 0) AT_STAMP(ws.n, 2);
+            auto issue_s = [&](int grp) {
+                GWalker& w = ws[grp];
+                const uint32_t s = w.g % KS;
+                if (w.j == 0) AT_STAMP(w.n, 2);
                 tc_fence_after();
-                const uint64_t qd = sw128_kmajor_desc(smem_u32(sQ + qs * kAtQBytes));
+                const uint64_t qd = sw128_kmajor_desc(smem_u32(sQ + grp * kAtQBytes));
                 const uint64_t kd = sw128_kmajor_desc(smem_u32(sK + s * kAtKBytes));
 #pragma unroll
                 for (int kk = 0; kk < kAtD / 16; ++kk)
-                    tc_mma<true>(tmem_base + 128u * (gs & 1), qd + 2u * kk, kd + 2u * kk, IDESC_S, kk != 0 ? 1u : 0u);
-                tc_commit(sfull0 + 8 * (gs & 1));
-                if (ws.j == 0) AT_STAMP(ws.n, 3);
-                if (ws.j == ws.it.nkb - 1) tc_commit(qempty0 + 8 * qs);  // Q is read by S only
-                ws.next(a);
-                ++gs;
+                    tc_mma<true>(tmem_base + 128u * grp, qd + 2u * kk, kd + 2u * kk, IDESC_S, kk != 0 ? 1u : 0u);
+                tc_commit(sfull0 + 8 * grp);
+                if (w.j == 0) AT_STAMP(w.n, 3);
+                if (w.j == w.nkb - 1) tc_commit(qempty0 + 8 * grp);  // Q is read by S only
+                w.next(a);
+                ++cs[grp];
             };
-            auto issue_pv = [&]() {
-                const uint32_t s = gp % KS;
+            auto issue_pv = [&](int grp) {
+                GWalker& w = wp[grp];
+                const uint32_t s = w.g % KS;
                 tc_fence_after();
-                const uint64_t pd = sw128_kmajor_desc(smem_u32(sP));
+                const uint64_t pd = sw128_kmajor_desc(smem_u32(sP + grp * kAtPBytes));
                 const uint64_t vd = sw128_mnmajor_desc(smem_u32(sV + s * kAtVBytes));
                 // K = 128 keys in 8 steps of 16: P advances 32 bytes within a
                 // 64-key block (+2) and 16 KiB between the blocks (+1024); V
-                // advances 16 key rows (2 KiB, +128).
+                // advances 16 key rows (2 KiB, +128). O accumulates over the
+                // item's blocks.
 #pragma unroll
                 for (int kk = 0; kk < kAtBN / 16; ++kk)
-                    tc_mma<true>(tmem_base + kAtOCol + 64u * (wp.n & 1), pd + 1024u * (kk >> 2) + 2u * (kk & 3),
-                                 vd + 128u * kk, IDESC_O,
-                                 (kk != 0 || wp.j != 0) ? 1u : 0u);  // O accumulates over the item's blocks
-                tc_commit(pvfull);
+                    tc_mma<true>(tmem_base + kAtOCol + 64u * grp, pd + 1024u * (kk >> 2) + 2u * (kk & 3),
+                                 vd + 128u * kk, IDESC_O, (kk != 0 || w.j != 0) ? 1u : 0u);
+                tc_commit(pvfull0 + 8 * grp);
                 tc_commit(kvempty0 + 8 * s);  // K and V of this block are no longer read
-                if (wp.j == wp.it.nkb - 1) AT_STAMP(wp.n, 6);
-                wp.next(a);
-                ++gp;
+                if (w.j == w.nkb - 1) AT_STAMP(w.n, 6);
+                w.next(a);
+                ++cp[grp];
             };
             bool ok = true;
             uint32_t idle = 0;
             unsigned long long t_idle = 0;
-            while (wp.valid) {
-                if (ws.valid && gs <= gp + 2 && s_ready()) {
-                    issue_s();
-                    idle = 0;
-                } else if (gp < gs && mbar_test(pfull, gp & 1)) {
-                    issue_pv();
+            while (wp[0].valid || wp[1].valid) {
+                bool progress = false;
+#pragma unroll
+                for (int grp = 0; grp < 2; ++grp) {
+                    if (ws[grp].valid && cs[grp] <= cp[grp] && s_ready(grp)) {
+                        issue_s(grp);
+                        progress = true;
+                    }
+                    if (cp[grp] < cs[grp] && mbar_test(pfull0 + 8 * grp, cp[grp] & 1)) {
+                        issue_pv(grp);
+                        progress = true;
+                    }
+                }
+                if (progress) {
                     idle = 0;
                 } else {
                     // Bounded: give up after kWaitNs without progress.
@@ -410,250 +460,215 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_constant_
             }
             if (!ok) give_up();
             // Do not reach the teardown before the last MMAs have completed.
-            if (gp > 0) mbar_wait(pvfull, (gp - 1) & 1);
-            if (gs > gp) mbar_wait(sfull0 + 8 * ((gs - 1) & 1), ((gs - 1) >> 1) & 1);
+            for (int grp = 0; grp < 2; ++grp) {
+                if (cp[grp] > 0) mbar_wait(pvfull0 + 8 * grp, (cp[grp] - 1) & 1);
+                if (cs[grp] > cp[grp]) mbar_wait(sfull0 + 8 * grp, (cs[grp] - 1) & 1);
+            }
         }
-    } else {
-        // ---- softmax and output: warp w holds TMEM lanes 32*(w%4).., key half (w-2)/4 ----
+    } else if (warp >= 4) {
+        regs_take_high();
+        // ---- softmax and output, two warpgroups working on alternate
+        // items; warp w reads TMEM lanes 32*(w%4).. (its 32 query rows), one
+        // thread per row, all 128 keys of a block ----
         pdl_wait();  // out and lse only after the previous kernel on the stream has finished
-        const int q = warp & 3, ew = warp - 2, half = ew >> 2;
-        const int r = 32 * q + lane;  // query row within the block = TMEM lane
+        const int grp = (warp - 4) >> 2;
+        const int q = warp & 3;
+        const int r = 32 * q + lane;            // TMEM lane = row of S, P and O
+        const int qq = grp ? 3 - q : q;         // the warp's query rows: 32 qq .. 32 qq + 31
+        const int qr = 32 * qq + lane;          // this thread's query row within the block
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
-        const uint32_t tS0 = tmem_base + lane_addr + 64u * half;  // + 128 for the odd blocks' S
-        const uint32_t tO0 = tmem_base + lane_addr + kAtOCol + 32u * half;  // + 64 for odd items' O
-        uint8_t* prow = sP + half * (kAtPBytes / 2) + (r >> 3) * 1024 + (r & 7) * 128;
-        // This warp's 32 x 32 output box (rows = its TMEM lanes, columns = its
-        // half of the head), 64-byte rows with the 64-byte swizzle of the
-        // output tensor map: 16-byte piece v of row i at piece v ^ ((i >> 1) & 3).
-        uint8_t* obox = sOut + ew * kAtOutBoxBytes;
-        uint8_t* orow = obox + lane * 64;
+        const uint32_t tS = tmem_base + lane_addr + 128u * grp;
+        const uint32_t tO = tmem_base + lane_addr + kAtOCol + 64u * grp;
+        uint8_t* sPg = sP + grp * kAtPBytes;
+        uint8_t* prow = sPg + (r >> 3) * 1024 + (r & 7) * 128;  // + 16 KiB for keys 64-127
+        // Output staging: the warp's rows of the group's P buffer (free once
+        // the item's last P.V has completed, until the warp writes its next P):
+        // two 32 x 32 boxes (head columns 0-31, 32-63), 64-byte rows with the
+        // 64-byte swizzle of the output map (piece v of row i at v ^ ((i >> 1) & 3)).
+        uint8_t* obox = sPg + q * 4096;
         const float NEG_INF = -INFINITY;
         const float sl2 = a.scale_log2;
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
+        const bool stamper = lane == 0 && q == 2;  // warps 6 and 10
 
-        // The current item: m is its running max of the raw scores, l its
-        // running sum (this half's keys). O accumulates in TMEM over the
-        // item's blocks; when a block raises the max, the softmax warps scale
-        // the accumulated O by alpha before the block's P.V adds to it. The
-        // item whose last P.V is still in flight: pit, pm, pl; its output is
-        // written during the next block.
-        float m = NEG_INF, l = 0.f;
-        bool pend = false;
-        Item pit = {0, 0, 0, 0};
-        float pm = 0.f, pl = 0.f;
-        bool ok_local = true;  // every wait since the last exchange succeeded
+        float m = NEG_INF, l = 0.f;   // running max of the raw scores, running sum
+        bool store_pending = false;   // this warp's boxes may still be read by a TMA store
         bool ok = true;
-
-        // Wait until the P.V of block gprev has completed (O is final for it).
-        auto wait_pv = [&](uint32_t gprev) -> bool {
-            const bool got = __all_sync(0xffffffffu, ok_local && mbar_wait(pvfull, gprev & 1));
-            if (got)
-                tc_fence_after();
-            else
-                ok_local = false;
-            return got;
-        };
-        // O / lt (lt: the row sum of both halves) into the warp's box, stored
-        // by TMA; lse.
-        auto finish = [&](const Item& e, uint32_t tO, float em, float lt) {
-            uint32_t ov[32];
-            tmem_ld32_async(tO, ov);
-            tmem_wait_ld(ov);
-            const float inv = 1.0f / lt;
-            if (lane == 0) bulk_wait_read_all();  // the box's previous store has read it
-            __syncwarp();
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-                *reinterpret_cast<uint4*>(orow + ((v ^ ((lane >> 1) & 3)) << 4)) = make_uint4(
-                    pack_bf16x2(__uint_as_float(ov[8 * v]) * inv, __uint_as_float(ov[8 * v + 1]) * inv),
-                    pack_bf16x2(__uint_as_float(ov[8 * v + 2]) * inv, __uint_as_float(ov[8 * v + 3]) * inv),
-                    pack_bf16x2(__uint_as_float(ov[8 * v + 4]) * inv, __uint_as_float(ov[8 * v + 5]) * inv),
-                    pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv, __uint_as_float(ov[8 * v + 7]) * inv));
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                // Rows past the sequence's end (t >= T) lie outside the map and are not written.
-                tma_store_3d(&tmO, smem_u32(obox), e.h * kAtD + 32 * half, e.qb * kAtBM + 32 * q, e.b);
-                bulk_commit();
-            }
-            const int qpos = e.qb * kAtBM + r;
-            if (a.lse && half == 0 && qpos < a.T)
-                a.lse[((size_t)e.b * a.H + e.h) * a.T + qpos] = (em * sl2 + lg2_hw(lt)) * 0.6931471805599453f;
-        };
-
-        Walker w;
-        w.init(a);
-        uint32_t g = 0;
+        uint32_t cnt = 0;             // this group's blocks so far
+        GWalker w;
+        w.init(a, grp);
         while (w.valid) {
-            const Item it = w.it;
+            const Item it = at_item(a, w.i);
             const int j = w.j;
             const bool last = j == it.nkb - 1;
-            const int qpos = it.qb * kAtBM + r;
-            const int kbase = j * kAtBN + 64 * half;
-            const uint32_t tS = tS0 + 128u * (g & 1);
-            const uint32_t sb_buf = g & 1, su = g >> 1;  // S buffer and its use
-            // Keys visible to this row: kpos < lim. Per 32-key chunk and warp:
-            // no row sees it (skipped: not read, not exponentiated), every row
-            // sees all of it (no mask), or the mask applies per key.
+            const int qpos = it.qb * kAtBM + qr;
+            // Keys visible to this row: kpos < lim. A 32-key chunk that no row
+            // of the warp sees is neither read nor exponentiated; one that every
+            // row sees whole needs no mask.
             const int lim = a.causal ? min(qpos + 1, a.T) : a.T;
-            const int wmax = a.causal ? min(it.qb * kAtBM + 32 * q + 32, a.T) : a.T;  // largest lim of the warp
-            const int wmin = a.causal ? min(it.qb * kAtBM + 32 * q + 1, a.T) : a.T;   // smallest
-            const bool live0 = kbase < wmax, live1 = kbase + 32 < wmax;
-            const bool mask0 = kbase + 32 > wmin, mask1 = kbase + 64 > wmin;
+            const int wmax = a.causal ? min(it.qb * kAtBM + 32 * qq + 32, a.T) : a.T;
+            const int wmin = a.causal ? min(it.qb * kAtBM + 32 * qq + 1, a.T) : a.T;
+            const int k0 = j * kAtBN;
 
-            // 1. the block's raw scores: both 32-key chunks of this half in one
-            //    round trip to TMEM; the buffer is released right after
-            uint32_t sa[32], sb[32];
-            bool got = __all_sync(0xffffffffu, ok_local && !aborted() && mbar_wait(sfull0 + 8 * sb_buf, su & 1));
-            if (warp == 2 && lane == 0 && j == 0) AT_STAMP(w.n, 4);
-            if (got) {
-                tc_fence_after();
-                if (live0) tmem_ld32_async(tS, sa);
-                if (live1) tmem_ld32_async(tS + 32, sb);
-                if (live0) tmem_wait_ld(sa);
-                if (live1) tmem_wait_ld(sb);
-            } else {
-                ok_local = false;
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sfree0 + 8 * sb_buf);
-            const bool use0 = got && live0, use1 = got && live1;
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                if (!use0 || (mask0 && kbase + c >= lim)) sa[c] = __float_as_uint(NEG_INF);
-                if (!use1 || (mask1 && kbase + 32 + c >= lim)) sb[c] = __float_as_uint(NEG_INF);
-            }
-
-            // 2. row max (raw scores; scale > 0 commutes with the max) across
-            //    the two halves; the pending item's row sums travel with it
-            float mx[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
-            if (use0) {
-#pragma unroll
-                for (int c = 0; c < 32; c += 2)
-                    mx[(c >> 1) & 1] = max3(mx[(c >> 1) & 1], __uint_as_float(sa[c]), __uint_as_float(sa[c + 1]));
-            }
-            if (use1) {
-#pragma unroll
-                for (int c = 0; c < 32; c += 2)
-                    mx[2 + ((c >> 1) & 1)] =
-                        max3(mx[2 + ((c >> 1) & 1)], __uint_as_float(sb[c]), __uint_as_float(sb[c + 1]));
-            }
-            const float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-            const int par = g & 1;
-            red_max[(par * 2 + half) * 128 + r] = mloc;
-            red_sum[(par * 2 + half) * 128 + r] = pl;
-            if (lane == 0) red_ok[par * 8 + ew] = ok_local ? 1 : 0;
-            named_bar_sync(1 + q, 64);
-            const float mo = red_max[(par * 2 + (half ^ 1)) * 128 + r];
-            const float plt = pl + red_sum[(par * 2 + (half ^ 1)) * 128 + r];
-            if (!(red_ok[par * 8 + ew] && red_ok[par * 8 + (ew ^ 4)])) {
+            // 1. the block's 128 raw scores of this row in one round trip to
+            //    TMEM (the chunks no row of the warp sees are not read), masked,
+            //    and their max (scale > 0 commutes with the max)
+            if (!__all_sync(0xffffffffu, !aborted() && mbar_wait(sfull0 + 8 * grp, cnt & 1))) {
                 ok = false;
                 break;
             }
-            const float m_new = fmaxf(m, fmaxf(mloc, mo));
+            if (stamper && j == 0) AT_STAMP(w.n, 4);
+            tc_fence_after();
+            uint32_t sv[4][32];
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch)
+                if (k0 + 32 * ch < wmax) tmem_ld32_async(tS + 32u * ch, sv[ch]);
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch)
+                if (k0 + 32 * ch < wmax) tmem_wait_ld(sv[ch]);
+            float mx[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                const int c0 = k0 + 32 * ch;
+                if (c0 >= wmax) continue;
+                if (c0 + 32 > wmin) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        if (c0 + c >= lim) sv[ch][c] = __float_as_uint(NEG_INF);
+                }
+#pragma unroll
+                for (int c = 0; c < 32; c += 2)
+                    mx[ch] = max3(mx[ch], __uint_as_float(sv[ch][c]), __uint_as_float(sv[ch][c + 1]));
+            }
+            const float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            const float m_new = fmaxf(m, mloc);
             const float m_use = m_new == NEG_INF ? 0.f : m_new;  // a row with no visible key so far
             const float alpha = ex2_hw((m - m_use) * sl2);      // 0 at the first block (m = -inf)
-            const float mb = m_use * sl2;
+            const uint64_t nmbx2 = f2_pack(-m_use * sl2, -m_use * sl2);
             m = m_new;
 
-            // 3. p = 2^(s * scale * log2 e - max), rounded to bf16 for P.V
-            uint32_t pk[32];
-            uint64_t ls2[2] = {0ull, 0ull};  // packed partial row sums (+0.0f pairs)
-            const uint64_t sl2x2 = f2_pack(sl2, sl2), nmbx2 = f2_pack(-mb, -mb);
+            // 2. the group's previous P.V has completed: P may be rewritten, and
+            //    a later block of the item rescales O by alpha before its P.V
+            if (cnt > 0 && j > 0) {
+                if (!__all_sync(0xffffffffu, mbar_wait(pvfull0 + 8 * grp, (cnt - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+                    uint32_t ov[2][32];
+                    tmem_ld32_async(tO, ov[0]);
+                    tmem_ld32_async(tO + 32u, ov[1]);
+                    tmem_wait_ld(ov[0]);
+                    tmem_wait_ld(ov[1]);
 #pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                uint32_t* sv = ch == 0 ? sa : sb;
-                if (ch == 0 ? use0 : use1) {
+                    for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+                        for (int d = 0; d < 32; ++d) ov[hh][d] = __float_as_uint(__uint_as_float(ov[hh][d]) * alpha);
+                        tmem_st32(tO + 32u * hh, ov[hh]);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            if (store_pending) {
+                if (lane == 0) bulk_wait_read_all();  // the boxes have been read out
+                __syncwarp();
+                store_pending = false;
+            }
+
+            // 3. p = 2^(s * scale * log2 e - max) per 32-key chunk, rounded to
+            //    bf16 into the group's P buffer (row r: 128-byte rows of two
+            //    K-major 64-key blocks, 16-byte pieces swizzled by r % 8)
+            uint64_t ls2[2] = {0ull, 0ull};  // packed partial row sums (+0.0f pairs)
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t pk[16];
+                if (k0 + 32 * ch < wmax) {
 #pragma unroll
                     for (int c = 0; c < 32; c += 2) {
                         float x0, x1;
-                        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2, nmbx2), x0,
-                                  x1);
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[ch][c]), __uint_as_float(sv[ch][c + 1])), sl2x2,
+                                         nmbx2),
+                                  x0, x1);
                         const float p0 = ex2_hw(x0), p1 = ex2_hw(x1);
                         ls2[(c >> 1) & 1] = f2_add(ls2[(c >> 1) & 1], f2_pack(p0, p1));
-                        pk[16 * ch + (c >> 1)] = pack_bf16x2(p0, p1);
+                        pk[c >> 1] = pack_bf16x2(p0, p1);
                     }
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) pk[16 * ch + c] = 0u;
+                    for (int c = 0; c < 16; ++c) pk[c] = 0u;
+                }
+                uint8_t* row = prow + (ch >> 1) * (kAtPBytes / 2);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int piece = 4 * (ch & 1) + i;
+                    *reinterpret_cast<uint4*>(row + ((piece ^ (r & 7)) << 4)) =
+                        make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                 }
             }
+            // S has been read, P written: release both
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(sfree0 + 8 * grp);
+                mbar_arrive(pfull0 + 8 * grp);
+            }
+            if (stamper && last) AT_STAMP(w.n, 5);
             float la, lb, lc, ld;
             f2_unpack(ls2[0], la, lb);
             f2_unpack(ls2[1], lc, ld);
             l = fmaf(l, alpha, (la + lb) + (lc + ld));
 
-            // 4. the previous block's P.V has completed: the P buffer is free,
-            //    and a later block of the item rescales the item's O by alpha
-            //    (before this block's P.V adds to it)
-            bool fin = false;
-            if (j > 0) {
-                const uint32_t tO = tO0 + 64u * (w.n & 1);
-                if (wait_pv(g - 1) && __any_sync(0xffffffffu, alpha != 1.0f)) {
-                    uint32_t ov[32];
-                    tmem_ld32_async(tO, ov);
-                    tmem_wait_ld(ov);
-#pragma unroll
-                    for (int d = 0; d < 32; ++d) ov[d] = __float_as_uint(__uint_as_float(ov[d]) * alpha);
-                    tmem_st32(tO, ov);
-                    tmem_wait_st();
-                }
-            } else if (pend) {
-                fin = wait_pv(g - 1);
-                pend = false;
-            }
-
-            // 5. P into shared memory: row r's 64 keys of this half as one
-            //    128-byte row of a K-major block, 16-byte pieces swizzled by r % 8
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                *reinterpret_cast<uint4*>(prow + ((i ^ (r & 7)) << 4)) =
-                    make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(pfull);
-            if (warp == 2 && lane == 0 && last) AT_STAMP(w.n, 5);
-
-            // 6. the previous item's output: its O is final and sits in the other
-            //    O buffer, which only the next item's first P.V overwrites, after
-            //    every warp has released that item's P (so after this load)
-            if (fin) {
-                if (warp == 2 && lane == 0) AT_STAMP(w.n - 1, 7);
-                finish(pit, tO0 + 64u * ((w.n - 1) & 1), pm, plt);
-                if (warp == 2 && lane == 0) AT_STAMP(w.n - 1, 8);
-                if (warp == 9 && lane == 0) AT_STAMP(w.n - 1, 9);
-            }
-            pl = j == 0 ? 0.f : pl;
-
+            // 4. the item's last block: wait for its P.V, write O / l (bf16)
+            //    by TMA store, and lse
             if (last) {
-                pend = true;
-                pit = it;
-                pm = m;
-                pl = l;
+                if (!__all_sync(0xffffffffu, mbar_wait(pvfull0 + 8 * grp, cnt & 1))) {
+                    ok = false;
+                    break;
+                }
+                if (stamper) AT_STAMP(w.n, 7);
+                tc_fence_after();
+                const float inv = 1.0f / l;
+                uint32_t ovv[2][32];
+                tmem_ld32_async(tO, ovv[0]);
+                tmem_ld32_async(tO + 32u, ovv[1]);
+                tmem_wait_ld(ovv[0]);
+                tmem_wait_ld(ovv[1]);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const uint32_t* ov = ovv[hh];
+                    uint8_t* orow = obox + hh * 2048 + lane * 64;
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        *reinterpret_cast<uint4*>(orow + ((v ^ ((lane >> 1) & 3)) << 4)) = make_uint4(
+                            pack_bf16x2(__uint_as_float(ov[8 * v]) * inv, __uint_as_float(ov[8 * v + 1]) * inv),
+                            pack_bf16x2(__uint_as_float(ov[8 * v + 2]) * inv, __uint_as_float(ov[8 * v + 3]) * inv),
+                            pack_bf16x2(__uint_as_float(ov[8 * v + 4]) * inv, __uint_as_float(ov[8 * v + 5]) * inv),
+                            pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv, __uint_as_float(ov[8 * v + 7]) * inv));
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    // Rows past the sequence's end (t >= T) lie outside the map and are not written.
+                    const int y = it.qb * kAtBM + 32 * qq;
+                    tma_store_3d(&tmO, smem_u32(obox), it.h * kAtD, y, it.b);
+                    tma_store_3d(&tmO, smem_u32(obox + 2048), it.h * kAtD + 32, y, it.b);
+                    bulk_commit();
+                }
+                store_pending = true;
+                if (a.lse && qpos < a.T)
+                    a.lse[((size_t)it.b * a.H + it.h) * a.T + qpos] = (m * sl2 + lg2_hw(l)) * 0.6931471805599453f;
+                if (stamper) AT_STAMP(w.n, 8);
+                if (lane == 0 && q == 1) AT_STAMP(w.n, 9);  // warps 5 and 9
                 m = NEG_INF;
                 l = 0.f;
             }
             w.next(a);
-            ++g;
+            ++cnt;
         }
-        if (ok && pend) {
-            // The last item: its P.V, then the row sums across the halves.
-            const bool got = wait_pv(g - 1);
-            if (warp == 2 && lane == 0) AT_STAMP(w.n - 1, 7);
-            const int par = g & 1;
-            red_sum[(par * 2 + half) * 128 + r] = pl;
-            if (lane == 0) red_ok[par * 8 + ew] = ok_local ? 1 : 0;
-            named_bar_sync(1 + q, 64);
-            const float plt = pl + red_sum[(par * 2 + (half ^ 1)) * 128 + r];
-            if (got && red_ok[par * 8 + ew] && red_ok[par * 8 + (ew ^ 4)])
-                finish(pit, tO0 + 64u * ((w.n - 1) & 1), pm, plt);
-            else
-                ok = false;
-            if (warp == 2 && lane == 0) AT_STAMP(w.n - 1, 8);
-            if (warp == 9 && lane == 0) AT_STAMP(w.n - 1, 9);
-        }
-        if (!ok || !ok_local) give_up();
+        if (!ok) give_up();
         if (lane == 0) bulk_wait_read_all();  // the output boxes are read out before the CTA exits
     }
 
@@ -705,6 +720,8 @@ int launch_attention(const AttnProblem& p) {
     // q and k: 64-column (128-byte) x 128-row boxes of the (B*T) x 3C tensor;
     // v: 64-column x 64-row boxes read MN-major.
     if (!make_kmajor_map(&tqk, p.qkv, true, (int)rows, 3 * C, 128)) return LIN_ERR_CUDA;
+    CUtensorMap tq32;  // q in 32-row boxes
+    if (!make_kmajor_map(&tq32, p.qkv, true, (int)rows, 3 * C, 32)) return LIN_ERR_CUDA;
     if (!make_mnmajor_map(&tv, p.qkv, (int)rows, 3 * C)) return LIN_ERR_CUDA;
     CUtensorMap to;
     if (!make_out3_map(&to, p.out, p.B, p.T, C)) return LIN_ERR_CUDA;
@@ -724,6 +741,13 @@ int launch_attention(const AttnProblem& p) {
     constexpr size_t smem = at_smem_bytes();
     static std::atomic<unsigned long long> attr_set{0};
     if (ensure_smem_attr(attr_set, attn_fwd_kernel, smem) != LIN_OK) return LIN_ERR_CUDA;
+    // The register split needs the kernel launched at kAtLaunchRegs a thread
+    // (else the softmax warpgroups' increase would wait forever): refuse otherwise.
+    static const int regs = []() {
+        cudaFuncAttributes fa;
+        return cudaFuncGetAttributes(&fa, attn_fwd_kernel) == cudaSuccess ? fa.numRegs : 0;
+    }();
+    if (regs < kAtLaunchRegs) return LIN_ERR_UNSUPPORTED;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kAtThreads);
@@ -734,7 +758,7 @@ int launch_attention(const AttnProblem& p) {
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = p.early_start ? 1 : 0;
-    if (cudaLaunchKernelEx(&cfg, attn_fwd_kernel, tqk, tv, to, a) != cudaSuccess) return LIN_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, attn_fwd_kernel, tqk, tq32, tv, to, a) != cudaSuccess) return LIN_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? LIN_OK : LIN_ERR_CUDA;
 }
 
