@@ -25,13 +25,12 @@
 //               (128 keys x 64, MN-major: two 64-key boxes) through a 3-deep
 //               ring, in item order. Before the dependency wait it asks the L2
 //               for its first items' tiles.
-//   warp 1      tcgen05.mma for both groups: S = Q K^T (M 128, N 128, K 64)
-//               into the group's TMEM S buffer (columns 0-127 or 128-255) and
-//               O += P V (M 128, N 64, K 128) into its O buffer (columns
-//               256-319 or 320-383). It polls the barriers and issues
-//               whatever has its inputs first.
-//   warps 2-5,  the two softmax groups: warp w reads TMEM lanes 32*(w%4)..
-//   warps 6-9   (its 32 query rows), one thread per row and all 128 keys of a
+//   warps 1, 2  tcgen05.mma, one issuing thread per softmax group: S = Q K^T
+//               (M 128, N 128, K 64) into the group's TMEM S buffer (columns
+//               0-127 or 128-255), then O += P V (M 128, N 64, K 128) into its
+//               O buffer (columns 256-319 or 320-383).
+//   warps 4-7,  the two softmax groups: warp w reads TMEM lanes 32*(w%4)..
+//   warps 8-11  (its 32 query rows), one thread per row and all 128 keys of a
 //               block, so no exchange between warps is needed. Scores are
 //               scaled into base-2 units (scale * log2 e) by a packed fp32x2
 //               FMA and exponentiated with the hardware ex2; P is rounded to
@@ -59,11 +58,11 @@ namespace {
 
 // Timeline stamps (timeline build only): record = blockIdx.x; [0] set up,
 // [1] producer past its dependency wait, [2] teardown; for the CTA's work item
-// n < 16, at 8 + 10 n + k: k 0 Q copy issued, 1 first K/V copy issued, 2 MMA
-// warp saw the first K/V block land, 3 first S MMAs committed, 4 the item's
-// softmax group (warp 2 or 6) saw the first S, 5 it released the last P, 6
-// last P.V MMAs committed, 7 warp 2 or 6 saw the last P.V, 8 it issued its
-// output store, 9 warp 5 or 9 issued its output store.
+// n < 16, at 8 + 10 n + k: k 0 Q copy issued, 1 first K/V copy issued, 2 the
+// group's MMA issuer saw the first S inputs ready, 3 first S MMAs committed, 4
+// the item's softmax group (warp 6 or 10) saw the first S, 5 it released the
+// last P, 6 last P.V MMAs committed, 7 warp 6 or 10 saw the last P.V, 8 it
+// issued its output store, 9 warp 5 or 9 issued its output store.
 __device__ unsigned long long g_timeline_attn[kTimelineCtas * kTimelineSlots];
 #define AT_STAMP(n, k) \
     do {                \
@@ -73,9 +72,9 @@ __device__ unsigned long long g_timeline_attn[kTimelineCtas * kTimelineSlots];
 constexpr int kAtBM = 128;                          // query rows per work item
 constexpr int kAtBN = 128;                          // keys per block
 constexpr int kAtD = 64;                            // head width
-constexpr int kAtThreads = 384;                     // warp 0 TMA, warp 1 MMA, warps 4-7 and 8-11 softmax
+constexpr int kAtThreads = 384;                     // warp 0 TMA, warps 1-2 MMA, warps 4-7 and 8-11 softmax
 // Register split (setmaxnreg, per warpgroup): launched at kAtLaunchRegs a
-// thread, warpgroup 0 (TMA, MMA, two idle warps) gives registers back down to
+// thread, warpgroup 0 (TMA, the two MMA issuers, an idle warp) gives registers back down to
 // kAtRegsLow and the two softmax warpgroups take kAtRegsHigh:
 // 128 * 72 + 256 * 216 = 64512 = 384 * 168. The host refuses to launch when
 // the compiled kernel holds fewer than kAtLaunchRegs registers a thread (the
@@ -232,19 +231,6 @@ __device__ __forceinline__ void regs_take_high() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kAtRegsHigh));
 }
 
-// Non-blocking test of an mbarrier phase (the MMA thread polls two barriers).
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
 __global__ void __launch_bounds__(kAtThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_constant__ CUtensorMap tmQ32,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const AttnArgs a) {
@@ -376,28 +362,23 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_constant_
                     mbar_wait(kvfull0 + 8 * (n % KS), (n / KS) & 1);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 2) {
         if (lane == 0) {
-            // ---- MMA issuer for both groups: per group, S of its next block
-            // (into its S buffer, once the softmax has read the last one) and
-            // P.V of its current block (once its P is in shared memory), at
-            // most one S ahead; whichever has its inputs first goes first ----
-            GWalker ws[2], wp[2];
-            uint32_t cs[2] = {0u, 0u}, cp[2] = {0u, 0u};  // S and P.V issued per group
-            for (int grp = 0; grp < 2; ++grp) {
-                ws[grp].init(a, grp);
-                wp[grp].init(a, grp);
-            }
-            auto s_ready = [&](int grp) -> bool {
-                const GWalker& w = ws[grp];
+            // ---- MMA issuer of group grp = warp - 1 (one thread per group):
+            // S of the group's block into its S buffer, then P.V of that block
+            // once its P is in shared memory; every wait blocks on one barrier ----
+            const int grp = warp - 1;
+            GWalker w;
+            w.init(a, grp);
+            uint32_t c = 0;  // the group's blocks issued
+            bool ok = true;
+            while (w.valid) {
                 const uint32_t s = w.g % KS, ph = (w.g / KS) & 1;
-                const uint32_t qph = (w.n / QS) & 1;  // Q stage = group
-                return (w.j != 0 || mbar_test(qfull0 + 8 * grp, qph)) && mbar_test(kvfull0 + 8 * s, ph) &&
-                       (cs[grp] == 0 || mbar_test(sfree0 + 8 * grp, (cs[grp] - 1) & 1));
-            };
-            auto issue_s = [&](int grp) {
-                GWalker& w = ws[grp];
-                const uint32_t s = w.g % KS;
+                if (aborted() || (w.j == 0 && !mbar_wait(qfull0 + 8 * grp, (w.n / QS) & 1)) ||
+                    !mbar_wait(kvfull0 + 8 * s, ph) || (c > 0 && !mbar_wait(sfree0 + 8 * grp, (c - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
                 if (w.j == 0) AT_STAMP(w.n, 2);
                 tc_fence_after();
                 const uint64_t qd = sw128_kmajor_desc(smem_u32(sQ + grp * kAtQBytes));
@@ -408,12 +389,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_constant_
                 tc_commit(sfull0 + 8 * grp);
                 if (w.j == 0) AT_STAMP(w.n, 3);
                 if (w.j == w.nkb - 1) tc_commit(qempty0 + 8 * grp);  // Q is read by S only
-                w.next(a);
-                ++cs[grp];
-            };
-            auto issue_pv = [&](int grp) {
-                GWalker& w = wp[grp];
-                const uint32_t s = w.g % KS;
+
+                if (aborted() || !mbar_wait(pfull0 + 8 * grp, c & 1)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
                 const uint64_t pd = sw128_kmajor_desc(smem_u32(sP + grp * kAtPBytes));
                 const uint64_t vd = sw128_mnmajor_desc(smem_u32(sV + s * kAtVBytes));
@@ -429,41 +409,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_constant_
                 tc_commit(kvempty0 + 8 * s);  // K and V of this block are no longer read
                 if (w.j == w.nkb - 1) AT_STAMP(w.n, 6);
                 w.next(a);
-                ++cp[grp];
-            };
-            bool ok = true;
-            uint32_t idle = 0;
-            unsigned long long t_idle = 0;
-            while (wp[0].valid || wp[1].valid) {
-                bool progress = false;
-#pragma unroll
-                for (int grp = 0; grp < 2; ++grp) {
-                    if (ws[grp].valid && cs[grp] <= cp[grp] && s_ready(grp)) {
-                        issue_s(grp);
-                        progress = true;
-                    }
-                    if (cp[grp] < cs[grp] && mbar_test(pfull0 + 8 * grp, cp[grp] & 1)) {
-                        issue_pv(grp);
-                        progress = true;
-                    }
-                }
-                if (progress) {
-                    idle = 0;
-                } else {
-                    // Bounded: give up after kWaitNs without progress.
-                    if (idle == 0) t_idle = global_ns();
-                    if ((++idle & 255u) == 0u && (aborted() || global_ns() - t_idle > kWaitNs || idle >= kWaitIters)) {
-                        ok = false;
-                        break;
-                    }
-                }
+                ++c;
             }
             if (!ok) give_up();
-            // Do not reach the teardown before the last MMAs have completed.
-            for (int grp = 0; grp < 2; ++grp) {
-                if (cp[grp] > 0) mbar_wait(pvfull0 + 8 * grp, (cp[grp] - 1) & 1);
-                if (cs[grp] > cp[grp]) mbar_wait(sfull0 + 8 * grp, (cs[grp] - 1) & 1);
-            }
+            // Do not reach the teardown before this group's MMAs have completed.
+            if (c > 0) mbar_wait(pvfull0 + 8 * grp, (c - 1) & 1);
+            if (!ok) mbar_wait(sfull0 + 8 * grp, c & 1);  // an S issued without its P.V
         }
     } else if (warp >= 4) {
         regs_take_high();
