@@ -1073,7 +1073,7 @@ def _med(a):
     return round(float(np.median(a)) / 1e3, 3) if len(a) else None
 
 
-def timeline_report() -> int:
+def timeline_report(which: str = "all") -> int:
     """Kernel timelines from the timeline build (stamps compiled in, see
     lin_timeline): one JSON line per case on stdout.
 
@@ -1085,7 +1085,14 @@ def timeline_report() -> int:
     skinny: four consecutive calls of the M = 16 layer in each calling mode;
     per call (us from the first CTA's start): first and last CTA start, median
     dependency-wait release, median first and last stage landed, last CTA
-    done."""
+    done.
+    attn: the fused attention forward on GPT-2's batched shape, one cold call
+    and the last of 20 back-to-back calls; per CTA work item n (medians over
+    CTAs, us from the first CTA's start) the stamps of lin_timeline's
+    attention record, and per item the softmax group's chain: S seen to P
+    released, P released to P.V issued (all four warps), P.V seen to output
+    stored.
+    `which` selects tc, skinny, attn or all."""
     import torch
 
     import oracle
@@ -1100,7 +1107,7 @@ def timeline_report() -> int:
     sink = torch.empty((), dtype=torch.float32, device=dev)
     sm = ctx.sm_count
 
-    for name in TIMELINE_TC:
+    for name in (TIMELINE_TC if which in ("all", "tc") else ()):
         layer = WORKLOADS[name]
         lb = LayerBench(torch, tll, oracle, layer, ctx, dev, stream, flush)
         if name == TIMELINE_TC[0]:
@@ -1145,6 +1152,11 @@ def timeline_report() -> int:
         del lb
         torch.cuda.empty_cache()
 
+    if which in ("all", "attn"):
+        timeline_attention(torch, tll, ctx, dev, stream, flush, sink)
+    if which not in ("all", "skinny"):
+        ctx.close()
+        return 0
     layer = WORKLOADS[DEFAULT_WORKLOAD]
     lb = LayerBench(torch, tll, oracle, layer, ctx, dev, stream, flush, want_chain=True)
     lb.parity()
@@ -1191,6 +1203,60 @@ def timeline_report() -> int:
     return 0
 
 
+def timeline_attention(torch, tll, ctx, dev, stream, flush, sink):
+    att = si.GPT2_ATTN_B64
+    q0 = torch.from_numpy(si.make_qkv(att)).to(dev).to(torch.bfloat16)
+    qs = [q0] + [q0.clone() for _ in range(11)]
+    out = torch.empty((att.B * att.T, att.C), dtype=torch.bfloat16, device=dev)
+    sm = ctx.sm_count
+
+    def call(i):
+        tll.attention_forward(qs[i % len(qs)], att.B, att.T, att.H, causal=att.causal, out=out, ctx=ctx,
+                              stream=stream)
+
+    def report(mode):
+        t = tll.timeline(tll.TIMELINE_ATTENTION)[:min(sm, att.B * att.H)]
+        t0 = t[:, 0][t[:, 0] > 0].min()
+        items = []
+        for n in range(6):
+            col = [t[:, 8 + 10 * n + k] for k in range(10)]
+            if not (col[4] > 0).any():
+                break
+            med = [_med(c[c > 0] - t0) if (c > 0).any() else None for c in col]
+            ok = (col[4] > 0) & (col[5] > 0) & (col[6] > 0) & (col[7] > 0) & (col[8] > 0)
+            items.append({"n": n, "group": n % 2, "stamps_us": med,
+                          "softmax_us": _med((col[5] - col[4])[ok]), "p_to_pv_us": _med((col[6] - col[5])[ok]),
+                          "output_us": _med((col[8] - col[7])[ok])})
+        print(json.dumps({"timeline": "attn_fwd_kernel", "workload": att.name, "mode": mode,
+                          "setup_us": _med(t[:, 0] - t0), "wait_released_us": _med(t[:, 1] - t0),
+                          "teardown_max_us": round(float(t[:, 2].max() - t0) / 1e3, 3), "items": items}), flush=True)
+
+    with torch.cuda.stream(stream):
+        call(0)
+        torch.sum(flush, dim=0, out=sink)
+    stream.synchronize()
+    tll.timeline_clear(tll.TIMELINE_ATTENTION)
+    with torch.cuda.stream(stream):
+        call(1)
+    stream.synchronize()
+    ctx.check(stream)
+    report("cold")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(20):
+            call(i)
+    g.replay()
+    stream.synchronize()
+    with torch.cuda.stream(stream):
+        torch.sum(flush, dim=0, out=sink)
+    stream.synchronize()
+    tll.timeline_clear(tll.TIMELINE_ATTENTION)
+    g.replay()
+    stream.synchronize()
+    ctx.check(stream)
+    report("last of 20 back to back")
+
+
 # ------------------------------------------------------------------- main
 
 BWD_BY_NAME = {w.name: w for w in BWD_WORKLOADS}
@@ -1211,7 +1277,7 @@ def main(argv=None):
     ap.add_argument("--profile-launches", type=int, default=0,
                     help="for ncu: only a parity-checked call and this many plain launches of the workload "
                          "(no graphs, no timing), then exit")
-    ap.add_argument("--timeline", action="store_true",
+    ap.add_argument("--timeline", nargs="?", const="all", default=None, choices=("all", "tc", "skinny", "attn"),
                     help="kernel timelines from the timeline build (JSON lines), then exit")
     args = ap.parse_args(argv)
     rank, world, local_rank = dist_env()
@@ -1238,7 +1304,7 @@ def main(argv=None):
     if args.profile_launches > 0:
         return profile_launches(args.workload, args.profile_launches)
     if args.timeline:
-        return timeline_report()
+        return timeline_report(args.timeline)
     if args.workload in BWD_BY_NAME:
         work = BWD_BY_NAME[args.workload]
         line = bench_backward(work, steps, warmup, world, rank, local_rank)

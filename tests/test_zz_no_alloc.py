@@ -105,3 +105,25 @@ def test_static_scratch_refuses_oversized_split():
     assert _static(lib, x, w, None, y, tll.EPI_NONE) == tll.ERR_WORKSPACE
     torch.cuda.synchronize()
     assert torch.equal(y, y0)  # nothing was launched
+
+
+def test_static_scratch_inside_graph_capture():
+    """What the entry exists for: after one eager call, the call can be
+    captured in a CUDA graph (nothing is allocated while capturing), and each
+    replay recomputes the layer (checked against the oracle)."""
+    lib = tll.library()
+    layer = si.GPT2_M128_FP32[3]  # fc2: a split through the static array
+    X, W, b = si.make_inputs(layer)
+    x, w, bias = torch.from_numpy(X).cuda(), torch.from_numpy(W).cuda(), torch.from_numpy(b).cuda()
+    y = torch.empty((layer.M, layer.N), device="cuda")
+    assert _static(lib, x, w, bias, y, tll.EPI_NONE) == tll.OK
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        assert _static(lib, x, w, bias, y, tll.EPI_NONE) == tll.OK
+    ref = oracle.linear(X, W, b)
+    for _ in range(2):
+        y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert oracle.rel_err(y.double().cpu().numpy(), ref) <= oracle.TOL[si.PREC_FP32]
