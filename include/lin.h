@@ -445,7 +445,11 @@ LIN_API int lin_forward_fp32_static(int M, int N, int K, const float* X, const f
  * (LIN_ERR_ALIGN), lse 4-byte aligned; B*T < 2^31. B, T or H == 0: nothing to
  * do. Asynchronous on `stream`; launched as a programmatic dependent of the
  * previous kernel (when LIN_OPT_PROGRAMMATIC_LAUNCH is on) but reads qkv and
- * writes out / lse only after that kernel has finished. */
+ * writes out / lse only after that kernel has finished (before that it only
+ * asks the L2 cache for its first tiles, which returns no data to the
+ * kernel). LIN_ERR_UNSUPPORTED also when the library was compiled so that
+ * the kernel holds fewer registers a thread than its warp-specialised
+ * register split needs (it then launches nothing). */
 LIN_API int lin_attention_forward(lin_ctx* ctx, int B, int T, int H, int D, const void* qkv, void* out, float* lse,
                                   int causal, float scale, void* stream);
 
