@@ -33,6 +33,8 @@ int main(void) {
     CHECK(lin_plan_query(152, -1, 1, 1, LIN_PREC_FP32, LIN_EPI_NONE, 0, &p) == LIN_ERR_ARG, "negative size refused");
     CHECK(lin_forward(NULL, 1, 1, 1, NULL, NULL, NULL, NULL, LIN_EPI_NONE, LIN_PREC_FP32, NULL) == LIN_ERR_ARG,
           "null context refused");
+    CHECK(lin_attention_forward(NULL, 1, 128, 12, 64, NULL, NULL, NULL, 1, 0.0f, NULL) == LIN_ERR_ARG,
+          "attention: null context refused");
     CHECK(lin_create(&ctx, 0, 0) != LIN_OK || ctx != NULL, "create fails cleanly or succeeds");
     if (ctx) lin_destroy(ctx);
     return 0;
