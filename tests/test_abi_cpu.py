@@ -317,7 +317,7 @@ def test_header_is_plain_c_and_links(tmp_path):
     assert r.returncode == 0, r.stderr
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
-    assert r.stdout.count("ok ") == 10
+    assert r.stdout.count("ok ") == 11
 
 
 def test_no_cpu_fallback_in_the_binding():
