@@ -1017,6 +1017,35 @@ def bench_reference(layer: si.Layer, steps: int, warmup: int):
     }
 
 
+def bench_reference_attention(att, steps: int, warmup: int):
+    """The oracle's attention timed on the host cores: each step computes a
+    bounded sample of the batch (whole sequences), scaled to the whole batch."""
+    import oracle
+
+    cores = oracle.max_threads()
+    qkv = si.make_qkv(att)
+    nb = max(1, min(att.B, 2))
+    sub = qkv[:nb * att.T]
+    scale = 1.0 / math.sqrt(att.D)
+    for _ in range(warmup):
+        oracle.attention(sub, nb, att.T, att.H, att.D, causal=att.causal, scale=scale, nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.attention(sub, nb, att.T, att.H, att.D, causal=att.causal, scale=scale, nthreads=cores)
+    el = (time.perf_counter() - t0) / steps
+    per_batch = el * att.B / nb
+    v = att.algorithmic_bytes() / per_batch / 1e9
+    sample = f"oracle attention on {nb} of {att.B} sequences per step, scaled to the whole batch"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "GB/s", "n_gpus": 1, "steps": steps,
+        "warmup": warmup, "ms_per_step": round(el * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": att.name, "B": att.B, "T": att.T, "H": att.H, "D": att.D, "causal": att.causal},
+        "cpu_baseline": {"value": round(v, 6), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(v, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 # ------------------------------------------------------------------- ncu
 
 def profile_launches(name: str, n: int) -> int:
@@ -1286,8 +1315,12 @@ def main(argv=None):
     if args.impl == "reference":
         if rank != 0:
             return 0
-        if args.workload in BWD_BY_NAME or args.workload in ATTN_WORKLOADS:
+        if args.workload in BWD_BY_NAME:
             print(json.dumps({"impl": "reference", "unavailable": "the reference arm times forward workloads only"}))
+            return 0
+        if args.workload in ATTN_WORKLOADS:
+            print(json.dumps(bench_reference_attention(ATTN_WORKLOADS[args.workload], min(steps, 200), warmup)),
+                  flush=True)
             return 0
         ref_steps = min(steps, 200)
         line = bench_reference(WORKLOADS[args.workload], ref_steps, warmup)
