@@ -80,3 +80,16 @@ def test_block_generation_equals_plain_definition(monkeypatch):
         b = x.view(np.uint32).astype(np.uint64)
         plain_bits = ((b + ((b >> 16) & 1) + 0x7FFF) >> 16).astype(np.uint16)
         assert np.array_equal(si.to_bf16_bits(x), plain_bits)
+
+
+def test_qkv_recipe():
+    """The attention input: (B*T) x 3C values drawn N(0, 1) from stream 4 and
+    rounded to bf16, the same for every call with the same seed."""
+    att = si.Attention("t", 2, 7, 3, 64, causal=True, seed=5)
+    a = si.make_qkv(att)
+    assert a.shape == (14, 3 * 192) and a.dtype == np.float32
+    assert np.array_equal(a, si.make_qkv(att))
+    assert np.array_equal(a, si.round_bf16(si.normal(5, 4, (14, 3 * 192), 0.0, 1.0)))
+    big = si.make_qkv(si.GPT2_ATTN_B64)
+    assert big.shape == (64 * 128, 3 * 768)
+    assert abs(float(big.mean())) < 0.01 and abs(float(big.std()) - 1.0) < 0.01
